@@ -1,0 +1,245 @@
+/*
+ * attn_oracle.c -- the correctness oracle for paged, block-sparse batched
+ * attention.  TEST INFRASTRUCTURE ONLY: nothing in the product library links,
+ * loads or calls this file; only the tests, the smoke check and the bench's
+ * CPU-baseline leg do.
+ *
+ * It is the plain definition of the result, written out in fp64, with no
+ * blocking, no splitting and no online softmax:
+ *
+ *   FlashInfer (paper summary page), section "연구 방법론 / 1. 통합된 KV 캐시
+ *   추상화": every KV storage (paged, radix tree, contiguous) is one
+ *   block-sparse matrix whose column blocks are KV pages.  Here the blocks of
+ *   request b are the pages kv_indices[kv_indptr[b] .. kv_indptr[b+1]); the
+ *   last one holds last_page_len[b] valid slots.
+ *
+ *   FlashInfer 0.6 wiki page, section "배경: LLM 디코드의 병목 구조": decode
+ *   reads the keys and values of every cached token and takes the scaled dot
+ *   product of the query with them, i.e. softmax(q K^T * scale) V.
+ *
+ *   FlashInfer 0.6 wiki page, section "커널 유형별 역할 / Decode 어텐션": GQA
+ *   and MQA; query head h reads KV head h / (Hq/Hkv) (contiguous groups; the
+ *   pages do not fix the mapping, this is the plain reading).
+ *
+ *   BatchAttention PR page, section "코드 분석 §1" (MaskMode template
+ *   parameter): the causal mask is aligned to the bottom right, so query
+ *   token t of a request with Lq queries and Lkv keys sees key j iff
+ *   j <= Lkv - Lq + t.
+ *
+ * LSE is the natural log of the sum of exp of the *scaled* scores.  A row
+ * that sees no key gets O = 0 and LSE = -inf (the pages are silent; this is
+ * the identity of the merge operator below).
+ *
+ * Merge of two partial states (the "process the dense and the sparse part
+ * separately, then combine" of the paper summary's section 1, and the
+ * split-KV of the wiki's SM103 MLA section):
+ *   s = log(exp(s_a) + exp(s_b)),  o = exp(s_a - s) o_a + exp(s_b - s) o_b.
+ *
+ * Storage element types: IEEE binary16 and bfloat16 are decoded from their bit
+ * definitions here (sign, exponent, fraction), exactly, into double.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_FP16 = 0, ORC_BF16 = 1, ORC_FP32 = 2 };
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double orc_decode_fp16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24); /* subnormal: f * 2^-14 * 2^-10 */
+    else if (e == 31)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+double orc_decode_bf16(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float x;
+    memcpy(&x, &bits, sizeof x);
+    return (double)x;
+}
+
+static double load_elem(const void* base, int dtype, int64_t idx)
+{
+    if (dtype == ORC_FP16) return orc_decode_fp16(((const uint16_t*)base)[idx]);
+    if (dtype == ORC_BF16) return orc_decode_bf16(((const uint16_t*)base)[idx]);
+    return (double)((const float*)base)[idx];
+}
+
+/* Everything that describes one batch of paged attention. */
+typedef struct {
+    int32_t batch;
+    const int32_t* qo_indptr;     /* [batch+1] query tokens of request b: [qo_indptr[b], qo_indptr[b+1]) */
+    const int32_t* kv_indptr;     /* [batch+1] pages of request b in kv_indices */
+    const int32_t* kv_indices;    /* physical page ids */
+    const int32_t* last_page_len; /* [batch] valid slots in the last page, 1..page_size */
+    int32_t num_qo_heads, num_kv_heads, head_dim, page_size, causal;
+    double sm_scale;
+    int32_t dtype;                /* element type of q, k, v */
+    const void* q;                /* [tokens, Hq, d] */
+    int64_t q_stride_tok, q_stride_head;
+    const void* k;                /* [pages, page_size, Hkv, d] */
+    int64_t k_stride_page, k_stride_slot, k_stride_head;
+    const void* v;
+    int64_t v_stride_page, v_stride_slot, v_stride_head;
+} orc_problem;
+
+static int32_t kv_len_of(const orc_problem* p, int b)
+{
+    int32_t np = p->kv_indptr[b + 1] - p->kv_indptr[b];
+    return np == 0 ? 0 : (np - 1) * p->page_size + p->last_page_len[b];
+}
+
+/* One query row: request b, query token t of that request, query head h.
+ * Writes o[head_dim] and *lse.  scores is caller scratch of >= kv_len entries. */
+static void attend_one(const orc_problem* p, int b, int t, int h, double* scores, double* o, double* lse)
+{
+    const int d = p->head_dim;
+    const int group = p->num_qo_heads / p->num_kv_heads;
+    const int hk = h / group;
+    const int32_t lq = p->qo_indptr[b + 1] - p->qo_indptr[b];
+    const int32_t lkv = kv_len_of(p, b);
+    const int64_t row = (int64_t)p->qo_indptr[b] + t;
+
+    /* visible keys are j = 0 .. nvis-1 */
+    int64_t nvis = lkv;
+    if (p->causal) {
+        int64_t last = (int64_t)lkv - lq + t; /* bottom-right aligned */
+        if (last + 1 < nvis) nvis = last + 1;
+    }
+    if (nvis < 0) nvis = 0;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    if (nvis == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+
+    const int64_t qbase = row * p->q_stride_tok + (int64_t)h * p->q_stride_head;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nvis; ++j) {
+        int64_t page = p->kv_indices[p->kv_indptr[b] + j / p->page_size];
+        int64_t slot = j % p->page_size;
+        int64_t kbase = page * p->k_stride_page + slot * p->k_stride_slot + (int64_t)hk * p->k_stride_head;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += load_elem(p->q, p->dtype, qbase + c) * load_elem(p->k, p->dtype, kbase + c);
+        scores[j] = p->sm_scale * dot;
+        if (scores[j] > m) m = scores[j];
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) sum += exp(scores[j] - m);
+    const double l = m + log(sum);
+    for (int64_t j = 0; j < nvis; ++j) {
+        int64_t page = p->kv_indices[p->kv_indptr[b] + j / p->page_size];
+        int64_t slot = j % p->page_size;
+        int64_t vbase = page * p->v_stride_page + slot * p->v_stride_slot + (int64_t)hk * p->v_stride_head;
+        double w = exp(scores[j] - l);
+        for (int c = 0; c < d; ++c) o[c] += w * load_elem(p->v, p->dtype, vbase + c);
+    }
+    *lse = l;
+}
+
+static int32_t request_of_row(const orc_problem* p, int32_t row)
+{
+    for (int b = 0; b < p->batch; ++b)
+        if (row >= p->qo_indptr[b] && row < p->qo_indptr[b + 1]) return b;
+    return -1;
+}
+
+static int32_t max_kv_len(const orc_problem* p)
+{
+    int32_t mx = 1;
+    for (int b = 0; b < p->batch; ++b) {
+        int32_t l = kv_len_of(p, b);
+        if (l > mx) mx = l;
+    }
+    return mx;
+}
+
+/* All rows: o[row][h][d], lse[row][h] for row in [0, qo_indptr[batch]).
+ * Returns 0, or -1 when scratch could not be allocated. */
+int orc_attention_all(const orc_problem* p, double* o, double* lse)
+{
+    const int64_t rows = p->qo_indptr[p->batch];
+    const int64_t n = rows * p->num_qo_heads;
+    const int32_t mx = max_kv_len(p);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* scores = (double*)malloc(sizeof(double) * (size_t)mx);
+        if (!scores) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t i = 0; i < n; ++i) {
+            if (!scores) continue;
+            int32_t row = (int32_t)(i / p->num_qo_heads);
+            int h = (int)(i % p->num_qo_heads);
+            int b = request_of_row(p, row);
+            attend_one(p, b, row - p->qo_indptr[b], h, scores, o + i * p->head_dim, lse + i);
+        }
+        free(scores);
+    }
+    return failed ? -1 : 0;
+}
+
+/* Selected (row, head) pairs only: o[i][d], lse[i].  Returns 0, -1 on
+ * allocation failure, -2 when a row lies outside every request. */
+int orc_attention_select(const orc_problem* p, int64_t n_sel, const int32_t* sel_row,
+                         const int32_t* sel_head, double* o, double* lse)
+{
+    const int32_t mx = max_kv_len(p);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* scores = (double*)malloc(sizeof(double) * (size_t)mx);
+        if (!scores) {
+#pragma omp atomic write
+            failed = -1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_sel; ++i) {
+            if (!scores) continue;
+            int b = request_of_row(p, sel_row[i]);
+            if (b < 0) {
+#pragma omp atomic write
+                failed = -2;
+                continue;
+            }
+            attend_one(p, b, sel_row[i] - p->qo_indptr[b], sel_head[i], scores, o + i * p->head_dim, lse + i);
+        }
+        free(scores);
+    }
+    return failed;
+}
+
+/* Merge n pairs of states (o_a, s_a), (o_b, s_b) of width d each. */
+void orc_merge_states(int64_t n, int32_t d, const double* o_a, const double* s_a, const double* o_b,
+                      const double* s_b, double* o_out, double* s_out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double sa = s_a[i], sb = s_b[i];
+        if (sa == -INFINITY && sb == -INFINITY) {
+            for (int c = 0; c < d; ++c) o_out[i * d + c] = 0.0;
+            s_out[i] = -INFINITY;
+            continue;
+        }
+        double mx = sa > sb ? sa : sb;
+        double s = mx + log(exp(sa - mx) + exp(sb - mx));
+        double wa = exp(sa - s), wb = exp(sb - s);
+        for (int c = 0; c < d; ++c) o_out[i * d + c] = wa * o_a[i * d + c] + wb * o_b[i * d + c];
+        s_out[i] = s;
+    }
+}

@@ -1,0 +1,192 @@
+"""Independent re-derivation of the work plan.  TEST INFRASTRUCTURE ONLY.
+
+The pages fix only the goal of the planner (FlashInfer paper summary, section
+"연구 방법론 / 3. 동적 부하 분산 스케줄링"): from each request's runtime
+sequence length, build on the CPU a plan that spreads the work evenly over all
+cores, with the tile size fixed at compile time; the plan is cached on the GPU
+and run by a fixed kernel launch.  The two CTA tile heights (128 and 16 query
+rows) come from the BatchAttention PR page, section "코드 분석 §1"
+(CTA_TILE_Q_1 = 128, CTA_TILE_Q_2 = 16).  The rule below is this library's own
+reading of that goal; this module restates it in plain Python, without sharing
+code with the C++ planner, so the two can be compared byte for byte.
+
+Rule:
+ 1. Request b has Lq query tokens, Lkv keys, R = Lq * G packed rows (packed row
+    r = t * G + g is query token t, head hk * G + g).  Tile height T = 16 if
+    R <= 16 (decode class) else 128 (prefill class).
+ 2. Units (b, hk, qt) for qt < ceil(R / T); rows [qt*T, min(R, (qt+1)*T)).
+    Visible KV length kv_eff = Lkv, or with the bottom-right causal mask
+    min(Lkv, Lkv - Lq + t_last + 1) with t_last = (row_end - 1) // G, floored
+    at 0.
+ 3. Per class, total = sum of kv_eff; chunk = max(min_chunk,
+    ceil(total / (num_ctas * split_factor))) rounded up to a multiple of the
+    class granule max(page_size, 64) (decode) or max(page_size, 128) (prefill).
+ 4. A unit with kv_eff = 0 gives one empty item.  Otherwise it splits into
+    n = ceil(kv_eff / chunk) items [i*chunk, min(kv_eff, (i+1)*chunk)).  When
+    n > 1 the unit becomes a merge unit (numbered in unit order) and its
+    items get consecutive fp32 partial-state rows, n * rows in all.
+ 5. cost = kv length of the item * class weight.  Items are sorted by
+    (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
+    load, ties to the smaller CTA index (longest processing time first).
+ 6. Output: header, per-CTA CSR offsets, items in CTA order (in assignment
+    order within a CTA), merge units, zeroed merge counters, request table.
+"""
+from __future__ import annotations
+
+import heapq
+
+import numpy as np
+
+MAGIC = 0x46495031
+HEADER_INTS = 16
+ITEM_INTS = 8
+MERGE_INTS = 8
+REQ_INTS = 4
+
+# fi_status values
+OK, INVALID_ARG, UNSUPPORTED, CAPACITY = 0, 1, 2, 3
+
+
+def _align4(n: int) -> int:
+    return (n + 3) // 4 * 4
+
+
+def _ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def int_workspace_ints(cfg: dict) -> int:
+    return (HEADER_INTS + _align4(cfg["num_ctas"] + 1) + ITEM_INTS * cfg["max_items"]
+            + MERGE_INTS * cfg["max_merge_units"] + _align4(cfg["max_merge_units"])
+            + REQ_INTS * cfg["max_batch"])
+
+
+def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads: int,
+              num_kv_heads: int, head_dim: int, page_size: int, causal: int, num_pages: int):
+    """Returns (status, workspace int32 array or None, info dict or None)."""
+    qo = [int(x) for x in qo_indptr]
+    kvp = [int(x) for x in kv_indptr]
+    lpl = [int(x) for x in last_page_len]
+    batch = len(qo) - 1
+    if batch < 0 or len(kvp) != batch + 1 or len(lpl) < batch:
+        return INVALID_ARG, None, None
+    if head_dim != 128 or page_size < 1 or page_size > 128 or page_size & (page_size - 1):
+        return UNSUPPORTED, None, None
+    if num_qo_heads < 1 or num_kv_heads < 1 or num_qo_heads % num_kv_heads:
+        return UNSUPPORTED, None, None
+    group = num_qo_heads // num_kv_heads
+    if group > 16:
+        return UNSUPPORTED, None, None
+    if causal not in (0, 1) or cfg["num_ctas"] < 1 or cfg["split_factor"] < 1:
+        return INVALID_ARG, None, None
+    if batch > cfg["max_batch"]:
+        return CAPACITY, None, None
+    if qo[0] != 0 or kvp[0] != 0:
+        return INVALID_ARG, None, None
+    for b in range(batch):
+        if qo[b + 1] < qo[b] or kvp[b + 1] < kvp[b]:
+            return INVALID_ARG, None, None
+        if kvp[b + 1] > kvp[b] and not (1 <= lpl[b] <= page_size):
+            return INVALID_ARG, None, None
+    if num_pages > 0:
+        idx = np.asarray(kv_indices[:kvp[batch]], dtype=np.int64)
+        if idx.size and (idx.min() < 0 or idx.max() >= num_pages):
+            return INVALID_ARG, None, None
+
+    C = cfg["num_ctas"]
+    lq = [qo[b + 1] - qo[b] for b in range(batch)]
+    npg = [kvp[b + 1] - kvp[b] for b in range(batch)]
+    lkv = [0 if npg[b] == 0 else (npg[b] - 1) * page_size + lpl[b] for b in range(batch)]
+
+    # units in (b, hk, qt) order: (b, hk, qt, T, row0, row1, kv_eff)
+    units = []
+    total = {16: 0, 128: 0}
+    for b in range(batch):
+        R = lq[b] * group
+        if R == 0:
+            continue
+        T = 16 if R <= 16 else 128
+        for hk in range(num_kv_heads):
+            for qt in range(_ceil_div(R, T)):
+                r0, r1 = qt * T, min(R, (qt + 1) * T)
+                if causal:
+                    t_last = (r1 - 1) // group
+                    kv_eff = max(0, min(lkv[b], lkv[b] - lq[b] + t_last + 1))
+                else:
+                    kv_eff = lkv[b]
+                units.append((b, hk, qt, T, r0, r1, kv_eff))
+                total[T] += kv_eff
+
+    chunk = {}
+    for T, min_chunk, gran in ((16, cfg["decode_min_chunk"], max(page_size, 64)),
+                               (128, cfg["prefill_min_chunk"], max(page_size, 128))):
+        want = max(min_chunk, _ceil_div(total[T], C * cfg["split_factor"]))
+        chunk[T] = _ceil_div(want, gran) * gran
+    weight = {16: cfg["decode_cost_weight"], 128: cfg["prefill_cost_weight"]}
+
+    items = []   # (sort key, fields)
+    merges = []
+    part_rows = 0
+    for (b, hk, qt, T, r0, r1, kv_eff) in units:
+        if kv_eff == 0:
+            items.append(((0, -T, b, hk, qt, 0), (b, hk, r0, r1, 0, 0, -1, -1)))
+            continue
+        n = _ceil_div(kv_eff, chunk[T])
+        if n == 1:
+            cost = kv_eff * weight[T]
+            items.append(((-cost, -T, b, hk, qt, 0), (b, hk, r0, r1, 0, kv_eff, -1, -1)))
+            continue
+        m = len(merges)
+        base = part_rows
+        nrows = r1 - r0
+        merges.append((b, hk, r0, r1, n, base, 0, 0))
+        part_rows += n * nrows
+        for i in range(n):
+            k0, k1 = i * chunk[T], min(kv_eff, (i + 1) * chunk[T])
+            cost = (k1 - k0) * weight[T]
+            items.append(((-cost, -T, b, hk, qt, i), (b, hk, r0, r1, k0, k1, base + i * nrows, m)))
+
+    if len(items) > cfg["max_items"] or len(merges) > cfg["max_merge_units"] \
+            or part_rows > cfg["max_partial_rows"]:
+        return CAPACITY, None, None
+
+    items.sort(key=lambda it: it[0])
+    heap = [(0, c) for c in range(C)]
+    per_cta = [[] for _ in range(C)]
+    for key, fields in items:
+        load, c = heapq.heappop(heap)
+        per_cta[c].append(fields)
+        heapq.heappush(heap, (load - key[0], c))
+
+    n_items, n_merge = len(items), len(merges)
+    off_cta = HEADER_INTS
+    off_items = off_cta + _align4(C + 1)
+    off_merge = off_items + ITEM_INTS * n_items
+    off_cnt = off_merge + MERGE_INTS * n_merge
+    off_req = off_cnt + _align4(n_merge)
+    total_ints = off_req + REQ_INTS * batch
+    if total_ints > int_workspace_ints(cfg):
+        return CAPACITY, None, None
+
+    ws = np.zeros(total_ints, dtype=np.int32)
+    ws[:HEADER_INTS] = [MAGIC, n_items, n_merge, C, batch, causal, off_cta, off_items, off_merge,
+                        off_cnt, off_req, 0, num_qo_heads, num_kv_heads, page_size, total_ints]
+    pos = 0
+    for c in range(C):
+        ws[off_cta + c] = pos
+        for fields in per_cta[c]:
+            ws[off_items + ITEM_INTS * pos: off_items + ITEM_INTS * (pos + 1)] = fields
+            pos += 1
+    ws[off_cta + C] = pos
+    for m, fields in enumerate(merges):
+        ws[off_merge + MERGE_INTS * m: off_merge + MERGE_INTS * (m + 1)] = fields
+    for b in range(batch):
+        ws[off_req + REQ_INTS * b: off_req + REQ_INTS * (b + 1)] = [qo[b], lq[b], kvp[b], lkv[b]]
+
+    n_dec = sum(1 for _, f in items if lq[f[0]] * group <= 16)
+    info = dict(num_ctas=C, num_items=n_items, num_merge_units=n_merge, batch=batch,
+                num_partial_rows=part_rows, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
+                head_dim=head_dim, page_size=page_size, causal=causal, chunk_decode=chunk[16],
+                chunk_prefill=chunk[128], num_decode_items=n_dec, num_prefill_items=n_items - n_dec,
+                int_ws_bytes_used=4 * total_ints, max_partial_rows=cfg["max_partial_rows"])
+    return OK, ws, info
