@@ -1,0 +1,192 @@
+/*
+ * fi.h -- C ABI of the GB300 (sm_103a) paged, block-sparse batched attention
+ * library.  Plain C types only: device pointers are `void*`/typed pointers to
+ * device memory, host pointers are marked HOST, a stream is a `cudaStream_t`
+ * passed as `void*` (NULL = legacy default stream).
+ *
+ * The split of the work into a host "plan" and a device "run" follows the
+ * FlashInfer paper summary, section "연구 방법론 / 3. 동적 부하 분산 스케줄링":
+ * the work plan is built on the CPU from each request's runtime length so that
+ * every SM gets an even share, it is then cached on the GPU, and the kernel
+ * launch itself never changes, so it can be captured once in a CUDA graph.
+ * The call shape (plan, then run(float workspace, int workspace, plan info,
+ * q, kv cache, out, lse)) and the K/V stride comparison inside run follow the
+ * BatchAttention PR page, section "코드 분석 §2".
+ *
+ * Ownership: the caller owns every buffer (device memory, the pinned host
+ * staging buffer, the stream).  The library keeps no global allocations and
+ * no handles.  Workspaces must outlive any CUDA graph that captured a run.
+ *
+ * Errors: every entry point returns an fi_status.  Argument and shape errors
+ * are detected on the host before anything is enqueued, and then no device
+ * memory is touched.  Kernel-side failures (a bounded wait that ran out) are
+ * recorded in a status word inside the int workspace; read it with
+ * fi_get_device_status().
+ */
+#ifndef FI_H_
+#define FI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FI_OK = 0,
+    FI_ERR_INVALID_ARG = 1,  /* malformed indptr, lengths out of range, null pointer, ... */
+    FI_ERR_UNSUPPORTED = 2,  /* head_dim, page_size, dtype or head ratio outside the supported set */
+    FI_ERR_CAPACITY = 3,     /* plan does not fit the workspace capacities of the config */
+    FI_ERR_ALIGNMENT = 4,    /* pointer or stride not 16-byte aligned */
+    FI_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+    FI_ERR_DEVICE_CHECK = 6, /* the kernel recorded a failed device-side check */
+    FI_ERR_TIMEOUT = 7       /* the kernel recorded a bounded wait that ran out */
+} fi_status;
+
+typedef enum { FI_FP16 = 0, FI_BF16 = 1, FI_FP32 = 2 } fi_dtype;
+
+/* Fixed at workspace creation.  Every plan made with one config fits the same
+ * workspaces and launches the same grid, which is what lets one captured
+ * graph serve any plan. */
+typedef struct {
+    int32_t num_ctas;            /* persistent CTAs of run (grid size); <= SMs x resident CTAs per SM */
+    int32_t max_batch;           /* requests per plan */
+    int32_t max_items;           /* work items per plan */
+    int32_t max_merge_units;     /* split units per plan */
+    int64_t max_partial_rows;    /* rows of fp32 partial state (head_dim floats + 1 LSE each) */
+    int32_t decode_min_chunk;    /* smallest KV chunk of a 16-row tile, tokens (default 256) */
+    int32_t prefill_min_chunk;   /* smallest KV chunk of a 128-row tile, tokens (default 1024) */
+    int32_t decode_cost_weight;  /* cost of one KV token in a 16-row tile (default 4) */
+    int32_t prefill_cost_weight; /* cost of one KV token in a 128-row tile (default 3) */
+    int32_t split_factor;        /* target chunks per CTA per tile class (default 4) */
+    int32_t reserved[3];
+} fi_plan_config;
+
+/* Plain data returned by fi_plan; passed to run by value semantics. */
+typedef struct {
+    int32_t num_ctas;
+    int32_t num_items;
+    int32_t num_merge_units;
+    int32_t batch;
+    int64_t num_partial_rows;
+    int32_t num_qo_heads, num_kv_heads, head_dim, page_size, causal;
+    int32_t chunk_decode;        /* KV tokens per chunk chosen for 16-row tiles */
+    int32_t chunk_prefill;       /* KV tokens per chunk chosen for 128-row tiles */
+    int32_t num_decode_items, num_prefill_items;
+    int32_t reserved;
+    int64_t int_ws_bytes_used;   /* bytes of the int workspace written (and copied) by the plan */
+    int64_t max_partial_rows;    /* capacity of the float workspace, from the config */
+} fi_plan_info;
+
+/* Defaults, with num_ctas derived from the device's SM count and the run
+ * kernel's occupancy (cudaOccupancyMaxActiveBlocksPerMultiprocessor), so a
+ * plan never asks for more CTAs than can be resident at once. */
+fi_status fi_default_plan_config(int device, fi_plan_config* out);
+
+/* Workspace sizes for a config (bytes).  The int workspace holds the plan,
+ * the merge counters and the device status word; the float workspace holds
+ * fp32 partial states of split work.  Both are device memory. */
+size_t fi_int_workspace_bytes(const fi_plan_config* cfg);
+size_t fi_float_workspace_bytes(const fi_plan_config* cfg, int32_t head_dim);
+
+/*
+ * fi_plan -- build the load-balanced split-KV work list on the host and copy
+ * it into int_workspace_dev with one cudaMemcpyAsync on `stream`.
+ *
+ * Paged KV as a block-sparse matrix (paper summary, "1. 통합된 KV 캐시 추상화";
+ * wiki, "FlashInfer 아키텍처 / 1) 블록-스파스 KV 포맷"): request b owns query
+ * tokens [qo_indptr[b], qo_indptr[b+1]) and pages
+ * kv_indices[kv_indptr[b] .. kv_indptr[b+1]); its KV length is
+ * (pages-1)*page_size + last_page_len[b] (0 when it has no page).
+ *
+ * All four arrays are HOST memory, int32: qo_indptr and kv_indptr have
+ * batch+1 entries, start at 0 and never decrease; last_page_len has batch
+ * entries in [1, page_size] for requests with pages; kv_indices has
+ * kv_indptr[batch] entries (read only for validation against num_pages when
+ * num_pages > 0).
+ *
+ * Supported: head_dim == 128; page_size a power of two in [1, 128];
+ * num_qo_heads % num_kv_heads == 0 with group size <= 16.
+ *
+ * pinned_staging_host: caller-owned pinned host buffer of at least
+ * fi_int_workspace_bytes(cfg) bytes; the plan is written there and copied
+ * from there asynchronously, so it must not be reused until the copy on
+ * `stream` has completed.  The plan rule is deterministic: equal inputs give
+ * byte-identical workspaces.
+ */
+fi_status fi_plan(const fi_plan_config* cfg, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                  const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch,
+                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                  int32_t causal, int32_t num_pages, void* int_workspace_dev, void* pinned_staging_host,
+                  size_t staging_bytes, void* stream, fi_plan_info* info_out);
+
+/*
+ * fi_plan_host -- the same rule as fi_plan, writing the workspace image into
+ * a HOST buffer only (no CUDA call).  Used to inspect a plan.
+ */
+fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                       const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch,
+                       int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                       int32_t causal, int32_t num_pages, void* workspace_host, size_t workspace_bytes,
+                       fi_plan_info* info_out);
+
+/*
+ * fi_batch_paged_attention_run -- one persistent kernel over the planned
+ * work list: O = softmax(scale * Q K^T + mask) V per query row and head, and
+ * LSE = log sum exp(scale * q.k) (natural log) over the visible keys.
+ *
+ * Layouts (all element strides; the last dimension is contiguous):
+ *   q  [q_num_tokens, num_qo_heads, head_dim]      strides (q_stride_tok, q_stride_head, 1)
+ *   k  [num_pages, page_size, num_kv_heads, d]     strides k_strides[0..2], 1
+ *   v  [num_pages, page_size, num_kv_heads, d]     strides v_strides[0..2], 1
+ *   o  [q_num_tokens, num_qo_heads, head_dim]      strides (o_stride_tok, o_stride_head, 1)
+ *   lse[q_num_tokens, num_qo_heads] fp32, contiguous; may be NULL.
+ * q, k, v and o share `dtype` (FI_FP16 or FI_BF16).  Every base pointer and
+ * every stride in bytes must be a multiple of 16.  K and V strides may differ
+ * (the equal-stride case is detected here, BatchAttention PR page, "코드 분석
+ * §2").  kv_indices_dev is the device copy of the page table given to the
+ * plan.  q_num_tokens and num_pages are the extents of the buffers (they may
+ * exceed what the plan uses, so a graph can be captured once at capacity).
+ * Query head h reads KV head h / (num_qo_heads / num_kv_heads); a query row
+ * with no visible key gets O = 0 and LSE = -inf.  Causal masks are aligned to
+ * the bottom right: query token t of a request sees key j iff
+ * j <= kv_len - qo_len + t.
+ *
+ * Asynchronous on `stream`; never allocates, synchronizes or copies from the
+ * host, so it can be captured in a CUDA graph.  The kernel reads the counts
+ * of the current plan from the int workspace.
+ */
+fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, int64_t q_stride_tok,
+                                       int64_t q_stride_head, int32_t q_num_tokens, const void* k_cache,
+                                       const int64_t k_strides[3], const void* v_cache,
+                                       const int64_t v_strides[3], int32_t num_pages,
+                                       const int32_t* kv_indices_dev, void* o, int64_t o_stride_tok,
+                                       int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale,
+                                       void* int_workspace_dev, void* float_workspace_dev, void* stream);
+
+/*
+ * fi_merge_states -- merge two attention states row by row (paper summary,
+ * "1. 통합된 KV 캐시 추상화": a shared dense prefix and per-request sparse
+ * suffixes are computed separately and combined):
+ *   s = log(exp(s_a) + exp(s_b)),  v = exp(s_a - s) v_a + exp(s_b - s) v_b.
+ * (v, -inf) is the identity; two -inf states give (0, -inf).
+ *   v_a, v_b, v_out [rows, heads, head_dim] contiguous, element type dtype
+ *   (FI_FP16, FI_BF16 or FI_FP32); s_a, s_b, s_out [rows, heads] fp32.
+ * v_out may alias v_a or v_b, s_out may alias s_a or s_b.  Asynchronous.
+ */
+fi_status fi_merge_states(const void* v_a, const float* s_a, const void* v_b, const float* s_b, void* v_out,
+                          float* s_out, int32_t rows, int32_t heads, int32_t head_dim, fi_dtype dtype,
+                          void* stream);
+
+/* Reads the device status word of an int workspace (synchronizes `stream`).
+ * *status_out is FI_OK, FI_ERR_TIMEOUT or FI_ERR_DEVICE_CHECK. */
+fi_status fi_get_device_status(const void* int_workspace_dev, void* stream, int32_t* status_out);
+
+const char* fi_status_string(fi_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FI_H_ */

@@ -1,0 +1,230 @@
+"""Python binding of libfi_gb300 (paged, block-sparse batched attention on sm_103a).
+
+Argument marshalling only: torch supplies device memory, pinned host memory and
+streams; every step of the hot path runs in the library's CUDA kernels (the
+planner runs on the host, as the plan/run split prescribes).  There is no CPU
+fallback: if the shared library is missing or fails to load, every call
+raises.
+
+    cfg = default_plan_config(0)
+    ws = Workspace(cfg)
+    info = plan(ws, qo_indptr, kv_indptr, kv_indices, last_page_len, 32, 8, 128, 16, causal=0)
+    run(ws, info, q, k_cache, v_cache, kv_indices_dev, o, lse, sm_scale)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _build
+
+FP16, BF16, FP32 = 0, 1, 2
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "capacity", 4: "alignment", 5: "cuda error",
+          6: "device check failed", 7: "device timeout"}
+_DTYPE = {torch.float16: FP16, torch.bfloat16: BF16, torch.float32: FP32}
+
+
+class FIError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+class PlanConfig(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("max_items", ctypes.c_int32),
+                ("max_merge_units", ctypes.c_int32), ("max_partial_rows", ctypes.c_int64),
+                ("decode_min_chunk", ctypes.c_int32), ("prefill_min_chunk", ctypes.c_int32),
+                ("decode_cost_weight", ctypes.c_int32), ("prefill_cost_weight", ctypes.c_int32),
+                ("split_factor", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int32), ("num_items", ctypes.c_int32), ("num_merge_units", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("num_partial_rows", ctypes.c_int64), ("num_qo_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("causal", ctypes.c_int32), ("chunk_decode", ctypes.c_int32), ("chunk_prefill", ctypes.c_int32),
+                ("num_decode_items", ctypes.c_int32), ("num_prefill_items", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("int_ws_bytes_used", ctypes.c_int64),
+                ("max_partial_rows", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+
+EXPORTS = ["fi_default_plan_config", "fi_int_workspace_bytes", "fi_float_workspace_bytes", "fi_plan",
+           "fi_plan_host", "fi_batch_paged_attention_run", "fi_merge_states", "fi_get_device_status",
+           "fi_status_string"]
+
+_lib = None
+
+
+def load(build_if_stale: bool = True) -> ctypes.CDLL:
+    """Load libfi_gb300.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build() if build_if_stale else _build.LIB_PATH
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    cfgp, infop = ctypes.POINTER(PlanConfig), ctypes.POINTER(PlanInfo)
+    lib.fi_default_plan_config.argtypes = [ctypes.c_int, cfgp]
+    lib.fi_int_workspace_bytes.argtypes = [cfgp]
+    lib.fi_int_workspace_bytes.restype = sz
+    lib.fi_float_workspace_bytes.argtypes = [cfgp, i32]
+    lib.fi_float_workspace_bytes.restype = sz
+    lib.fi_plan.argtypes = [cfgp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, infop]
+    lib.fi_plan_host.argtypes = [cfgp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, sz, infop]
+    lib.fi_batch_paged_attention_run.argtypes = [infop, vp, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp, i64, i64,
+                                                 vp, ctypes.c_int, ctypes.c_float, vp, vp, vp]
+    lib.fi_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, vp]
+    lib.fi_get_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+    lib.fi_status_string.argtypes = [ctypes.c_int]
+    lib.fi_status_string.restype = ctypes.c_char_p
+    for name in ("fi_default_plan_config", "fi_plan", "fi_plan_host", "fi_batch_paged_attention_run",
+                 "fi_merge_states", "fi_get_device_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise FIError(status, where)
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+
+
+def default_plan_config(device: int = 0, **overrides) -> PlanConfig:
+    cfg = PlanConfig()
+    _check(load().fi_default_plan_config(device, ctypes.byref(cfg)), "fi_default_plan_config")
+    for k, v in overrides.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+def make_plan_config(num_ctas: int, **overrides) -> PlanConfig:
+    """A config without asking the device (host-side planning and tests)."""
+    cfg = PlanConfig(num_ctas=num_ctas, max_batch=8192, max_items=1 << 17, max_merge_units=1 << 15,
+                     max_partial_rows=1 << 19, decode_min_chunk=256, prefill_min_chunk=1024, decode_cost_weight=4,
+                     prefill_cost_weight=3, split_factor=4)
+    for k, v in overrides.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+def int_workspace_bytes(cfg: PlanConfig) -> int:
+    return int(load().fi_int_workspace_bytes(ctypes.byref(cfg)))
+
+
+def float_workspace_bytes(cfg: PlanConfig, head_dim: int = 128) -> int:
+    return int(load().fi_float_workspace_bytes(ctypes.byref(cfg), head_dim))
+
+
+class Workspace:
+    """Device int/float workspaces plus two pinned staging buffers for plans."""
+
+    def __init__(self, cfg: PlanConfig, head_dim: int = 128, device="cuda"):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        ib, fb = int_workspace_bytes(cfg), float_workspace_bytes(cfg, head_dim)
+        self.int_ws = torch.zeros((ib + 15) // 16 * 4, dtype=torch.int32, device=self.device)
+        self.float_ws = torch.zeros((fb + 15) // 16 * 4, dtype=torch.float32, device=self.device)
+        self._staging = [torch.empty(ib, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+        self._events = [None, None]
+        self._next = 0
+
+
+def plan_host(cfg: PlanConfig, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads: int,
+              num_kv_heads: int, head_dim: int, page_size: int, causal: int, num_pages: int = 0):
+    """Host-only planning: returns (status, int32 workspace image or None, PlanInfo)."""
+    lib = load()
+    qo, kvp, kvi, lpl = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)
+    nbytes = int_workspace_bytes(cfg)
+    buf = np.zeros(nbytes // 4, dtype=np.int32)
+    info = PlanInfo()
+    st = lib.fi_plan_host(ctypes.byref(cfg), qo.ctypes.data, kvp.ctypes.data, kvi.ctypes.data if kvi.size else None,
+                          lpl.ctypes.data if lpl.size else None, len(qo) - 1, num_qo_heads, num_kv_heads, head_dim,
+                          page_size, causal, num_pages, buf.ctypes.data, nbytes, ctypes.byref(info))
+    if st != 0:
+        return st, None, info
+    return st, buf[:info.int_ws_bytes_used // 4].copy(), info
+
+
+def plan(ws: Workspace, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads: int, num_kv_heads: int,
+         head_dim: int, page_size: int, causal: int, num_pages: int = 0, stream=None) -> PlanInfo:
+    """Plan on the host and enqueue the copy of the work list into ws.int_ws."""
+    lib = load()
+    qo, kvp, kvi, lpl = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)
+    i = ws._next
+    ws._next ^= 1
+    if ws._events[i] is not None:
+        ws._events[i].synchronize()  # the staging buffer's previous copy has landed
+    info = PlanInfo()
+    staging = ws._staging[i]
+    st = lib.fi_plan(ctypes.byref(ws.cfg), qo.ctypes.data, kvp.ctypes.data, kvi.ctypes.data if kvi.size else None,
+                     lpl.ctypes.data if lpl.size else None, len(qo) - 1, num_qo_heads, num_kv_heads, head_dim,
+                     page_size, causal, num_pages, ws.int_ws.data_ptr(), staging.data_ptr(), staging.numel(),
+                     _stream_ptr(stream), ctypes.byref(info))
+    _check(st, "fi_plan")
+    ev = torch.cuda.Event()
+    ev.record(stream if stream is not None else torch.cuda.current_stream())
+    ws._events[i] = ev
+    return info
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPE:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DTYPE[t.dtype]
+
+
+def run(ws: Workspace, info: PlanInfo, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+        kv_indices_dev: torch.Tensor, o: torch.Tensor, lse: torch.Tensor | None, sm_scale: float, stream=None):
+    """Enqueue the persistent attention kernel for the current plan of `ws`."""
+    lib = load()
+    if kv_indices_dev.dtype != torch.int32 or not kv_indices_dev.is_contiguous():
+        raise TypeError("kv_indices must be a contiguous int32 device tensor")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise TypeError("lse must be contiguous fp32")
+    if q.dtype != k_cache.dtype or q.dtype != v_cache.dtype or q.dtype != o.dtype:
+        raise TypeError("q, k, v and o must share one dtype")
+    ks = (ctypes.c_int64 * 3)(*k_cache.stride()[:3])
+    vs = (ctypes.c_int64 * 3)(*v_cache.stride()[:3])
+    st = lib.fi_batch_paged_attention_run(
+        ctypes.byref(info), q.data_ptr(), q.stride(0), q.stride(1), q.shape[0], k_cache.data_ptr(), ks,
+        v_cache.data_ptr(), vs, k_cache.shape[0], kv_indices_dev.data_ptr(), o.data_ptr(), o.stride(0), o.stride(1),
+        lse.data_ptr() if lse is not None else None, _dtype_code(q), float(sm_scale), ws.int_ws.data_ptr(),
+        ws.float_ws.data_ptr(), _stream_ptr(stream))
+    _check(st, "fi_batch_paged_attention_run")
+
+
+def merge_states(v_a, s_a, v_b, s_b, v_out, s_out, stream=None):
+    """v_* [rows, heads, 128] (fp16/bf16/fp32, contiguous), s_* [rows, heads] fp32."""
+    lib = load()
+    for t in (v_a, v_b, v_out, s_a, s_b, s_out):
+        if not t.is_contiguous():
+            raise TypeError("merge_states needs contiguous tensors")
+    rows, heads, d = v_a.shape
+    st = lib.fi_merge_states(v_a.data_ptr(), s_a.data_ptr(), v_b.data_ptr(), s_b.data_ptr(), v_out.data_ptr(),
+                             s_out.data_ptr(), rows, heads, d, _dtype_code(v_a), _stream_ptr(stream))
+    _check(st, "fi_merge_states")
+
+
+def device_status(ws: Workspace, stream=None) -> int:
+    """Status word of the last run on ws (0 = ok, 7 = a bounded wait ran out)."""
+    out = ctypes.c_int32(0)
+    _check(load().fi_get_device_status(ws.int_ws.data_ptr(), _stream_ptr(stream), ctypes.byref(out)),
+           "fi_get_device_status")
+    return out.value

@@ -1,0 +1,246 @@
+// attention.cu -- C-ABI entry points of the run kernel, the state merge
+// kernel, the default plan config and the device status query.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/fi.h"
+#include "attention_kernel.cuh"
+
+namespace fi {
+
+// ------------------------------------------------------------ merge kernel
+
+// Storage <-> fp32 for 8 consecutive elements.
+template <typename T>
+struct Vec8 {
+  __device__ __forceinline__ static void load(const T* p, float (&f)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const float2 a = Elem<T>::to_float2(u.x), b = Elem<T>::to_float2(u.y);
+    const float2 c = Elem<T>::to_float2(u.z), d = Elem<T>::to_float2(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+  }
+  __device__ __forceinline__ static void store(T* p, const float (&f)[8]) {
+    uint4 u;
+    u.x = Elem<T>::from_float2(f[0], f[1]);
+    u.y = Elem<T>::from_float2(f[2], f[3]);
+    u.z = Elem<T>::from_float2(f[4], f[5]);
+    u.w = Elem<T>::from_float2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+  }
+};
+
+template <>
+struct Vec8<float> {
+  __device__ __forceinline__ static void load(const float* p, float (&f)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+  __device__ __forceinline__ static void store(float* p, const float (&f)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+};
+
+// One (row, head) state per 16 threads, 8 elements per thread (head_dim 128).
+// Every thread of a state reads both inputs before any thread writes, so the
+// output may alias either input.
+template <typename T>
+__global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__ va, const float* sa, const T* vb,
+                                                            const float* sb, T* vo, float* so, int64_t states) {
+  const int64_t st = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int part = threadIdx.x & 15;
+  if (st >= states) return;
+  const float la = sa[st] * 1.4426950408889634f;  // natural log -> log2
+  const float lb = sb[st] * 1.4426950408889634f;
+  float a[8], b[8], r[8];
+  Vec8<T>::load(va + st * kHeadDim + part * 8, a);
+  Vec8<T>::load(vb + st * kHeadDim + part * 8, b);
+  float lse;
+  if (la == -INFINITY && lb == -INFINITY) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) r[c] = 0.f;
+    lse = -INFINITY;
+  } else {
+    const float mx = fmaxf(la, lb);
+    const float wa = ex2(la - mx), wb = ex2(lb - mx);
+    const float inv = 1.f / (wa + wb);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) r[c] = (wa * a[c] + wb * b[c]) * inv;
+    lse = (mx + __log2f(wa + wb)) * 0.69314718055994531f;
+  }
+  __syncwarp();
+  Vec8<T>::store(vo + st * kHeadDim + part * 8, r);
+  if (part == 0) so[st] = lse;
+}
+
+// ------------------------------------------------------------ launch helpers
+
+// The shared-memory opt-in is set once per device and instantiation, so a
+// run enqueued inside a stream capture makes no non-stream CUDA call.
+constexpr int kMaxDevices = 64;
+
+template <typename T, bool kEqualKV>
+cudaError_t launch_run(const RunParams& p, int num_ctas, cudaStream_t stream) {
+  static bool configured[kMaxDevices] = {};
+  auto kern = paged_attention_kernel<T, kEqualKV>;
+  const int smem = int(sizeof(RunSmem));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
+  }
+  kern<<<num_ctas, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool stride_ok(int64_t elems) { return elems > 0 && (elems * 2) % 16 == 0; }
+
+}  // namespace fi
+
+using namespace fi;
+
+extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
+  if (!out) return FI_ERR_INVALID_ARG;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return FI_ERR_CUDA;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) return FI_ERR_CUDA;
+  auto kern = paged_attention_kernel<__nv_bfloat16, false>;
+  const int smem = int(sizeof(RunSmem));
+  int per_sm = 0;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  cudaSetDevice(prev);
+  if (e != cudaSuccess || per_sm < 1) return FI_ERR_CUDA;
+  std::memset(out, 0, sizeof *out);
+  out->num_ctas = sms * per_sm;
+  out->max_batch = 8192;
+  out->max_items = 1 << 17;
+  out->max_merge_units = 1 << 15;
+  out->max_partial_rows = int64_t(1) << 19;
+  out->decode_min_chunk = 256;
+  out->prefill_min_chunk = 1024;
+  out->decode_cost_weight = 4;
+  out->prefill_cost_weight = 3;
+  out->split_factor = 4;
+  return FI_OK;
+}
+
+extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, int64_t q_stride_tok,
+                                                  int64_t q_stride_head, int32_t q_num_tokens, const void* k_cache,
+                                                  const int64_t k_strides[3], const void* v_cache,
+                                                  const int64_t v_strides[3], int32_t num_pages,
+                                                  const int32_t* kv_indices_dev, void* o, int64_t o_stride_tok,
+                                                  int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale,
+                                                  void* int_workspace_dev, void* float_workspace_dev, void* stream) {
+  if (!info || !q || !k_cache || !v_cache || !k_strides || !v_strides || !kv_indices_dev || !o ||
+      !int_workspace_dev)
+    return FI_ERR_INVALID_ARG;
+  if (info->num_ctas < 1 || q_num_tokens < 1 || num_pages < 1 || !std::isfinite(sm_scale))
+    return FI_ERR_INVALID_ARG;
+  if (info->num_partial_rows > 0 && !float_workspace_dev) return FI_ERR_INVALID_ARG;
+  if (info->head_dim != kHeadDim) return FI_ERR_UNSUPPORTED;
+  if (dtype != FI_FP16 && dtype != FI_BF16) return FI_ERR_UNSUPPORTED;
+  const int P = info->page_size;
+  if (P < 1 || P > 128 || (P & (P - 1))) return FI_ERR_UNSUPPORTED;
+  if (info->num_kv_heads < 1 || info->num_qo_heads % info->num_kv_heads) return FI_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      !aligned16(int_workspace_dev) || (float_workspace_dev && !aligned16(float_workspace_dev)) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FI_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i)
+    if (!stride_ok(k_strides[i]) || !stride_ok(v_strides[i])) return FI_ERR_ALIGNMENT;
+  if (!stride_ok(q_stride_tok) || !stride_ok(q_stride_head) || !stride_ok(o_stride_tok) || !stride_ok(o_stride_head))
+    return FI_ERR_ALIGNMENT;
+
+  RunParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const uint16_t*>(q);
+  p.q_stride_tok = q_stride_tok;
+  p.q_stride_head = q_stride_head;
+  p.k = static_cast<const uint16_t*>(k_cache);
+  p.k_stride_page = k_strides[0];
+  p.k_stride_slot = k_strides[1];
+  p.k_stride_head = k_strides[2];
+  p.v = static_cast<const uint16_t*>(v_cache);
+  p.v_stride_page = v_strides[0];
+  p.v_stride_slot = v_strides[1];
+  p.v_stride_head = v_strides[2];
+  p.kv_indices = kv_indices_dev;
+  p.o = static_cast<uint16_t*>(o);
+  p.o_stride_tok = o_stride_tok;
+  p.o_stride_head = o_stride_head;
+  p.lse = lse;
+  p.iws = static_cast<int32_t*>(int_workspace_dev);
+  p.fws = static_cast<float*>(float_workspace_dev);
+  p.partial_o_offset = fi_partial_o_offset(info->max_partial_rows);
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.num_qo_heads = info->num_qo_heads;
+  p.num_kv_heads = info->num_kv_heads;
+  p.group = info->num_qo_heads / info->num_kv_heads;
+  p.page_size = P;
+  int lp = 0;
+  while ((1 << lp) < P) ++lp;
+  p.log2_page = lp;
+
+  // The K/V stride comparison of the BatchAttention PR page ("코드 분석 §2"):
+  // equal strides let V's address reuse K's offset arithmetic.
+  const bool equal = k_strides[0] == v_strides[0] && k_strides[1] == v_strides[1] && k_strides[2] == v_strides[2];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == FI_BF16)
+    e = equal ? launch_run<__nv_bfloat16, true>(p, info->num_ctas, s)
+              : launch_run<__nv_bfloat16, false>(p, info->num_ctas, s);
+  else
+    e = equal ? launch_run<__half, true>(p, info->num_ctas, s) : launch_run<__half, false>(p, info->num_ctas, s);
+  return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
+extern "C" fi_status fi_merge_states(const void* v_a, const float* s_a, const void* v_b, const float* s_b,
+                                     void* v_out, float* s_out, int32_t rows, int32_t heads, int32_t head_dim,
+                                     fi_dtype dtype, void* stream) {
+  if (!v_a || !s_a || !v_b || !s_b || !v_out || !s_out || rows < 0 || heads < 1) return FI_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim) return FI_ERR_UNSUPPORTED;
+  if (dtype != FI_FP16 && dtype != FI_BF16 && dtype != FI_FP32) return FI_ERR_UNSUPPORTED;
+  if (!aligned16(v_a) || !aligned16(v_b) || !aligned16(v_out)) return FI_ERR_ALIGNMENT;
+  const int64_t states = int64_t(rows) * heads;
+  if (states == 0) return FI_OK;
+  const int64_t blocks = (states * 16 + 255) / 256;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (dtype) {
+    case FI_BF16:
+      merge_states_kernel<__nv_bfloat16><<<unsigned(blocks), 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(v_a), s_a, static_cast<const __nv_bfloat16*>(v_b), s_b,
+          static_cast<__nv_bfloat16*>(v_out), s_out, states);
+      break;
+    case FI_FP16:
+      merge_states_kernel<__half><<<unsigned(blocks), 256, 0, s>>>(static_cast<const __half*>(v_a), s_a,
+                                                                   static_cast<const __half*>(v_b), s_b,
+                                                                   static_cast<__half*>(v_out), s_out, states);
+      break;
+    default:
+      merge_states_kernel<float><<<unsigned(blocks), 256, 0, s>>>(static_cast<const float*>(v_a), s_a,
+                                                                  static_cast<const float*>(v_b), s_b,
+                                                                  static_cast<float*>(v_out), s_out, states);
+  }
+  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
+extern "C" fi_status fi_get_device_status(const void* int_workspace_dev, void* stream, int32_t* status_out) {
+  if (!int_workspace_dev || !status_out) return FI_ERR_INVALID_ARG;
+  int32_t word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, static_cast<const int32_t*>(int_workspace_dev) + FI_H_STATUS, sizeof word,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FI_ERR_CUDA;
+  *status_out = (word & kStatusTimeout) ? FI_ERR_TIMEOUT : (word & kStatusBadPlan) ? FI_ERR_DEVICE_CHECK : FI_OK;
+  return FI_OK;
+}

@@ -1,0 +1,436 @@
+// attention_kernel.cuh -- persistent paged-attention kernel, CUDA-core path.
+//
+// One CTA per SM walks its slice of the planned work list (the plan/run split
+// of the FlashInfer paper summary, "3. 동적 부하 분산 스케줄링").  Per item
+// (request b, KV head hk, packed query rows [row0,row1), KV tokens [kv0,kv1)):
+//
+//  * warp 0 streams the chunk's K and V, 64 tokens per stage, into a 4-deep
+//    shared-memory ring with 16-byte cp.async copies whose completion arrives
+//    on the stage's mbarrier.  The page ids of a stage are first staged in
+//    shared memory (wiki page, "1) 블록-스파스 KV 포맷": page indices are
+//    prefetched into shared memory so the kernel reaches KV blocks without
+//    indexing overhead).  Each K/V row of one head is 256 contiguous bytes.
+//  * warps 1..8 hold the G query heads that share KV head hk (GQA packing,
+//    wiki page "Decode 어텐션") in registers, 4 packed rows per half-warp,
+//    and score every KV token read from shared memory once for all of them.
+//    A half-warp owns one token at a time (16 lanes x 8 dims); partial dot
+//    products are reduced with a 5-shuffle butterfly that leaves each lane
+//    the full score of one row.  Softmax is online with a lazily moved
+//    running max (log2 domain).
+//  * the half-warps' states are merged in shared memory; an unsplit item
+//    writes O (storage type) and LSE (natural log), a split item writes its
+//    fp32 partial state, and the CTA that finishes the last chunk of a split
+//    unit merges the unit's partials in chunk order (no inter-CTA waits).
+#pragma once
+#include "attention.cuh"
+
+namespace fi {
+
+__device__ __forceinline__ int32_t ws_header(const int32_t* iws, int f) { return __ldg(iws + f); }
+
+// Row group layout of one pass: ng groups of 4 rows (ng a power of two),
+// 8/ng consumer warps share a group and split its tokens.
+__device__ __forceinline__ int groups_in_pass(int rows) {
+  int g = (rows + kRowsPerGroup - 1) / kRowsPerGroup;
+  return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
+}
+
+// ---------------------------------------------------------------- producer
+
+template <typename T, bool kEqualKV>
+__device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
+                        int32_t off_req) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane >> 4;  // which of the two rows of a copy step
+  const int chunk16 = lane & 15;
+  const int lp = p.log2_page;
+  uint32_t it = 0;
+  for (int32_t i = item_begin; i < item_end; ++i) {
+    const Item item = load_item(p.iws, off_items, i);
+    const Request rq = load_request(p.iws, off_req, item.b);
+    const int nrows = item.row1 - item.row0;
+    const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
+    const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
+    const uint16_t* kh = p.k + int64_t(item.hk) * p.k_stride_head + chunk16 * 8;
+    const uint16_t* vh = p.v + int64_t(item.hk) * p.v_stride_head + chunk16 * 8;
+    const int32_t* pages = p.kv_indices + rq.page_start;
+    for (int pass = 0; pass < passes; ++pass) {
+      // page ids of the next stage, prefetched into registers one stage ahead
+      int32_t nx0 = 0, nx1 = 0;
+      auto fetch_ids = [&](int st) {
+        const int j0 = item.kv0 + st * kStageTokens;
+        const int jn = min(kStageTokens, item.kv1 - j0);
+        const int pg0 = j0 >> lp;
+        const int npg = ((j0 + jn - 1) >> lp) - pg0 + 1;
+        nx0 = lane < npg ? __ldg(pages + pg0 + lane) : 0;
+        nx1 = lane + 32 < npg ? __ldg(pages + pg0 + lane + 32) : 0;
+      };
+      if (nst > 0) fetch_ids(0);
+      for (int st = 0; st < nst; ++st, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        const bool ok = mbar_wait_bounded(&sm.empty[s], ph ^ 1, &sm.abort);
+        if (!ok || sm.abort) continue;
+        sm.pidx[s][lane] = nx0;
+        sm.pidx[s][lane + 32] = nx1;
+        if (st + 1 < nst) fetch_ids(st + 1);
+        __syncwarp();
+        const int j0 = item.kv0 + st * kStageTokens;
+        const int jn = min(kStageTokens, item.kv1 - j0);
+        const int pg0 = j0 >> lp;
+#pragma unroll 4
+        for (int t2 = 0; t2 < kStageTokens; t2 += 2) {
+          const int tok = t2 + sub;
+          const bool valid = tok < jn;
+          const int j = j0 + tok;
+          const int64_t page = valid ? sm.pidx[s][(j >> lp) - pg0] : 0;
+          const int64_t slot = j & (p.page_size - 1);
+          const uint16_t* ks = valid ? kh + page * p.k_stride_page + slot * p.k_stride_slot : p.k;
+          const uint16_t* vs;
+          if constexpr (kEqualKV)
+            vs = valid ? ks + (p.v - p.k) : p.v;  // one offset serves both caches
+          else
+            vs = valid ? vh + page * p.v_stride_page + slot * p.v_stride_slot : p.v;
+          cp_async_16(&sm.k[s][tok][chunk16 * 8], ks, valid ? 16u : 0u);
+          cp_async_16(&sm.v[s][tok][chunk16 * 8], vs, valid ? 16u : 0u);
+        }
+        cp_async_mbar_arrive_noinc(&sm.full[s]);
+      }
+    }
+  }
+  cp_async_wait_all();
+}
+
+// ---------------------------------------------------------------- consumer
+
+// Sum of v[0..3] over the 16 lanes of a half-warp, leaving lane L with the
+// sum of row (L >> 2) & 3: two exchange steps that halve the number of values
+// each lane carries, then two plain butterfly steps.
+__device__ __forceinline__ float reduce_rows4(float v0, float v1, float v2, float v3, int lane16) {
+  const bool hi8 = lane16 & 8;
+  float a0 = hi8 ? v2 : v0, a1 = hi8 ? v3 : v1;
+  const float b0 = hi8 ? v0 : v2, b1 = hi8 ? v1 : v3;
+  a0 += __shfl_xor_sync(0xffffffffu, b0, 8);
+  a1 += __shfl_xor_sync(0xffffffffu, b1, 8);
+  const bool hi4 = lane16 & 4;
+  float keep = hi4 ? a1 : a0;
+  const float send = hi4 ? a0 : a1;
+  keep += __shfl_xor_sync(0xffffffffu, send, 4);
+  keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+  keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+  return keep;
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const float2 a = Elem<T>::to_float2(u.x), b = Elem<T>::to_float2(u.y);
+  const float2 c = Elem<T>::to_float2(u.z), d = Elem<T>::to_float2(u.w);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+template <typename T>
+__device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
+                        int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal) {
+  const int cw = (threadIdx.x >> 5) - 1;  // consumer warp 0..7
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;
+  const int L = lane & 15;
+  const int hwid = cw * 2 + half;
+  const int my_row = L >> 2;  // row of the group whose full score this lane holds
+  const int ct = cw * 32 + lane;  // consumer thread 0..255
+  const int G = p.group;
+  uint32_t it = 0;
+
+  for (int32_t i = item_begin; i < item_end; ++i) {
+    const Item item = load_item(p.iws, off_items, i);
+    const Request rq = load_request(p.iws, off_req, item.b);
+    const int nrows = item.row1 - item.row0;
+    const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
+    const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
+
+    for (int pass = 0; pass < passes; ++pass) {
+      const int prow0 = pass * kRowsPerPass;
+      const int prows = min(kRowsPerPass, nrows - prow0);
+      const int ng = groups_in_pass(prows);
+      const int wpg = kConsumerWarps / ng;
+      const int g = cw % ng;
+      const int slice = cw / ng;
+      const int nhw = 2 * wpg;             // half-warps sharing this row group
+      const int hw = slice * 2 + half;     // index among them
+      const int blocks = kStageTokens / (nhw * kTokBlock);
+
+      // Query rows of this group, pre-scaled by scale*log2(e).
+      float q[kRowsPerGroup][8];
+      int lim_mine = -1;
+#pragma unroll
+      for (int r = 0; r < kRowsPerGroup; ++r) {
+        const int prow = prow0 + g * kRowsPerGroup + r;
+        int lim = -1;
+        if (prow < nrows) {
+          const int row = item.row0 + prow;
+          const int t = row / G;
+          const int head = item.hk * G + (row - t * G);
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(
+              p.q + int64_t(rq.qo_start + t) * p.q_stride_tok + int64_t(head) * p.q_stride_head + L * 8));
+          unpack8<T>(u, q[r]);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) q[r][c] *= p.scale_log2;
+          lim = causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) q[r][c] = 0.f;
+        }
+        if (r == my_row) lim_mine = lim;
+      }
+
+      float o[kRowsPerGroup][8];
+#pragma unroll
+      for (int r = 0; r < kRowsPerGroup; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) o[r][c] = 0.f;
+      float m = -INFINITY, l = 0.f;
+
+      for (int st = 0; st < nst; ++st, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        const bool ok = mbar_wait_bounded(&sm.full[s], ph, &sm.abort);
+        if (ok && !sm.abort) {
+          const int j0 = item.kv0 + st * kStageTokens;
+          for (int blk = 0; blk < blocks; ++blk) {
+            float sc[kTokBlock];
+#pragma unroll
+            for (int u = 0; u < kTokBlock; ++u) {
+              const int tok = hw + (blk * kTokBlock + u) * nhw;
+              const uint4 kv = *reinterpret_cast<const uint4*>(&sm.k[s][tok][L * 8]);
+              float f[8];
+              unpack8<T>(kv, f);
+              float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                d0 = fmaf(q[0][c], f[c], d0);
+                d1 = fmaf(q[1][c], f[c], d1);
+                d2 = fmaf(q[2][c], f[c], d2);
+                d3 = fmaf(q[3][c], f[c], d3);
+              }
+              const float sfull = reduce_rows4(d0, d1, d2, d3, L);
+              const int j = j0 + tok;
+              sc[u] = (j < item.kv1 && j <= lim_mine) ? sfull : -INFINITY;
+            }
+            float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            float m_new = m;
+            if (mx > m + kLazyRescale) m_new = mx;  // also taken on the first visible key (m = -inf)
+            const float alpha = (m_new == m) ? 1.f : ex2(m - m_new);
+            float ps[kTokBlock];
+            float psum = 0.f;
+#pragma unroll
+            for (int u = 0; u < kTokBlock; ++u) {
+              ps[u] = (m_new == -INFINITY) ? 0.f : ex2(sc[u] - m_new);
+              psum += ps[u];
+            }
+            l = l * alpha + psum;
+            m = m_new;
+            float* x = reinterpret_cast<float*>(sm.xch[hwid]);
+            if ((L & 3) == 0) {
+#pragma unroll
+              for (int u = 0; u < kTokBlock; ++u) x[u * 4 + my_row] = ps[u];
+              x[kTokBlock * 4 + my_row] = alpha;
+            }
+            __syncwarp();
+            const float4 al = sm.xch[hwid][kTokBlock];
+            if (__any_sync(0xffffffffu, al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f)) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                o[0][c] *= al.x;
+                o[1][c] *= al.y;
+                o[2][c] *= al.z;
+                o[3][c] *= al.w;
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < kTokBlock; ++u) {
+              const int tok = hw + (blk * kTokBlock + u) * nhw;
+              const float4 pu = sm.xch[hwid][u];
+              const uint4 vv = *reinterpret_cast<const uint4*>(&sm.v[s][tok][L * 8]);
+              float f[8];
+              unpack8<T>(vv, f);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                o[0][c] = fmaf(pu.x, f[c], o[0][c]);
+                o[1][c] = fmaf(pu.y, f[c], o[1][c]);
+                o[2][c] = fmaf(pu.z, f[c], o[2][c]);
+                o[3][c] = fmaf(pu.w, f[c], o[3][c]);
+              }
+            }
+            __syncwarp();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
+      }
+
+      // This half-warp's state -> shared memory, then merge per row.
+#pragma unroll
+      for (int r = 0; r < kRowsPerGroup; ++r) {
+        float4* dst = reinterpret_cast<float4*>(&sm.comb_o[hwid][r][L * 8]);
+        dst[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
+        dst[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
+      }
+      if ((L & 3) == 0) {
+        sm.comb_m[hwid][my_row] = m;
+        sm.comb_l[hwid][my_row] = l;
+      }
+      named_barrier_sync(1, 32 * kConsumerWarps);
+      if (!sm.abort) {
+        for (int task = ct; task < prows * 32; task += 32 * kConsumerWarps) {
+          const int pr = task >> 5, ch = task & 31;
+          const int gg = pr / kRowsPerGroup, r = pr % kRowsPerGroup;
+          float M = -INFINITY;
+          for (int sl = 0; sl < wpg; ++sl)
+            for (int h2 = 0; h2 < 2; ++h2) M = fmaxf(M, sm.comb_m[(gg + sl * ng) * 2 + h2][r]);
+          float Ls = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (M != -INFINITY) {
+            for (int sl = 0; sl < wpg; ++sl)
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const int id = (gg + sl * ng) * 2 + h2;
+                const float w = ex2(sm.comb_m[id][r] - M);
+                Ls += w * sm.comb_l[id][r];
+                const float4 v = *reinterpret_cast<const float4*>(&sm.comb_o[id][r][ch * 4]);
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+              }
+          }
+          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+          acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+          const float lse_v = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+          const int prow = prow0 + pr;
+          if (item.part < 0) {
+            const int row = item.row0 + prow;
+            const int t = row / G;
+            const int head = item.hk * G + (row - t * G);
+            const int64_t tok = rq.qo_start + t;
+            uint2 packed;
+            packed.x = Elem<T>::from_float2(acc.x, acc.y);
+            packed.y = Elem<T>::from_float2(acc.z, acc.w);
+            *reinterpret_cast<uint2*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + ch * 4) =
+                packed;
+            if (ch == 0 && p.lse) p.lse[tok * p.num_qo_heads + head] = lse_v;
+          } else {
+            const int64_t prw = int64_t(item.part) + prow;
+            *reinterpret_cast<float4*>(p.fws + p.partial_o_offset + prw * kHeadDim + ch * 4) = acc;
+            if (ch == 0) p.fws[prw] = lse_v;
+          }
+        }
+      }
+      named_barrier_sync(1, 32 * kConsumerWarps);
+    }
+
+    // Split unit: the CTA that completes its last chunk merges all chunks.
+    // The barriers here depend only on the plan, never on the abort flag,
+    // so every consumer warp passes the same sequence of them.
+    if (item.merge >= 0) {
+      __threadfence();
+      named_barrier_sync(1, 32 * kConsumerWarps);
+      if (ct == 0) {
+        int last = 0;
+        if (!sm.abort) {
+          const int32_t n = __ldg(p.iws + off_merge + FI_MERGE_INTS * item.merge + 4);
+          const int old = atomicAdd(p.iws + off_cnt + item.merge, 1);
+          last = (old == n - 1);
+        }
+        sm.merge_last = last;
+      }
+      named_barrier_sync(1, 32 * kConsumerWarps);
+      if (sm.merge_last) {
+        __threadfence();
+        const int32_t* mu = p.iws + off_merge + FI_MERGE_INTS * item.merge;
+        const int n = __ldg(mu + 4);
+        const int base = __ldg(mu + 5);
+        for (int task = ct; task < nrows * 32; task += 32 * kConsumerWarps) {
+          const int pr = task >> 5, ch = task & 31;
+          float M = -INFINITY;
+          for (int c = 0; c < n; ++c) M = fmaxf(M, __ldcg(p.fws + base + c * nrows + pr));
+          float Ls = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (M != -INFINITY) {
+            for (int c = 0; c < n; ++c) {
+              const int64_t prw = int64_t(base) + c * nrows + pr;
+              const float w = ex2((__ldcg(p.fws + prw) - M) * 1.4426950408889634f);
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(p.fws + p.partial_o_offset + prw * kHeadDim) + ch);
+              Ls += w;
+              acc.x += w * v.x;
+              acc.y += w * v.y;
+              acc.z += w * v.z;
+              acc.w += w * v.w;
+            }
+          }
+          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+          const int row = item.row0 + pr;
+          const int t = row / G;
+          const int head = item.hk * G + (row - t * G);
+          const int64_t tok = rq.qo_start + t;
+          uint2 packed;
+          packed.x = Elem<T>::from_float2(acc.x * inv, acc.y * inv);
+          packed.y = Elem<T>::from_float2(acc.z * inv, acc.w * inv);
+          *reinterpret_cast<uint2*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + ch * 4) = packed;
+          if (ch == 0 && p.lse) p.lse[tok * p.num_qo_heads + head] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
+        }
+        if (ct == 0) p.iws[off_cnt + item.merge] = 0;  // ready for the next run of this plan
+      }
+      named_barrier_sync(1, 32 * kConsumerWarps);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <typename T, bool kEqualKV>
+__global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __grid_constant__ RunParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  RunSmem& sm = *reinterpret_cast<RunSmem*>(smem_raw);
+  const int32_t* iws = p.iws;
+  const int32_t magic = ws_header(iws, FI_H_MAGIC);
+  const int32_t n_items = ws_header(iws, FI_H_NUM_ITEMS);
+  const int32_t n_ctas = ws_header(iws, FI_H_NUM_CTAS);
+  const int32_t off_cta = ws_header(iws, FI_H_OFF_CTA);
+  bool bad = magic != FI_PLAN_MAGIC || n_ctas != int32_t(gridDim.x);
+  int32_t begin = 0, end = 0;
+  if (!bad) {
+    begin = __ldg(iws + off_cta + blockIdx.x);
+    end = __ldg(iws + off_cta + blockIdx.x + 1);
+    bad = begin < 0 || end < begin || end > n_items;
+  }
+  if (bad) {
+    if (threadIdx.x == 0) atomicOr(p.iws + FI_H_STATUS, kStatusBadPlan);
+    return;
+  }
+  const int32_t off_items = ws_header(iws, FI_H_OFF_ITEMS);
+  const int32_t off_req = ws_header(iws, FI_H_OFF_REQUESTS);
+  const int32_t off_merge = ws_header(iws, FI_H_OFF_MERGE);
+  const int32_t off_cnt = ws_header(iws, FI_H_OFF_COUNTERS);
+  const int causal = ws_header(iws, FI_H_CAUSAL);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 32);              // one cp.async arrival per producer lane
+      mbar_init(&sm.empty[s], kConsumerWarps); // one arrival per consumer warp
+    }
+    sm.abort = 0;
+    sm.merge_last = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (threadIdx.x < 32) {
+    produce<T, kEqualKV>(p, sm, begin, end, off_items, off_req);
+  } else {
+    consume<T>(p, sm, begin, end, off_items, off_req, off_merge, off_cnt, causal);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && sm.abort) atomicOr(p.iws + FI_H_STATUS, sm.abort);
+}
+
+}  // namespace fi

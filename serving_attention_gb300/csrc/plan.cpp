@@ -1,0 +1,291 @@
+// plan.cpp -- host planner of the persistent paged-attention kernel.
+//
+// FlashInfer paper summary, section "연구 방법론 / 3. 동적 부하 분산
+// 스케줄링": tile sizes are fixed when the kernel is compiled; at run time the
+// scheduler takes every request's sequence length and builds, on the CPU, a
+// plan that gives all SMs an even share of the work.  The plan is copied to
+// the GPU once per step and the kernel launch never changes, so one CUDA graph
+// replays any plan.  The two tile heights (128 query rows for prefill work,
+// 16 for decode work) are the CTA_TILE_Q_1 / CTA_TILE_Q_2 pair of the
+// BatchAttention PR page, section "코드 분석 §1".
+//
+// Rule (this library's reading of that goal; the pages give no cost model):
+//  * request b -> R = qo_len * G packed rows (row t*G+g = token t, head hk*G+g);
+//    tile T = 16 when R <= 16, else 128;
+//  * unit (b, hk, q-tile) with its visible KV length (bottom-right causal);
+//  * per tile class, a KV chunk length = max(min_chunk, total / (CTAs * split))
+//    rounded up to the class granule; units longer than a chunk are split
+//    into chunks whose fp32 partial states are merged by the kernel;
+//  * chunks are dealt out longest-first to the least-loaded CTA (LPT).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
+
+#include "../../include/fi.h"
+#include "plan_layout.h"
+
+namespace {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round4(int64_t n) { return (n + 3) & ~int64_t(3); }
+
+struct Unit {
+  int32_t b, hk, qt, tile, row0, row1;
+  int64_t kv_eff;
+};
+
+struct Chunk {
+  int64_t cost;
+  int32_t tile, b, hk, qt, idx;
+  int32_t fields[FI_ITEM_INTS];
+};
+
+// Order of the longest-processing-time deal: cost descending, then the
+// 128-row class first, then (b, hk, q-tile, chunk) ascending.  Keys are unique.
+bool deal_before(const Chunk& x, const Chunk& y) {
+  if (x.cost != y.cost) return x.cost > y.cost;
+  if (x.tile != y.tile) return x.tile > y.tile;
+  if (x.b != y.b) return x.b < y.b;
+  if (x.hk != y.hk) return x.hk < y.hk;
+  if (x.qt != y.qt) return x.qt < y.qt;
+  return x.idx < y.idx;
+}
+
+}  // namespace
+
+extern "C" size_t fi_int_workspace_bytes(const fi_plan_config* cfg) {
+  if (!cfg) return 0;
+  int64_t ints = FI_HEADER_INTS + round4(int64_t(cfg->num_ctas) + 1) + int64_t(FI_ITEM_INTS) * cfg->max_items +
+                 int64_t(FI_MERGE_INTS) * cfg->max_merge_units + round4(cfg->max_merge_units) +
+                 int64_t(FI_REQ_INTS) * cfg->max_batch;
+  return size_t(ints) * 4;
+}
+
+extern "C" size_t fi_float_workspace_bytes(const fi_plan_config* cfg, int32_t head_dim) {
+  if (!cfg || head_dim <= 0) return 0;
+  return size_t(fi_partial_o_offset(cfg->max_partial_rows) + cfg->max_partial_rows * int64_t(head_dim)) * 4;
+}
+
+extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                  const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch,
+                                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t page_size, int32_t causal, int32_t num_pages, void* workspace_host,
+                                  size_t workspace_bytes, fi_plan_info* info_out) {
+  if (!cfg || !info_out || !workspace_host || batch < 0) return FI_ERR_INVALID_ARG;
+  if (batch > 0 && (!qo_indptr || !kv_indptr || !last_page_len)) return FI_ERR_INVALID_ARG;
+  if (head_dim != 128) return FI_ERR_UNSUPPORTED;
+  if (page_size < 1 || page_size > 128 || (page_size & (page_size - 1))) return FI_ERR_UNSUPPORTED;
+  if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads) return FI_ERR_UNSUPPORTED;
+  const int32_t group = num_qo_heads / num_kv_heads;
+  if (group > 16) return FI_ERR_UNSUPPORTED;
+  if ((causal != 0 && causal != 1) || cfg->num_ctas < 1 || cfg->split_factor < 1) return FI_ERR_INVALID_ARG;
+  if (cfg->decode_min_chunk < 1 || cfg->prefill_min_chunk < 1) return FI_ERR_INVALID_ARG;
+  if (batch > cfg->max_batch) return FI_ERR_CAPACITY;
+  if (workspace_bytes < fi_int_workspace_bytes(cfg)) return FI_ERR_CAPACITY;
+
+  const int32_t* qo = qo_indptr;
+  const int32_t* kvp = kv_indptr;
+  if (batch > 0 && (qo[0] != 0 || kvp[0] != 0)) return FI_ERR_INVALID_ARG;
+  std::vector<int32_t> lq(batch), lkv(batch);
+  for (int32_t b = 0; b < batch; ++b) {
+    if (qo[b + 1] < qo[b] || kvp[b + 1] < kvp[b]) return FI_ERR_INVALID_ARG;
+    const int32_t pages = kvp[b + 1] - kvp[b];
+    if (pages > 0 && (last_page_len[b] < 1 || last_page_len[b] > page_size)) return FI_ERR_INVALID_ARG;
+    lq[b] = qo[b + 1] - qo[b];
+    const int64_t len = pages == 0 ? 0 : int64_t(pages - 1) * page_size + last_page_len[b];
+    if (len > INT32_MAX) return FI_ERR_UNSUPPORTED;
+    lkv[b] = int32_t(len);
+  }
+  if (num_pages > 0 && batch > 0) {
+    if (!kv_indices && kvp[batch] > 0) return FI_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < kvp[batch]; ++i)
+      if (kv_indices[i] < 0 || kv_indices[i] >= num_pages) return FI_ERR_INVALID_ARG;
+  }
+
+  // Units, in (b, hk, q-tile) order, and per-class visible-KV totals.
+  std::vector<Unit> units;
+  int64_t total_dec = 0, total_pre = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t rows = int64_t(lq[b]) * group;
+    if (rows == 0) continue;
+    const int32_t tile = rows <= FI_TILE_DECODE ? FI_TILE_DECODE : FI_TILE_PREFILL;
+    const int32_t tiles = int32_t(ceil_div(rows, tile));
+    for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
+      for (int32_t qt = 0; qt < tiles; ++qt) {
+        Unit u;
+        u.b = b;
+        u.hk = hk;
+        u.qt = qt;
+        u.tile = tile;
+        u.row0 = qt * tile;
+        u.row1 = int32_t(std::min<int64_t>(rows, int64_t(qt + 1) * tile));
+        int64_t vis = lkv[b];
+        if (causal) {
+          const int64_t last_token = (u.row1 - 1) / group;
+          vis = std::min<int64_t>(vis, int64_t(lkv[b]) - lq[b] + last_token + 1);
+          if (vis < 0) vis = 0;
+        }
+        u.kv_eff = vis;
+        (tile == FI_TILE_DECODE ? total_dec : total_pre) += vis;
+        units.push_back(u);
+      }
+    }
+  }
+
+  const int64_t slots = int64_t(cfg->num_ctas) * cfg->split_factor;
+  auto pick_chunk = [&](int64_t total, int64_t min_chunk, int64_t granule) {
+    int64_t c = std::max<int64_t>(min_chunk, ceil_div(total, slots));
+    return ceil_div(c, granule) * granule;
+  };
+  const int64_t chunk_dec = pick_chunk(total_dec, cfg->decode_min_chunk, std::max(page_size, FI_GRANULE_DECODE));
+  const int64_t chunk_pre = pick_chunk(total_pre, cfg->prefill_min_chunk, std::max(page_size, FI_GRANULE_PREFILL));
+
+  // Chunks of every unit; split units become merge units in unit order.
+  std::vector<Chunk> chunks;
+  chunks.reserve(units.size() * 2);
+  std::vector<int32_t> merge_rows;  // FI_MERGE_INTS per merge unit
+  int64_t partial_rows = 0;
+  for (const Unit& u : units) {
+    const int64_t chunk = u.tile == FI_TILE_DECODE ? chunk_dec : chunk_pre;
+    const int64_t weight = u.tile == FI_TILE_DECODE ? cfg->decode_cost_weight : cfg->prefill_cost_weight;
+    const int64_t n = u.kv_eff == 0 ? 1 : ceil_div(u.kv_eff, chunk);
+    int32_t merge_id = -1;
+    int64_t base = -1;
+    const int32_t nrows = u.row1 - u.row0;
+    if (n > 1) {
+      merge_id = int32_t(merge_rows.size() / FI_MERGE_INTS);
+      base = partial_rows;
+      partial_rows += n * nrows;
+      const int32_t m[FI_MERGE_INTS] = {u.b, u.hk, u.row0, u.row1, int32_t(n), int32_t(base), 0, 0};
+      merge_rows.insert(merge_rows.end(), m, m + FI_MERGE_INTS);
+    }
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t k0 = i * chunk;
+      const int64_t k1 = std::min(u.kv_eff, (i + 1) * chunk);
+      Chunk c;
+      c.cost = (k1 - k0) * weight;
+      c.tile = u.tile;
+      c.b = u.b;
+      c.hk = u.hk;
+      c.qt = u.qt;
+      c.idx = int32_t(i);
+      const int32_t f[FI_ITEM_INTS] = {u.b,         u.hk,       u.row0,
+                                       u.row1,      int32_t(k0), int32_t(k1),
+                                       n > 1 ? int32_t(base + i * nrows) : -1, merge_id};
+      std::memcpy(c.fields, f, sizeof f);
+      chunks.push_back(c);
+    }
+  }
+  const int64_t n_items = int64_t(chunks.size());
+  const int64_t n_merge = int64_t(merge_rows.size() / FI_MERGE_INTS);
+  if (n_items > cfg->max_items || n_merge > cfg->max_merge_units || partial_rows > cfg->max_partial_rows)
+    return FI_ERR_CAPACITY;
+
+  // Longest processing time first onto the least-loaded CTA (ties: lower CTA).
+  std::sort(chunks.begin(), chunks.end(), deal_before);
+  const int32_t C = cfg->num_ctas;
+  using Load = std::pair<int64_t, int32_t>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+  for (int32_t c = 0; c < C; ++c) least.push(Load(0, c));
+  std::vector<int32_t> owner(chunks.size());
+  std::vector<int32_t> per_cta(C, 0);
+  for (size_t i = 0; i < chunks.size(); ++i) {
+    Load l = least.top();
+    least.pop();
+    owner[i] = l.second;
+    per_cta[l.second] += 1;
+    least.push(Load(l.first + chunks[i].cost, l.second));
+  }
+
+  const int64_t off_cta = FI_HEADER_INTS;
+  const int64_t off_items = off_cta + round4(C + 1);
+  const int64_t off_merge = off_items + FI_ITEM_INTS * n_items;
+  const int64_t off_cnt = off_merge + FI_MERGE_INTS * n_merge;
+  const int64_t off_req = off_cnt + round4(n_merge);
+  const int64_t total_ints = off_req + int64_t(FI_REQ_INTS) * batch;
+  if (size_t(total_ints) * 4 > fi_int_workspace_bytes(cfg)) return FI_ERR_CAPACITY;
+
+  int32_t* ws = static_cast<int32_t*>(workspace_host);
+  std::memset(ws, 0, size_t(total_ints) * 4);
+  // CTA c's items occupy [start[c], start[c+1]); within a CTA they keep the
+  // order in which the deal handed them out.
+  std::vector<int32_t> start(C + 1, 0);
+  for (int32_t c = 0; c < C; ++c) start[c + 1] = start[c] + per_cta[c];
+  for (int32_t c = 0; c <= C; ++c) ws[off_cta + c] = start[c];
+  std::vector<int32_t> fill(start.begin(), start.end() - 1);
+  int64_t n_decode = 0;
+  for (size_t i = 0; i < chunks.size(); ++i) {
+    const int32_t slot = fill[owner[i]]++;
+    std::memcpy(ws + off_items + int64_t(FI_ITEM_INTS) * slot, chunks[i].fields, sizeof chunks[i].fields);
+    if (chunks[i].tile == FI_TILE_DECODE) ++n_decode;
+  }
+  if (n_merge) std::memcpy(ws + off_merge, merge_rows.data(), merge_rows.size() * 4);
+  for (int32_t b = 0; b < batch; ++b) {
+    int32_t* r = ws + off_req + int64_t(FI_REQ_INTS) * b;
+    r[0] = qo[b];
+    r[1] = lq[b];
+    r[2] = kvp[b];
+    r[3] = lkv[b];
+  }
+  const int32_t header[FI_HEADER_INTS] = {FI_PLAN_MAGIC,      int32_t(n_items),   int32_t(n_merge), C,
+                                          batch,              causal,             int32_t(off_cta), int32_t(off_items),
+                                          int32_t(off_merge), int32_t(off_cnt),   int32_t(off_req), 0,
+                                          num_qo_heads,       num_kv_heads,       page_size,        int32_t(total_ints)};
+  std::memcpy(ws, header, sizeof header);
+
+  fi_plan_info info;
+  std::memset(&info, 0, sizeof info);
+  info.num_ctas = C;
+  info.num_items = int32_t(n_items);
+  info.num_merge_units = int32_t(n_merge);
+  info.batch = batch;
+  info.num_partial_rows = partial_rows;
+  info.num_qo_heads = num_qo_heads;
+  info.num_kv_heads = num_kv_heads;
+  info.head_dim = head_dim;
+  info.page_size = page_size;
+  info.causal = causal;
+  info.chunk_decode = int32_t(chunk_dec);
+  info.chunk_prefill = int32_t(chunk_pre);
+  info.num_decode_items = int32_t(n_decode);
+  info.num_prefill_items = int32_t(n_items - n_decode);
+  info.int_ws_bytes_used = total_ints * 4;
+  info.max_partial_rows = cfg->max_partial_rows;
+  *info_out = info;
+  return FI_OK;
+}
+
+extern "C" fi_status fi_plan(const fi_plan_config* cfg, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch,
+                             int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                             int32_t causal, int32_t num_pages, void* int_workspace_dev, void* pinned_staging_host,
+                             size_t staging_bytes, void* stream, fi_plan_info* info_out) {
+  if (!int_workspace_dev || !pinned_staging_host) return FI_ERR_INVALID_ARG;
+  fi_status st = fi_plan_host(cfg, qo_indptr, kv_indptr, kv_indices, last_page_len, batch, num_qo_heads,
+                              num_kv_heads, head_dim, page_size, causal, num_pages, pinned_staging_host,
+                              staging_bytes, info_out);
+  if (st != FI_OK) return st;
+  cudaError_t e = cudaMemcpyAsync(int_workspace_dev, pinned_staging_host, size_t(info_out->int_ws_bytes_used),
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
+extern "C" const char* fi_status_string(fi_status s) {
+  switch (s) {
+    case FI_OK: return "ok";
+    case FI_ERR_INVALID_ARG: return "invalid argument";
+    case FI_ERR_UNSUPPORTED: return "unsupported shape, page size or dtype";
+    case FI_ERR_CAPACITY: return "plan exceeds workspace capacity";
+    case FI_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case FI_ERR_CUDA: return "CUDA runtime error";
+    case FI_ERR_DEVICE_CHECK: return "device-side check failed";
+    case FI_ERR_TIMEOUT: return "device-side bounded wait ran out";
+  }
+  return "unknown status";
+}

@@ -1,0 +1,53 @@
+// plan_layout.h -- layout of the int workspace written by the planner and
+// read by the persistent kernel.  All fields are int32.
+//
+//   header[16]   FI_H_* below
+//   cta_indptr   num_ctas + 1 entries: CTA c runs items [cta_indptr[c], cta_indptr[c+1])
+//   items        FI_ITEM_INTS each: {b, hk, row0, row1, kv0, kv1, part, merge}
+//                  rows are packed rows of request b (row = token * G + g),
+//                  [kv0, kv1) the KV token range of this chunk,
+//                  part = first fp32 partial-state row or -1 (unsplit),
+//                  merge = merge unit or -1
+//   merge units  FI_MERGE_INTS each: {b, hk, row0, row1, n_chunks, part_base, 0, 0};
+//                  chunk i of the unit wrote partial rows part_base + i * (row1 - row0) ...
+//   counters     one per merge unit, zero between runs (the merging CTA resets it)
+//   requests     FI_REQ_INTS each: {qo_start, qo_len, page_start, kv_len}
+// Every section starts on a multiple of 4 ints (16 bytes).
+//
+// Float workspace: partial LSE (natural log) at [0, max_partial_rows), partial
+// O (already divided by its own softmax sum) at
+// fi_partial_o_offset(max_partial_rows), head_dim floats per row.
+#pragma once
+#include <stdint.h>
+
+#define FI_PLAN_MAGIC 0x46495031
+#define FI_HEADER_INTS 16
+#define FI_ITEM_INTS 8
+#define FI_MERGE_INTS 8
+#define FI_REQ_INTS 4
+
+#define FI_TILE_DECODE 16
+#define FI_TILE_PREFILL 128
+#define FI_GRANULE_DECODE 64
+#define FI_GRANULE_PREFILL 128
+
+enum {
+  FI_H_MAGIC = 0,
+  FI_H_NUM_ITEMS = 1,
+  FI_H_NUM_MERGE = 2,
+  FI_H_NUM_CTAS = 3,
+  FI_H_BATCH = 4,
+  FI_H_CAUSAL = 5,
+  FI_H_OFF_CTA = 6,
+  FI_H_OFF_ITEMS = 7,
+  FI_H_OFF_MERGE = 8,
+  FI_H_OFF_COUNTERS = 9,
+  FI_H_OFF_REQUESTS = 10,
+  FI_H_STATUS = 11,
+  FI_H_NUM_QO_HEADS = 12,
+  FI_H_NUM_KV_HEADS = 13,
+  FI_H_PAGE_SIZE = 14,
+  FI_H_TOTAL_INTS = 15
+};
+
+static inline int64_t fi_partial_o_offset(int64_t max_partial_rows) { return (max_partial_rows + 63) / 64 * 64; }

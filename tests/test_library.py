@@ -1,0 +1,72 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol its
+header declares, and rejects bad arguments on the host before touching CUDA."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import serving_attention_gb300 as fi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(fi_[a-z_0-9]+)\s*\(", text, re.M))
+    return names
+
+
+def test_exports_every_declared_symbol():
+    lib = fi.load()
+    names = _declared()
+    assert {"fi_plan", "fi_batch_paged_attention_run", "fi_merge_states"} <= names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(fi.EXPORTS) <= names
+
+
+def test_status_strings():
+    lib = fi.load()
+    for s in range(8):
+        assert lib.fi_status_string(s)
+
+
+def test_run_rejects_bad_arguments_before_cuda():
+    lib = fi.load()
+    info = fi.PlanInfo(num_ctas=1, head_dim=128, page_size=16, num_qo_heads=8, num_kv_heads=2)
+    ks = (ctypes.c_int64 * 3)(4096, 256, 128)
+    args = [ctypes.byref(info), 16, 1024, 128, 4, 32, ks, 64, ks, 10, 48, 80, 1024, 128, None, fi.BF16, 0.1, 96,
+            112, None]
+    # the pointers are fake: only argument checks that return before any CUDA call are exercised
+    bad = list(args)
+    bad[0] = None
+    assert lib.fi_batch_paged_attention_run(*bad) == 1
+    bad = list(args)
+    bad[1] = 18  # misaligned q
+    assert lib.fi_batch_paged_attention_run(*bad) == 4
+    bad = list(args)
+    bad[15] = fi.FP32
+    assert lib.fi_batch_paged_attention_run(*bad) == 2
+    bad = list(args)
+    bad[6] = (ctypes.c_int64 * 3)(4096, 250, 128)  # stride not a multiple of 16 bytes
+    assert lib.fi_batch_paged_attention_run(*bad) == 4
+
+
+def test_merge_rejects_bad_arguments_before_cuda():
+    lib = fi.load()
+    assert lib.fi_merge_states(None, 16, 32, 48, 64, 80, 4, 2, 128, fi.BF16, None) == 1
+    assert lib.fi_merge_states(16, 16, 32, 48, 64, 80, 4, 2, 64, fi.BF16, None) == 2
+    assert lib.fi_merge_states(18, 16, 32, 48, 64, 80, 4, 2, 128, fi.BF16, None) == 4
+    assert lib.fi_merge_states(16, 16, 32, 48, 64, 80, 0, 2, 128, fi.BF16, None) == 0  # nothing to do
+
+
+def test_workspace_sizes():
+    cfg = fi.make_plan_config(152)
+    assert fi.int_workspace_bytes(cfg) % 16 == 0
+    assert fi.float_workspace_bytes(cfg, 128) >= cfg.max_partial_rows * 129 * 4

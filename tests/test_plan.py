@@ -1,0 +1,195 @@
+"""The host planner (C++, through the C ABI, no GPU) against the independent
+Python re-derivation of the same rule, byte for byte, plus the invariants the
+rule promises (coverage, no empty work, LPT balance, determinism)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import serving_attention_gb300 as fi
+import workloads
+from oracle import plan_ref
+
+HEADER = 16
+
+
+def _cfg(num_ctas=148, **kw):
+    c = fi.make_plan_config(num_ctas, **kw)
+    return c, c.as_dict()
+
+
+def _plan_both(cfg, cfgd, qo, kvp, kvi, lpl, hq, hkv, page, causal, num_pages):
+    st_c, ws_c, info_c = fi.plan_host(cfg, qo, kvp, kvi, lpl, hq, hkv, 128, page, causal, num_pages)
+    st_p, ws_p, info_p = plan_ref.make_plan(cfgd, qo, kvp, kvi, lpl, hq, hkv, 128, page, causal, num_pages)
+    assert st_c == st_p, (st_c, st_p)
+    if st_c == 0:
+        assert np.array_equal(ws_c, ws_p), np.nonzero(ws_c != ws_p)[0][:10]
+        got = info_c.as_dict()
+        for k, v in info_p.items():
+            assert got[k] == v, (k, got[k], v)
+    return st_c, ws_c, info_c
+
+
+def _random_lengths(rng, batch, page):
+    qo = rng.choice([1, 1, 1, 2, 4, 5, 17, 40, 130, 300], size=batch)
+    kv = rng.integers(0, 3000, size=batch)
+    kv[rng.random(batch) < 0.1] = 0
+    return qo, kv
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_plan_matches_reference_random(seed):
+    rng = np.random.default_rng(seed)
+    batch = int(rng.integers(1, 40))
+    page = int(rng.choice([1, 2, 4, 16, 32, 128]))
+    hkv = int(rng.choice([1, 2, 8]))
+    group = int(rng.choice([1, 2, 4, 8, 16]))
+    causal = int(rng.integers(0, 2))
+    qo, kv = _random_lengths(rng, batch, page)
+    kvp, lpl = workloads._pages_for(kv, page)
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    nnz = int(kvp[-1])
+    kvi = rng.permutation(nnz + 5)[:nnz].astype(np.int32)
+    cfg, cfgd = _cfg(num_ctas=int(rng.choice([1, 7, 148, 152])), split_factor=int(rng.integers(1, 6)),
+                     decode_min_chunk=int(rng.choice([64, 256])), prefill_min_chunk=int(rng.choice([128, 1024])))
+    st, ws, info = _plan_both(cfg, cfgd, qop, kvp, kvi, lpl, hkv * group, hkv, page, causal, nnz + 5)
+    assert st == 0
+    _check_invariants(ws, qop, kv, hkv * group, hkv, causal, cfgd)
+
+
+def _check_invariants(ws, qop, kv, hq, hkv, causal, cfgd):
+    G = hq // hkv
+    n_items, n_merge, C = ws[1], ws[2], ws[3]
+    off_cta, off_items, off_merge, off_cnt, off_req = ws[6], ws[7], ws[8], ws[9], ws[10]
+    cta = ws[off_cta:off_cta + C + 1]
+    assert cta[0] == 0 and cta[-1] == n_items and np.all(np.diff(cta) >= 0)
+    items = ws[off_items:off_items + 8 * n_items].reshape(-1, 8)
+    assert np.all(ws[off_cnt:off_cnt + n_merge] == 0)
+    req = ws[off_req:off_req + 4 * (len(qop) - 1)].reshape(-1, 4)
+    assert np.array_equal(req[:, 3], kv)
+    # coverage: per (b, hk) the row ranges tile [0, R); per unit the chunks tile [0, kv_eff)
+    by_unit = {}
+    for it in items:
+        b, hk, r0, r1, k0, k1, part, merge = (int(x) for x in it)
+        by_unit.setdefault((b, hk, r0, r1), []).append((k0, k1, part, merge))
+    for b in range(len(qop) - 1):
+        R = int(qop[b + 1] - qop[b]) * G
+        for hk in range(hkv):
+            units = sorted((r0, r1) for (bb, h, r0, r1) in by_unit if bb == b and h == hk)
+            if R == 0:
+                assert not units
+                continue
+            assert units[0][0] == 0 and units[-1][1] == R
+            assert all(units[i][1] == units[i + 1][0] for i in range(len(units) - 1))
+            for (r0, r1) in units:
+                chunks = sorted(by_unit[(b, hk, r0, r1)])
+                lq, lkv = int(qop[b + 1] - qop[b]), int(kv[b])
+                t_last = (r1 - 1) // G
+                need = min(lkv, max(0, lkv - lq + t_last + 1)) if causal else lkv
+                assert chunks[0][0] == 0 and chunks[-1][1] == need
+                assert all(chunks[i][1] == chunks[i + 1][0] for i in range(len(chunks) - 1))
+                if need > 0:
+                    assert all(k1 > k0 for (k0, k1, _, _) in chunks), "empty chunk in a non-empty unit"
+                else:
+                    assert len(chunks) == 1
+                if len(chunks) > 1:
+                    m = chunks[0][3]
+                    assert m >= 0 and all(c[3] == m for c in chunks)
+                    mu = ws[off_merge + 8 * m: off_merge + 8 * m + 8]
+                    assert tuple(mu[:4]) == (b, hk, r0, r1) and mu[4] == len(chunks)
+                    parts = [c[2] for c in chunks]
+                    assert parts == [mu[5] + i * (r1 - r0) for i in range(len(chunks))]
+                else:
+                    assert chunks[0][2] == -1 and chunks[0][3] == -1
+    # LPT bound: max CTA load <= mean load + largest item
+    w = {16: cfgd["decode_cost_weight"], 128: cfgd["prefill_cost_weight"]}
+    cost = []
+    for it in items:
+        R = int(qop[it[0] + 1] - qop[it[0]]) * G
+        cost.append((int(it[5]) - int(it[4])) * w[16 if R <= 16 else 128])
+    cost = np.array(cost, dtype=np.int64)
+    loads = np.array([cost[cta[c]:cta[c + 1]].sum() for c in range(C)])
+    if cost.size:
+        assert loads.max() <= cost.sum() / C + cost.max()
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "llama8b_decode", "ragged_prefill", "continuous_batch"])
+def test_plan_matches_reference_workloads(name):
+    rng_lengths = {
+        "tiny_decode": lambda: (np.ones(4, np.int64), np.random.default_rng(1000).integers(1, 513, size=4), 8, 2, 16, 0),
+        "llama8b_decode": lambda: (np.ones(64, np.int64),
+                                   workloads.llama8b_decode_lengths(np.random.default_rng(2000)), 32, 8, 16, 0),
+        "ragged_prefill": lambda: (*workloads.ragged_prefill_lengths(np.random.default_rng(3000)), 32, 8, 16, 1),
+        "continuous_batch": lambda: (*workloads.continuous_batch_lengths(np.random.default_rng(5000)), 32, 8, 16, 1),
+    }
+    qo, kv, hq, hkv, page, causal = rng_lengths[name]()
+    kvp, lpl = workloads._pages_for(np.asarray(kv), page)
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    nnz = int(kvp[-1])
+    kvi = np.random.default_rng(7).permutation(nnz).astype(np.int32)
+    cfg, cfgd = _cfg(num_ctas=152)
+    st, ws, info = _plan_both(cfg, cfgd, qop, kvp, kvi, lpl, hq, hkv, page, causal, nnz)
+    assert st == 0
+    _check_invariants(ws, qop, np.asarray(kv), hq, hkv, causal, cfgd)
+
+
+def test_plan_is_deterministic():
+    rng = np.random.default_rng(9)
+    qo, kv = _random_lengths(rng, 30, 16)
+    kvp, lpl = workloads._pages_for(kv, 16)
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    kvi = np.arange(int(kvp[-1]), dtype=np.int32)
+    cfg, _ = _cfg()
+    a = fi.plan_host(cfg, qop, kvp, kvi, lpl, 32, 8, 128, 16, 1)[1]
+    b = fi.plan_host(cfg, qop, kvp, kvi, lpl, 32, 8, 128, 16, 1)[1]
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("case,status", [
+    ("head_dim", 2), ("page_size", 2), ("heads", 2), ("group", 2), ("indptr", 1), ("lpl", 1), ("index", 1),
+    ("capacity", 3), ("causal", 1),
+])
+def test_plan_rejects(case, status):
+    qo = np.array([0, 1, 3], np.int32)
+    kvp = np.array([0, 2, 3], np.int32)
+    kvi = np.array([0, 1, 2], np.int32)
+    lpl = np.array([5, 16], np.int32)
+    args = dict(hq=8, hkv=2, d=128, page=16, causal=0, num_pages=3)
+    cfg, cfgd = _cfg()
+    if case == "head_dim":
+        args["d"] = 64
+    elif case == "page_size":
+        args["page"] = 12
+    elif case == "heads":
+        args["hq"] = 7
+    elif case == "group":
+        args["hq"], args["hkv"] = 34, 1
+    elif case == "indptr":
+        qo = np.array([0, 3, 1], np.int32)
+    elif case == "lpl":
+        lpl = np.array([0, 16], np.int32)
+    elif case == "index":
+        kvi = np.array([0, 1, 3], np.int32)
+    elif case == "capacity":
+        cfg, cfgd = _cfg(max_items=1)
+    elif case == "causal":
+        args["causal"] = 2
+    st, ws, _ = fi.plan_host(cfg, qo, kvp, kvi, lpl, args["hq"], args["hkv"], args["d"], args["page"],
+                             args["causal"], args["num_pages"])
+    assert st == status and ws is None
+    st_p, _, _ = plan_ref.make_plan(cfgd, qo, kvp, kvi, lpl, args["hq"], args["hkv"], args["d"], args["page"],
+                                    args["causal"], args["num_pages"])
+    assert st_p == status
+
+
+def test_default_capacity_holds_every_workload():
+    """The default config's capacities hold all five workloads (10 draws of the mix)."""
+    cfg, cfgd = _cfg(num_ctas=152)
+    cases = [workloads.continuous_batch_lengths(np.random.default_rng(5000 + r)) + (1,) for r in range(10)]
+    cases.append(workloads.ragged_prefill_lengths(np.random.default_rng(3000)) + (1,))
+    cases.append((np.ones(64, np.int64), workloads.llama8b_decode_lengths(np.random.default_rng(2000)), 0))
+    for qo, kv, causal in cases:
+        kvp, lpl = workloads._pages_for(np.asarray(kv), 16)
+        qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+        st, ws, info = fi.plan_host(cfg, qop, kvp, np.zeros(int(kvp[-1]), np.int32), lpl, 32, 8, 128, 16, causal)
+        assert st == 0, st
