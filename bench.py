@@ -1,0 +1,432 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+Headline (N=1): the Llama-3-8B-shaped decode batch -- 64 requests, one query
+token each, KV lengths floor(exp U(ln 512, ln 32768)), 32 query / 8 KV heads,
+head_dim 128, pages of 16 shuffled over a pool sized to the total, bf16.  One
+step = fi_plan on the host (work list copied to the device) + one launch of
+the persistent kernel through the C ABI.  The metric is algorithmic HBM bytes
+(K and V of every visible token once per KV head, plus Q, O and LSE) per
+second of device time; the KV cache (2 GB) is larger than L2, so no flush is
+needed between steps.
+
+The same JSON line also reports the ragged causal prefill batch (TFLOP/s,
+tensor-core bound) and the continuous-batching mix replayed through one CUDA
+graph across 10 re-plans, each against its own roof.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+path has no exchange step); rank 0 prints the line with the max over ranks.
+`--impl reference` times the fp64 CPU oracle on bounded samples of the same
+workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-KV attention: decode HBM GB/s, prefill TFLOPS (fraction of GB300 roof)"
+WORKLOAD = ("llama8b_decode: 64 requests, qo_len 1, kv_len floor(exp U(ln 512, ln 32768)), 32 q / 8 kv heads, "
+            "head_dim 128, page 16, shuffled pages, bf16, N(0,1)")
+HOT_KERNEL = "paged_attention_kernel"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "serving_attention_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_per_launch(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t.get(workload)
+        if e and e.get("kernel_hash") == _kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fi_clocks_{os.getpid()}_{index}.csv")
+
+    def __enter__(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = np.array([num(r[1]) for r in rows])
+        mx = np.array([num(r[2]) for r in rows])
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.nanmedian(sm)), "sm_max_mhz": float(np.nanmax(mx)), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- workload
+
+
+def algorithmic(b):
+    """Decode bytes (KV once per KV head + Q + O + LSE) and attention FLOPs of a batch.
+    FLOPs: 'formula' = 4*qo*kv*d*Hq (halved when causal), 'exact' = 4*d*Hq*visible pairs."""
+    kv = b.kv_lens().astype(np.float64)
+    qo = b.qo_lens().astype(np.float64)
+    d, hq, hkv = 128, b.num_qo_heads, b.num_kv_heads
+    kv_bytes = float((kv * hkv * d * 2 * 2).sum())
+    io_bytes = float(qo.sum() * hq * (d * 2 * 2 + 4))
+    pairs = qo * (kv - qo) + qo * (qo + 1) / 2 if b.causal else qo * kv
+    exact = float((4 * d * hq * pairs).sum())
+    formula = float((4 * d * hq * qo * kv).sum() / (2 if b.causal else 1))
+    return kv_bytes + io_bytes, formula, exact
+
+
+def _device_setup(local_rank):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    return torch.device("cuda", local_rank)
+
+
+def bench_decode(dev, steps, warmup, clocks_index):
+    import torch
+
+    import serving_attention_gb300 as fi
+    import workloads
+
+    b = workloads.llama8b_decode(device=dev)
+    cfg = fi.default_plan_config(dev.index)
+    ws = fi.Workspace(cfg, device=dev)
+    kvi = torch.as_tensor(b.kv_indices, device=dev)
+    o = torch.empty_like(b.q)
+    lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    args = (b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 32, 8, 128, 16, 0, b.num_pages)
+
+    def step(ev=None):
+        info = fi.plan(ws, *args)
+        if ev is not None:
+            ev[0].record(stream)
+        fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+        if ev is not None:
+            ev[1].record(stream)
+        return info
+
+    for _ in range(warmup):
+        info = step()
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0, "device status not ok"
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(clocks_index) as cs:
+        t0.record(stream)
+        for i in range(steps):
+            step(kev[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    kern_ms = [a.elapsed_time(c) for a, c in kev]
+    assert fi.device_status(ws) == 0, "device status not ok"
+    nbytes, _, _ = algorithmic(b)
+
+    # end to end through the public API from pinned host buffers: Q and the
+    # page table in (plus the plan's work list), O and LSE out.  The KV cache
+    # stays resident in HBM: it is the serving state that persists across steps.
+    q_h = b.q.cpu().pin_memory()
+    kvi_h = torch.as_tensor(b.kv_indices).pin_memory()
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d = torch.empty_like(b.q)
+    h2d = q_h.numel() * q_h.element_size() + kvi_h.numel() * 4
+    d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        kvi.copy_(kvi_h, non_blocking=True)
+        info = fi.plan(ws, *args)
+        fi.run(ws, info, q_d, b.k, b.v, kvi, o, lse, b.sm_scale)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        return info
+
+    for _ in range(warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        info_e = e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    plan_bytes = info_e.int_ws_bytes_used
+    return dict(batch=b, total_ms=total_ms, kern_ms=kern_ms, bytes=nbytes, clocks=cs.summary(), e2e_ms=e2e_ms,
+                h2d=h2d + plan_bytes, d2h=d2h, info=info)
+
+
+def bench_secondary(dev, reps=5):
+    """Prefill TFLOP/s and the continuous-batching mix, CUDA events, L2 flushed between reps."""
+    import torch
+
+    import serving_attention_gb300 as fi
+    import workloads
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    cfg = fi.default_plan_config(dev.index)
+    ws = fi.Workspace(cfg, device=dev)
+    for name, maker in (("ragged_prefill", workloads.ragged_prefill), ("continuous_batch", workloads.continuous_batch)):
+        b = maker(device=dev)
+        info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                       128, b.page_size, b.causal, b.num_pages)
+        kvi = torch.as_tensor(b.kv_indices, device=dev)
+        o = torch.empty_like(b.q)
+        lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
+        fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            c.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(c))
+        assert fi.device_status(ws) == 0
+        ms = float(np.median(ts))
+        nbytes, formula, exact = algorithmic(b)
+        out[name] = dict(ms=ms, tflops_formula=formula / ms / 1e9, tflops_exact=exact / ms / 1e9,
+                         decode_gbs=nbytes / ms / 1e6, items=info.num_items)
+        del b, o, lse, g
+        torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------- reference arm
+
+
+def reference_sample(budget_s: float):
+    """Time the fp64 oracle on whole requests of the decode workload (all heads)
+    until about budget_s of CPU work; returns (GB/s of algorithmic bytes, sample text, cores)."""
+    import torch
+
+    import oracle
+    import workloads
+
+    b = workloads.llama8b_decode(device="cpu")
+    q, k, v = workloads.host_views(b)
+    prob = oracle.Problem(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 32, 8, 16, 0, b.sm_scale,
+                          oracle.BF16, q, k, v)
+    kv = b.kv_lens()
+    order = np.argsort(kv)  # short requests first so the sample spans several
+    done_bytes, t_used, n_req = 0.0, 0.0, 0
+    for r in order:
+        rows = np.full(32, int(b.qo_indptr[r]), np.int32)
+        heads = np.arange(32, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.attention_select(prob, rows, heads)
+        t_used += time.perf_counter() - t0
+        done_bytes += kv[r] * 8 * 128 * 2 * 2 + 32 * (128 * 2 * 2 + 4)
+        n_req += 1
+        if t_used >= budget_s:
+            break
+    cores = os.cpu_count()
+    return done_bytes / t_used / 1e9, f"{n_req} of 64 requests (all 32 heads), {done_bytes / 1e9:.2f} GB of KV", cores, t_used
+
+
+# ----------------------------------------------------------------- driver
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
+        return dist, int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+_DIST = None
+
+
+def _barrier():
+    if _DIST is not None:
+        _DIST.barrier()
+
+
+def _max_over_ranks(x: float, dev) -> float:
+    if _DIST is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    _DIST.all_reduce(t, op=_DIST.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    global _DIST
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    a = ap.parse_args()
+    dist, rank, world, local = _dist()
+    _DIST = dist
+    hbm, tf, tf_sus, peak_src = _peaks()
+
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        steps = max(1, a.steps)
+        per = max(0.5, min(a.cpu_budget, 150.0 / (steps + a.warmup)))
+        for _ in range(a.warmup):
+            reference_sample(per / 4)
+        vals, used = [], 0.0
+        for _ in range(steps):
+            gbs, sample, cores, t = reference_sample(per)
+            vals.append(gbs)
+            used += t
+        v = float(np.median(vals))
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": steps,
+                "warmup": a.warmup, "ms_per_step": used / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "global_batch": 64, "kind": "fp64 CPU oracle"},
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    import serving_attention_gb300 as fi
+
+    fi.load()
+    dev = _device_setup(local)
+    r = bench_decode(dev, a.steps, a.warmup, clocks_index=local)
+    total_ms = _max_over_ranks(r["total_ms"], dev)
+    value = r["bytes"] * world / (total_ms / a.steps) / 1e6  # GB/s over all ranks
+    kern_ms = float(np.mean(r["kern_ms"]))
+    achieved = r["bytes"] / kern_ms / 1e6
+    e2e_ms = _max_over_ranks(r["e2e_ms"], dev)
+    e2e = r["bytes"] * world / (e2e_ms / a.steps) / 1e6
+    traffic = _traffic_per_launch("llama8b_decode")
+    sec = None if (a.no_secondary or rank != 0) else bench_secondary(dev)
+    cpu = None
+    if rank == 0 and world == 1:
+        gbs, sample, cores, t = reference_sample(a.cpu_budget)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample + f", {t:.1f} s"}
+    if rank != 0:
+        return
+    info = r["info"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 64 * world, "per_gpu_batch": 64,
+                   "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (2.0 GB of KV per step)",
+                   "step": "fi_plan (host, work list copied to device) + one persistent kernel launch",
+                   "num_ctas": info.num_ctas, "items": info.num_items, "split_units": info.num_merge_units},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "kernel": HOT_KERNEL, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": r["bytes"], "kernel_ms": kern_ms},
+        "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},
+        "gpu_launches": a.steps,
+        "clocks": r["clocks"],
+        "cpu_baseline": cpu,
+    }
+    if sec:
+        p = sec["ragged_prefill"]
+        m = sec["continuous_batch"]
+        line["prefill"] = {"workload": "ragged_prefill: 16 requests, qo U[128,4096], prefix U[0,2048], causal",
+                           "ms": p["ms"], "tflops_formula": p["tflops_formula"], "tflops_exact": p["tflops_exact"],
+                           "peak_tflops": tf, "frac_formula": p["tflops_formula"] / tf, "bound": "tensor"}
+        line["mix"] = {"workload": "continuous_batch: 8 chunked prefill (512) + 120 zipf decode, unequal K/V strides",
+                       "ms": m["ms"], "decode_gbs_over_kernel": m["decode_gbs"],
+                       "tflops_exact_over_kernel": m["tflops_exact"]}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

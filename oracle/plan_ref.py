@@ -28,8 +28,9 @@ Rule:
  5. cost = kv length of the item * class weight.  Items are sorted by
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
     load, ties to the smaller CTA index (longest processing time first).
- 6. Output: header, per-CTA CSR offsets, items in CTA order (in assignment
-    order within a CTA), merge units, zeroed merge counters, request table.
+ 6. Output: header, per-CTA CSR offsets, items in CTA order (within a CTA the
+    128-row items first, then the 16-row items, each in the order dealt),
+    merge units, zeroed merge counters, request table.
 """
 from __future__ import annotations
 
@@ -174,7 +175,9 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos
-        for fields in per_cta[c]:
+        # 128-row tiles first, then 16-row tiles, each in the order dealt
+        mine = [f for f in per_cta[c] if lq[f[0]] * group > 16] + [f for f in per_cta[c] if lq[f[0]] * group <= 16]
+        for fields in mine:
             ws[off_items + ITEM_INTS * pos: off_items + ITEM_INTS * (pos + 1)] = fields
             pos += 1
     ws[off_cta + C] = pos

@@ -86,7 +86,7 @@ template <typename T, bool kEqualKV>
 cudaError_t launch_run(const RunParams& p, int num_ctas, cudaStream_t stream) {
   static bool configured[kMaxDevices] = {};
   auto kern = paged_attention_kernel<T, kEqualKV>;
-  const int smem = int(sizeof(RunSmem));
+  const int smem = int(kSmemBytes);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -102,6 +102,44 @@ cudaError_t launch_run(const RunParams& p, int num_ctas, cudaStream_t stream) {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool stride_ok(int64_t elems) { return elems > 0 && (elems * 2) % 16 == 0; }
 
+// cuTensorMapEncodeTiled, fetched through the runtime so the library does
+// not link the driver library directly.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return EncodeTiledFn(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// 16-bit tensor map with 128-byte swizzle; dims/strides innermost first,
+// strides in elements (the innermost stride is 1).
+bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank, const uint64_t* dims,
+              const int64_t* strides_elems, const uint32_t* box) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) gstride[i] = cuuint64_t(strides_elems[i]) * 2;
+  return enc(map, type, cuuint32_t(rank), const_cast<void*>(base), gdim, gstride, bdim, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fi
 
 using namespace fi;
@@ -113,7 +151,7 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) return FI_ERR_CUDA;
   auto kern = paged_attention_kernel<__nv_bfloat16, false>;
-  const int smem = int(sizeof(RunSmem));
+  const int smem = int(kSmemBytes);
   int per_sm = 0;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
@@ -189,6 +227,27 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   int lp = 0;
   while ((1 << lp) < P) ++lp;
   p.log2_page = lp;
+  p.num_pages = num_pages;
+
+  // 128-row tiles go to the tensor cores when every TMA box of a page is a
+  // whole number of 1024-byte swizzle atoms (P >= 8) and a tile holds whole
+  // tokens (G divides 128); otherwise the CUDA-core path runs them.
+  const int G = p.group;
+  p.tc_prefill = (P >= kMinTmaPage && kTileM % G == 0) ? 1 : 0;
+  if (p.tc_prefill) {
+    const CUtensorMapDataType tt =
+        dtype == FI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t qd[3] = {uint64_t(kHeadDim), uint64_t(info->num_qo_heads), uint64_t(q_num_tokens)};
+    const int64_t qs[2] = {q_stride_head, q_stride_tok};
+    const uint32_t qb[3] = {64u, uint32_t(G), uint32_t(kTileM / G)};
+    const uint64_t kd[4] = {uint64_t(kHeadDim), uint64_t(info->num_kv_heads), uint64_t(P), uint64_t(num_pages)};
+    const int64_t ks[3] = {k_strides[2], k_strides[1], k_strides[0]};  // head, slot, page
+    const int64_t vs[3] = {v_strides[2], v_strides[1], v_strides[0]};
+    const uint32_t kb[4] = {64u, 1u, uint32_t(P), 1u};
+    if (!make_map(&p.tm_q, tt, q, 3, qd, qs, qb) || !make_map(&p.tm_k, tt, k_cache, 4, kd, ks, kb) ||
+        !make_map(&p.tm_v, tt, v_cache, 4, kd, vs, kb))
+      return FI_ERR_UNSUPPORTED;
+  }
 
   // The K/V stride comparison of the BatchAttention PR page ("코드 분석 §2"):
   // equal strides let V's address reuse K's offset arithmetic.

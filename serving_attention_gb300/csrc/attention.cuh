@@ -1,6 +1,7 @@
 // attention.cuh -- parameters and shared-memory layout of the persistent
-// paged-attention kernel (CUDA-core path).
+// paged-attention kernel.
 #pragma once
+#include <cuda.h>
 #include <stdint.h>
 
 #include "plan_layout.h"
@@ -9,6 +10,8 @@
 namespace fi {
 
 constexpr int kHeadDim = 128;
+
+// CUDA-core path (16-row decode tiles; 128-row tiles when pages are < 8 tokens)
 constexpr int kStageTokens = 64;       // KV tokens per pipeline stage
 constexpr int kStages = 4;             // depth of the K/V ring
 constexpr int kConsumerWarps = 8;
@@ -20,7 +23,19 @@ constexpr int kHalfWarps = 2 * kConsumerWarps;
 constexpr int kTokBlock = 4;           // tokens a half-warp scores before one softmax update
 constexpr float kLazyRescale = 8.0f;   // log2 units: keep a stale max until it is 2^8 off
 
+// Tensor-core path (128-row tiles): 128 x 128 S and O tiles in tensor memory.
+constexpr int kTileM = 128;            // packed query rows per tile
+constexpr int kTileN = 128;            // KV tokens per tile
+constexpr int kTmemCols = 512;         // S (2 buffers x 128 cols) + O (128 cols), rounded to a power of two
+constexpr int kTmemO = 256;            // first column of O
+constexpr int kMinTmaPage = 8;         // pages of >= 8 tokens keep every TMA box 1024-byte aligned
+constexpr int kSoftmaxWarp0 = 4;       // warps 4..7: one per TMEM lane quarter
+constexpr int kMmaWarp = 1;
+
 struct RunParams {
+  CUtensorMap tm_q;  // [q tokens, Hq, d] boxes of (64 dims, G heads, 128/G tokens), 128-byte swizzle
+  CUtensorMap tm_k;  // [pages, P, Hkv, d] boxes of (64 dims, 1 head, P slots, 1 page), 128-byte swizzle
+  CUtensorMap tm_v;
   const uint16_t* q;
   int64_t q_stride_tok, q_stride_head;
   const uint16_t* k;
@@ -35,10 +50,11 @@ struct RunParams {
   float* fws;
   int64_t partial_o_offset;  // floats
   float scale_log2;          // sm_scale * log2(e)
-  int32_t num_qo_heads, num_kv_heads, group, page_size, log2_page;
+  int32_t num_qo_heads, num_kv_heads, group, page_size, log2_page, num_pages;
+  int32_t tc_prefill;        // 128-row tiles on the tensor cores (else CUDA cores)
 };
 
-struct alignas(128) RunSmem {
+struct DecodeBufs {
   uint16_t k[kStages][kStageTokens][kHeadDim];
   uint16_t v[kStages][kStageTokens][kHeadDim];
   float comb_o[kHalfWarps][kRowsPerGroup][kHeadDim];
@@ -46,11 +62,32 @@ struct alignas(128) RunSmem {
   float comb_l[kHalfWarps][kRowsPerGroup];
   float4 xch[kHalfWarps][kTokBlock + 1];  // per half-warp: p of each token (4 rows), then alpha
   int32_t pidx[kStages][kStageTokens];
+};
+
+// Every [128][64] block is one 16 KB operand half: 128 rows of 64 elements
+// (128 bytes), 128-byte swizzled as TMA writes it and tcgen05 reads it.
+struct PrefillBufs {
+  uint16_t q[2][kTileM][64];        // [d half][row][dim]
+  uint16_t k[2][2][kTileN][64];     // [stage][d half][token][dim]
+  uint16_t v[2][2][kTileN][64];
+};
+
+struct alignas(1024) RunSmem {
+  union {
+    DecodeBufs dec;
+    PrefillBufs pf;
+  };
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t q_full, q_empty, o_ready, o_free, drain;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2];
+  uint32_t tmem_base;
   volatile int abort;  // set by the role whose bounded wait ran out
   int merge_last;
+  int merge_last_pf;
 };
+
+constexpr size_t kSmemBytes = sizeof(RunSmem) + 1024;  // slack to align the base to 1024 bytes
 
 struct Item {
   int32_t b, hk, row0, row1, kv0, kv1, part, merge;

@@ -23,6 +23,7 @@
 //    unit merges the unit's partials in chunk order (no inter-CTA waits).
 #pragma once
 #include "attention.cuh"
+#include "tc.cuh"
 
 namespace fi {
 
@@ -71,8 +72,8 @@ __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int
         const uint32_t ph = (it / kStages) & 1;
         const bool ok = mbar_wait_bounded(&sm.empty[s], ph ^ 1, &sm.abort);
         if (!ok || sm.abort) continue;
-        sm.pidx[s][lane] = nx0;
-        sm.pidx[s][lane + 32] = nx1;
+        sm.dec.pidx[s][lane] = nx0;
+        sm.dec.pidx[s][lane + 32] = nx1;
         if (st + 1 < nst) fetch_ids(st + 1);
         __syncwarp();
         const int j0 = item.kv0 + st * kStageTokens;
@@ -83,7 +84,7 @@ __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int
           const int tok = t2 + sub;
           const bool valid = tok < jn;
           const int j = j0 + tok;
-          const int64_t page = valid ? sm.pidx[s][(j >> lp) - pg0] : 0;
+          const int64_t page = valid ? sm.dec.pidx[s][(j >> lp) - pg0] : 0;
           const int64_t slot = j & (p.page_size - 1);
           const uint16_t* ks = valid ? kh + page * p.k_stride_page + slot * p.k_stride_slot : p.k;
           const uint16_t* vs;
@@ -91,14 +92,78 @@ __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int
             vs = valid ? ks + (p.v - p.k) : p.v;  // one offset serves both caches
           else
             vs = valid ? vh + page * p.v_stride_page + slot * p.v_stride_slot : p.v;
-          cp_async_16(&sm.k[s][tok][chunk16 * 8], ks, valid ? 16u : 0u);
-          cp_async_16(&sm.v[s][tok][chunk16 * 8], vs, valid ? 16u : 0u);
+          cp_async_16(&sm.dec.k[s][tok][chunk16 * 8], ks, valid ? 16u : 0u);
+          cp_async_16(&sm.dec.v[s][tok][chunk16 * 8], vs, valid ? 16u : 0u);
         }
         cp_async_mbar_arrive_noinc(&sm.full[s]);
       }
     }
   }
   cp_async_wait_all();
+}
+
+// ---------------------------------------------------------------- split merge
+
+// Split unit: every chunk wrote its fp32 partial state; the CTA whose
+// atomic increment completes the unit's counter merges the chunks in chunk
+// order (deterministic), writes O and LSE, and resets the counter.  No CTA
+// ever waits for another.  `nthreads` threads with index `tid` take part and
+// synchronise on named barrier `bar`; the barrier sequence depends only on
+// the plan, never on the abort flag, so all participating warps pass it.
+template <typename T>
+__device__ void merge_split_unit(const RunParams& p, const Item& item, const Request& rq, int32_t off_merge,
+                                 int32_t off_cnt, int tid, int nthreads, int bar, int* flag, int aborted) {
+  const int G = p.group;
+  const int nrows = item.row1 - item.row0;
+  __threadfence();
+  named_barrier_sync(bar, nthreads);
+  if (tid == 0) {
+    int last = 0;
+    if (!aborted) {
+      const int32_t n = __ldg(p.iws + off_merge + FI_MERGE_INTS * item.merge + 4);
+      const int old = atomicAdd(p.iws + off_cnt + item.merge, 1);
+      last = (old == n - 1);
+    }
+    *reinterpret_cast<volatile int*>(flag) = last;
+  }
+  named_barrier_sync(bar, nthreads);
+  if (*reinterpret_cast<volatile int*>(flag)) {
+    __threadfence();
+    const int32_t* mu = p.iws + off_merge + FI_MERGE_INTS * item.merge;
+    const int n = __ldg(mu + 4);
+    const int base = __ldg(mu + 5);
+    for (int task = tid; task < nrows * 32; task += nthreads) {
+      const int pr = task >> 5, ch = task & 31;
+      float M = -INFINITY;
+      for (int c = 0; c < n; ++c) M = fmaxf(M, __ldcg(p.fws + base + c * nrows + pr));
+      float Ls = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+        for (int c = 0; c < n; ++c) {
+          const int64_t prw = int64_t(base) + c * nrows + pr;
+          const float w = ex2((__ldcg(p.fws + prw) - M) * 1.4426950408889634f);
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(p.fws + p.partial_o_offset + prw * kHeadDim) + ch);
+          Ls += w;
+          acc.x += w * v.x;
+          acc.y += w * v.y;
+          acc.z += w * v.z;
+          acc.w += w * v.w;
+        }
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      const int row = item.row0 + pr;
+      const int t = row / G;
+      const int head = item.hk * G + (row - t * G);
+      const int64_t tok = rq.qo_start + t;
+      uint2 packed;
+      packed.x = Elem<T>::from_float2(acc.x * inv, acc.y * inv);
+      packed.y = Elem<T>::from_float2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + ch * 4) = packed;
+      if (ch == 0 && p.lse) p.lse[tok * p.num_qo_heads + head] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
+    }
+    if (tid == 0) p.iws[off_cnt + item.merge] = 0;  // ready for the next run of this plan
+  }
+  named_barrier_sync(bar, nthreads);
 }
 
 // ---------------------------------------------------------------- consumer
@@ -202,7 +267,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
 #pragma unroll
             for (int u = 0; u < kTokBlock; ++u) {
               const int tok = hw + (blk * kTokBlock + u) * nhw;
-              const uint4 kv = *reinterpret_cast<const uint4*>(&sm.k[s][tok][L * 8]);
+              const uint4 kv = *reinterpret_cast<const uint4*>(&sm.dec.k[s][tok][L * 8]);
               float f[8];
               unpack8<T>(kv, f);
               float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
@@ -230,14 +295,14 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
             }
             l = l * alpha + psum;
             m = m_new;
-            float* x = reinterpret_cast<float*>(sm.xch[hwid]);
+            float* x = reinterpret_cast<float*>(sm.dec.xch[hwid]);
             if ((L & 3) == 0) {
 #pragma unroll
               for (int u = 0; u < kTokBlock; ++u) x[u * 4 + my_row] = ps[u];
               x[kTokBlock * 4 + my_row] = alpha;
             }
             __syncwarp();
-            const float4 al = sm.xch[hwid][kTokBlock];
+            const float4 al = sm.dec.xch[hwid][kTokBlock];
             if (__any_sync(0xffffffffu, al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f)) {
 #pragma unroll
               for (int c = 0; c < 8; ++c) {
@@ -250,8 +315,8 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
 #pragma unroll
             for (int u = 0; u < kTokBlock; ++u) {
               const int tok = hw + (blk * kTokBlock + u) * nhw;
-              const float4 pu = sm.xch[hwid][u];
-              const uint4 vv = *reinterpret_cast<const uint4*>(&sm.v[s][tok][L * 8]);
+              const float4 pu = sm.dec.xch[hwid][u];
+              const uint4 vv = *reinterpret_cast<const uint4*>(&sm.dec.v[s][tok][L * 8]);
               float f[8];
               unpack8<T>(vv, f);
 #pragma unroll
@@ -272,13 +337,13 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
       // This half-warp's state -> shared memory, then merge per row.
 #pragma unroll
       for (int r = 0; r < kRowsPerGroup; ++r) {
-        float4* dst = reinterpret_cast<float4*>(&sm.comb_o[hwid][r][L * 8]);
+        float4* dst = reinterpret_cast<float4*>(&sm.dec.comb_o[hwid][r][L * 8]);
         dst[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
         dst[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
       }
       if ((L & 3) == 0) {
-        sm.comb_m[hwid][my_row] = m;
-        sm.comb_l[hwid][my_row] = l;
+        sm.dec.comb_m[hwid][my_row] = m;
+        sm.dec.comb_l[hwid][my_row] = l;
       }
       named_barrier_sync(1, 32 * kConsumerWarps);
       if (!sm.abort) {
@@ -287,16 +352,16 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
           const int gg = pr / kRowsPerGroup, r = pr % kRowsPerGroup;
           float M = -INFINITY;
           for (int sl = 0; sl < wpg; ++sl)
-            for (int h2 = 0; h2 < 2; ++h2) M = fmaxf(M, sm.comb_m[(gg + sl * ng) * 2 + h2][r]);
+            for (int h2 = 0; h2 < 2; ++h2) M = fmaxf(M, sm.dec.comb_m[(gg + sl * ng) * 2 + h2][r]);
           float Ls = 0.f;
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
           if (M != -INFINITY) {
             for (int sl = 0; sl < wpg; ++sl)
               for (int h2 = 0; h2 < 2; ++h2) {
                 const int id = (gg + sl * ng) * 2 + h2;
-                const float w = ex2(sm.comb_m[id][r] - M);
-                Ls += w * sm.comb_l[id][r];
-                const float4 v = *reinterpret_cast<const float4*>(&sm.comb_o[id][r][ch * 4]);
+                const float w = ex2(sm.dec.comb_m[id][r] - M);
+                Ls += w * sm.dec.comb_l[id][r];
+                const float4 v = *reinterpret_cast<const float4*>(&sm.dec.comb_o[id][r][ch * 4]);
                 acc.x += w * v.x;
                 acc.y += w * v.y;
                 acc.z += w * v.z;
@@ -328,69 +393,37 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
       named_barrier_sync(1, 32 * kConsumerWarps);
     }
 
-    // Split unit: the CTA that completes its last chunk merges all chunks.
-    // The barriers here depend only on the plan, never on the abort flag,
-    // so every consumer warp passes the same sequence of them.
-    if (item.merge >= 0) {
-      __threadfence();
-      named_barrier_sync(1, 32 * kConsumerWarps);
-      if (ct == 0) {
-        int last = 0;
-        if (!sm.abort) {
-          const int32_t n = __ldg(p.iws + off_merge + FI_MERGE_INTS * item.merge + 4);
-          const int old = atomicAdd(p.iws + off_cnt + item.merge, 1);
-          last = (old == n - 1);
-        }
-        sm.merge_last = last;
-      }
-      named_barrier_sync(1, 32 * kConsumerWarps);
-      if (sm.merge_last) {
-        __threadfence();
-        const int32_t* mu = p.iws + off_merge + FI_MERGE_INTS * item.merge;
-        const int n = __ldg(mu + 4);
-        const int base = __ldg(mu + 5);
-        for (int task = ct; task < nrows * 32; task += 32 * kConsumerWarps) {
-          const int pr = task >> 5, ch = task & 31;
-          float M = -INFINITY;
-          for (int c = 0; c < n; ++c) M = fmaxf(M, __ldcg(p.fws + base + c * nrows + pr));
-          float Ls = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (M != -INFINITY) {
-            for (int c = 0; c < n; ++c) {
-              const int64_t prw = int64_t(base) + c * nrows + pr;
-              const float w = ex2((__ldcg(p.fws + prw) - M) * 1.4426950408889634f);
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(p.fws + p.partial_o_offset + prw * kHeadDim) + ch);
-              Ls += w;
-              acc.x += w * v.x;
-              acc.y += w * v.y;
-              acc.z += w * v.z;
-              acc.w += w * v.w;
-            }
-          }
-          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-          const int row = item.row0 + pr;
-          const int t = row / G;
-          const int head = item.hk * G + (row - t * G);
-          const int64_t tok = rq.qo_start + t;
-          uint2 packed;
-          packed.x = Elem<T>::from_float2(acc.x * inv, acc.y * inv);
-          packed.y = Elem<T>::from_float2(acc.z * inv, acc.w * inv);
-          *reinterpret_cast<uint2*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + ch * 4) = packed;
-          if (ch == 0 && p.lse) p.lse[tok * p.num_qo_heads + head] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
-        }
-        if (ct == 0) p.iws[off_cnt + item.merge] = 0;  // ready for the next run of this plan
-      }
-      named_barrier_sync(1, 32 * kConsumerWarps);
-    }
+    if (item.merge >= 0)
+      merge_split_unit<T>(p, item, rq, off_merge, off_cnt, ct, 32 * kConsumerWarps, 1, &sm.merge_last, sm.abort);
   }
 }
 
+}  // namespace fi
+
+#include "prefill_kernel.cuh"
+
+namespace fi {
+
 // ---------------------------------------------------------------- kernel
+
+// A CTA's items come prefill-class (128-row tiles) first, then decode-class
+// (16-row tiles); returns the index of its first decode-class item.
+__device__ __forceinline__ int32_t first_decode_item(const RunParams& p, int32_t begin, int32_t end, int32_t off_items,
+                                                     int32_t off_req) {
+  int32_t i = begin;
+  while (i < end) {
+    const Item it = load_item(p.iws, off_items, i);
+    const Request rq = load_request(p.iws, off_req, it.b);
+    if (rq.qo_len * p.group <= FI_TILE_DECODE) break;
+    ++i;
+  }
+  return i;
+}
 
 template <typename T, bool kEqualKV>
 __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __grid_constant__ RunParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  RunSmem& sm = *reinterpret_cast<RunSmem*>(smem_raw);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  RunSmem& sm = *reinterpret_cast<RunSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int32_t* iws = p.iws;
   const int32_t magic = ws_header(iws, FI_H_MAGIC);
   const int32_t n_items = ws_header(iws, FI_H_NUM_ITEMS);
@@ -412,24 +445,67 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   const int32_t off_merge = ws_header(iws, FI_H_OFF_MERGE);
   const int32_t off_cnt = ws_header(iws, FI_H_OFF_COUNTERS);
   const int causal = ws_header(iws, FI_H_CAUSAL);
+  const int warp = threadIdx.x >> 5;
+  const int32_t mid = p.tc_prefill ? first_decode_item(p, begin, end, off_items, off_req) : begin;
+  const bool tc_phase = mid > begin;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 32);              // one cp.async arrival per producer lane
       mbar_init(&sm.empty[s], kConsumerWarps); // one arrival per consumer warp
     }
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.o_ready, 1);
+    mbar_init(&sm.o_free, 4);  // one arrival per softmax warp
+    mbar_init(&sm.drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.p_full[s], 4);
+      mbar_init(&sm.pv_done[s], 1);
+    }
     sm.abort = 0;
     sm.merge_last = 0;
+    sm.merge_last_pf = 0;
     fence_mbar_init();
   }
-  __syncthreads();
-
-  if (threadIdx.x < 32) {
-    produce<T, kEqualKV>(p, sm, begin, end, off_items, off_req);
-  } else {
-    consume<T>(p, sm, begin, end, off_items, off_req, off_merge, off_cnt, causal);
+  if (tc_phase && warp == kMmaWarp) {
+    tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
   }
+  tc::fence_before_sync();
   __syncthreads();
+  tc::fence_after_sync();
+
+  if (tc_phase) {
+    if (warp == 0) {
+      pf_produce(p, sm, begin, mid, off_items, off_req);
+    } else if (warp == kMmaWarp) {
+      if ((threadIdx.x & 31) == 0) pf_mma<T>(p, sm, begin, mid, off_items, off_req);
+      __syncwarp();
+    } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+      pf_softmax<T>(p, sm, begin, mid, off_items, off_req, off_merge, off_cnt, causal);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+  }
+
+  if (warp == 0) {
+    produce<T, kEqualKV>(p, sm, mid, end, off_items, off_req);
+  } else {
+    consume<T>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tc_phase && warp == kMmaWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(sm.tmem_base, kTmemCols);
+  }
   if (threadIdx.x == 0 && sm.abort) atomicOr(p.iws + FI_H_STATUS, sm.abort);
 }
 

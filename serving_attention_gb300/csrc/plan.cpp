@@ -213,17 +213,22 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
 
   int32_t* ws = static_cast<int32_t*>(workspace_host);
   std::memset(ws, 0, size_t(total_ints) * 4);
-  // CTA c's items occupy [start[c], start[c+1]); within a CTA they keep the
-  // order in which the deal handed them out.
+  // CTA c's items occupy [start[c], start[c+1]): its 128-row items first,
+  // then its 16-row items, each kept in the order the deal handed them out
+  // (one switch between the kernel's two tile paths per CTA at most).
   std::vector<int32_t> start(C + 1, 0);
   for (int32_t c = 0; c < C; ++c) start[c + 1] = start[c] + per_cta[c];
   for (int32_t c = 0; c <= C; ++c) ws[off_cta + c] = start[c];
   std::vector<int32_t> fill(start.begin(), start.end() - 1);
   int64_t n_decode = 0;
-  for (size_t i = 0; i < chunks.size(); ++i) {
-    const int32_t slot = fill[owner[i]]++;
-    std::memcpy(ws + off_items + int64_t(FI_ITEM_INTS) * slot, chunks[i].fields, sizeof chunks[i].fields);
-    if (chunks[i].tile == FI_TILE_DECODE) ++n_decode;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int32_t tile = pass == 0 ? FI_TILE_PREFILL : FI_TILE_DECODE;
+    for (size_t i = 0; i < chunks.size(); ++i) {
+      if (chunks[i].tile != tile) continue;
+      const int32_t slot = fill[owner[i]]++;
+      std::memcpy(ws + off_items + int64_t(FI_ITEM_INTS) * slot, chunks[i].fields, sizeof chunks[i].fields);
+      if (tile == FI_TILE_DECODE) ++n_decode;
+    }
   }
   if (n_merge) std::memcpy(ws + off_merge, merge_rows.data(), merge_rows.size() * 4);
   for (int32_t b = 0; b < batch; ++b) {

@@ -57,6 +57,21 @@ def test_tiny_decode_full():
     assert info.num_items > 0
 
 
+@pytest.mark.parametrize("qo,kv,causal,dtype", [
+    ([32], [128], 0, "bf16"),          # one 128-row tile against one 128-token KV tile
+    ([32], [128], 1, "bf16"),          # the same with the causal diagonal
+    ([32], [77], 0, "fp16"),           # ragged KV tail inside the tile
+    ([40], [300], 1, "bf16"),          # two row tiles (128 + 32 rows), three KV tiles
+    ([64, 33], [1000, 40], 1, "bf16"), # two requests, long and short
+])
+def test_tensor_core_tiles(qo, kv, causal, dtype):
+    """128-row tiles on the tensor cores (page 16, G 4), smallest cases first."""
+    b = workloads.make_batch("tc", dtype, qo, kv, 8, 2, 16, causal, 300 + len(qo) + kv[0], DEV,
+                             pool_pages=sum((k + 15) // 16 for k in kv) + 2)
+    info = _full_check(b)
+    assert info.num_prefill_items > 0
+
+
 @pytest.mark.parametrize("seed,page,group,causal,dtype,qo_max,kv_max", [
     (101, 16, 4, 0, "bf16", 1, 700), (102, 1, 4, 0, "bf16", 1, 300), (103, 4, 1, 1, "fp16", 3, 500),
     (104, 16, 8, 1, "bf16", 2, 900), (105, 64, 4, 1, "bf16", 40, 400), (106, 16, 4, 1, "fp16", 70, 300),
