@@ -82,10 +82,10 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
 // run enqueued inside a stream capture makes no non-stream CUDA call.
 constexpr int kMaxDevices = 64;
 
-template <typename T, bool kEqualKV>
+template <typename T>
 cudaError_t launch_run(const RunParams& p, int num_ctas, cudaStream_t stream) {
   static bool configured[kMaxDevices] = {};
-  auto kern = paged_attention_kernel<T, kEqualKV>;
+  auto kern = paged_attention_kernel<T>;
   const int smem = int(kSmemBytes);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -121,10 +121,10 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// 16-bit tensor map with 128-byte swizzle; dims/strides innermost first,
-// strides in elements (the innermost stride is 1).
+// 16-bit tensor map; dims/strides innermost first, strides in elements (the
+// innermost stride is 1).  Out-of-bounds boxes fill with zeros.
 bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank, const uint64_t* dims,
-              const int64_t* strides_elems, const uint32_t* box) {
+              const int64_t* strides_elems, const uint32_t* box, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   cuuint64_t gdim[5], gstride[4];
@@ -136,7 +136,7 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int 
   }
   for (int i = 0; i + 1 < rank; ++i) gstride[i] = cuuint64_t(strides_elems[i]) * 2;
   return enc(map, type, cuuint32_t(rank), const_cast<void*>(base), gdim, gstride, bdim, estride,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -150,7 +150,7 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return FI_ERR_CUDA;
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) return FI_ERR_CUDA;
-  auto kern = paged_attention_kernel<__nv_bfloat16, false>;
+  auto kern = paged_attention_kernel<__nv_bfloat16>;
   const int smem = int(kSmemBytes);
   int per_sm = 0;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -234,31 +234,32 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   // tokens (G divides 128); otherwise the CUDA-core path runs them.
   const int G = p.group;
   p.tc_prefill = (P >= kMinTmaPage && kTileM % G == 0) ? 1 : 0;
+  // K and V get tensor maps of their own, each with its own strides: the
+  // copy engine does the page/slot/head address arithmetic for both, so
+  // equal and unequal K/V strides (the comparison of the BatchAttention PR
+  // page, "코드 분석 §2") take the same path.
+  const CUtensorMapDataType tt = dtype == FI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t kd[4] = {uint64_t(kHeadDim), uint64_t(info->num_kv_heads), uint64_t(P), uint64_t(num_pages)};
+  const int64_t ks[3] = {k_strides[2], k_strides[1], k_strides[0]};  // head, slot, page
+  const int64_t vs[3] = {v_strides[2], v_strides[1], v_strides[0]};
+  const uint32_t kbd[4] = {uint32_t(kHeadDim), 1u, uint32_t(P < kStageTokens ? P : kStageTokens), 1u};
+  if (!make_map(&p.tm_kd, tt, k_cache, 4, kd, ks, kbd, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&p.tm_vd, tt, v_cache, 4, kd, vs, kbd, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return FI_ERR_UNSUPPORTED;
   if (p.tc_prefill) {
-    const CUtensorMapDataType tt =
-        dtype == FI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const uint64_t qd[3] = {uint64_t(kHeadDim), uint64_t(info->num_qo_heads), uint64_t(q_num_tokens)};
     const int64_t qs[2] = {q_stride_head, q_stride_tok};
     const uint32_t qb[3] = {64u, uint32_t(G), uint32_t(kTileM / G)};
-    const uint64_t kd[4] = {uint64_t(kHeadDim), uint64_t(info->num_kv_heads), uint64_t(P), uint64_t(num_pages)};
-    const int64_t ks[3] = {k_strides[2], k_strides[1], k_strides[0]};  // head, slot, page
-    const int64_t vs[3] = {v_strides[2], v_strides[1], v_strides[0]};
     const uint32_t kb[4] = {64u, 1u, uint32_t(P), 1u};
-    if (!make_map(&p.tm_q, tt, q, 3, qd, qs, qb) || !make_map(&p.tm_k, tt, k_cache, 4, kd, ks, kb) ||
-        !make_map(&p.tm_v, tt, v_cache, 4, kd, vs, kb))
+    if (!make_map(&p.tm_q, tt, q, 3, qd, qs, qb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.tm_k, tt, k_cache, 4, kd, ks, kb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.tm_v, tt, v_cache, 4, kd, vs, kb, CU_TENSOR_MAP_SWIZZLE_128B))
       return FI_ERR_UNSUPPORTED;
   }
 
-  // The K/V stride comparison of the BatchAttention PR page ("코드 분석 §2"):
-  // equal strides let V's address reuse K's offset arithmetic.
-  const bool equal = k_strides[0] == v_strides[0] && k_strides[1] == v_strides[1] && k_strides[2] == v_strides[2];
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (dtype == FI_BF16)
-    e = equal ? launch_run<__nv_bfloat16, true>(p, info->num_ctas, s)
-              : launch_run<__nv_bfloat16, false>(p, info->num_ctas, s);
-  else
-    e = equal ? launch_run<__half, true>(p, info->num_ctas, s) : launch_run<__half, false>(p, info->num_ctas, s);
+  const cudaError_t e = dtype == FI_BF16 ? launch_run<__nv_bfloat16>(p, info->num_ctas, s)
+                                         : launch_run<__half>(p, info->num_ctas, s);
   return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 

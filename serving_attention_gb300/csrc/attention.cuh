@@ -36,6 +36,8 @@ struct RunParams {
   CUtensorMap tm_q;  // [q tokens, Hq, d] boxes of (64 dims, G heads, 128/G tokens), 128-byte swizzle
   CUtensorMap tm_k;  // [pages, P, Hkv, d] boxes of (64 dims, 1 head, P slots, 1 page), 128-byte swizzle
   CUtensorMap tm_v;
+  CUtensorMap tm_kd;  // [pages, P, Hkv, d] boxes of (128 dims, 1 head, min(P, 64) slots, 1 page), no swizzle
+  CUtensorMap tm_vd;
   const uint16_t* q;
   int64_t q_stride_tok, q_stride_head;
   const uint16_t* k;
@@ -61,7 +63,6 @@ struct DecodeBufs {
   float comb_m[kHalfWarps][kRowsPerGroup];
   float comb_l[kHalfWarps][kRowsPerGroup];
   float4 xch[kHalfWarps][kTokBlock + 1];  // per half-warp: p of each token (4 rows), then alpha
-  int32_t pidx[kStages][kStageTokens];
 };
 
 // Every [128][64] block is one 16 KB operand half: 128 rows of 64 elements
@@ -87,7 +88,7 @@ struct alignas(1024) RunSmem {
   int merge_last_pf;
 };
 
-constexpr size_t kSmemBytes = sizeof(RunSmem) + 1024;  // slack to align the base to 1024 bytes
+constexpr size_t kSmemBytes = sizeof(RunSmem);
 
 struct Item {
   int32_t b, hk, row0, row1, kv0, kv1, part, merge;

@@ -5,11 +5,9 @@
 // (request b, KV head hk, packed query rows [row0,row1), KV tokens [kv0,kv1)):
 //
 //  * warp 0 streams the chunk's K and V, 64 tokens per stage, into a 4-deep
-//    shared-memory ring with 16-byte cp.async copies whose completion arrives
-//    on the stage's mbarrier.  The page ids of a stage are first staged in
-//    shared memory (wiki page, "1) 블록-스파스 KV 포맷": page indices are
-//    prefetched into shared memory so the kernel reaches KV blocks without
-//    indexing overhead).  Each K/V row of one head is 256 contiguous bytes.
+//    shared-memory ring: one TMA box per page and tensor, completion counted
+//    in bytes on the stage's mbarrier (see produce()).  Each K/V row of one
+//    head is 256 contiguous bytes.
 //  * warps 1..8 hold the G query heads that share KV head hk (GQA packing,
 //    wiki page "Decode 어텐션") in registers, 4 packed rows per half-warp,
 //    and score every KV token read from shared memory once for all of them.
@@ -38,68 +36,72 @@ __device__ __forceinline__ int groups_in_pass(int rows) {
 
 // ---------------------------------------------------------------- producer
 
-template <typename T, bool kEqualKV>
+// K and V of one stage: 64 tokens of one KV head.  One unswizzled 4-D TMA box
+// (128 dims, 1 head, min(P, 64) slots, 1 page) per page and tensor, issued by
+// one lane per page; the page ids of the next stage are loaded one stage
+// ahead into the issuing lanes' registers (the wiki page's page-index
+// prefetch, "1) 블록-스파스 KV 포맷").  Pages past the request are addressed
+// out of bounds and arrive as zeros; stage tokens past the chunk are masked
+// by the consumers.
 __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
                         int32_t off_req) {
   const int lane = threadIdx.x & 31;
-  const int sub = lane >> 4;  // which of the two rows of a copy step
-  const int chunk16 = lane & 15;
-  const int lp = p.log2_page;
+  const int lp = p.log2_page, P = p.page_size;
+  const int boxes = P >= kStageTokens ? 1 : (kStageTokens >> lp);  // per stage and tensor
+  const int box_slots = P >= kStageTokens ? kStageTokens : P;
+  constexpr uint32_t kStageBytes = 2u * kStageTokens * kHeadDim * 2u;
+  if (lane == 0) {
+    tc::prefetch_tensormap(&p.tm_kd);
+    tc::prefetch_tensormap(&p.tm_vd);
+  }
   uint32_t it = 0;
+  int armed[kStages];
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) armed[s] = -1;
   for (int32_t i = item_begin; i < item_end; ++i) {
     const Item item = load_item(p.iws, off_items, i);
     const Request rq = load_request(p.iws, off_req, item.b);
     const int nrows = item.row1 - item.row0;
     const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
     const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
-    const uint16_t* kh = p.k + int64_t(item.hk) * p.k_stride_head + chunk16 * 8;
-    const uint16_t* vh = p.v + int64_t(item.hk) * p.v_stride_head + chunk16 * 8;
+    const int npages = (rq.kv_len + P - 1) >> lp;
     const int32_t* pages = p.kv_indices + rq.page_start;
     for (int pass = 0; pass < passes; ++pass) {
-      // page ids of the next stage, prefetched into registers one stage ahead
       int32_t nx0 = 0, nx1 = 0;
       auto fetch_ids = [&](int st) {
-        const int j0 = item.kv0 + st * kStageTokens;
-        const int jn = min(kStageTokens, item.kv1 - j0);
-        const int pg0 = j0 >> lp;
-        const int npg = ((j0 + jn - 1) >> lp) - pg0 + 1;
-        nx0 = lane < npg ? __ldg(pages + pg0 + lane) : 0;
-        nx1 = lane + 32 < npg ? __ldg(pages + pg0 + lane + 32) : 0;
+        const int pg0 = (item.kv0 + st * kStageTokens) >> lp;
+        nx0 = (lane < boxes && pg0 + lane < npages) ? __ldg(pages + pg0 + lane) : p.num_pages;
+        nx1 = (lane + 32 < boxes && pg0 + lane + 32 < npages) ? __ldg(pages + pg0 + lane + 32) : p.num_pages;
       };
       if (nst > 0) fetch_ids(0);
       for (int st = 0; st < nst; ++st, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        const bool ok = mbar_wait_bounded(&sm.empty[s], ph ^ 1, &sm.abort);
-        if (!ok || sm.abort) continue;
-        sm.dec.pidx[s][lane] = nx0;
-        sm.dec.pidx[s][lane + 32] = nx1;
+        const int32_t id0 = nx0, id1 = nx1;
         if (st + 1 < nst) fetch_ids(st + 1);
+        if (!warp_wait(&sm.empty[s], ph ^ 1, &sm.abort)) continue;
+        if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
         __syncwarp();
         const int j0 = item.kv0 + st * kStageTokens;
-        const int jn = min(kStageTokens, item.kv1 - j0);
-        const int pg0 = j0 >> lp;
-#pragma unroll 4
-        for (int t2 = 0; t2 < kStageTokens; t2 += 2) {
-          const int tok = t2 + sub;
-          const bool valid = tok < jn;
-          const int j = j0 + tok;
-          const int64_t page = valid ? sm.dec.pidx[s][(j >> lp) - pg0] : 0;
-          const int64_t slot = j & (p.page_size - 1);
-          const uint16_t* ks = valid ? kh + page * p.k_stride_page + slot * p.k_stride_slot : p.k;
-          const uint16_t* vs;
-          if constexpr (kEqualKV)
-            vs = valid ? ks + (p.v - p.k) : p.v;  // one offset serves both caches
-          else
-            vs = valid ? vh + page * p.v_stride_page + slot * p.v_stride_slot : p.v;
-          cp_async_16(&sm.dec.k[s][tok][chunk16 * 8], ks, valid ? 16u : 0u);
-          cp_async_16(&sm.dec.v[s][tok][chunk16 * 8], vs, valid ? 16u : 0u);
+        const int slot0 = P > kStageTokens ? (j0 & (P - 1)) : 0;
+        if (lane < boxes) {
+          tc::tma_load_4d(&sm.dec.k[s][lane * box_slots][0], &p.tm_kd, &sm.full[s], 0, item.hk, slot0, id0);
+          tc::tma_load_4d(&sm.dec.v[s][lane * box_slots][0], &p.tm_vd, &sm.full[s], 0, item.hk, slot0, id0);
         }
-        cp_async_mbar_arrive_noinc(&sm.full[s]);
+        if (lane + 32 < boxes) {
+          tc::tma_load_4d(&sm.dec.k[s][(lane + 32) * box_slots][0], &p.tm_kd, &sm.full[s], 0, item.hk, slot0, id1);
+          tc::tma_load_4d(&sm.dec.v[s][(lane + 32) * box_slots][0], &p.tm_vd, &sm.full[s], 0, item.hk, slot0, id1);
+        }
+        armed[s] = ph;
       }
     }
   }
-  cp_async_wait_all();
+  // Every load this warp armed has landed before the CTA moves on.
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s)
+      if (armed[s] >= 0) mbar_wait_drain(&sm.full[s], armed[s]);
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- split merge
@@ -420,16 +422,20 @@ __device__ __forceinline__ int32_t first_decode_item(const RunParams& p, int32_t
   return i;
 }
 
-template <typename T, bool kEqualKV>
+template <typename T>
 __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __grid_constant__ RunParams p) {
+  // Casting the __shared__ array itself keeps every access below in the
+  // shared address space (LDS/STS rather than generic loads).  The swizzled
+  // TMA/MMA operand blocks need a 1024-byte aligned base; it is checked, and
+  // a misaligned base is reported instead of being used.
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  RunSmem& sm = *reinterpret_cast<RunSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  RunSmem& sm = *reinterpret_cast<RunSmem*>(smem_raw);
   const int32_t* iws = p.iws;
   const int32_t magic = ws_header(iws, FI_H_MAGIC);
   const int32_t n_items = ws_header(iws, FI_H_NUM_ITEMS);
   const int32_t n_ctas = ws_header(iws, FI_H_NUM_CTAS);
   const int32_t off_cta = ws_header(iws, FI_H_OFF_CTA);
-  bool bad = magic != FI_PLAN_MAGIC || n_ctas != int32_t(gridDim.x);
+  bool bad = magic != FI_PLAN_MAGIC || n_ctas != int32_t(gridDim.x) || (smem_u32(smem_raw) & 1023u) != 0;
   int32_t begin = 0, end = 0;
   if (!bad) {
     begin = __ldg(iws + off_cta + blockIdx.x);
@@ -451,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 32);              // one cp.async arrival per producer lane
+      mbar_init(&sm.full[s], 1);               // the producer's arrive.expect_tx; TMA completes the bytes
       mbar_init(&sm.empty[s], kConsumerWarps); // one arrival per consumer warp
     }
     mbar_init(&sm.q_full, 1);
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   }
 
   if (warp == 0) {
-    produce<T, kEqualKV>(p, sm, mid, end, off_items, off_req);
+    produce(p, sm, mid, end, off_items, off_req);
   } else {
     consume<T>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal);
   }

@@ -29,21 +29,6 @@
 
 namespace fi {
 
-// Warp-uniform bounded wait: lane 0 waits, the result is broadcast.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort) && !*abort;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// Bounded wait that ignores the abort flag: used to drain a role's own
-// asynchronous copies or MMAs before the CTA leaves.
-__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitBudgetClocks) return;
-}
-
 constexpr uint32_t kQBytes = 2u * kTileM * 64u * 2u;   // two 64-dim halves of 128 rows, 16-bit
 constexpr uint32_t kKVBytes = 2u * kTileN * 64u * 2u;
 
