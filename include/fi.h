@@ -166,6 +166,42 @@ fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, 
                                        void* int_workspace_dev, void* float_workspace_dev, void* stream);
 
 /*
+ * fi_batch_paged_attention_run_static_scratch -- fi_batch_paged_attention_run
+ * for callers that cannot allocate device memory.  The paper has no
+ * counterpart; it exists for this library's users.
+ *
+ * Who needs it: code that has no device allocator at hand or must not call
+ * one at this point -- a plugin that its host runtime gives only fixed input
+ * and output buffers, a server that reserved all device memory up front, or
+ * code for which an allocation would synchronise the device.  Such a caller
+ * cannot provide the float workspace, so here the split-KV partial states
+ * live in one fixed device array inside the library, sized for at most 32768
+ * partial rows (about 17 MB; every GPU that loads the library holds it until
+ * the process exits).  The call itself allocates nothing.
+ *
+ * Arguments are those of fi_batch_paged_attention_run without
+ * float_workspace_dev; the caller still passes the inputs, the outputs and
+ * the int workspace filled by fi_plan.  Returns FI_ERR_CAPACITY, before
+ * anything is enqueued, when info->num_partial_rows exceeds 32768 (plan with
+ * fewer CTAs, a larger split chunk or a smaller batch).
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (the current one); make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents;
+ * nothing in it has to start at zero (every partial row is written before it
+ * is read; the merge counters live in the int workspace).  Calls whose
+ * kernels overlap on the GPU (other streams, other threads) race on the
+ * array: serialise them.
+ */
+fi_status fi_batch_paged_attention_run_static_scratch(const fi_plan_info* info, const void* q, int64_t q_stride_tok,
+                                                      int64_t q_stride_head, int32_t q_num_tokens, const void* k_cache,
+                                                      const int64_t k_strides[3], const void* v_cache,
+                                                      const int64_t v_strides[3], int32_t num_pages,
+                                                      const int32_t* kv_indices_dev, void* o, int64_t o_stride_tok,
+                                                      int64_t o_stride_head, float* lse, fi_dtype dtype,
+                                                      float sm_scale, void* int_workspace_dev, void* stream);
+
+/*
  * fi_merge_states -- merge two attention states row by row (paper summary,
  * "1. 통합된 KV 캐시 추상화": a shared dense prefix and per-request sparse
  * suffixes are computed separately and combined):

@@ -57,8 +57,8 @@ class PlanInfo(ctypes.Structure):
 
 
 EXPORTS = ["fi_default_plan_config", "fi_int_workspace_bytes", "fi_float_workspace_bytes", "fi_plan",
-           "fi_plan_host", "fi_batch_paged_attention_run", "fi_merge_states", "fi_get_device_status",
-           "fi_status_string"]
+           "fi_plan_host", "fi_batch_paged_attention_run", "fi_batch_paged_attention_run_static_scratch",
+           "fi_merge_states", "fi_get_device_status", "fi_status_string"]
 
 _lib = None
 
@@ -81,6 +81,9 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
     lib.fi_plan_host.argtypes = [cfgp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, sz, infop]
     lib.fi_batch_paged_attention_run.argtypes = [infop, vp, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp, i64, i64,
                                                  vp, ctypes.c_int, ctypes.c_float, vp, vp, vp]
+    lib.fi_batch_paged_attention_run_static_scratch.argtypes = [infop, vp, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp,
+                                                                i64, i64, vp, ctypes.c_int, ctypes.c_float, vp, vp]
+    lib.fi_batch_paged_attention_run_static_scratch.restype = ctypes.c_int
     lib.fi_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, vp]
     lib.fi_get_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.fi_status_string.argtypes = [ctypes.c_int]
@@ -208,6 +211,30 @@ def run(ws: Workspace, info: PlanInfo, q: torch.Tensor, k_cache: torch.Tensor, v
         lse.data_ptr() if lse is not None else None, _dtype_code(q), float(sm_scale), ws.int_ws.data_ptr(),
         ws.float_ws.data_ptr(), _stream_ptr(stream))
     _check(st, "fi_batch_paged_attention_run")
+
+
+STATIC_SCRATCH_PARTIAL_ROWS = 32768
+
+
+def run_static_scratch(ws: Workspace, info: PlanInfo, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                       kv_indices_dev: torch.Tensor, o: torch.Tensor, lse: torch.Tensor | None, sm_scale: float,
+                       stream=None):
+    """run() for callers that cannot allocate: the split-KV partial states go
+    to the library's fixed device array (at most 32768 partial rows) instead
+    of ws.float_ws.  Calls that overlap on the GPU race on that array."""
+    lib = load()
+    if kv_indices_dev.dtype != torch.int32 or not kv_indices_dev.is_contiguous():
+        raise TypeError("kv_indices must be a contiguous int32 device tensor")
+    if q.dtype != k_cache.dtype or q.dtype != v_cache.dtype or q.dtype != o.dtype:
+        raise TypeError("q, k, v and o must share one dtype")
+    ks = (ctypes.c_int64 * 3)(*k_cache.stride()[:3])
+    vs = (ctypes.c_int64 * 3)(*v_cache.stride()[:3])
+    st = lib.fi_batch_paged_attention_run_static_scratch(
+        ctypes.byref(info), q.data_ptr(), q.stride(0), q.stride(1), q.shape[0], k_cache.data_ptr(), ks,
+        v_cache.data_ptr(), vs, k_cache.shape[0], kv_indices_dev.data_ptr(), o.data_ptr(), o.stride(0), o.stride(1),
+        lse.data_ptr() if lse is not None else None, _dtype_code(q), float(sm_scale), ws.int_ws.data_ptr(),
+        _stream_ptr(stream))
+    _check(st, "fi_batch_paged_attention_run_static_scratch")
 
 
 def merge_states(v_a, s_a, v_b, s_b, v_out, s_out, stream=None):

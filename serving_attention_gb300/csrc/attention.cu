@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/fi.h"
 #include "attention_kernel.cuh"
@@ -303,4 +304,61 @@ extern "C" fi_status fi_get_device_status(const void* int_workspace_dev, void* s
     return FI_ERR_CUDA;
   *status_out = (word & kStatusTimeout) ? FI_ERR_TIMEOUT : (word & kStatusBadPlan) ? FI_ERR_DEVICE_CHECK : FI_OK;
   return FI_OK;
+}
+
+// ------------------------------------------------------------ run without caller scratch
+
+// Some callers cannot hand the library a float workspace: code that runs
+// where no device allocator is reachable (a plugin given fixed input/output
+// buffers by its host runtime, a server that reserved all device memory up
+// front and owns no spare block), or code that must not allocate at that
+// point because an allocation would synchronise the device or be recorded
+// into a stream it does not control.  For them the split-KV partial states
+// live in one fixed device array defined here, sized for at most
+// kStaticPartialRows partial rows (about 17 MB, held by every GPU that loads
+// this library until the process exits).
+namespace fi {
+constexpr int64_t kStaticPartialRows = 32768;  // a multiple of 64: partial O starts right after the LSEs
+constexpr int64_t kStaticScratchFloats = kStaticPartialRows + kStaticPartialRows * kHeadDim;
+static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
+
+std::mutex g_static_scratch_mu;
+float* g_static_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device (in host code the symbol is only a stand-in, not an address).
+fi_status static_scratch_address(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FI_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FI_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (!g_static_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return FI_ERR_CUDA;
+    g_static_scratch_ptr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_static_scratch_ptr[dev];
+  return FI_OK;
+}
+}  // namespace fi
+
+extern "C" fi_status fi_batch_paged_attention_run_static_scratch(
+    const fi_plan_info* info, const void* q, int64_t q_stride_tok, int64_t q_stride_head, int32_t q_num_tokens,
+    const void* k_cache, const int64_t k_strides[3], const void* v_cache, const int64_t v_strides[3],
+    int32_t num_pages, const int32_t* kv_indices_dev, void* o, int64_t o_stride_tok, int64_t o_stride_head,
+    float* lse, fi_dtype dtype, float sm_scale, void* int_workspace_dev, void* stream) {
+  if (!info) return FI_ERR_INVALID_ARG;
+  if (info->num_partial_rows > kStaticPartialRows) return FI_ERR_CAPACITY;  // plan needs more partial rows
+  float* scratch = nullptr;
+  const fi_status st = static_scratch_address(&scratch);
+  if (st != FI_OK) return st;
+  // The same run as fi_batch_paged_attention_run, with the fixed array as
+  // its float workspace (laid out for kStaticPartialRows rows).  Nothing in
+  // that array has to start at zero: every partial row is written before it
+  // is read, and the merge counters live in the caller's int workspace.
+  fi_plan_info local = *info;
+  local.max_partial_rows = kStaticPartialRows;
+  return fi_batch_paged_attention_run(&local, q, q_stride_tok, q_stride_head, q_num_tokens, k_cache, k_strides,
+                                      v_cache, v_strides, num_pages, kv_indices_dev, o, o_stride_tok, o_stride_head,
+                                      lse, dtype, sm_scale, int_workspace_dev, scratch, stream);
 }

@@ -1,0 +1,68 @@
+"""fi_batch_paged_attention_run_static_scratch against fi_batch_paged_attention_run.
+
+The static-scratch entry point serves callers that cannot allocate device
+memory (no allocator reachable where they run, all memory reserved up front,
+or an allocation would synchronise the device): it keeps the split-KV partial
+states in a fixed array inside the library instead of a caller-provided float
+workspace.  Its output must match the regular entry point's on the same plan,
+call after call (the array keeps the previous call's contents), and a plan
+that needs more partial rows than the array holds must be refused before
+anything is enqueued.  This file is collected last on purpose."""
+from __future__ import annotations
+
+import ctypes
+
+import pytest
+import torch
+
+import serving_attention_gb300 as fi
+import workloads
+from helpers import LSE_TOL, O_TOL
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _outputs(b):
+    o = torch.full_like(b.q, float("nan"))
+    lse = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    return o, lse
+
+
+@pytest.mark.parametrize("case", ["decode", "prefill"])
+def test_static_scratch_matches_regular_run(case):
+    if case == "decode":
+        b = workloads.llama8b_decode(device=DEV, batch=16)
+        cfg = fi.default_plan_config(0)
+    else:  # 128-row tiles split into 256-token chunks
+        b = workloads.make_batch("split_prefill", "bf16", [64, 40], [1500, 700], 8, 2, 16, 1, 4242, DEV,
+                                 pool_pages=160)
+        cfg = fi.default_plan_config(0, prefill_min_chunk=256, split_factor=16)
+    ws = fi.Workspace(cfg, device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                   128, b.page_size, b.causal, b.num_pages)
+    assert 0 < info.num_partial_rows <= fi.STATIC_SCRATCH_PARTIAL_ROWS, "the case must use split-KV partial states"
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    n = b.total_qo
+    o_ref, lse_ref = _outputs(b)
+    fi.run(ws, info, b.q, b.k, b.v, kvi, o_ref, lse_ref, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0
+    for call in range(2):
+        o, lse = _outputs(b)
+        fi.run_static_scratch(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+        torch.cuda.synchronize()
+        assert fi.device_status(ws) == 0, f"device status after call {call}"
+        err_o = float((o[:n].float() - o_ref[:n].float()).abs().max())
+        err_l = float((lse[:n] - lse_ref[:n]).abs().max())
+        assert err_o <= O_TOL and err_l <= LSE_TOL, (call, err_o, err_l)
+
+
+def test_static_scratch_refuses_oversized_plan():
+    lib = fi.load()
+    info = fi.PlanInfo(num_ctas=1, head_dim=128, page_size=16, num_qo_heads=8, num_kv_heads=2,
+                       num_partial_rows=fi.STATIC_SCRATCH_PARTIAL_ROWS + 1)
+    ks = (ctypes.c_int64 * 3)(4096, 256, 128)
+    st = lib.fi_batch_paged_attention_run_static_scratch(ctypes.byref(info), 16, 1024, 128, 4, 32, ks, 64, ks, 10, 48,
+                                                         80, 1024, 128, None, fi.BF16, 0.1, 96, None)
+    assert st == 3  # FI_ERR_CAPACITY, returned before anything is enqueued
