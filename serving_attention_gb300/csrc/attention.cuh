@@ -15,7 +15,8 @@ constexpr int kHeadDim = 128;
 constexpr int kStageTokens = 64;       // KV tokens per pipeline stage
 constexpr int kStages = 4;             // depth of the K/V ring
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);  // warp 0 = producer
+constexpr int kFirstConsumerWarp = 4;  // warps 4..11 consume (warp 0 produces)
+constexpr int kThreads = 32 * 12;
 constexpr int kRowsPerGroup = 4;       // query rows a half-warp carries in registers
 constexpr int kGroupsPerPass = 8;
 constexpr int kRowsPerPass = kRowsPerGroup * kGroupsPerPass;
@@ -26,11 +27,13 @@ constexpr float kLazyRescale = 8.0f;   // log2 units: keep a stale max until it 
 // Tensor-core path (128-row tiles): 128 x 128 S and O tiles in tensor memory.
 constexpr int kTileM = 128;            // packed query rows per tile
 constexpr int kTileN = 128;            // KV tokens per tile
-constexpr int kTmemCols = 512;         // S (2 buffers x 128 cols) + O (128 cols), rounded to a power of two
-constexpr int kTmemO = 256;            // first column of O
+constexpr int kTmemCols = 512;         // S (2 buffers x 128 cols) + O (2 buffers x 128 cols)
+constexpr int kTmemO = 256;            // first column of O buffer 0
 constexpr int kMinTmaPage = 8;         // pages of >= 8 tokens keep every TMA box 1024-byte aligned
-constexpr int kSoftmaxWarp0 = 4;       // warps 4..7: one per TMEM lane quarter
+constexpr int kSoftmaxWarp0 = 4;       // warps 4..7 own S/O columns 0..63, warps 8..11 columns 64..127
+constexpr int kSoftmaxThreads = 256;
 constexpr int kMmaWarp = 1;
+constexpr int kVWarp = 2;              // loads V tiles; warp 0 loads Q and K tiles
 
 struct RunParams {
   CUtensorMap tm_q;  // [q tokens, Hq, d] boxes of (64 dims, G heads, 128/G tokens), 128-byte swizzle
@@ -68,7 +71,7 @@ struct DecodeBufs {
 // Every [128][64] block is one 16 KB operand half: 128 rows of 64 elements
 // (128 bytes), 128-byte swizzled as TMA writes it and tcgen05 reads it.
 struct PrefillBufs {
-  uint16_t q[2][kTileM][64];        // [d half][row][dim]
+  uint16_t q[2][2][kTileM][64];     // [buffer][d half][row][dim]
   uint16_t k[2][2][kTileN][64];     // [stage][d half][token][dim]
   uint16_t v[2][2][kTileN][64];
 };
@@ -80,8 +83,10 @@ struct alignas(1024) RunSmem {
   };
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t q_full, q_empty, o_ready, o_free, drain;
+  uint64_t q_full[2], q_empty[2], o_ready[2], o_free[2], drain;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2];
+  float xmax[2][2][kTileM];  // [tile parity][column half][row]: the two halves' row maxima
+  float xsum[2][2][kTileM];  // [item parity][column half][row]: the halves' row sums at the epilogue
   uint32_t tmem_base;
   volatile int abort;  // set by the role whose bounded wait ran out
   int merge_last;

@@ -8,7 +8,7 @@
 //    shared-memory ring: one TMA box per page and tensor, completion counted
 //    in bytes on the stage's mbarrier (see produce()).  Each K/V row of one
 //    head is 256 contiguous bytes.
-//  * warps 1..8 hold the G query heads that share KV head hk (GQA packing,
+//  * warps 4..11 hold the G query heads that share KV head hk (GQA packing,
 //    wiki page "Decode 어텐션") in registers, 4 packed rows per half-warp,
 //    and score every KV token read from shared memory once for all of them.
 //    A half-warp owns one token at a time (16 lanes x 8 dims); partial dot
@@ -199,7 +199,7 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
 template <typename T>
 __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
                         int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal) {
-  const int cw = (threadIdx.x >> 5) - 1;  // consumer warp 0..7
+  const int cw = (threadIdx.x >> 5) - kFirstConsumerWarp;  // consumer warp 0..7
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
   const int L = lane & 15;
@@ -460,18 +460,18 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
       mbar_init(&sm.full[s], 1);               // the producer's arrive.expect_tx; TMA completes the bytes
       mbar_init(&sm.empty[s], kConsumerWarps); // one arrival per consumer warp
     }
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
-    mbar_init(&sm.o_ready, 1);
-    mbar_init(&sm.o_free, 4);  // one arrival per softmax warp
     mbar_init(&sm.drain, 1);
     for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+      mbar_init(&sm.o_ready[s], 1);
+      mbar_init(&sm.o_free[s], kSoftmaxThreads / 32);  // one arrival per softmax warp
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
       mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.p_full[s], 4);
+      mbar_init(&sm.p_full[s], kSoftmaxThreads / 32);
       mbar_init(&sm.pv_done[s], 1);
     }
     sm.abort = 0;
@@ -489,11 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
 
   if (tc_phase) {
     if (warp == 0) {
-      pf_produce(p, sm, begin, mid, off_items, off_req);
+      pf_produce<false>(p, sm, begin, mid, off_items, off_req);
+    } else if (warp == kVWarp) {
+      pf_produce<true>(p, sm, begin, mid, off_items, off_req);
     } else if (warp == kMmaWarp) {
-      if ((threadIdx.x & 31) == 0) pf_mma<T>(p, sm, begin, mid, off_items, off_req);
+      if ((threadIdx.x & 31) == 0) pf_mma<T>(p, sm, begin, mid, off_items);
       __syncwarp();
-    } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+    } else if (warp >= kSoftmaxWarp0) {
       pf_softmax<T>(p, sm, begin, mid, off_items, off_req, off_merge, off_cnt, causal);
     }
     tc::fence_before_sync();
@@ -503,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
 
   if (warp == 0) {
     produce(p, sm, mid, end, off_items, off_req);
-  } else {
+  } else if (warp >= kFirstConsumerWarp) {
     consume<T>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal);
   }
   tc::fence_before_sync();
