@@ -188,6 +188,15 @@ __device__ __forceinline__ float reduce_rows4(float v0, float v1, float v2, floa
   return keep;
 }
 
+// 8 storage elements -> 4 fp32 pairs (element 2i in .x, 2i+1 in .y).
+template <typename T>
+__device__ __forceinline__ void unpack4x2(const uint4& u, float2 (&f)[4]) {
+  f[0] = Elem<T>::to_float2(u.x);
+  f[1] = Elem<T>::to_float2(u.y);
+  f[2] = Elem<T>::to_float2(u.z);
+  f[3] = Elem<T>::to_float2(u.w);
+}
+
 template <typename T>
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   const float2 a = Elem<T>::to_float2(u.x), b = Elem<T>::to_float2(u.y);
@@ -227,8 +236,9 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
       const int hw = slice * 2 + half;     // index among them
       const int blocks = kStageTokens / (nhw * kTokBlock);
 
-      // Query rows of this group, pre-scaled by scale*log2(e).
-      float q[kRowsPerGroup][8];
+      // Query rows of this group, pre-scaled by scale*log2(e), as dim pairs
+      // for the packed fp32 FMA (dims 2i, 2i+1 of this lane's 8).
+      float2 q[kRowsPerGroup][4];
       int lim_mine = -1;
 #pragma unroll
       for (int r = 0; r < kRowsPerGroup; ++r) {
@@ -240,22 +250,22 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
           const int head = item.hk * G + (row - t * G);
           const uint4 u = __ldg(reinterpret_cast<const uint4*>(
               p.q + int64_t(rq.qo_start + t) * p.q_stride_tok + int64_t(head) * p.q_stride_head + L * 8));
-          unpack8<T>(u, q[r]);
+          unpack4x2<T>(u, q[r]);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) q[r][c] *= p.scale_log2;
+          for (int c = 0; c < 4; ++c) q[r][c] = make_float2(q[r][c].x * p.scale_log2, q[r][c].y * p.scale_log2);
           lim = causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1;
         } else {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) q[r][c] = 0.f;
+          for (int c = 0; c < 4; ++c) q[r][c] = make_float2(0.f, 0.f);
         }
         if (r == my_row) lim_mine = lim;
       }
 
-      float o[kRowsPerGroup][8];
+      float2 o[kRowsPerGroup][4];
 #pragma unroll
       for (int r = 0; r < kRowsPerGroup; ++r)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) o[r][c] = 0.f;
+        for (int c = 0; c < 4; ++c) o[r][c] = make_float2(0.f, 0.f);
       float m = -INFINITY, l = 0.f;
 
       for (int st = 0; st < nst; ++st, ++it) {
@@ -270,17 +280,17 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
             for (int u = 0; u < kTokBlock; ++u) {
               const int tok = hw + (blk * kTokBlock + u) * nhw;
               const uint4 kv = *reinterpret_cast<const uint4*>(&sm.dec.k[s][tok][L * 8]);
-              float f[8];
-              unpack8<T>(kv, f);
-              float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+              float2 f[4];
+              unpack4x2<T>(kv, f);
+              float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                d0 = fmaf(q[0][c], f[c], d0);
-                d1 = fmaf(q[1][c], f[c], d1);
-                d2 = fmaf(q[2][c], f[c], d2);
-                d3 = fmaf(q[3][c], f[c], d3);
+              for (int c = 0; c < 4; ++c) {
+                a0 = fma2(q[0][c], f[c], a0);
+                a1 = fma2(q[1][c], f[c], a1);
+                a2 = fma2(q[2][c], f[c], a2);
+                a3 = fma2(q[3][c], f[c], a3);
               }
-              const float sfull = reduce_rows4(d0, d1, d2, d3, L);
+              const float sfull = reduce_rows4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y, L);
               const int j = j0 + tok;
               sc[u] = (j < item.kv1 && j <= lim_mine) ? sfull : -INFINITY;
             }
@@ -307,11 +317,11 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
             const float4 al = sm.dec.xch[hwid][kTokBlock];
             if (__any_sync(0xffffffffu, al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f)) {
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                o[0][c] *= al.x;
-                o[1][c] *= al.y;
-                o[2][c] *= al.z;
-                o[3][c] *= al.w;
+              for (int c = 0; c < 4; ++c) {
+                o[0][c] = make_float2(o[0][c].x * al.x, o[0][c].y * al.x);
+                o[1][c] = make_float2(o[1][c].x * al.y, o[1][c].y * al.y);
+                o[2][c] = make_float2(o[2][c].x * al.z, o[2][c].y * al.z);
+                o[3][c] = make_float2(o[3][c].x * al.w, o[3][c].y * al.w);
               }
             }
 #pragma unroll
@@ -319,14 +329,16 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
               const int tok = hw + (blk * kTokBlock + u) * nhw;
               const float4 pu = sm.dec.xch[hwid][u];
               const uint4 vv = *reinterpret_cast<const uint4*>(&sm.dec.v[s][tok][L * 8]);
-              float f[8];
-              unpack8<T>(vv, f);
+              float2 f[4];
+              unpack4x2<T>(vv, f);
+              const float2 p0 = make_float2(pu.x, pu.x), p1 = make_float2(pu.y, pu.y);
+              const float2 p2 = make_float2(pu.z, pu.z), p3 = make_float2(pu.w, pu.w);
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                o[0][c] = fmaf(pu.x, f[c], o[0][c]);
-                o[1][c] = fmaf(pu.y, f[c], o[1][c]);
-                o[2][c] = fmaf(pu.z, f[c], o[2][c]);
-                o[3][c] = fmaf(pu.w, f[c], o[3][c]);
+              for (int c = 0; c < 4; ++c) {
+                o[0][c] = fma2(p0, f[c], o[0][c]);
+                o[1][c] = fma2(p1, f[c], o[1][c]);
+                o[2][c] = fma2(p2, f[c], o[2][c]);
+                o[3][c] = fma2(p3, f[c], o[3][c]);
               }
             }
             __syncwarp();
@@ -340,8 +352,8 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
 #pragma unroll
       for (int r = 0; r < kRowsPerGroup; ++r) {
         float4* dst = reinterpret_cast<float4*>(&sm.dec.comb_o[hwid][r][L * 8]);
-        dst[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
-        dst[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
+        dst[0] = make_float4(o[r][0].x, o[r][0].y, o[r][1].x, o[r][1].y);
+        dst[1] = make_float4(o[r][2].x, o[r][2].y, o[r][3].x, o[r][3].y);
       }
       if ((L & 3) == 0) {
         sm.dec.comb_m[hwid][my_row] = m;

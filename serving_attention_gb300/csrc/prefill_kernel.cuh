@@ -208,7 +208,10 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
     }
     if (progress) {
       idle_since = clock64();
-    } else if (clock64() - idle_since > kWaitBudgetClocks) {
+    } else {
+      __nanosleep(32);  // leave the issue slots of this SM sub-partition to the softmax warps
+    }
+    if (!progress && clock64() - idle_since > kWaitBudgetClocks) {
       sm.abort = kStatusTimeout;
       break;
     }
@@ -272,11 +275,14 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
               for (int e = 0; e < 32; ++e)
                 if (kbase + h * 32 + e > lim) sv[h][e] = 0xff800000u;  // -inf
           }
+          // eight independent running maxima, then a tree: no long dependency chain
+          float mx8[8];
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(sv[0][a]);
 #pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              mx = fmaxf(mx, fmaxf(__uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1])));
+          for (int e = 8; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e >> 5][e & 31]));
+          mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         }
         // the two halves of the row agree on its max (double-buffered by tile parity)
         sm.xmax[j & 1][half][r] = mx;
@@ -307,7 +313,9 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         }
         // P = 2^(s*c - m) as 16-bit pairs over the first 32 columns of this half
         const float msub = (m_new == -INFINITY) ? 0.f : m_new;
-        float sum = 0.f;
+        float sum8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[16];
@@ -315,13 +323,13 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
           for (int e = 0; e < 16; ++e) {
             const float a = ex2(fmaf(__uint_as_float(sv[h][2 * e]), c, -msub));
             const float b = ex2(fmaf(__uint_as_float(sv[h][2 * e + 1]), c, -msub));
-            sum += a + b;
+            sum8[e & 7] += a + b;  // eight independent partial sums
             pk[e] = tc::pack2<T>(a, b);
           }
           tc::tmem_st16(tl + st * kTileN + c0 + h * 16, pk);
         }
         tc::tmem_st_wait();
-        l += sum;
+        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         m = m_new;
         have_o = true;
         tc::fence_before_sync();
