@@ -345,7 +345,69 @@ def bench_secondary(dev, reps=5):
                          decode_gbs=nbytes / ms / 1e6, items=info.num_items)
         del b, o, lse, g
         torch.cuda.empty_cache()
+    out["shared_prefix"] = bench_shared_prefix(dev, flush, reps)
     return out
+
+
+def bench_shared_prefix(dev, flush, reps=5):
+    """Composable format: the dense prefix run (tensor cores, 64 branch queries),
+    the page-1 suffix run and fi_merge_states, captured in one CUDA graph,
+    against one run over the flat page-1 layout (prefix pages repeated in every
+    branch's page list)."""
+    import torch
+
+    import serving_attention_gb300 as fi
+    import workloads
+
+    d = workloads.shared_prefix(device=dev)
+    pre, suf, flat = d["prefix"], d["suffix"], d["flat"]
+    cfg = fi.default_plan_config(dev.index)
+
+    def prepared(b):
+        ws = fi.Workspace(cfg, device=dev)
+        info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                       128, b.page_size, b.causal, b.num_pages)
+        kvi = torch.as_tensor(b.kv_indices, device=dev)
+        o = torch.empty_like(b.q)
+        lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
+        return ws, info, kvi, o, lse
+
+    P, S, F = prepared(pre), prepared(suf), prepared(flat)
+    o_m = torch.empty_like(pre.q)
+    l_m = torch.empty(pre.q.shape[:2], dtype=torch.float32, device=dev)
+
+    def composable():
+        fi.run(P[0], P[1], pre.q, pre.k, pre.v, P[2], P[3], P[4], pre.sm_scale)
+        fi.run(S[0], S[1], suf.q, suf.k, suf.v, S[2], S[3], S[4], suf.sm_scale)
+        fi.merge_states(P[3], P[4], S[3], S[4], o_m, l_m)
+
+    def flat_run():
+        fi.run(F[0], F[1], flat.q, flat.k, flat.v, F[2], F[3], F[4], flat.sm_scale)
+
+    res = {}
+    for name, fn in (("composable", composable), ("flat", flat_run)):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            c.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(c))
+        res[name] = float(np.median(ts))
+    # algorithmic bytes of the composable form: the prefix KV once, every suffix token once, Q in, O/LSE out
+    suffix_tokens = int(suf.kv_lens().sum())
+    nbytes = (pre.meta["prefix_len"] + suffix_tokens) * 8 * 128 * 2 * 2 + 64 * 32 * (128 * 2 * 2 + 4)
+    return {"workload": "shared_prefix: 8192-token dense prefix + 64 branches, suffix U[64,512] at page 1",
+            "composable_ms": res["composable"], "flat_ms": res["flat"],
+            "composable_gbs": nbytes / res["composable"] / 1e6, "speedup_vs_flat": res["flat"] / res["composable"],
+            "launches": 3}
 
 
 PROFILE_CASES = {
@@ -537,6 +599,8 @@ def main():
         line["mix"] = {"workload": "continuous_batch: 8 chunked prefill (512) + 120 zipf decode, unequal K/V strides",
                        "ms": m["ms"], "decode_gbs_over_kernel": m["decode_gbs"],
                        "tflops_exact_over_kernel": m["tflops_exact"]}
+        sp = sec["shared_prefix"]
+        line["shared_prefix"] = dict(sp, frac_of_hbm=sp["composable_gbs"] / hbm)
     print(json.dumps(line))
 
 
