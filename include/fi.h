@@ -56,9 +56,9 @@ typedef struct {
     int32_t max_merge_units;     /* split units per plan */
     int64_t max_partial_rows;    /* rows of fp32 partial state (head_dim floats + 1 LSE each) */
     int32_t decode_min_chunk;    /* smallest KV chunk of a 16-row tile, tokens (default 256) */
-    int32_t prefill_min_chunk;   /* smallest KV chunk of a 128-row tile, tokens (default 1024) */
+    int32_t prefill_min_chunk;   /* smallest KV chunk of a 256-row tile, tokens (default 1024) */
     int32_t decode_cost_weight;  /* cost of one KV token in a 16-row tile (default 4) */
-    int32_t prefill_cost_weight; /* cost of one KV token in a 128-row tile (default 3) */
+    int32_t prefill_cost_weight; /* cost of one KV token in a 256-row tile (default 6) */
     int32_t split_factor;        /* target chunks per CTA per tile class (default 4) */
     int32_t reserved[3];
 } fi_plan_config;
@@ -72,7 +72,7 @@ typedef struct {
     int64_t num_partial_rows;
     int32_t num_qo_heads, num_kv_heads, head_dim, page_size, causal;
     int32_t chunk_decode;        /* KV tokens per chunk chosen for 16-row tiles */
-    int32_t chunk_prefill;       /* KV tokens per chunk chosen for 128-row tiles */
+    int32_t chunk_prefill;       /* KV tokens per chunk chosen for 256-row tiles */
     int32_t num_decode_items, num_prefill_items;
     int32_t reserved;
     int64_t int_ws_bytes_used;   /* bytes of the int workspace written (and copied) by the plan */

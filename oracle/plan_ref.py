@@ -4,16 +4,18 @@ The pages fix only the goal of the planner (FlashInfer paper summary, section
 "연구 방법론 / 3. 동적 부하 분산 스케줄링"): from each request's runtime
 sequence length, build on the CPU a plan that spreads the work evenly over all
 cores, with the tile size fixed at compile time; the plan is cached on the GPU
-and run by a fixed kernel launch.  The two CTA tile heights (128 and 16 query
-rows) come from the BatchAttention PR page, section "코드 분석 §1"
-(CTA_TILE_Q_1 = 128, CTA_TILE_Q_2 = 16).  The rule below is this library's own
+and run by a fixed kernel launch.  The two tile classes follow the pair of
+CTA tile heights on the BatchAttention PR page, section "코드 분석 §1"
+(CTA_TILE_Q_1 = 128, CTA_TILE_Q_2 = 16): 16-row decode tiles, and prefill
+tiles of two 128-row halves that share every K/V tile (256 rows).  The rule
+below is this library's own
 reading of that goal; this module restates it in plain Python, without sharing
 code with the C++ planner, so the two can be compared byte for byte.
 
 Rule:
  1. Request b has Lq query tokens, Lkv keys, R = Lq * G packed rows (packed row
     r = t * G + g is query token t, head hk * G + g).  Tile height T = 16 if
-    R <= 16 (decode class) else 128 (prefill class).
+    R <= 16 (decode class) else 256 (prefill class).
  2. Units (b, hk, qt) for qt < ceil(R / T); rows [qt*T, min(R, (qt+1)*T)).
     Visible KV length kv_eff = Lkv, or with the bottom-right causal mask
     min(Lkv, Lkv - Lq + t_last + 1) with t_last = (row_end - 1) // G, floored
@@ -29,7 +31,7 @@ Rule:
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
     load, ties to the smaller CTA index (longest processing time first).
  6. Output: header, per-CTA CSR offsets, items in CTA order (within a CTA the
-    128-row items first, then the 16-row items, each in the order dealt),
+    256-row items first, then the 16-row items, each in the order dealt),
     merge units, zeroed merge counters, request table.
 """
 from __future__ import annotations
@@ -39,6 +41,7 @@ import heapq
 import numpy as np
 
 MAGIC = 0x46495031
+TILE_DECODE, TILE_PREFILL = 16, 256
 HEADER_INTS = 16
 ITEM_INTS = 8
 MERGE_INTS = 8
@@ -101,12 +104,12 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
 
     # units in (b, hk, qt) order: (b, hk, qt, T, row0, row1, kv_eff)
     units = []
-    total = {16: 0, 128: 0}
+    total = {TILE_DECODE: 0, TILE_PREFILL: 0}
     for b in range(batch):
         R = lq[b] * group
         if R == 0:
             continue
-        T = 16 if R <= 16 else 128
+        T = TILE_DECODE if R <= TILE_DECODE else TILE_PREFILL
         for hk in range(num_kv_heads):
             for qt in range(_ceil_div(R, T)):
                 r0, r1 = qt * T, min(R, (qt + 1) * T)
@@ -119,11 +122,11 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
                 total[T] += kv_eff
 
     chunk = {}
-    for T, min_chunk, gran in ((16, cfg["decode_min_chunk"], max(page_size, 64)),
-                               (128, cfg["prefill_min_chunk"], max(page_size, 128))):
+    for T, min_chunk, gran in ((TILE_DECODE, cfg["decode_min_chunk"], max(page_size, 64)),
+                               (TILE_PREFILL, cfg["prefill_min_chunk"], max(page_size, 128))):
         want = max(min_chunk, _ceil_div(total[T], C * cfg["split_factor"]))
         chunk[T] = _ceil_div(want, gran) * gran
-    weight = {16: cfg["decode_cost_weight"], 128: cfg["prefill_cost_weight"]}
+    weight = {TILE_DECODE: cfg["decode_cost_weight"], TILE_PREFILL: cfg["prefill_cost_weight"]}
 
     items = []   # (sort key, fields)
     merges = []
@@ -175,7 +178,7 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos
-        # 128-row tiles first, then 16-row tiles, each in the order dealt
+        # prefill-class tiles first, then 16-row tiles, each in the order dealt
         mine = [f for f in per_cta[c] if lq[f[0]] * group > 16] + [f for f in per_cta[c] if lq[f[0]] * group <= 16]
         for fields in mine:
             ws[off_items + ITEM_INTS * pos: off_items + ITEM_INTS * (pos + 1)] = fields
@@ -190,6 +193,6 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     info = dict(num_ctas=C, num_items=n_items, num_merge_units=n_merge, batch=batch,
                 num_partial_rows=part_rows, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
                 head_dim=head_dim, page_size=page_size, causal=causal, chunk_decode=chunk[16],
-                chunk_prefill=chunk[128], num_decode_items=n_dec, num_prefill_items=n_items - n_dec,
+                chunk_prefill=chunk[TILE_PREFILL], num_decode_items=n_dec, num_prefill_items=n_items - n_dec,
                 int_ws_bytes_used=4 * total_ints, max_partial_rows=cfg["max_partial_rows"])
     return OK, ws, info

@@ -121,7 +121,7 @@ def make_plan_config(num_ctas: int, **overrides) -> PlanConfig:
     """A config without asking the device (host-side planning and tests)."""
     cfg = PlanConfig(num_ctas=num_ctas, max_batch=8192, max_items=1 << 17, max_merge_units=1 << 15,
                      max_partial_rows=1 << 19, decode_min_chunk=256, prefill_min_chunk=1024, decode_cost_weight=4,
-                     prefill_cost_weight=3, split_factor=4)
+                     prefill_cost_weight=6, split_factor=4)
     for k, v in overrides.items():
         setattr(cfg, k, v)
     return cfg

@@ -167,7 +167,7 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   out->decode_min_chunk = 256;
   out->prefill_min_chunk = 1024;
   out->decode_cost_weight = 4;
-  out->prefill_cost_weight = 3;
+  out->prefill_cost_weight = 6;
   out->split_factor = 4;
   return FI_OK;
 }
@@ -230,7 +230,7 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   p.log2_page = lp;
   p.num_pages = num_pages;
 
-  // 128-row tiles go to the tensor cores when every TMA box of a page is a
+  // Prefill-class items go to the tensor cores when every TMA box of a page is a
   // whole number of 1024-byte swizzle atoms (P >= 8) and a tile holds whole
   // tokens (G divides 128); otherwise the CUDA-core path runs them.
   const int G = p.group;

@@ -11,7 +11,7 @@ namespace fi {
 
 constexpr int kHeadDim = 128;
 
-// CUDA-core path (16-row decode tiles; 128-row tiles when pages are < 8 tokens)
+// CUDA-core path (16-row decode tiles; prefill-class items too when pages are < 8 tokens)
 constexpr int kStageTokens = 64;       // KV tokens per pipeline stage
 constexpr int kStages = 4;             // depth of the K/V ring
 constexpr int kConsumerWarps = 8;
@@ -24,13 +24,14 @@ constexpr int kHalfWarps = 2 * kConsumerWarps;
 constexpr int kTokBlock = 4;           // tokens a half-warp scores before one softmax update
 constexpr float kLazyRescale = 8.0f;   // log2 units: keep a stale max until it is 2^8 off
 
-// Tensor-core path (128-row tiles): 128 x 128 S and O tiles in tensor memory.
-constexpr int kTileM = 128;            // packed query rows per tile
+// Tensor-core path (prefill-class items of up to two 128-row M tiles):
+// 128 x 128 S and O tiles in tensor memory.
+constexpr int kTileM = 128;            // packed query rows per M tile
 constexpr int kTileN = 128;            // KV tokens per tile
-constexpr int kTmemCols = 512;         // S (2 buffers x 128 cols) + O (2 buffers x 128 cols)
-constexpr int kTmemO = 256;            // first column of O buffer 0
+constexpr int kTmemCols = 512;         // S of M tiles A, B (128 cols each), then O of A, B
+constexpr int kTmemO = 256;            // first column of O of M tile A
 constexpr int kMinTmaPage = 8;         // pages of >= 8 tokens keep every TMA box 1024-byte aligned
-constexpr int kSoftmaxWarp0 = 4;       // warps 4..7 own S/O columns 0..63, warps 8..11 columns 64..127
+constexpr int kSoftmaxWarp0 = 4;       // warps 4..7 own KV columns 0..63 of each tile, warps 8..11 columns 64..127
 constexpr int kSoftmaxThreads = 256;
 constexpr int kMmaWarp = 1;
 constexpr int kVWarp = 2;              // loads V tiles; warp 0 loads Q and K tiles
@@ -56,7 +57,7 @@ struct RunParams {
   int64_t partial_o_offset;  // floats
   float scale_log2;          // sm_scale * log2(e)
   int32_t num_qo_heads, num_kv_heads, group, page_size, log2_page, num_pages;
-  int32_t tc_prefill;        // 128-row tiles on the tensor cores (else CUDA cores)
+  int32_t tc_prefill;        // prefill-class items on the tensor cores (else CUDA cores)
 };
 
 struct DecodeBufs {
@@ -71,7 +72,7 @@ struct DecodeBufs {
 // Every [128][64] block is one 16 KB operand half: 128 rows of 64 elements
 // (128 bytes), 128-byte swizzled as TMA writes it and tcgen05 reads it.
 struct PrefillBufs {
-  uint16_t q[2][2][kTileM][64];     // [buffer][d half][row][dim]
+  uint16_t q[2][2][kTileM][64];     // [M tile][d half][row][dim]
   uint16_t k[2][2][kTileN][64];     // [stage][d half][token][dim]
   uint16_t v[2][2][kTileN][64];
 };
@@ -83,10 +84,11 @@ struct alignas(1024) RunSmem {
   };
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t q_full[2], q_empty[2], o_ready[2], o_free[2], drain;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2];
-  float xmax[2][2][kTileM];  // [tile parity][column half][row]: the two halves' row maxima
-  float xsum[2][2][kTileM];  // [item parity][column half][row]: the halves' row sums at the epilogue
+  uint64_t q_full, q_empty, drain;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];   // [ring stage]
+  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];    // [M tile of the item]
+  float xmax[2][2][kTileM];     // [slot][column half][row]: row max of each half of an S tile
+  float xsum[2][2][2][kTileM];  // [item slot][M tile][column half][row]: row sums at the epilogue
   uint32_t tmem_base;
   volatile int abort;  // set by the role whose bounded wait ran out
   int merge_last;

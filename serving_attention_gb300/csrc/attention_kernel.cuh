@@ -420,7 +420,7 @@ namespace fi {
 
 // ---------------------------------------------------------------- kernel
 
-// A CTA's items come prefill-class (128-row tiles) first, then decode-class
+// A CTA's items come prefill-class (256-row tiles) first, then decode-class
 // (16-row tiles); returns the index of its first decode-class item.
 __device__ __forceinline__ int32_t first_decode_item(const RunParams& p, int32_t begin, int32_t end, int32_t off_items,
                                                      int32_t off_req) {
@@ -473,18 +473,17 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
       mbar_init(&sm.empty[s], kConsumerWarps); // one arrival per consumer warp
     }
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.q_full[s], 1);
-      mbar_init(&sm.q_empty[s], 1);
-      mbar_init(&sm.o_ready[s], 1);
-      mbar_init(&sm.o_free[s], kSoftmaxThreads / 32);  // one arrival per softmax warp
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
       mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.p_full[s], kSoftmaxThreads / 32);
-      mbar_init(&sm.pv_done[s], 1);
+      mbar_init(&sm.o_ready[s], 1);
+      mbar_init(&sm.p_full[s], 8);  // one arrival per softmax warp
+      mbar_init(&sm.o_free[s], 8);
     }
     sm.abort = 0;
     sm.merge_last = 0;

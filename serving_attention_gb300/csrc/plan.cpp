@@ -5,13 +5,14 @@
 // scheduler takes every request's sequence length and builds, on the CPU, a
 // plan that gives all SMs an even share of the work.  The plan is copied to
 // the GPU once per step and the kernel launch never changes, so one CUDA graph
-// replays any plan.  The two tile heights (128 query rows for prefill work,
-// 16 for decode work) are the CTA_TILE_Q_1 / CTA_TILE_Q_2 pair of the
-// BatchAttention PR page, section "코드 분석 §1".
+// replays any plan.  The two tile classes follow the CTA_TILE_Q_1 = 128 /
+// CTA_TILE_Q_2 = 16 pair of the BatchAttention PR page, section "코드 분석 §1":
+// 16 rows for decode work, and for prefill work two 128-row halves that share
+// every K/V tile (256 rows).
 //
 // Rule (this library's reading of that goal; the pages give no cost model):
 //  * request b -> R = qo_len * G packed rows (row t*G+g = token t, head hk*G+g);
-//    tile T = 16 when R <= 16, else 128;
+//    tile T = 16 when R <= 16, else 256;
 //  * unit (b, hk, q-tile) with its visible KV length (bottom-right causal);
 //  * per tile class, a KV chunk length = max(min_chunk, total / (CTAs * split))
 //    rounded up to the class granule; units longer than a chunk are split
@@ -47,7 +48,7 @@ struct Chunk {
 };
 
 // Order of the longest-processing-time deal: cost descending, then the
-// 128-row class first, then (b, hk, q-tile, chunk) ascending.  Keys are unique.
+// prefill class first, then (b, hk, q-tile, chunk) ascending.  Keys are unique.
 bool deal_before(const Chunk& x, const Chunk& y) {
   if (x.cost != y.cost) return x.cost > y.cost;
   if (x.tile != y.tile) return x.tile > y.tile;
@@ -213,7 +214,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
 
   int32_t* ws = static_cast<int32_t*>(workspace_host);
   std::memset(ws, 0, size_t(total_ints) * 4);
-  // CTA c's items occupy [start[c], start[c+1]): its 128-row items first,
+  // CTA c's items occupy [start[c], start[c+1]): its prefill-class items first,
   // then its 16-row items, each kept in the order the deal handed them out
   // (one switch between the kernel's two tile paths per CTA at most).
   std::vector<int32_t> start(C + 1, 0);

@@ -27,7 +27,7 @@
 #define FI_REQ_INTS 4
 
 #define FI_TILE_DECODE 16
-#define FI_TILE_PREFILL 128
+#define FI_TILE_PREFILL 256  // two 128-row M tiles sharing each K/V tile
 #define FI_GRANULE_DECODE 64
 #define FI_GRANULE_PREFILL 128
 

@@ -58,14 +58,15 @@ def test_tiny_decode_full():
 
 
 @pytest.mark.parametrize("qo,kv,causal,dtype", [
-    ([32], [128], 0, "bf16"),          # one 128-row tile against one 128-token KV tile
+    ([32], [128], 0, "bf16"),          # one 128-row M tile against one 128-token KV tile
     ([32], [128], 1, "bf16"),          # the same with the causal diagonal
     ([32], [77], 0, "fp16"),           # ragged KV tail inside the tile
     ([40], [300], 1, "bf16"),          # two row tiles (128 + 32 rows), three KV tiles
     ([64, 33], [1000, 40], 1, "bf16"), # two requests, long and short
+    ([100], [600], 1, "bf16"),         # 400 rows: a 256-row item and a 144-row item
 ])
 def test_tensor_core_tiles(qo, kv, causal, dtype):
-    """128-row tiles on the tensor cores (page 16, G 4), smallest cases first."""
+    """Prefill-class items (one or two 128-row M tiles) on the tensor cores, page 16, G 4."""
     b = workloads.make_batch("tc", dtype, qo, kv, 8, 2, 16, causal, 300 + len(qo) + kv[0], DEV,
                              pool_pages=sum((k + 15) // 16 for k in kv) + 2)
     info = _full_check(b)

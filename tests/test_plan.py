@@ -102,11 +102,11 @@ def _check_invariants(ws, qop, kv, hq, hkv, causal, cfgd):
                 else:
                     assert chunks[0][2] == -1 and chunks[0][3] == -1
     # LPT bound: max CTA load <= mean load + largest item
-    w = {16: cfgd["decode_cost_weight"], 128: cfgd["prefill_cost_weight"]}
+    w = {16: cfgd["decode_cost_weight"], plan_ref.TILE_PREFILL: cfgd["prefill_cost_weight"]}
     cost = []
     for it in items:
         R = int(qop[it[0] + 1] - qop[it[0]]) * G
-        cost.append((int(it[5]) - int(it[4])) * w[16 if R <= 16 else 128])
+        cost.append((int(it[5]) - int(it[4])) * w[16 if R <= 16 else plan_ref.TILE_PREFILL])
     cost = np.array(cost, dtype=np.int64)
     loads = np.array([cost[cta[c]:cta[c + 1]].sum() for c in range(C)])
     if cost.size:

@@ -34,7 +34,7 @@ def test_static_scratch_matches_regular_run(case):
     if case == "decode":
         b = workloads.llama8b_decode(device=DEV, batch=16)
         cfg = fi.default_plan_config(0)
-    else:  # 128-row tiles split into 256-token chunks
+    else:  # prefill-class items split into 256-token chunks
         b = workloads.make_batch("split_prefill", "bf16", [64, 40], [1500, 700], 8, 2, 16, 1, 4242, DEV,
                                  pool_pages=160)
         cfg = fi.default_plan_config(0, prefill_min_chunk=256, split_factor=16)
