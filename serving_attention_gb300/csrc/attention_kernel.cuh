@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
     } else if (warp == kVWarp) {
       pf_produce<true>(p, sm, begin, mid, off_items, off_req);
     } else if (warp == kMmaWarp) {
-      if ((threadIdx.x & 31) == 0) pf_mma<T>(p, sm, begin, mid, off_items);
+      pf_mma<T>(p, sm, begin, mid, off_items);
       __syncwarp();
     } else if (warp >= kSoftmaxWarp0) {
       pf_softmax<T>(p, sm, begin, mid, off_items, off_req, off_merge, off_cnt, causal);

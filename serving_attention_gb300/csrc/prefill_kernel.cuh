@@ -15,8 +15,9 @@
 //    ([pages, slots, heads, dims], box (64, 1, P, 1)) into a 2-stage ring,
 //    128-byte swizzled; pages past the request read out of bounds as zeros.
 //    Warp 2 does the same for V on its own ring.
-//  * warp 1, one thread (MMA): S_m = Q_m K^T as 8 tcgen05.mma (M128 N128 K16,
-//    both operands K-major in shared memory) into tensor memory, and
+//  * warp 1 (MMA; the whole warp runs the loop, one elected lane issues):
+//    S_m = Q_m K^T as 8 tcgen05.mma (M128 N128 K16, both operands K-major in
+//    shared memory) into tensor memory, and
 //    O_m += P_m V with P_m read back from tensor memory (it overwrites the S_m
 //    columns already consumed, as 16-bit pairs) and V as an MN-major operand.
 //    Order per KV tile j: P V of A for tile j, S of A for tile j+1, P V of B
@@ -130,47 +131,56 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
   __syncwarp();
 }
 
-// Single thread: issues every MMA of the CTA's prefill-class items in the
-// fixed order described at the top of this file, each after a bounded wait
-// for exactly what it reads.
+// Warp 1, converged: every lane walks the items and waits; one elected lane
+// issues each MMA and commit (the tc::*_warp forms), which keeps the operands
+// warp-uniform so that the issue keeps pace with the tensor pipe.  The MMAs
+// follow the fixed order described at the top of this file, each after a
+// bounded wait for exactly what it reads.
 template <typename T>
 __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t idesc_qk = tc::idesc_f16(kBf16, false, kTileM, kTileN);
   constexpr uint32_t idesc_pv = tc::idesc_f16(kBf16, true, kTileM, kHeadDim);
+  const int lane = threadIdx.x & 31;
   const uint32_t tmem = sm.tmem_base;
-  uint32_t kt = 0, pe = 0;           // KV tiles and non-empty items so far
-  uint32_t tiles_m[2] = {0, 0};      // per M tile: P V issued so far (phases of p_full)
-  uint32_t items_m[2] = {0, 0};      // per M tile: items finished (phases of o_free)
+  // Shared-memory descriptors of the first block of each operand buffer; the
+  // start-address field counts 16-byte units, so the other blocks and the K16
+  // steps are constant offsets: a 64-dim half is 16 KB (1024 units), an M
+  // tile or ring stage 32 KB (2048), 16 dims along a swizzled row 32 bytes
+  // (2), 16 V tokens 2 KB (128).  Every sum is a real shared-memory address,
+  // which stays below 2^18 bytes: the field never carries.
+  const uint64_t dq = tc::smem_desc_sw128(smem_u32(&sm.pf.q[0][0][0][0]), 16, 1024);
+  const uint64_t dk = tc::smem_desc_sw128(smem_u32(&sm.pf.k[0][0][0][0]), 16, 1024);
+  const uint64_t dv = tc::smem_desc_sw128(smem_u32(&sm.pf.v[0][0][0][0]), 64 * kTileN * 2, 1024);
+  uint32_t kt = 0, pe = 0;       // KV tiles and non-empty items so far
+  uint32_t tiles_m[2] = {0, 0};  // per M tile: P V issued so far (phases of p_full)
+  uint32_t items_m[2] = {0, 0};  // per M tile: items finished (phases of o_free)
   bool issued = false;
-  auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_bounded(bar, parity, &sm.abort); };
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return warp_wait(bar, parity, &sm.abort); };
   auto issue_s = [&](int m, int st) {
-    const uint32_t q_lo = smem_u32(&sm.pf.q[m][0][0][0]), q_hi = smem_u32(&sm.pf.q[m][1][0][0]);
-    const uint32_t k_lo = smem_u32(&sm.pf.k[st][0][0][0]), k_hi = smem_u32(&sm.pf.k[st][1][0][0]);
+    const uint64_t a0 = dq + 2048u * m, b0k = dk + 2048u * st;
 #pragma unroll
     for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-      const uint32_t off = (kk & 3) * 32;  // 16 dims = 32 bytes along the swizzled 128-byte row
-      const uint64_t adesc = tc::smem_desc_sw128((kk < 4 ? q_lo : q_hi) + off, 16, 1024);
-      const uint64_t bdesc = tc::smem_desc_sw128((kk < 4 ? k_lo : k_hi) + off, 16, 1024);
-      tc::mma_ss(tmem + m * kTileN, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+      const uint32_t step = 1024u * (kk >> 2) + 2u * (kk & 3);
+      tc::mma_ss_warp(tmem + m * kTileN, a0 + step, b0k + step, idesc_qk, kk > 0 ? 1u : 0u);
     }
-    tc::mma_commit(&sm.s_full[m]);
+    tc::mma_commit_warp(&sm.s_full[m]);
     issued = true;
   };
   auto issue_pv = [&](int m, int st, bool first) {
-    const uint32_t v_lo = smem_u32(&sm.pf.v[st][0][0][0]);
+    // V is [token][dim]: MN-major B; next 64 dims at +16 KB, next 8 tokens at +1 KB
+    const uint64_t bv = dv + 2048u * st;
     const uint32_t o_tmem = tmem + kTmemO + m * kHeadDim;
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
-      // V is [token][dim]: MN-major B; next 64 dims at +16 KB, next 8 tokens at +1 KB
-      const uint64_t bdesc = tc::smem_desc_sw128(v_lo + kk * 16 * 128, 64 * kTileN * 2, 1024);
       // P_m of tokens 16kk..16kk+15: 8 columns of 16-bit pairs in the S_m buffer
       // (tokens 0..63 at columns 0..31, tokens 64..127 at columns 64..95)
       const uint32_t p_col = kk * 8 + (kk >= 4 ? 32 : 0);
-      tc::mma_ts(o_tmem, tmem + m * kTileN + p_col, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+      tc::mma_ts_warp(o_tmem, tmem + m * kTileN + p_col, bv + 128u * kk, idesc_pv, (!first || kk > 0) ? 1u : 0u);
     }
   };
-  for (int32_t i = b0; i < b1 && !sm.abort; ++i) {
+  for (int32_t i = b0; i < b1; ++i) {
+    if (__shfl_sync(0xffffffffu, sm.abort, 0)) break;
     const Item it = load_item(p.iws, off_items, i);
     const int ntiles = item_kv_tiles(it);
     if (ntiles == 0) continue;
@@ -179,8 +189,8 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
     if (!ok) break;
     tc::fence_after_sync();
     for (int m = 0; m < nm; ++m) issue_s(m, kt & 1);
-    tc::mma_commit(&sm.k_empty[kt & 1]);
-    if (ntiles == 1) tc::mma_commit(&sm.q_empty);  // the item's last read of Q
+    tc::mma_commit_warp(&sm.k_empty[kt & 1]);
+    if (ntiles == 1) tc::mma_commit_warp(&sm.q_empty);  // the item's last read of Q
     for (int j = 0; j < ntiles && ok; ++j) {
       const uint32_t g = kt + j;  // KV tile in the CTA's stream
       const int st = g & 1;
@@ -194,7 +204,7 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
         issue_pv(m, st, j == 0);
         ++tiles_m[m];
         if (!more) {
-          tc::mma_commit(&sm.o_ready[m]);
+          tc::mma_commit_warp(&sm.o_ready[m]);
           continue;
         }
         if (m == 0) {
@@ -205,10 +215,10 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
         issue_s(m, st_next);
       }
       if (!ok) break;
-      tc::mma_commit(&sm.v_empty[st]);
+      tc::mma_commit_warp(&sm.v_empty[st]);
       if (more) {
-        tc::mma_commit(&sm.k_empty[st_next]);
-        if (j + 2 == ntiles) tc::mma_commit(&sm.q_empty);
+        tc::mma_commit_warp(&sm.k_empty[st_next]);
+        if (j + 2 == ntiles) tc::mma_commit_warp(&sm.q_empty);
       }
     }
     if (!ok) break;
@@ -218,8 +228,9 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
   }
   // No MMA may still run when the CTA leaves the prefill phase.
   if (issued) {
-    tc::mma_commit(&sm.drain);
-    mbar_wait_drain(&sm.drain, 0);
+    tc::mma_commit_warp(&sm.drain);
+    if (lane == 0) mbar_wait_drain(&sm.drain, 0);
+    __syncwarp();
   }
 }
 

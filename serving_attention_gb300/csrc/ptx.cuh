@@ -71,11 +71,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-// Warp-uniform bounded wait: lane 0 waits, the result is broadcast.
+// Warp-uniform bounded wait, called by a converged warp.  Every lane polls
+// (a branch around a single polling lane costs more than the poll itself);
+// lane 0's view of completion, abort and budget is broadcast, so all lanes
+// leave on the same iteration with the same result: false when the budget ran
+// out (the abort flag is then set) or another role gave up.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort) && !*abort;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  const long long t0 = clock64();
+  while (true) {
+    const int done = mbar_try_wait(bar, parity) ? 1 : 0;
+    const int gave_up = *abort != 0 ? 2 : 0;
+    const int late = clock64() - t0 > kWaitBudgetClocks ? 4 : 0;
+    const int st = __shfl_sync(0xffffffffu, done | gave_up | late, 0);
+    if (st & 2) return false;
+    if (st & 1) return true;
+    if (st & 4) {
+      *abort = kStatusTimeout;  // every lane stores the same value
+      return false;
+    }
+  }
 }
 
 // Bounded wait that ignores the abort flag: used to drain a role's own
