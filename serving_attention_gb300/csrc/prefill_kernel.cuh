@@ -156,7 +156,6 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
   uint32_t tiles_m[2] = {0, 0};  // per M tile: P V issued so far (phases of p_full)
   uint32_t items_m[2] = {0, 0};  // per M tile: items finished (phases of o_free)
   bool issued = false;
-  auto wait = [&](uint64_t* bar, uint32_t parity) { return warp_wait(bar, parity, &sm.abort); };
   auto issue_s = [&](int m, int st) {
     const uint64_t a0 = dq + 2048u * m, b0k = dk + 2048u * st;
 #pragma unroll
@@ -185,7 +184,8 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
     const int ntiles = item_kv_tiles(it);
     if (ntiles == 0) continue;
     const int nm = item_m_tiles(it);
-    bool ok = wait(&sm.q_full, pe & 1) && wait(&sm.k_full[kt & 1], (kt >> 1) & 1);
+    bool ok = warp_wait_all(2, &sm.q_full, pe & 1, &sm.k_full[kt & 1], (kt >> 1) & 1, nullptr, 0, nullptr, 0,
+                            &sm.abort);
     if (!ok) break;
     tc::fence_after_sync();
     for (int m = 0; m < nm; ++m) issue_s(m, kt & 1);
@@ -197,8 +197,15 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
       const bool more = j + 1 < ntiles;
       const int st_next = (g + 1) & 1;
       for (int m = 0; m < nm && ok; ++m) {
-        ok = wait(&sm.p_full[m], tiles_m[m] & 1) && (m > 0 || wait(&sm.v_full[st], (g >> 1) & 1)) &&
-             (j > 0 || wait(&sm.o_free[m], (items_m[m] & 1) ^ 1));
+        // Everything this step reads, polled at once: P_m of tile j; for M
+        // tile A also V of tile j and K of tile j+1; at an item's first tile
+        // the O_m columns.  Entries that do not apply repeat the first.
+        uint64_t* const pb = &sm.p_full[m];
+        const uint32_t pp = tiles_m[m] & 1;
+        const bool kv = m == 0, need_k = kv && more;
+        ok = warp_wait_all(4, pb, pp, kv ? &sm.v_full[st] : pb, kv ? (g >> 1) & 1 : pp,
+                           j == 0 ? &sm.o_free[m] : pb, j == 0 ? (items_m[m] & 1) ^ 1 : pp,
+                           need_k ? &sm.k_full[st_next] : pb, need_k ? ((g + 1) >> 1) & 1 : pp, &sm.abort);
         if (!ok) break;
         tc::fence_after_sync();
         issue_pv(m, st, j == 0);
@@ -206,11 +213,6 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
         if (!more) {
           tc::mma_commit_warp(&sm.o_ready[m]);
           continue;
-        }
-        if (m == 0) {
-          ok = wait(&sm.k_full[st_next], ((g + 1) >> 1) & 1);
-          if (!ok) break;
-          tc::fence_after_sync();
         }
         issue_s(m, st_next);
       }

@@ -77,6 +77,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // leave on the same iteration with the same result: false when the budget ran
 // out (the abort flag is then set) or another role gave up.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  // Fast path: one poll, no read of the abort flag (a shared-memory read is
+  // slow while the tensor core streams its operands from shared memory).
+  if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1 : 0, 0)) return true;
   const long long t0 = clock64();
   while (true) {
     const int done = mbar_try_wait(bar, parity) ? 1 : 0;
@@ -87,6 +90,32 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     if (st & 1) return true;
     if (st & 4) {
       *abort = kStatusTimeout;  // every lane stores the same value
+      return false;
+    }
+  }
+}
+
+// Warp-uniform bounded wait for up to four barrier phases at once: lane l
+// polls entry l (lanes past n repeat entry 0), so one instruction covers the
+// whole list.  Same results and abort behaviour as warp_wait.
+__device__ __forceinline__ bool warp_wait_all(int n, uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
+                                              uint64_t* b2, uint32_t p2, uint64_t* b3, uint32_t p3,
+                                              volatile int* abort) {
+  const int lane = threadIdx.x & 31;
+  const int e = lane < n ? lane : 0;
+  uint64_t* bar = e == 0 ? b0 : e == 1 ? b1 : e == 2 ? b2 : b3;
+  const uint32_t parity = e == 0 ? p0 : e == 1 ? p1 : e == 2 ? p2 : p3;
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (true) {
+    const int done = __all_sync(0xffffffffu, mbar_try_wait(bar, parity)) ? 1 : 0;
+    const int gave_up = *abort != 0 ? 2 : 0;
+    const int late = clock64() - t0 > kWaitBudgetClocks ? 4 : 0;
+    const int st = __shfl_sync(0xffffffffu, done | gave_up | late, 0);
+    if (st & 2) return false;
+    if (st & 1) return true;
+    if (st & 4) {
+      *abort = kStatusTimeout;
       return false;
     }
   }
