@@ -291,13 +291,14 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
               for (int e = 0; e < 32; ++e)
                 if (kbase + h * 32 + e > lim[mt]) sv[h][e] = 0xff800000u;  // -inf
           }
-          float mx8[8];
+          // 64-value max in four independent chains of three-input maxima
+          auto val = [&](int e) { return __uint_as_float(sv[e >> 5][e & 31]); };
+          float mx4[4];
 #pragma unroll
-          for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(sv[0][a]);
+          for (int a = 0; a < 4; ++a) mx4[a] = max3(val(3 * a), val(3 * a + 1), val(3 * a + 2));
 #pragma unroll
-          for (int e = 8; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e >> 5][e & 31]));
-          mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int e = 12; e < 64; e += 2) mx4[(e >> 1) & 3] = max3(mx4[(e >> 1) & 3], val(e), val(e + 1));
+          mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
         }
         // the two halves of the row agree on its max (slots alternate)
         sm.xmax[ev & 1][half][r] = mx;
@@ -326,23 +327,26 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         }
         // P = 2^(s*c - m) as 16-bit pairs over the first 32 columns of this half
         const float msub = (m_new == -INFINITY) ? 0.f : m_new;
-        float sum8[8];
+        const float2 cc = make_float2(c, c), nms = make_float2(-msub, -msub);
+        float2 sum4[4];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) sum8[a] = 0.f;
+        for (int a = 0; a < 4; ++a) sum4[a] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float a = ex2(fmaf(__uint_as_float(sv[h][2 * e]), c, -msub));
-            const float b = ex2(fmaf(__uint_as_float(sv[h][2 * e + 1]), c, -msub));
-            sum8[e & 7] += a + b;
-            pk[e] = tc::pack2<T>(a, b);
+            const float2 x =
+                fma2(make_float2(__uint_as_float(sv[h][2 * e]), __uint_as_float(sv[h][2 * e + 1])), cc, nms);
+            const float2 pe = make_float2(ex2(x.x), ex2(x.y));
+            sum4[e & 3] = add2(sum4[e & 3], pe);
+            pk[e] = tc::pack2<T>(pe.x, pe.y);
           }
           tc::tmem_st16(tl + mt * kTileN + c0 + h * 16, pk);
         }
         tc::tmem_st_wait();
-        lrun[mt] += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        const float2 s01 = add2(sum4[0], sum4[1]), s23 = add2(sum4[2], sum4[3]), s = add2(s01, s23);
+        lrun[mt] += s.x + s.y;
         mrun[mt] = m_new;
         tc::fence_before_sync();
         __syncwarp();
