@@ -31,8 +31,20 @@ constexpr int kTileN = 128;            // KV tokens per tile
 constexpr int kTmemCols = 512;         // S of M tiles A, B (128 cols each), then O of A, B
 constexpr int kTmemO = 256;            // first column of O of M tile A
 constexpr int kMinTmaPage = 8;         // pages of >= 8 tokens keep every TMA box 1024-byte aligned
-constexpr int kSoftmaxWarp0 = 4;       // warps 4..7 own KV columns 0..63 of each tile, warps 8..11 columns 64..127
+constexpr int kSoftmaxWarp0 = 4;       // warps 4..7 own the rows of M tile A, warps 8..11 those of M tile B
 constexpr int kSoftmaxThreads = 256;
+// Register budgets of the tensor-core phase, per thread: warps 0..3 (loaders,
+// MMA) drop to kRegsLoader, the two softmax warpgroups rise to kRegsSoftmax
+// (a full 128-column S row per thread), and all return to kRegsLaunch before
+// the CUDA-core phase.  kRegsLoader * 128 + kRegsSoftmax * 256 must not
+// exceed the registers the CTA was launched with; the host launches only a
+// build whose register count is at least kRegsLaunch (an increase that
+// cannot be met would wait forever).
+constexpr int kPhaseBarrier = 3;       // named barrier ending the tensor-core phase (1: decode, 2: merge)
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsLoader = 104;
+constexpr int kRegsSoftmax = 192;
+static_assert(kRegsLoader * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads, "register split exceeds the launch");
 constexpr int kMmaWarp = 1;
 constexpr int kVWarp = 2;              // loads V tiles; warp 0 loads Q and K tiles
 
@@ -86,9 +98,8 @@ struct alignas(1024) RunSmem {
   uint64_t empty[kStages];
   uint64_t q_full, q_empty, drain;
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];   // [ring stage]
-  uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];    // [M tile of the item]
-  float xmax[2][2][kTileM];     // [slot][column half][row]: row max of each half of an S tile
-  float xsum[2][2][2][kTileM];  // [item slot][M tile][column half][row]: row sums at the epilogue
+  uint64_t s_full[2], o_ready[2], o_free[2];  // [M tile of the item]
+  uint64_t p_full[2][2];                      // [M tile][P of KV tokens 0..63, 64..127]
   uint32_t tmem_base;
   volatile int abort;  // set by the role whose bounded wait ran out
   int merge_last;

@@ -482,8 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
       mbar_init(&sm.v_empty[s], 1);
       mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.o_ready[s], 1);
-      mbar_init(&sm.p_full[s], 8);  // one arrival per softmax warp
-      mbar_init(&sm.o_free[s], 8);
+      mbar_init(&sm.p_full[s][0], 4);  // one arrival per warp of the M tile's softmax warpgroup
+      mbar_init(&sm.p_full[s][1], 4);
+      mbar_init(&sm.o_free[s], 4);
     }
     sm.abort = 0;
     sm.merge_last = 0;
@@ -499,19 +500,31 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   tc::fence_after_sync();
 
   if (tc_phase) {
-    if (warp == 0) {
-      pf_produce<false>(p, sm, begin, mid, off_items, off_req);
-    } else if (warp == kVWarp) {
-      pf_produce<true>(p, sm, begin, mid, off_items, off_req);
-    } else if (warp == kMmaWarp) {
-      pf_mma<T>(p, sm, begin, mid, off_items);
-      __syncwarp();
-    } else if (warp >= kSoftmaxWarp0) {
+    // Each branch returns to kRegsLaunch before the code paths merge: the
+    // softmax warpgroups release their registers before the phase barrier,
+    // the loader warpgroup takes its share back after it.
+    if (warp < kSoftmaxWarp0) {
+      tc::setmaxnreg_dec<kRegsLoader>();
+      if (warp == 0) {
+        pf_produce<false>(p, sm, begin, mid, off_items, off_req);
+      } else if (warp == kVWarp) {
+        pf_produce<true>(p, sm, begin, mid, off_items, off_req);
+      } else if (warp == kMmaWarp) {
+        pf_mma<T>(p, sm, begin, mid, off_items);
+        __syncwarp();
+      }
+      tc::fence_before_sync();
+      named_barrier_sync_unaligned(kPhaseBarrier, kThreads);
+      tc::fence_after_sync();
+      tc::setmaxnreg_inc<kRegsLaunch>();
+    } else {
+      tc::setmaxnreg_inc<kRegsSoftmax>();
       pf_softmax<T>(p, sm, begin, mid, off_items, off_req, off_merge, off_cnt, causal);
+      tc::setmaxnreg_dec<kRegsLaunch>();
+      tc::fence_before_sync();
+      named_barrier_sync_unaligned(kPhaseBarrier, kThreads);
+      tc::fence_after_sync();
     }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
   }
 
   if (warp == 0) {

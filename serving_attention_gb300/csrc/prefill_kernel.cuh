@@ -25,17 +25,18 @@
 //    tensor core works on the other one.  The commit after S_m(j+1) also
 //    covers P_m V(j), so a softmax that sees S_m(j+1) knows O_m is complete
 //    through tile j.
-//  * warps 4..11 (softmax): warp w and warp w+4 hold the same 32 query rows
-//    (TMEM lanes 32(w%4)..), one the KV columns 0..63 of each tile and the
-//    other 64..127; both work through M tile A, then B.  Per tile and M tile:
-//    one 64-column load of S, the bottom-right causal mask and the chunk end,
-//    the row max of the half, exchanged with the partner warp through shared
-//    memory; the running max moves lazily (only when it grows by more than
-//    2^8, then each half rescales its O columns in tensor memory); P goes
-//    back as 16-bit pairs -- columns 0..31 of the S buffer for the first
-//    half, 64..95 for the second.  At the end each half reads its 64 O
-//    columns, divides by the row sum (the two halves' shares added) and
-//    stores O; the first half stores LSE (or the fp32 partial state).
+//  * warps 4..7 (M tile A) and 8..11 (M tile B) (softmax): thread = query
+//    row = TMEM lane, the whole 128-column S row in registers (the loaders
+//    and the MMA warp give up registers for it, setmaxnreg).  Per KV tile:
+//    one load of the S row, the bottom-right causal mask and the chunk end,
+//    the row max; the running max moves lazily (only when it grows by more
+//    than 2^8, then the O row is rescaled in tensor memory); P goes back as
+//    16-bit pairs into the first 64 columns of the S buffer, in two halves
+//    of 64 KV tokens with a barrier each, so P V starts on the first half
+//    while the second is computed.  The two warpgroups run on different M
+//    tiles, so on every SM sub-partition one warp computes while the other
+//    waits.  At the end: read O, divide by the row sum, store O and LSE (or
+//    an fp32 partial state).
 #pragma once
 #include <type_traits>
 
@@ -166,16 +167,14 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
     tc::mma_commit_warp(&sm.s_full[m]);
     issued = true;
   };
-  auto issue_pv = [&](int m, int st, bool first) {
+  auto issue_pv = [&](int m, int st, bool first, int half) {
     // V is [token][dim]: MN-major B; next 64 dims at +16 KB, next 8 tokens at +1 KB
     const uint64_t bv = dv + 2048u * st;
     const uint32_t o_tmem = tmem + kTmemO + m * kHeadDim;
 #pragma unroll
-    for (int kk = 0; kk < kTileN / 16; ++kk) {
-      // P_m of tokens 16kk..16kk+15: 8 columns of 16-bit pairs in the S_m buffer
-      // (tokens 0..63 at columns 0..31, tokens 64..127 at columns 64..95)
-      const uint32_t p_col = kk * 8 + (kk >= 4 ? 32 : 0);
-      tc::mma_ts_warp(o_tmem, tmem + m * kTileN + p_col, bv + 128u * kk, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+    for (int kk = 4 * half; kk < 4 * half + 4; ++kk) {
+      // P_m of tokens 16kk..16kk+15: columns 8kk..8kk+7 of the S_m buffer, 16-bit pairs
+      tc::mma_ts_warp(o_tmem, tmem + m * kTileN + kk * 8, bv + 128u * kk, idesc_pv, (!first || kk > 0) ? 1u : 0u);
     }
   };
   for (int32_t i = b0; i < b1; ++i) {
@@ -197,10 +196,12 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
       const bool more = j + 1 < ntiles;
       const int st_next = (g + 1) & 1;
       for (int m = 0; m < nm && ok; ++m) {
-        // Everything this step reads, polled at once: P_m of tile j; for M
-        // tile A also V of tile j and K of tile j+1; at an item's first tile
-        // the O_m columns.  Entries that do not apply repeat the first.
-        uint64_t* const pb = &sm.p_full[m];
+        // Everything this step reads, polled at once: P_m of tile j (tokens
+        // 0..63); for M tile A also V of tile j and K of tile j+1; at an
+        // item's first tile the O_m columns.  Entries that do not apply
+        // repeat the first.  The second half of P is awaited on its own, so
+        // the first four P V steps overlap the end of the softmax.
+        uint64_t* const pb = &sm.p_full[m][0];
         const uint32_t pp = tiles_m[m] & 1;
         const bool kv = m == 0, need_k = kv && more;
         ok = warp_wait_all(4, pb, pp, kv ? &sm.v_full[st] : pb, kv ? (g >> 1) & 1 : pp,
@@ -208,7 +209,11 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
                            need_k ? &sm.k_full[st_next] : pb, need_k ? ((g + 1) >> 1) & 1 : pp, &sm.abort);
         if (!ok) break;
         tc::fence_after_sync();
-        issue_pv(m, st, j == 0);
+        issue_pv(m, st, j == 0, 0);
+        ok = warp_wait(&sm.p_full[m][1], pp, &sm.abort);
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_pv(m, st, false, 1);
         ++tiles_m[m];
         if (!more) {
           tc::mma_commit_warp(&sm.o_ready[m]);
@@ -240,153 +245,132 @@ template <typename T>
 __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items,
                            int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal) {
   const int sw = (threadIdx.x >> 5) - kSoftmaxWarp0;  // 0..7
-  const int half = sw >> 2;                            // column half: 0 -> 0..63, 1 -> 64..127
+  const int mt = sw >> 2;                              // this warpgroup's M tile: 0 = A, 1 = B
   const int w = sw & 3;                                // == warp % 4: TMEM lanes 32w..32w+31
   const int lane = threadIdx.x & 31;
-  const int r = 32 * w + lane;                         // row within an M tile == TMEM lane
-  const int tid = half * kTileM + r;                   // 0..255
-  const uint32_t pair_bar = 3 + w;                     // warps 4+w and 8+w hold the same rows
+  const int r = 32 * w + lane;                         // row within the M tile == TMEM lane
+  const int tid = mt * kTileM + r;                     // 0..255
   const uint32_t tl = sm.tmem_base + (uint32_t(32 * w) << 16);
-  const int c0 = half * 64;
+  const uint32_t s_cols = tl + mt * kTileN, o_cols = tl + kTmemO + mt * kHeadDim;
   const int G = p.group;
   const float c = p.scale_log2;
-  uint32_t tiles[2] = {0, 0}, items[2] = {0, 0};  // per M tile: phases of s_full / o_ready
-  uint32_t ev = 0;                                 // max exchanges so far (slot parity)
+  uint32_t tiles = 0, items = 0;  // phases of s_full[mt] and o_ready[mt]
   for (int32_t i = b0; i < b1; ++i) {
     const Item item = load_item(p.iws, off_items, i);
     const Request rq = load_request(p.iws, off_req, item.b);
     const int nrows = item.row1 - item.row0;
     const int ntiles = item_kv_tiles(item);
-    const int nm = item_m_tiles(item);
-    // per M tile: this thread's row, its visible limit and its running state
-    int lim[2];
-    float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int prow = mt * kTileM + r;
-      lim[mt] = -1;
+    const int prow = mt * kTileM + r;  // packed row within the item
+    if (mt < item_m_tiles(item)) {
+      int lim = -1;  // last visible KV token of this row (-1: padding row)
       if (prow < nrows) {
         const int t = (item.row0 + prow) / G;
-        lim[mt] = min(causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1, item.kv1 - 1);
+        lim = min(causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1, item.kv1 - 1);
       }
-    }
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int kbase = item.kv0 + j * kTileN + c0;
-      for (int mt = 0; mt < nm; ++mt) {
-        ok = ok && warp_wait(&sm.s_full[mt], tiles[mt] & 1, &sm.abort);
-        ++tiles[mt];
-        uint32_t sv[2][32];
-        float mx = -INFINITY;
-        const bool masked = kbase + 63 > lim[mt];  // causal diagonal, chunk end or padding row
-        if (ok) {
-          tc::fence_after_sync();
-          tc::tmem_ld32(tl + mt * kTileN + c0, sv[0]);
-          tc::tmem_ld32(tl + mt * kTileN + c0 + 32, sv[1]);
-          tc::tmem_ld_wait();
-          if (masked) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (kbase + h * 32 + e > lim[mt]) sv[h][e] = 0xff800000u;  // -inf
-          }
-          // 64-value max in four independent chains of three-input maxima
-          auto val = [&](int e) { return __uint_as_float(sv[e >> 5][e & 31]); };
-          float mx4[4];
-#pragma unroll
-          for (int a = 0; a < 4; ++a) mx4[a] = max3(val(3 * a), val(3 * a + 1), val(3 * a + 2));
-#pragma unroll
-          for (int e = 12; e < 64; e += 2) mx4[(e >> 1) & 3] = max3(mx4[(e >> 1) & 3], val(e), val(e + 1));
-          mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-        }
-        // the two halves of the row agree on its max (slots alternate)
-        sm.xmax[ev & 1][half][r] = mx;
-        named_barrier_sync(pair_bar, 64);
-        mx = fmaxf(mx, sm.xmax[ev & 1][half ^ 1][r]) * c;
-        ++ev;
+      float mrun = -INFINITY, lrun = 0.f;
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j) {
+        ok = ok && warp_wait(&sm.s_full[mt], tiles & 1, &sm.abort);
+        ++tiles;
         if (!ok) continue;
-        const float m_old = mrun[mt];
+        tc::fence_after_sync();
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) tc::tmem_ld32(s_cols + 32 * h, sv[h]);
+        tc::tmem_ld_wait();
+        const int kbase = item.kv0 + j * kTileN;
+        if (kbase + kTileN - 1 > lim) {  // causal diagonal, chunk end or padding row
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (kbase + 32 * h + e > lim) sv[h][e] = 0xff800000u;  // -inf
+        }
+        // row max in four independent chains of three-input maxima
+        auto val = [&](int e) { return __uint_as_float(sv[e >> 5][e & 31]); };
+        float mx4[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) mx4[a] = max3(val(3 * a), val(3 * a + 1), val(3 * a + 2));
+#pragma unroll
+        for (int e = 12; e < kTileN; e += 2) mx4[(e >> 1) & 3] = max3(mx4[(e >> 1) & 3], val(e), val(e + 1));
+        const float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * c;
+        const float m_old = mrun;
         const float m_new = (mx > m_old + kLazyRescale) ? mx : m_old;
         const bool rescale = (m_new != m_old) && j > 0;
         if (__any_sync(0xffffffffu, rescale)) {
           // O holds P V of every earlier tile (covered by this S's commit)
           const float alpha = rescale ? ex2(m_old - m_new) : 1.f;
-          const uint32_t o_cols = kTmemO + mt * kHeadDim + c0;
 #pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 4; ++h) {
             uint32_t ov[32];
-            tc::tmem_ld32(tl + o_cols + h * 32, ov);
+            tc::tmem_ld32(o_cols + 32 * h, ov);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tc::tmem_st32(tl + o_cols + h * 32, ov);
+            tc::tmem_st32(o_cols + 32 * h, ov);
           }
           tc::tmem_st_wait();
-          if (rescale) lrun[mt] *= alpha;
+          if (rescale) lrun *= alpha;
         }
-        // P = 2^(s*c - m) as 16-bit pairs over the first 32 columns of this half
+        // P = 2^(s*c - m) as 16-bit pairs over the first 64 columns of the S
+        // buffer, published in two halves of 64 KV tokens each
         const float msub = (m_new == -INFINITY) ? 0.f : m_new;
         const float2 cc = make_float2(c, c), nms = make_float2(-msub, -msub);
         float2 sum4[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) sum4[a] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[16];
+        for (int half = 0; half < 2; ++half) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 x =
-                fma2(make_float2(__uint_as_float(sv[h][2 * e]), __uint_as_float(sv[h][2 * e + 1])), cc, nms);
-            const float2 pe = make_float2(ex2(x.x), ex2(x.y));
-            sum4[e & 3] = add2(sum4[e & 3], pe);
-            pk[e] = tc::pack2<T>(pe.x, pe.y);
+          for (int h = 2 * half; h < 2 * half + 2; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 x =
+                  fma2(make_float2(__uint_as_float(sv[h][2 * e]), __uint_as_float(sv[h][2 * e + 1])), cc, nms);
+              const float2 pe = make_float2(ex2(x.x), ex2(x.y));
+              sum4[e & 3] = add2(sum4[e & 3], pe);
+              pk[e] = tc::pack2<T>(pe.x, pe.y);
+            }
+            tc::tmem_st16(s_cols + 16 * h, pk);
           }
-          tc::tmem_st16(tl + mt * kTileN + c0 + h * 16, pk);
+          tc::tmem_st_wait();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.p_full[mt][half]);
         }
-        tc::tmem_st_wait();
-        const float2 s01 = add2(sum4[0], sum4[1]), s23 = add2(sum4[2], sum4[3]), s = add2(s01, s23);
-        lrun[mt] += s.x + s.y;
-        mrun[mt] = m_new;
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full[mt]);
+        const float2 s01 = add2(sum4[0], sum4[1]), s23 = add2(sum4[2], sum4[3]), s4 = add2(s01, s23);
+        lrun += s4.x + s4.y;
+        mrun = m_new;
       }
-    }
-    // Epilogue per M tile: the row sum is the two halves' shares; O / l in
-    // the storage type (or the fp32 partial state of a split unit), LSE in
-    // natural log.
-    for (int mt = 0; mt < nm; ++mt) {
+      // Epilogue: O / l in the storage type (or the fp32 partial state of a
+      // split unit), LSE in natural log.
       bool have_o = false;
       if (ntiles > 0) {
-        ok = ok && warp_wait(&sm.o_ready[mt], items[mt] & 1, &sm.abort);
-        ++items[mt];
+        ok = ok && warp_wait(&sm.o_ready[mt], items & 1, &sm.abort);
+        ++items;
         have_o = ok;
         if (ok) tc::fence_after_sync();
       }
-      sm.xsum[i & 1][mt][half][r] = lrun[mt];  // slots alternate by item
-      named_barrier_sync(pair_bar, 64);
-      const float l = lrun[mt] + sm.xsum[i & 1][mt][half ^ 1][r];
-      const int prow = mt * kTileM + r;
       const bool write = prow < nrows && !sm.abort;
       const int row = item.row0 + prow;
       const int t = row / G;
       const int head = item.hk * G + (row - t * G);
       const int64_t tok = int64_t(rq.qo_start) + t;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse_v = l > 0.f ? (mrun[mt] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
+      const float lse_v = lrun > 0.f ? (mrun + __log2f(lrun)) * 0.69314718055994531f : -INFINITY;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < 4; ++h) {
         uint32_t ov[32];
         if (have_o) {
-          tc::tmem_ld32(tl + kTmemO + mt * kHeadDim + c0 + h * 32, ov);
+          tc::tmem_ld32(o_cols + 32 * h, ov);
           tc::tmem_ld_wait();
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] = 0u;
         }
         if (write) {
-          const int col = c0 + h * 32;
+          const int col = 32 * h;
           if (item.part < 0) {
             uint4* dst =
                 reinterpret_cast<uint4*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + col);
@@ -415,7 +399,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.o_free[mt]);
       }
-      if (write && half == 0) {
+      if (write) {
         if (item.part < 0) {
           if (p.lse) p.lse[tok * p.num_qo_heads + head] = lse_v;
         } else {

@@ -13,6 +13,7 @@ enum : int32_t { kStatusTimeout = 1, kStatusBadPlan = 2 };
 // A bounded wait gives up after this many SM clocks (about half a second at
 // 2 GHz) and reports kStatusTimeout instead of hanging the GPU.
 constexpr long long kWaitBudgetClocks = 1000000000LL;
+constexpr int kPollsPerCheck = 8;  // polls of a warp-wide wait between checks of the abort flag and the budget
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,12 +83,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1 : 0, 0)) return true;
   const long long t0 = clock64();
   while (true) {
-    const int done = mbar_try_wait(bar, parity) ? 1 : 0;
+    // a few polls between the checks of the abort flag and the budget
+#pragma unroll 1
+    for (int k = 0; k < kPollsPerCheck; ++k)
+      if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1 : 0, 0)) return true;
     const int gave_up = *abort != 0 ? 2 : 0;
     const int late = clock64() - t0 > kWaitBudgetClocks ? 4 : 0;
-    const int st = __shfl_sync(0xffffffffu, done | gave_up | late, 0);
+    const int st = __shfl_sync(0xffffffffu, gave_up | late, 0);
     if (st & 2) return false;
-    if (st & 1) return true;
     if (st & 4) {
       *abort = kStatusTimeout;  // every lane stores the same value
       return false;
@@ -108,12 +111,13 @@ __device__ __forceinline__ bool warp_wait_all(int n, uint64_t* b0, uint32_t p0, 
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const long long t0 = clock64();
   while (true) {
-    const int done = __all_sync(0xffffffffu, mbar_try_wait(bar, parity)) ? 1 : 0;
+#pragma unroll 1
+    for (int k = 0; k < kPollsPerCheck; ++k)
+      if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     const int gave_up = *abort != 0 ? 2 : 0;
     const int late = clock64() - t0 > kWaitBudgetClocks ? 4 : 0;
-    const int st = __shfl_sync(0xffffffffu, done | gave_up | late, 0);
+    const int st = __shfl_sync(0xffffffffu, gave_up | late, 0);
     if (st & 2) return false;
-    if (st & 1) return true;
     if (st & 4) {
       *abort = kStatusTimeout;
       return false;
@@ -155,6 +159,12 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// The same barrier reached from different places in the code (barrier.sync
+// without .aligned): the roles of a CTA meet here from their own branches.
+__device__ __forceinline__ void named_barrier_sync_unaligned(uint32_t id, uint32_t threads) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Packed fp32 fused multiply-add of two lanes at once: a * b + c per lane,

@@ -133,6 +133,22 @@ __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
       : "memory");
 }
 
+// Per-warpgroup register budget (every thread of the warpgroup executes it).
+// An increase waits until other warpgroups of the CTA have released enough
+// registers, so the budgets of all warpgroups must add up to no more than
+// the launch's register count times the CTA's threads.
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+template <uint32_t kRegs>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg range");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // Arrive once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
