@@ -258,7 +258,9 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
     const int64_t qs[2] = {q_stride_head, q_stride_tok};
     const uint32_t qb[3] = {64u, uint32_t(G), uint32_t(kTileM / G)};
     const uint32_t kb[4] = {64u, 1u, uint32_t(P), 1u};
+    const int64_t os[2] = {o_stride_head, o_stride_tok};
     if (!make_map(&p.tm_q, tt, q, 3, qd, qs, qb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&p.tm_o, tt, o, 3, qd, os, qb, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.tm_k, tt, k_cache, 4, kd, ks, kb, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.tm_v, tt, v_cache, 4, kd, vs, kb, CU_TENSOR_MAP_SWIZZLE_128B))
       return FI_ERR_UNSUPPORTED;

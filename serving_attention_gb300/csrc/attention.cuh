@@ -41,6 +41,7 @@ constexpr int kSoftmaxThreads = 256;
 // build whose register count is at least kRegsLaunch (an increase that
 // cannot be met would wait forever).
 constexpr int kPhaseBarrier = 3;       // named barrier ending the tensor-core phase (1: decode, 2: merge)
+constexpr int kEpilogueBarrier0 = 4;   // named barriers 4, 5: one per softmax warpgroup (output staging)
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsLoader = 104;
 constexpr int kRegsSoftmax = 192;
@@ -54,6 +55,7 @@ struct RunParams {
   CUtensorMap tm_v;
   CUtensorMap tm_kd;  // [pages, P, Hkv, d] boxes of (128 dims, 1 head, min(P, 64) slots, 1 page), no swizzle
   CUtensorMap tm_vd;
+  CUtensorMap tm_o;   // O as [q tokens, Hq, d] with the boxes of tm_q: stores of whole 128-row output tiles
   const uint16_t* q;
   int64_t q_stride_tok, q_stride_head;
   const uint16_t* k;
@@ -87,6 +89,7 @@ struct PrefillBufs {
   uint16_t q[2][2][kTileM][64];     // [M tile][d half][row][dim]
   uint16_t k[2][2][kTileN][64];     // [stage][d half][token][dim]
   uint16_t v[2][2][kTileN][64];
+  uint16_t ostage[2][kTileM][64];   // [M tile][row][dim]: one d half of an output tile on its way to a TMA store
 };
 
 struct alignas(1024) RunSmem {
@@ -107,6 +110,7 @@ struct alignas(1024) RunSmem {
 };
 
 constexpr size_t kSmemBytes = sizeof(RunSmem);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of the run kernel exceeds one CTA's limit");
 
 struct Item {
   int32_t b, hk, row0, row1, kv0, kv1, part, merge;

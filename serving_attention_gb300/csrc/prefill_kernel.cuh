@@ -35,8 +35,9 @@
 //    of 64 KV tokens with a barrier each, so P V starts on the first half
 //    while the second is computed.  The two warpgroups run on different M
 //    tiles, so on every SM sub-partition one warp computes while the other
-//    waits.  At the end: read O, divide by the row sum, store O and LSE (or
-//    an fp32 partial state).
+//    waits.  At the end: read O, divide by the row sum, store O (a whole
+//    output tile through shared memory and TMA stores) and LSE, or an fp32
+//    partial state.
 #pragma once
 #include <type_traits>
 
@@ -286,14 +287,14 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
             for (int e = 0; e < 32; ++e)
               if (kbase + 32 * h + e > lim) sv[h][e] = 0xff800000u;  // -inf
         }
-        // row max in four independent chains of three-input maxima
-        auto val = [&](int e) { return __uint_as_float(sv[e >> 5][e & 31]); };
-        float mx4[4];
+        // row max in eight independent chains
+        float mx8[8];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) mx4[a] = max3(val(3 * a), val(3 * a + 1), val(3 * a + 2));
+        for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(sv[0][a]);
 #pragma unroll
-        for (int e = 12; e < kTileN; e += 2) mx4[(e >> 1) & 3] = max3(mx4[(e >> 1) & 3], val(e), val(e + 1));
-        const float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * c;
+        for (int e = 8; e < kTileN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e >> 5][e & 31]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
         const float m_old = mrun;
         const float m_new = (mx > m_old + kLazyRescale) ? mx : m_old;
         const bool rescale = (m_new != m_old) && j > 0;
@@ -344,13 +345,28 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         mrun = m_new;
       }
       // Epilogue: O / l in the storage type (or the fp32 partial state of a
-      // split unit), LSE in natural log.
+      // split unit), LSE in natural log.  The O row leaves tensor memory in
+      // one load, and the O columns go back to the MMA warp right away.
       bool have_o = false;
       if (ntiles > 0) {
         ok = ok && warp_wait(&sm.o_ready[mt], items & 1, &sm.abort);
         ++items;
         have_o = ok;
-        if (ok) tc::fence_after_sync();
+      }
+      uint32_t ov[4][32];
+      if (have_o) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int h = 0; h < 4; ++h) tc::tmem_ld32(o_cols + 32 * h, ov[h]);
+        tc::tmem_ld_wait();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.o_free[mt]);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[h][e] = 0u;
       }
       const bool write = prow < nrows && !sm.abort;
       const int row = item.row0 + prow;
@@ -359,45 +375,53 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
       const int64_t tok = int64_t(rq.qo_start) + t;
       const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
       const float lse_v = lrun > 0.f ? (mrun + __log2f(lrun)) * 0.69314718055994531f : -INFINITY;
-#pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        uint32_t ov[32];
-        if (have_o) {
-          tc::tmem_ld32(o_cols + 32 * h, ov);
-          tc::tmem_ld_wait();
-        } else {
+      auto pack8 = [&](int h, int e0) {  // 8 normalised values as 16-bit pairs
+        uint4 u;
+        u.x = tc::pack2<T>(__uint_as_float(ov[h][e0]) * inv, __uint_as_float(ov[h][e0 + 1]) * inv);
+        u.y = tc::pack2<T>(__uint_as_float(ov[h][e0 + 2]) * inv, __uint_as_float(ov[h][e0 + 3]) * inv);
+        u.z = tc::pack2<T>(__uint_as_float(ov[h][e0 + 4]) * inv, __uint_as_float(ov[h][e0 + 5]) * inv);
+        u.w = tc::pack2<T>(__uint_as_float(ov[h][e0 + 6]) * inv, __uint_as_float(ov[h][e0 + 7]) * inv);
+        return u;
+      };
+      if (item.part < 0 && (mt + 1) * kTileM <= nrows) {
+        // A whole 128-row tile of an unsplit item leaves through shared
+        // memory: per d half, each thread writes its row as 128 bytes in the
+        // 128-byte swizzled layout of the Q tile, then one thread of the
+        // warpgroup stores the box (64 dims, G heads, 128/G tokens) with TMA.
+        const uint32_t wg_bar = kEpilogueBarrier0 + mt;
+        uint16_t* stage = &sm.pf.ostage[mt][0][0];
+        uint4* my_row = reinterpret_cast<uint4*>(stage + r * 64);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int cch = 0; cch < 8; ++cch) my_row[cch ^ (r & 7)] = pack8(2 * half + (cch >> 2), 8 * (cch & 3));
+          fence_proxy_async_smem();
+          named_barrier_sync(wg_bar, 128);
+          if ((threadIdx.x & 127) == 0 && !sm.abort) {
+            tc::tma_store_3d(&p.tm_o, stage, 64 * half, item.hk * G, rq.qo_start + (item.row0 + mt * kTileM) / G);
+            tc::bulk_commit();
+            tc::bulk_wait_read_all();  // the staging rows may be written again
+          }
+          named_barrier_sync(wg_bar, 128);
         }
-        if (write) {
+      } else if (write) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
           const int col = 32 * h;
           if (item.part < 0) {
             uint4* dst =
                 reinterpret_cast<uint4*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + col);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float* f = reinterpret_cast<const float*>(&ov[8 * e]);
-              uint4 u;
-              u.x = tc::pack2<T>(f[0] * inv, f[1] * inv);
-              u.y = tc::pack2<T>(f[2] * inv, f[3] * inv);
-              u.z = tc::pack2<T>(f[4] * inv, f[5] * inv);
-              u.w = tc::pack2<T>(f[6] * inv, f[7] * inv);
-              dst[e] = u;
-            }
+            for (int e = 0; e < 4; ++e) dst[e] = pack8(h, 8 * e);
           } else {
             float4* dst = reinterpret_cast<float4*>(p.fws + p.partial_o_offset +
                                                     (int64_t(item.part) + prow) * kHeadDim + col);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
-                                   __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
+              dst[e] = make_float4(__uint_as_float(ov[h][4 * e]) * inv, __uint_as_float(ov[h][4 * e + 1]) * inv,
+                                   __uint_as_float(ov[h][4 * e + 2]) * inv, __uint_as_float(ov[h][4 * e + 3]) * inv);
           }
         }
-      }
-      if (have_o) {
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.o_free[mt]);
       }
       if (write) {
         if (item.part < 0) {
@@ -410,6 +434,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
     if (item.merge >= 0)
       merge_split_unit<T>(p, item, rq, off_merge, off_cnt, tid, kSoftmaxThreads, 2, &sm.merge_last_pf, sm.abort);
   }
+  if ((threadIdx.x & 127) == 0) tc::bulk_wait_all();  // output tiles written before the CTA moves on
 }
 
 }  // namespace fi

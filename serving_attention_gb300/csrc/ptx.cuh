@@ -43,6 +43,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware until the phase
+// completes or about kSuspendHintNs nanoseconds pass, instead of spinning:
+// a waiting warp then takes no issue slots from the warps that compute.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking: has the phase with `parity` of `bar` completed?
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -86,7 +102,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     // a few polls between the checks of the abort flag and the budget
 #pragma unroll 1
     for (int k = 0; k < kPollsPerCheck; ++k)
-      if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1 : 0, 0)) return true;
+      if (__shfl_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity) ? 1 : 0, 0)) return true;
     const int gave_up = *abort != 0 ? 2 : 0;
     const int late = clock64() - t0 > kWaitBudgetClocks ? 4 : 0;
     const int st = __shfl_sync(0xffffffffu, gave_up | late, 0);
@@ -113,7 +129,7 @@ __device__ __forceinline__ bool warp_wait_all(int n, uint64_t* b0, uint32_t p0, 
   while (true) {
 #pragma unroll 1
     for (int k = 0; k < kPollsPerCheck; ++k)
-      if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+      if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity))) return true;
     const int gave_up = *abort != 0 ? 2 : 0;
     const int late = clock64() - t0 > kWaitBudgetClocks ? 4 : 0;
     const int st = __shfl_sync(0xffffffffu, gave_up | late, 0);
