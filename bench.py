@@ -346,7 +346,61 @@ def bench_secondary(dev, reps=5):
         del b, o, lse, g
         torch.cuda.empty_cache()
     out["shared_prefix"] = bench_shared_prefix(dev, flush, reps)
+    out["kv_strides"] = bench_kv_strides(dev, flush, reps)
     return out
+
+
+def bench_kv_strides(dev, flush, reps=5):
+    """Equal against independent K/V strides on the same values: V either
+    shares K's layout or sits in a pool with one padding head (its slot and
+    page strides then differ from K's).  The BatchAttention PR page reports
+    the equal-stride module 1.0456x faster on B200; here both layouts run
+    the same kernel, the copy engine computing K and V addresses from their
+    own tensor maps."""
+    import torch
+
+    import serving_attention_gb300 as fi
+    import workloads
+
+    cfg = fi.default_plan_config(dev.index)
+    res = {}
+    for name, maker in (("llama8b_decode", workloads.llama8b_decode), ("continuous_batch", workloads.continuous_batch)):
+        b = maker(device=dev)
+        ws = fi.Workspace(cfg, device=dev)
+        info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                       128, b.page_size, b.causal, b.num_pages)
+        kvi = torch.as_tensor(b.kv_indices, device=dev)
+        o = torch.empty_like(b.q)
+        lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
+        shape = list(b.v.shape)
+        v_equal = b.v.contiguous()
+        v_pool = torch.empty(shape[:2] + [shape[2] + 1, shape[3]], dtype=b.v.dtype, device=dev)
+        v_pool[:, :, :shape[2]].copy_(b.v)
+        v_unequal = v_pool[:, :, :shape[2]]
+        times = {}
+        for tag, v in (("equal", v_equal), ("unequal", v_unequal)):
+            fi.run(ws, info, b.q, b.k, v, kvi, o, lse, b.sm_scale)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fi.run(ws, info, b.q, b.k, v, kvi, o, lse, b.sm_scale)
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                c.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(c))
+            times[tag] = float(np.median(ts))
+            del g
+        assert fi.device_status(ws) == 0
+        res[name] = {"equal_ms": times["equal"], "unequal_ms": times["unequal"],
+                     "equal_speedup": times["unequal"] / times["equal"]}
+        del b, o, lse, v_equal, v_pool, v_unequal
+        torch.cuda.empty_cache()
+    res["workload"] = "llama8b_decode and continuous_batch with V in K's layout or in a pool with a padding head"
+    return res
 
 
 def bench_shared_prefix(dev, flush, reps=5):
@@ -601,6 +655,7 @@ def main():
                        "tflops_exact_over_kernel": m["tflops_exact"]}
         sp = sec["shared_prefix"]
         line["shared_prefix"] = dict(sp, frac_of_hbm=sp["composable_gbs"] / hbm)
+        line["kv_strides"] = sec["kv_strides"]
     print(json.dumps(line))
 
 
