@@ -60,7 +60,24 @@ typedef struct {
     int32_t decode_cost_weight;  /* cost of one KV token in a 16-row tile (default 4) */
     int32_t prefill_cost_weight; /* cost of one KV token in a 256-row tile (default 6) */
     int32_t split_factor;        /* target chunks per CTA per tile class (default 4) */
-    int32_t reserved[3];
+    /* Mask and logit variant, constant for a model (FlashInfer 0.6 wiki page,
+     * "Blackwell (SM100/SM103) 전용 경로 / CuTe-DSL GQA Decode 커널": sliding
+     * window and attention sink; FlashInfer paper summary, "2. 유연한 어텐션
+     * 변형 지원": logits transforms).  Query token t of a request with Lq
+     * queries and Lkv keys sits at q_pos = Lkv - Lq + t.
+     *   window_left >= 0: key j is visible only if j >= q_pos - window_left
+     *     (-1, the default: no window); the plan skips KV chunks that no row
+     *     of a tile can see;
+     *   sink_tokens: keys j < sink_tokens stay visible whatever the window
+     *     says (the causal bound still applies; default 0);
+     *   logits_soft_cap > 0: the softmax logit is
+     *     cap * tanh(sm_scale * q.k / cap) (0, the default: sm_scale * q.k);
+     *     run then launches the capped kernel (fi_plan_info.variant bit 0).
+     * Negative sink_tokens, window_left < -1 or a negative or non-finite cap
+     * are FI_ERR_INVALID_ARG. */
+    int32_t window_left;
+    int32_t sink_tokens;
+    float logits_soft_cap;
 } fi_plan_config;
 
 /* Plain data returned by fi_plan; passed to run by value semantics. */
@@ -74,7 +91,7 @@ typedef struct {
     int32_t chunk_decode;        /* KV tokens per chunk chosen for 16-row tiles */
     int32_t chunk_prefill;       /* KV tokens per chunk chosen for 256-row tiles */
     int32_t num_decode_items, num_prefill_items;
-    int32_t reserved;
+    int32_t variant;             /* bit 0: logits soft-cap on (copied from the config) */
     int64_t int_ws_bytes_used;   /* bytes of the int workspace written (and copied) by the plan */
     int64_t max_partial_rows;    /* capacity of the float workspace, from the config */
 } fi_plan_info;

@@ -63,6 +63,9 @@ class _Problem(ctypes.Structure):
         ("v_stride_page", ctypes.c_int64),
         ("v_stride_slot", ctypes.c_int64),
         ("v_stride_head", ctypes.c_int64),
+        ("window_left", ctypes.c_int32),
+        ("sink_tokens", ctypes.c_int32),
+        ("logits_soft_cap", ctypes.c_double),
     ]
 
 
@@ -109,7 +112,7 @@ class Problem:
     for fp16/bf16, float32 for fp32) with arbitrary element strides."""
 
     def __init__(self, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads,
-                 page_size, causal, sm_scale, dtype, q, k, v):
+                 page_size, causal, sm_scale, dtype, q, k, v, window_left=-1, sink_tokens=0, logits_soft_cap=0.0):
         self.qo_indptr = np.ascontiguousarray(qo_indptr, dtype=np.int32)
         self.kv_indptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)
         self.kv_indices = np.ascontiguousarray(kv_indices, dtype=np.int32)
@@ -131,7 +134,7 @@ class Problem:
                            _ptr(self.kv_indices) if self.kv_indices.size else 0, _ptr(self.last_page_len),
                            num_qo_heads, num_kv_heads, q.shape[2], page_size, int(causal), float(sm_scale),
                            dtype, _ptr(q), qs[0], qs[1], _ptr(k), ks[0], ks[1], ks[2], _ptr(v), vs[0], vs[1],
-                           vs[2])
+                           vs[2], int(window_left), int(sink_tokens), float(logits_soft_cap))
 
     @property
     def num_rows(self) -> int:

@@ -26,9 +26,23 @@
  *   token t of a request with Lq queries and Lkv keys sees key j iff
  *   j <= Lkv - Lq + t.
  *
- * LSE is the natural log of the sum of exp of the *scaled* scores.  A row
- * that sees no key gets O = 0 and LSE = -inf (the pages are silent; this is
- * the identity of the merge operator below).
+ * Mask and logit variants (FlashInfer 0.6 wiki page, section "Blackwell
+ * (SM100/SM103) 전용 경로 / CuTe-DSL GQA Decode 커널": sliding-window and
+ * attention-sink masking; FlashInfer paper summary, section "2. 유연한 어텐션
+ * 변형 지원": user-defined logits transforms and masks).  The pages name the
+ * variants without formulas; the plain readings used here:
+ *   sliding window (window_left W >= 0, off when < 0): query token t, at
+ *     position q_pos = Lkv - Lq + t (the bottom-right alignment of the causal
+ *     mask), also needs j >= q_pos - W;
+ *   attention sink (sink_tokens S >= 0): keys j < S stay visible whatever the
+ *     window says (the causal bound still applies);
+ *   logits soft-cap (cap > 0, off when 0): the logit fed to the softmax is
+ *     cap * tanh(scale * q.k / cap) instead of scale * q.k.
+ *
+ * LSE is the natural log of the sum of exp of the logits (the *scaled*, and
+ * when capped the capped, scores).  A row that sees no key gets O = 0 and
+ * LSE = -inf (the pages are silent; this is the identity of the merge
+ * operator below).
  *
  * Merge of two partial states (the "process the dense and the sparse part
  * separately, then combine" of the paper summary's section 1, and the
@@ -93,6 +107,9 @@ typedef struct {
     int64_t k_stride_page, k_stride_slot, k_stride_head;
     const void* v;
     int64_t v_stride_page, v_stride_slot, v_stride_head;
+    int32_t window_left;          /* < 0: no sliding window */
+    int32_t sink_tokens;          /* keys j < sink_tokens ignore the window */
+    double logits_soft_cap;       /* 0: plain scaled logits */
 } orc_problem;
 
 static int32_t kv_len_of(const orc_problem* p, int b)
@@ -112,35 +129,45 @@ static void attend_one(const orc_problem* p, int b, int t, int h, double* scores
     const int32_t lkv = kv_len_of(p, b);
     const int64_t row = (int64_t)p->qo_indptr[b] + t;
 
-    /* visible keys are j = 0 .. nvis-1 */
+    /* keys j = 0 .. nvis-1 pass the length and causal bounds; of those, a
+     * sliding window keeps j >= q_pos - W, and the sink keeps j < S anyway */
+    const int64_t q_pos = (int64_t)lkv - lq + t; /* bottom-right aligned */
     int64_t nvis = lkv;
-    if (p->causal) {
-        int64_t last = (int64_t)lkv - lq + t; /* bottom-right aligned */
-        if (last + 1 < nvis) nvis = last + 1;
-    }
+    if (p->causal && q_pos + 1 < nvis) nvis = q_pos + 1;
     if (nvis < 0) nvis = 0;
+    const int64_t win_lo = p->window_left >= 0 ? q_pos - p->window_left : INT64_MIN;
+    int64_t nseen = 0;
     for (int c = 0; c < d; ++c) o[c] = 0.0;
-    if (nvis == 0) {
-        *lse = -INFINITY;
-        return;
-    }
 
     const int64_t qbase = row * p->q_stride_tok + (int64_t)h * p->q_stride_head;
     double m = -INFINITY;
     for (int64_t j = 0; j < nvis; ++j) {
+        if (j < win_lo && j >= p->sink_tokens) {
+            scores[j] = -INFINITY; /* outside the window and not a sink key */
+            continue;
+        }
+        ++nseen;
         int64_t page = p->kv_indices[p->kv_indptr[b] + j / p->page_size];
         int64_t slot = j % p->page_size;
         int64_t kbase = page * p->k_stride_page + slot * p->k_stride_slot + (int64_t)hk * p->k_stride_head;
         double dot = 0.0;
         for (int c = 0; c < d; ++c)
             dot += load_elem(p->q, p->dtype, qbase + c) * load_elem(p->k, p->dtype, kbase + c);
-        scores[j] = p->sm_scale * dot;
+        double logit = p->sm_scale * dot;
+        if (p->logits_soft_cap > 0.0) logit = p->logits_soft_cap * tanh(logit / p->logits_soft_cap);
+        scores[j] = logit;
         if (scores[j] > m) m = scores[j];
     }
+    if (nseen == 0) {
+        *lse = -INFINITY;
+        return;
+    }
     double sum = 0.0;
-    for (int64_t j = 0; j < nvis; ++j) sum += exp(scores[j] - m);
+    for (int64_t j = 0; j < nvis; ++j)
+        if (scores[j] != -INFINITY) sum += exp(scores[j] - m);
     const double l = m + log(sum);
     for (int64_t j = 0; j < nvis; ++j) {
+        if (scores[j] == -INFINITY) continue;
         int64_t page = p->kv_indices[p->kv_indptr[b] + j / p->page_size];
         int64_t slot = j % p->page_size;
         int64_t vbase = page * p->v_stride_page + slot * p->v_stride_slot + (int64_t)hk * p->v_stride_head;

@@ -16,23 +16,31 @@ Rule:
  1. Request b has Lq query tokens, Lkv keys, R = Lq * G packed rows (packed row
     r = t * G + g is query token t, head hk * G + g).  Tile height T = 16 if
     R <= 16 (decode class) else 256 (prefill class).
- 2. Units (b, hk, qt) for qt < ceil(R / T); rows [qt*T, min(R, (qt+1)*T)).
-    Visible KV length kv_eff = Lkv, or with the bottom-right causal mask
-    min(Lkv, Lkv - Lq + t_last + 1) with t_last = (row_end - 1) // G, floored
-    at 0.
+ 2. Units (b, hk, qt) for qt < ceil(R / T); rows [qt*T, min(R, (qt+1)*T)),
+    tokens t_first = row0 // G .. t_last = (row_end - 1) // G, at KV positions
+    q_pos(t) = Lkv - Lq + t (bottom-right alignment).  Visible end hi = Lkv,
+    or with the causal mask min(Lkv, q_pos(t_last) + 1), floored at 0.
+    Visible KV ranges: [0, hi) without a sliding window.  With window W >= 0
+    and S sink tokens: lo = max(0, q_pos(t_first) - W) rounded down to the
+    class granule (below); if lo <= min(S, hi) one range [0, hi), else the
+    sink range [0, min(S, hi)) (when not empty) followed by [lo, hi).
+    kv_eff = the summed length of the ranges.
  3. Per class, total = sum of kv_eff; chunk = max(min_chunk,
     ceil(total / (num_ctas * split_factor))) rounded up to a multiple of the
     class granule max(page_size, 64) (decode) or max(page_size, 128) (prefill).
- 4. A unit with kv_eff = 0 gives one empty item.  Otherwise it splits into
-    n = ceil(kv_eff / chunk) items [i*chunk, min(kv_eff, (i+1)*chunk)).  When
-    n > 1 the unit becomes a merge unit (numbered in unit order) and its
-    items get consecutive fp32 partial-state rows, n * rows in all.
+ 4. A unit with kv_eff = 0 gives one empty item.  Otherwise each range
+    [s, e) splits into ceil((e - s) / chunk) items [s + i*chunk,
+    min(e, s + (i+1)*chunk)), ranges in order, chunk numbers running across
+    them.  When a unit has n > 1 items it becomes a merge unit (numbered in
+    unit order) and its items get consecutive fp32 partial-state rows,
+    n * rows in all.
  5. cost = kv length of the item * class weight.  Items are sorted by
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
     load, ties to the smaller CTA index (longest processing time first).
- 6. Output: header, per-CTA CSR offsets, items in CTA order (within a CTA the
-    256-row items first, then the 16-row items, each in the order dealt),
-    merge units, zeroed merge counters, request table.
+ 6. Output: header (with the variant: window, sink, soft-cap bits), per-CTA
+    CSR offsets, items in CTA order (within a CTA the 256-row items first,
+    then the 16-row items, each in the order dealt), merge units, zeroed merge
+    counters, request table.
 """
 from __future__ import annotations
 
@@ -42,7 +50,7 @@ import numpy as np
 
 MAGIC = 0x46495031
 TILE_DECODE, TILE_PREFILL = 16, 256
-HEADER_INTS = 16
+HEADER_INTS = 20
 ITEM_INTS = 8
 MERGE_INTS = 8
 REQ_INTS = 4
@@ -83,6 +91,10 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
         return UNSUPPORTED, None, None
     if causal not in (0, 1) or cfg["num_ctas"] < 1 or cfg["split_factor"] < 1:
         return INVALID_ARG, None, None
+    window, sink = cfg.get("window_left", -1), cfg.get("sink_tokens", 0)
+    cap = float(np.float32(cfg.get("logits_soft_cap", 0.0)))
+    if window < -1 or sink < 0 or not (cap >= 0.0) or cap == float("inf"):
+        return INVALID_ARG, None, None
     if batch > cfg["max_batch"]:
         return CAPACITY, None, None
     if qo[0] != 0 or kvp[0] != 0:
@@ -102,7 +114,21 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     npg = [kvp[b + 1] - kvp[b] for b in range(batch)]
     lkv = [0 if npg[b] == 0 else (npg[b] - 1) * page_size + lpl[b] for b in range(batch)]
 
-    # units in (b, hk, qt) order: (b, hk, qt, T, row0, row1, kv_eff)
+    granule = {TILE_DECODE: max(page_size, 64), TILE_PREFILL: max(page_size, 128)}
+
+    def ranges_of(b, T, r0, r1):
+        q_first = lkv[b] - lq[b] + r0 // group
+        q_last = lkv[b] - lq[b] + (r1 - 1) // group
+        hi = max(0, min(lkv[b], q_last + 1) if causal else lkv[b])
+        if window < 0:
+            return [(0, hi)]
+        lo = max(0, q_first - window) // granule[T] * granule[T]
+        sink_end = min(sink, hi)
+        if lo <= sink_end:
+            return [(0, hi)]
+        return ([(0, sink_end)] if sink_end > 0 else []) + [(lo, hi)]
+
+    # units in (b, hk, qt) order: (b, hk, qt, T, row0, row1, ranges)
     units = []
     total = {TILE_DECODE: 0, TILE_PREFILL: 0}
     for b in range(batch):
@@ -113,13 +139,9 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
         for hk in range(num_kv_heads):
             for qt in range(_ceil_div(R, T)):
                 r0, r1 = qt * T, min(R, (qt + 1) * T)
-                if causal:
-                    t_last = (r1 - 1) // group
-                    kv_eff = max(0, min(lkv[b], lkv[b] - lq[b] + t_last + 1))
-                else:
-                    kv_eff = lkv[b]
-                units.append((b, hk, qt, T, r0, r1, kv_eff))
-                total[T] += kv_eff
+                rng = ranges_of(b, T, r0, r1)
+                units.append((b, hk, qt, T, r0, r1, rng))
+                total[T] += sum(e - s for s, e in rng)
 
     chunk = {}
     for T, min_chunk, gran in ((TILE_DECODE, cfg["decode_min_chunk"], max(page_size, 64)),
@@ -131,22 +153,26 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     items = []   # (sort key, fields)
     merges = []
     part_rows = 0
-    for (b, hk, qt, T, r0, r1, kv_eff) in units:
-        if kv_eff == 0:
+    for (b, hk, qt, T, r0, r1, rng) in units:
+        pieces = []
+        for s_, e_ in rng:
+            for i in range(_ceil_div(e_ - s_, chunk[T])):
+                pieces.append((s_ + i * chunk[T], min(e_, s_ + (i + 1) * chunk[T])))
+        if not pieces:
             items.append(((0, -T, b, hk, qt, 0), (b, hk, r0, r1, 0, 0, -1, -1)))
             continue
-        n = _ceil_div(kv_eff, chunk[T])
+        n = len(pieces)
         if n == 1:
-            cost = kv_eff * weight[T]
-            items.append(((-cost, -T, b, hk, qt, 0), (b, hk, r0, r1, 0, kv_eff, -1, -1)))
+            k0, k1 = pieces[0]
+            cost = (k1 - k0) * weight[T]
+            items.append(((-cost, -T, b, hk, qt, 0), (b, hk, r0, r1, k0, k1, -1, -1)))
             continue
         m = len(merges)
         base = part_rows
         nrows = r1 - r0
         merges.append((b, hk, r0, r1, n, base, 0, 0))
         part_rows += n * nrows
-        for i in range(n):
-            k0, k1 = i * chunk[T], min(kv_eff, (i + 1) * chunk[T])
+        for i, (k0, k1) in enumerate(pieces):
             cost = (k1 - k0) * weight[T]
             items.append(((-cost, -T, b, hk, qt, i), (b, hk, r0, r1, k0, k1, base + i * nrows, m)))
 
@@ -173,8 +199,10 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
         return CAPACITY, None, None
 
     ws = np.zeros(total_ints, dtype=np.int32)
+    cap_bits = int(np.array([cap], dtype=np.float32).view(np.int32)[0])
     ws[:HEADER_INTS] = [MAGIC, n_items, n_merge, C, batch, causal, off_cta, off_items, off_merge,
-                        off_cnt, off_req, 0, num_qo_heads, num_kv_heads, page_size, total_ints]
+                        off_cnt, off_req, 0, num_qo_heads, num_kv_heads, page_size, total_ints,
+                        window, sink, cap_bits, 0]
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos
@@ -194,5 +222,6 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
                 num_partial_rows=part_rows, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
                 head_dim=head_dim, page_size=page_size, causal=causal, chunk_decode=chunk[16],
                 chunk_prefill=chunk[TILE_PREFILL], num_decode_items=n_dec, num_prefill_items=n_items - n_dec,
-                int_ws_bytes_used=4 * total_ints, max_partial_rows=cfg["max_partial_rows"])
+                int_ws_bytes_used=4 * total_ints, max_partial_rows=cfg["max_partial_rows"],
+                variant=1 if cap > 0 else 0)
     return OK, ws, info

@@ -37,10 +37,11 @@ class PlanConfig(ctypes.Structure):
                 ("max_merge_units", ctypes.c_int32), ("max_partial_rows", ctypes.c_int64),
                 ("decode_min_chunk", ctypes.c_int32), ("prefill_min_chunk", ctypes.c_int32),
                 ("decode_cost_weight", ctypes.c_int32), ("prefill_cost_weight", ctypes.c_int32),
-                ("split_factor", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("split_factor", ctypes.c_int32), ("window_left", ctypes.c_int32), ("sink_tokens", ctypes.c_int32),
+                ("logits_soft_cap", ctypes.c_float)]
 
     def as_dict(self) -> dict:
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 class PlanInfo(ctypes.Structure):
@@ -49,11 +50,11 @@ class PlanInfo(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("causal", ctypes.c_int32), ("chunk_decode", ctypes.c_int32), ("chunk_prefill", ctypes.c_int32),
                 ("num_decode_items", ctypes.c_int32), ("num_prefill_items", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("int_ws_bytes_used", ctypes.c_int64),
+                ("variant", ctypes.c_int32), ("int_ws_bytes_used", ctypes.c_int64),
                 ("max_partial_rows", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 EXPORTS = ["fi_default_plan_config", "fi_int_workspace_bytes", "fi_float_workspace_bytes", "fi_plan",
@@ -121,7 +122,7 @@ def make_plan_config(num_ctas: int, **overrides) -> PlanConfig:
     """A config without asking the device (host-side planning and tests)."""
     cfg = PlanConfig(num_ctas=num_ctas, max_batch=8192, max_items=1 << 17, max_merge_units=1 << 15,
                      max_partial_rows=1 << 19, decode_min_chunk=256, prefill_min_chunk=1024, decode_cost_weight=4,
-                     prefill_cost_weight=6, split_factor=4)
+                     prefill_cost_weight=6, split_factor=4, window_left=-1, sink_tokens=0, logits_soft_cap=0.0)
     for k, v in overrides.items():
         setattr(cfg, k, v)
     return cfg

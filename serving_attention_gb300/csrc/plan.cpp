@@ -13,7 +13,11 @@
 // Rule (this library's reading of that goal; the pages give no cost model):
 //  * request b -> R = qo_len * G packed rows (row t*G+g = token t, head hk*G+g);
 //    tile T = 16 when R <= 16, else 256;
-//  * unit (b, hk, q-tile) with its visible KV length (bottom-right causal);
+//  * unit (b, hk, q-tile) with its visible KV ranges: [0, hi) with hi the
+//    bottom-right causal end; with a sliding window W and S sink tokens, the
+//    window range starts at the first token's q_pos - W rounded down to the
+//    class granule, and the sink range [0, min(S, hi)) comes first unless
+//    the two touch (then one range [0, hi));
 //  * per tile class, a KV chunk length = max(min_chunk, total / (CTAs * split))
 //    rounded up to the class granule; units longer than a chunk are split
 //    into chunks whose fp32 partial states are merged by the kernel;
@@ -21,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <functional>
@@ -38,7 +43,9 @@ inline int64_t round4(int64_t n) { return (n + 3) & ~int64_t(3); }
 
 struct Unit {
   int32_t b, hk, qt, tile, row0, row1;
-  int64_t kv_eff;
+  int64_t r_begin[2], r_end[2];  // visible KV ranges, in KV order
+  int32_t n_ranges;
+  int64_t kv_eff;                // summed length of the ranges
 };
 
 struct Chunk {
@@ -87,6 +94,9 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   if (group > 16) return FI_ERR_UNSUPPORTED;
   if ((causal != 0 && causal != 1) || cfg->num_ctas < 1 || cfg->split_factor < 1) return FI_ERR_INVALID_ARG;
   if (cfg->decode_min_chunk < 1 || cfg->prefill_min_chunk < 1) return FI_ERR_INVALID_ARG;
+  const int32_t window = cfg->window_left, sink = cfg->sink_tokens;
+  const float cap = cfg->logits_soft_cap;
+  if (window < -1 || sink < 0 || !(cap >= 0.f) || cap == HUGE_VALF) return FI_ERR_INVALID_ARG;
   if (batch > cfg->max_batch) return FI_ERR_CAPACITY;
   if (workspace_bytes < fi_int_workspace_bytes(cfg)) return FI_ERR_CAPACITY;
 
@@ -126,14 +136,33 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
         u.tile = tile;
         u.row0 = qt * tile;
         u.row1 = int32_t(std::min<int64_t>(rows, int64_t(qt + 1) * tile));
-        int64_t vis = lkv[b];
-        if (causal) {
-          const int64_t last_token = (u.row1 - 1) / group;
-          vis = std::min<int64_t>(vis, int64_t(lkv[b]) - lq[b] + last_token + 1);
-          if (vis < 0) vis = 0;
+        const int64_t q_first = int64_t(lkv[b]) - lq[b] + u.row0 / group;
+        const int64_t q_last = int64_t(lkv[b]) - lq[b] + (u.row1 - 1) / group;
+        int64_t hi = causal ? std::min<int64_t>(lkv[b], q_last + 1) : int64_t(lkv[b]);
+        if (hi < 0) hi = 0;
+        u.n_ranges = 1;
+        u.r_begin[0] = 0;
+        u.r_end[0] = hi;
+        if (window >= 0) {
+          const int64_t gran = tile == FI_TILE_DECODE ? std::max(page_size, FI_GRANULE_DECODE)
+                                                      : std::max(page_size, FI_GRANULE_PREFILL);
+          const int64_t lo = std::max<int64_t>(0, q_first - window) / gran * gran;
+          const int64_t sink_end = std::min<int64_t>(sink, hi);
+          if (lo > sink_end) {
+            u.n_ranges = 0;
+            if (sink_end > 0) {
+              u.r_begin[0] = 0;
+              u.r_end[0] = sink_end;
+              u.n_ranges = 1;
+            }
+            u.r_begin[u.n_ranges] = lo;
+            u.r_end[u.n_ranges] = hi;
+            ++u.n_ranges;
+          }
         }
-        u.kv_eff = vis;
-        (tile == FI_TILE_DECODE ? total_dec : total_pre) += vis;
+        u.kv_eff = 0;
+        for (int r = 0; r < u.n_ranges; ++r) u.kv_eff += u.r_end[r] - u.r_begin[r];
+        (tile == FI_TILE_DECODE ? total_dec : total_pre) += u.kv_eff;
         units.push_back(u);
       }
     }
@@ -155,7 +184,10 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   for (const Unit& u : units) {
     const int64_t chunk = u.tile == FI_TILE_DECODE ? chunk_dec : chunk_pre;
     const int64_t weight = u.tile == FI_TILE_DECODE ? cfg->decode_cost_weight : cfg->prefill_cost_weight;
-    const int64_t n = u.kv_eff == 0 ? 1 : ceil_div(u.kv_eff, chunk);
+    int64_t n = 0;
+    for (int r = 0; r < u.n_ranges; ++r) n += ceil_div(u.r_end[r] - u.r_begin[r], chunk);
+    const bool empty = n == 0;
+    if (empty) n = 1;
     int32_t merge_id = -1;
     int64_t base = -1;
     const int32_t nrows = u.row1 - u.row0;
@@ -166,9 +198,9 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
       const int32_t m[FI_MERGE_INTS] = {u.b, u.hk, u.row0, u.row1, int32_t(n), int32_t(base), 0, 0};
       merge_rows.insert(merge_rows.end(), m, m + FI_MERGE_INTS);
     }
-    for (int64_t i = 0; i < n; ++i) {
-      const int64_t k0 = i * chunk;
-      const int64_t k1 = std::min(u.kv_eff, (i + 1) * chunk);
+    // chunk i of the unit: ranges in KV order, chunk numbers running across them
+    int64_t i = 0;
+    auto emit = [&](int64_t k0, int64_t k1) {
       Chunk c;
       c.cost = (k1 - k0) * weight;
       c.tile = u.tile;
@@ -181,6 +213,13 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
                                        n > 1 ? int32_t(base + i * nrows) : -1, merge_id};
       std::memcpy(c.fields, f, sizeof f);
       chunks.push_back(c);
+      ++i;
+    };
+    if (empty) {
+      emit(0, 0);
+    } else {
+      for (int r = 0; r < u.n_ranges; ++r)
+        for (int64_t k0 = u.r_begin[r]; k0 < u.r_end[r]; k0 += chunk) emit(k0, std::min(u.r_end[r], k0 + chunk));
     }
   }
   const int64_t n_items = int64_t(chunks.size());
@@ -239,10 +278,13 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
     r[2] = kvp[b];
     r[3] = lkv[b];
   }
+  int32_t cap_bits;
+  std::memcpy(&cap_bits, &cap, 4);
   const int32_t header[FI_HEADER_INTS] = {FI_PLAN_MAGIC,      int32_t(n_items),   int32_t(n_merge), C,
                                           batch,              causal,             int32_t(off_cta), int32_t(off_items),
                                           int32_t(off_merge), int32_t(off_cnt),   int32_t(off_req), 0,
-                                          num_qo_heads,       num_kv_heads,       page_size,        int32_t(total_ints)};
+                                          num_qo_heads,       num_kv_heads,       page_size,        int32_t(total_ints),
+                                          window,             sink,               cap_bits,         0};
   std::memcpy(ws, header, sizeof header);
 
   fi_plan_info info;
@@ -263,6 +305,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   info.num_prefill_items = int32_t(n_items - n_decode);
   info.int_ws_bytes_used = total_ints * 4;
   info.max_partial_rows = cfg->max_partial_rows;
+  info.variant = cap > 0.f ? 1 : 0;
   *info_out = info;
   return FI_OK;
 }

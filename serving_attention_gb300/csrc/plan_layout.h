@@ -1,7 +1,8 @@
 // plan_layout.h -- layout of the int workspace written by the planner and
 // read by the persistent kernel.  All fields are int32.
 //
-//   header[16]   FI_H_* below
+//   header[20]   FI_H_* below (the mask / logit variant of the plan's config
+//                  included: window_left, sink_tokens, soft-cap as float bits)
 //   cta_indptr   num_ctas + 1 entries: CTA c runs items [cta_indptr[c], cta_indptr[c+1])
 //   items        FI_ITEM_INTS each: {b, hk, row0, row1, kv0, kv1, part, merge}
 //                  rows are packed rows of request b (row = token * G + g),
@@ -21,7 +22,7 @@
 #include <stdint.h>
 
 #define FI_PLAN_MAGIC 0x46495031
-#define FI_HEADER_INTS 16
+#define FI_HEADER_INTS 20
 #define FI_ITEM_INTS 8
 #define FI_MERGE_INTS 8
 #define FI_REQ_INTS 4
@@ -47,7 +48,10 @@ enum {
   FI_H_NUM_QO_HEADS = 12,
   FI_H_NUM_KV_HEADS = 13,
   FI_H_PAGE_SIZE = 14,
-  FI_H_TOTAL_INTS = 15
+  FI_H_TOTAL_INTS = 15,
+  FI_H_WINDOW_LEFT = 16,
+  FI_H_SINK_TOKENS = 17,
+  FI_H_SOFT_CAP_BITS = 18
 };
 
 static inline int64_t fi_partial_o_offset(int64_t max_partial_rows) { return (max_partial_rows + 63) / 64 * 64; }

@@ -10,7 +10,7 @@ import serving_attention_gb300 as fi
 import workloads
 from oracle import plan_ref
 
-HEADER = 16
+HEADER = 20
 
 
 def _cfg(num_ctas=148, **kw):
@@ -111,6 +111,100 @@ def _check_invariants(ws, qop, kv, hq, hkv, causal, cfgd):
     loads = np.array([cost[cta[c]:cta[c + 1]].sum() for c in range(C)])
     if cost.size:
         assert loads.max() <= cost.sum() / C + cost.max()
+
+
+def _visible(lkv, lq, t, causal, window, sink):
+    """Keys query token t may see under the mask reading (brute force)."""
+    q_pos = lkv - lq + t
+    return {j for j in range(lkv) if (not causal or j <= q_pos) and (window < 0 or j >= q_pos - window or j < sink)}
+
+
+def _check_variant_coverage(ws, qop, kv, hq, hkv, causal, page, window, sink):
+    """Every key a row can see lies in one of its unit's chunks; chunks are
+    disjoint, start on the class granule and none is invisible to all rows."""
+    G = hq // hkv
+    n_items, off_items = ws[1], ws[7]
+    items = ws[off_items:off_items + 8 * n_items].reshape(-1, 8)
+    by_unit = {}
+    for it in items:
+        b, hk, r0, r1, k0, k1 = (int(x) for x in it[:6])
+        by_unit.setdefault((b, hk, r0, r1), []).append((k0, k1))
+    for (b, hk, r0, r1), chunks in by_unit.items():
+        lq, lkv = int(qop[b + 1] - qop[b]), int(kv[b])
+        gran = max(page, 64) if lq * G <= 16 else max(page, 128)
+        need = set()
+        for t in range(r0 // G, (r1 - 1) // G + 1):
+            need |= _visible(lkv, lq, t, causal, window, sink)
+        chunks = sorted(chunks)
+        covered = set()
+        for k0, k1 in chunks:
+            if k1 == k0:
+                assert len(chunks) == 1 and not need
+                continue
+            assert k0 % gran == 0, (k0, gran)
+            span = set(range(k0, k1))
+            assert not (span & covered) and span & need, (b, hk, r0, k0, k1)
+            covered |= span
+        assert need <= covered
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_plan_with_window_and_sink_matches_reference(seed):
+    rng = np.random.default_rng(100 + seed)
+    batch = int(rng.integers(1, 24))
+    page = int(rng.choice([1, 4, 16, 64]))
+    hkv = int(rng.choice([1, 2, 8]))
+    group = int(rng.choice([1, 4, 8]))
+    causal = int(rng.integers(0, 2))
+    qo, kv = _random_lengths(rng, batch, page)
+    kvp, lpl = workloads._pages_for(kv, page)
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    nnz = int(kvp[-1])
+    kvi = rng.permutation(nnz + 2)[:nnz].astype(np.int32)
+    window = int(rng.choice([-1, 0, 5, 127, 300, 1000, 4096]))
+    sink = int(rng.choice([0, 0, 4, 64, 700]))
+    cap = float(rng.choice([0.0, 30.0]))
+    cfg, cfgd = _cfg(num_ctas=int(rng.choice([1, 7, 152])), split_factor=int(rng.integers(1, 6)),
+                     decode_min_chunk=int(rng.choice([64, 256])), prefill_min_chunk=int(rng.choice([128, 1024])),
+                     window_left=window, sink_tokens=sink, logits_soft_cap=cap)
+    st, ws, info = _plan_both(cfg, cfgd, qop, kvp, kvi, lpl, hkv * group, hkv, page, causal, nnz + 2)
+    assert st == 0
+    assert info.variant == (1 if cap > 0 else 0)
+    assert tuple(ws[16:19]) == (window, sink, int(np.array([cap], np.float32).view(np.int32)[0]))
+    _check_variant_coverage(ws, qop, kv, hkv * group, hkv, causal, page, window, sink)
+
+
+def test_window_skips_chunks():
+    """A 4096-token window on the long decode requests plans far less KV than the full attention."""
+    qo, kv = np.ones(64, np.int64), workloads.llama8b_decode_lengths(np.random.default_rng(2000))
+    kvp, lpl = workloads._pages_for(kv, 16)
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    kvi = np.arange(int(kvp[-1]), dtype=np.int32)
+
+    def planned_kv(**kw):
+        cfg, _ = _cfg(num_ctas=152, **kw)
+        st, ws, _ = fi.plan_host(cfg, qop, kvp, kvi, lpl, 32, 8, 128, 16, 0)
+        assert st == 0
+        items = ws[ws[7]:ws[7] + 8 * ws[1]].reshape(-1, 8)
+        return int((items[:, 5] - items[:, 4]).sum())
+
+    full = planned_kv()
+    windowed = planned_kv(window_left=4096, sink_tokens=4)
+    expect = int(sum(min(k, 4096 + 1 + 64) for k in kv)) * 8  # window + the granule it rounds to, per KV head
+    assert windowed <= expect + 64 * 8 * 64 and windowed < full / 2
+
+
+@pytest.mark.parametrize("field,value", [("window_left", -2), ("sink_tokens", -1), ("logits_soft_cap", -1.0),
+                                         ("logits_soft_cap", float("inf")), ("logits_soft_cap", float("nan"))])
+def test_plan_rejects_bad_variant(field, value):
+    qo = np.array([0, 1], np.int32)
+    kvp = np.array([0, 1], np.int32)
+    cfg, cfgd = _cfg(**{field: value})
+    st, ws, _ = fi.plan_host(cfg, qo, kvp, np.array([0], np.int32), np.array([3], np.int32), 8, 2, 128, 16, 0)
+    assert st == 1 and ws is None
+    st_p, _, _ = plan_ref.make_plan(cfgd, qo, kvp, np.array([0], np.int32), np.array([3], np.int32), 8, 2, 128, 16,
+                                    0, 1)
+    assert st_p == 1
 
 
 @pytest.mark.parametrize("name", ["tiny_decode", "llama8b_decode", "ragged_prefill", "continuous_batch"])
