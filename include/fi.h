@@ -91,7 +91,7 @@ typedef struct {
     int32_t chunk_decode;        /* KV tokens per chunk chosen for 16-row tiles */
     int32_t chunk_prefill;       /* KV tokens per chunk chosen for 256-row tiles */
     int32_t num_decode_items, num_prefill_items;
-    int32_t variant;             /* bit 0: logits soft-cap on (copied from the config) */
+    int32_t variant;             /* bit 0: logits soft-cap on; bit 1: sliding window (and sink) mask on */
     int64_t int_ws_bytes_used;   /* bytes of the int workspace written (and copied) by the plan */
     int64_t max_partial_rows;    /* capacity of the float workspace, from the config */
 } fi_plan_info;

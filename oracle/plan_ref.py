@@ -223,5 +223,5 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
                 head_dim=head_dim, page_size=page_size, causal=causal, chunk_decode=chunk[16],
                 chunk_prefill=chunk[TILE_PREFILL], num_decode_items=n_dec, num_prefill_items=n_items - n_dec,
                 int_ws_bytes_used=4 * total_ints, max_partial_rows=cfg["max_partial_rows"],
-                variant=1 if cap > 0 else 0)
+                variant=(1 if cap > 0 else 0) | (2 if window >= 0 else 0))
     return OK, ws, info

@@ -8,7 +8,7 @@
 #include <mutex>
 
 #include "../../include/fi.h"
-#include "attention_kernel.cuh"
+#include "launch.h"
 
 namespace fi {
 
@@ -77,35 +77,6 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
   if (part == 0) so[st] = lse;
 }
 
-// ------------------------------------------------------------ launch helpers
-
-// The shared-memory opt-in is set once per device and instantiation, so a
-// run enqueued inside a stream capture makes no non-stream CUDA call.
-constexpr int kMaxDevices = 64;
-
-template <typename T>
-cudaError_t launch_run(const RunParams& p, int num_ctas, cudaStream_t stream) {
-  static bool configured[kMaxDevices] = {};
-  auto kern = paged_attention_kernel<T>;
-  const int smem = int(kSmemBytes);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices || !configured[dev]) {
-    // The tensor-core phase moves registers between warpgroups; that needs the
-    // launch to hold at least kRegsLaunch registers per thread.
-    cudaFuncAttributes fa{};
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs < kRegsLaunch) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) configured[dev] = true;
-  }
-  kern<<<num_ctas, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
-}
-
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool stride_ok(int64_t elems) { return elems > 0 && (elems * 2) % 16 == 0; }
 
@@ -157,11 +128,8 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return FI_ERR_CUDA;
   int prev = 0;
   if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) return FI_ERR_CUDA;
-  auto kern = paged_attention_kernel<__nv_bfloat16>;
-  const int smem = int(kSmemBytes);
   int per_sm = 0;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  const cudaError_t e = run_kernel_occupancy(&per_sm);
   cudaSetDevice(prev);
   if (e != cudaSuccess || per_sm < 1) return FI_ERR_CUDA;
   std::memset(out, 0, sizeof *out);
@@ -270,8 +238,21 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = dtype == FI_BF16 ? launch_run<__nv_bfloat16>(p, info->num_ctas, s)
-                                         : launch_run<__half>(p, info->num_ctas, s);
+  // The plan's variant picks the instantiation: bit 0 logits soft-cap, bit 1
+  // sliding window / sink mask; the plain kernel carries neither.
+  const bool capped = (info->variant & 1) != 0, masked = (info->variant & 2) != 0;
+  cudaError_t e;
+  if (dtype == FI_BF16) {
+    e = capped ? (masked ? launch_run<__nv_bfloat16, true, true>(p, info->num_ctas, s)
+                         : launch_run<__nv_bfloat16, true, false>(p, info->num_ctas, s))
+               : (masked ? launch_run<__nv_bfloat16, false, true>(p, info->num_ctas, s)
+                         : launch_run<__nv_bfloat16, false, false>(p, info->num_ctas, s));
+  } else {
+    e = capped ? (masked ? launch_run<__half, true, true>(p, info->num_ctas, s)
+                         : launch_run<__half, true, false>(p, info->num_ctas, s))
+               : (masked ? launch_run<__half, false, true>(p, info->num_ctas, s)
+                         : launch_run<__half, false, false>(p, info->num_ctas, s));
+  }
   return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 

@@ -112,6 +112,32 @@ struct alignas(1024) RunSmem {
 constexpr size_t kSmemBytes = sizeof(RunSmem);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of the run kernel exceeds one CTA's limit");
 
+// Mask and logit variant of a plan (written into the workspace header by the
+// planner): key j of a query at q_pos is visible only if j >= q_pos -
+// window_left (window_left >= 0) or j < sink; with a soft-cap the logit is
+// cap * tanh(scale * q.k / cap).  In the log2 domain the kernels work in,
+// with u = scale * log2(e) * q.k, that is cap_a * tanh-form below with
+// cap_a = cap * log2(e) and cap_b = 2 / cap.
+struct Variant {
+  int32_t window_left, sink;
+  float cap_a, cap_b;
+};
+
+// Soft-capped log2-domain logit from the plain one, by the identity
+// tanh y = 1 - 2 / (e^(2y) + 1): with t = 2^(u * cap_b) = e^(2y),
+// cap_a * tanh y = cap_a - 2 cap_a / (t + 1).  t = +inf gives cap_a and
+// t = 0 gives -cap_a, so the bound holds at both ends.
+__device__ __forceinline__ float soft_cap_log2(float u, float cap_a, float cap_b) {
+  const float t = ex2(u * cap_b);
+  return cap_a - __fdividef(2.f * cap_a, t + 1.f);
+}
+
+// Lowest visible key of a query at q_pos under the window (a bound below 0
+// when there is no window).
+__device__ __forceinline__ int window_low(const Variant& v, int q_pos) {
+  return v.window_left >= 0 ? q_pos - v.window_left : -1;
+}
+
 struct Item {
   int32_t b, hk, row0, row1, kv0, kv1, part, merge;
 };

@@ -43,7 +43,7 @@ __device__ __forceinline__ int groups_in_pass(int rows) {
 // prefetch, "1) 블록-스파스 KV 포맷").  Pages past the request are addressed
 // out of bounds and arrive as zeros; stage tokens past the chunk are masked
 // by the consumers.
-__device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
+static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
                         int32_t off_req) {
   const int lane = threadIdx.x & 31;
   const int lp = p.log2_page, P = p.page_size;
@@ -205,9 +205,9 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
-template <typename T>
+template <typename T, bool kCap, bool kMask>
 __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
-                        int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal) {
+                        int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, const Variant var) {
   const int cw = (threadIdx.x >> 5) - kFirstConsumerWarp;  // consumer warp 0..7
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
@@ -239,7 +239,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
       // Query rows of this group, pre-scaled by scale*log2(e), as dim pairs
       // for the packed fp32 FMA (dims 2i, 2i+1 of this lane's 8).
       float2 q[kRowsPerGroup][4];
-      int lim_mine = -1;
+      int lim_mine = -1, lo_mine = 0;
 #pragma unroll
       for (int r = 0; r < kRowsPerGroup; ++r) {
         const int prow = prow0 + g * kRowsPerGroup + r;
@@ -254,6 +254,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
 #pragma unroll
           for (int c = 0; c < 4; ++c) q[r][c] = make_float2(q[r][c].x * p.scale_log2, q[r][c].y * p.scale_log2);
           lim = causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1;
+          if (kMask && r == my_row) lo_mine = window_low(var, rq.kv_len - rq.qo_len + t);
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c) q[r][c] = make_float2(0.f, 0.f);
@@ -290,9 +291,11 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
                 a2 = fma2(q[2][c], f[c], a2);
                 a3 = fma2(q[3][c], f[c], a3);
               }
-              const float sfull = reduce_rows4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y, L);
+              float sfull = reduce_rows4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y, L);
+              if (kCap) sfull = soft_cap_log2(sfull, var.cap_a, var.cap_b);
               const int j = j0 + tok;
-              sc[u] = (j < item.kv1 && j <= lim_mine) ? sfull : -INFINITY;
+              const bool seen = j < item.kv1 && j <= lim_mine && (!kMask || j >= lo_mine || j < var.sink);
+              sc[u] = seen ? sfull : -INFINITY;
             }
             float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
             float m_new = m;
@@ -434,7 +437,7 @@ __device__ __forceinline__ int32_t first_decode_item(const RunParams& p, int32_t
   return i;
 }
 
-template <typename T>
+template <typename T, bool kCap, bool kMask>
 __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __grid_constant__ RunParams p) {
   // Casting the __shared__ array itself keeps every access below in the
   // shared address space (LDS/STS rather than generic loads).  The swizzled
@@ -463,6 +466,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   const int32_t off_merge = ws_header(iws, FI_H_OFF_MERGE);
   const int32_t off_cnt = ws_header(iws, FI_H_OFF_COUNTERS);
   const int causal = ws_header(iws, FI_H_CAUSAL);
+  Variant var;
+  var.window_left = ws_header(iws, FI_H_WINDOW_LEFT);
+  var.sink = ws_header(iws, FI_H_SINK_TOKENS);
+  const float cap = __int_as_float(ws_header(iws, FI_H_SOFT_CAP_BITS));
+  var.cap_a = cap * 1.4426950408889634f;
+  var.cap_b = cap > 0.f ? 2.f / cap : 0.f;
   const int warp = threadIdx.x >> 5;
   const int32_t mid = p.tc_prefill ? first_decode_item(p, begin, end, off_items, off_req) : begin;
   const bool tc_phase = mid > begin;
@@ -519,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
       tc::setmaxnreg_inc<kRegsLaunch>();
     } else {
       tc::setmaxnreg_inc<kRegsSoftmax>();
-      pf_softmax<T>(p, sm, begin, mid, off_items, off_req, off_merge, off_cnt, causal);
+      pf_softmax<T, kCap, kMask>(p, sm, begin, mid, off_items, off_req, off_merge, off_cnt, causal, var);
       tc::setmaxnreg_dec<kRegsLaunch>();
       tc::fence_before_sync();
       named_barrier_sync_unaligned(kPhaseBarrier, kThreads);
@@ -530,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   if (warp == 0) {
     produce(p, sm, mid, end, off_items, off_req);
   } else if (warp >= kFirstConsumerWarp) {
-    consume<T>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal);
+    consume<T, kCap, kMask>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal, var);
   }
   tc::fence_before_sync();
   __syncthreads();

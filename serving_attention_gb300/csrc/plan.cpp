@@ -305,7 +305,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   info.num_prefill_items = int32_t(n_items - n_decode);
   info.int_ws_bytes_used = total_ints * 4;
   info.max_partial_rows = cfg->max_partial_rows;
-  info.variant = cap > 0.f ? 1 : 0;
+  info.variant = (cap > 0.f ? 1 : 0) | (window >= 0 ? 2 : 0);
   *info_out = info;
   return FI_OK;
 }

@@ -242,9 +242,9 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
   }
 }
 
-template <typename T>
+template <typename T, bool kCap, bool kMask>
 __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items,
-                           int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal) {
+                           int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, const Variant var) {
   const int sw = (threadIdx.x >> 5) - kSoftmaxWarp0;  // 0..7
   const int mt = sw >> 2;                              // this warpgroup's M tile: 0 = A, 1 = B
   const int w = sw & 3;                                // == warp % 4: TMEM lanes 32w..32w+31
@@ -255,6 +255,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
   const uint32_t s_cols = tl + mt * kTileN, o_cols = tl + kTmemO + mt * kHeadDim;
   const int G = p.group;
   const float c = p.scale_log2;
+  const float cs = kCap ? 1.f : c;  // scale still to apply to the (capped) logits
   uint32_t tiles = 0, items = 0;  // phases of s_full[mt] and o_ready[mt]
   for (int32_t i = b0; i < b1; ++i) {
     const Item item = load_item(p.iws, off_items, i);
@@ -263,10 +264,11 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
     const int ntiles = item_kv_tiles(item);
     const int prow = mt * kTileM + r;  // packed row within the item
     if (mt < item_m_tiles(item)) {
-      int lim = -1;  // last visible KV token of this row (-1: padding row)
+      int lim = -1, lo = 0;  // visible KV tokens of this row: [lo, lim] and the sink (lim -1: padding row)
       if (prow < nrows) {
         const int t = (item.row0 + prow) / G;
         lim = min(causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1, item.kv1 - 1);
+        if (kMask) lo = window_low(var, rq.kv_len - rq.qo_len + t);
       }
       float mrun = -INFINITY, lrun = 0.f;
       bool ok = true;
@@ -280,12 +282,21 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         for (int h = 0; h < 4; ++h) tc::tmem_ld32(s_cols + 32 * h, sv[h]);
         tc::tmem_ld_wait();
         const int kbase = item.kv0 + j * kTileN;
-        if (kbase + kTileN - 1 > lim) {  // causal diagonal, chunk end or padding row
+        if (kCap) {  // capped log2-domain logits; the mask below then works on them
 #pragma unroll
           for (int h = 0; h < 4; ++h)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (kbase + 32 * h + e > lim) sv[h][e] = 0xff800000u;  // -inf
+              sv[h][e] = __float_as_uint(soft_cap_log2(__uint_as_float(sv[h][e]) * c, var.cap_a, var.cap_b));
+        }
+        if (kbase + kTileN - 1 > lim || (kMask && kbase < lo)) {  // causal diagonal, chunk end, padding row, window
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int key = kbase + 32 * h + e;
+              if (key > lim || (kMask && key < lo && key >= var.sink)) sv[h][e] = 0xff800000u;  // -inf
+            }
         }
         // row max in eight independent chains
         float mx8[8];
@@ -294,7 +305,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
 #pragma unroll
         for (int e = 8; e < kTileN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e >> 5][e & 31]));
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * c;
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * cs;
         const float m_old = mrun;
         const float m_new = (mx > m_old + kLazyRescale) ? mx : m_old;
         const bool rescale = (m_new != m_old) && j > 0;
@@ -316,7 +327,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         // P = 2^(s*c - m) as 16-bit pairs over the first 64 columns of the S
         // buffer, published in two halves of 64 KV tokens each
         const float msub = (m_new == -INFINITY) ? 0.f : m_new;
-        const float2 cc = make_float2(c, c), nms = make_float2(-msub, -msub);
+        const float2 cc = make_float2(cs, cs), nms = make_float2(-msub, -msub);
         float2 sum4[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) sum4[a] = make_float2(0.f, 0.f);

@@ -73,6 +73,17 @@ def test_tensor_core_tiles(qo, kv, causal, dtype):
     assert info.num_prefill_items > 0
 
 
+@pytest.mark.parametrize("scale,dtype", [(1.5, "bf16"), (2.0, "bf16"), (4.0, "fp16")])
+def test_peaked_softmax_tensor_cores(scale, dtype):
+    """Queries scaled up so a few keys dominate each row: O must stay within the
+    bar although P enters the P V MMA rounded to 16 bits (bf16 keeps 8
+    significant bits, fp16 11, hence the larger fp16 scale)."""
+    b = workloads.make_batch("peak", dtype, [64, 33], [1000, 40], 8, 2, 16, 1, 777, DEV, pool_pages=70)
+    b.q.mul_(scale)
+    info = _full_check(b)
+    assert info.num_prefill_items > 0
+
+
 @pytest.mark.parametrize("seed,page,group,causal,dtype,qo_max,kv_max", [
     (101, 16, 4, 0, "bf16", 1, 700), (102, 1, 4, 0, "bf16", 1, 300), (103, 4, 1, 1, "fp16", 3, 500),
     (104, 16, 8, 1, "bf16", 2, 900), (105, 64, 4, 1, "bf16", 40, 400), (106, 16, 4, 1, "fp16", 70, 300),

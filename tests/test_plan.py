@@ -169,7 +169,7 @@ def test_plan_with_window_and_sink_matches_reference(seed):
                      window_left=window, sink_tokens=sink, logits_soft_cap=cap)
     st, ws, info = _plan_both(cfg, cfgd, qop, kvp, kvi, lpl, hkv * group, hkv, page, causal, nnz + 2)
     assert st == 0
-    assert info.variant == (1 if cap > 0 else 0)
+    assert info.variant == (1 if cap > 0 else 0) | (2 if window >= 0 else 0)
     assert tuple(ws[16:19]) == (window, sink, int(np.array([cap], np.float32).view(np.int32)[0]))
     _check_variant_coverage(ws, qop, kv, hkv * group, hkv, causal, page, window, sink)
 
