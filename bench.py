@@ -347,6 +347,80 @@ def bench_secondary(dev, reps=5):
         torch.cuda.empty_cache()
     out["shared_prefix"] = bench_shared_prefix(dev, flush, reps)
     out["kv_strides"] = bench_kv_strides(dev, flush, reps)
+    out["variants"] = bench_variants(dev, flush, reps)
+    return out
+
+
+def _graph_ms(fn, flush, reps):
+    import torch
+
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        c.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(c))
+    del g
+    return float(np.median(ts))
+
+
+def bench_variants(dev, flush, reps=5):
+    """Mask and logit variants: the decode workload with a 4096-token sliding
+    window and 4 sink tokens (GB/s over the keys a query can see; the plan
+    skips the rest), and the ragged prefill with a logits soft-cap of 30."""
+    import torch
+
+    import serving_attention_gb300 as fi
+    import workloads
+
+    out = {}
+    b = workloads.llama8b_decode(device=dev)
+    kvi = torch.as_tensor(b.kv_indices, device=dev)
+    o = torch.empty_like(b.q)
+    lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
+    window, sink = 4096, 4
+    times = {}
+    for tag, kw in (("full", {}), ("window", dict(window_left=window, sink_tokens=sink))):
+        cfg = fi.default_plan_config(dev.index, **kw)
+        ws = fi.Workspace(cfg, device=dev)
+        info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                       128, b.page_size, b.causal, b.num_pages)
+        times[tag] = _graph_ms(lambda: fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale), flush, reps)
+        assert fi.device_status(ws) == 0
+    kv = b.kv_lens().astype(np.int64)
+    visible = np.minimum(kv, window + 1) + np.clip(kv - (window + 1), 0, sink)
+    vis_bytes = float(visible.sum()) * b.num_kv_heads * 128 * 2 * 2 + b.batch * b.num_qo_heads * (128 * 2 * 2 + 4)
+    out["window_decode"] = {"workload": "llama8b_decode with window_left 4096, sink_tokens 4",
+                            "ms": times["window"], "full_ms": times["full"],
+                            "gbs_visible": vis_bytes / times["window"] / 1e6,
+                            "speedup_vs_full": times["full"] / times["window"]}
+    del b, o, lse, kvi
+    torch.cuda.empty_cache()
+    b = workloads.ragged_prefill(device=dev)
+    kvi = torch.as_tensor(b.kv_indices, device=dev)
+    o = torch.empty_like(b.q)
+    lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
+    for tag, kw in (("plain", {}), ("capped", dict(logits_soft_cap=30.0))):
+        cfg = fi.default_plan_config(dev.index, **kw)
+        ws = fi.Workspace(cfg, device=dev)
+        info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                       128, b.page_size, b.causal, b.num_pages)
+        times[tag] = _graph_ms(lambda: fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale), flush, reps)
+        assert fi.device_status(ws) == 0
+    _, _, exact = algorithmic(b)
+    out["capped_prefill"] = {"workload": "ragged_prefill with logits_soft_cap 30", "ms": times["capped"],
+                             "plain_ms": times["plain"], "tflops_exact": exact / times["capped"] / 1e9,
+                             "cost_vs_plain": times["capped"] / times["plain"]}
+    del b, o, lse, kvi
+    torch.cuda.empty_cache()
     return out
 
 
@@ -656,6 +730,7 @@ def main():
         sp = sec["shared_prefix"]
         line["shared_prefix"] = dict(sp, frac_of_hbm=sp["composable_gbs"] / hbm)
         line["kv_strides"] = sec["kv_strides"]
+        line["variants"] = sec["variants"]
     print(json.dumps(line))
 
 
