@@ -34,7 +34,8 @@ Rule:
     them.  When a unit has n > 1 items it becomes a merge unit (numbered in
     unit order) and its items get consecutive fp32 partial-state rows,
     n * rows in all.
- 5. cost = kv length of the item * class weight.  Items are sorted by
+ 5. cost = (kv length of the item + 256) * class weight, the 256 standing for
+    the fixed per-item latency of the kernel.  Items are sorted by
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
     load, ties to the smaller CTA index (longest processing time first).
  6. Output: header (with the variant: window, sink, soft-cap bits), per-CTA
@@ -54,6 +55,7 @@ HEADER_INTS = 20
 ITEM_INTS = 8
 MERGE_INTS = 8
 REQ_INTS = 4
+ITEM_COST_TOKENS = 256
 
 # fi_status values
 OK, INVALID_ARG, UNSUPPORTED, CAPACITY = 0, 1, 2, 3
@@ -159,12 +161,12 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
             for i in range(_ceil_div(e_ - s_, chunk[T])):
                 pieces.append((s_ + i * chunk[T], min(e_, s_ + (i + 1) * chunk[T])))
         if not pieces:
-            items.append(((0, -T, b, hk, qt, 0), (b, hk, r0, r1, 0, 0, -1, -1)))
+            items.append(((-ITEM_COST_TOKENS * weight[T], -T, b, hk, qt, 0), (b, hk, r0, r1, 0, 0, -1, -1)))
             continue
         n = len(pieces)
         if n == 1:
             k0, k1 = pieces[0]
-            cost = (k1 - k0) * weight[T]
+            cost = (k1 - k0 + ITEM_COST_TOKENS) * weight[T]
             items.append(((-cost, -T, b, hk, qt, 0), (b, hk, r0, r1, k0, k1, -1, -1)))
             continue
         m = len(merges)
@@ -173,7 +175,7 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
         merges.append((b, hk, r0, r1, n, base, 0, 0))
         part_rows += n * nrows
         for i, (k0, k1) in enumerate(pieces):
-            cost = (k1 - k0) * weight[T]
+            cost = (k1 - k0 + ITEM_COST_TOKENS) * weight[T]
             items.append(((-cost, -T, b, hk, qt, i), (b, hk, r0, r1, k0, k1, base + i * nrows, m)))
 
     if len(items) > cfg["max_items"] or len(merges) > cfg["max_merge_units"] \

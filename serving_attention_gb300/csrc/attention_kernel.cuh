@@ -239,7 +239,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
       // Query rows of this group, pre-scaled by scale*log2(e), as dim pairs
       // for the packed fp32 FMA (dims 2i, 2i+1 of this lane's 8).
       float2 q[kRowsPerGroup][4];
-      int lim_mine = -1, lo_mine = 0;
+      int lim_mine = -1, lo_mine = 0;  // this lane's row: visible keys [lo, lim] (and the sink)
 #pragma unroll
       for (int r = 0; r < kRowsPerGroup; ++r) {
         const int prow = prow0 + g * kRowsPerGroup + r;
@@ -261,6 +261,9 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
         }
         if (r == my_row) lim_mine = lim;
       }
+      // With a window, key j of the chunk is visible to this lane's row iff
+      // (unsigned)(j - lo_mine) < vis_cnt or j < sink (one range compare).
+      const unsigned vis_cnt = kMask ? unsigned(max(0, min(lim_mine, item.kv1 - 1) + 1 - lo_mine)) : 0u;
 
       float2 o[kRowsPerGroup][4];
 #pragma unroll
@@ -294,7 +297,8 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
               float sfull = reduce_rows4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y, L);
               if (kCap) sfull = soft_cap_log2(sfull, var.cap_a, var.cap_b);
               const int j = j0 + tok;
-              const bool seen = j < item.kv1 && j <= lim_mine && (!kMask || j >= lo_mine || j < var.sink);
+              const bool seen = kMask ? (unsigned(j - lo_mine) < vis_cnt || j < var.sink)
+                                      : (j < item.kv1 && j <= lim_mine);
               sc[u] = seen ? sfull : -INFINITY;
             }
             float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));

@@ -21,7 +21,10 @@
 //  * per tile class, a KV chunk length = max(min_chunk, total / (CTAs * split))
 //    rounded up to the class granule; units longer than a chunk are split
 //    into chunks whose fp32 partial states are merged by the kernel;
-//  * chunks are dealt out longest-first to the least-loaded CTA (LPT).
+//  * chunks are dealt out longest-first to the least-loaded CTA (LPT); an
+//    item's cost is its KV length plus a fixed FI_ITEM_COST_TOKENS (the
+//    per-item latency of the kernel), times the class weight, so that many
+//    short items do not pile up on one CTA.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -202,7 +205,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
     int64_t i = 0;
     auto emit = [&](int64_t k0, int64_t k1) {
       Chunk c;
-      c.cost = (k1 - k0) * weight;
+      c.cost = (k1 - k0 + FI_ITEM_COST_TOKENS) * weight;
       c.tile = u.tile;
       c.b = u.b;
       c.hk = u.hk;

@@ -31,6 +31,7 @@
 #define FI_TILE_PREFILL 256  // two 128-row M tiles sharing each K/V tile
 #define FI_GRANULE_DECODE 64
 #define FI_GRANULE_PREFILL 128
+#define FI_ITEM_COST_TOKENS 256  // fixed cost of a work item in the deal, in KV tokens of its class
 
 enum {
   FI_H_MAGIC = 0,

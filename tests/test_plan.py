@@ -106,7 +106,7 @@ def _check_invariants(ws, qop, kv, hq, hkv, causal, cfgd):
     cost = []
     for it in items:
         R = int(qop[it[0] + 1] - qop[it[0]]) * G
-        cost.append((int(it[5]) - int(it[4])) * w[16 if R <= 16 else plan_ref.TILE_PREFILL])
+        cost.append((int(it[5]) - int(it[4]) + plan_ref.ITEM_COST_TOKENS) * w[16 if R <= 16 else plan_ref.TILE_PREFILL])
     cost = np.array(cost, dtype=np.int64)
     loads = np.array([cost[cta[c]:cta[c + 1]].sum() for c in range(C)])
     if cost.size:
