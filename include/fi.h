@@ -78,6 +78,23 @@ typedef struct {
     int32_t window_left;
     int32_t sink_tokens;
     float logits_soft_cap;
+    /* RoPE fused into the attention loaders (FlashInfer paper summary,
+     * "주요 실험 결과": a custom kernel fusing RoPE with attention).  The
+     * cache holds keys WITHOUT rotation; the kernel rotates q and k on the
+     * fly, Llama style: dims i and i + 64 form a pair rotated by the angle
+     * (pos / rope_scale) * rope_theta^(-2i/128), i < 64, with key j at
+     * position j and query token t of a request at position Lkv - Lq + t
+     * (the bottom-right alignment of the causal mask).
+     *   rope_max_positions > 0 turns it on: positions must stay below it (a
+     *     plan with a longer request, or with Lq > Lkv, is
+     *     FI_ERR_INVALID_ARG), and the int workspace then also holds a
+     *     cos/sin table for these positions, filled by fi_rope_init;
+     *   rope_theta > 0 (10000 for Llama 2, 500000 for Llama 3);
+     *   rope_scale > 0 divides the positions (1 = no scaling). */
+    int32_t rope_max_positions;
+    float rope_theta;
+    float rope_scale;
+    int32_t reserved;
 } fi_plan_config;
 
 /* Plain data returned by fi_plan; passed to run by value semantics. */
@@ -91,7 +108,7 @@ typedef struct {
     int32_t chunk_decode;        /* KV tokens per chunk chosen for 16-row tiles */
     int32_t chunk_prefill;       /* KV tokens per chunk chosen for 256-row tiles */
     int32_t num_decode_items, num_prefill_items;
-    int32_t variant;             /* bit 0: logits soft-cap on; bit 1: sliding window (and sink) mask on */
+    int32_t variant;             /* bit 0: logits soft-cap; bit 1: sliding window (and sink) mask; bit 2: RoPE */
     int64_t int_ws_bytes_used;   /* bytes of the int workspace written (and copied) by the plan */
     int64_t max_partial_rows;    /* capacity of the float workspace, from the config */
 } fi_plan_info;
@@ -102,10 +119,22 @@ typedef struct {
 fi_status fi_default_plan_config(int device, fi_plan_config* out);
 
 /* Workspace sizes for a config (bytes).  The int workspace holds the plan,
- * the merge counters and the device status word; the float workspace holds
- * fp32 partial states of split work.  Both are device memory. */
+ * the merge counters and the device status word (and, with RoPE, the cos/sin
+ * table after them); the float workspace holds fp32 partial states of split
+ * work.  Both are device memory. */
 size_t fi_int_workspace_bytes(const fi_plan_config* cfg);
 size_t fi_float_workspace_bytes(const fi_plan_config* cfg, int32_t head_dim);
+
+/*
+ * fi_rope_init -- fill the RoPE cos/sin table of an int workspace made for
+ * `cfg` (rope_max_positions > 0): cos and sin of (pos / rope_scale) *
+ * rope_theta^(-2i/128) for pos < rope_max_positions and i < 64, computed in
+ * fp64 and stored as fp32.  Once per workspace (and again if the config's
+ * RoPE fields change); plans never overwrite the table.  Asynchronous on
+ * `stream`.  FI_ERR_INVALID_ARG when the config has no RoPE or a theta or
+ * scale <= 0.
+ */
+fi_status fi_rope_init(const fi_plan_config* cfg, void* int_workspace_dev, void* stream);
 
 /*
  * fi_plan -- build the load-balanced split-KV work list on the host and copy

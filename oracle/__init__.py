@@ -66,6 +66,9 @@ class _Problem(ctypes.Structure):
         ("window_left", ctypes.c_int32),
         ("sink_tokens", ctypes.c_int32),
         ("logits_soft_cap", ctypes.c_double),
+        ("rope", ctypes.c_int32),
+        ("rope_theta", ctypes.c_double),
+        ("rope_scale", ctypes.c_double),
     ]
 
 
@@ -112,7 +115,8 @@ class Problem:
     for fp16/bf16, float32 for fp32) with arbitrary element strides."""
 
     def __init__(self, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads,
-                 page_size, causal, sm_scale, dtype, q, k, v, window_left=-1, sink_tokens=0, logits_soft_cap=0.0):
+                 page_size, causal, sm_scale, dtype, q, k, v, window_left=-1, sink_tokens=0, logits_soft_cap=0.0,
+                 rope=0, rope_theta=10000.0, rope_scale=1.0):
         self.qo_indptr = np.ascontiguousarray(qo_indptr, dtype=np.int32)
         self.kv_indptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)
         self.kv_indices = np.ascontiguousarray(kv_indices, dtype=np.int32)
@@ -134,7 +138,10 @@ class Problem:
                            _ptr(self.kv_indices) if self.kv_indices.size else 0, _ptr(self.last_page_len),
                            num_qo_heads, num_kv_heads, q.shape[2], page_size, int(causal), float(sm_scale),
                            dtype, _ptr(q), qs[0], qs[1], _ptr(k), ks[0], ks[1], ks[2], _ptr(v), vs[0], vs[1],
-                           vs[2], int(window_left), int(sink_tokens), float(logits_soft_cap))
+                           vs[2], int(window_left), int(sink_tokens), float(logits_soft_cap), int(rope),
+                           float(rope_theta), float(rope_scale))
+        if rope and q.shape[2] > 512:
+            raise ValueError("the oracle's RoPE path holds at most 512 dims")
 
     @property
     def num_rows(self) -> int:

@@ -39,6 +39,15 @@
  *   logits soft-cap (cap > 0, off when 0): the logit fed to the softmax is
  *     cap * tanh(scale * q.k / cap) instead of scale * q.k.
  *
+ * RoPE fused into attention (FlashInfer paper summary, section "주요 실험
+ * 결과": a kernel fusing RoPE with attention; the page gives no formula).
+ * The plain reading, Llama style: before the dot product, q and every key are
+ * rotated by their positions; dims i and i + d/2 form a pair rotated by
+ * a = (pos / rope_scale) * rope_theta^(-2i/d):
+ *   x_i' = x_i cos a - x_{i+d/2} sin a,   x_{i+d/2}' = x_{i+d/2} cos a + x_i sin a.
+ * Key j sits at position j and query token t at Lkv - Lq + t (the alignment
+ * of the causal mask).  The cache holds unrotated keys.
+ *
  * LSE is the natural log of the sum of exp of the logits (the *scaled*, and
  * when capped the capped, scores).  A row that sees no key gets O = 0 and
  * LSE = -inf (the pages are silent; this is the identity of the merge
@@ -110,7 +119,22 @@ typedef struct {
     int32_t window_left;          /* < 0: no sliding window */
     int32_t sink_tokens;          /* keys j < sink_tokens ignore the window */
     double logits_soft_cap;       /* 0: plain scaled logits */
+    int32_t rope;                 /* 1: rotate q and k by position (RoPE) */
+    double rope_theta, rope_scale;
 } orc_problem;
+
+/* RoPE rotation of x[0..d) at position pos, in place (pairs i, i + d/2). */
+static void rope_rotate(const orc_problem* p, double* x, int64_t pos)
+{
+    const int half = p->head_dim / 2;
+    for (int i = 0; i < half; ++i) {
+        const double a = ((double)pos / p->rope_scale) * pow(p->rope_theta, -2.0 * i / p->head_dim);
+        const double c = cos(a), sn = sin(a);
+        const double x0 = x[i], x1 = x[i + half];
+        x[i] = x0 * c - x1 * sn;
+        x[i + half] = x1 * c + x0 * sn;
+    }
+}
 
 static int32_t kv_len_of(const orc_problem* p, int b)
 {
@@ -140,6 +164,11 @@ static void attend_one(const orc_problem* p, int b, int t, int h, double* scores
     for (int c = 0; c < d; ++c) o[c] = 0.0;
 
     const int64_t qbase = row * p->q_stride_tok + (int64_t)h * p->q_stride_head;
+    double qr[512], kr[512]; /* rotated q and key (RoPE only; head_dim <= 512) */
+    if (p->rope) {
+        for (int c = 0; c < d; ++c) qr[c] = load_elem(p->q, p->dtype, qbase + c);
+        rope_rotate(p, qr, q_pos);
+    }
     double m = -INFINITY;
     for (int64_t j = 0; j < nvis; ++j) {
         if (j < win_lo && j >= p->sink_tokens) {
@@ -151,8 +180,14 @@ static void attend_one(const orc_problem* p, int b, int t, int h, double* scores
         int64_t slot = j % p->page_size;
         int64_t kbase = page * p->k_stride_page + slot * p->k_stride_slot + (int64_t)hk * p->k_stride_head;
         double dot = 0.0;
-        for (int c = 0; c < d; ++c)
-            dot += load_elem(p->q, p->dtype, qbase + c) * load_elem(p->k, p->dtype, kbase + c);
+        if (p->rope) {
+            for (int c = 0; c < d; ++c) kr[c] = load_elem(p->k, p->dtype, kbase + c);
+            rope_rotate(p, kr, j);
+            for (int c = 0; c < d; ++c) dot += qr[c] * kr[c];
+        } else {
+            for (int c = 0; c < d; ++c)
+                dot += load_elem(p->q, p->dtype, qbase + c) * load_elem(p->k, p->dtype, kbase + c);
+        }
         double logit = p->sm_scale * dot;
         if (p->logits_soft_cap > 0.0) logit = p->logits_soft_cap * tanh(logit / p->logits_soft_cap);
         scores[j] = logit;

@@ -38,7 +38,8 @@ Rule:
     the fixed per-item latency of the kernel.  Items are sorted by
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
     load, ties to the smaller CTA index (longest processing time first).
- 6. Output: header (with the variant: window, sink, soft-cap bits), per-CTA
+ 6. Output: header (with the variant: window, sink, soft-cap bits, and for
+    RoPE its position capacity, theta and scale bits and the table offset), per-CTA
     CSR offsets, items in CTA order (within a CTA the 256-row items first,
     then the 16-row items, each in the order dealt), merge units, zeroed merge
     counters, request table.
@@ -51,7 +52,8 @@ import numpy as np
 
 MAGIC = 0x46495031
 TILE_DECODE, TILE_PREFILL = 16, 256
-HEADER_INTS = 20
+HEADER_INTS = 24
+ROPE_PAIRS = 64
 ITEM_INTS = 8
 MERGE_INTS = 8
 REQ_INTS = 4
@@ -97,6 +99,11 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     cap = float(np.float32(cfg.get("logits_soft_cap", 0.0)))
     if window < -1 or sink < 0 or not (cap >= 0.0) or cap == float("inf"):
         return INVALID_ARG, None, None
+    rope_max = cfg.get("rope_max_positions", 0)
+    theta = float(np.float32(cfg.get("rope_theta", 10000.0)))
+    rscale = float(np.float32(cfg.get("rope_scale", 1.0)))
+    if rope_max < 0 or (rope_max > 0 and not (0 < theta < float("inf") and 0 < rscale < float("inf"))):
+        return INVALID_ARG, None, None
     if batch > cfg["max_batch"]:
         return CAPACITY, None, None
     if qo[0] != 0 or kvp[0] != 0:
@@ -105,6 +112,11 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
         if qo[b + 1] < qo[b] or kvp[b + 1] < kvp[b]:
             return INVALID_ARG, None, None
         if kvp[b + 1] > kvp[b] and not (1 <= lpl[b] <= page_size):
+            return INVALID_ARG, None, None
+        # RoPE positions (keys 0 .. Lkv-1, queries Lkv-Lq .. Lkv-1) must lie in the table
+        n_pg = kvp[b + 1] - kvp[b]
+        lkv_b = 0 if n_pg == 0 else (n_pg - 1) * page_size + lpl[b]
+        if rope_max > 0 and (lkv_b > rope_max or qo[b + 1] - qo[b] > lkv_b):
             return INVALID_ARG, None, None
     if num_pages > 0:
         idx = np.asarray(kv_indices[:kvp[batch]], dtype=np.int64)
@@ -201,10 +213,14 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
         return CAPACITY, None, None
 
     ws = np.zeros(total_ints, dtype=np.int32)
-    cap_bits = int(np.array([cap], dtype=np.float32).view(np.int32)[0])
+    def bits(x):
+        return int(np.array([x], dtype=np.float32).view(np.int32)[0])
+
+    rope_off = (int_workspace_ints(cfg) * 4 + 255) // 256 * 256 // 4 if rope_max > 0 else 0
     ws[:HEADER_INTS] = [MAGIC, n_items, n_merge, C, batch, causal, off_cta, off_items, off_merge,
                         off_cnt, off_req, 0, num_qo_heads, num_kv_heads, page_size, total_ints,
-                        window, sink, cap_bits, 0]
+                        window, sink, bits(cap), rope_max,
+                        bits(theta) if rope_max > 0 else 0, bits(rscale) if rope_max > 0 else 0, rope_off, 0]
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos
@@ -225,5 +241,5 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
                 head_dim=head_dim, page_size=page_size, causal=causal, chunk_decode=chunk[16],
                 chunk_prefill=chunk[TILE_PREFILL], num_decode_items=n_dec, num_prefill_items=n_items - n_dec,
                 int_ws_bytes_used=4 * total_ints, max_partial_rows=cfg["max_partial_rows"],
-                variant=(1 if cap > 0 else 0) | (2 if window >= 0 else 0))
+                variant=(1 if cap > 0 else 0) | (2 if window >= 0 else 0) | (4 if rope_max > 0 else 0))
     return OK, ws, info

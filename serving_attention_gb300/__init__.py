@@ -38,10 +38,11 @@ class PlanConfig(ctypes.Structure):
                 ("decode_min_chunk", ctypes.c_int32), ("prefill_min_chunk", ctypes.c_int32),
                 ("decode_cost_weight", ctypes.c_int32), ("prefill_cost_weight", ctypes.c_int32),
                 ("split_factor", ctypes.c_int32), ("window_left", ctypes.c_int32), ("sink_tokens", ctypes.c_int32),
-                ("logits_soft_cap", ctypes.c_float)]
+                ("logits_soft_cap", ctypes.c_float), ("rope_max_positions", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("rope_scale", ctypes.c_float), ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
-        return {f: getattr(self, f) for f, _ in self._fields_}
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
 
 
 class PlanInfo(ctypes.Structure):
@@ -59,7 +60,7 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ["fi_default_plan_config", "fi_int_workspace_bytes", "fi_float_workspace_bytes", "fi_plan",
            "fi_plan_host", "fi_batch_paged_attention_run", "fi_batch_paged_attention_run_static_scratch",
-           "fi_merge_states", "fi_get_device_status", "fi_status_string"]
+           "fi_merge_states", "fi_get_device_status", "fi_status_string", "fi_rope_init"]
 
 _lib = None
 
@@ -87,10 +88,11 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
     lib.fi_batch_paged_attention_run_static_scratch.restype = ctypes.c_int
     lib.fi_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, vp]
     lib.fi_get_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+    lib.fi_rope_init.argtypes = [cfgp, vp, vp]
     lib.fi_status_string.argtypes = [ctypes.c_int]
     lib.fi_status_string.restype = ctypes.c_char_p
     for name in ("fi_default_plan_config", "fi_plan", "fi_plan_host", "fi_batch_paged_attention_run",
-                 "fi_merge_states", "fi_get_device_status"):
+                 "fi_merge_states", "fi_get_device_status", "fi_rope_init"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -122,7 +124,8 @@ def make_plan_config(num_ctas: int, **overrides) -> PlanConfig:
     """A config without asking the device (host-side planning and tests)."""
     cfg = PlanConfig(num_ctas=num_ctas, max_batch=8192, max_items=1 << 17, max_merge_units=1 << 15,
                      max_partial_rows=1 << 19, decode_min_chunk=256, prefill_min_chunk=1024, decode_cost_weight=4,
-                     prefill_cost_weight=6, split_factor=4, window_left=-1, sink_tokens=0, logits_soft_cap=0.0)
+                     prefill_cost_weight=6, split_factor=4, window_left=-1, sink_tokens=0, logits_soft_cap=0.0,
+                     rope_max_positions=0, rope_theta=10000.0, rope_scale=1.0)
     for k, v in overrides.items():
         setattr(cfg, k, v)
     return cfg
@@ -148,6 +151,10 @@ class Workspace:
         self._staging = [torch.empty(ib, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
         self._events = [None, None]
         self._next = 0
+        if cfg.rope_max_positions > 0:  # the RoPE cos/sin table lives in the int workspace
+            with torch.cuda.device(self.device):
+                _check(load().fi_rope_init(ctypes.byref(cfg), self.int_ws.data_ptr(), _stream_ptr(None)),
+                       "fi_rope_init")
 
 
 def plan_host(cfg: PlanConfig, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads: int,

@@ -9,6 +9,7 @@
 
 #include "../../include/fi.h"
 #include "launch.h"
+#include "workspace.h"
 
 namespace fi {
 
@@ -75,6 +76,19 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
   __syncwarp();
   Vec8<T>::store(vo + st * kHeadDim + part * 8, r);
   if (part == 0) so[st] = lse;
+}
+
+// RoPE table: (cos, sin) of (pos / scale) * theta^(-2i/128) for pos <
+// max_pos, i < 64, computed in fp64 and rounded once to fp32.
+__global__ void rope_table_kernel(float2* table, int64_t entries, double theta, double inv_scale) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= entries) return;
+  const int64_t pos = idx / FI_ROPE_PAIRS;
+  const int i = int(idx % FI_ROPE_PAIRS);
+  const double freq = pow(theta, -2.0 * i / double(2 * FI_ROPE_PAIRS));
+  double sn, cs;
+  sincos(double(pos) * inv_scale * freq, &sn, &cs);
+  table[idx] = make_float2(float(cs), float(sn));
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -146,6 +160,9 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   out->window_left = -1;
   out->sink_tokens = 0;
   out->logits_soft_cap = 0.f;
+  out->rope_max_positions = 0;
+  out->rope_theta = 10000.f;
+  out->rope_scale = 1.f;
   return FI_OK;
 }
 
@@ -254,6 +271,20 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
                          : launch_run<__half, false, false>(p, info->num_ctas, s));
   }
   return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
+extern "C" fi_status fi_rope_init(const fi_plan_config* cfg, void* int_workspace_dev, void* stream) {
+  if (!cfg || !int_workspace_dev || cfg->rope_max_positions <= 0) return FI_ERR_INVALID_ARG;
+  if (!(cfg->rope_theta > 0.f && cfg->rope_theta < HUGE_VALF && cfg->rope_scale > 0.f && cfg->rope_scale < HUGE_VALF))
+    return FI_ERR_INVALID_ARG;
+  if (!aligned16(int_workspace_dev)) return FI_ERR_ALIGNMENT;
+  float2* table = reinterpret_cast<float2*>(static_cast<char*>(int_workspace_dev) +
+                                            fi_rope_table_offset(plan_capacity_ints(cfg)));
+  const int64_t entries = int64_t(cfg->rope_max_positions) * FI_ROPE_PAIRS;
+  const int64_t blocks = (entries + 255) / 256;
+  rope_table_kernel<<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      table, entries, double(cfg->rope_theta), 1.0 / double(cfg->rope_scale));
+  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 
 extern "C" fi_status fi_merge_states(const void* v_a, const float* s_a, const void* v_b, const float* s_b,

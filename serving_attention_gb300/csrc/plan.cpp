@@ -38,6 +38,7 @@
 
 #include "../../include/fi.h"
 #include "plan_layout.h"
+#include "workspace.h"
 
 namespace {
 
@@ -70,12 +71,17 @@ bool deal_before(const Chunk& x, const Chunk& y) {
 
 }  // namespace
 
+int64_t fi::plan_capacity_ints(const fi_plan_config* cfg) {
+  return FI_HEADER_INTS + round4(int64_t(cfg->num_ctas) + 1) + int64_t(FI_ITEM_INTS) * cfg->max_items +
+         int64_t(FI_MERGE_INTS) * cfg->max_merge_units + round4(cfg->max_merge_units) +
+         int64_t(FI_REQ_INTS) * cfg->max_batch;
+}
+
 extern "C" size_t fi_int_workspace_bytes(const fi_plan_config* cfg) {
   if (!cfg) return 0;
-  int64_t ints = FI_HEADER_INTS + round4(int64_t(cfg->num_ctas) + 1) + int64_t(FI_ITEM_INTS) * cfg->max_items +
-                 int64_t(FI_MERGE_INTS) * cfg->max_merge_units + round4(cfg->max_merge_units) +
-                 int64_t(FI_REQ_INTS) * cfg->max_batch;
-  return size_t(ints) * 4;
+  const int64_t plan_ints = fi::plan_capacity_ints(cfg);
+  if (cfg->rope_max_positions <= 0) return size_t(plan_ints) * 4;
+  return size_t(fi_rope_table_offset(plan_ints) + int64_t(cfg->rope_max_positions) * FI_ROPE_PAIRS * 8);
 }
 
 extern "C" size_t fi_float_workspace_bytes(const fi_plan_config* cfg, int32_t head_dim) {
@@ -100,8 +106,12 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   const int32_t window = cfg->window_left, sink = cfg->sink_tokens;
   const float cap = cfg->logits_soft_cap;
   if (window < -1 || sink < 0 || !(cap >= 0.f) || cap == HUGE_VALF) return FI_ERR_INVALID_ARG;
+  const int32_t rope_max = cfg->rope_max_positions;
+  if (rope_max < 0 || (rope_max > 0 && !(cfg->rope_theta > 0.f && cfg->rope_theta < HUGE_VALF &&
+                                         cfg->rope_scale > 0.f && cfg->rope_scale < HUGE_VALF)))
+    return FI_ERR_INVALID_ARG;
   if (batch > cfg->max_batch) return FI_ERR_CAPACITY;
-  if (workspace_bytes < fi_int_workspace_bytes(cfg)) return FI_ERR_CAPACITY;
+  if (workspace_bytes < size_t(fi::plan_capacity_ints(cfg)) * 4) return FI_ERR_CAPACITY;
 
   const int32_t* qo = qo_indptr;
   const int32_t* kvp = kv_indptr;
@@ -115,6 +125,8 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
     const int64_t len = pages == 0 ? 0 : int64_t(pages - 1) * page_size + last_page_len[b];
     if (len > INT32_MAX) return FI_ERR_UNSUPPORTED;
     lkv[b] = int32_t(len);
+    // RoPE positions: keys 0 .. Lkv-1 and queries Lkv-Lq .. Lkv-1 inside the table
+    if (rope_max > 0 && (len > rope_max || lq[b] > len)) return FI_ERR_INVALID_ARG;
   }
   if (num_pages > 0 && batch > 0) {
     if (!kv_indices && kvp[batch] > 0) return FI_ERR_INVALID_ARG;
@@ -252,7 +264,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   const int64_t off_cnt = off_merge + FI_MERGE_INTS * n_merge;
   const int64_t off_req = off_cnt + round4(n_merge);
   const int64_t total_ints = off_req + int64_t(FI_REQ_INTS) * batch;
-  if (size_t(total_ints) * 4 > fi_int_workspace_bytes(cfg)) return FI_ERR_CAPACITY;
+  if (total_ints > fi::plan_capacity_ints(cfg)) return FI_ERR_CAPACITY;
 
   int32_t* ws = static_cast<int32_t*>(workspace_host);
   std::memset(ws, 0, size_t(total_ints) * 4);
@@ -281,13 +293,19 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
     r[2] = kvp[b];
     r[3] = lkv[b];
   }
-  int32_t cap_bits;
+  int32_t cap_bits, theta_bits = 0, scale_bits = 0;
   std::memcpy(&cap_bits, &cap, 4);
+  if (rope_max > 0) {
+    std::memcpy(&theta_bits, &cfg->rope_theta, 4);
+    std::memcpy(&scale_bits, &cfg->rope_scale, 4);
+  }
+  const int32_t rope_off = rope_max > 0 ? int32_t(fi_rope_table_offset(fi::plan_capacity_ints(cfg)) / 4) : 0;
   const int32_t header[FI_HEADER_INTS] = {FI_PLAN_MAGIC,      int32_t(n_items),   int32_t(n_merge), C,
                                           batch,              causal,             int32_t(off_cta), int32_t(off_items),
                                           int32_t(off_merge), int32_t(off_cnt),   int32_t(off_req), 0,
                                           num_qo_heads,       num_kv_heads,       page_size,        int32_t(total_ints),
-                                          window,             sink,               cap_bits,         0};
+                                          window,             sink,               cap_bits,         rope_max,
+                                          theta_bits,         scale_bits,         rope_off,         0};
   std::memcpy(ws, header, sizeof header);
 
   fi_plan_info info;
@@ -308,7 +326,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   info.num_prefill_items = int32_t(n_items - n_decode);
   info.int_ws_bytes_used = total_ints * 4;
   info.max_partial_rows = cfg->max_partial_rows;
-  info.variant = (cap > 0.f ? 1 : 0) | (window >= 0 ? 2 : 0);
+  info.variant = (cap > 0.f ? 1 : 0) | (window >= 0 ? 2 : 0) | (rope_max > 0 ? 4 : 0);
   *info_out = info;
   return FI_OK;
 }

@@ -1,8 +1,8 @@
 // plan_layout.h -- layout of the int workspace written by the planner and
 // read by the persistent kernel.  All fields are int32.
 //
-//   header[20]   FI_H_* below (the mask / logit variant of the plan's config
-//                  included: window_left, sink_tokens, soft-cap as float bits)
+//   header[24]   FI_H_* below (the variant of the plan's config included:
+//                  window_left, sink_tokens, soft-cap as float bits, RoPE)
 //   cta_indptr   num_ctas + 1 entries: CTA c runs items [cta_indptr[c], cta_indptr[c+1])
 //   items        FI_ITEM_INTS each: {b, hk, row0, row1, kv0, kv1, part, merge}
 //                  rows are packed rows of request b (row = token * G + g),
@@ -13,6 +13,10 @@
 //                  chunk i of the unit wrote partial rows part_base + i * (row1 - row0) ...
 //   counters     one per merge unit, zero between runs (the merging CTA resets it)
 //   requests     FI_REQ_INTS each: {qo_start, qo_len, page_start, kv_len}
+//   ...          (the rest of the plan capacity)
+//   rope table   with RoPE: float2 (cos, sin) [rope_max_positions][64] at
+//                  fi_rope_table_offset(capacity) bytes, filled by
+//                  fi_rope_init, never part of a plan's copy
 // Every section starts on a multiple of 4 ints (16 bytes).
 //
 // Float workspace: partial LSE (natural log) at [0, max_partial_rows), partial
@@ -22,7 +26,7 @@
 #include <stdint.h>
 
 #define FI_PLAN_MAGIC 0x46495031
-#define FI_HEADER_INTS 20
+#define FI_HEADER_INTS 24
 #define FI_ITEM_INTS 8
 #define FI_MERGE_INTS 8
 #define FI_REQ_INTS 4
@@ -52,7 +56,17 @@ enum {
   FI_H_TOTAL_INTS = 15,
   FI_H_WINDOW_LEFT = 16,
   FI_H_SINK_TOKENS = 17,
-  FI_H_SOFT_CAP_BITS = 18
+  FI_H_SOFT_CAP_BITS = 18,
+  FI_H_ROPE_MAX_POS = 19,     // 0: no RoPE
+  FI_H_ROPE_THETA_BITS = 20,
+  FI_H_ROPE_SCALE_BITS = 21,
+  FI_H_ROPE_TABLE_OFF = 22    // ints from the workspace start to the cos/sin table
 };
+
+#define FI_ROPE_PAIRS 64  // dims i and i + 64 of head_dim 128 form a rotated pair
+
+// Byte offset of the RoPE table in an int workspace whose plan region holds
+// `plan_ints` int32 (256-byte aligned).
+static inline int64_t fi_rope_table_offset(int64_t plan_ints) { return (plan_ints * 4 + 255) / 256 * 256; }
 
 static inline int64_t fi_partial_o_offset(int64_t max_partial_rows) { return (max_partial_rows + 63) / 64 * 64; }

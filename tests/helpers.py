@@ -15,11 +15,13 @@ LSE_TOL = 1e-3
 
 
 def oracle_problem(b: workloads.PagedBatch, window_left: int = -1, sink_tokens: int = 0,
-                   logits_soft_cap: float = 0.0) -> oracle.Problem:
+                   logits_soft_cap: float = 0.0, rope: int = 0, rope_theta: float = 10000.0,
+                   rope_scale: float = 1.0) -> oracle.Problem:
     q, k, v = workloads.host_views(b)
     return oracle.Problem(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads,
                           b.num_kv_heads, b.page_size, b.causal, b.sm_scale, ORACLE_DTYPE[b.dtype], q, k, v,
-                          window_left=window_left, sink_tokens=sink_tokens, logits_soft_cap=logits_soft_cap)
+                          window_left=window_left, sink_tokens=sink_tokens, logits_soft_cap=logits_soft_cap,
+                          rope=rope, rope_theta=rope_theta, rope_scale=rope_scale)
 
 
 def gpu_run(b: workloads.PagedBatch, cfg=None, ws=None, stream=None, o=None, lse=None):

@@ -10,7 +10,7 @@ import serving_attention_gb300 as fi
 import workloads
 from oracle import plan_ref
 
-HEADER = 20
+HEADER = 24
 
 
 def _cfg(num_ctas=148, **kw):
@@ -192,6 +192,46 @@ def test_window_skips_chunks():
     windowed = planned_kv(window_left=4096, sink_tokens=4)
     expect = int(sum(min(k, 4096 + 1 + 64) for k in kv)) * 8  # window + the granule it rounds to, per KV head
     assert windowed <= expect + 64 * 8 * 64 and windowed < full / 2
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_with_rope_matches_reference(seed):
+    rng = np.random.default_rng(200 + seed)
+    batch = int(rng.integers(1, 12))
+    page = int(rng.choice([1, 16]))
+    kv = rng.integers(1, 3000, size=batch)
+    qo = np.minimum(kv, rng.choice([1, 1, 7, 300], size=batch))  # RoPE needs Lq <= Lkv
+    kvp, lpl = workloads._pages_for(kv, page)
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    nnz = int(kvp[-1])
+    kvi = rng.permutation(nnz).astype(np.int32)
+    cfg, cfgd = _cfg(num_ctas=152, rope_max_positions=4096, rope_theta=float(rng.choice([1e4, 5e5])),
+                     rope_scale=float(rng.choice([1.0, 8.0])), window_left=int(rng.choice([-1, 500])))
+    st, ws, info = _plan_both(cfg, cfgd, qop, kvp, kvi, lpl, 32, 8, 16 if page == 16 else 1, 1, nnz)
+    assert st == 0 and info.variant & 4
+    assert ws[19] == 4096 and ws[22] * 4 == (plan_ref.int_workspace_ints(cfgd) * 4 + 255) // 256 * 256
+    assert fi.int_workspace_bytes(cfg) == ws[22] * 4 + 4096 * 64 * 8
+
+
+@pytest.mark.parametrize("case", ["long", "lq_gt_lkv", "theta", "scale", "negative"])
+def test_plan_rejects_bad_rope(case):
+    kv = np.array([100, 3000]) if case == "long" else np.array([100, 10])
+    qo = np.array([1, 20]) if case == "lq_gt_lkv" else np.array([1, 2])
+    kvp, lpl = workloads._pages_for(kv, 16)
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    kw = dict(rope_max_positions=2048)
+    if case == "theta":
+        kw["rope_theta"] = 0.0
+    elif case == "scale":
+        kw["rope_scale"] = -1.0
+    elif case == "negative":
+        kw["rope_max_positions"] = -5
+    cfg, cfgd = _cfg(**kw)
+    kvi = np.arange(int(kvp[-1]), dtype=np.int32)
+    st, ws, _ = fi.plan_host(cfg, qop, kvp, kvi, lpl, 8, 2, 128, 16, 1)
+    assert st == 1 and ws is None
+    st_p, _, _ = plan_ref.make_plan(cfgd, qop, kvp, kvi, lpl, 8, 2, 128, 16, 1, 0)
+    assert st_p == 1
 
 
 @pytest.mark.parametrize("field,value", [("window_left", -2), ("sink_tokens", -1), ("logits_soft_cap", -1.0),
