@@ -91,6 +91,20 @@ __global__ void rope_table_kernel(float2* table, int64_t entries, double theta, 
   table[idx] = make_float2(float(cs), float(sn));
 }
 
+template <typename T>
+cudaError_t launch_variant(const RunParams& p, int num_ctas, int variant, cudaStream_t s) {
+  switch (variant & 7) {
+    case 0: return launch_run<T, false, false, false>(p, num_ctas, s);
+    case 1: return launch_run<T, true, false, false>(p, num_ctas, s);
+    case 2: return launch_run<T, false, true, false>(p, num_ctas, s);
+    case 3: return launch_run<T, true, true, false>(p, num_ctas, s);
+    case 4: return launch_run<T, false, false, true>(p, num_ctas, s);
+    case 5: return launch_run<T, true, false, true>(p, num_ctas, s);
+    case 6: return launch_run<T, false, true, true>(p, num_ctas, s);
+    default: return launch_run<T, true, true, true>(p, num_ctas, s);
+  }
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool stride_ok(int64_t elems) { return elems > 0 && (elems * 2) % 16 == 0; }
 
@@ -256,20 +270,9 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The plan's variant picks the instantiation: bit 0 logits soft-cap, bit 1
-  // sliding window / sink mask; the plain kernel carries neither.
-  const bool capped = (info->variant & 1) != 0, masked = (info->variant & 2) != 0;
-  cudaError_t e;
-  if (dtype == FI_BF16) {
-    e = capped ? (masked ? launch_run<__nv_bfloat16, true, true>(p, info->num_ctas, s)
-                         : launch_run<__nv_bfloat16, true, false>(p, info->num_ctas, s))
-               : (masked ? launch_run<__nv_bfloat16, false, true>(p, info->num_ctas, s)
-                         : launch_run<__nv_bfloat16, false, false>(p, info->num_ctas, s));
-  } else {
-    e = capped ? (masked ? launch_run<__half, true, true>(p, info->num_ctas, s)
-                         : launch_run<__half, true, false>(p, info->num_ctas, s))
-               : (masked ? launch_run<__half, false, true>(p, info->num_ctas, s)
-                         : launch_run<__half, false, false>(p, info->num_ctas, s));
-  }
+  // sliding window / sink mask, bit 2 RoPE; the plain kernel carries none.
+  const cudaError_t e = dtype == FI_BF16 ? launch_variant<__nv_bfloat16>(p, info->num_ctas, info->variant, s)
+                                         : launch_variant<__half>(p, info->num_ctas, info->variant, s);
   return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 

@@ -48,6 +48,7 @@ constexpr int kRegsSoftmax = 192;
 static_assert(kRegsLoader * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads, "register split exceeds the launch");
 constexpr int kMmaWarp = 1;
 constexpr int kVWarp = 2;              // loads V tiles; warp 0 loads Q and K tiles
+constexpr int kRopeWarp = 3;           // RoPE: rotates the Q and K tiles in shared memory
 
 struct RunParams {
   CUtensorMap tm_q;  // [q tokens, Hq, d] boxes of (64 dims, G heads, 128/G tokens), 128-byte swizzle
@@ -103,6 +104,8 @@ struct alignas(1024) RunSmem {
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];   // [ring stage]
   uint64_t s_full[2], o_ready[2], o_free[2];  // [M tile of the item]
   uint64_t p_full[2][2];                      // [M tile][P of KV tokens 0..63, 64..127]
+  uint64_t rot[kStages];                      // RoPE, decode: stage rotated (after full[])
+  uint64_t q_rot, k_rot[2];                   // RoPE, prefill: Q tiles / K ring stage rotated
   uint32_t tmem_base;
   volatile int abort;  // set by the role whose bounded wait ran out
   int merge_last;
@@ -121,6 +124,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory of the run kernel exceeds
 struct Variant {
   int32_t window_left, sink;
   float cap_a, cap_b;
+  const float2* rope_table;  // RoPE: (cos, sin)[position][64 pairs], or null
 };
 
 // Soft-capped log2-domain logit from the plain one, by the identity

@@ -20,6 +20,8 @@
 //    fp32 partial state, and the CTA that finishes the last chunk of a split
 //    unit merges the unit's partials in chunk order (no inter-CTA waits).
 #pragma once
+#include <type_traits>
+
 #include "attention.cuh"
 #include "tc.cuh"
 
@@ -205,7 +207,91 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
 }
 
-template <typename T, bool kCap, bool kMask>
+template <typename T>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 u;
+  u.x = Elem<T>::from_float2(f[0], f[1]);
+  u.y = Elem<T>::from_float2(f[2], f[3]);
+  u.z = Elem<T>::from_float2(f[4], f[5]);
+  u.w = Elem<T>::from_float2(f[6], f[7]);
+  return u;
+}
+
+// RoPE of 8 dim pairs in 16-bit storage: lo holds dims i..i+7 of the first
+// half of a head, hi dims i+64..i+71; cs the (cos, sin) of their 8 angles.
+// x_i' = x_i cos - x_{i+64} sin, x_{i+64}' = x_{i+64} cos + x_i sin, in fp32,
+// rounded once to fp16 whatever the input type: fp16 keeps 11 significant
+// bits where bf16 keeps 8, and the rotated q and k meet only each other
+// (S = q.k), so the score does not carry a bf16 rounding of the rotation.
+// Rotated values must stay inside the fp16 range (|x| < 65504).
+template <typename T>
+__device__ __forceinline__ void rope_pairs8(uint4& lo, uint4& hi, const float2* __restrict__ cs) {
+  float a[8], b[8], cw[8], sw[8];
+  unpack8<T>(lo, a);
+  unpack8<T>(hi, b);
+  const float4* c4 = reinterpret_cast<const float4*>(cs);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 t = __ldg(c4 + k);
+    cw[2 * k] = t.x;
+    sw[2 * k] = t.y;
+    cw[2 * k + 1] = t.z;
+    sw[2 * k + 1] = t.w;
+  }
+  float ra[8], rb[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ra[e] = fmaf(a[e], cw[e], -b[e] * sw[e]);
+    rb[e] = fmaf(b[e], cw[e], a[e] * sw[e]);
+  }
+  lo = pack8<__half>(ra);
+  hi = pack8<__half>(rb);
+}
+
+// Decode phase with RoPE: warps 1..3 (idle otherwise) walk the producer's
+// stage sequence, rotate every landed K stage in shared memory (task = one
+// token and one 8-dim chunk of each half; the rotated keys are fp16) and
+// release it to the consumers on rot[]; the consumers wait on rot[] instead
+// of full[] and read the keys as fp16.  Tokens past the
+// chunk end are left alone (they are masked, and their positions may lie
+// past the table).
+template <typename T>
+__device__ void rope_decode(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
+                            const Variant& var) {
+  const int rt = threadIdx.x - 32;  // 0..95
+  const int lane = threadIdx.x & 31;
+  uint32_t it = 0;
+  for (int32_t i = item_begin; i < item_end; ++i) {
+    const Item item = load_item(p.iws, off_items, i);
+    const int nrows = item.row1 - item.row0;
+    const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
+    const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
+    for (int pass = 0; pass < passes; ++pass) {
+      for (int st = 0; st < nst; ++st, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!warp_wait(&sm.full[s], ph, &sm.abort)) continue;
+        const int j0 = item.kv0 + st * kStageTokens;
+        for (int task = rt; task < kStageTokens * 8; task += 96) {
+          const int tok = task >> 3, c = task & 7;
+          const int pos = j0 + tok;
+          if (pos >= item.kv1) continue;
+          uint4* plo = reinterpret_cast<uint4*>(&sm.dec.k[s][tok][8 * c]);
+          uint4* phi = reinterpret_cast<uint4*>(&sm.dec.k[s][tok][64 + 8 * c]);
+          uint4 lo = *plo, hi = *phi;
+          rope_pairs8<T>(lo, hi, var.rope_table + int64_t(pos) * FI_ROPE_PAIRS + 8 * c);
+          *plo = lo;
+          *phi = hi;
+        }
+        fence_proxy_async_smem();  // before the stage's next TMA write
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.rot[s]);
+      }
+    }
+  }
+}
+
+template <typename T, bool kCap, bool kMask, bool kRope>
 __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
                         int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, const Variant var) {
   const int cw = (threadIdx.x >> 5) - kFirstConsumerWarp;  // consumer warp 0..7
@@ -261,6 +347,30 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
         }
         if (r == my_row) lim_mine = lim;
       }
+      if (kRope) {
+        // Rotate the query rows: this lane holds dims 8L..8L+7, the lane L^8
+        // of the same half-warp the other member of each pair.
+        const int f0 = (L & 7) * 8;
+        const float sgn = L < 8 ? -1.f : 1.f;
+#pragma unroll
+        for (int r = 0; r < kRowsPerGroup; ++r) {
+          float2 pq[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            pq[c] = make_float2(__shfl_xor_sync(0xffffffffu, q[r][c].x, 8), __shfl_xor_sync(0xffffffffu, q[r][c].y, 8));
+          const int prow = prow0 + g * kRowsPerGroup + r;
+          if (prow < nrows) {
+            const int t = (item.row0 + prow) / G;
+            const float4* cs = reinterpret_cast<const float4*>(
+                var.rope_table + int64_t(rq.kv_len - rq.qo_len + t) * FI_ROPE_PAIRS + f0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float4 w = __ldg(cs + c);  // (cos, sin) of dims 2c and 2c+1 of the lane
+              q[r][c] = make_float2(fmaf(q[r][c].x, w.x, sgn * pq[c].x * w.y), fmaf(q[r][c].y, w.z, sgn * pq[c].y * w.w));
+            }
+          }
+        }
+      }
       // With a window, key j of the chunk is visible to this lane's row iff
       // (unsigned)(j - lo_mine) < vis_cnt or j < sink (one range compare).
       const unsigned vis_cnt = kMask ? unsigned(max(0, min(lim_mine, item.kv1 - 1) + 1 - lo_mine)) : 0u;
@@ -275,7 +385,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
       for (int st = 0; st < nst; ++st, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        const bool ok = mbar_wait_bounded(&sm.full[s], ph, &sm.abort);
+        const bool ok = mbar_wait_bounded(kRope ? &sm.rot[s] : &sm.full[s], ph, &sm.abort);
         if (ok && !sm.abort) {
           const int j0 = item.kv0 + st * kStageTokens;
           for (int blk = 0; blk < blocks; ++blk) {
@@ -285,7 +395,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
               const int tok = hw + (blk * kTokBlock + u) * nhw;
               const uint4 kv = *reinterpret_cast<const uint4*>(&sm.dec.k[s][tok][L * 8]);
               float2 f[4];
-              unpack4x2<T>(kv, f);
+              unpack4x2<std::conditional_t<kRope, __half, T>>(kv, f);  // rotated keys are fp16
               float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
@@ -441,7 +551,7 @@ __device__ __forceinline__ int32_t first_decode_item(const RunParams& p, int32_t
   return i;
 }
 
-template <typename T, bool kCap, bool kMask>
+template <typename T, bool kCap, bool kMask, bool kRope>
 __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __grid_constant__ RunParams p) {
   // Casting the __shared__ array itself keeps every access below in the
   // shared address space (LDS/STS rather than generic loads).  The swizzled
@@ -476,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   const float cap = __int_as_float(ws_header(iws, FI_H_SOFT_CAP_BITS));
   var.cap_a = cap * 1.4426950408889634f;
   var.cap_b = cap > 0.f ? 2.f / cap : 0.f;
+  var.rope_table = kRope ? reinterpret_cast<const float2*>(iws + ws_header(iws, FI_H_ROPE_TABLE_OFF)) : nullptr;
   const int warp = threadIdx.x >> 5;
   const int32_t mid = p.tc_prefill ? first_decode_item(p, begin, end, off_items, off_req) : begin;
   const bool tc_phase = mid > begin;
@@ -488,6 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
     mbar_init(&sm.drain, 1);
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.q_rot, 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&sm.rot[s], 3);  // warps 1..3
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
@@ -495,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
       mbar_init(&sm.v_empty[s], 1);
       mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.o_ready[s], 1);
+      mbar_init(&sm.k_rot[s], 1);
       mbar_init(&sm.p_full[s][0], 4);  // one arrival per warp of the M tile's softmax warpgroup
       mbar_init(&sm.p_full[s][1], 4);
       mbar_init(&sm.o_free[s], 4);
@@ -523,8 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
       } else if (warp == kVWarp) {
         pf_produce<true>(p, sm, begin, mid, off_items, off_req);
       } else if (warp == kMmaWarp) {
-        pf_mma<T>(p, sm, begin, mid, off_items);
+        pf_mma<T, kRope>(p, sm, begin, mid, off_items);
         __syncwarp();
+      } else if (kRope && warp == kRopeWarp) {
+        pf_rope<T>(p, sm, begin, mid, off_items, off_req, var);
       }
       tc::fence_before_sync();
       named_barrier_sync_unaligned(kPhaseBarrier, kThreads);
@@ -543,7 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   if (warp == 0) {
     produce(p, sm, mid, end, off_items, off_req);
   } else if (warp >= kFirstConsumerWarp) {
-    consume<T, kCap, kMask>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal, var);
+    consume<T, kCap, kMask, kRope>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal, var);
+  } else if (kRope && warp >= 1 && warp <= 3) {
+    rope_decode<T>(p, sm, mid, end, off_items, var);
   }
   tc::fence_before_sync();
   __syncthreads();

@@ -10,10 +10,10 @@ namespace fi {
 
 // The shared-memory opt-in is set once per device and instantiation, so a
 // run enqueued inside a stream capture makes no non-stream CUDA call.
-template <typename T, bool kCap, bool kMask>
+template <typename T, bool kCap, bool kMask, bool kRope>
 cudaError_t launch_run(const RunParams& p, int num_ctas, cudaStream_t stream) {
   static bool configured[kMaxDevices] = {};
-  auto kern = paged_attention_kernel<T, kCap, kMask>;
+  auto kern = paged_attention_kernel<T, kCap, kMask, kRope>;
   const int smem = int(kSmemBytes);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

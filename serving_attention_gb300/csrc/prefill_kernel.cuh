@@ -138,10 +138,67 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
 // warp-uniform so that the issue keeps pace with the tensor pipe.  The MMAs
 // follow the fixed order described at the top of this file, each after a
 // bounded wait for exactly what it reads.
+// RoPE, one warp: rotate each item's Q tiles once they land (positions
+// Lkv - Lq + t of their tokens) and every K tile of the ring (positions kv0 +
+// row), in place in the 128-byte swizzled layout: dims i and i+64 of a row
+// sit at the same chunk position of the two 64-dim halves.  The MMA warp
+// waits on q_rot / k_rot, which follow q_full / k_full; the stages go back to
+// the loaders only through the MMA's commits, after the rotated tiles were
+// read.  Rows past the item's rows or past the chunk end are left alone.
 template <typename T>
+__device__ void pf_rope(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items, int32_t off_req,
+                        const Variant& var) {
+  const int lane = threadIdx.x & 31;
+  const int G = p.group;
+  uint32_t kt = 0, pe = 0;
+  // tile of 128 rows x (two 64-dim halves); pos_of(row) < 0: leave the row
+  auto rotate_tile = [&](uint16_t* lo_half, uint16_t* hi_half, auto pos_of) {
+    for (int task = lane; task < kTileM * 8; task += 32) {
+      const int row = task >> 3, c = task & 7;
+      const int pos = pos_of(row);
+      if (pos < 0) continue;
+      const int pc = c ^ (row & 7);  // swizzled position of 16-byte chunk c
+      uint4* plo = reinterpret_cast<uint4*>(lo_half + row * 64 + pc * 8);
+      uint4* phi = reinterpret_cast<uint4*>(hi_half + row * 64 + pc * 8);
+      uint4 lo = *plo, hi = *phi;
+      rope_pairs8<T>(lo, hi, var.rope_table + int64_t(pos) * FI_ROPE_PAIRS + c * 8);
+      *plo = lo;
+      *phi = hi;
+    }
+    fence_proxy_async_smem();  // the rotated operands are read by the tensor core
+    __syncwarp();
+  };
+  for (int32_t i = b0; i < b1; ++i) {
+    const Item it = load_item(p.iws, off_items, i);
+    const int ntiles = item_kv_tiles(it);
+    if (ntiles == 0) continue;
+    const Request rq = load_request(p.iws, off_req, it.b);
+    const int nrows = it.row1 - it.row0;
+    const int nm = item_m_tiles(it);
+    if (!warp_wait(&sm.q_full, pe & 1, &sm.abort)) break;
+    for (int m = 0; m < nm; ++m)
+      rotate_tile(&sm.pf.q[m][0][0][0], &sm.pf.q[m][1][0][0], [&](int row) {
+        const int prow = m * kTileM + row;
+        return prow < nrows ? rq.kv_len - rq.qo_len + (it.row0 + prow) / G : -1;
+      });
+    if (lane == 0) mbar_arrive(&sm.q_rot);
+    ++pe;
+    for (int j = 0; j < ntiles; ++j, ++kt) {
+      const int st = kt & 1;
+      if (!warp_wait(&sm.k_full[st], (kt >> 1) & 1, &sm.abort)) break;
+      const int k0 = it.kv0 + j * kTileN;
+      rotate_tile(&sm.pf.k[st][0][0][0], &sm.pf.k[st][1][0][0],
+                  [&](int row) { return k0 + row < it.kv1 ? k0 + row : -1; });
+      if (lane == 0) mbar_arrive(&sm.k_rot[st]);
+    }
+  }
+}
+
+template <typename T, bool kRope>
 __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-  constexpr uint32_t idesc_qk = tc::idesc_f16(kBf16, false, kTileM, kTileN);
+  // rotated Q and K (RoPE) are fp16 whatever the input type; P and V keep it
+  constexpr uint32_t idesc_qk = tc::idesc_f16(kBf16 && !kRope, false, kTileM, kTileN);
   constexpr uint32_t idesc_pv = tc::idesc_f16(kBf16, true, kTileM, kHeadDim);
   const int lane = threadIdx.x & 31;
   const uint32_t tmem = sm.tmem_base;
@@ -184,8 +241,10 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
     const int ntiles = item_kv_tiles(it);
     if (ntiles == 0) continue;
     const int nm = item_m_tiles(it);
-    bool ok = warp_wait_all(2, &sm.q_full, pe & 1, &sm.k_full[kt & 1], (kt >> 1) & 1, nullptr, 0, nullptr, 0,
-                            &sm.abort);
+    // with RoPE the operands are read once the rotation warp has released them
+    uint64_t* const q_bar = kRope ? &sm.q_rot : &sm.q_full;
+    uint64_t* const k_bars = kRope ? sm.k_rot : sm.k_full;
+    bool ok = warp_wait_all(2, q_bar, pe & 1, &k_bars[kt & 1], (kt >> 1) & 1, nullptr, 0, nullptr, 0, &sm.abort);
     if (!ok) break;
     tc::fence_after_sync();
     for (int m = 0; m < nm; ++m) issue_s(m, kt & 1);
@@ -207,7 +266,7 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
         const bool kv = m == 0, need_k = kv && more;
         ok = warp_wait_all(4, pb, pp, kv ? &sm.v_full[st] : pb, kv ? (g >> 1) & 1 : pp,
                            j == 0 ? &sm.o_free[m] : pb, j == 0 ? (items_m[m] & 1) ^ 1 : pp,
-                           need_k ? &sm.k_full[st_next] : pb, need_k ? ((g + 1) >> 1) & 1 : pp, &sm.abort);
+                           need_k ? &k_bars[st_next] : pb, need_k ? ((g + 1) >> 1) & 1 : pp, &sm.abort);
         if (!ok) break;
         tc::fence_after_sync();
         issue_pv(m, st, j == 0, 0);

@@ -3,10 +3,10 @@
 
 namespace fi {
 
-template cudaError_t launch_run<__nv_bfloat16, false, false>(const RunParams&, int, cudaStream_t);
+template cudaError_t launch_run<__nv_bfloat16, false, false, false>(const RunParams&, int, cudaStream_t);
 
 cudaError_t run_kernel_occupancy(int* per_sm) {
-  auto kern = paged_attention_kernel<__nv_bfloat16, false, false>;
+  auto kern = paged_attention_kernel<__nv_bfloat16, false, false, false>;
   const int smem = int(kSmemBytes);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kern, kThreads, smem);

@@ -4,8 +4,8 @@
 
 namespace fi {
 
-template cudaError_t launch_run<__nv_bfloat16, true, false>(const RunParams&, int, cudaStream_t);
-template cudaError_t launch_run<__nv_bfloat16, false, true>(const RunParams&, int, cudaStream_t);
-template cudaError_t launch_run<__nv_bfloat16, true, true>(const RunParams&, int, cudaStream_t);
+template cudaError_t launch_run<__nv_bfloat16, true, false, false>(const RunParams&, int, cudaStream_t);
+template cudaError_t launch_run<__nv_bfloat16, false, true, false>(const RunParams&, int, cudaStream_t);
+template cudaError_t launch_run<__nv_bfloat16, true, true, false>(const RunParams&, int, cudaStream_t);
 
 }  // namespace fi

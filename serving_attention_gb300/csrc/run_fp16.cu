@@ -3,6 +3,6 @@
 
 namespace fi {
 
-template cudaError_t launch_run<__half, false, false>(const RunParams&, int, cudaStream_t);
+template cudaError_t launch_run<__half, false, false, false>(const RunParams&, int, cudaStream_t);
 
 }  // namespace fi

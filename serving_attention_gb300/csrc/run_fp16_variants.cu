@@ -4,8 +4,8 @@
 
 namespace fi {
 
-template cudaError_t launch_run<__half, true, false>(const RunParams&, int, cudaStream_t);
-template cudaError_t launch_run<__half, false, true>(const RunParams&, int, cudaStream_t);
-template cudaError_t launch_run<__half, true, true>(const RunParams&, int, cudaStream_t);
+template cudaError_t launch_run<__half, true, false, false>(const RunParams&, int, cudaStream_t);
+template cudaError_t launch_run<__half, false, true, false>(const RunParams&, int, cudaStream_t);
+template cudaError_t launch_run<__half, true, true, false>(const RunParams&, int, cudaStream_t);
 
 }  // namespace fi
