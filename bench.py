@@ -421,7 +421,55 @@ def bench_variants(dev, flush, reps=5):
                              "cost_vs_plain": times["capped"] / times["plain"]}
     del b, o, lse, kvi
     torch.cuda.empty_cache()
+    out["rope"] = bench_rope(dev, flush, reps)
     return out
+
+
+def bench_rope(dev, flush, reps=5):
+    """RoPE on unrotated cached keys: fused into the attention loaders, against
+    the unfused form -- every key rotated into a copy by a separate pass
+    (fi_rope_apply_k: read K, write K), then the plain kernel -- and against
+    the plain kernel alone (no rotation at all)."""
+    import torch
+
+    import serving_attention_gb300 as fi
+    import workloads
+
+    res = {}
+    for name, maker, theta, max_pos in (("llama8b_decode", workloads.llama8b_decode, 500000.0, 32768),
+                                        ("ragged_prefill", workloads.ragged_prefill, 10000.0, 8192)):
+        b = maker(device=dev)
+        kvi = torch.as_tensor(b.kv_indices, device=dev)
+        o = torch.empty_like(b.q)
+        lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
+        k_rot = torch.empty_like(b.k)
+        max_kv = int(b.kv_lens().max())
+        cfg_p = fi.default_plan_config(dev.index)
+        cfg_r = fi.default_plan_config(dev.index, rope_max_positions=max_pos, rope_theta=theta)
+        ws_p, ws_r = fi.Workspace(cfg_p, device=dev), fi.Workspace(cfg_r, device=dev)
+        args = (b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads, 128,
+                b.page_size, b.causal, b.num_pages)
+        info_p, info_r = fi.plan(ws_p, *args), fi.plan(ws_r, *args)
+
+        def fused():
+            fi.run(ws_r, info_r, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+
+        def unfused():
+            fi.rope_apply_k(ws_r, info_r, b.k, k_rot, kvi, max_kv)
+            fi.run(ws_p, info_p, b.q, k_rot, b.v, kvi, o, lse, b.sm_scale)
+
+        def plain():
+            fi.run(ws_p, info_p, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+
+        t = {k: _graph_ms(f, flush, reps) for k, f in (("fused", fused), ("unfused", unfused), ("plain", plain))}
+        assert fi.device_status(ws_r) == 0 and fi.device_status(ws_p) == 0
+        res[name] = {"fused_ms": t["fused"], "unfused_ms": t["unfused"], "plain_ms": t["plain"],
+                     "fusion_speedup": t["unfused"] / t["fused"], "fused_cost_vs_plain": t["fused"] / t["plain"]}
+        del b, o, lse, kvi, k_rot, ws_p, ws_r
+        torch.cuda.empty_cache()
+    res["workload"] = ("cached keys unrotated; llama8b_decode with theta 5e5, ragged_prefill with theta 1e4; "
+                       "unfused = fi_rope_apply_k over every cached key, then the plain kernel")
+    return res
 
 
 def bench_kv_strides(dev, flush, reps=5):

@@ -128,13 +128,29 @@ size_t fi_float_workspace_bytes(const fi_plan_config* cfg, int32_t head_dim);
 /*
  * fi_rope_init -- fill the RoPE cos/sin table of an int workspace made for
  * `cfg` (rope_max_positions > 0): cos and sin of (pos / rope_scale) *
- * rope_theta^(-2i/128) for pos < rope_max_positions and i < 64, computed in
+ * rope_theta^(-2i/128) for pos < max(rope_max_positions, 16) and i < 64, computed in
  * fp64 and stored as fp32.  Once per workspace (and again if the config's
  * RoPE fields change); plans never overwrite the table.  Asynchronous on
  * `stream`.  FI_ERR_INVALID_ARG when the config has no RoPE or a theta or
  * scale <= 0.
  */
 fi_status fi_rope_init(const fi_plan_config* cfg, void* int_workspace_dev, void* stream);
+
+/*
+ * fi_rope_apply_k -- the unfused form: rotate, outside attention, every key
+ * of the plan's requests (key j at position j, the same rotation the fused
+ * kernel applies) from k_in into k_out, both [num_pages, page_size,
+ * num_kv_heads, 128] with their own strides (elements, multiples of 16
+ * bytes) and the plan's page ids; k_out may be k_in.  Output in the cache's
+ * own type.  Uses the plan in int_workspace_dev (request table and RoPE
+ * table: the plan must have been made with RoPE, else FI_ERR_INVALID_ARG);
+ * max_kv_len bounds the requests' KV lengths (keys past it are not rotated).
+ * Asynchronous on `stream`.
+ */
+fi_status fi_rope_apply_k(const fi_plan_info* info, const void* int_workspace_dev, int32_t max_kv_len,
+                          const void* k_in, const int64_t k_in_strides[3], void* k_out,
+                          const int64_t k_out_strides[3], const int32_t* kv_indices_dev, fi_dtype dtype,
+                          void* stream);
 
 /*
  * fi_plan -- build the load-balanced split-KV work list on the host and copy

@@ -60,7 +60,7 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ["fi_default_plan_config", "fi_int_workspace_bytes", "fi_float_workspace_bytes", "fi_plan",
            "fi_plan_host", "fi_batch_paged_attention_run", "fi_batch_paged_attention_run_static_scratch",
-           "fi_merge_states", "fi_get_device_status", "fi_status_string", "fi_rope_init"]
+           "fi_merge_states", "fi_get_device_status", "fi_status_string", "fi_rope_init", "fi_rope_apply_k"]
 
 _lib = None
 
@@ -89,10 +89,11 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
     lib.fi_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, vp]
     lib.fi_get_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.fi_rope_init.argtypes = [cfgp, vp, vp]
+    lib.fi_rope_apply_k.argtypes = [infop, vp, i32, vp, vp, vp, vp, vp, ctypes.c_int, vp]
     lib.fi_status_string.argtypes = [ctypes.c_int]
     lib.fi_status_string.restype = ctypes.c_char_p
     for name in ("fi_default_plan_config", "fi_plan", "fi_plan_host", "fi_batch_paged_attention_run",
-                 "fi_merge_states", "fi_get_device_status", "fi_rope_init"):
+                 "fi_merge_states", "fi_get_device_status", "fi_rope_init", "fi_rope_apply_k"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -255,6 +256,16 @@ def merge_states(v_a, s_a, v_b, s_b, v_out, s_out, stream=None):
     st = lib.fi_merge_states(v_a.data_ptr(), s_a.data_ptr(), v_b.data_ptr(), s_b.data_ptr(), v_out.data_ptr(),
                              s_out.data_ptr(), rows, heads, d, _dtype_code(v_a), _stream_ptr(stream))
     _check(st, "fi_merge_states")
+
+
+def rope_apply_k(ws: Workspace, info: PlanInfo, k_in, k_out, kv_indices, max_kv_len: int, stream=None):
+    """Unfused RoPE: rotate the keys of the plan's requests from k_in into k_out
+    ([pages, page_size, Hkv, 128], same dtype; k_out may be k_in)."""
+    ks_in = (ctypes.c_int64 * 3)(*k_in.stride()[:3])
+    ks_out = (ctypes.c_int64 * 3)(*k_out.stride()[:3])
+    _check(load().fi_rope_apply_k(ctypes.byref(info), ws.int_ws.data_ptr(), int(max_kv_len), k_in.data_ptr(), ks_in,
+                                  k_out.data_ptr(), ks_out, kv_indices.data_ptr(), _dtype_code(k_in),
+                                  _stream_ptr(stream)), "fi_rope_apply_k")
 
 
 def device_status(ws: Workspace, stream=None) -> int:

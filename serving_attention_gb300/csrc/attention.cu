@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "../../include/fi.h"
+#include "attention_kernel.cuh"
 #include "launch.h"
 #include "workspace.h"
 
@@ -89,6 +90,39 @@ __global__ void rope_table_kernel(float2* table, int64_t entries, double theta, 
   double sn, cs;
   sincos(double(pos) * inv_scale * freq, &sn, &cs);
   table[idx] = make_float2(float(cs), float(sn));
+}
+
+// Standalone RoPE of the keys of a plan's requests (key j at position j),
+// from k_in to k_out (same page ids; they may be the same cache).  One block
+// per request and 64-key chunk; a task is one key, one KV head and one
+// 8-dim chunk of each half.
+template <typename T>
+__global__ void __launch_bounds__(256) rope_apply_k_kernel(const int32_t* __restrict__ iws, const uint16_t* k_in,
+                                                           int64_t ki0, int64_t ki1, int64_t ki2, uint16_t* k_out,
+                                                           int64_t ko0, int64_t ko1, int64_t ko2,
+                                                           const int32_t* __restrict__ kv_indices, int log2_page,
+                                                           int num_kv_heads) {
+  const int b = blockIdx.y;
+  if (b >= __ldg(iws + FI_H_BATCH)) return;
+  const Request rq = load_request(iws, __ldg(iws + FI_H_OFF_REQUESTS), b);
+  const int j0 = blockIdx.x * 64;
+  if (j0 >= rq.kv_len) return;
+  const float2* table = reinterpret_cast<const float2*>(iws + __ldg(iws + FI_H_ROPE_TABLE_OFF));
+  const int P = 1 << log2_page;
+  const int tasks = 64 * num_kv_heads * 8;
+  for (int task = threadIdx.x; task < tasks; task += blockDim.x) {
+    const int key = task / (num_kv_heads * 8), rem = task - key * (num_kv_heads * 8);
+    const int h = rem >> 3, c = rem & 7;
+    const int j = j0 + key;
+    if (j >= rq.kv_len) continue;
+    const int64_t page = __ldg(kv_indices + rq.page_start + (j >> log2_page));
+    const int slot = j & (P - 1);
+    const int64_t ib = page * ki0 + slot * ki1 + h * ki2 + 8 * c, ob = page * ko0 + slot * ko1 + h * ko2 + 8 * c;
+    uint4 lo = *reinterpret_cast<const uint4*>(k_in + ib), hi = *reinterpret_cast<const uint4*>(k_in + ib + 64);
+    rope_pairs8<T, T>(lo, hi, table + int64_t(j) * FI_ROPE_PAIRS + 8 * c);
+    *reinterpret_cast<uint4*>(k_out + ob) = lo;
+    *reinterpret_cast<uint4*>(k_out + ob + 64) = hi;
+  }
 }
 
 template <typename T>
@@ -283,10 +317,42 @@ extern "C" fi_status fi_rope_init(const fi_plan_config* cfg, void* int_workspace
   if (!aligned16(int_workspace_dev)) return FI_ERR_ALIGNMENT;
   float2* table = reinterpret_cast<float2*>(static_cast<char*>(int_workspace_dev) +
                                             fi_rope_table_offset(plan_capacity_ints(cfg)));
-  const int64_t entries = int64_t(cfg->rope_max_positions) * FI_ROPE_PAIRS;
+  const int64_t entries = fi_rope_table_rows(cfg->rope_max_positions) * FI_ROPE_PAIRS;
   const int64_t blocks = (entries + 255) / 256;
   rope_table_kernel<<<unsigned(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       table, entries, double(cfg->rope_theta), 1.0 / double(cfg->rope_scale));
+  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
+extern "C" fi_status fi_rope_apply_k(const fi_plan_info* info, const void* int_workspace_dev, int32_t max_kv_len,
+                                     const void* k_in, const int64_t k_in_strides[3], void* k_out,
+                                     const int64_t k_out_strides[3], const int32_t* kv_indices_dev, fi_dtype dtype,
+                                     void* stream) {
+  if (!info || !int_workspace_dev || !k_in || !k_out || !k_in_strides || !k_out_strides || !kv_indices_dev ||
+      max_kv_len < 0)
+    return FI_ERR_INVALID_ARG;
+  if (!(info->variant & 4)) return FI_ERR_INVALID_ARG;  // the plan carries no RoPE table
+  if (info->head_dim != kHeadDim) return FI_ERR_UNSUPPORTED;
+  if (dtype != FI_FP16 && dtype != FI_BF16) return FI_ERR_UNSUPPORTED;
+  if (!aligned16(k_in) || !aligned16(k_out)) return FI_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i)
+    if (!stride_ok(k_in_strides[i]) || !stride_ok(k_out_strides[i])) return FI_ERR_ALIGNMENT;
+  if (info->batch == 0 || max_kv_len == 0) return FI_OK;
+  int lp = 0;
+  while ((1 << lp) < info->page_size) ++lp;
+  const dim3 grid(unsigned((max_kv_len + 63) / 64), unsigned(info->batch));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int32_t* iws = static_cast<const int32_t*>(int_workspace_dev);
+  const uint16_t* ki = static_cast<const uint16_t*>(k_in);
+  uint16_t* ko = static_cast<uint16_t*>(k_out);
+  if (dtype == FI_BF16)
+    rope_apply_k_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(iws, ki, k_in_strides[0], k_in_strides[1], k_in_strides[2],
+                                                            ko, k_out_strides[0], k_out_strides[1], k_out_strides[2],
+                                                            kv_indices_dev, lp, info->num_kv_heads);
+  else
+    rope_apply_k_kernel<__half><<<grid, 256, 0, s>>>(iws, ki, k_in_strides[0], k_in_strides[1], k_in_strides[2], ko,
+                                                     k_out_strides[0], k_out_strides[1], k_out_strides[2],
+                                                     kv_indices_dev, lp, info->num_kv_heads);
   return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 

@@ -48,7 +48,6 @@ constexpr int kRegsSoftmax = 192;
 static_assert(kRegsLoader * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads, "register split exceeds the launch");
 constexpr int kMmaWarp = 1;
 constexpr int kVWarp = 2;              // loads V tiles; warp 0 loads Q and K tiles
-constexpr int kRopeWarp = 3;           // RoPE: rotates the Q and K tiles in shared memory
 
 struct RunParams {
   CUtensorMap tm_q;  // [q tokens, Hq, d] boxes of (64 dims, G heads, 128/G tokens), 128-byte swizzle

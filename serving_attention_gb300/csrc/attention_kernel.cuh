@@ -223,29 +223,49 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 // rounded once to fp16 whatever the input type: fp16 keeps 11 significant
 // bits where bf16 keeps 8, and the rotated q and k meet only each other
 // (S = q.k), so the score does not carry a bf16 rounding of the rotation.
-// Rotated values must stay inside the fp16 range (|x| < 65504).
-template <typename T>
-__device__ __forceinline__ void rope_pairs8(uint4& lo, uint4& hi, const float2* __restrict__ cs) {
-  float a[8], b[8], cw[8], sw[8];
+// Rotated values must stay inside the fp16 range (|x| < 65504).  (TOut
+// other than fp16: the standalone rotation utility, which writes the cache's
+// own type.)
+template <typename T, typename TOut = __half>
+__device__ __forceinline__ void rope_rotate8(uint4& lo, uint4& hi, const float2 (&cs)[8]) {
+  float a[8], b[8];
   unpack8<T>(lo, a);
   unpack8<T>(hi, b);
-  const float4* c4 = reinterpret_cast<const float4*>(cs);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float4 t = __ldg(c4 + k);
-    cw[2 * k] = t.x;
-    sw[2 * k] = t.y;
-    cw[2 * k + 1] = t.z;
-    sw[2 * k + 1] = t.w;
-  }
   float ra[8], rb[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    ra[e] = fmaf(a[e], cw[e], -b[e] * sw[e]);
-    rb[e] = fmaf(b[e], cw[e], a[e] * sw[e]);
+    ra[e] = fmaf(a[e], cs[e].x, -b[e] * cs[e].y);
+    rb[e] = fmaf(b[e], cs[e].x, a[e] * cs[e].y);
   }
-  lo = pack8<__half>(ra);
-  hi = pack8<__half>(rb);
+  lo = pack8<TOut>(ra);
+  hi = pack8<TOut>(rb);
+}
+
+// (cos, sin) of 8 consecutive frequencies of one position: 64 bytes of the table.
+__device__ __forceinline__ void rope_load8(float2 (&cs)[8], const float2* __restrict__ p) {
+  const float4* p4 = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 t = __ldg(p4 + k);
+    cs[2 * k] = make_float2(t.x, t.y);
+    cs[2 * k + 1] = make_float2(t.z, t.w);
+  }
+}
+
+// Angles of the next position of a walk with a fixed stride: multiply by the
+// stride's (cos, sin) (angle addition), so a walk needs only its first row
+// and the stride's row from the table; fp32 drift over 32 steps is ~1e-6.
+__device__ __forceinline__ void rope_advance8(float2 (&cs)[8], const float2 (&step)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    cs[e] = make_float2(fmaf(cs[e].x, step[e].x, -cs[e].y * step[e].y), fmaf(cs[e].y, step[e].x, cs[e].x * step[e].y));
+}
+
+template <typename T, typename TOut = __half>
+__device__ __forceinline__ void rope_pairs8(uint4& lo, uint4& hi, const float2* __restrict__ cs) {
+  float2 c[8];
+  rope_load8(c, cs);
+  rope_rotate8<T, TOut>(lo, hi, c);
 }
 
 // Decode phase with RoPE: warps 1..3 (idle otherwise) walk the producer's
@@ -260,6 +280,12 @@ __device__ void rope_decode(const RunParams& p, RunSmem& sm, int32_t item_begin,
                             const Variant& var) {
   const int rt = threadIdx.x - 32;  // 0..95
   const int lane = threadIdx.x & 31;
+  // thread = (8-frequency chunk c, token group g): tokens g, g+12, g+24, ...
+  // of each stage, one walk with stride 12 per stage
+  constexpr int kGroups = 12;
+  const int c = rt & 7, g = rt >> 3;
+  float2 step[8];
+  rope_load8(step, var.rope_table + kGroups * FI_ROPE_PAIRS + 8 * c);
   uint32_t it = 0;
   for (int32_t i = item_begin; i < item_end; ++i) {
     const Item item = load_item(p.iws, off_items, i);
@@ -270,18 +296,34 @@ __device__ void rope_decode(const RunParams& p, RunSmem& sm, int32_t item_begin,
       for (int st = 0; st < nst; ++st, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        if (!warp_wait(&sm.full[s], ph, &sm.abort)) continue;
         const int j0 = item.kv0 + st * kStageTokens;
-        for (int task = rt; task < kStageTokens * 8; task += 96) {
-          const int tok = task >> 3, c = task & 7;
-          const int pos = j0 + tok;
-          if (pos >= item.kv1) continue;
+        float2 cs[8];
+        if (j0 + g < item.kv1) rope_load8(cs, var.rope_table + int64_t(j0 + g) * FI_ROPE_PAIRS + 8 * c);
+        if (!warp_wait(&sm.full[s], ph, &sm.abort)) continue;
+        // two tokens of the walk per iteration (independent loads and math)
+        for (int tok = g; tok < kStageTokens && j0 + tok < item.kv1; tok += 2 * kGroups) {
+          const int tok2 = tok + kGroups;
+          const bool second = tok2 < kStageTokens && j0 + tok2 < item.kv1;
+          float2 cs2[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cs2[e] = cs[e];
+          rope_advance8(cs2, step);
           uint4* plo = reinterpret_cast<uint4*>(&sm.dec.k[s][tok][8 * c]);
           uint4* phi = reinterpret_cast<uint4*>(&sm.dec.k[s][tok][64 + 8 * c]);
-          uint4 lo = *plo, hi = *phi;
-          rope_pairs8<T>(lo, hi, var.rope_table + int64_t(pos) * FI_ROPE_PAIRS + 8 * c);
+          uint4* plo2 = reinterpret_cast<uint4*>(&sm.dec.k[s][second ? tok2 : tok][8 * c]);
+          uint4* phi2 = reinterpret_cast<uint4*>(&sm.dec.k[s][second ? tok2 : tok][64 + 8 * c]);
+          uint4 lo = *plo, hi = *phi, lo2 = *plo2, hi2 = *phi2;
+          rope_rotate8<T>(lo, hi, cs);
+          if (second) rope_rotate8<T>(lo2, hi2, cs2);
           *plo = lo;
           *phi = hi;
+          if (second) {
+            *plo2 = lo2;
+            *phi2 = hi2;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cs[e] = cs2[e];
+          rope_advance8(cs, step);
         }
         fence_proxy_async_smem();  // before the stage's next TMA write
         __syncwarp();
@@ -599,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
     mbar_init(&sm.drain, 1);
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
-    mbar_init(&sm.q_rot, 1);
+    mbar_init(&sm.q_rot, 2);
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.rot[s], 3);  // warps 1..3
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.k_full[s], 1);
@@ -608,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
       mbar_init(&sm.v_empty[s], 1);
       mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.o_ready[s], 1);
-      mbar_init(&sm.k_rot[s], 1);
+      mbar_init(&sm.k_rot[s], 2);  // the two rotation warps
       mbar_init(&sm.p_full[s][0], 4);  // one arrival per warp of the M tile's softmax warpgroup
       mbar_init(&sm.p_full[s][1], 4);
       mbar_init(&sm.o_free[s], 4);
@@ -633,14 +675,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
     if (warp < kSoftmaxWarp0) {
       tc::setmaxnreg_dec<kRegsLoader>();
       if (warp == 0) {
-        pf_produce<false>(p, sm, begin, mid, off_items, off_req);
-      } else if (warp == kVWarp) {
-        pf_produce<true>(p, sm, begin, mid, off_items, off_req);
+        pf_produce<kRope ? kProduceQKV : kProduceQK>(p, sm, begin, mid, off_items, off_req);
       } else if (warp == kMmaWarp) {
         pf_mma<T, kRope>(p, sm, begin, mid, off_items);
         __syncwarp();
-      } else if (kRope && warp == kRopeWarp) {
-        pf_rope<T>(p, sm, begin, mid, off_items, off_req, var);
+      } else if (kRope) {
+        pf_rope<T>(p, sm, begin, mid, off_items, off_req, var);  // warps 2 and 3
+      } else if (warp == kVWarp) {
+        pf_produce<kProduceV>(p, sm, begin, mid, off_items, off_req);
       }
       tc::fence_before_sync();
       named_barrier_sync_unaligned(kPhaseBarrier, kThreads);

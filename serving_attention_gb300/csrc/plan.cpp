@@ -81,7 +81,7 @@ extern "C" size_t fi_int_workspace_bytes(const fi_plan_config* cfg) {
   if (!cfg) return 0;
   const int64_t plan_ints = fi::plan_capacity_ints(cfg);
   if (cfg->rope_max_positions <= 0) return size_t(plan_ints) * 4;
-  return size_t(fi_rope_table_offset(plan_ints) + int64_t(cfg->rope_max_positions) * FI_ROPE_PAIRS * 8);
+  return size_t(fi_rope_table_offset(plan_ints) + fi_rope_table_rows(cfg->rope_max_positions) * FI_ROPE_PAIRS * 8);
 }
 
 extern "C" size_t fi_float_workspace_bytes(const fi_plan_config* cfg, int32_t head_dim) {

@@ -65,6 +65,12 @@ enum {
 
 #define FI_ROPE_PAIRS 64  // dims i and i + 64 of head_dim 128 form a rotated pair
 
+// Rows of the RoPE table: every position below rope_max_positions, and at
+// least 16 (the kernels read the rows of their walk strides, 4 and 12).
+static inline int64_t fi_rope_table_rows(int32_t rope_max_positions) {
+  return rope_max_positions > 16 ? rope_max_positions : 16;
+}
+
 // Byte offset of the RoPE table in an int workspace whose plan region holds
 // `plan_ints` int32 (256-byte aligned).
 static inline int64_t fi_rope_table_offset(int64_t plan_ints) { return (plan_ints * 4 + 255) / 256 * 256; }

@@ -52,24 +52,44 @@ constexpr uint32_t kKVBytes = 2u * kTileN * 64u * 2u;
 __device__ __forceinline__ int item_kv_tiles(const Item& it) { return (it.kv1 - it.kv0 + kTileN - 1) / kTileN; }
 __device__ __forceinline__ int item_m_tiles(const Item& it) { return it.row1 - it.row0 > kTileM ? 2 : 1; }
 
-// Producers.  Warp 0 loads Q and K, warp 2 loads V; each walks the same tile
-// stream and waits only on its own ring.  The page ids of the next KV tile
-// are loaded while the current tile's stage is awaited.
-template <bool kIsV>
+// Producers.  Warp 0 loads Q and K, warp 2 loads V (kProduceQK, kProduceV);
+// each walks the same tile stream and waits only on its own ring.  With RoPE
+// warp 0 loads all three (kProduceQKV) so that warp 2 is free to rotate.  The
+// page ids of the next KV tile are loaded while the current tile's stages
+// are awaited.
+enum { kProduceQK = 0, kProduceV = 1, kProduceQKV = 2 };
+
+template <int kMode>
 __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items,
                            int32_t off_req) {
+  constexpr bool kQK = kMode != kProduceV, kV = kMode != kProduceQK;
   const int lane = threadIdx.x & 31;
   const int G = p.group, lp = p.log2_page, P = p.page_size;
   const int ppt = kTileN >> lp;  // pages per KV tile
-  const CUtensorMap* map = kIsV ? &p.tm_v : &p.tm_k;
-  uint64_t* full = kIsV ? sm.v_full : sm.k_full;
-  uint64_t* empty = kIsV ? sm.v_empty : sm.k_empty;
   if (lane == 0) {
-    if (!kIsV) tc::prefetch_tensormap(&p.tm_q);
-    tc::prefetch_tensormap(map);
+    if (kQK) {
+      tc::prefetch_tensormap(&p.tm_q);
+      tc::prefetch_tensormap(&p.tm_k);
+    }
+    if (kV) tc::prefetch_tensormap(&p.tm_v);
   }
   uint32_t kt = 0, pe = 0;
-  int q_armed = -1, armed[2] = {-1, -1};  // parity of the last armed phase
+  int q_armed = -1, k_armed[2] = {-1, -1}, v_armed[2] = {-1, -1};  // parity of the last armed phase
+  // One ring stage of K or V for the pages cur[] of the tile (one 4-D box per
+  // page and 64-dim half).
+  auto load_stage = [&](const CUtensorMap* map, uint64_t* full, uint16_t (*buf)[kTileN][64], int st, int hk,
+                        const int32_t (&cur)[4]) {
+    if (lane == 0) mbar_arrive_expect_tx(&full[st], kKVBytes);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = lane + 32 * u;
+      if (e < ppt) {
+        tc::tma_load_4d(&buf[0][e * P][0], map, &full[st], 0, hk, 0, cur[u]);
+        tc::tma_load_4d(&buf[1][e * P][0], map, &full[st], 64, hk, 0, cur[u]);
+      }
+    }
+  };
   for (int32_t i = b0; i < b1; ++i) {
     const Item it = load_item(p.iws, off_items, i);
     const Request rq = load_request(p.iws, off_req, it.b);
@@ -77,7 +97,7 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
     if (ntiles == 0) continue;
     const int npages = (rq.kv_len + P - 1) >> lp;
     const int32_t* pages = p.kv_indices + rq.page_start;
-    if (!kIsV) {
+    if (kQK) {
       const int nm = item_m_tiles(it);
       if (warp_wait(&sm.q_empty, (pe & 1) ^ 1, &sm.abort) && lane == 0) {
         mbar_arrive_expect_tx(&sm.q_full, nm * kQTileBytes);
@@ -106,20 +126,13 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
 #pragma unroll
       for (int u = 0; u < 4; ++u) cur[u] = pid[u];
       if (j + 1 < ntiles) fetch_ids(j + 1);
-      if (warp_wait(&empty[st], ph ^ 1, &sm.abort)) {
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], kKVBytes);
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = lane + 32 * u;
-          if (e < ppt) {
-            uint16_t* lo = kIsV ? &sm.pf.v[st][0][e * P][0] : &sm.pf.k[st][0][e * P][0];
-            uint16_t* hi = kIsV ? &sm.pf.v[st][1][e * P][0] : &sm.pf.k[st][1][e * P][0];
-            tc::tma_load_4d(lo, map, &full[st], 0, it.hk, 0, cur[u]);
-            tc::tma_load_4d(hi, map, &full[st], 64, it.hk, 0, cur[u]);
-          }
-        }
-        armed[st] = ph;
+      if (kQK && warp_wait(&sm.k_empty[st], ph ^ 1, &sm.abort)) {
+        load_stage(&p.tm_k, sm.k_full, sm.pf.k[st], st, it.hk, cur);
+        k_armed[st] = ph;
+      }
+      if (kV && warp_wait(&sm.v_empty[st], ph ^ 1, &sm.abort)) {
+        load_stage(&p.tm_v, sm.v_full, sm.pf.v[st], st, it.hk, cur);
+        v_armed[st] = ph;
       }
     }
     ++pe;
@@ -127,47 +140,61 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
   // Every load this warp armed has landed before the CTA moves on.
   if (lane == 0) {
     if (q_armed >= 0) mbar_wait_drain(&sm.q_full, q_armed);
-    for (int s = 0; s < 2; ++s)
-      if (armed[s] >= 0) mbar_wait_drain(&full[s], armed[s]);
+    for (int s = 0; s < 2; ++s) {
+      if (k_armed[s] >= 0) mbar_wait_drain(&sm.k_full[s], k_armed[s]);
+      if (v_armed[s] >= 0) mbar_wait_drain(&sm.v_full[s], v_armed[s]);
+    }
   }
   __syncwarp();
 }
 
-// Warp 1, converged: every lane walks the items and waits; one elected lane
-// issues each MMA and commit (the tc::*_warp forms), which keeps the operands
-// warp-uniform so that the issue keeps pace with the tensor pipe.  The MMAs
-// follow the fixed order described at the top of this file, each after a
-// bounded wait for exactly what it reads.
-// RoPE, one warp: rotate each item's Q tiles once they land (positions
-// Lkv - Lq + t of their tokens) and every K tile of the ring (positions kv0 +
-// row), in place in the 128-byte swizzled layout: dims i and i+64 of a row
-// sit at the same chunk position of the two 64-dim halves.  The MMA warp
-// waits on q_rot / k_rot, which follow q_full / k_full; the stages go back to
-// the loaders only through the MMA's commits, after the rotated tiles were
-// read.  Rows past the item's rows or past the chunk end are left alone.
 template <typename T>
 __device__ void pf_rope(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items, int32_t off_req,
                         const Variant& var) {
   const int lane = threadIdx.x & 31;
   const int G = p.group;
-  uint32_t kt = 0, pe = 0;
-  // tile of 128 rows x (two 64-dim halves); pos_of(row) < 0: leave the row
-  auto rotate_tile = [&](uint16_t* lo_half, uint16_t* hi_half, auto pos_of) {
-    for (int task = lane; task < kTileM * 8; task += 32) {
-      const int row = task >> 3, c = task & 7;
-      const int pos = pos_of(row);
-      if (pos < 0) continue;
-      const int pc = c ^ (row & 7);  // swizzled position of 16-byte chunk c
-      uint4* plo = reinterpret_cast<uint4*>(lo_half + row * 64 + pc * 8);
-      uint4* phi = reinterpret_cast<uint4*>(hi_half + row * 64 + pc * 8);
-      uint4 lo = *plo, hi = *phi;
-      rope_pairs8<T>(lo, hi, var.rope_table + int64_t(pos) * FI_ROPE_PAIRS + c * 8);
-      *plo = lo;
-      *phi = hi;
+  // Warps 2 and 3 (the loads all go through warp 0 with RoPE).  Lane = (8-
+  // frequency chunk c, position group g): positions g, g+8, g+16, ... of a
+  // tile, walked two at a time with stride 8.
+  constexpr int kStride = 8;
+  const int c = lane & 7, g = (lane >> 3) + 4 * ((threadIdx.x >> 5) - kVWarp);
+  float2 step[8];
+  rope_load8(step, var.rope_table + kStride * FI_ROPE_PAIRS + 8 * c);
+  auto rotate_row = [&](uint16_t* lo_half, uint16_t* hi_half, int row, const float2 (&cs)[8]) {
+    const int pc = c ^ (row & 7);  // swizzled position of 16-byte chunk c
+    uint4* plo = reinterpret_cast<uint4*>(lo_half + row * 64 + pc * 8);
+    uint4* phi = reinterpret_cast<uint4*>(hi_half + row * 64 + pc * 8);
+    uint4 lo = *plo, hi = *phi;
+    rope_rotate8<T>(lo, hi, cs);
+    *plo = lo;
+    *phi = hi;
+  };
+  // Rotate `npos` consecutive positions from pos0; position u covers rows
+  // [u*rpp, u*rpp + rpp) of the tile (rpp = G for Q, 1 for K), rows < nrows.
+  auto rotate_tile = [&](uint16_t* lo_half, uint16_t* hi_half, int pos0, int npos, int rpp, int nrows) {
+    if (g < npos) {
+      float2 ca[8], cb[8];
+      rope_load8(ca, var.rope_table + int64_t(pos0 + g) * FI_ROPE_PAIRS + 8 * c);
+      for (int u = g; u < npos; u += 2 * kStride) {
+        const bool second = u + kStride < npos;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cb[e] = ca[e];
+        rope_advance8(cb, step);
+        for (int rr = 0; rr < rpp; ++rr) {
+          const int row = u * rpp + rr;
+          if (row >= nrows) break;
+          rotate_row(lo_half, hi_half, row, ca);
+          if (second && (u + kStride) * rpp + rr < nrows) rotate_row(lo_half, hi_half, (u + kStride) * rpp + rr, cb);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ca[e] = cb[e];
+        rope_advance8(ca, step);
+      }
     }
     fence_proxy_async_smem();  // the rotated operands are read by the tensor core
     __syncwarp();
   };
+  uint32_t kt = 0, pe = 0;
   for (int32_t i = b0; i < b1; ++i) {
     const Item it = load_item(p.iws, off_items, i);
     const int ntiles = item_kv_tiles(it);
@@ -176,19 +203,20 @@ __device__ void pf_rope(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1,
     const int nrows = it.row1 - it.row0;
     const int nm = item_m_tiles(it);
     if (!warp_wait(&sm.q_full, pe & 1, &sm.abort)) break;
-    for (int m = 0; m < nm; ++m)
-      rotate_tile(&sm.pf.q[m][0][0][0], &sm.pf.q[m][1][0][0], [&](int row) {
-        const int prow = m * kTileM + row;
-        return prow < nrows ? rq.kv_len - rq.qo_len + (it.row0 + prow) / G : -1;
-      });
+    for (int m = 0; m < nm; ++m) {
+      // M tile m: rows m*128 .. of the item; G rows (heads) per token
+      const int rows_m = min(kTileM, nrows - m * kTileM);
+      const int qpos0 = rq.kv_len - rq.qo_len + (it.row0 + m * kTileM) / G;
+      rotate_tile(&sm.pf.q[m][0][0][0], &sm.pf.q[m][1][0][0], qpos0, (rows_m + G - 1) / G, G, rows_m);
+    }
     if (lane == 0) mbar_arrive(&sm.q_rot);
     ++pe;
     for (int j = 0; j < ntiles; ++j, ++kt) {
       const int st = kt & 1;
       if (!warp_wait(&sm.k_full[st], (kt >> 1) & 1, &sm.abort)) break;
       const int k0 = it.kv0 + j * kTileN;
-      rotate_tile(&sm.pf.k[st][0][0][0], &sm.pf.k[st][1][0][0],
-                  [&](int row) { return k0 + row < it.kv1 ? k0 + row : -1; });
+      const int nk = min(kTileN, it.kv1 - k0);
+      rotate_tile(&sm.pf.k[st][0][0][0], &sm.pf.k[st][1][0][0], k0, nk, 1, nk);
       if (lane == 0) mbar_arrive(&sm.k_rot[st]);
     }
   }

@@ -91,3 +91,31 @@ def test_rope_ragged_prefill_sampled():
         rows += [q0, (q0 + q1) // 2, q1 - 1]
     _sampled(b, dict(max_pos=8192, theta=10000.0), dict(rope=1, rope_theta=10000.0), np.array(rows, np.int64),
              np.array([0, 17, 31]))
+
+
+def test_unfused_rotation_utility():
+    """fi_rope_apply_k rotates every key of the plan's requests (key j at
+    position j) into the copy, each element within one rounding of the cache
+    type (bf16 keeps 8 significant bits) of the fp64 rotation; keys of no
+    request are left alone."""
+    b = workloads.random_batch(451, batch=5, qo_max=1, kv_max=900, num_qo_heads=8, num_kv_heads=2, page_size=16,
+                               causal=0, device=DEV, kv_min=1)
+    cfg = _cfg(2048)
+    ws = fi.Workspace(cfg, device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 0, b.num_pages)
+    k_rot = torch.zeros_like(b.k)
+    fi.rope_apply_k(ws, info, b.k, k_rot, torch.as_tensor(b.kv_indices, device=DEV), int(b.kv_lens().max()))
+    torch.cuda.synchronize()
+    k64, r64 = b.k.double().cpu().numpy(), k_rot.double().cpu().numpy()
+    freq = 10000.0 ** (-2.0 * np.arange(64) / 128)
+    used = np.zeros(b.k.shape[:2], bool)
+    for r in range(b.batch):
+        pages = b.kv_indices[b.kv_indptr[r]:b.kv_indptr[r + 1]]
+        for j in range(int(b.kv_lens()[r])):
+            pg, sl = int(pages[j // 16]), j % 16
+            used[pg, sl] = True
+            c, sn = np.cos(j * freq), np.sin(j * freq)
+            x0, x1 = k64[pg, sl, :, :64], k64[pg, sl, :, 64:]
+            want = np.concatenate([x0 * c - x1 * sn, x1 * c + x0 * sn], axis=-1)
+            assert np.all(np.abs(r64[pg, sl] - want) <= 2.0 ** -8 * np.abs(want) + 1e-30), (r, j)
+    assert np.all(r64[~used] == 0)

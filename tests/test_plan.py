@@ -211,6 +211,8 @@ def test_plan_with_rope_matches_reference(seed):
     assert st == 0 and info.variant & 4
     assert ws[19] == 4096 and ws[22] * 4 == (plan_ref.int_workspace_ints(cfgd) * 4 + 255) // 256 * 256
     assert fi.int_workspace_bytes(cfg) == ws[22] * 4 + 4096 * 64 * 8
+    small, _ = _cfg(num_ctas=152, rope_max_positions=3)
+    assert fi.int_workspace_bytes(small) == (plan_ref.int_workspace_ints(small.as_dict()) * 4 + 255) // 256 * 256 + 16 * 64 * 8
 
 
 @pytest.mark.parametrize("case", ["long", "lq_gt_lkv", "theta", "scale", "negative"])
