@@ -79,7 +79,7 @@ typedef struct {
     int32_t sink_tokens;
     float logits_soft_cap;
     /* RoPE fused into the attention loaders (FlashInfer paper summary,
-     * "주요 실험 결과": a custom kernel fusing RoPE with attention).  The
+     * "주요 성능 테스트 결과 / 2. 커널 수준 성능": a custom kernel fusing RoPE with attention).  The
      * cache holds keys WITHOUT rotation; the kernel rotates q and k on the
      * fly, Llama style: dims i and i + 64 form a pair rotated by the angle
      * (pos / rope_scale) * rope_theta^(-2i/128), i < 64, with key j at

@@ -39,8 +39,9 @@
  *   logits soft-cap (cap > 0, off when 0): the logit fed to the softmax is
  *     cap * tanh(scale * q.k / cap) instead of scale * q.k.
  *
- * RoPE fused into attention (FlashInfer paper summary, section "주요 실험
- * 결과": a kernel fusing RoPE with attention; the page gives no formula).
+ * RoPE fused into attention (FlashInfer paper summary, section "주요 성능
+ * 테스트 결과 / 2. 커널 수준 성능": a kernel fusing RoPE with attention; the
+ * page gives no formula).
  * The plain reading, Llama style: before the dot product, q and every key are
  * rotated by their positions; dims i and i + d/2 form a pair rotated by
  * a = (pos / rope_scale) * rope_theta^(-2i/d):

@@ -1,6 +1,6 @@
 """Pins of the oracle's RoPE against things other than itself.
 
-Reading (the FlashInfer paper summary, section "주요 실험 결과", names a kernel
+Reading (the FlashInfer paper summary, section "주요 성능 테스트 결과 / 2. 커널 수준 성능", names a kernel
 that fuses RoPE with attention but gives no formula): Llama-style rotary
 embedding on q and k, dims i and i + d/2 rotated by (pos / scale) *
 theta^(-2i/d), key j at position j, query token t at Lkv - Lq + t.
