@@ -427,8 +427,8 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
       for (int st = 0; st < nst; ++st, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        const bool ok = mbar_wait_bounded(kRope ? &sm.rot[s] : &sm.full[s], ph, &sm.abort);
-        if (ok && !sm.abort) {
+        // warp-uniform result: the body below shuffles across the warp
+        if (warp_wait(kRope ? &sm.rot[s] : &sm.full[s], ph, &sm.abort)) {
           const int j0 = item.kv0 + st * kStageTokens;
           for (int blk = 0; blk < blocks; ++blk) {
             float sc[kTokBlock];

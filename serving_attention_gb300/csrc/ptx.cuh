@@ -72,22 +72,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with `parity` of `bar`.  Returns false when the wait
-// ran out of budget or another role already gave up (*abort != 0); in both
-// cases *abort is set so every role of the CTA leaves its loop.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > kWaitBudgetClocks) {
-      *abort = kStatusTimeout;
-      return false;
-    }
-  }
-}
-
 // Warp-uniform bounded wait, called by a converged warp.  Every lane polls
 // (a branch around a single polling lane costs more than the poll itself);
 // lane 0's view of completion, abort and budget is broadcast, so all lanes
