@@ -8,6 +8,7 @@ baseline leg may import this package.  It shares no code with the CUDA library
   result, walking the page table (see that file's header for the passages).
 * `merge_states` -- attn_oracle.c: the LSE-weighted merge of two states.
 * `plan_ref.make_plan` -- the plan rule restated in Python.
+* `mla.mla_decode` -- absorbed-MLA decode (latent cache), numpy fp64.
 """
 from __future__ import annotations
 

@@ -22,6 +22,8 @@ Workloads (sizes as the BASELINE configs state them):
   continuous_batch   bf16, 8 chunked-prefill requests (qo 512, prefix U{0..16384}, causal) + 120 decode
                      requests with kv clip(zipf(1.2), 128, 65536); V stored with one extra padding head,
                      so K and V strides differ
+  mla_decode         bf16 absorbed-MLA decode, 64 requests, qo 1, the llama8b_decode length mix, 128 heads,
+                     latent 512 + RoPE key 64 per token, page 64
 """
 from __future__ import annotations
 
@@ -296,3 +298,103 @@ def host_views(b: PagedBatch):
     v = np.lib.stride_tricks.as_strided(vb, shape=tuple(b.v.shape),
                                         strides=tuple(s * vb.itemsize for s in b.v.stride()))
     return q, k, v
+
+
+# ---------------------------------------------------------------- MLA decode inputs
+
+MLA_DC = 512   # latent (compressed KV) dims
+MLA_DR = 64    # decoupled RoPE key dims
+
+
+@dataclass
+class MlaBatch:
+    """Absorbed-MLA decode inputs: one query token per request.
+    q_nope [B, H, 512] is the query already multiplied by the absorbed key
+    up-projection, q_pe [B, H, 64] its RoPE part; ckv [pages, P, 512] holds the
+    latents and kpe [pages, P, 64] the RoPE keys, paged like the GQA cache."""
+    name: str
+    kv_indptr: np.ndarray
+    kv_indices: np.ndarray
+    last_page_len: np.ndarray
+    num_heads: int
+    page_size: int
+    sm_scale: float
+    q_nope: torch.Tensor
+    q_pe: torch.Tensor
+    ckv: torch.Tensor
+    kpe: torch.Tensor
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return len(self.kv_indptr) - 1
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.ckv.shape[0])
+
+    def kv_lens(self) -> np.ndarray:
+        pages = np.diff(self.kv_indptr).astype(np.int64)
+        return np.where(pages == 0, 0, (pages - 1) * self.page_size + self.last_page_len[:self.batch])
+
+
+def make_mla_batch(name: str, kv_lens, num_heads: int, page_size: int, seed: int, device="cpu",
+                   pool_pages: int | None = None, poison: bool = True, rng: np.random.Generator | None = None,
+                   sm_scale: float | None = None) -> MlaBatch:
+    """Shuffled physical pages, N(0,1) bf16 values.  The default scale is that
+    of the un-absorbed head, 1/sqrt(128 + 64).  Poison as for the GQA batches:
+    NaN in unreferenced pages, +BIG in both caches past last_page_len."""
+    rng = rng if rng is not None else np.random.default_rng(seed)
+    kv_lens = np.asarray(kv_lens, dtype=np.int64)
+    kv_indptr, last = _pages_for(kv_lens, page_size)
+    nnz = int(kv_indptr[-1])
+    pool = max(nnz, pool_pages or 0, 1)
+    kv_indices = rng.permutation(pool)[:nnz].astype(np.int32)
+    gen = _gen(device, seed)
+    B = len(kv_lens)
+    bf = torch.bfloat16
+    q_nope = torch.empty((max(B, 1), num_heads, MLA_DC), dtype=bf, device=device)
+    q_pe = torch.empty((max(B, 1), num_heads, MLA_DR), dtype=bf, device=device)
+    ckv = torch.empty((pool, page_size, MLA_DC), dtype=bf, device=device)
+    kpe = torch.empty((pool, page_size, MLA_DR), dtype=bf, device=device)
+    for t in (q_nope, q_pe, ckv, kpe):
+        _fill_normal(t, gen)
+    b = MlaBatch(name, kv_indptr, kv_indices, last, num_heads, page_size,
+                 float(sm_scale if sm_scale is not None else 1.0 / np.sqrt(128 + MLA_DR)), q_nope, q_pe, ckv, kpe)
+    if poison:
+        used = np.zeros(pool, dtype=bool)
+        used[kv_indices] = True
+        unused = np.nonzero(~used)[0]
+        with torch.no_grad():
+            if unused.size:
+                idx = torch.as_tensor(unused, device=device, dtype=torch.long)
+                ckv.index_fill_(0, idx, float("nan"))
+                kpe.index_fill_(0, idx, float("nan"))
+            for r in range(B):
+                n = int(kv_indptr[r + 1] - kv_indptr[r])
+                lpl = int(last[r])
+                if n == 0 or lpl == page_size:
+                    continue
+                page = int(kv_indices[kv_indptr[r + 1] - 1])
+                ckv[page, lpl:] = _BIG["bf16"]
+                kpe[page, lpl:] = _BIG["bf16"]
+    return b
+
+
+def mla_decode(device="cpu", replan: int = 0, batch: int = 64, num_heads: int = 128,
+               page_size: int = 64) -> MlaBatch:
+    """DeepSeek-V3-shaped absorbed-MLA decode: 128 heads, latent 512 + RoPE
+    64, page 64, the llama8b_decode length mix."""
+    seed = 1000 * 6 + replan
+    rng = np.random.default_rng(seed)
+    kv = llama8b_decode_lengths(rng, batch)
+    return make_mla_batch("mla_decode", kv, num_heads, page_size, seed, device, rng=rng)
+
+
+def random_mla_batch(seed: int, batch: int, kv_max: int, num_heads: int, page_size: int, device="cpu",
+                     kv_min: int = 0) -> MlaBatch:
+    rng = np.random.default_rng(seed)
+    kv = rng.integers(kv_min, kv_max + 1, size=batch)
+    extra = int(rng.integers(0, 8))
+    pool = int(((kv + page_size - 1) // page_size).sum()) + extra
+    return make_mla_batch(f"random_mla{seed}", kv, num_heads, page_size, seed, device, pool_pages=pool, rng=rng)
