@@ -243,3 +243,83 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
                 int_ws_bytes_used=4 * total_ints, max_partial_rows=cfg["max_partial_rows"],
                 variant=(1 if cap > 0 else 0) | (2 if window >= 0 else 0) | (4 if rope_max > 0 else 0))
     return OK, ws, info
+
+
+# ---------------------------------------------------------------- MLA decode plan
+
+MLA_MAGIC = 0x464D4C31
+MLA_HEADER_INTS = 16
+MLA_BLOCK = 64
+MLA_UNIT_COST_TOKENS = 192
+
+
+def mla_make_plan(kv_indptr, last_page_len, page_size: int, num_heads: int, num_pairs: int, min_chunk: int,
+                  split_factor: int) -> np.ndarray:
+    """The absorbed-MLA decode plan, restated.  Rule:
+     1. L_b = (pages_b - 1) * page_size + last_page_len[b] (0 without pages).
+     2. chunk = max(min_chunk, ceil(sum L / (pairs * split)) rounded up to 64).
+     3. Request b with L_b > 0: n = ceil(L_b / chunk) pieces of
+        ceil(L_b / n) tokens rounded up to 64, the last one what is left.
+        Several pieces: consecutive partial slots and a merge entry
+        (b, first slot, count); no piece (L_b = 0): merge entry (b, 0, 0).
+     4. cost = tokens + 192; pieces sorted by decreasing cost, equal costs in
+        (request, position) order; each to the least-loaded pair (ties: lower
+        pair); a pair runs its pieces in the order received.
+     5. Image: header[16], pair offsets (pairs + 1, padded to 4), units
+        {b, kv0, kv1, slot or -1}, requests {kv_indptr[b], L_b} (padded to 4),
+        merge entries {b, slot0, count, 0}."""
+    kv_indptr = [int(x) for x in kv_indptr]
+    B = len(kv_indptr) - 1
+    L = []
+    for b in range(B):
+        n = kv_indptr[b + 1] - kv_indptr[b]
+        L.append(0 if n == 0 else (n - 1) * page_size + int(last_page_len[b]))
+    total = sum(L)
+    per = -(-total // (num_pairs * split_factor))
+    chunk = max(min_chunk, -(-per // MLA_BLOCK) * MLA_BLOCK)
+    pieces, merge, slots = [], [], 0
+    for b in range(B):
+        if L[b] == 0:
+            merge.append((b, 0, 0, 0))
+            continue
+        n = -(-L[b] // chunk)
+        size = -(-(-(-L[b] // n)) // MLA_BLOCK) * MLA_BLOCK
+        mine = [[b, k0, min(L[b], k0 + size), -1] for k0 in range(0, L[b], size)]
+        if len(mine) > 1:
+            for i, p in enumerate(mine):
+                p[3] = slots + i
+            merge.append((b, slots, len(mine), 0))
+            slots += len(mine)
+        pieces += mine
+    order = sorted(range(len(pieces)), key=lambda i: (-(pieces[i][2] - pieces[i][1] + MLA_UNIT_COST_TOKENS), i))
+    load = [0] * num_pairs
+    owned = [[] for _ in range(num_pairs)]
+    for i in order:
+        p = min(range(num_pairs), key=lambda q: (load[q], q))
+        owned[p].append(i)
+        load[p] += pieces[i][2] - pieces[i][1] + MLA_UNIT_COST_TOKENS
+
+    def r4(n):
+        return (n + 3) // 4 * 4
+
+    off_pair = MLA_HEADER_INTS
+    off_units = off_pair + r4(num_pairs + 1)
+    off_req = off_units + 4 * len(pieces)
+    off_merge = off_req + r4(2 * B)
+    total_ints = off_merge + 4 * len(merge)
+    img = np.zeros(total_ints, dtype=np.int32)
+    img[:MLA_HEADER_INTS] = [MLA_MAGIC, len(pieces), num_pairs, B, num_heads, page_size, off_pair, off_units,
+                             off_req, off_merge, len(merge), 0, chunk, total_ints, slots, 0]
+    at = 0
+    for p in range(num_pairs):
+        img[off_pair + p] = at
+        for i in owned[p]:
+            img[off_units + 4 * at:off_units + 4 * at + 4] = pieces[i]
+            at += 1
+    img[off_pair + num_pairs] = at
+    for b in range(B):
+        img[off_req + 2 * b] = kv_indptr[b]
+        img[off_req + 2 * b + 1] = L[b]
+    for k, m in enumerate(merge):
+        img[off_merge + 4 * k:off_merge + 4 * k + 4] = m
+    return img

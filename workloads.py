@@ -81,11 +81,12 @@ def torch_dtype(name: str) -> torch.dtype:
     return _TORCH[name]
 
 
-def _fill_normal(t: torch.Tensor, gen: torch.Generator, chunk: int = 1 << 26) -> None:
+def _fill_normal(t: torch.Tensor, gen: torch.Generator, chunk: int = 1 << 26, std: float = 1.0) -> None:
     flat = t.view(-1)
     for s in range(0, flat.numel(), chunk):
         part = flat[s:s + chunk]
-        part.copy_(torch.randn(part.numel(), generator=gen, device=t.device, dtype=torch.float32))
+        x = torch.randn(part.numel(), generator=gen, device=t.device, dtype=torch.float32)
+        part.copy_(x if std == 1.0 else x * std)
 
 
 def _gen(device, seed: int) -> torch.Generator:
@@ -304,6 +305,7 @@ def host_views(b: PagedBatch):
 
 MLA_DC = 512   # latent (compressed KV) dims
 MLA_DR = 64    # decoupled RoPE key dims
+MLA_Q_STD = (1.0 / 3.0) ** 0.5
 
 
 @dataclass
@@ -341,7 +343,8 @@ class MlaBatch:
 def make_mla_batch(name: str, kv_lens, num_heads: int, page_size: int, seed: int, device="cpu",
                    pool_pages: int | None = None, poison: bool = True, rng: np.random.Generator | None = None,
                    sm_scale: float | None = None) -> MlaBatch:
-    """Shuffled physical pages, N(0,1) bf16 values.  The default scale is that
+    """Shuffled physical pages, N(0,1) bf16 latents and RoPE keys, N(0,1/3)
+    queries.  The default scale is that
     of the un-absorbed head, 1/sqrt(128 + 64).  Poison as for the GQA batches:
     NaN in unreferenced pages, +BIG in both caches past last_page_len."""
     rng = rng if rng is not None else np.random.default_rng(seed)
@@ -357,8 +360,10 @@ def make_mla_batch(name: str, kv_lens, num_heads: int, page_size: int, seed: int
     q_pe = torch.empty((max(B, 1), num_heads, MLA_DR), dtype=bf, device=device)
     ckv = torch.empty((pool, page_size, MLA_DC), dtype=bf, device=device)
     kpe = torch.empty((pool, page_size, MLA_DR), dtype=bf, device=device)
-    for t in (q_nope, q_pe, ckv, kpe):
-        _fill_normal(t, gen)
+    # queries N(0, 1/3): with 576 contracted dims and scale 1/sqrt(192) the
+    # logits then spread like those of the GQA workloads (unit variance)
+    for t, std in ((q_nope, MLA_Q_STD), (q_pe, MLA_Q_STD), (ckv, 1.0), (kpe, 1.0)):
+        _fill_normal(t, gen, std=std)
     b = MlaBatch(name, kv_indptr, kv_indices, last, num_heads, page_size,
                  float(sm_scale if sm_scale is not None else 1.0 / np.sqrt(128 + MLA_DR)), q_nope, q_pe, ckv, kpe)
     if poison:
