@@ -348,6 +348,49 @@ def bench_secondary(dev, reps=5):
     out["shared_prefix"] = bench_shared_prefix(dev, flush, reps)
     out["kv_strides"] = bench_kv_strides(dev, flush, reps)
     out["variants"] = bench_variants(dev, flush, reps)
+    out["mla"] = bench_mla(dev, flush, reps)
+    return out
+
+
+def mla_algorithmic(b):
+    """Bytes and flops of one absorbed-MLA decode: every cached latent (512)
+    and RoPE key (64) once, the page ids, q (576) and o (512) per head, the
+    LSE; flops 2 * H * (576 + 512) per cached token (Q K^T and P V)."""
+    lens = b.kv_lens().astype(np.int64)
+    tok = int(lens.sum())
+    H, B = b.num_heads, b.batch
+    pages = int(b.kv_indptr[-1])
+    nbytes = tok * (512 + 64) * 2 + pages * 4 + B * H * ((576 + 512) * 2 + 4)
+    flops = 2 * H * (576 + 512) * tok
+    return nbytes, flops
+
+
+def bench_mla(dev, flush, reps=5):
+    """Absorbed-MLA decode (decode kernel + merge kernel, one C-ABI call) on
+    the 64-request length-mix workload, graph-replayed, L2 flushed."""
+    import torch
+
+    from serving_attention_gb300 import mla
+    import workloads
+
+    b = workloads.mla_decode(device=dev)
+    cfg = mla.default_config(dev.index)
+    ws = mla.MlaWorkspace(cfg, device=dev)
+    info = mla.plan(ws, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_heads, b.page_size, b.num_pages)
+    kvi = torch.as_tensor(b.kv_indices, device=dev)
+    o = torch.empty(b.q_nope.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(b.q_nope.shape[:2], dtype=torch.float32, device=dev)
+    ms = _graph_ms(lambda: mla.decode_run(ws, info, b.q_nope, b.q_pe, b.ckv, b.kpe, kvi, o, lse, b.sm_scale),
+                   flush, reps)
+    import serving_attention_gb300 as fi
+    assert fi.device_status(ws) == 0
+    nbytes, flops = mla_algorithmic(b)
+    out = {"workload": "mla_decode: 64 requests, kv floor(exp U(ln 512, ln 32768)), 128 heads, latent 512 + RoPE 64,"
+                       " page 64, bf16", "ms": ms, "gbs": nbytes / ms / 1e6, "tflops": flops / ms / 1e9,
+           "algorithmic_bytes": nbytes, "flops": flops, "pairs": info.num_pairs, "chunks": info.num_units,
+           "split_chunks": info.num_parts, "launches": 2}
+    del b, o, lse, ws
+    torch.cuda.empty_cache()
     return out
 
 
@@ -592,6 +635,8 @@ PROFILE_CASES = {
     "ragged_prefill": lambda dev: __import__("workloads").ragged_prefill(device=dev),
     "ragged_prefill_4": lambda dev: __import__("workloads").ragged_prefill(device=dev, batch=4),
     "continuous_batch": lambda dev: __import__("workloads").continuous_batch(device=dev),
+    "mla_decode": lambda dev: __import__("workloads").mla_decode(device=dev),
+    "mla_decode_16": lambda dev: __import__("workloads").mla_decode(device=dev, batch=16),
 }
 
 
@@ -604,6 +649,8 @@ def profile_case(name: str, launches: int) -> int:
 
     dev = _device_setup(0)
     b = PROFILE_CASES[name](dev)
+    if name.startswith("mla"):
+        return _profile_mla(name, b, dev, launches)
     ws = fi.Workspace(fi.default_plan_config(0), device=dev)
     info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads, 128,
                    b.page_size, b.causal, b.num_pages)
@@ -617,6 +664,27 @@ def profile_case(name: str, launches: int) -> int:
     nbytes, formula, exact = algorithmic(b)
     print(json.dumps({"profile": name, "launches": launches, "items": info.num_items, "status": st,
                       "algorithmic_bytes": nbytes, "flops_exact": exact, "flops_formula": formula}))
+    return 0 if st == 0 else 3
+
+
+def _profile_mla(name, b, dev, launches: int) -> int:
+    import torch
+
+    import serving_attention_gb300 as fi
+    from serving_attention_gb300 import mla
+
+    ws = mla.MlaWorkspace(mla.default_config(0), device=dev)
+    info = mla.plan(ws, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_heads, b.page_size, b.num_pages)
+    kvi = torch.as_tensor(b.kv_indices, device=dev)
+    o = torch.empty(b.q_nope.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(b.q_nope.shape[:2], dtype=torch.float32, device=dev)
+    for _ in range(launches):
+        mla.decode_run(ws, info, b.q_nope, b.q_pe, b.ckv, b.kpe, kvi, o, lse, b.sm_scale)
+    torch.cuda.synchronize()
+    st = fi.device_status(ws)
+    nbytes, flops = mla_algorithmic(b)
+    print(json.dumps({"profile": name, "launches": launches, "chunks": info.num_units, "status": st,
+                      "algorithmic_bytes": nbytes, "flops": flops}))
     return 0 if st == 0 else 3
 
 
@@ -779,6 +847,8 @@ def main():
         line["shared_prefix"] = dict(sp, frac_of_hbm=sp["composable_gbs"] / hbm)
         line["kv_strides"] = sec["kv_strides"]
         line["variants"] = sec["variants"]
+        ml = sec["mla"]
+        line["mla"] = dict(ml, frac_of_hbm=ml["gbs"] / hbm, frac_of_tensor=ml["tflops"] / tf)
     print(json.dumps(line))
 
 

@@ -68,6 +68,7 @@ constexpr uint32_t kTmemCols = 512;  // O: columns 0..255; S buffers: 256..319 a
 constexpr uint32_t kTmemS = 256;
 constexpr float kLazyRescale = 8.0f;  // log2 units: keep a stale max until it is 2^8 off
 constexpr int kMergeThreads = 128;
+constexpr int kMergeBlocksPerPair = 16;
 
 // One KV block of this CTA's half: the latent rows as 4 groups of 64 dims
 // (128-byte rows, 128-byte swizzle, 8 KB each) and the RoPE rows (64-byte
@@ -81,15 +82,17 @@ struct Smem {
   uint16_t q_lat[kGroups][kRows][64];  // this CTA's latent half of the 128 query rows
   uint16_t q_rope[kRows][kRopeHalf];   // and its RoPE quarter
   Stage st[kStages];
-  float xbuf[kRows][kBlk];             // the partner's partial logits of the current block
+  uint4 xbuf[kBlk / 4][kRows];         // the partner's partial logits of the current block: chunk q
+                                       // (logits 4q..4q+3) of row r at [q][r], so a warp's stores are
+                                       // 512 contiguous bytes
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full, q_empty;
   uint64_t s_full[2];                  // S buffer b holds the logits of a block (MMA commit)
   uint64_t p_full;                     // P of the current block is in TMEM (the 4 softmax warps)
   uint64_t pv_done;                    // P V of a block has completed (MMA commit)
   uint64_t o_ready, o_free;            // O of a chunk complete / read out by the epilogue
-  uint64_t xfull;                      // the partner's 128 threads wrote their logits into xbuf
-  uint64_t xfree;                      // the partner's 128 threads read the logits this CTA sent
+  uint64_t xfull;                      // the partner's logits have landed in xbuf (32 KB of complete_tx)
+  uint64_t xfree;                      // the partner's 4 softmax warps read the logits this CTA sent
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -134,8 +137,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+// Asynchronous store into another CTA's shared memory that, once it has
+// landed, completes its 16 bytes on that CTA's barrier `remote_bar` (no fence
+// in the issuing thread: the receiver's wait on the barrier orders the data).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
                : "memory");
 }
 
@@ -373,11 +382,10 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
   const uint32_t tl = sm.tmem_base + (uint32_t(32 * w) << 16);
   const float c = p.scale_log2;
   const uint32_t peer = rank ^ 1u;
-  const uint32_t x_remote = mapa_shared(smem_u32(&sm.xbuf[r][0]), peer);
+  const uint32_t x_remote = mapa_shared(smem_u32(&sm.xbuf[0][r]), peer);
   const uint32_t xfull_remote = mapa_shared(smem_u32(&sm.xfull), peer);
   const uint32_t xfree_remote = mapa_shared(smem_u32(&sm.xfree), peer);
-  const uint4* x_local = reinterpret_cast<const uint4*>(&sm.xbuf[r][0]);
-  const int sw = r & 15;  // 16-byte chunk c of a row sits at chunk c ^ sw (spreads the rows over the banks)
+  constexpr uint32_t kChunkStride = kRows * 16;  // bytes from chunk q to chunk q + 1 of a row
   const bool row_ok = r < p.num_heads;
   int g = 0, nu = 0;
   bool ok = true;
@@ -395,30 +403,33 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
       tc::tmem_ld32(scol, sv[0]);
       tc::tmem_ld32(scol + 32, sv[1]);
       tc::tmem_ld_wait();
+      // This block's 32 KB from the partner completes xfull's phase gb (its
+      // previous phase completed before this thread read the previous block).
+      if (r == 0) mbar_arrive_expect_tx(&sm.xfull, kRows * kBlk * 4);
       // send this CTA's partial row once the partner has read the previous one
       if (gb > 0) {
         ok = warp_wait_cluster(&sm.xfree, (gb - 1) & 1, &sm.abort);
         if (!ok) break;
       }
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < kBlk / 4; ++q) {
         const uint32_t* v = &sv[q >> 3][4 * (q & 7)];
-        st_cluster_v4(x_remote + 16u * uint32_t(q ^ sw), v[0], v[1], v[2], v[3]);
+        st_async_v4(x_remote + kChunkStride * uint32_t(q), v[0], v[1], v[2], v[3], xfull_remote);
       }
-      mbar_arrive_cluster(xfull_remote);
       ok = warp_wait_cluster(&sm.xfull, gb & 1, &sm.abort);
       if (!ok) break;
       float s[kBlk];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const uint4 x = x_local[q ^ sw];
+      for (int q = 0; q < kBlk / 4; ++q) {
+        const uint4 x = sm.xbuf[q][r];
         const uint32_t* v = &sv[q >> 3][4 * (q & 7)];
         s[4 * q + 0] = __uint_as_float(v[0]) + __uint_as_float(x.x);
         s[4 * q + 1] = __uint_as_float(v[1]) + __uint_as_float(x.y);
         s[4 * q + 2] = __uint_as_float(v[2]) + __uint_as_float(x.z);
         s[4 * q + 3] = __uint_as_float(v[3]) + __uint_as_float(x.w);
       }
-      mbar_arrive_cluster(xfree_remote);  // the partner may send its next block
+      __syncwarp();  // the warp's reads of xbuf come before its release below
+      if (lane == 0) mbar_arrive_cluster(xfree_remote);  // the partner may send its next block
       const int ntok = min(kBlk, u.kv1 - (u.kv0 + j * kBlk));
       if (ntok < kBlk) {
 #pragma unroll
@@ -569,8 +580,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.o_ready, 1);
     mbar_init(&sm.o_free, 4);
-    mbar_init(&sm.xfull, kSoftmaxThreads);  // every softmax thread of the partner
-    mbar_init(&sm.xfree, kSoftmaxThreads);
+    mbar_init(&sm.xfull, 1);       // softmax thread 0's arrive.expect_tx; the partner's stores complete the bytes
+    mbar_init(&sm.xfree, 4);       // the partner's four softmax warps
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -755,7 +766,10 @@ extern "C" fi_status fi_mla_decode_run(const fi_mla_plan_info* info, const void*
   mla_decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return FI_ERR_CUDA;
-  mla_merge_kernel<<<grid, kMergeThreads, 0, s>>>(p.iws, p.fws, p.partial_o_offset, p.o, lse, H);
+  // the merge reads each partial state once: enough blocks to keep several
+  // tasks' loads in flight per SM (the count of tasks is known on the device)
+  mla_merge_kernel<<<kMergeBlocksPerPair * info->num_pairs, kMergeThreads, 0, s>>>(p.iws, p.fws, p.partial_o_offset,
+                                                                                   p.o, lse, H);
   e = cudaGetLastError();
   return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }

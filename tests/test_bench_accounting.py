@@ -30,3 +30,11 @@ def test_causal_prefill_flops():
     _, formula, exact = bench.algorithmic(b)
     assert exact == 4 * 128 * 4 * _count(b)
     assert formula == 4 * 128 * 4 * float((np.array([3, 5, 2]) * np.array([7, 5, 9])).sum()) / 2
+
+
+def test_mla_bytes_and_flops():
+    b = workloads.make_mla_batch("acct", [5, 0, 70], 16, 8, 3, pool_pages=12)
+    nbytes, flops = bench.mla_algorithmic(b)
+    pages = 1 + 0 + 9
+    assert nbytes == 75 * (512 + 64) * 2 + pages * 4 + 3 * 16 * (576 * 2 + 512 * 2 + 4)
+    assert flops == 75 * 16 * (2 * 576 + 2 * 512)
