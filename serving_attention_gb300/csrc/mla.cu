@@ -23,11 +23,14 @@
 //    memory and adds the other's: both then hold the same full S (fp32
 //    addition is commutative, so bit for bit the same), take the same
 //    softmax decisions, and accumulate P V into their own half of O;
-//  * roles per CTA: warp 0 loads Q and the KV blocks with TMA (3 stages);
-//    warp 1 issues the MMAs (S = Q K^T over 288 dims into TMEM, then O += P V
-//    with P read from TMEM over the S columns, N = 256); warps 4..7 run the
-//    softmax (one head row per thread = one TMEM lane), the exchange and the
-//    epilogue;
+//  * tensor memory holds O (256 columns), the two S buffers (64 each) and the
+//    CTA's latent half of Q (256 bf16 dims per row, 128 columns), so shared
+//    memory keeps only the RoPE quarter of Q and five KV stages;
+//  * roles per CTA: warp 0 loads the RoPE part of Q and the KV blocks with TMA;
+//    warp 1 issues the MMAs (S = Q K^T over 288 dims into TMEM, the latent part
+//    with Q read from TMEM, then O += P V with P read from TMEM over the S
+//    columns, N = 256); warps 4..7 write Q into TMEM, run the softmax (one head
+//    row per thread = one TMEM lane), the exchange and the epilogue;
 //  * S of block j+1 is issued before P V of block j, so the softmax of one
 //    block overlaps the MMAs of the next; the rare lazy rescale of O waits
 //    for the P V in flight first;
@@ -60,12 +63,13 @@ constexpr int kHalf = kDc / 2;              // latent dims per CTA of the pair
 constexpr int kRopeHalf = FI_MLA_ROPE_DIM / 2;  // RoPE dims per CTA
 constexpr int kBlk = FI_MLA_BLOCK;          // KV tokens per block
 constexpr int kGroups = kHalf / 64;         // 128-byte swizzled column groups of a CTA's latent half
-constexpr int kStages = 3;
-constexpr int kThreads = 256;
-constexpr int kProducerWarp = 0, kMmaWarp = 1, kAllocWarp = 2, kSoftmaxWarp0 = 4;
+constexpr int kStages = 4;
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kAllocWarp = 2, kSoftmaxWarp0 = 4, kExchangeWarp0 = 8;
 constexpr int kSoftmaxThreads = 128;
-constexpr uint32_t kTmemCols = 512;  // O: columns 0..255; S buffers: 256..319 and 320..383
+constexpr uint32_t kTmemCols = 512;  // O: 0..255; S buffers: 256..319, 320..383; Q: 384..511
 constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemQ = 384;
 constexpr float kLazyRescale = 8.0f;  // log2 units: keep a stale max until it is 2^8 off
 constexpr int kMergeThreads = 128;
 constexpr int kMergeBlocksPerPair = 16;
@@ -79,20 +83,22 @@ struct Stage {
 };
 
 struct Smem {
-  uint16_t q_lat[kGroups][kRows][64];  // this CTA's latent half of the 128 query rows
-  uint16_t q_rope[kRows][kRopeHalf];   // and its RoPE quarter
+  uint16_t q_rope[kRows][kRopeHalf];   // this CTA's RoPE quarter of the 128 query rows
   Stage st[kStages];
-  uint4 xbuf[kBlk / 4][kRows];         // the partner's partial logits of the current block: chunk q
-                                       // (logits 4q..4q+3) of row r at [q][r], so a warp's stores are
+  uint4 xbuf[2][kBlk / 4][kRows];      // the partner's partial logits of block g in buffer g % 2: chunk
+                                       // q (logits 4q..4q+3) of row r at [q][r], so a warp's stores are
                                        // 512 contiguous bytes
   uint64_t full[kStages], empty[kStages];
-  uint64_t q_full, q_empty;
+  uint64_t q_full;                     // the RoPE part of Q has landed (TMA)
+  uint64_t q_lat_full;                 // the latent part of Q is in TMEM (the 4 softmax warps)
+  uint64_t q_empty;                    // the chunk's last S has completed (MMA commit)
   uint64_t s_full[2];                  // S buffer b holds the logits of a block (MMA commit)
   uint64_t p_full;                     // P of the current block is in TMEM (the 4 softmax warps)
   uint64_t pv_done;                    // P V of a block has completed (MMA commit)
   uint64_t o_ready, o_free;            // O of a chunk complete / read out by the epilogue
-  uint64_t xfull;                      // the partner's logits have landed in xbuf (32 KB of complete_tx)
-  uint64_t xfree;                      // the partner's 4 softmax warps read the logits this CTA sent
+  uint64_t xfull[2];                   // the partner's logits have landed in xbuf[b] (32 KB of complete_tx)
+  uint64_t xfree[2];                   // the partner's 4 softmax warps read the logits sent into their xbuf[b]
+  uint64_t s_read[2];                  // the exchange warps have read S buffer b (P may overwrite it)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -102,14 +108,15 @@ static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 static_assert(offsetof(Smem, q_rope) % 1024 == 0 && offsetof(Smem, st) % 1024 == 0 && sizeof(Stage) % 1024 == 0 &&
                   offsetof(Stage, rope) % 1024 == 0,
               "swizzled operand blocks start on 1024-byte boundaries");
-constexpr uint32_t kQBytes = kGroups * kRows * 128 + kRows * kRopeHalf * 2;  // one Q load
+constexpr uint32_t kQBytes = kRows * kRopeHalf * 2;  // one load of the RoPE part of Q
 constexpr uint32_t kRowBytes = kGroups * 128 + kRopeHalf * 2;                // one token of a KV block
 
 struct Params {
-  CUtensorMap tm_qn;   // q_nope [rows][heads][512], box 64 x 128 x 1, 128-byte swizzle
   CUtensorMap tm_qp;   // q_pe   [rows][heads][64],  box 32 x 128 x 1, 64-byte swizzle
   CUtensorMap tm_ckv;  // ckv    [pages][P][512],    box 64 x P x 1, 128-byte swizzle
   CUtensorMap tm_kpe;  // kpe    [pages][P][64],     box 32 x P x 1, 64-byte swizzle
+  const uint16_t* q_nope;  // [rows][heads][512] bf16, element strides below
+  int64_t qn_stride_tok, qn_stride_head;
   const int32_t* iws;
   int32_t* status;
   const int32_t* kv_indices;
@@ -220,7 +227,9 @@ __device__ void producer(const Params& p, Smem& sm, uint32_t rank, int32_t begin
   const int P = p.page_size;
   const int x_lat = kHalf * int(rank), x_rope = kRopeHalf * int(rank);
   int it = 0, nu = 0;
-  int armed[kStages] = {-1, -1, -1};
+  int armed[kStages];
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) armed[s] = -1;
   int q_armed = -1;
   bool ok = true;
   for (int32_t i = begin; i < end && ok; ++i) {
@@ -230,8 +239,6 @@ __device__ void producer(const Params& p, Smem& sm, uint32_t rank, int32_t begin
     if (!ok) break;
     if (lane == 0) {
       mbar_arrive_expect_tx(&sm.q_full, kQBytes);
-#pragma unroll
-      for (int a = 0; a < kGroups; ++a) tc::tma_load_3d(&sm.q_lat[a][0][0], &p.tm_qn, &sm.q_full, x_lat + 64 * a, 0, u.b);
       tc::tma_load_3d(&sm.q_rope[0][0], &p.tm_qp, &sm.q_full, x_rope, 0, u.b);
     }
     q_armed = nu & 1;
@@ -276,11 +283,11 @@ __device__ void mma_issuer(const Params& p, Smem& sm, int32_t begin, int32_t end
   constexpr uint32_t idesc_pv = tc::idesc_f16(true, true, kRows, kHalf);
   const uint32_t tmem = sm.tmem_base;
   // Descriptors of the first block of each operand; the start-address field
-  // counts 16-byte units: a Q column group is 16 KB (1024), a KV column group
-  // 8 KB (512), a stage sizeof(Stage) / 16, 16 dims along a swizzled row 32
-  // bytes (2), 16 V tokens 2 KB (128).  Every sum is a real shared-memory
+  // counts 16-byte units: a KV column group is 8 KB (512), a stage
+  // sizeof(Stage) / 16, 16 dims along a swizzled row 32 bytes (2), 16 V tokens
+  // 2 KB (128).  The latent part of Q is the A operand in TMEM: 16 dims are 8
+  // columns of 16-bit pairs.  Every sum is a real shared-memory
   // address below 2^18 bytes, so the field never carries.
-  const uint64_t dq = tc::smem_desc_sw128(smem_u32(&sm.q_lat[0][0][0]), 16, 1024);
   const uint64_t dqr = smem_desc_sw64(smem_u32(&sm.q_rope[0][0]), 512);
   const uint64_t dk = tc::smem_desc_sw128(smem_u32(&sm.st[0].lat[0][0][0]), 16, 1024);
   const uint64_t dkr = smem_desc_sw64(smem_u32(&sm.st[0].rope[0][0]), 512);
@@ -314,9 +321,8 @@ __device__ void mma_issuer(const Params& p, Smem& sm, int32_t begin, int32_t end
     const uint64_t k0 = dk + kStageUnits * s, r0 = dkr + kStageUnits * s;
 #pragma unroll
     for (int kk = 0; kk < kHalf / 16; ++kk) {
-      const uint32_t sq = 1024u * uint32_t(kk >> 2) + 2u * uint32_t(kk & 3);
       const uint32_t sk = 512u * uint32_t(kk >> 2) + 2u * uint32_t(kk & 3);
-      tc::mma_ss_warp(d, dq + sq, k0 + sk, idesc_s, kk > 0 ? 1u : 0u);
+      tc::mma_ts_warp(d, tmem + kTmemQ + 8u * kk, k0 + sk, idesc_s, kk > 0 ? 1u : 0u);
     }
 #pragma unroll
     for (int kk = 0; kk < kRopeHalf / 16; ++kk) tc::mma_ss_warp(d, dqr + 2u * kk, r0 + 2u * kk, idesc_s, 1u);
@@ -328,7 +334,7 @@ __device__ void mma_issuer(const Params& p, Smem& sm, int32_t begin, int32_t end
     const Unit u = load_unit(p.iws, off_units, i);
     const int nb = unit_blocks(u);
     auto ntok = [&](int j) { return min(kBlk, u.kv1 - (u.kv0 + j * kBlk)); };
-    ok = warp_wait(&sm.q_full, nu & 1, &sm.abort);
+    ok = warp_wait_all(2, &sm.q_full, nu & 1, &sm.q_lat_full, nu & 1, nullptr, 0, nullptr, 0, &sm.abort);
     if (!ok) break;
     tc::fence_after_sync();
     for (int j = 0; j < nb && j < 2 && ok; ++j) {
@@ -382,16 +388,41 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
   const uint32_t tl = sm.tmem_base + (uint32_t(32 * w) << 16);
   const float c = p.scale_log2;
   const uint32_t peer = rank ^ 1u;
-  const uint32_t x_remote = mapa_shared(smem_u32(&sm.xbuf[0][r]), peer);
-  const uint32_t xfull_remote = mapa_shared(smem_u32(&sm.xfull), peer);
-  const uint32_t xfree_remote = mapa_shared(smem_u32(&sm.xfree), peer);
-  constexpr uint32_t kChunkStride = kRows * 16;  // bytes from chunk q to chunk q + 1 of a row
+  const uint32_t xfree_remote[2] = {mapa_shared(smem_u32(&sm.xfree[0]), peer),
+                                    mapa_shared(smem_u32(&sm.xfree[1]), peer)};
   const bool row_ok = r < p.num_heads;
   int g = 0, nu = 0;
   bool ok = true;
   for (int32_t i = begin; i < end && ok; ++i) {
     const Unit u = load_unit(p.iws, off_units, i);
     const int nb = unit_blocks(u);
+    // The chunk's query rows into TMEM once the previous chunk's last S has
+    // read them: this CTA's 256 latent dims of row r as 128 columns of pairs
+    // (rows past the heads are zeros).
+    ok = warp_wait(&sm.q_empty, (nu & 1) ^ 1, &sm.abort);
+    if (!ok) break;
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + int64_t(u.b) * p.qn_stride_tok +
+                                                        int64_t(row_ok ? r : 0) * p.qn_stride_head) +
+                         kHalf / 8 * int(rank);
+      uint32_t qv[4][32];
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 v = row_ok ? __ldg(src + 8 * h + e) : make_uint4(0u, 0u, 0u, 0u);
+          qv[h][4 * e] = v.x;
+          qv[h][4 * e + 1] = v.y;
+          qv[h][4 * e + 2] = v.z;
+          qv[h][4 * e + 3] = v.w;
+        }
+#pragma unroll
+      for (int h = 0; h < 4; ++h) tc::tmem_st32(tl + kTmemQ + 32u * h, qv[h]);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.q_lat_full);
+    }
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < nb; ++j) {
       const int gb = g + j;
@@ -403,33 +434,25 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
       tc::tmem_ld32(scol, sv[0]);
       tc::tmem_ld32(scol + 32, sv[1]);
       tc::tmem_ld_wait();
-      // This block's 32 KB from the partner completes xfull's phase gb (its
-      // previous phase completed before this thread read the previous block).
-      if (r == 0) mbar_arrive_expect_tx(&sm.xfull, kRows * kBlk * 4);
-      // send this CTA's partial row once the partner has read the previous one
-      if (gb > 0) {
-        ok = warp_wait_cluster(&sm.xfree, (gb - 1) & 1, &sm.abort);
-        if (!ok) break;
-      }
-#pragma unroll
-      for (int q = 0; q < kBlk / 4; ++q) {
-        const uint32_t* v = &sv[q >> 3][4 * (q & 7)];
-        st_async_v4(x_remote + kChunkStride * uint32_t(q), v[0], v[1], v[2], v[3], xfull_remote);
-      }
-      ok = warp_wait_cluster(&sm.xfull, gb & 1, &sm.abort);
+      // the partner's half of the logits, sent by its exchange warps
+      const int xb = gb & 1;
+      ok = warp_wait_cluster(&sm.xfull[xb], (gb >> 1) & 1, &sm.abort);
       if (!ok) break;
       float s[kBlk];
 #pragma unroll
       for (int q = 0; q < kBlk / 4; ++q) {
-        const uint4 x = sm.xbuf[q][r];
+        const uint4 x = sm.xbuf[xb][q][r];
         const uint32_t* v = &sv[q >> 3][4 * (q & 7)];
         s[4 * q + 0] = __uint_as_float(v[0]) + __uint_as_float(x.x);
         s[4 * q + 1] = __uint_as_float(v[1]) + __uint_as_float(x.y);
         s[4 * q + 2] = __uint_as_float(v[2]) + __uint_as_float(x.z);
         s[4 * q + 3] = __uint_as_float(v[3]) + __uint_as_float(x.w);
       }
+      // Arm the buffer's next use (block gb + 2): its phase for block gb has
+      // completed, and the partner sends block gb + 2 only after the release below.
+      if (r == 0) mbar_arrive_expect_tx(&sm.xfull[xb], kRows * kBlk * 4);
       __syncwarp();  // the warp's reads of xbuf come before its release below
-      if (lane == 0) mbar_arrive_cluster(xfree_remote);  // the partner may send its next block
+      if (lane == 0) mbar_arrive_cluster(xfree_remote[xb]);  // the partner may send block gb + 2
       const int ntok = min(kBlk, u.kv1 - (u.kv0 + j * kBlk));
       if (ntok < kBlk) {
 #pragma unroll
@@ -477,6 +500,9 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
         sum4[e & 3] = add2(sum4[e & 3], pe);
         pk[e] = tc::pack2<__nv_bfloat16>(pe.x, pe.y);
       }
+      // P overwrites the S buffer once this CTA's exchange warps have read it
+      ok = warp_wait(&sm.s_read[gb & 1], (gb >> 1) & 1, &sm.abort);
+      if (!ok) break;
       tc::tmem_st32(scol, pk);
       tc::tmem_st_wait();
       tc::fence_before_sync();
@@ -538,6 +564,55 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
   }
 }
 
+// Warps 8..11: thread r reads this CTA's partial logits of each block from
+// TMEM (the same lanes as softmax thread r) as soon as S is complete, which is
+// a block ahead of the softmax, and stores them asynchronously into the
+// partner's xbuf; the bytes complete the partner's xfull.  The softmax of
+// both CTAs then finds the other half already there.
+__device__ void exchange_role(const Params& p, Smem& sm, uint32_t rank, int32_t begin, int32_t end,
+                              int32_t off_units) {
+  const int w = (threadIdx.x >> 5) - kExchangeWarp0;  // == warp % 4
+  const int lane = threadIdx.x & 31;
+  const int r = 32 * w + lane;
+  const uint32_t tl = sm.tmem_base + (uint32_t(32 * w) << 16);
+  const uint32_t peer = rank ^ 1u;
+  const uint32_t x_remote[2] = {mapa_shared(smem_u32(&sm.xbuf[0][0][r]), peer),
+                                mapa_shared(smem_u32(&sm.xbuf[1][0][r]), peer)};
+  const uint32_t xfull_remote[2] = {mapa_shared(smem_u32(&sm.xfull[0]), peer),
+                                    mapa_shared(smem_u32(&sm.xfull[1]), peer)};
+  constexpr uint32_t kChunkStride = kRows * 16;  // bytes from chunk q to chunk q + 1 of a row
+  int g = 0;
+  bool ok = true;
+  for (int32_t i = begin; i < end && ok; ++i) {
+    const int nb = unit_blocks(load_unit(p.iws, off_units, i));
+    for (int j = 0; j < nb; ++j) {
+      const int gb = g + j, xb = gb & 1;
+      ok = warp_wait(&sm.s_full[xb], (gb >> 1) & 1, &sm.abort);
+      if (!ok) break;
+      tc::fence_after_sync();
+      uint32_t sv[2][32];
+      const uint32_t scol = tl + kTmemS + 64u * uint32_t(xb);
+      tc::tmem_ld32(scol, sv[0]);
+      tc::tmem_ld32(scol + 32, sv[1]);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_read[xb]);
+      // the partner's softmax has read what was sent into this buffer for block gb - 2
+      if (gb >= 2) {
+        ok = warp_wait_cluster(&sm.xfree[xb], ((gb >> 1) - 1) & 1, &sm.abort);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int q = 0; q < kBlk / 4; ++q) {
+        const uint32_t* v = &sv[q >> 3][4 * (q & 7)];
+        st_async_v4(x_remote[xb] + kChunkStride * uint32_t(q), v[0], v[1], v[2], v[3], xfull_remote[xb]);
+      }
+    }
+    g += nb;
+  }
+}
+
 // ---------------------------------------------------------------- kernels
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -573,6 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&sm.empty[s], 1);  // MMA commit
     }
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_lat_full, 4);  // the four softmax warps
     mbar_init(&sm.q_empty, 1);
     mbar_init(&sm.s_full[0], 1);
     mbar_init(&sm.s_full[1], 1);
@@ -580,10 +656,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sm.pv_done, 1);
     mbar_init(&sm.o_ready, 1);
     mbar_init(&sm.o_free, 4);
-    mbar_init(&sm.xfull, 1);       // softmax thread 0's arrive.expect_tx; the partner's stores complete the bytes
-    mbar_init(&sm.xfree, 4);       // the partner's four softmax warps
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.xfull[b], 1);  // softmax thread 0's arrive.expect_tx; the partner's stores complete the bytes
+      mbar_init(&sm.xfree[b], 4);  // the partner's four softmax warps
+      mbar_init(&sm.s_read[b], 4); // this CTA's four exchange warps
+    }
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
+    // blocks 0 and 1 of the pair's stream land in xbuf 0 and 1
+    mbar_arrive_expect_tx(&sm.xfull[0], kRows * kBlk * 4);
+    mbar_arrive_expect_tx(&sm.xfull[1], kRows * kBlk * 4);
     fence_mbar_init();
   }
   if (warp == kAllocWarp) {
@@ -599,6 +681,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     producer(p, sm, rank, begin, end, off_units, off_req);
   } else if (warp == kMmaWarp) {
     mma_issuer(p, sm, begin, end, off_units);
+  } else if (warp >= kExchangeWarp0) {
+    exchange_role(p, sm, rank, begin, end, off_units);
   } else if (warp >= kSoftmaxWarp0) {
     softmax_role(p, sm, rank, begin, end, off_units);
   }
@@ -733,11 +817,8 @@ extern "C" fi_status fi_mla_decode_run(const fi_mla_plan_info* info, const void*
   Params p;
   std::memset(&p, 0, sizeof p);
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t qn_d[3] = {uint64_t(kDc), uint64_t(H), uint64_t(q_rows)};
-  const int64_t qn_s[2] = {q_nope_stride_head, q_nope_stride_tok};
   const uint64_t qp_d[3] = {uint64_t(FI_MLA_ROPE_DIM), uint64_t(H), uint64_t(q_rows)};
   const int64_t qp_s[2] = {q_pe_stride_head, q_pe_stride_tok};
-  const uint32_t qn_b[3] = {64u, uint32_t(kRows), 1u};
   const uint32_t qp_b[3] = {uint32_t(kRopeHalf), uint32_t(kRows), 1u};
   const uint64_t ckv_d[3] = {uint64_t(kDc), uint64_t(P), uint64_t(num_pages)};
   const int64_t ckv_s[2] = {ckv_stride_slot, ckv_stride_page};
@@ -745,11 +826,13 @@ extern "C" fi_status fi_mla_decode_run(const fi_mla_plan_info* info, const void*
   const int64_t kpe_s[2] = {kpe_stride_slot, kpe_stride_page};
   const uint32_t ckv_b[3] = {64u, uint32_t(P), 1u};
   const uint32_t kpe_b[3] = {uint32_t(kRopeHalf), uint32_t(P), 1u};
-  if (!make_map(&p.tm_qn, bf, q_nope, 3, qn_d, qn_s, qn_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&p.tm_qp, bf, q_pe, 3, qp_d, qp_s, qp_b, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_map(&p.tm_qp, bf, q_pe, 3, qp_d, qp_s, qp_b, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&p.tm_ckv, bf, ckv, 3, ckv_d, ckv_s, ckv_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&p.tm_kpe, bf, kpe, 3, kpe_d, kpe_s, kpe_b, CU_TENSOR_MAP_SWIZZLE_64B))
     return FI_ERR_UNSUPPORTED;
+  p.q_nope = static_cast<const uint16_t*>(q_nope);
+  p.qn_stride_tok = q_nope_stride_tok;
+  p.qn_stride_head = q_nope_stride_head;
   p.iws = static_cast<const int32_t*>(int_workspace_dev);
   p.status = static_cast<int32_t*>(int_workspace_dev) + FI_MLA_H_STATUS;
   p.kv_indices = kv_indices_dev;
