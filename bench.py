@@ -53,8 +53,12 @@ def _peaks():
 
 
 def _kernel_hash() -> str:
+    """Hash of the sources the paged-attention kernel is built from (the MLA
+    files build other kernels and are left out)."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "serving_attention_gb300", "csrc", "*"))):
+        if os.path.basename(f).startswith("mla"):
+            continue
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
