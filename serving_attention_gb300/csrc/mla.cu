@@ -72,7 +72,7 @@ constexpr uint32_t kTmemS = 256;
 constexpr uint32_t kTmemQ = 384;
 constexpr float kLazyRescale = 8.0f;  // log2 units: keep a stale max until it is 2^8 off
 constexpr int kMergeThreads = 128;
-constexpr int kMergeBlocksPerPair = 16;
+constexpr int kMergeBlocksPerPair = 32;
 
 // One KV block of this CTA's half: the latent rows as 4 groups of 64 dims
 // (128-byte rows, 128-byte swizzle, 8 KB each) and the RoPE rows (64-byte
@@ -705,46 +705,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // Merge of the chunks of split requests (the LSE-weighted combination of
-// partial states), and (0, -inf) for requests with no cached token.  One
-// block per (merge entry, head) task, grid-stride; thread t holds dims
-// 4t..4t+3.
+// partial states), and (0, -inf) for requests with no cached token.  One warp
+// per (merge entry, head) task, grid-stride; lane l holds dims 16l..16l+15,
+// so each part's row is one coalesced 2 KB read per warp.
 __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(const int32_t* iws, const float* fws,
                                                                   int64_t partial_o_offset, uint16_t* o, float* lse,
                                                                   int32_t num_heads) {
   const int32_t n_merge = __ldg(iws + FI_MLA_H_NUM_MERGE);
   const int32_t off_merge = __ldg(iws + FI_MLA_H_OFF_MERGE);
   const int64_t tasks = int64_t(n_merge) * num_heads;
-  const int t = threadIdx.x;
-  for (int64_t task = blockIdx.x; task < tasks; task += gridDim.x) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kWarps = kMergeThreads / 32;
+  for (int64_t task = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); task < tasks;
+       task += int64_t(gridDim.x) * kWarps) {
     const int32_t mi = int32_t(task / num_heads), h = int32_t(task - int64_t(mi) * num_heads);
     const int4 e = __ldg(reinterpret_cast<const int4*>(iws + off_merge) + mi);  // {b, part0, n_parts, 0}
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     float out_lse = -INFINITY;
     if (e.z > 0) {
       float M = -INFINITY;
-      for (int k = 0; k < e.z; ++k) M = fmaxf(M, __ldg(fws + int64_t(e.y + k) * kRows + h));
+      for (int k = lane; k < e.z; k += 32) M = fmaxf(M, __ldg(fws + int64_t(e.y + k) * kRows + h));
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, d));
       float L = 0.f;
       for (int k = 0; k < e.z; ++k) {
         const float s = __ldg(fws + int64_t(e.y + k) * kRows + h);
         const float wgt = M == -INFINITY ? 0.f : expf(s - M);
-        const float4 v = __ldg(reinterpret_cast<const float4*>(fws + partial_o_offset +
-                                                               (int64_t(e.y + k) * kRows + h) * kDc) + t);
+        const float4* v =
+            reinterpret_cast<const float4*>(fws + partial_o_offset + (int64_t(e.y + k) * kRows + h) * kDc) + 4 * lane;
+        float4 x[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[q] = __ldg(v + q);
         L += wgt;
-        acc.x += wgt * v.x;
-        acc.y += wgt * v.y;
-        acc.z += wgt * v.z;
-        acc.w += wgt * v.w;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[4 * q] += wgt * x[q].x;
+          acc[4 * q + 1] += wgt * x[q].y;
+          acc[4 * q + 2] += wgt * x[q].z;
+          acc[4 * q + 3] += wgt * x[q].w;
+        }
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[k] *= inv;
       out_lse = L > 0.f ? M + logf(L) : -INFINITY;
     }
     const int64_t row = int64_t(e.x) * num_heads + h;
-    uint2 pk;
-    pk.x = tc::pack2<__nv_bfloat16>(acc.x, acc.y);
-    pk.y = tc::pack2<__nv_bfloat16>(acc.z, acc.w);
-    reinterpret_cast<uint2*>(o + row * kDc)[t] = pk;
-    if (lse && t == 0) lse[row] = out_lse;
+    uint4 pk[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      pk[q].x = tc::pack2<__nv_bfloat16>(acc[8 * q], acc[8 * q + 1]);
+      pk[q].y = tc::pack2<__nv_bfloat16>(acc[8 * q + 2], acc[8 * q + 3]);
+      pk[q].z = tc::pack2<__nv_bfloat16>(acc[8 * q + 4], acc[8 * q + 5]);
+      pk[q].w = tc::pack2<__nv_bfloat16>(acc[8 * q + 6], acc[8 * q + 7]);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(o + row * kDc) + 2 * lane;
+    dst[0] = pk[0];
+    dst[1] = pk[1];
+    if (lse && lane == 0) lse[row] = out_lse;
   }
 }
 
@@ -792,7 +812,7 @@ extern "C" fi_status fi_mla_default_config(int device, fi_mla_config* out) {
   out->max_units = 1 << 15;
   out->max_parts = 512;
   out->min_chunk = 512;
-  out->split_factor = 3;
+  out->split_factor = 2;
   return FI_OK;
 }
 
