@@ -240,26 +240,47 @@ def bench_decode(dev, steps, warmup, clocks_index):
 
     b = workloads.llama8b_decode(device=dev)
     cfg = fi.default_plan_config(dev.index)
-    ws = fi.Workspace(cfg, device=dev)
+    # Two workspaces, used by alternate steps: the plan of step i + 1 (host
+    # planning and its copy to the device, on a side stream) overlaps the
+    # kernel of step i, as in a serving loop; a workspace is re-planned only
+    # once the kernel that read it has finished.
+    wss = [fi.Workspace(cfg, device=dev), fi.Workspace(cfg, device=dev)]
     kvi = torch.as_tensor(b.kv_indices, device=dev)
     o = torch.empty_like(b.q)
     lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=dev)
     args = (b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 32, 8, 128, 16, 0, b.num_pages)
+    released = [None, None]  # per workspace: event after the last kernel that read it
 
-    def step(ev=None):
-        info = fi.plan(ws, *args)
-        if ev is not None:
-            ev[0].record(stream)
-        fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
-        if ev is not None:
-            ev[1].record(stream)
+    def plan_on_side(k, copies=()):
+        with torch.cuda.stream(side):
+            if released[k] is not None:
+                side.wait_event(released[k])
+            for dst, src in copies:
+                dst.copy_(src, non_blocking=True)
+            info = fi.plan(wss[k], *args, stream=side)
+            ready = torch.cuda.Event()
+            ready.record(side)
+        stream.wait_event(ready)
         return info
 
-    for _ in range(warmup):
-        info = step()
+    def step(i, ev=None):
+        k = i & 1
+        info = plan_on_side(k)
+        if ev is not None:
+            ev[0].record(stream)
+        fi.run(wss[k], info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+        if ev is not None:
+            ev[1].record(stream)
+        released[k] = torch.cuda.Event()
+        released[k].record(stream)
+        return info
+
+    for i in range(warmup):
+        info = step(i)
     torch.cuda.synchronize()
-    assert fi.device_status(ws) == 0, "device status not ok"
+    assert all(fi.device_status(w) == 0 for w in wss), "device status not ok"
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier()
@@ -268,44 +289,62 @@ def bench_decode(dev, steps, warmup, clocks_index):
     with (nv if nv.lib is not None else ClockSampler(clocks_index)) as cs:
         t0.record(stream)
         for i in range(steps):
-            step(kev[i])
+            step(i, kev[i])
         t1.record(stream)
         torch.cuda.synchronize()
     total_ms = t0.elapsed_time(t1)
     kern_ms = [a.elapsed_time(c) for a, c in kev]
-    assert fi.device_status(ws) == 0, "device status not ok"
+    assert all(fi.device_status(w) == 0 for w in wss), "device status not ok"
     nbytes, _, _ = algorithmic(b)
 
     # end to end through the public API from pinned host buffers: Q and the
-    # page table in (plus the plan's work list), O and LSE out.  The KV cache
-    # stays resident in HBM: it is the serving state that persists across steps.
+    # page table in (plus the plan's work list), O and LSE out, every step.
+    # The KV cache stays resident in HBM: it is the serving state that
+    # persists across steps.  Inputs of step i + 1 go in on the side stream
+    # while step i computes, outputs of step i come back on a third stream
+    # while step i + 1 computes (double-buffered device copies).
     q_h = b.q.cpu().pin_memory()
     kvi_h = torch.as_tensor(b.kv_indices).pin_memory()
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d = torch.empty_like(b.q)
+    o_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+    lse_h = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
+    q_d = [torch.empty_like(b.q) for _ in range(2)]
+    kvi_d = [torch.empty_like(kvi) for _ in range(2)]
+    o_d = [torch.empty_like(o) for _ in range(2)]
+    lse_d = [torch.empty_like(lse) for _ in range(2)]
+    out = torch.cuda.Stream(device=dev)
+    drained = [None, None]  # per buffer set: event after its outputs were copied back
     h2d = q_h.numel() * q_h.element_size() + kvi_h.numel() * 4
-    d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
+    d2h = o_h[0].numel() * o_h[0].element_size() + lse_h[0].numel() * 4
 
-    def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        kvi.copy_(kvi_h, non_blocking=True)
-        info = fi.plan(ws, *args)
-        fi.run(ws, info, q_d, b.k, b.v, kvi, o, lse, b.sm_scale)
-        o_h.copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+    def e2e_step(i):
+        k = i & 1
+        info = plan_on_side(k, ((q_d[k], q_h), (kvi_d[k], kvi_h)))
+        if drained[k] is not None:
+            stream.wait_event(drained[k])
+        fi.run(wss[k], info, q_d[k], b.k, b.v, kvi_d[k], o_d[k], lse_d[k], b.sm_scale)
+        released[k] = torch.cuda.Event()
+        released[k].record(stream)
+        with torch.cuda.stream(out):
+            out.wait_event(released[k])
+            o_h[k].copy_(o_d[k], non_blocking=True)
+            lse_h[k].copy_(lse_d[k], non_blocking=True)
+            drained[k] = torch.cuda.Event()
+            drained[k].record(out)
         return info
 
-    for _ in range(warmup):
-        e2e_step()
+    for i in range(warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        info_e = e2e_step()
+    for i in range(steps):
+        info_e = e2e_step(i)
+    stream.wait_stream(out)  # the last step's outputs are on the host before the clock stops
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    # the pipelined copies moved the right data: same inputs, same (deterministic) kernel
+    assert torch.equal(o_h[(steps - 1) & 1], o.cpu()), "end-to-end output differs from the device-timed run"
     plan_bytes = info_e.int_ws_bytes_used
     return dict(batch=b, total_ms=total_ms, kern_ms=kern_ms, bytes=nbytes, clocks=cs.summary(), e2e_ms=e2e_ms,
                 h2d=h2d + plan_bytes, d2h=d2h, info=info)

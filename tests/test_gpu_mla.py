@@ -64,6 +64,7 @@ def _compare(o, lse, o_ref, l_ref):
     ([700, 333, 1], 16, 16, 128),                     # 16 heads: zero rows in the 128-row tile
     ([257, 1500], 128, 8, 64),                        # page 8: eight pages per block, many chunks
     ([2049, 4000], 64, 32, 512),
+    ([3000, 64], 128, 64, 64),                        # 47 chunks of one request: more parts than a warp has lanes
 ])
 def test_mla_small_full(lens, heads, page, min_chunk):
     b = workloads.make_mla_batch("mla", lens, heads, page, 700 + sum(lens),
