@@ -24,6 +24,7 @@ DEV = torch.device("cuda:0")
 
 
 def _run(b: workloads.MlaBatch, cfg=None, ws=None):
+    assert b.ckv.is_cuda and b.q_nope.is_cuda, "inputs live in device memory"
     if cfg is None:
         cfg = mla.default_config(0)
     if ws is None:
@@ -67,7 +68,7 @@ def _compare(o, lse, o_ref, l_ref):
     ([3000, 64], 128, 64, 64),                        # 47 chunks of one request: more parts than a warp has lanes
 ])
 def test_mla_small_full(lens, heads, page, min_chunk):
-    b = workloads.make_mla_batch("mla", lens, heads, page, 700 + sum(lens),
+    b = workloads.make_mla_batch("mla", lens, heads, page, 700 + sum(lens), device=DEV,
                                  pool_pages=sum((n + page - 1) // page for n in lens) + 3)
     cfg = mla.default_config(0, min_chunk=min_chunk)
     o, lse, info, _ = _run(b, cfg)
@@ -78,7 +79,7 @@ def test_mla_small_full(lens, heads, page, min_chunk):
 
 @pytest.mark.parametrize("seed", [801, 802])
 def test_mla_random_batches(seed):
-    b = workloads.random_mla_batch(seed, batch=24, kv_max=6000, num_heads=128, page_size=64)
+    b = workloads.random_mla_batch(seed, batch=24, kv_max=6000, num_heads=128, page_size=64, device=DEV)
     _compare(*_run(b, mla.default_config(0, min_chunk=256))[:2], *_oracle(b))
 
 
@@ -94,9 +95,23 @@ def test_mla_full_size_sampled():
 
 
 def test_mla_repeatable():
-    b = workloads.random_mla_batch(811, batch=8, kv_max=4000, num_heads=128, page_size=64)
+    b = workloads.random_mla_batch(811, batch=8, kv_max=4000, num_heads=128, page_size=64, device=DEV)
     cfg = mla.default_config(0, min_chunk=128)
     ws = mla.MlaWorkspace(cfg, device=DEV)
     o1, l1, _, _ = _run(b, cfg, ws)
     o2, l2, _, _ = _run(b, cfg, ws)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_mla_single_head_full_pages():
+    b = workloads.make_mla_batch("mla1", [64, 128, 65, 32], 1, 32, 821, device=DEV, pool_pages=12)
+    _compare(*_run(b, mla.default_config(0, min_chunk=64))[:2], *_oracle(b))
+
+
+def test_mla_one_long_request():
+    """65,536 cached tokens in one request: split over every pair, merged from
+    hundreds of partial states (part count near the workspace's capacity)."""
+    b = workloads.make_mla_batch("mla_long", [65536], 128, 64, 822, device=DEV)
+    o, lse, info, _ = _run(b, mla.default_config(0, min_chunk=128, max_parts=512))
+    assert info.num_parts > 100
+    _compare(o[:1], lse[:1], *_oracle(b))
