@@ -12,8 +12,9 @@ namespace fi {
 constexpr int kHeadDim = 128;
 
 // CUDA-core path (16-row decode tiles; prefill-class items too when pages are < 8 tokens)
-constexpr int kStageTokens = 64;       // KV tokens per pipeline stage
-constexpr int kStages = 4;             // depth of the K/V ring
+constexpr int kStageTokens = 128;      // KV tokens per pipeline stage
+constexpr int kStages = 3;             // depth of the K/V ring
+constexpr int kBoxLanes = kStageTokens / 32;  // page boxes a producer lane issues per stage at page size 1
 constexpr int kConsumerWarps = 8;
 constexpr int kFirstConsumerWarp = 4;  // warps 4..11 consume (warp 0 produces)
 constexpr int kThreads = 32 * 12;

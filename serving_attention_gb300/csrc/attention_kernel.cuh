@@ -4,7 +4,7 @@
 // of the FlashInfer paper summary, "3. 동적 부하 분산 스케줄링").  Per item
 // (request b, KV head hk, packed query rows [row0,row1), KV tokens [kv0,kv1)):
 //
-//  * warp 0 streams the chunk's K and V, 64 tokens per stage, into a 4-deep
+//  * warp 0 streams the chunk's K and V, 128 tokens per stage, into a 3-deep
 //    shared-memory ring: one TMA box per page and tensor, completion counted
 //    in bytes on the stage's mbarrier (see produce()).  Each K/V row of one
 //    head is 256 contiguous bytes.
@@ -38,12 +38,13 @@ __device__ __forceinline__ int groups_in_pass(int rows) {
 
 // ---------------------------------------------------------------- producer
 
-// K and V of one stage: 64 tokens of one KV head.  One unswizzled 4-D TMA box
-// (128 dims, 1 head, min(P, 64) slots, 1 page) per page and tensor, issued by
-// one lane per page; the page ids of the next stage are loaded one stage
-// ahead into the issuing lanes' registers (the wiki page's page-index
-// prefetch, "1) 블록-스파스 KV 포맷").  Pages past the request are addressed
-// out of bounds and arrive as zeros; stage tokens past the chunk are masked
+// K and V of one stage: 128 tokens of one KV head.  One unswizzled 4-D TMA box
+// (128 dims, 1 head, min(P, 128) slots, 1 page) per page and tensor, issued by
+// lane (box % 32); the page ids of the next stage are loaded one stage ahead
+// into the issuing lanes' registers (the wiki page's page-index prefetch,
+// "1) 블록-스파스 KV 포맷").  Pages past the chunk (which need not fill its last
+// stage) are addressed out of bounds and arrive as zeros without a read of
+// HBM; stage tokens past the chunk are masked
 // by the consumers.
 static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
                         int32_t off_req) {
@@ -66,33 +67,38 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
     const int nrows = item.row1 - item.row0;
     const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
     const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
-    const int npages = (rq.kv_len + P - 1) >> lp;
+    const int npages = min((rq.kv_len + P - 1) >> lp, (item.kv1 + P - 1) >> lp);  // pages the chunk touches
     const int32_t* pages = p.kv_indices + rq.page_start;
     for (int pass = 0; pass < passes; ++pass) {
-      int32_t nx0 = 0, nx1 = 0;
+      int32_t nx[kBoxLanes];  // page ids of the next stage's boxes lane, lane + 32, ...
       auto fetch_ids = [&](int st) {
         const int pg0 = (item.kv0 + st * kStageTokens) >> lp;
-        nx0 = (lane < boxes && pg0 + lane < npages) ? __ldg(pages + pg0 + lane) : p.num_pages;
-        nx1 = (lane + 32 < boxes && pg0 + lane + 32 < npages) ? __ldg(pages + pg0 + lane + 32) : p.num_pages;
+#pragma unroll
+        for (int r = 0; r < kBoxLanes; ++r) {
+          const int bx = lane + 32 * r;
+          nx[r] = (bx < boxes && pg0 + bx < npages) ? __ldg(pages + pg0 + bx) : p.num_pages;
+        }
       };
       if (nst > 0) fetch_ids(0);
       for (int st = 0; st < nst; ++st, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        const int32_t id0 = nx0, id1 = nx1;
+        int32_t id[kBoxLanes];
+#pragma unroll
+        for (int r = 0; r < kBoxLanes; ++r) id[r] = nx[r];
         if (st + 1 < nst) fetch_ids(st + 1);
         if (!warp_wait(&sm.empty[s], ph ^ 1, &sm.abort)) continue;
         if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
         __syncwarp();
         const int j0 = item.kv0 + st * kStageTokens;
         const int slot0 = P > kStageTokens ? (j0 & (P - 1)) : 0;
-        if (lane < boxes) {
-          tc::tma_load_4d(&sm.dec.k[s][lane * box_slots][0], &p.tm_kd, &sm.full[s], 0, item.hk, slot0, id0);
-          tc::tma_load_4d(&sm.dec.v[s][lane * box_slots][0], &p.tm_vd, &sm.full[s], 0, item.hk, slot0, id0);
-        }
-        if (lane + 32 < boxes) {
-          tc::tma_load_4d(&sm.dec.k[s][(lane + 32) * box_slots][0], &p.tm_kd, &sm.full[s], 0, item.hk, slot0, id1);
-          tc::tma_load_4d(&sm.dec.v[s][(lane + 32) * box_slots][0], &p.tm_vd, &sm.full[s], 0, item.hk, slot0, id1);
+#pragma unroll
+        for (int r = 0; r < kBoxLanes; ++r) {
+          const int bx = lane + 32 * r;
+          if (bx < boxes) {
+            tc::tma_load_4d(&sm.dec.k[s][bx * box_slots][0], &p.tm_kd, &sm.full[s], 0, item.hk, slot0, id[r]);
+            tc::tma_load_4d(&sm.dec.v[s][bx * box_slots][0], &p.tm_vd, &sm.full[s], 0, item.hk, slot0, id[r]);
+          }
         }
         armed[s] = ph;
       }
