@@ -204,7 +204,7 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   out->prefill_min_chunk = 1024;
   out->decode_cost_weight = 4;
   out->prefill_cost_weight = 6;
-  out->split_factor = 4;
+  out->split_factor = 1;
   out->window_left = -1;
   out->sink_tokens = 0;
   out->logits_soft_cap = 0.f;
