@@ -49,7 +49,7 @@ typedef struct {
     int32_t max_units;      /* KV chunks per plan */
     int32_t max_parts;      /* chunks of split requests per plan (fp32 partial states) */
     int32_t min_chunk;      /* smallest chunk, tokens, a multiple of 64 (default 512) */
-    int32_t split_factor;   /* target chunks per pair (default 2) */
+    int32_t split_factor;   /* target chunks per pair (default 1) */
     int32_t reserved[2];
 } fi_mla_config;
 

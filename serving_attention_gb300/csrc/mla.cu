@@ -812,7 +812,7 @@ extern "C" fi_status fi_mla_default_config(int device, fi_mla_config* out) {
   out->max_units = 1 << 15;
   out->max_parts = 512;
   out->min_chunk = 512;
-  out->split_factor = 2;
+  out->split_factor = 1;
   return FI_OK;
 }
 

@@ -77,7 +77,7 @@ def default_config(device: int = 0, **overrides) -> MlaConfig:
 def make_config(num_pairs: int, **overrides) -> MlaConfig:
     """A config without a device query (host planning, tests)."""
     cfg = MlaConfig(num_pairs=num_pairs, max_batch=4096, max_units=1 << 15, max_parts=512, min_chunk=512,
-                    split_factor=2)
+                    split_factor=1)
     for k, v in overrides.items():
         setattr(cfg, k, v)
     return cfg
