@@ -25,15 +25,18 @@
 //    softmax decisions, and accumulate P V into their own half of O;
 //  * tensor memory holds O (256 columns), the two S buffers (64 each) and the
 //    CTA's latent half of Q (256 bf16 dims per row, 128 columns), so shared
-//    memory keeps only the RoPE quarter of Q and five KV stages;
+//    memory keeps only the RoPE quarter of Q, four KV stages and two 32 KB
+//    exchange buffers;
 //  * roles per CTA: warp 0 loads the RoPE part of Q and the KV blocks with TMA;
 //    warp 1 issues the MMAs (S = Q K^T over 288 dims into TMEM, the latent part
 //    with Q read from TMEM, then O += P V with P read from TMEM over the S
 //    columns, N = 256); warps 4..7 write Q into TMEM, run the softmax (one head
-//    row per thread = one TMEM lane), the exchange and the epilogue;
-//  * S of block j+1 is issued before P V of block j, so the softmax of one
-//    block overlaps the MMAs of the next; the rare lazy rescale of O waits
-//    for the P V in flight first;
+//    row per thread = one TMEM lane) and the epilogue; warps 8..11 send each
+//    block's partial logits to the partner as soon as S is in TMEM;
+//  * S runs one block ahead of the softmax (S of block j + 2 is issued right
+//    after P V of block j, into the buffer P of block j occupied), so the
+//    softmax of one block overlaps the MMAs of the next; the rare lazy
+//    rescale of O waits for the P V in flight first;
 //  * a request cut into several chunks writes fp32 partial states that
 //    mla_merge_kernel combines (LSE-weighted).
 #include <cuda.h>
