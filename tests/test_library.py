@@ -70,3 +70,37 @@ def test_workspace_sizes():
     cfg = fi.make_plan_config(152)
     assert fi.int_workspace_bytes(cfg) % 16 == 0
     assert fi.float_workspace_bytes(cfg, 128) >= cfg.max_partial_rows * 129 * 4
+
+
+def test_mla_run_rejects_bad_arguments_before_cuda():
+    from serving_attention_gb300 import mla
+
+    lib = mla.load()
+    info = mla.MlaPlanInfo(num_pairs=2, batch=2, num_heads=128, page_size=64, max_parts=4)
+    # fake, 16-byte aligned pointers: only checks that return before any CUDA call run
+    args = [ctypes.byref(info), 16, 65536, 512, 32, 8192, 64, 2, 48, 32768, 512, 64, 4096, 64, 10, 80, 96, 112,
+            0.07, 128, 144, None]
+    bad = list(args)
+    bad[0] = None
+    assert lib.fi_mla_decode_run(*bad) == 1                     # no plan info
+    bad = list(args)
+    bad[7] = 1
+    assert lib.fi_mla_decode_run(*bad) == 1                     # fewer query rows than the plan's batch
+    bad = list(args)
+    bad[1] = 24
+    assert lib.fi_mla_decode_run(*bad) == 4                     # misaligned q_nope
+    bad = list(args)
+    bad[10] = 500
+    assert lib.fi_mla_decode_run(*bad) == 4                     # slot stride not a multiple of 16 bytes
+    info_bad = mla.MlaPlanInfo(num_pairs=2, batch=2, num_heads=128, page_size=4, max_parts=4)
+    bad = list(args)
+    bad[0] = ctypes.byref(info_bad)
+    assert lib.fi_mla_decode_run(*bad) == 2                     # page size 4
+    info_bad = mla.MlaPlanInfo(num_pairs=2, batch=2, num_heads=129, page_size=64, max_parts=4)
+    bad[0] = ctypes.byref(info_bad)
+    assert lib.fi_mla_decode_run(*bad) == 2                     # more than 128 heads
+    info_split = mla.MlaPlanInfo(num_pairs=2, batch=2, num_heads=128, page_size=64, max_parts=4, num_parts=3)
+    bad = list(args)
+    bad[0] = ctypes.byref(info_split)
+    bad[20] = None
+    assert lib.fi_mla_decode_run(*bad) == 1                     # split chunks need the float workspace
