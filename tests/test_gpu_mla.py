@@ -115,3 +115,15 @@ def test_mla_one_long_request():
     o, lse, info, _ = _run(b, mla.default_config(0, min_chunk=128, max_parts=512, split_factor=2))
     assert info.num_parts > 100
     _compare(o[:1], lse[:1], *_oracle(b))
+
+
+def test_mla_combined_576_layouts():
+    """Cache rows of 576 (latent then RoPE key) and query rows of 576 (nope then
+    pe), passed as strided views: the entry takes each part's own strides."""
+    b = workloads.make_mla_batch("mla576", [700, 64, 1], 128, 64, 831, device=DEV, pool_pages=16)
+    kv = torch.cat([b.ckv, b.kpe], dim=-1).contiguous()            # [pages, P, 576]
+    qq = torch.cat([b.q_nope, b.q_pe], dim=-1).contiguous()        # [B, H, 576]
+    v = workloads.MlaBatch(b.name, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_heads, b.page_size,
+                           b.sm_scale, qq[..., :512], qq[..., 512:], kv[..., :512], kv[..., 512:])
+    assert v.ckv.stride(1) == 576 and v.q_pe.stride(1) == 576
+    _compare(*_run(v, mla.default_config(0, min_chunk=128))[:2], *_oracle(b))
