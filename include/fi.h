@@ -281,6 +281,16 @@ fi_status fi_merge_states(const void* v_a, const float* s_a, const void* v_b, co
  * *status_out is FI_OK, FI_ERR_TIMEOUT or FI_ERR_DEVICE_CHECK. */
 fi_status fi_get_device_status(const void* int_workspace_dev, void* stream, int32_t* status_out);
 
+/*
+ * fi_selftest_bounded_wait -- check the failure path without a fault: one
+ * warp waits, with the kernels' own bounded wait (about 0.5 s of SM clocks),
+ * on a barrier that nothing completes; when the wait gives up it records
+ * FI_ERR_TIMEOUT in the status word of int_workspace_dev (the next plan
+ * copied into that workspace clears it).  Asynchronous on `stream`; read the
+ * result with fi_get_device_status.  The context stays usable.
+ */
+fi_status fi_selftest_bounded_wait(void* int_workspace_dev, void* stream);
+
 const char* fi_status_string(fi_status s);
 
 #ifdef __cplusplus

@@ -60,7 +60,8 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ["fi_default_plan_config", "fi_int_workspace_bytes", "fi_float_workspace_bytes", "fi_plan",
            "fi_plan_host", "fi_batch_paged_attention_run", "fi_batch_paged_attention_run_static_scratch",
-           "fi_merge_states", "fi_get_device_status", "fi_status_string", "fi_rope_init", "fi_rope_apply_k"]
+           "fi_merge_states", "fi_get_device_status", "fi_status_string", "fi_rope_init", "fi_rope_apply_k",
+           "fi_selftest_bounded_wait"]
 
 _lib = None
 
@@ -90,6 +91,8 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
     lib.fi_get_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.fi_rope_init.argtypes = [cfgp, vp, vp]
     lib.fi_rope_apply_k.argtypes = [infop, vp, i32, vp, vp, vp, vp, vp, ctypes.c_int, vp]
+    lib.fi_selftest_bounded_wait.argtypes = [vp, vp]
+    lib.fi_selftest_bounded_wait.restype = ctypes.c_int
     lib.fi_status_string.argtypes = [ctypes.c_int]
     lib.fi_status_string.restype = ctypes.c_char_p
     for name in ("fi_default_plan_config", "fi_plan", "fi_plan_host", "fi_batch_paged_attention_run",
@@ -266,6 +269,11 @@ def rope_apply_k(ws: Workspace, info: PlanInfo, k_in, k_out, kv_indices, max_kv_
     _check(load().fi_rope_apply_k(ctypes.byref(info), ws.int_ws.data_ptr(), int(max_kv_len), k_in.data_ptr(), ks_in,
                                   k_out.data_ptr(), ks_out, kv_indices.data_ptr(), _dtype_code(k_in),
                                   _stream_ptr(stream)), "fi_rope_apply_k")
+
+
+def selftest_bounded_wait(ws, stream=None):
+    """Enqueue the bounded-wait self-test on ws's int workspace (see fi.h)."""
+    _check(load().fi_selftest_bounded_wait(ws.int_ws.data_ptr(), _stream_ptr(stream)), "fi_selftest_bounded_wait")
 
 
 def device_status(ws: Workspace, stream=None) -> int:

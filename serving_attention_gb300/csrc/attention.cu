@@ -386,6 +386,34 @@ extern "C" fi_status fi_merge_states(const void* v_a, const float* s_a, const vo
   return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 
+namespace fi {
+
+// One warp waits, through the same bounded wait the kernels use, on an
+// mbarrier nothing arrives on: the wait gives up after its budget, and the
+// status word records the timeout exactly as a stalled kernel role would.
+__global__ void bounded_wait_selftest_kernel(int32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = warp_wait(&bar, 0, &abort_flag);
+  if (threadIdx.x == 0 && !ok) atomicOr(status, abort_flag);
+}
+
+}  // namespace fi
+
+extern "C" fi_status fi_selftest_bounded_wait(void* int_workspace_dev, void* stream) {
+  if (!int_workspace_dev) return FI_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(int_workspace_dev) & 15u) return FI_ERR_ALIGNMENT;
+  fi::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<int32_t*>(int_workspace_dev) + FI_H_STATUS);
+  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
 extern "C" fi_status fi_get_device_status(const void* int_workspace_dev, void* stream, int32_t* status_out) {
   if (!int_workspace_dev || !status_out) return FI_ERR_INVALID_ARG;
   int32_t word = 0;

@@ -1,0 +1,84 @@
+"""Failure detection on the GPU without a fault: a bounded wait that runs out
+and a plan that does not match its launch both end in a status word the host
+reads, and the context and the workspace stay usable afterwards."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from helpers import LSE_TOL, O_TOL, compare, gpu_run, oracle_problem
+import oracle
+import serving_attention_gb300 as fi
+from serving_attention_gb300 import mla
+import workloads
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+FI_ERR_DEVICE_CHECK, FI_ERR_TIMEOUT = 6, 7
+
+
+def _tiny():
+    return workloads.random_batch(901, batch=4, qo_max=1, kv_max=600, num_qo_heads=8, num_kv_heads=2, page_size=16,
+                                  causal=0, device=DEV, kv_min=1)
+
+
+def _check_parity(b, o, lse):
+    o_ref, l_ref = oracle.attention(oracle_problem(b))
+    n = b.total_qo
+    err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
+    assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
+
+
+def test_bounded_wait_runs_out_and_the_context_survives():
+    b = _tiny()
+    cfg = fi.default_plan_config(0)
+    ws = fi.Workspace(cfg, device=DEV)
+    fi.selftest_bounded_wait(ws)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == FI_ERR_TIMEOUT
+    # a new plan clears the status word; the same workspace then runs normally
+    o, lse, _, _ = gpu_run(b, cfg=cfg, ws=ws)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0
+    _check_parity(b, o, lse)
+
+
+def test_plan_that_does_not_match_the_launch_is_reported():
+    b = _tiny()
+    cfg = fi.default_plan_config(0)
+    ws = fi.Workspace(cfg, device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 0, b.num_pages)
+    bad = fi.PlanInfo.from_buffer_copy(info)
+    bad.num_ctas = info.num_ctas - 2  # grid no longer matches the plan's header
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    o = torch.full_like(b.q, float("nan"))
+    lse = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    fi.run(ws, bad, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == FI_ERR_DEVICE_CHECK
+    assert torch.isnan(o).all()  # no CTA did any work
+    o, lse, _, _ = gpu_run(b, cfg=cfg, ws=ws)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0
+    _check_parity(b, o, lse)
+
+
+def test_mla_plan_that_does_not_match_the_launch_is_reported():
+    b = workloads.make_mla_batch("mla_bad", [300, 64], 128, 64, 902, device=DEV, pool_pages=8)
+    cfg = mla.default_config(0)
+    ws = mla.MlaWorkspace(cfg, device=DEV)
+    info = mla.plan(ws, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_heads, b.page_size, b.num_pages)
+    bad = mla.MlaPlanInfo.from_buffer_copy(info)
+    bad.num_pairs = info.num_pairs - 1
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    o = torch.empty(b.q_nope.shape, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(b.q_nope.shape[:2], dtype=torch.float32, device=DEV)
+    mla.decode_run(ws, bad, b.q_nope, b.q_pe, b.ckv, b.kpe, kvi, o, lse, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == FI_ERR_DEVICE_CHECK
+    # re-planned, the same workspace runs normally
+    info = mla.plan(ws, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_heads, b.page_size, b.num_pages)
+    mla.decode_run(ws, info, b.q_nope, b.q_pe, b.ckv, b.kpe, kvi, o, lse, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0
+    assert torch.isfinite(o.float()).all()
