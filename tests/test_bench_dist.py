@@ -59,7 +59,7 @@ def test_whole_job_aggregate():
 
 
 def test_reference_arm_under_torchrun_prints_once():
-    """The launch the driver uses for N > 1, on CPU: rank 0 alone prints one line."""
+    """A torch.distributed.run launch with two ranks, on CPU: rank 0 alone prints one line."""
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
            "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference", "--gpus", "2",
            "--steps", "1", "--warmup", "1", "--cpu-budget", "0.5"]

@@ -13,7 +13,7 @@ Poison (so indexing and masking mistakes show as large errors):
     in V (BIG = 6e4 for fp16, 1e30 for bf16), finite so that a correctly
     masked slot contributes exactly 0.
 
-Workloads (sizes as the BASELINE configs state them):
+Workloads (the serving mixes they stand in for, with their sizes):
   tiny_decode        fp16, 4 requests, qo 1, kv U{1..512}, 8/2 heads, page 16, 256-page pool
   llama8b_decode     bf16, 64 requests, qo 1, kv floor(exp U(ln 512, ln 32768)), 32/8 heads, page 16
   ragged_prefill     bf16, 16 requests, qo U{128..4096}, prefix U{0..2048}, causal, 32/8 heads, page 16
