@@ -289,6 +289,27 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   if (!make_map(&p.tm_kd, tt, k_cache, 4, kd, ks, kbd, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map(&p.tm_vd, tt, v_cache, 4, kd, vs, kbd, CU_TENSOR_MAP_SWIZZLE_NONE))
     return FI_ERR_UNSUPPORTED;
+  // Page size 1 where a page's stride is a whole number R >= Hkv of head
+  // strides: each cache is a plain matrix of rows of 128 dims, row
+  // page * R + head, and the decode stages fetch four rows per TMA gather
+  // instead of one single-row box per token.
+  auto rows_per_page = [&](const int64_t* st) -> int64_t {
+    if (st[2] <= 0 || st[0] % st[2]) return 0;
+    const int64_t r = st[0] / st[2];
+    return (r >= info->num_kv_heads && (int64_t(num_pages) + 1) * r < (int64_t(1) << 31)) ? r : 0;
+  };
+  const int64_t rk = rows_per_page(k_strides), rv = rows_per_page(v_strides);
+  if (P == 1 && rk > 0 && rv > 0) {
+    const uint64_t gk[2] = {uint64_t(kHeadDim), uint64_t(num_pages) * uint64_t(rk)};
+    const uint64_t gv[2] = {uint64_t(kHeadDim), uint64_t(num_pages) * uint64_t(rv)};
+    const uint32_t gb[2] = {uint32_t(kHeadDim), 1u};
+    if (!make_map(&p.tm_kg, tt, k_cache, 2, gk, &k_strides[2], gb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&p.tm_vg, tt, v_cache, 2, gv, &v_strides[2], gb, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return FI_ERR_UNSUPPORTED;
+    p.gather_rows = 1;
+    p.gather_rows_k = int32_t(rk);
+    p.gather_rows_v = int32_t(rv);
+  }
   if (p.tc_prefill) {
     const uint64_t qd[3] = {uint64_t(kHeadDim), uint64_t(info->num_qo_heads), uint64_t(q_num_tokens)};
     const int64_t qs[2] = {q_stride_head, q_stride_tok};

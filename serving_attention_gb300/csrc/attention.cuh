@@ -54,8 +54,10 @@ struct RunParams {
   CUtensorMap tm_q;  // [q tokens, Hq, d] boxes of (64 dims, G heads, 128/G tokens), 128-byte swizzle
   CUtensorMap tm_k;  // [pages, P, Hkv, d] boxes of (64 dims, 1 head, P slots, 1 page), 128-byte swizzle
   CUtensorMap tm_v;
-  CUtensorMap tm_kd;  // [pages, P, Hkv, d] boxes of (128 dims, 1 head, min(P, 64) slots, 1 page), no swizzle
+  CUtensorMap tm_kd;  // [pages, P, Hkv, d] boxes of (128 dims, 1 head, min(P, 128) slots, 1 page), no swizzle
   CUtensorMap tm_vd;
+  CUtensorMap tm_kg;  // page size 1: [pages * rows_per_page, d], rows of 128 dims gathered four at a time
+  CUtensorMap tm_vg;
   CUtensorMap tm_o;   // O as [q tokens, Hq, d] with the boxes of tm_q: stores of whole 128-row output tiles
   const uint16_t* q;
   int64_t q_stride_tok, q_stride_head;
@@ -73,6 +75,9 @@ struct RunParams {
   float scale_log2;          // sm_scale * log2(e)
   int32_t num_qo_heads, num_kv_heads, group, page_size, log2_page, num_pages;
   int32_t tc_prefill;        // prefill-class items on the tensor cores (else CUDA cores)
+  int32_t gather_rows;       // page size 1: decode stages by 4-row gathers of rows page * rows_k/v + head
+  int32_t gather_rows_k;     // page stride / head stride of K (>= Hkv)
+  int32_t gather_rows_v;     // the same for V
 };
 
 struct DecodeBufs {

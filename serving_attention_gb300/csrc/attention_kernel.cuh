@@ -54,8 +54,8 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
   const int box_slots = P >= kStageTokens ? kStageTokens : P;
   constexpr uint32_t kStageBytes = 2u * kStageTokens * kHeadDim * 2u;
   if (lane == 0) {
-    tc::prefetch_tensormap(&p.tm_kd);
-    tc::prefetch_tensormap(&p.tm_vd);
+    tc::prefetch_tensormap(p.gather_rows ? &p.tm_kg : &p.tm_kd);
+    tc::prefetch_tensormap(p.gather_rows ? &p.tm_vg : &p.tm_vd);
   }
   uint32_t it = 0;
   int armed[kStages];
@@ -70,12 +70,14 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
     const int npages = min((rq.kv_len + P - 1) >> lp, (item.kv1 + P - 1) >> lp);  // pages the chunk touches
     const int32_t* pages = p.kv_indices + rq.page_start;
     for (int pass = 0; pass < passes; ++pass) {
-      int32_t nx[kBoxLanes];  // page ids of the next stage's boxes lane, lane + 32, ...
+      // page ids of the next stage's boxes: lane, lane + 32, ... (box loads)
+      // or 4 * lane .. 4 * lane + 3 (the four rows of a lane's gather)
+      int32_t nx[kBoxLanes];
       auto fetch_ids = [&](int st) {
         const int pg0 = (item.kv0 + st * kStageTokens) >> lp;
 #pragma unroll
         for (int r = 0; r < kBoxLanes; ++r) {
-          const int bx = lane + 32 * r;
+          const int bx = p.gather_rows ? kBoxLanes * lane + r : lane + 32 * r;
           nx[r] = (bx < boxes && pg0 + bx < npages) ? __ldg(pages + pg0 + bx) : p.num_pages;
         }
       };
@@ -92,12 +94,24 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
         __syncwarp();
         const int j0 = item.kv0 + st * kStageTokens;
         const int slot0 = P > kStageTokens ? (j0 & (P - 1)) : 0;
+        if (p.gather_rows) {
+          // page size 1: lane l brings tokens 4l..4l+3 of K and of V with one
+          // four-row gather each (row page * rows_per_page + hk; pages past
+          // the chunk are rows past the tensor and arrive as zeros)
+          static_assert(kBoxLanes == 4, "one four-row gather per lane and tensor");
+          const int rk = p.gather_rows_k, rv = p.gather_rows_v;
+          tc::tma_gather4_2d(&sm.dec.k[s][4 * lane][0], &p.tm_kg, &sm.full[s], 0, id[0] * rk + item.hk,
+                             id[1] * rk + item.hk, id[2] * rk + item.hk, id[3] * rk + item.hk);
+          tc::tma_gather4_2d(&sm.dec.v[s][4 * lane][0], &p.tm_vg, &sm.full[s], 0, id[0] * rv + item.hk,
+                             id[1] * rv + item.hk, id[2] * rv + item.hk, id[3] * rv + item.hk);
+        } else {
 #pragma unroll
-        for (int r = 0; r < kBoxLanes; ++r) {
-          const int bx = lane + 32 * r;
-          if (bx < boxes) {
-            tc::tma_load_4d(&sm.dec.k[s][bx * box_slots][0], &p.tm_kd, &sm.full[s], 0, item.hk, slot0, id[r]);
-            tc::tma_load_4d(&sm.dec.v[s][bx * box_slots][0], &p.tm_vd, &sm.full[s], 0, item.hk, slot0, id[r]);
+          for (int r = 0; r < kBoxLanes; ++r) {
+            const int bx = lane + 32 * r;
+            if (bx < boxes) {
+              tc::tma_load_4d(&sm.dec.k[s][bx * box_slots][0], &p.tm_kd, &sm.full[s], 0, item.hk, slot0, id[r]);
+              tc::tma_load_4d(&sm.dec.v[s][bx * box_slots][0], &p.tm_vd, &sm.full[s], 0, item.hk, slot0, id[r]);
+            }
           }
         }
         armed[s] = ph;

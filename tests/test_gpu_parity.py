@@ -118,6 +118,38 @@ def test_equal_and_unequal_strides_agree():
     assert torch.equal(o1[:n], o2[:n]) and torch.equal(l1[:n], l2[:n])
 
 
+def _pad_pages(t: torch.Tensor, pad: int):
+    """The same values in a cache whose pages are `pad` elements longer (page
+    stride no longer a whole number of head strides)."""
+    pool, P, H, D = t.shape
+    buf = torch.zeros((pool, P * H * D + pad), dtype=t.dtype, device=t.device)
+    view = buf.as_strided((pool, P, H, D), (P * H * D + pad, H * D, D, 1))
+    view.copy_(t)
+    return buf, view
+
+
+def test_page1_gather_and_box_fetches_agree():
+    """Page size 1.  K contiguous (2 rows per page) and V with a padding head
+    (3 rows per page) are fetched by four-row gathers; padded pages (page
+    stride 264 elements, not a multiple of the 128-element head stride) by one
+    box per token.  Both match the oracle, and both fetches land the same
+    bytes in shared memory, so the outputs are identical."""
+    b = workloads.random_batch(211, batch=7, qo_max=1, kv_max=700, num_qo_heads=8, num_kv_heads=2, page_size=1,
+                               causal=0, device=DEV, kv_min=0, v_pad_heads=1)
+    cfg = fi.default_plan_config(0, num_ctas=6, decode_min_chunk=64, split_factor=3)
+    _full_check(b, cfg=cfg)
+    o1, l1, _, _ = gpu_run(b, cfg=cfg)
+    kb, kp = _pad_pages(b.k, 8)
+    vb, vp = _pad_pages(b.v, 8)
+    b2 = workloads.PagedBatch(b.name, b.dtype, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len,
+                              b.num_qo_heads, b.num_kv_heads, b.page_size, b.causal, b.sm_scale, b.q, kp, vp, kb, vb)
+    _full_check(b2, cfg=cfg)
+    o2, l2, _, _ = gpu_run(b2, cfg=cfg)
+    torch.cuda.synchronize()
+    n = b.total_qo
+    assert torch.equal(o1[:n], o2[:n]) and torch.equal(l1[:n], l2[:n])
+
+
 def test_llama8b_decode_sampled():
     b = workloads.llama8b_decode(device=DEV)
     o, lse, info, ws = gpu_run(b)
