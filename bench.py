@@ -612,8 +612,9 @@ def bench_kv_strides(dev, flush, reps=5):
 
 
 def bench_shared_prefix(dev, flush, reps=5):
-    """Composable format: the dense prefix run (tensor cores, 64 branch queries),
-    the page-1 suffix run and fi_merge_states, captured in one CUDA graph,
+    """Composable format: the dense prefix run (tensor cores, 64 branch queries,
+    its split units merged by the late-merge launch that follows it), the page-1
+    suffix run and fi_merge_states, captured in one CUDA graph,
     against one run over the flat page-1 layout (prefix pages repeated in every
     branch's page list)."""
     import torch
@@ -669,7 +670,7 @@ def bench_shared_prefix(dev, flush, reps=5):
     return {"workload": "shared_prefix: 8192-token dense prefix + 64 branches, suffix U[64,512] at page 1",
             "composable_ms": res["composable"], "flat_ms": res["flat"],
             "composable_gbs": nbytes / res["composable"] / 1e6, "speedup_vs_flat": res["flat"] / res["composable"],
-            "launches": 3}
+            "launches": 3 + (1 if P[1].num_late_merge_units else 0) + (1 if S[1].num_late_merge_units else 0)}
 
 
 PROFILE_CASES = {

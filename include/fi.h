@@ -111,6 +111,8 @@ typedef struct {
     int32_t variant;             /* bit 0: logits soft-cap; bit 1: sliding window (and sink) mask; bit 2: RoPE */
     int64_t int_ws_bytes_used;   /* bytes of the int workspace written (and copied) by the plan */
     int64_t max_partial_rows;    /* capacity of the float workspace, from the config */
+    int32_t num_late_merge_units; /* split units of prefill-class tiles: merged by a second launch */
+    int32_t reserved;
 } fi_plan_info;
 
 /* Defaults, with num_ctas derived from the device's SM count and the run
@@ -217,7 +219,11 @@ fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_indptr, cons
  *
  * Asynchronous on `stream`; never allocates, synchronizes or copies from the
  * host, so it can be captured in a CUDA graph.  The kernel reads the counts
- * of the current plan from the int workspace.
+ * of the current plan from the int workspace.  When the plan has late merge
+ * units (info->num_late_merge_units > 0: split units of prefill-class tiles)
+ * a second kernel follows on the same stream and merges their partial states
+ * row-parallel; it merges nothing when the run has set the status word.
+ * `info` must be the one the plan returned for this workspace.
  */
 fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, int64_t q_stride_tok,
                                        int64_t q_stride_head, int32_t q_num_tokens, const void* k_cache,

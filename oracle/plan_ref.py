@@ -33,7 +33,9 @@ Rule:
     min(e, s + (i+1)*chunk)), ranges in order, chunk numbers running across
     them.  When a unit has n > 1 items it becomes a merge unit (numbered in
     unit order) and its items get consecutive fp32 partial-state rows,
-    n * rows in all.
+    n * rows in all.  A merge unit of a 256-row (prefill-class) unit carries
+    the flag 1 in its seventh field ("late": merged after the run by a
+    launch of its own), a 16-row unit 0 (merged inside the run).
  5. cost = (kv length of the item + 256) * class weight, the 256 standing for
     the fixed per-item latency of the kernel.  Items are sorted by
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
@@ -184,7 +186,7 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
         m = len(merges)
         base = part_rows
         nrows = r1 - r0
-        merges.append((b, hk, r0, r1, n, base, 0, 0))
+        merges.append((b, hk, r0, r1, n, base, 0 if T == TILE_DECODE else 1, 0))
         part_rows += n * nrows
         for i, (k0, k1) in enumerate(pieces):
             cost = (k1 - k0 + ITEM_COST_TOKENS) * weight[T]
@@ -236,7 +238,8 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
         ws[off_req + REQ_INTS * b: off_req + REQ_INTS * (b + 1)] = [qo[b], lq[b], kvp[b], lkv[b]]
 
     n_dec = sum(1 for _, f in items if lq[f[0]] * group <= 16)
-    info = dict(num_ctas=C, num_items=n_items, num_merge_units=n_merge, batch=batch,
+    info = dict(num_ctas=C, num_items=n_items, num_merge_units=n_merge,
+                num_late_merge_units=sum(1 for m in merges if m[6]), batch=batch,
                 num_partial_rows=part_rows, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,
                 head_dim=head_dim, page_size=page_size, causal=causal, chunk_decode=chunk[16],
                 chunk_prefill=chunk[TILE_PREFILL], num_decode_items=n_dec, num_prefill_items=n_items - n_dec,

@@ -52,7 +52,8 @@ class PlanInfo(ctypes.Structure):
                 ("causal", ctypes.c_int32), ("chunk_decode", ctypes.c_int32), ("chunk_prefill", ctypes.c_int32),
                 ("num_decode_items", ctypes.c_int32), ("num_prefill_items", ctypes.c_int32),
                 ("variant", ctypes.c_int32), ("int_ws_bytes_used", ctypes.c_int64),
-                ("max_partial_rows", ctypes.c_int64)]
+                ("max_partial_rows", ctypes.c_int64), ("num_late_merge_units", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -196,6 +196,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   chunks.reserve(units.size() * 2);
   std::vector<int32_t> merge_rows;  // FI_MERGE_INTS per merge unit
   int64_t partial_rows = 0;
+  int32_t n_late = 0;  // merge units of prefill-class tiles, merged after the run
   for (const Unit& u : units) {
     const int64_t chunk = u.tile == FI_TILE_DECODE ? chunk_dec : chunk_pre;
     const int64_t weight = u.tile == FI_TILE_DECODE ? cfg->decode_cost_weight : cfg->prefill_cost_weight;
@@ -210,8 +211,10 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
       merge_id = int32_t(merge_rows.size() / FI_MERGE_INTS);
       base = partial_rows;
       partial_rows += n * nrows;
-      const int32_t m[FI_MERGE_INTS] = {u.b, u.hk, u.row0, u.row1, int32_t(n), int32_t(base), 0, 0};
+      const int32_t late = u.tile == FI_TILE_DECODE ? 0 : 1;
+      const int32_t m[FI_MERGE_INTS] = {u.b, u.hk, u.row0, u.row1, int32_t(n), int32_t(base), late, 0};
       merge_rows.insert(merge_rows.end(), m, m + FI_MERGE_INTS);
+      n_late += late;
     }
     // chunk i of the unit: ranges in KV order, chunk numbers running across them
     int64_t i = 0;
@@ -313,6 +316,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   info.num_ctas = C;
   info.num_items = int32_t(n_items);
   info.num_merge_units = int32_t(n_merge);
+  info.num_late_merge_units = n_late;
   info.batch = batch;
   info.num_partial_rows = partial_rows;
   info.num_qo_heads = num_qo_heads;

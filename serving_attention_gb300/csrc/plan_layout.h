@@ -9,9 +9,13 @@
 //                  [kv0, kv1) the KV token range of this chunk,
 //                  part = first fp32 partial-state row or -1 (unsplit),
 //                  merge = merge unit or -1
-//   merge units  FI_MERGE_INTS each: {b, hk, row0, row1, n_chunks, part_base, 0, 0};
+//   merge units  FI_MERGE_INTS each: {b, hk, row0, row1, n_chunks, part_base, late, 0};
 //                  chunk i of the unit wrote partial rows part_base + i * (row1 - row0) ...
-//   counters     one per merge unit, zero between runs (the merging CTA resets it)
+//                  late = 1 (units of prefill-class tiles): merged after the run by
+//                  a row-parallel merge launch; late = 0: merged inside the run by
+//                  the CTA that finishes the unit's last chunk
+//   counters     one per merge unit, zero between runs (the merging CTA resets it;
+//                  late units never touch theirs)
 //   requests     FI_REQ_INTS each: {qo_start, qo_len, page_start, kv_len}
 //   ...          (the rest of the plan capacity)
 //   rope table   with RoPE: float2 (cos, sin) [rope_max_positions][64] at
@@ -30,6 +34,7 @@
 #define FI_ITEM_INTS 8
 #define FI_MERGE_INTS 8
 #define FI_REQ_INTS 4
+#define FI_MERGE_LATE 6  // index of the late flag in a merge unit
 
 #define FI_TILE_DECODE 16
 #define FI_TILE_PREFILL 256  // two 128-row M tiles sharing each K/V tile

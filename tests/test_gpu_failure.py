@@ -63,6 +63,30 @@ def test_plan_that_does_not_match_the_launch_is_reported():
     _check_parity(b, o, lse)
 
 
+def test_late_merge_skips_a_failed_run():
+    """With split prefill units the run is followed by the late merge launch;
+    when the run reports an error the merge writes nothing either."""
+    b = workloads.random_batch(903, batch=3, qo_max=60, kv_max=1500, num_qo_heads=8, num_kv_heads=2,
+                               page_size=16, causal=1, device=DEV, qo_min=20, kv_min=600)
+    cfg = fi.default_plan_config(0, num_ctas=6, prefill_min_chunk=128, split_factor=4)
+    ws = fi.Workspace(cfg, device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    assert info.num_late_merge_units > 0
+    bad = fi.PlanInfo.from_buffer_copy(info)
+    bad.num_ctas = info.num_ctas - 1
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    o = torch.full_like(b.q, float("nan"))
+    lse = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    fi.run(ws, bad, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == FI_ERR_DEVICE_CHECK
+    assert torch.isnan(o).all() and torch.isnan(lse).all()
+    o, lse, _, _ = gpu_run(b, cfg=cfg, ws=ws)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0
+    _check_parity(b, o, lse)
+
+
 def test_mla_plan_that_does_not_match_the_launch_is_reported():
     b = workloads.make_mla_batch("mla_bad", [300, 64], 128, 64, 902, device=DEV, pool_pages=8)
     cfg = mla.default_config(0)

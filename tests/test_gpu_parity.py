@@ -99,6 +99,18 @@ def test_random_small_full(seed, page, group, causal, dtype, qo_max, kv_max):
     assert info.num_items >= 6
 
 
+def test_late_merge_of_prefill_split_units():
+    """Prefill-class split units are merged after the run by the row-parallel
+    merge launch: 3 to 19 chunks per unit (past the merge's 4-wide load
+    groups, with ragged tails), row counts that are not multiples of the
+    8-row blocks, causal rows that see few keys."""
+    b = workloads.random_batch(221, batch=5, qo_max=130, kv_max=2600, num_qo_heads=8, num_kv_heads=2,
+                               page_size=16, causal=1, device=DEV, qo_min=37, kv_min=200)
+    cfg = fi.default_plan_config(0, num_ctas=40, prefill_min_chunk=128, split_factor=6)
+    info = _full_check(b, cfg=cfg)
+    assert info.num_late_merge_units == info.num_merge_units == 16  # 3 to 19 chunks per unit
+
+
 def test_empty_and_blind_rows():
     b = workloads.make_batch("edge", "bf16", [2, 1, 4, 3], [0, 5, 2, 40], 8, 2, 4, 1, 77, DEV, pool_pages=20)
     _full_check(b)

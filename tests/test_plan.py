@@ -97,6 +97,8 @@ def _check_invariants(ws, qop, kv, hq, hkv, causal, cfgd):
                     assert m >= 0 and all(c[3] == m for c in chunks)
                     mu = ws[off_merge + 8 * m: off_merge + 8 * m + 8]
                     assert tuple(mu[:4]) == (b, hk, r0, r1) and mu[4] == len(chunks)
+                    # merged after the run exactly when the unit is of the prefill class
+                    assert mu[6] == (1 if lq * G > 16 else 0) and mu[7] == 0
                     parts = [c[2] for c in chunks]
                     assert parts == [mu[5] + i * (r1 - r0) for i in range(len(chunks))]
                 else:
