@@ -11,7 +11,8 @@ needed between steps.
 
 The same JSON line also reports the ragged causal prefill batch (TFLOP/s,
 tensor-core bound) and the continuous-batching mix replayed through one CUDA
-graph across 10 re-plans, each against its own roof.
+graph across 10 re-plans (with its decode requests also timed on their own),
+each against its own roof.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -346,8 +347,13 @@ def bench_decode(dev, steps, warmup, clocks_index):
     # the pipelined copies moved the right data: same inputs, same (deterministic) kernel
     assert torch.equal(o_h[(steps - 1) & 1], o.cpu()), "end-to-end output differs from the device-timed run"
     plan_bytes = info_e.int_ws_bytes_used
+    plan_us = []
+    for _ in range(20):
+        t = time.perf_counter()
+        fi.plan_host(cfg, *args)
+        plan_us.append((time.perf_counter() - t) * 1e6)
     return dict(batch=b, total_ms=total_ms, kern_ms=kern_ms, bytes=nbytes, clocks=cs.summary(), e2e_ms=e2e_ms,
-                h2d=h2d + plan_bytes, d2h=d2h, info=info)
+                h2d=h2d + plan_bytes, d2h=d2h, info=info, plan_host_us=float(np.median(plan_us)))
 
 
 def bench_secondary(dev, reps=5):
@@ -361,7 +367,7 @@ def bench_secondary(dev, reps=5):
     out = {}
     cfg = fi.default_plan_config(dev.index)
     ws = fi.Workspace(cfg, device=dev)
-    for name, maker in (("ragged_prefill", workloads.ragged_prefill), ("continuous_batch", workloads.continuous_batch)):
+    for name, maker in (("ragged_prefill", workloads.ragged_prefill),):
         b = maker(device=dev)
         info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
                        128, b.page_size, b.causal, b.num_pages)
@@ -372,27 +378,134 @@ def bench_secondary(dev, reps=5):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            g.replay()
-            c.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(c))
+        ts = _replay_times(g, flush, 4 * reps)
+        warm = _replay_times(g, None, 4 * reps)
         assert fi.device_status(ws) == 0
         ms = float(np.median(ts))
         nbytes, formula, exact = algorithmic(b)
-        out[name] = dict(ms=ms, tflops_formula=formula / ms / 1e9, tflops_exact=exact / ms / 1e9,
+        out[name] = dict(ms=ms, ms_p10_p90=_p10_p90(ts), warm_l2_ms=float(np.median(warm)),
+                         tflops_formula=formula / ms / 1e9, tflops_exact=exact / ms / 1e9,
                          decode_gbs=nbytes / ms / 1e6, items=info.num_items)
         del b, o, lse, g
         torch.cuda.empty_cache()
+    out["continuous_batch"] = bench_mix(dev, flush, reps)
     out["shared_prefix"] = bench_shared_prefix(dev, flush, reps)
     out["kv_strides"] = bench_kv_strides(dev, flush, reps)
     out["variants"] = bench_variants(dev, flush, reps)
     out["mla"] = bench_mla(dev, flush, reps)
     return out
+
+
+def _replay_times(g, flush, reps):
+    """CUDA-event times (ms) of `reps` replays of graph g, each after an L2
+    flush when `flush` is a buffer (else back to back, warm L2)."""
+    import torch
+
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        c.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(c))
+    return ts
+
+
+def _p10_p90(ts):
+    return [float(np.percentile(ts, 10)), float(np.percentile(ts, 90))]
+
+
+def bench_mix(dev, flush, reps=5, replans=10):
+    """The continuous-batching mix as a serving loop runs it: buffers at the
+    capacity of the first `replans` seeded draws, one graph captured from
+    draw 0, then per draw new contents, a re-plan (host, with its copy) and
+    `reps` replays with L2 flushed.  Reports the median over draws of each
+    draw's median, p10/p90 over all replays, and the decode part alone: the
+    120 decode requests of every draw planned on their own and replayed
+    through a second graph (their queries and outputs are the buffers' rows
+    after the 8 x 512 prefill tokens)."""
+    import torch
+
+    import serving_attention_gb300 as fi
+    import workloads
+
+    pages, tokens = workloads.continuous_batch_capacity(replans)
+    cfg = fi.default_plan_config(dev.index)
+    b0 = workloads.continuous_batch(device=dev, replan=0, pool_pages=pages, q_tokens=tokens)
+    n_pf = 8
+    s0 = int(b0.qo_indptr[n_pf])  # decode rows start after the prefill tokens (the same for every draw)
+    q_buf, k_buf, v_base, v_buf = b0.q, b0.k_base, b0.v_base, b0.v
+    kvi_buf = torch.zeros(pages, dtype=torch.int32, device=dev)
+    kvi_dec = torch.zeros(pages, dtype=torch.int32, device=dev)
+    o = torch.zeros_like(q_buf)
+    lse = torch.zeros(q_buf.shape[:2], dtype=torch.float32, device=dev)
+    ws, ws_d = fi.Workspace(cfg, device=dev), fi.Workspace(cfg, device=dev)
+
+    def decode_part(b):
+        kvp = b.kv_indptr[n_pf:] - b.kv_indptr[n_pf]
+        return workloads.PagedBatch("continuous_batch.decode", b.dtype, b.qo_indptr[n_pf:] - s0, kvp,
+                                    b.kv_indices[b.kv_indptr[n_pf]:b.kv_indptr[-1]], b.last_page_len[n_pf:],
+                                    32, 8, 16, 1, b.sm_scale, q_buf[s0:], k_buf, v_buf, k_buf, v_base)
+
+    def plan(wsx, b, kvi):
+        info = fi.plan(wsx, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 32, 8, 128, 16, 1, pages)
+        kvi[:b.kv_indices.size].copy_(torch.as_tensor(b.kv_indices, device=dev))
+        return info
+
+    d0 = decode_part(b0)
+    info = plan(ws, b0, kvi_buf)
+    info_d = plan(ws_d, d0, kvi_dec)
+    run_all = lambda: fi.run(ws, info, q_buf, k_buf, v_buf, kvi_buf, o, lse, b0.sm_scale)  # noqa: E731
+    run_dec = lambda: fi.run(ws_d, info_d, q_buf[s0:], k_buf, v_buf, kvi_dec, o[s0:], lse[s0:],  # noqa: E731
+                             b0.sm_scale)
+    graphs = []
+    for fn in (run_all, run_dec):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    per, per_d, all_ts, gbs_d, plan_us, tf_exact, dec_gbs = [], [], [], [], [], [], []
+    for r in range(replans):
+        if r == 0:
+            b = b0
+        else:
+            b = workloads.continuous_batch(device=dev, replan=r, pool_pages=pages, q_tokens=tokens)
+            q_buf.copy_(b.q)
+            k_buf.copy_(b.k_base)
+            v_base.copy_(b.v_base)
+            b.q, b.k, b.v, b.k_base, b.v_base = q_buf, k_buf, v_buf, k_buf, v_base  # frees the draw's own copies
+        t = time.perf_counter()
+        fi.plan_host(cfg, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 32, 8, 128, 16, 1, pages)
+        plan_us.append((time.perf_counter() - t) * 1e6)
+        info_r = plan(ws, b, kvi_buf)
+        assert info_r.num_ctas == info.num_ctas
+        ts = _replay_times(graphs[0], flush, reps)
+        assert fi.device_status(ws) == 0
+        all_ts += ts
+        ms = float(np.median(ts))
+        per.append(ms)
+        nbytes, _, exact = algorithmic(b)
+        tf_exact.append(exact / ms / 1e9)
+        dec_gbs.append(nbytes / ms / 1e6)
+        d = decode_part(b)
+        plan(ws_d, d, kvi_dec)
+        ts_d = _replay_times(graphs[1], flush, reps)
+        assert fi.device_status(ws_d) == 0
+        ms_d = float(np.median(ts_d))
+        per_d.append(ms_d)
+        gbs_d.append(algorithmic(d)[0] / ms_d / 1e6)
+    del graphs
+    torch.cuda.synchronize()
+    return dict(ms=float(np.median(per)), ms_per_replan=per, ms_p10_p90=_p10_p90(all_ts),
+                tflops_exact=float(np.median(tf_exact)), decode_gbs=float(np.median(dec_gbs)),
+                decode_part_ms=float(np.median(per_d)), decode_part_gbs=float(np.median(gbs_d)),
+                decode_part_gbs_per_replan=gbs_d, plan_host_us=float(np.median(plan_us)), replans=replans,
+                items=info.num_items)
 
 
 def mla_algorithmic(b):
@@ -647,28 +760,21 @@ def bench_shared_prefix(dev, flush, reps=5):
     def flat_run():
         fi.run(F[0], F[1], flat.q, flat.k, flat.v, F[2], F[3], F[4], flat.sm_scale)
 
-    res = {}
+    res, spread = {}, {}
     for name, fn in (("composable", composable), ("flat", flat_run)):
         fn()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            g.replay()
-            c.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(c))
+        ts = _replay_times(g, flush, 20 * reps if name == "composable" else reps)
         res[name] = float(np.median(ts))
+        spread[name] = _p10_p90(ts)
     # algorithmic bytes of the composable form: the prefix KV once, every suffix token once, Q in, O/LSE out
     suffix_tokens = int(suf.kv_lens().sum())
     nbytes = (pre.meta["prefix_len"] + suffix_tokens) * 8 * 128 * 2 * 2 + 64 * 32 * (128 * 2 * 2 + 4)
     return {"workload": "shared_prefix: 8192-token dense prefix + 64 branches, suffix U[64,512] at page 1",
-            "composable_ms": res["composable"], "flat_ms": res["flat"],
+            "composable_ms": res["composable"], "composable_ms_p10_p90": spread["composable"], "flat_ms": res["flat"],
             "composable_gbs": nbytes / res["composable"] / 1e6, "speedup_vs_flat": res["flat"] / res["composable"],
             "launches": 3 + (1 if P[1].num_late_merge_units else 0) + (1 if S[1].num_late_merge_units else 0)}
 
@@ -881,7 +987,9 @@ def main():
                    "num_ctas": info.num_ctas, "items": info.num_items, "split_units": info.num_merge_units},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic, "kernel": HOT_KERNEL, "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": r["bytes"], "kernel_ms": kern_ms},
+                     "algorithmic_bytes_per_launch": r["bytes"], "kernel_ms": kern_ms,
+                     "kernel_ms_p10_p90": _p10_p90(r["kern_ms"])},
+        "plan_host_us": r["plan_host_us"],
         "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},
         "gpu_launches": a.steps,
         "clocks": r["clocks"],
@@ -893,9 +1001,15 @@ def main():
         line["prefill"] = {"workload": "ragged_prefill: 16 requests, qo U[128,4096], prefix U[0,2048], causal",
                            "ms": p["ms"], "tflops_formula": p["tflops_formula"], "tflops_exact": p["tflops_exact"],
                            "peak_tflops": tf, "frac_formula": p["tflops_formula"] / tf, "bound": "tensor"}
-        line["mix"] = {"workload": "continuous_batch: 8 chunked prefill (512) + 120 zipf decode, unequal K/V strides",
-                       "ms": m["ms"], "decode_gbs_over_kernel": m["decode_gbs"],
-                       "tflops_exact_over_kernel": m["tflops_exact"]}
+        line["prefill"].update(ms_p10_p90=p["ms_p10_p90"], warm_l2_ms=p["warm_l2_ms"])
+        line["mix"] = {"workload": "continuous_batch: 8 chunked prefill (512) + 120 zipf decode, unequal K/V strides, "
+                                   f"{m['replans']} re-plans through one graph",
+                       "ms": m["ms"], "ms_per_replan": m["ms_per_replan"], "ms_p10_p90": m["ms_p10_p90"],
+                       "decode_gbs_over_kernel": m["decode_gbs"], "tflops_exact_over_kernel": m["tflops_exact"],
+                       "decode_part": {"ms": m["decode_part_ms"], "gbs": m["decode_part_gbs"],
+                                       "frac_of_hbm": m["decode_part_gbs"] / hbm,
+                                       "gbs_per_replan": m["decode_part_gbs_per_replan"]},
+                       "plan_host_us": m["plan_host_us"]}
         sp = sec["shared_prefix"]
         line["shared_prefix"] = dict(sp, frac_of_hbm=sp["composable_gbs"] / hbm)
         line["kv_strides"] = sec["kv_strides"]

@@ -219,11 +219,15 @@ fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_indptr, cons
  *
  * Asynchronous on `stream`; never allocates, synchronizes or copies from the
  * host, so it can be captured in a CUDA graph.  The kernel reads the counts
- * of the current plan from the int workspace.  When the plan has late merge
- * units (info->num_late_merge_units > 0: split units of prefill-class tiles)
- * a second kernel follows on the same stream and merges their partial states
- * row-parallel; it merges nothing when the run has set the status word.
- * `info` must be the one the plan returned for this workspace.
+ * of the current plan from the int workspace.  When info->num_late_merge_units
+ * > 0 (split units of prefill-class tiles) a second kernel follows on the
+ * same stream and merges those units row-parallel, reading its counts from
+ * the workspace too; it merges nothing when the run has set the status word.
+ * With info->num_late_merge_units == 0 (as in a graph captured from a plan
+ * without late units) the run merges any late units of the current plan
+ * itself, one CTA per unit: correct either way, faster with the second
+ * kernel, so capture from a plan with late units when later plans may have
+ * them.
  */
 fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, int64_t q_stride_tok,
                                        int64_t q_stride_head, int32_t q_num_tokens, const void* k_cache,

@@ -35,7 +35,8 @@ Rule:
     unit order) and its items get consecutive fp32 partial-state rows,
     n * rows in all.  A merge unit of a 256-row (prefill-class) unit carries
     the flag 1 in its seventh field ("late": merged after the run by a
-    launch of its own), a 16-row unit 0 (merged inside the run).
+    launch of its own), a 16-row unit 0 (merged inside the run); the
+    header's last field counts the late units.
  5. cost = (kv length of the item + 256) * class weight, the 256 standing for
     the fixed per-item latency of the kernel.  Items are sorted by
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
@@ -222,7 +223,8 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     ws[:HEADER_INTS] = [MAGIC, n_items, n_merge, C, batch, causal, off_cta, off_items, off_merge,
                         off_cnt, off_req, 0, num_qo_heads, num_kv_heads, page_size, total_ints,
                         window, sink, bits(cap), rope_max,
-                        bits(theta) if rope_max > 0 else 0, bits(rscale) if rope_max > 0 else 0, rope_off, 0]
+                        bits(theta) if rope_max > 0 else 0, bits(rscale) if rope_max > 0 else 0, rope_off,
+                        sum(1 for m in merges if m[6])]
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos

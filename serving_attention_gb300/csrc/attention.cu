@@ -80,74 +80,80 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
 }
 
 // Late merge of split units (those the plan marks late: prefill-class
-// tiles), launched after the run on the same stream.  Block (unit, 8-row
-// group), one warp per packed row, lane l holding dims 4l..4l+3.  The
-// arithmetic and the chunk order are those of the in-run merge, so a unit's
-// result does not depend on which of the two merged it.  Nothing is merged
-// when the status word reports an error (the partial states may be
-// incomplete).
+// tiles), launched after the run on the same stream.  Tasks are (merge unit,
+// packed row) pairs, unit-major, walked by every warp of a fixed grid with a
+// grid stride, and the counts come from the workspace header, so a graph
+// captured once replays correctly for any later plan.  Lane l holds dims
+// 4l..4l+3.  The arithmetic and the chunk order are those of the in-run
+// merge, so a unit's result does not depend on which of the two merged it.
+// Nothing is merged when the status word reports an error (the partial
+// states may be incomplete).
 template <typename T>
 __global__ void __launch_bounds__(256) late_merge_kernel(const int32_t* __restrict__ iws,
                                                          const float* __restrict__ fws, int64_t partial_o_offset,
                                                          T* o, int64_t o_stride_tok, int64_t o_stride_head,
                                                          float* lse, int num_qo_heads, int group) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (iws[FI_H_STATUS] != 0) return;
-  const int32_t* mu = iws + iws[FI_H_OFF_MERGE] + int64_t(FI_MERGE_INTS) * blockIdx.x;
-  if (!mu[FI_MERGE_LATE]) return;
-  const int row0 = mu[2], nrows = mu[3] - row0;
-  const int pr = int(blockIdx.y) * 8 + warp;
-  if (pr >= nrows) return;
-  const int n = mu[4];
-  const int64_t base = mu[5];
-  const int32_t* rq = iws + iws[FI_H_OFF_REQUESTS] + int64_t(FI_REQ_INTS) * mu[0];
-  constexpr int kUnroll = 4;
-  float M = -INFINITY;
-  for (int c = 0; c < n; ++c) M = fmaxf(M, __ldcg(fws + base + int64_t(c) * nrows + pr));
-  float Ls = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int c0 = 0; c0 < n; c0 += kUnroll) {
-      float l[kUnroll];
-      float4 v[kUnroll];
+  const int lane = threadIdx.x & 31;
+  if (iws[FI_H_STATUS] != 0 || iws[FI_H_NUM_LATE_MERGE] == 0) return;
+  const int64_t tasks = int64_t(iws[FI_H_NUM_MERGE]) * FI_TILE_PREFILL;
+  const int32_t* merge = iws + iws[FI_H_OFF_MERGE];
+  const int32_t* reqs = iws + iws[FI_H_OFF_REQUESTS];
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t task = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks; task += warps) {
+    const int32_t* mu = merge + FI_MERGE_INTS * (task / FI_TILE_PREFILL);
+    const int pr = int(task % FI_TILE_PREFILL);
+    const int row0 = mu[2], nrows = mu[3] - row0;
+    if (!mu[FI_MERGE_LATE] || pr >= nrows) continue;
+    const int n = mu[4];
+    const int64_t base = mu[5];
+    constexpr int kUnroll = 4;
+    float M = -INFINITY;
+    for (int c = 0; c < n; ++c) M = fmaxf(M, __ldcg(fws + base + int64_t(c) * nrows + pr));
+    float Ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int c0 = 0; c0 < n; c0 += kUnroll) {
+        float l[kUnroll];
+        float4 v[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (c0 + u < n) {
-          const int64_t prw = base + int64_t(c0 + u) * nrows + pr;
-          l[u] = __ldcg(fws + prw);
-          v[u] = __ldcg(reinterpret_cast<const float4*>(fws + partial_o_offset + prw * kHeadDim) + lane);
+        for (int u = 0; u < kUnroll; ++u) {
+          if (c0 + u < n) {
+            const int64_t prw = base + int64_t(c0 + u) * nrows + pr;
+            l[u] = __ldcg(fws + prw);
+            v[u] = __ldcg(reinterpret_cast<const float4*>(fws + partial_o_offset + prw * kHeadDim) + lane);
+          }
         }
-      }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (c0 + u < n) {
-          const float w = ex2((l[u] - M) * 1.4426950408889634f);
-          Ls += w;
-          acc.x += w * v[u].x;
-          acc.y += w * v[u].y;
-          acc.z += w * v[u].z;
-          acc.w += w * v[u].w;
+        for (int u = 0; u < kUnroll; ++u) {
+          if (c0 + u < n) {
+            const float w = ex2((l[u] - M) * 1.4426950408889634f);
+            Ls += w;
+            acc.x += w * v[u].x;
+            acc.y += w * v[u].y;
+            acc.z += w * v[u].z;
+            acc.w += w * v[u].w;
+          }
         }
       }
     }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    const int row = row0 + pr;
+    const int t = row / group;
+    const int head = mu[1] * group + (row - t * group);
+    const int64_t tok = int64_t(reqs[FI_REQ_INTS * mu[0]]) + t;
+    uint2 packed;
+    packed.x = Elem<T>::from_float2(acc.x * inv, acc.y * inv);
+    packed.y = Elem<T>::from_float2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(o + tok * o_stride_tok + int64_t(head) * o_stride_head + lane * 4) = packed;
+    if (lane == 0 && lse) lse[tok * num_qo_heads + head] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
   }
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-  const int row = row0 + pr;
-  const int t = row / group;
-  const int head = mu[1] * group + (row - t * group);
-  const int64_t tok = int64_t(rq[0]) + t;
-  uint2 packed;
-  packed.x = Elem<T>::from_float2(acc.x * inv, acc.y * inv);
-  packed.y = Elem<T>::from_float2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(o + tok * o_stride_tok + int64_t(head) * o_stride_head + lane * 4) = packed;
-  if (lane == 0 && lse) lse[tok * num_qo_heads + head] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
 }
 
 template <typename T>
-cudaError_t launch_late_merge(const RunParams& p, int32_t num_merge_units, cudaStream_t s) {
-  const dim3 grid(unsigned(num_merge_units), unsigned(FI_TILE_PREFILL / 8));
-  late_merge_kernel<T><<<grid, 256, 0, s>>>(p.iws, p.fws, p.partial_o_offset, reinterpret_cast<T*>(p.o),
-                                            p.o_stride_tok, p.o_stride_head, p.lse, p.num_qo_heads, p.group);
+cudaError_t launch_late_merge(const RunParams& p, int32_t blocks, cudaStream_t s) {
+  late_merge_kernel<T><<<unsigned(blocks), 256, 0, s>>>(p.iws, p.fws, p.partial_o_offset, reinterpret_cast<T*>(p.o),
+                                                        p.o_stride_tok, p.o_stride_head, p.lse, p.num_qo_heads,
+                                                        p.group);
   return cudaGetLastError();
 }
 
@@ -398,11 +404,15 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The plan's variant picks the instantiation: bit 0 logits soft-cap, bit 1
   // sliding window / sink mask, bit 2 RoPE; the plain kernel carries none.
+  // The late merge follows the run when the plan in `info` has late units;
+  // a graph captured from a plan without any replays no late merge, and the
+  // run then merges late units of later plans itself.
+  p.late_merge = info->num_late_merge_units > 0 ? 1 : 0;
   cudaError_t e = dtype == FI_BF16 ? launch_variant<__nv_bfloat16>(p, info->num_ctas, info->variant, s)
                                    : launch_variant<__half>(p, info->num_ctas, info->variant, s);
-  if (e == cudaSuccess && info->num_late_merge_units > 0)
-    e = dtype == FI_BF16 ? launch_late_merge<__nv_bfloat16>(p, info->num_merge_units, s)
-                         : launch_late_merge<__half>(p, info->num_merge_units, s);
+  if (e == cudaSuccess && p.late_merge)
+    e = dtype == FI_BF16 ? launch_late_merge<__nv_bfloat16>(p, info->num_ctas, s)
+                         : launch_late_merge<__half>(p, info->num_ctas, s);
   return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 

@@ -75,6 +75,7 @@ struct RunParams {
   float scale_log2;          // sm_scale * log2(e)
   int32_t num_qo_heads, num_kv_heads, group, page_size, log2_page, num_pages;
   int32_t tc_prefill;        // prefill-class items on the tensor cores (else CUDA cores)
+  int32_t late_merge;        // the late merge launch follows this run (else late units merge in the run)
   int32_t gather_rows;       // page size 1: decode stages by 4-row gathers of rows page * rows_k/v + head
   int32_t gather_rows_k;     // page stride / head stride of K (>= Hkv)
   int32_t gather_rows_v;     // the same for V

@@ -135,12 +135,12 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
 // synchronise on named barrier `bar`; the barrier sequence depends only on
 // the plan, never on the abort flag, so all participating warps pass it.
 // Units the plan marks late (prefill-class tiles, up to 256 rows) are left to
-// the row-parallel merge launched after the run: one SM reading all their
-// partial states would hold the run's end back.
+// the row-parallel merge launched after the run, when one follows: one SM
+// reading all their partial states would hold the run's end back.
 template <typename T>
 __device__ void merge_split_unit(const RunParams& p, const Item& item, const Request& rq, int32_t off_merge,
                                  int32_t off_cnt, int tid, int nthreads, int bar, int* flag, int aborted) {
-  if (__ldg(p.iws + off_merge + FI_MERGE_INTS * item.merge + FI_MERGE_LATE)) return;
+  if (p.late_merge && __ldg(p.iws + off_merge + FI_MERGE_INTS * item.merge + FI_MERGE_LATE)) return;
   const int G = p.group;
   const int nrows = item.row1 - item.row0;
   __threadfence();

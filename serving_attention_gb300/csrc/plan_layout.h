@@ -15,7 +15,9 @@
 //                  a row-parallel merge launch; late = 0: merged inside the run by
 //                  the CTA that finishes the unit's last chunk
 //   counters     one per merge unit, zero between runs (the merging CTA resets it;
-//                  late units never touch theirs)
+//                  late units merged after the run never touch theirs; when the run
+//                  is not followed by the late merge, as when a graph was captured
+//                  from a plan without late units, it merges them itself)
 //   requests     FI_REQ_INTS each: {qo_start, qo_len, page_start, kv_len}
 //   ...          (the rest of the plan capacity)
 //   rope table   with RoPE: float2 (cos, sin) [rope_max_positions][64] at
@@ -65,7 +67,8 @@ enum {
   FI_H_ROPE_MAX_POS = 19,     // 0: no RoPE
   FI_H_ROPE_THETA_BITS = 20,
   FI_H_ROPE_SCALE_BITS = 21,
-  FI_H_ROPE_TABLE_OFF = 22    // ints from the workspace start to the cos/sin table
+  FI_H_ROPE_TABLE_OFF = 22,   // ints from the workspace start to the cos/sin table
+  FI_H_NUM_LATE_MERGE = 23    // merge units flagged late
 };
 
 #define FI_ROPE_PAIRS 64  // dims i and i + 64 of head_dim 128 form a rotated pair

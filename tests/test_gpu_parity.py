@@ -111,6 +111,66 @@ def test_late_merge_of_prefill_split_units():
     assert info.num_late_merge_units == info.num_merge_units == 16  # 3 to 19 chunks per unit
 
 
+def test_graph_templates_with_and_without_late_units():
+    """A graph captured from a plan without late units replays a plan with
+    them (the run merges them itself); a graph captured from a plan with late
+    units replays one without (the late merge finds nothing) and one with
+    them again.  Both merges give the same bits, and every replay matches the
+    oracle."""
+    cfg = fi.default_plan_config(0, num_ctas=40, prefill_min_chunk=128, decode_min_chunk=64, split_factor=6)
+    bB = workloads.make_batch("graph_pf", "bf16", [80, 45, 61, 90], [1900, 1200, 1500, 1000], 8, 2, 16, 1, 231,
+                              DEV, poison=False)
+    rng = np.random.default_rng(232)
+    kvA = rng.integers(1, 600, size=6)
+    kvpA, lplA = workloads._pages_for(kvA, 16)
+    kviA = rng.permutation(bB.num_pages)[:kvpA[-1]].astype(np.int32)
+    bA = workloads.PagedBatch("graph_dec", "bf16", np.arange(7, dtype=np.int32), kvpA, kviA, lplA, 8, 2, 16, 0,
+                              bB.sm_scale, bB.q, bB.k, bB.v, bB.k_base, bB.v_base)
+    kvi_buf = torch.zeros(bB.num_pages, dtype=torch.int32, device=DEV)
+    refs = {}
+
+    def replan(ws, b):
+        info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, b.causal,
+                       b.num_pages)
+        kvi_buf[:b.kv_indices.size].copy_(torch.as_tensor(b.kv_indices, device=DEV))
+        return info
+
+    def check(b, o, lse):
+        if b.name not in refs:
+            refs[b.name] = oracle.attention(oracle_problem(b))
+        n = b.total_qo
+        err_o, err_l = compare(o[:n], lse[:n], *refs[b.name])
+        assert err_o <= O_TOL and err_l <= LSE_TOL, (b.name, err_o, err_l)
+
+    outs = {}
+    for first, later in ((bA, [bB]), (bB, [bA, bB])):
+        ws = fi.Workspace(cfg, device=DEV)
+        o = torch.full_like(bB.q, float("nan"))
+        lse = torch.full(bB.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+        info = replan(ws, first)
+        assert (info.num_late_merge_units > 0) == (first is bB)
+        fi.run(ws, info, bB.q, bB.k, bB.v, kvi_buf, o, lse, bB.sm_scale)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fi.run(ws, info, bB.q, bB.k, bB.v, kvi_buf, o, lse, bB.sm_scale)
+        for b in [first] + later:
+            info_b = replan(ws, b)
+            assert info_b.num_ctas == info.num_ctas
+            o.fill_(float("nan"))
+            lse.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert fi.device_status(ws) == 0
+            check(b, o, lse)
+            if b is bB:
+                outs[first.name] = (o[:b.total_qo].clone(), lse[:b.total_qo].clone())
+        del graph
+    # bB merged in the run (template bA) and by the late merge (template bB)
+    assert torch.equal(outs["graph_dec"][0], outs["graph_pf"][0])
+    assert torch.equal(outs["graph_dec"][1], outs["graph_pf"][1])
+
+
 def test_empty_and_blind_rows():
     b = workloads.make_batch("edge", "bf16", [2, 1, 4, 3], [0, 5, 2, 40], 8, 2, 4, 1, 77, DEV, pool_pages=20)
     _full_check(b)
