@@ -418,6 +418,16 @@ def _p10_p90(ts):
     return [float(np.percentile(ts, 10)), float(np.percentile(ts, 90))]
 
 
+def tail_requests(b, first: int):
+    """Requests first.. of a batch as a batch of their own: (qo_indptr,
+    kv_indptr, kv_indices, last_page_len) re-based to start at 0, and the
+    query row where they start in the original batch."""
+    start = int(b.qo_indptr[first])
+    k0, k1 = int(b.kv_indptr[first]), int(b.kv_indptr[-1])
+    return (b.qo_indptr[first:] - start, b.kv_indptr[first:] - k0, b.kv_indices[k0:k1],
+            b.last_page_len[first:len(b.qo_indptr) - 1], start)
+
+
 def bench_mix(dev, flush, reps=5, replans=10):
     """The continuous-batching mix as a serving loop runs it: buffers at the
     capacity of the first `replans` seeded draws, one graph captured from
@@ -445,10 +455,10 @@ def bench_mix(dev, flush, reps=5, replans=10):
     ws, ws_d = fi.Workspace(cfg, device=dev), fi.Workspace(cfg, device=dev)
 
     def decode_part(b):
-        kvp = b.kv_indptr[n_pf:] - b.kv_indptr[n_pf]
-        return workloads.PagedBatch("continuous_batch.decode", b.dtype, b.qo_indptr[n_pf:] - s0, kvp,
-                                    b.kv_indices[b.kv_indptr[n_pf]:b.kv_indptr[-1]], b.last_page_len[n_pf:],
-                                    32, 8, 16, 1, b.sm_scale, q_buf[s0:], k_buf, v_buf, k_buf, v_base)
+        qo, kvp, kvi, lpl, start = tail_requests(b, n_pf)
+        assert start == s0
+        return workloads.PagedBatch("continuous_batch.decode", b.dtype, qo, kvp, kvi, lpl, 32, 8, 16, 1,
+                                    b.sm_scale, q_buf[s0:], k_buf, v_buf, k_buf, v_base)
 
     def plan(wsx, b, kvi):
         info = fi.plan(wsx, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 32, 8, 128, 16, 1, pages)

@@ -38,3 +38,22 @@ def test_mla_bytes_and_flops():
     pages = 1 + 0 + 9
     assert nbytes == 75 * (512 + 64) * 2 + pages * 4 + 3 * 16 * (576 * 2 + 512 * 2 + 4)
     assert flops == 75 * 16 * (2 * 576 + 2 * 512)
+
+
+def test_mix_decode_part_is_the_decode_requests():
+    """The mix's decode part: requests 8.. re-based as a batch of their own
+    hold exactly the decode requests' pages, lengths and query rows, and
+    their bytes are the mix's bytes minus the prefill requests'."""
+    b = workloads.continuous_batch(n_prefill=3, n_decode=7, chunk=16, prefix_max=40, kv_max=300)
+    qo, kvp, kvi, lpl, start = bench.tail_requests(b, 3)
+    assert start == 3 * 16 and qo[0] == 0 and np.array_equal(np.diff(qo), np.ones(7))
+    assert kvp[0] == 0 and kvp[-1] == kvi.size
+    for r in range(7):
+        orig = b.kv_indices[b.kv_indptr[3 + r]:b.kv_indptr[4 + r]]
+        assert np.array_equal(kvi[kvp[r]:kvp[r + 1]], orig)
+    assert np.array_equal(lpl, b.last_page_len[3:])
+    d = workloads.PagedBatch("d", b.dtype, qo, kvp, kvi, lpl, 32, 8, 16, 1, b.sm_scale, b.q[start:], b.k, b.v)
+    assert np.array_equal(d.kv_lens(), b.kv_lens()[3:])
+    head = workloads.PagedBatch("h", b.dtype, b.qo_indptr[:4], b.kv_indptr[:4], b.kv_indices, b.last_page_len[:3],
+                                32, 8, 16, 1, b.sm_scale, b.q, b.k, b.v)
+    assert bench.algorithmic(d)[0] + bench.algorithmic(head)[0] == bench.algorithmic(b)[0]
