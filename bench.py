@@ -742,6 +742,29 @@ def bench_shared_prefix(dev, flush, reps=5):
     branch's page list)."""
     import torch
 
+    composable, flat_run, nbytes, late = _shared_prefix_runs(dev)
+    res, spread = {}, {}
+    for name, fn in (("composable", composable), ("flat", flat_run)):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        ts = _replay_times(g, flush, 20 * reps if name == "composable" else reps)
+        res[name] = float(np.median(ts))
+        spread[name] = _p10_p90(ts)
+    return {"workload": "shared_prefix: 8192-token dense prefix + 64 branches, suffix U[64,512] at page 1",
+            "composable_ms": res["composable"], "composable_ms_p10_p90": spread["composable"], "flat_ms": res["flat"],
+            "composable_gbs": nbytes / res["composable"] / 1e6, "speedup_vs_flat": res["flat"] / res["composable"],
+            "launches": 3 + late}
+
+
+def _shared_prefix_runs(dev):
+    """The shared-prefix workload planned three ways: returns the composable
+    step (prefix run, suffix run, state merge), the flat run, the algorithmic
+    bytes of the composable form and how many late-merge launches it adds."""
+    import torch
+
     import serving_attention_gb300 as fi
     import workloads
 
@@ -770,23 +793,16 @@ def bench_shared_prefix(dev, flush, reps=5):
     def flat_run():
         fi.run(F[0], F[1], flat.q, flat.k, flat.v, F[2], F[3], F[4], flat.sm_scale)
 
-    res, spread = {}, {}
-    for name, fn in (("composable", composable), ("flat", flat_run)):
-        fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        ts = _replay_times(g, flush, 20 * reps if name == "composable" else reps)
-        res[name] = float(np.median(ts))
-        spread[name] = _p10_p90(ts)
     # algorithmic bytes of the composable form: the prefix KV once, every suffix token once, Q in, O/LSE out
     suffix_tokens = int(suf.kv_lens().sum())
     nbytes = (pre.meta["prefix_len"] + suffix_tokens) * 8 * 128 * 2 * 2 + 64 * 32 * (128 * 2 * 2 + 4)
-    return {"workload": "shared_prefix: 8192-token dense prefix + 64 branches, suffix U[64,512] at page 1",
-            "composable_ms": res["composable"], "composable_ms_p10_p90": spread["composable"], "flat_ms": res["flat"],
-            "composable_gbs": nbytes / res["composable"] / 1e6, "speedup_vs_flat": res["flat"] / res["composable"],
-            "launches": 3 + (1 if P[1].num_late_merge_units else 0) + (1 if S[1].num_late_merge_units else 0)}
+    late = (1 if P[1].num_late_merge_units else 0) + (1 if S[1].num_late_merge_units else 0)
+
+    def check():
+        return max(fi.device_status(x[0]) for x in (P, S, F))
+
+    composable.check = check
+    return composable, flat_run, nbytes, late
 
 
 PROFILE_CASES = {
@@ -797,6 +813,7 @@ PROFILE_CASES = {
     "continuous_batch": lambda dev: __import__("workloads").continuous_batch(device=dev),
     "mla_decode": lambda dev: __import__("workloads").mla_decode(device=dev),
     "mla_decode_16": lambda dev: __import__("workloads").mla_decode(device=dev, batch=16),
+    "shared_prefix": None,  # the composable step: prefix run (+ late merge), suffix run, state merge
 }
 
 
@@ -808,6 +825,15 @@ def profile_case(name: str, launches: int) -> int:
     import serving_attention_gb300 as fi
 
     dev = _device_setup(0)
+    if name == "shared_prefix":
+        composable, _, nbytes, late = _shared_prefix_runs(dev)
+        for _ in range(launches):
+            composable()
+        torch.cuda.synchronize()
+        st = composable.check()
+        print(json.dumps({"profile": name, "launches": launches, "kernels_per_launch": 3 + late, "status": st,
+                          "algorithmic_bytes": nbytes}))
+        return 0 if st == 0 else 3
     b = PROFILE_CASES[name](dev)
     if name.startswith("mla"):
         return _profile_mla(name, b, dev, launches)

@@ -84,8 +84,9 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
 // packed row) pairs, unit-major, walked by every warp of a fixed grid with a
 // grid stride, and the counts come from the workspace header, so a graph
 // captured once replays correctly for any later plan.  Lane l holds dims
-// 4l..4l+3.  The arithmetic and the chunk order are those of the in-run
-// merge, so a unit's result does not depend on which of the two merged it.
+// 4l..4l+3.  The arithmetic and the chunk order of the sums are those of the
+// in-run merge, so a unit's result does not depend on which of the two
+// merged it.
 // Nothing is merged when the status word reports an error (the partial
 // states may be incomplete).
 template <typename T>
@@ -106,32 +107,39 @@ __global__ void __launch_bounds__(256) late_merge_kernel(const int32_t* __restri
     if (!mu[FI_MERGE_LATE] || pr >= nrows) continue;
     const int n = mu[4];
     const int64_t base = mu[5];
-    constexpr int kUnroll = 4;
+    const float* part_lse = fws + base + pr;  // chunk c at [c * nrows]
+    const float4* part_o = reinterpret_cast<const float4*>(fws + partial_o_offset + (base + pr) * kHeadDim) + lane;
+    const int64_t o_step = int64_t(nrows) * (kHeadDim / 4);  // float4s from chunk c to c + 1
+    // groups of 32 chunks: lane c holds chunk c's LSE, the group's max comes
+    // from a butterfly, and the partial rows are loaded 8 at a time ahead of
+    // their use; the weights and sums still run in chunk order
     float M = -INFINITY;
-    for (int c = 0; c < n; ++c) M = fmaxf(M, __ldcg(fws + base + int64_t(c) * nrows + pr));
+    for (int c0 = 0; c0 < n; c0 += 32)
+      M = fmaxf(M, c0 + lane < n ? __ldcg(part_lse + int64_t(c0 + lane) * nrows) : -INFINITY);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float Ls = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-      for (int c0 = 0; c0 < n; c0 += kUnroll) {
-        float l[kUnroll];
-        float4 v[kUnroll];
+      for (int c0 = 0; c0 < n; c0 += 32) {
+        const float w_mine =
+            c0 + lane < n ? ex2((__ldcg(part_lse + int64_t(c0 + lane) * nrows) - M) * 1.4426950408889634f) : 0.f;
+        const int cn = min(32, n - c0);
+        for (int g0 = 0; g0 < cn; g0 += 8) {
+          float4 v[8];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          if (c0 + u < n) {
-            const int64_t prw = base + int64_t(c0 + u) * nrows + pr;
-            l[u] = __ldcg(fws + prw);
-            v[u] = __ldcg(reinterpret_cast<const float4*>(fws + partial_o_offset + prw * kHeadDim) + lane);
-          }
-        }
+          for (int u = 0; u < 8; ++u)
+            if (g0 + u < cn) v[u] = __ldcg(part_o + int64_t(c0 + g0 + u) * o_step);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          if (c0 + u < n) {
-            const float w = ex2((l[u] - M) * 1.4426950408889634f);
-            Ls += w;
-            acc.x += w * v[u].x;
-            acc.y += w * v[u].y;
-            acc.z += w * v[u].z;
-            acc.w += w * v[u].w;
+          for (int u = 0; u < 8; ++u) {
+            const float w = __shfl_sync(0xffffffffu, w_mine, (g0 + u) & 31);
+            if (g0 + u < cn) {
+              Ls += w;
+              acc.x += w * v[u].x;
+              acc.y += w * v[u].y;
+              acc.z += w * v[u].z;
+              acc.w += w * v[u].w;
+            }
           }
         }
       }
@@ -411,8 +419,8 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   cudaError_t e = dtype == FI_BF16 ? launch_variant<__nv_bfloat16>(p, info->num_ctas, info->variant, s)
                                    : launch_variant<__half>(p, info->num_ctas, info->variant, s);
   if (e == cudaSuccess && p.late_merge)
-    e = dtype == FI_BF16 ? launch_late_merge<__nv_bfloat16>(p, info->num_ctas, s)
-                         : launch_late_merge<__half>(p, info->num_ctas, s);
+    e = dtype == FI_BF16 ? launch_late_merge<__nv_bfloat16>(p, 4 * info->num_ctas, s)
+                         : launch_late_merge<__half>(p, 4 * info->num_ctas, s);
   return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 
