@@ -605,16 +605,21 @@ namespace fi {
 
 // A CTA's items come prefill-class (256-row tiles) first, then decode-class
 // (16-row tiles); returns the index of its first decode-class item.
+// Called by whole warps: lane l looks at item i0 + l (its request's row count
+// decides the class), so 32 items cost two dependent loads, not 64.
 __device__ __forceinline__ int32_t first_decode_item(const RunParams& p, int32_t begin, int32_t end, int32_t off_items,
                                                      int32_t off_req) {
-  int32_t i = begin;
-  while (i < end) {
-    const Item it = load_item(p.iws, off_items, i);
-    const Request rq = load_request(p.iws, off_req, it.b);
-    if (rq.qo_len * p.group <= FI_TILE_DECODE) break;
-    ++i;
+  const int lane = threadIdx.x & 31;
+  for (int32_t i0 = begin; i0 < end; i0 += 32) {
+    bool dec = true;  // past the CTA's last item counts as the boundary
+    if (i0 + lane < end) {
+      const int32_t b = __ldg(p.iws + off_items + FI_ITEM_INTS * (i0 + lane));
+      dec = __ldg(p.iws + off_req + FI_REQ_INTS * b + 1) * p.group <= FI_TILE_DECODE;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, dec);
+    if (m) return min(end, i0 + __ffs(m) - 1);
   }
-  return i;
+  return end;
 }
 
 template <typename T, bool kCap, bool kMask, bool kRope>
