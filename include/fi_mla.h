@@ -48,9 +48,9 @@ typedef struct {
     int32_t max_batch;      /* requests per plan */
     int32_t max_units;      /* KV chunks per plan */
     int32_t max_parts;      /* chunks of split requests per plan (fp32 partial states) */
-    int32_t min_chunk;      /* smallest chunk, tokens, a multiple of 64 (default 512) */
-    int32_t split_factor;   /* target chunks per pair (default 1) */
-    int32_t reserved[2];
+    int32_t min_chunk;      /* shortest piece cut off a request (a request's last piece may be
+                               shorter), tokens, a multiple of 64 (default 256) */
+    int32_t reserved[3];
 } fi_mla_config;
 
 typedef struct {
@@ -61,7 +61,7 @@ typedef struct {
     int32_t batch;
     int32_t num_heads;
     int32_t page_size;
-    int32_t chunk;          /* tokens per chunk chosen by the plan */
+    int32_t chunk;          /* the first pair's budget, token-equivalents (tokens + 192 per piece) */
     int64_t int_ws_bytes_used;
     int32_t max_parts;
     int32_t reserved;

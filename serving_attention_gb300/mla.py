@@ -25,8 +25,7 @@ EXPORTS = ["fi_mla_default_config", "fi_mla_int_workspace_bytes", "fi_mla_float_
 
 class MlaConfig(ctypes.Structure):
     _fields_ = [("num_pairs", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("max_units", ctypes.c_int32),
-                ("max_parts", ctypes.c_int32), ("min_chunk", ctypes.c_int32), ("split_factor", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("max_parts", ctypes.c_int32), ("min_chunk", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_ if k != "reserved"}
@@ -76,8 +75,7 @@ def default_config(device: int = 0, **overrides) -> MlaConfig:
 
 def make_config(num_pairs: int, **overrides) -> MlaConfig:
     """A config without a device query (host planning, tests)."""
-    cfg = MlaConfig(num_pairs=num_pairs, max_batch=4096, max_units=1 << 15, max_parts=512, min_chunk=512,
-                    split_factor=1)
+    cfg = MlaConfig(num_pairs=num_pairs, max_batch=4096, max_units=1 << 15, max_parts=512, min_chunk=256)
     for k, v in overrides.items():
         setattr(cfg, k, v)
     return cfg

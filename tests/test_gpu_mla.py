@@ -109,11 +109,11 @@ def test_mla_single_head_full_pages():
 
 
 def test_mla_one_long_request():
-    """65,536 cached tokens in one request: split over every pair, merged from
-    hundreds of partial states (part count near the workspace's capacity)."""
+    """65,536 cached tokens in one request: one piece on every pair, merged
+    from as many partial states as there are pairs."""
     b = workloads.make_mla_batch("mla_long", [65536], 128, 64, 822, device=DEV)
-    o, lse, info, _ = _run(b, mla.default_config(0, min_chunk=128, max_parts=512, split_factor=2))
-    assert info.num_parts > 100
+    o, lse, info, _ = _run(b, mla.default_config(0, min_chunk=128, max_parts=512))
+    assert info.num_parts == info.num_units == info.num_pairs
     _compare(o[:1], lse[:1], *_oracle(b))
 
 
