@@ -255,7 +255,7 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
 MLA_MAGIC = 0x464D4C31
 MLA_HEADER_INTS = 16
 MLA_BLOCK = 64
-MLA_UNIT_COST_TOKENS = 192
+MLA_UNIT_COST_TOKENS = 448
 
 
 def mla_make_plan(kv_indptr, last_page_len, page_size: int, num_heads: int, num_pairs: int,
@@ -264,15 +264,15 @@ def mla_make_plan(kv_indptr, last_page_len, page_size: int, num_heads: int, num_
      1. L_b = (pages_b - 1) * page_size + last_page_len[b] (0 without pages).
      2. The requests with L_b > 0, in index order, are one stream of tokens;
         the pairs take consecutive pieces of it, pair 0 first.
-     3. A piece costs its tokens + 192.  When pair c starts, with T tokens
+     3. A piece costs its tokens + 448.  When pair c starts, with T tokens
         and n requests (started or not) still unplaced and q = pairs - c
-        pairs left, its budget is max(ceil((T + 192 * (n + q - 1)) / q),
-        192 + min_chunk).
+        pairs left, its budget is max(ceil((T + 448 * (n + q - 1)) / q),
+        448 + min_chunk).
      4. Pair c repeatedly takes the next piece of the current request: the
-        rest of the request if that fits in (budget left - 192) rounded down
+        rest of the request if that fits in (budget left - 448) rounded down
         to a multiple of 64, else that rounded amount; it takes nothing and
         stops if the piece would be shorter than both the rest and
-        min_chunk.  After each piece it stops when the budget left minus 192
+        min_chunk.  After each piece it stops when the budget left minus 448
         is under 64.  The last pair takes all that is left, whatever its
         budget.
      5. A request in several pieces gets consecutive partial slots in stream

@@ -29,7 +29,7 @@
 #define FI_MLA_MERGE_INTS 4
 #define FI_MLA_BLOCK 64              // KV tokens per block of the decode kernel
 #define FI_MLA_ROWS 128              // query heads per tile (the MMA's M)
-#define FI_MLA_UNIT_COST_TOKENS 192  // fixed cost of a chunk in the deal, in KV tokens
+#define FI_MLA_UNIT_COST_TOKENS 448  // fixed cost of a piece in the split, in KV tokens (measured)
 
 enum {
   FI_MLA_H_MAGIC = 0,

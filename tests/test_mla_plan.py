@@ -88,7 +88,7 @@ def _pair_costs(img):
     units = _units(img)
     off, P = img[6], img[2]
     ptr = img[off:off + P + 1]
-    return np.array([(units[ptr[p]:ptr[p + 1], 2] - units[ptr[p]:ptr[p + 1], 1] + 192).sum() for p in range(P)])
+    return np.array([(units[ptr[p]:ptr[p + 1], 2] - units[ptr[p]:ptr[p + 1], 1] + plan_ref.MLA_UNIT_COST_TOKENS).sum() for p in range(P)])
 
 
 @pytest.mark.parametrize("pairs", [74, 76])
@@ -112,7 +112,7 @@ def test_split_balance_random(seed):
     _, img, info = _plan(b, 76)
     cost = _pair_costs(img)
     used = cost[cost > 0]
-    assert cost.max() <= used.mean() + 2 * (192 + 256) + 64
+    assert cost.max() <= used.mean() + 2 * (plan_ref.MLA_UNIT_COST_TOKENS + 256) + 64
 
 
 def test_rejects():
