@@ -398,42 +398,38 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
   const uint32_t xfree_remote[2] = {mapa_shared(smem_u32(&sm.xfree[0]), peer),
                                     mapa_shared(smem_u32(&sm.xfree[1]), peer)};
   const bool row_ok = r < p.num_heads;
-  // The query rows of chunk `chunk` into TMEM once the previous chunk's last S
-  // has read them: this CTA's 256 latent dims of row r as 128 columns of pairs
-  // (rows past the heads are zeros).
-  auto load_q = [&](const Unit& q_unit, int chunk) -> bool {
-    if (!warp_wait(&sm.q_empty, (chunk & 1) ^ 1, &sm.abort)) return false;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + int64_t(q_unit.b) * p.qn_stride_tok +
-                                                      int64_t(row_ok ? r : 0) * p.qn_stride_head) +
-                       kHalf / 8 * int(rank);
-    uint32_t qv[4][32];
-#pragma unroll
-    for (int h = 0; h < 4; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint4 v = row_ok ? __ldg(src + 8 * h + e) : make_uint4(0u, 0u, 0u, 0u);
-        qv[h][4 * e] = v.x;
-        qv[h][4 * e + 1] = v.y;
-        qv[h][4 * e + 2] = v.z;
-        qv[h][4 * e + 3] = v.w;
-      }
-#pragma unroll
-    for (int h = 0; h < 4; ++h) tc::tmem_st32(tl + kTmemQ + 32u * h, qv[h]);
-    tc::tmem_st_wait();
-    tc::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.q_lat_full);
-    return true;
-  };
   int g = 0, nu = 0;
   bool ok = true;
-  Unit u{};
-  if (begin < end) {
-    u = load_unit(p.iws, off_units, begin);
-    ok = load_q(u, 0);
-  }
   for (int32_t i = begin; i < end && ok; ++i) {
+    const Unit u = load_unit(p.iws, off_units, i);
     const int nb = unit_blocks(u);
+    // The chunk's query rows into TMEM once the previous chunk's last S has
+    // read them: this CTA's 256 latent dims of row r as 128 columns of pairs
+    // (rows past the heads are zeros).
+    ok = warp_wait(&sm.q_empty, (nu & 1) ^ 1, &sm.abort);
+    if (!ok) break;
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + int64_t(u.b) * p.qn_stride_tok +
+                                                        int64_t(row_ok ? r : 0) * p.qn_stride_head) +
+                         kHalf / 8 * int(rank);
+      uint32_t qv[4][32];
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 v = row_ok ? __ldg(src + 8 * h + e) : make_uint4(0u, 0u, 0u, 0u);
+          qv[h][4 * e] = v.x;
+          qv[h][4 * e + 1] = v.y;
+          qv[h][4 * e + 2] = v.z;
+          qv[h][4 * e + 3] = v.w;
+        }
+#pragma unroll
+      for (int h = 0; h < 4; ++h) tc::tmem_st32(tl + kTmemQ + 32u * h, qv[h]);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.q_lat_full);
+    }
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j < nb; ++j) {
       const int gb = g + j;
@@ -528,15 +524,6 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
       m = m_new;
     }
     if (!ok) break;
-    // The next chunk's Q goes in before this chunk's epilogue (its last S has
-    // read Q already), so the MMA warp computes the next chunk's first logits
-    // and the exchange warps send them while the epilogue runs.
-    Unit u_next{};
-    if (i + 1 < end) {
-      u_next = load_unit(p.iws, off_units, i + 1);
-      ok = load_q(u_next, nu + 1);
-      if (!ok) break;
-    }
     // Epilogue: O / l -- bf16 output of an unsplit chunk, else the fp32
     // partial state; LSE in natural log (written by CTA 0 of the pair).
     ok = warp_wait(&sm.o_ready, nu & 1, &sm.abort);
@@ -585,7 +572,6 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
     }
     g += nb;
     ++nu;
-    u = u_next;
   }
 }
 
