@@ -287,7 +287,7 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   out->max_merge_units = 1 << 15;
   out->max_partial_rows = int64_t(1) << 19;
   out->decode_min_chunk = 256;
-  out->prefill_min_chunk = 512;
+  out->prefill_min_chunk = 1024;
   out->decode_cost_weight = 4;
   out->prefill_cost_weight = 6;
   out->split_factor = 1;
