@@ -35,9 +35,11 @@
 //    of 64 KV tokens with a barrier each, so P V starts on the first half
 //    while the second is computed.  The two warpgroups run on different M
 //    tiles, so on every SM sub-partition one warp computes while the other
-//    waits.  At the end: read O, divide by the row sum, store O (a whole
-//    output tile through shared memory and TMA stores) and LSE, or an fp32
-//    partial state.
+//    waits.  Two row sums: one of the 16-bit P values that P V multiplies,
+//    which divides O (so O weighs every key by exactly what P V used), and
+//    one of the fp32 P, the exact normaliser, which gives LSE.  At the end:
+//    read O, divide by its row sum, store O (a whole output tile through
+//    shared memory and TMA stores) and LSE, or an fp32 partial state.
 #pragma once
 #include <type_traits>
 
@@ -357,7 +359,9 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         lim = min(causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1, item.kv1 - 1);
         if (kMask) lo = window_low(var, rq.kv_len - rq.qo_len + t);
       }
-      float mrun = -INFINITY, lrun = 0.f;
+      // lrun: sum of the fp32 P (the exact normaliser, for LSE); lrun_r: sum
+      // of the 16-bit P that P V multiplies (the normaliser of O)
+      float mrun = -INFINITY, lrun = 0.f, lrun_r = 0.f;
       bool ok = true;
       for (int j = 0; j < ntiles; ++j) {
         ok = ok && warp_wait(&sm.s_full[mt], tiles & 1, &sm.abort);
@@ -385,14 +389,18 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
               if (key > lim || (kMask && key < lo && key >= var.sink)) sv[h][e] = 0xff800000u;  // -inf
             }
         }
-        // row max in eight independent chains
+        // row max in eight independent chains of three-input maxima
+        auto sval = [&](int e) { return __uint_as_float(sv[e >> 5][e & 31]); };
         float mx8[8];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(sv[0][a]);
+        for (int a = 0; a < 8; ++a) mx8[a] = sval(a);
 #pragma unroll
-        for (int e = 8; e < kTileN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e >> 5][e & 31]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * cs;
+        for (int e = 8; e + 16 <= kTileN; e += 16)
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx8[a] = max3(mx8[a], sval(e + a), sval(e + 8 + a));
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(mx8[a], sval(kTileN - 8 + a));
+        const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * cs;
         const float m_old = mrun;
         const float m_new = (mx > m_old + kLazyRescale) ? mx : m_old;
         const bool rescale = (m_new != m_old) && j > 0;
@@ -409,15 +417,19 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
             tc::tmem_st32(o_cols + 32 * h, ov);
           }
           tc::tmem_st_wait();
-          if (rescale) lrun *= alpha;
+          if (rescale) {
+            lrun *= alpha;
+            lrun_r *= alpha;
+          }
         }
         // P = 2^(s*c - m) as 16-bit pairs over the first 64 columns of the S
         // buffer, published in two halves of 64 KV tokens each
         const float msub = (m_new == -INFINITY) ? 0.f : m_new;
         const float2 cc = make_float2(cs, cs), nms = make_float2(-msub, -msub);
-        float2 sum4[4];
+        float2 sum4[4], sumr[2];
 #pragma unroll
         for (int a = 0; a < 4; ++a) sum4[a] = make_float2(0.f, 0.f);
+        sumr[0] = sumr[1] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -430,6 +442,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
               const float2 pe = make_float2(ex2(x.x), ex2(x.y));
               sum4[e & 3] = add2(sum4[e & 3], pe);
               pk[e] = tc::pack2<T>(pe.x, pe.y);
+              tc::add_packed2<T>(sumr[e & 1], pk[e]);
             }
             tc::tmem_st16(s_cols + 16 * h, pk);
           }
@@ -440,6 +453,8 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         }
         const float2 s01 = add2(sum4[0], sum4[1]), s23 = add2(sum4[2], sum4[3]), s4 = add2(s01, s23);
         lrun += s4.x + s4.y;
+        const float2 sr = add2(sumr[0], sumr[1]);
+        lrun_r += sr.x + sr.y;
         mrun = m_new;
       }
       // Epilogue: O / l in the storage type (or the fp32 partial state of a
@@ -471,7 +486,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
       const int t = row / G;
       const int head = item.hk * G + (row - t * G);
       const int64_t tok = int64_t(rq.qo_start) + t;
-      const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
+      const float inv = lrun_r > 0.f ? 1.f / lrun_r : 0.f;
       const float lse_v = lrun > 0.f ? (mrun + __log2f(lrun)) * 0.69314718055994531f : -INFINITY;
       auto pack8 = [&](int h, int e0) {  // 8 normalised values as 16-bit pairs
         uint4 u;

@@ -219,5 +219,23 @@ __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
   return r;
 }
 
+// acc.x += low half of the packed pair, acc.y += high half, each 16-bit value
+// widened exactly (the mixed-precision fp32 add of sm_100+): the row sum of
+// the softmax is taken over the very P values the P V MMA multiplies.
+template <typename T>
+__device__ __forceinline__ void add_packed2(float2& acc, uint32_t pk);
+template <>
+__device__ __forceinline__ void add_packed2<__nv_bfloat16>(float2& acc, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y) : "r"(pk));
+}
+template <>
+__device__ __forceinline__ void add_packed2<__half>(float2& acc, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y) : "r"(pk));
+}
+
 }  // namespace tc
 }  // namespace fi

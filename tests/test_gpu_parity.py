@@ -73,16 +73,18 @@ def test_tensor_core_tiles(qo, kv, causal, dtype):
     assert info.num_prefill_items > 0
 
 
-@pytest.mark.parametrize("scale,dtype", [(1.5, "bf16"), (2.0, "bf16"), (4.0, "fp16")])
+@pytest.mark.parametrize("scale,dtype", [(1.5, "bf16"), (2.0, "bf16"), (4.0, "bf16"), (4.0, "fp16"), (8.0, "fp16")])
 @pytest.mark.parametrize("prefill_min_chunk", [1024, 512])
 def test_peaked_softmax_tensor_cores(scale, dtype, prefill_min_chunk):
-    """Queries scaled up so a few keys dominate each row: O must stay within the
-    bar although P enters the P V MMA rounded to 16 bits (bf16 keeps 8
-    significant bits, fp16 11, hence the larger fp16 scale), whole (1024-token
-    chunks) and split in two (512).  Here single keys dominate, so outputs
-    reach |o| ~ 3, where half an ulp of the stored bf16 value is up to 2^-8
-    |o| (7.8e-3): the bar is 8e-3 for the computation plus that storage
-    rounding (2^-11 |o| for fp16), as for the MLA outputs."""
+    """Queries scaled up so a few keys dominate each row, whole (1024-token
+    chunks) and split in two (512, merged by the late merge).  P enters the
+    P V MMA rounded to 16 bits; O is divided by the sum of those rounded P,
+    so a key that dominates its row passes its value through unchanged, and
+    LSE comes from the sum of the fp32 P.  The bar is the flat 8e-3 wherever
+    the stored outputs stay below 4 in magnitude.  At bf16 x4 single keys
+    push |o| past 4, where half an ulp of the stored bf16 value is 2^-6 by
+    itself, more than the whole bar; there the bar adds that storage
+    rounding (2^-8 |o_ref|)."""
     b = workloads.make_batch("peak", dtype, [64, 33], [1000, 40], 8, 2, 16, 1, 777, DEV, pool_pages=70)
     b.q.mul_(scale)
     cfg = fi.default_plan_config(0, prefill_min_chunk=prefill_min_chunk)
@@ -92,11 +94,14 @@ def test_peaked_softmax_tensor_cores(scale, dtype, prefill_min_chunk):
     assert (info.num_late_merge_units > 0) == (prefill_min_chunk == 512)
     o_ref, l_ref = oracle.attention(oracle_problem(b))
     n = b.total_qo
-    compare(o[:n], lse[:n], o_ref, l_ref)  # the exact checks: finite, empty rows
-    rel = 2.0 ** -8 if dtype == "bf16" else 2.0 ** -11
-    excess = np.abs(o[:n].float().cpu().numpy() - o_ref) - (O_TOL + rel * np.abs(o_ref))
-    err_l = float(np.abs(lse[:n].cpu().numpy() - l_ref).max())
-    assert excess.max() <= 0 and err_l <= LSE_TOL, (float(excess.max()), err_l)
+    err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
+    assert err_l <= LSE_TOL, err_l
+    if dtype == "bf16" and scale > 2.0:
+        assert np.abs(o_ref).max() > 4.0  # the storage rounding alone can exceed the flat bar
+        excess = np.abs(o[:n].float().cpu().numpy() - o_ref) - (O_TOL + 2.0 ** -8 * np.abs(o_ref))
+        assert excess.max() <= 0, float(excess.max())
+    else:
+        assert err_o <= O_TOL, err_o
 
 
 @pytest.mark.parametrize("seed,page,group,causal,dtype,qo_max,kv_max", [
