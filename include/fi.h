@@ -219,7 +219,12 @@ fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_indptr, cons
  *
  * Asynchronous on `stream`; never allocates, synchronizes or copies from the
  * host, so it can be captured in a CUDA graph.  The kernel reads the counts
- * of the current plan from the int workspace.  When info->num_late_merge_units
+ * of the current plan from the int workspace, and before any work checks that
+ * plan against this launch: its CTA count (the grid), its partial-state rows
+ * (info->max_partial_rows, the float workspace's capacity), its query tokens
+ * (q_num_tokens), its head counts and its page size.  A mismatch -- a
+ * workspace re-planned after `info` was taken, or `info` of another config --
+ * records FI_ERR_DEVICE_CHECK in the status word and nothing is written.  When info->num_late_merge_units
  * > 0 (split units of prefill-class tiles) a second kernel follows on the
  * same stream and merges those units row-parallel, reading its counts from
  * the workspace too; it merges nothing when the run has set the status word.
@@ -255,7 +260,11 @@ fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, 
  * float_workspace_dev; the caller still passes the inputs, the outputs and
  * the int workspace filled by fi_plan.  Returns FI_ERR_CAPACITY, before
  * anything is enqueued, when info->num_partial_rows exceeds 32768 (plan with
- * fewer CTAs, a larger split chunk or a smaller batch).
+ * fewer CTAs, a larger split chunk or a smaller batch).  The kernel repeats
+ * that check on the plan it finds in the int workspace: a workspace
+ * re-planned beyond 32768 partial rows after `info` was taken is refused on
+ * the device (FI_ERR_DEVICE_CHECK in the status word, nothing written, the
+ * array never written past its end).
  *
  * The first call on a device looks up the array's device address on that
  * device (the current one); make that first call before any stream capture.

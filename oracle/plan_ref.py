@@ -35,14 +35,16 @@ Rule:
     unit order) and its items get consecutive fp32 partial-state rows,
     n * rows in all.  A merge unit of a 256-row (prefill-class) unit carries
     the flag 1 in its seventh field ("late": merged after the run by a
-    launch of its own), a 16-row unit 0 (merged inside the run); the
-    header's last field counts the late units.
+    launch of its own), a 16-row unit 0 (merged inside the run); a header
+    field counts the late units.
  5. cost = (kv length of the item + 256) * class weight, the 256 standing for
     the fixed per-item latency of the kernel.  Items are sorted by
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
     load, ties to the smaller CTA index (longest processing time first).
  6. Output: header (with the variant: window, sink, soft-cap bits, and for
-    RoPE its position capacity, theta and scale bits and the table offset), per-CTA
+    RoPE its position capacity, theta and scale bits and the table offset;
+    then the count of late units, the partial rows used, the batch's query
+    tokens and two zero fields), per-CTA
     CSR offsets, items in CTA order (within a CTA the 256-row items first,
     then the 16-row items, each in the order dealt), merge units, zeroed merge
     counters, request table.
@@ -55,7 +57,7 @@ import numpy as np
 
 MAGIC = 0x46495031
 TILE_DECODE, TILE_PREFILL = 16, 256
-HEADER_INTS = 24
+HEADER_INTS = 28
 ROPE_PAIRS = 64
 ITEM_INTS = 8
 MERGE_INTS = 8
@@ -224,7 +226,7 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
                         off_cnt, off_req, 0, num_qo_heads, num_kv_heads, page_size, total_ints,
                         window, sink, bits(cap), rope_max,
                         bits(theta) if rope_max > 0 else 0, bits(rscale) if rope_max > 0 else 0, rope_off,
-                        sum(1 for m in merges if m[6])]
+                        sum(1 for m in merges if m[6]), part_rows, qo[batch] if batch > 0 else 0, 0, 0]
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos

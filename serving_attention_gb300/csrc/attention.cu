@@ -348,6 +348,8 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   p.iws = static_cast<int32_t*>(int_workspace_dev);
   p.fws = static_cast<float*>(float_workspace_dev);
   p.partial_o_offset = fi_partial_o_offset(info->max_partial_rows);
+  p.max_partial_rows = p.fws ? info->max_partial_rows : 0;
+  p.q_num_tokens = q_num_tokens;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.num_qo_heads = info->num_qo_heads;
   p.num_kv_heads = info->num_kv_heads;

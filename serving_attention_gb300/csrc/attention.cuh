@@ -72,6 +72,8 @@ struct RunParams {
   int32_t* iws;
   float* fws;
   int64_t partial_o_offset;  // floats
+  int64_t max_partial_rows;  // partial-state rows the float workspace holds
+  int32_t q_num_tokens;      // rows of Q and O
   float scale_log2;          // sm_scale * log2(e)
   int32_t num_qo_heads, num_kv_heads, group, page_size, log2_page, num_pages;
   int32_t tc_prefill;        // prefill-class items on the tensor cores (else CUDA cores)

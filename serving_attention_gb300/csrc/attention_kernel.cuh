@@ -635,7 +635,17 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   const int32_t n_items = ws_header(iws, FI_H_NUM_ITEMS);
   const int32_t n_ctas = ws_header(iws, FI_H_NUM_CTAS);
   const int32_t off_cta = ws_header(iws, FI_H_OFF_CTA);
-  bool bad = magic != FI_PLAN_MAGIC || n_ctas != int32_t(gridDim.x) || (smem_u32(smem_raw) & 1023u) != 0;
+  // The plan in the workspace must also fit the buffers of this launch: its
+  // partial rows the float workspace, its query tokens Q and O, its head
+  // counts and page size the tensor maps.  A workspace re-planned after the
+  // arguments were checked on the host is refused here, before any write.
+  // (The header fields share one cache line; their loads go out together.)
+  const int32_t h_rows = ws_header(iws, FI_H_PARTIAL_ROWS), h_qo = ws_header(iws, FI_H_TOTAL_QO);
+  const int32_t h_hq = ws_header(iws, FI_H_NUM_QO_HEADS), h_hkv = ws_header(iws, FI_H_NUM_KV_HEADS);
+  const int32_t h_page = ws_header(iws, FI_H_PAGE_SIZE);
+  bool bad = magic != FI_PLAN_MAGIC || n_ctas != int32_t(gridDim.x) || (smem_u32(smem_raw) & 1023u) != 0 ||
+             h_rows < 0 || h_rows > p.max_partial_rows || h_qo < 0 || h_qo > p.q_num_tokens ||
+             h_hq != p.num_qo_heads || h_hkv != p.num_kv_heads || h_page != p.page_size;
   int32_t begin = 0, end = 0;
   if (!bad) {
     begin = __ldg(iws + off_cta + blockIdx.x);

@@ -125,6 +125,8 @@ struct Params {
   const int32_t* kv_indices;
   float* fws;
   int64_t partial_o_offset;
+  int64_t max_parts;   // partial-state slots the float workspace holds
+  int32_t q_rows;      // rows of the queries and outputs
   uint16_t* o;         // [rows][heads][512] bf16
   float* lse;          // [rows][heads] or null
   float scale_log2;
@@ -645,6 +647,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     end = __ldg(iws + off_pair + pair + 1);
     bad = begin < 0 || end < begin || end > n_units;
   }
+  // The plan in the workspace must fit the buffers of this launch (a
+  // workspace re-planned after the host checked the arguments is refused
+  // here, before any write).
+  if (!bad)
+    bad = __ldg(iws + FI_MLA_H_NUM_PARTS) < 0 || __ldg(iws + FI_MLA_H_NUM_PARTS) > p.max_parts ||
+          __ldg(iws + FI_MLA_H_BATCH) > p.q_rows || __ldg(iws + FI_MLA_H_NUM_HEADS) != p.num_heads ||
+          __ldg(iws + FI_MLA_H_PAGE_SIZE) != p.page_size;
   if (bad) {
     if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPlan);
     return;
@@ -710,10 +719,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Merge of the chunks of split requests (the LSE-weighted combination of
 // partial states), and (0, -inf) for requests with no cached token.  One warp
 // per (merge entry, head) task, grid-stride; lane l holds dims 16l..16l+15,
-// so each part's row is one coalesced 2 KB read per warp.
+// so each part's row is one coalesced 2 KB read per warp.  Nothing is merged
+// when the decode kernel has set the status word (its partial states may be
+// incomplete, or the plan may not fit this launch's buffers).
 __global__ void __launch_bounds__(kMergeThreads) mla_merge_kernel(const int32_t* iws, const float* fws,
                                                                   int64_t partial_o_offset, uint16_t* o, float* lse,
                                                                   int32_t num_heads) {
+  if (*reinterpret_cast<const volatile int32_t*>(iws + FI_MLA_H_STATUS) != 0) return;
   const int32_t n_merge = __ldg(iws + FI_MLA_H_NUM_MERGE);
   const int32_t off_merge = __ldg(iws + FI_MLA_H_OFF_MERGE);
   const int64_t tasks = int64_t(n_merge) * num_heads;
@@ -868,6 +880,8 @@ extern "C" fi_status fi_mla_decode_run(const fi_mla_plan_info* info, const void*
   p.kv_indices = kv_indices_dev;
   p.fws = static_cast<float*>(float_workspace_dev);
   p.partial_o_offset = fi_mla_partial_o_offset(info->max_parts > 0 ? info->max_parts : 1);
+  p.max_parts = p.fws ? info->max_parts : 0;
+  p.q_rows = q_rows;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.scale_log2 = sm_scale * 1.4426950408889634f;

@@ -308,7 +308,8 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
                                           int32_t(off_merge), int32_t(off_cnt),   int32_t(off_req), 0,
                                           num_qo_heads,       num_kv_heads,       page_size,        int32_t(total_ints),
                                           window,             sink,               cap_bits,         rope_max,
-                                          theta_bits,         scale_bits,         rope_off,         n_late};
+                                          theta_bits,         scale_bits,         rope_off,         n_late,
+                                          int32_t(partial_rows), batch > 0 ? qo[batch] : 0, 0, 0};
   std::memcpy(ws, header, sizeof header);
 
   fi_plan_info info;

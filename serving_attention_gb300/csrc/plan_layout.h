@@ -1,8 +1,10 @@
 // plan_layout.h -- layout of the int workspace written by the planner and
 // read by the persistent kernel.  All fields are int32.
 //
-//   header[24]   FI_H_* below (the variant of the plan's config included:
-//                  window_left, sink_tokens, soft-cap as float bits, RoPE)
+//   header[28]   FI_H_* below (the variant of the plan's config included:
+//                  window_left, sink_tokens, soft-cap as float bits, RoPE;
+//                  the partial rows and query tokens the plan uses, which the
+//                  kernel compares with the buffers it was launched with)
 //   cta_indptr   num_ctas + 1 entries: CTA c runs items [cta_indptr[c], cta_indptr[c+1])
 //   items        FI_ITEM_INTS each: {b, hk, row0, row1, kv0, kv1, part, merge}
 //                  rows are packed rows of request b (row = token * G + g),
@@ -32,7 +34,7 @@
 #include <stdint.h>
 
 #define FI_PLAN_MAGIC 0x46495031
-#define FI_HEADER_INTS 24
+#define FI_HEADER_INTS 28
 #define FI_ITEM_INTS 8
 #define FI_MERGE_INTS 8
 #define FI_REQ_INTS 4
@@ -68,7 +70,9 @@ enum {
   FI_H_ROPE_THETA_BITS = 20,
   FI_H_ROPE_SCALE_BITS = 21,
   FI_H_ROPE_TABLE_OFF = 22,   // ints from the workspace start to the cos/sin table
-  FI_H_NUM_LATE_MERGE = 23    // merge units flagged late
+  FI_H_NUM_LATE_MERGE = 23,   // merge units flagged late
+  FI_H_PARTIAL_ROWS = 24,     // fp32 partial-state rows the items write (0: no split unit)
+  FI_H_TOTAL_QO = 25          // query tokens of the batch (qo_indptr[batch]); 26, 27 stay 0
 };
 
 #define FI_ROPE_PAIRS 64  // dims i and i + 64 of head_dim 128 form a rotated pair
