@@ -388,12 +388,42 @@ def bench_secondary(dev, reps=5):
                          decode_gbs=nbytes / ms / 1e6, items=info.num_items)
         del b, o, lse, g
         torch.cuda.empty_cache()
+    out["tiny_decode"] = bench_tiny(dev, flush, reps)
     out["continuous_batch"] = bench_mix(dev, flush, reps)
     out["shared_prefix"] = bench_shared_prefix(dev, flush, reps)
     out["kv_strides"] = bench_kv_strides(dev, flush, reps)
     out["variants"] = bench_variants(dev, flush, reps)
     out["mla"] = bench_mla(dev, flush, reps)
     return out
+
+
+def bench_tiny(dev, flush, reps=5):
+    """The tiny fp16 decode batch (4 requests, kv U{1..512}, 8 q / 2 kv heads):
+    about 1 MB of KV, so the launch and one item's load chain set its time;
+    graph replay, L2 flushed between replays."""
+    import torch
+
+    import serving_attention_gb300 as fi
+    import workloads
+
+    b = workloads.tiny_decode(device=dev)
+    ws = fi.Workspace(fi.default_plan_config(dev.index), device=dev)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads, 128,
+                   b.page_size, b.causal, b.num_pages)
+    kvi = torch.as_tensor(b.kv_indices, device=dev)
+    o = torch.empty_like(b.q)
+    lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
+    fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+    ts = _replay_times(g, flush, 20 * reps)
+    assert fi.device_status(ws) == 0
+    ms = float(np.median(ts))
+    nbytes, _, _ = algorithmic(b)
+    return {"workload": "tiny_decode: 4 requests, kv U{1..512}, 8 q / 2 kv heads, page 16, fp16", "ms": ms,
+            "ms_p10_p90": _p10_p90(ts), "gbs": nbytes / ms / 1e6, "algorithmic_bytes": nbytes, "items": info.num_items,
+            "graded": False}
 
 
 def _replay_times(g, flush, reps):
@@ -877,37 +907,171 @@ def _profile_mla(name, b, dev, launches: int) -> int:
 # ----------------------------------------------------------------- reference arm
 
 
-def reference_sample(budget_s: float):
-    """Time the fp64 oracle on whole requests of the decode workload (all heads)
-    until about budget_s of CPU work; returns (GB/s of algorithmic bytes, sample text, cores)."""
-    import torch
-
+def _oracle_problem(b):
     import oracle
     import workloads
 
-    b = workloads.llama8b_decode(device="cpu")
     q, k, v = workloads.host_views(b)
-    prob = oracle.Problem(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 32, 8, 16, 0, b.sm_scale,
-                          oracle.BF16, q, k, v)
+    dt = oracle.BF16 if b.dtype == "bf16" else oracle.FP16
+    return oracle.Problem(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.num_qo_heads, b.num_kv_heads,
+                          b.page_size, b.causal, b.sm_scale, dt, q, k, v)
+
+
+def _time_rows(prob, rows_list, budget_s, work_of):
+    """Run the oracle on whole query rows (all heads each), one group of rows
+    per call, cycling through rows_list until about budget_s of CPU time;
+    returns (work done, seconds, calls)."""
+    import oracle
+
+    heads = np.arange(prob.num_qo_heads, dtype=np.int32)
+    done, t_used, calls, i = 0.0, 0.0, 0, 0
+    while t_used < budget_s:
+        rows = rows_list[i % len(rows_list)]
+        rr = np.repeat(np.asarray(rows, np.int32), heads.size)
+        hh = np.tile(heads, len(rows))
+        t0 = time.perf_counter()
+        oracle.attention_select(prob, rr, hh)
+        t_used += time.perf_counter() - t0
+        done += work_of(rows)
+        calls += 1
+        i += 1
+    return done, t_used, calls
+
+
+def reference_sample(budget_s: float):
+    """Time the fp64 oracle on whole requests of the decode workload (all heads)
+    until about budget_s of CPU work; returns (GB/s of algorithmic bytes, sample text, cores, seconds)."""
+    import workloads
+
+    b = workloads.llama8b_decode(device="cpu")
+    prob = _oracle_problem(b)
     kv = b.kv_lens()
     order = np.argsort(kv)  # short requests first so a small budget still spans several
-    done_bytes, t_used, n_req, passes = 0.0, 0.0, 0, 0
-    while t_used < budget_s:
-        for r in order:
-            rows = np.full(32, int(b.qo_indptr[r]), np.int32)
-            heads = np.arange(32, dtype=np.int32)
-            t0 = time.perf_counter()
-            oracle.attention_select(prob, rows, heads)
-            t_used += time.perf_counter() - t0
-            done_bytes += kv[r] * 8 * 128 * 2 * 2 + 32 * (128 * 2 * 2 + 4)
-            n_req += 1
-            if t_used >= budget_s:
-                break
-        passes += 1
-    cores = os.cpu_count()
-    sample = f"{n_req} request decodes (all 32 heads each) over {passes} pass(es) of the 64-request batch, " \
-             f"{done_bytes / 1e9:.2f} GB of KV"
-    return done_bytes / t_used / 1e9, sample, cores, t_used
+    rows_list = [[int(b.qo_indptr[r])] for r in order]
+    row_req = {int(b.qo_indptr[r]): int(r) for r in range(b.batch)}
+    nbytes = lambda rows: sum(kv[row_req[x]] * 8 * 128 * 2 * 2 + 32 * (128 * 2 * 2 + 4) for x in rows)  # noqa: E731
+    done, t_used, calls = _time_rows(prob, rows_list, budget_s, nbytes)
+    sample = f"{calls} request decodes (all 32 heads each) of the 64-request batch, {done / 1e9:.2f} GB of KV"
+    return done / t_used / 1e9, sample, _omp_threads(), t_used
+
+
+def reference_sample_prefill(budget_s: float):
+    """The oracle on query rows (all 32 heads) spread over the ragged prefill
+    batch; returns (TFLOP/s over visible pairs, sample text, seconds)."""
+    import workloads
+
+    b = workloads.ragged_prefill(device="cpu")
+    prob = _oracle_problem(b)
+    qo, kv = b.qo_lens(), b.kv_lens()
+    rng = np.random.default_rng(31)
+    rows_list, vis = [], {}
+    for r in range(b.batch):
+        for t in rng.choice(int(qo[r]), size=4, replace=False):
+            row = int(b.qo_indptr[r]) + int(t)
+            vis[row] = int(kv[r]) - int(qo[r]) + int(t) + 1  # bottom-right causal: keys the row sees
+            rows_list.append([row])
+    rng.shuffle(rows_list)
+    flops = lambda rows: sum(4.0 * 128 * 32 * vis[x] for x in rows)  # noqa: E731
+    done, t_used, calls = _time_rows(prob, rows_list, budget_s, flops)
+    sample = f"{calls} query rows (all 32 heads each) drawn over the 16 prefill requests, {done / 1e12:.3f} TFLOP"
+    return done / t_used / 1e12, sample, t_used
+
+
+def reference_sample_mix(budget_s: float):
+    """The oracle on the continuous-batching mix (draw 0): its 8 prefill
+    chunks and 16 of its 120 decode requests (a seeded choice) are built as
+    one batch of the same lengths; rows of both parts are timed, and the
+    step time is extrapolated from each part's rate (visible-pair FLOPs for
+    the prefill chunks, KV bytes for the decode requests).  Returns
+    (estimated ms per mix step, detail dict, seconds)."""
+    import workloads
+
+    rng = np.random.default_rng(1000 * 5)
+    qo, kv = workloads.continuous_batch_lengths(rng)
+    pick = np.sort(np.random.default_rng(32).choice(np.arange(8, 128), size=16, replace=False))
+    idx = np.concatenate([np.arange(8), pick])
+    b = workloads.make_batch("continuous_batch.sample", "bf16", qo[idx], kv[idx], 32, 8, 16, 1, 5032, "cpu")
+    prob = _oracle_problem(b)
+    rows_p, vis = [], {}
+    for r in range(8):
+        for t in np.random.default_rng(33 + r).choice(512, size=4, replace=False):
+            row = int(b.qo_indptr[r]) + int(t)
+            vis[row] = int(kv[idx[r]]) - 512 + int(t) + 1
+            rows_p.append([row])
+    rows_d = [[int(b.qo_indptr[r])] for r in range(8, 24)]
+    dkv = {int(b.qo_indptr[r]): int(kv[idx[r]]) for r in range(8, 24)}
+    fp, tp, cp = _time_rows(prob, rows_p, budget_s / 2, lambda rows: sum(4.0 * 128 * 32 * vis[x] for x in rows))
+    by, td, cd = _time_rows(prob, rows_d, budget_s / 2, lambda rows: sum(dkv[x] * 8 * 128 * 4.0 for x in rows))
+    full_flops = float(sum(4.0 * 128 * 32 * (kv[r] - 512 + t + 1) for r in range(8) for t in range(512)))
+    full_bytes = float((kv[8:] * 8 * 128 * 4.0).sum())
+    step_s = full_flops / (fp / tp) + full_bytes / (by / td)
+    detail = {"prefill_tflops": fp / tp / 1e12, "decode_gbs": by / td / 1e9,
+              "sample": f"{cp} prefill-chunk query rows and {cd} decode requests (all 32 heads each) of draw 0; "
+                        "step time = its prefill FLOPs and decode KV bytes at the sampled rates"}
+    return step_s * 1e3, detail, tp + td
+
+
+def _omp_threads() -> int:
+    v = os.environ.get("OMP_NUM_THREADS", "")
+    return int(v) if v.isdigit() and int(v) > 0 else (os.cpu_count() or 1)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine()
+
+
+def cpu_leg(name: str, budget_s: float) -> dict:
+    """One CPU-baseline leg, as a dict (also the body of --cpu-leg)."""
+    if name == "decode":
+        v, sample, cores, t = reference_sample(budget_s)
+        return {"value": v, "unit": "GB/s", "cores": cores, "sample": sample, "seconds": t}
+    if name == "prefill":
+        v, sample, t = reference_sample_prefill(budget_s)
+        return {"value": v, "unit": "TFLOP/s", "cores": _omp_threads(), "sample": sample, "seconds": t}
+    ms, detail, t = reference_sample_mix(budget_s)
+    return dict(detail, value=ms, unit="ms per step (estimated)", cores=_omp_threads(), seconds=t)
+
+
+def cpu_leg_one_core(name: str, budget_s: float):
+    """The same leg in a child process limited to one OpenMP thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    try:
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-leg", name, "--cpu-budget",
+                              str(budget_s)], capture_output=True, text=True, env=env, timeout=600)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: the all-core figure stands
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+
+
+def cpu_baselines(budget_s: float) -> dict:
+    """The oracle on the host cores: decode (the headline's workload), ragged
+    prefill and the continuous-batching mix on all cores, and decode and
+    prefill on one core, with the CPU model."""
+    dec = cpu_leg("decode", budget_s)
+    out = {"value": dec["value"], "unit": "GB/s", "cores": dec["cores"], "kind": "oracle",
+           "sample": dec["sample"] + f", {dec['seconds']:.1f} s", "cpu_model": cpu_model()}
+    out["one_core"] = {"decode": cpu_leg_one_core("decode", budget_s / 3),
+                       "prefill": cpu_leg_one_core("prefill", budget_s / 3)}
+    out["prefill"] = cpu_leg("prefill", budget_s / 2)
+    out["mix"] = cpu_leg("mix", budget_s / 2)
+    return out
 
 
 # ----------------------------------------------------------------- driver
@@ -962,9 +1126,13 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES), help="only launch the kernel on this workload")
     ap.add_argument("--launches", type=int, default=2)
+    ap.add_argument("--cpu-leg", choices=["decode", "prefill", "mix"], help=argparse.SUPPRESS)
     a = ap.parse_args()
     if a.profile:
         sys.exit(profile_case(a.profile, a.launches))
+    if a.cpu_leg:  # one CPU-baseline leg in this process (the one-core child of cpu_baselines)
+        print(json.dumps(cpu_leg(a.cpu_leg, a.cpu_budget)))
+        return
     dist, rank, world, local = _dist()
     _DIST = dist
     hbm, tf, tf_sus, peak_src = _peaks()
@@ -1008,8 +1176,7 @@ def main():
     sec = None if (a.no_secondary or rank != 0) else bench_secondary(dev)
     cpu = None
     if rank == 0 and world == 1:
-        gbs, sample, cores, t = reference_sample(a.cpu_budget)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample + f", {t:.1f} s"}
+        cpu = cpu_baselines(a.cpu_budget)
     if rank != 0:
         return
     info = r["info"]
@@ -1018,7 +1185,8 @@ def main():
         "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": 64 * world, "per_gpu_batch": 64,
-                   "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (2.0 GB of KV per step)",
+                   "parallelism": f"replicas{world}",
+                   "l2": f"inputs larger than L2 ({r['bytes'] / 1e9:.2f} GB of KV per step)",
                    "step": "fi_plan (host, work list copied to device) + one persistent kernel launch",
                    "num_ctas": info.num_ctas, "items": info.num_items, "split_units": info.num_merge_units},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
@@ -1046,6 +1214,8 @@ def main():
                                        "frac_of_hbm": m["decode_part_gbs"] / hbm,
                                        "gbs_per_replan": m["decode_part_gbs_per_replan"]},
                        "plan_host_us": m["plan_host_us"]}
+        t1 = sec["tiny_decode"]
+        line["tiny_decode"] = dict(t1, frac_of_hbm=t1["gbs"] / hbm)
         sp = sec["shared_prefix"]
         line["shared_prefix"] = dict(sp, frac_of_hbm=sp["composable_gbs"] / hbm)
         line["kv_strides"] = sec["kv_strides"]
