@@ -765,34 +765,41 @@ def bench_kv_strides(dev, flush, reps=5):
 
 
 def bench_shared_prefix(dev, flush, reps=5):
-    """Composable format: the dense prefix run (tensor cores, 64 branch queries,
-    its split units merged by the late-merge launch that follows it), the page-1
-    suffix run and fi_merge_states, captured in one CUDA graph,
-    against one run over the flat page-1 layout (prefix pages repeated in every
-    branch's page list)."""
+    """Composable format as one cascade plan: the dense prefix is the shared
+    block of all 64 branch queries (tensor cores), the page-1 suffixes their
+    own keys, in one persistent launch followed by the cascade merge; against
+    the same step as separate calls (prefix run with its late merge, suffix
+    run, fi_merge_states) and one run over the flat page-1 layout (prefix
+    pages repeated in every branch's page list).  Each captured in a CUDA
+    graph, L2 flushed between replays."""
     import torch
 
-    composable, flat_run, nbytes, late = _shared_prefix_runs(dev)
+    cascade, separate, flat_run, nbytes, late = _shared_prefix_runs(dev)
     res, spread = {}, {}
-    for name, fn in (("composable", composable), ("flat", flat_run)):
+    for name, fn in (("cascade", cascade), ("separate", separate), ("flat", flat_run)):
         fn()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()
-        ts = _replay_times(g, flush, 20 * reps if name == "composable" else reps)
+        ts = _replay_times(g, flush, reps if name == "flat" else 20 * reps)
         res[name] = float(np.median(ts))
         spread[name] = _p10_p90(ts)
+    assert cascade.check() == 0
     return {"workload": "shared_prefix: 8192-token dense prefix + 64 branches, suffix U[64,512] at page 1",
-            "composable_ms": res["composable"], "composable_ms_p10_p90": spread["composable"], "flat_ms": res["flat"],
-            "composable_gbs": nbytes / res["composable"] / 1e6, "speedup_vs_flat": res["flat"] / res["composable"],
-            "launches": 3 + late}
+            "composable_ms": res["cascade"], "composable_ms_p10_p90": spread["cascade"],
+            "composable_gbs": nbytes / res["cascade"] / 1e6, "launches": 2,
+            "form": "one cascade plan: one persistent launch + the cascade merge",
+            "separate_ms": res["separate"], "separate_launches": 3 + late, "flat_ms": res["flat"],
+            "speedup_vs_flat": res["flat"] / res["cascade"], "speedup_vs_separate": res["separate"] / res["cascade"],
+            "algorithmic_bytes": nbytes}
 
 
 def _shared_prefix_runs(dev):
-    """The shared-prefix workload planned three ways: returns the composable
-    step (prefix run, suffix run, state merge), the flat run, the algorithmic
-    bytes of the composable form and how many late-merge launches it adds."""
+    """The shared-prefix workload planned three ways: returns the cascade step
+    (one plan: prefix block + suffixes), the separate step (prefix run, suffix
+    run, state merge), the flat run, the algorithmic bytes of the composable
+    form and how many late-merge launches the separate step adds."""
     import torch
 
     import serving_attention_gb300 as fi
@@ -814,6 +821,15 @@ def _shared_prefix_runs(dev):
     P, S, F = prepared(pre), prepared(suf), prepared(flat)
     o_m = torch.empty_like(pre.q)
     l_m = torch.empty(pre.q.shape[:2], dtype=torch.float32, device=dev)
+    wsc = fi.Workspace(cfg, device=dev)
+    info_c = fi.plan_cascade(wsc, pre.qo_indptr, pre.kv_indptr, pre.kv_indices, pre.last_page_len, pre.page_size,
+                             suf.qo_indptr, suf.kv_indptr, suf.kv_indices, suf.last_page_len, 32, 8, 128, 1, 0,
+                             suf.num_pages, pre.num_pages)
+    o_c = torch.empty_like(suf.q)
+    l_c = torch.empty(suf.q.shape[:2], dtype=torch.float32, device=dev)
+
+    def cascade():
+        fi.run_cascade(wsc, info_c, suf.q, suf.k, suf.v, S[2], pre.k, pre.v, P[2], o_c, l_c, suf.sm_scale)
 
     def composable():
         fi.run(P[0], P[1], pre.q, pre.k, pre.v, P[2], P[3], P[4], pre.sm_scale)
@@ -829,10 +845,10 @@ def _shared_prefix_runs(dev):
     late = (1 if P[1].num_late_merge_units else 0) + (1 if S[1].num_late_merge_units else 0)
 
     def check():
-        return max(fi.device_status(x[0]) for x in (P, S, F))
+        return max(fi.device_status(x) for x in (P[0], S[0], F[0], wsc))
 
-    composable.check = check
-    return composable, flat_run, nbytes, late
+    cascade.check = composable.check = check
+    return cascade, composable, flat_run, nbytes, late
 
 
 PROFILE_CASES = {
@@ -843,7 +859,8 @@ PROFILE_CASES = {
     "continuous_batch": lambda dev: __import__("workloads").continuous_batch(device=dev),
     "mla_decode": lambda dev: __import__("workloads").mla_decode(device=dev),
     "mla_decode_16": lambda dev: __import__("workloads").mla_decode(device=dev, batch=16),
-    "shared_prefix": None,  # the composable step: prefix run (+ late merge), suffix run, state merge
+    "shared_prefix": None,  # the cascade step: one persistent launch + the cascade merge
+    "shared_prefix_separate": None,  # prefix run (+ late merge), suffix run, state merge
 }
 
 
@@ -855,13 +872,15 @@ def profile_case(name: str, launches: int) -> int:
     import serving_attention_gb300 as fi
 
     dev = _device_setup(0)
-    if name == "shared_prefix":
-        composable, _, nbytes, late = _shared_prefix_runs(dev)
+    if name in ("shared_prefix", "shared_prefix_separate"):
+        cascade, separate, _, nbytes, late = _shared_prefix_runs(dev)
+        fn = cascade if name == "shared_prefix" else separate
         for _ in range(launches):
-            composable()
+            fn()
         torch.cuda.synchronize()
-        st = composable.check()
-        print(json.dumps({"profile": name, "launches": launches, "kernels_per_launch": 3 + late, "status": st,
+        st = fn.check()
+        print(json.dumps({"profile": name, "launches": launches,
+                          "kernels_per_launch": 2 if name == "shared_prefix" else 3 + late, "status": st,
                           "algorithmic_bytes": nbytes}))
         return 0 if st == 0 else 3
     b = PROFILE_CASES[name](dev)

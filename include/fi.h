@@ -112,7 +112,9 @@ typedef struct {
     int64_t int_ws_bytes_used;   /* bytes of the int workspace written (and copied) by the plan */
     int64_t max_partial_rows;    /* capacity of the float workspace, from the config */
     int32_t num_late_merge_units; /* split units of prefill-class tiles: merged by a second launch */
-    int32_t reserved;
+    int32_t num_shared;          /* cascade plan: shared blocks (0 for a one-level plan) */
+    int32_t num_cascade_merges;  /* cascade plan: entries of the cascade merge (a second launch) */
+    int32_t prefill_caches;      /* caches read by prefill-class units: bit 0 the ordinary one, bit 1 the shared one */
 } fi_plan_info;
 
 /* Defaults, with num_ctas derived from the device's SM count and the run
@@ -196,6 +198,67 @@ fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_indptr, cons
                        fi_plan_info* info_out);
 
 /*
+ * fi_plan_cascade -- plan one launch over a two-level KV layout: every query
+ * row attends to the keys of its shared block (level 0, read from a shared
+ * cache; e.g. a prompt prefix common to several requests, stored once as a
+ * dense block) and to its own request's pages (level 1), and the two partial
+ * results are merged by their log-sum-exp (paper summary, "1. 통합된 KV 캐시
+ * 추상화": composable formats -- a shared prefix as one dense block, the
+ * request-specific suffixes as a sparse format, computed apart and merged;
+ * and "주요 성능 테스트 결과 / 1. 엔드투엔드 성능", parallel generation).  One
+ * run then computes both levels in a single persistent launch (the shared
+ * blocks' units on the tensor cores when they have more than 16 packed rows)
+ * and a second, small launch merges them.
+ *
+ * Level 1 is an ordinary batch (qo_indptr, kv_indptr, kv_indices,
+ * last_page_len: HOST arrays as for fi_plan, pages of page_size in the
+ * requests' own cache), covering query rows [0, qo_indptr[batch]).  Level 0:
+ * num_shared >= 1 blocks (HOST arrays, num_shared + 1 / num_shared + 1 /
+ * shared_kv_indptr[num_shared] / num_shared entries); block s owns query rows
+ * [shared_qo_indptr[s], shared_qo_indptr[s+1]) -- the blocks start at 0, cover
+ * every row, and no request straddles two -- and the pages
+ * shared_kv_indices[shared_kv_indptr[s] .. shared_kv_indptr[s+1]) of the
+ * shared cache (pages of shared_page_size, its last page holding
+ * shared_last_page_len[s] slots).  A block with no page adds nothing.
+ *
+ * Visibility: every key of a row's block is visible to the row (the block
+ * precedes all of its queries); the row's own keys follow `causal`, aligned
+ * to the bottom right of the request's own keys, and a causal request must
+ * hold at least as many keys as queries (its queries are among its keys).
+ * That is attention over the concatenation block ++ own pages with the
+ * bottom-right causal mask.  The logits soft-cap applies; a sliding window,
+ * sink tokens or RoPE in `cfg` are FI_ERR_UNSUPPORTED here (their positions
+ * would have to span two caches).
+ *
+ * The plan numbers the blocks first in its request table; every unit writes
+ * fp32 partial states (float workspace) and fi_plan_info.num_cascade_merges
+ * > 0 tells the run to follow with the cascade merge.  Other rules, errors,
+ * staging and copy as for fi_plan; FI_ERR_CAPACITY also when the merge
+ * entries (runs of up to 16 packed rows of one unit) exceed
+ * cfg->max_merge_units or the requests and blocks together exceed
+ * cfg->max_batch.
+ */
+fi_status fi_plan_cascade(const fi_plan_config* cfg, const int32_t* shared_qo_indptr,
+                          const int32_t* shared_kv_indptr, const int32_t* shared_kv_indices,
+                          const int32_t* shared_last_page_len, int32_t num_shared, int32_t shared_page_size,
+                          int32_t shared_num_pages, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                          const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch,
+                          int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                          int32_t causal, int32_t num_pages, void* int_workspace_dev, void* pinned_staging_host,
+                          size_t staging_bytes, void* stream, fi_plan_info* info_out);
+
+/* fi_plan_cascade_host -- the same rule, writing the workspace image into a
+ * HOST buffer only (no CUDA call). */
+fi_status fi_plan_cascade_host(const fi_plan_config* cfg, const int32_t* shared_qo_indptr,
+                               const int32_t* shared_kv_indptr, const int32_t* shared_kv_indices,
+                               const int32_t* shared_last_page_len, int32_t num_shared, int32_t shared_page_size,
+                               int32_t shared_num_pages, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                               const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch,
+                               int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                               int32_t causal, int32_t num_pages, void* workspace_host, size_t workspace_bytes,
+                               fi_plan_info* info_out);
+
+/*
  * fi_batch_paged_attention_run -- one persistent kernel over the planned
  * work list: O = softmax(scale * Q K^T + mask) V per query row and head, and
  * LSE = log sum exp(scale * q.k) (natural log) over the visible keys.
@@ -241,6 +304,33 @@ fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, 
                                        const int32_t* kv_indices_dev, void* o, int64_t o_stride_tok,
                                        int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale,
                                        void* int_workspace_dev, void* float_workspace_dev, void* stream);
+
+/*
+ * fi_batch_paged_attention_run_cascade -- the run of a plan made by
+ * fi_plan_cascade: the arguments of fi_batch_paged_attention_run for the
+ * requests' own cache (k_cache, v_cache, their strides, num_pages,
+ * kv_indices_dev), plus the shared blocks' cache: shared_k_cache and
+ * shared_v_cache [shared_num_pages, shared_page_size, num_kv_heads, d] with
+ * their own strides (elements, multiples of 16 bytes) and the device copy of
+ * shared_kv_indices.  The two caches may be views of one allocation (a dense
+ * prefix viewed as pages of 16 inside a pool of pages of 1, say).  One
+ * persistent launch computes every unit of both levels into the float
+ * workspace, then a second launch merges each row's shared and own states in
+ * that order and writes O (storage type) and LSE (natural log).  A row whose
+ * block and own pages are both empty gets O = 0, LSE = -inf.  Asynchronous,
+ * capture-safe and checked on the device as fi_batch_paged_attention_run
+ * (the plan's shared page size must equal shared_page_size).
+ * fi_batch_paged_attention_run given a cascade plan returns
+ * FI_ERR_INVALID_ARG (it has no shared cache).
+ */
+fi_status fi_batch_paged_attention_run_cascade(
+    const fi_plan_info* info, const void* q, int64_t q_stride_tok, int64_t q_stride_head, int32_t q_num_tokens,
+    const void* k_cache, const int64_t k_strides[3], const void* v_cache, const int64_t v_strides[3],
+    int32_t num_pages, const int32_t* kv_indices_dev, const void* shared_k_cache, const int64_t shared_k_strides[3],
+    const void* shared_v_cache, const int64_t shared_v_strides[3], int32_t shared_num_pages,
+    const int32_t* shared_kv_indices_dev, int32_t shared_page_size, void* o, int64_t o_stride_tok,
+    int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale, void* int_workspace_dev,
+    void* float_workspace_dev, void* stream);
 
 /*
  * fi_batch_paged_attention_run_static_scratch -- fi_batch_paged_attention_run

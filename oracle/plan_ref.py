@@ -57,11 +57,13 @@ import numpy as np
 
 MAGIC = 0x46495031
 TILE_DECODE, TILE_PREFILL = 16, 256
-HEADER_INTS = 28
+HEADER_INTS = 32
 ROPE_PAIRS = 64
 ITEM_INTS = 8
 MERGE_INTS = 8
 REQ_INTS = 4
+CASCADE_INTS = 12
+CASCADE_ROWS = 16
 ITEM_COST_TOKENS = 256
 
 # fi_status values
@@ -79,66 +81,160 @@ def _ceil_div(a: int, b: int) -> int:
 def int_workspace_ints(cfg: dict) -> int:
     return (HEADER_INTS + _align4(cfg["num_ctas"] + 1) + ITEM_INTS * cfg["max_items"]
             + MERGE_INTS * cfg["max_merge_units"] + _align4(cfg["max_merge_units"])
-            + REQ_INTS * cfg["max_batch"])
+            + REQ_INTS * cfg["max_batch"] + CASCADE_INTS * cfg["max_merge_units"])
 
 
-def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads: int,
-              num_kv_heads: int, head_dim: int, page_size: int, causal: int, num_pages: int):
-    """Returns (status, workspace int32 array or None, info dict or None)."""
+def _pow2_page(page_size: int) -> bool:
+    return 1 <= page_size <= 128 and page_size & (page_size - 1) == 0
+
+
+def _config_status(cfg, head_dim, num_qo_heads, num_kv_heads, page_size, causal):
+    """Status of the config and shapes (0 when they are acceptable)."""
+    if head_dim != 128 or not _pow2_page(page_size):
+        return UNSUPPORTED
+    if num_qo_heads < 1 or num_kv_heads < 1 or num_qo_heads % num_kv_heads:
+        return UNSUPPORTED
+    if num_qo_heads // num_kv_heads > 16:
+        return UNSUPPORTED
+    if causal not in (0, 1) or cfg["num_ctas"] < 1 or cfg["split_factor"] < 1:
+        return INVALID_ARG
+    window, sink = cfg.get("window_left", -1), cfg.get("sink_tokens", 0)
+    cap = float(np.float32(cfg.get("logits_soft_cap", 0.0)))
+    if window < -1 or sink < 0 or not (cap >= 0.0) or cap == float("inf"):
+        return INVALID_ARG
+    rope_max = cfg.get("rope_max_positions", 0)
+    theta = float(np.float32(cfg.get("rope_theta", 10000.0)))
+    rscale = float(np.float32(cfg.get("rope_scale", 1.0)))
+    if rope_max < 0 or (rope_max > 0 and not (0 < theta < float("inf") and 0 < rscale < float("inf"))):
+        return INVALID_ARG
+    return OK
+
+
+def _requests_of(qo_indptr, kv_indptr, kv_indices, last_page_len, page_size, num_pages, rope_max):
+    """One level's requests as [qo_start, qo_len, page_start, kv_len] lists
+    (status, list): the indptr arrays start at 0 and never decrease, a
+    request with pages fills its last page with 1..page_size slots, page ids
+    lie in [0, num_pages) when num_pages > 0, and with RoPE every position
+    lies in the table."""
     qo = [int(x) for x in qo_indptr]
     kvp = [int(x) for x in kv_indptr]
     lpl = [int(x) for x in last_page_len]
     batch = len(qo) - 1
     if batch < 0 or len(kvp) != batch + 1 or len(lpl) < batch:
+        return INVALID_ARG, None
+    if batch > 0 and (qo[0] != 0 or kvp[0] != 0):
+        return INVALID_ARG, None
+    reqs = []
+    for b in range(batch):
+        if qo[b + 1] < qo[b] or kvp[b + 1] < kvp[b]:
+            return INVALID_ARG, None
+        n_pg = kvp[b + 1] - kvp[b]
+        if n_pg > 0 and not (1 <= lpl[b] <= page_size):
+            return INVALID_ARG, None
+        lkv_b = 0 if n_pg == 0 else (n_pg - 1) * page_size + lpl[b]
+        lq_b = qo[b + 1] - qo[b]
+        if rope_max > 0 and (lkv_b > rope_max or lq_b > lkv_b):
+            return INVALID_ARG, None
+        reqs.append([qo[b], lq_b, kvp[b], lkv_b])
+    if num_pages > 0 and batch > 0:
+        idx = np.asarray(kv_indices[:kvp[batch]], dtype=np.int64)
+        if idx.size and (idx.min() < 0 or idx.max() >= num_pages):
+            return INVALID_ARG, None
+    return OK, reqs
+
+
+def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads: int,
+              num_kv_heads: int, head_dim: int, page_size: int, causal: int, num_pages: int):
+    """Returns (status, workspace int32 array or None, info dict or None)."""
+    st = _config_status(cfg, head_dim, num_qo_heads, num_kv_heads, page_size, causal)
+    if st:
+        return st, None, None
+    if len(qo_indptr) - 1 > cfg["max_batch"]:
+        return CAPACITY, None, None
+    st, reqs = _requests_of(qo_indptr, kv_indptr, kv_indices, last_page_len, page_size, num_pages,
+                            cfg.get("rope_max_positions", 0))
+    if st:
+        return st, None, None
+    total_qo = int(qo_indptr[-1]) if len(reqs) else 0
+    return _plan(cfg, reqs, 0, page_size, [], total_qo, num_qo_heads, num_kv_heads, head_dim, page_size, causal)
+
+
+def make_cascade_plan(cfg: dict, shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len,
+                      shared_page_size: int, shared_num_pages: int, qo_indptr, kv_indptr, kv_indices,
+                      last_page_len, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                      causal: int, num_pages: int):
+    """The two-level (cascade) plan: shared blocks, then the ordinary
+    requests, in one request table.  Block s covers query rows
+    [shared_qo_indptr[s], shared_qo_indptr[s+1]) -- the blocks cover every
+    row and no request straddles two -- and its keys (a shared cache, pages
+    of shared_page_size) are all visible to those rows; each ordinary
+    request's own keys follow the causal flag, and a causal request has at
+    least as many keys as queries.  Every unit writes partial states; the
+    cascade merge entries name, per run of output rows, the partial rows of
+    the block's chunks and of the request's chunks.  Windows, sinks and RoPE
+    are not offered with two levels."""
+    num_shared = len(shared_qo_indptr) - 1
+    if num_shared < 1:
         return INVALID_ARG, None, None
-    if head_dim != 128 or page_size < 1 or page_size > 128 or page_size & (page_size - 1):
+    st = _config_status(cfg, head_dim, num_qo_heads, num_kv_heads, page_size, causal)
+    if st:
+        return st, None, None
+    if not _pow2_page(shared_page_size):
         return UNSUPPORTED, None, None
-    if num_qo_heads < 1 or num_kv_heads < 1 or num_qo_heads % num_kv_heads:
+    if cfg.get("window_left", -1) >= 0 or cfg.get("rope_max_positions", 0) > 0:
         return UNSUPPORTED, None, None
+    batch = len(qo_indptr) - 1
+    if batch + num_shared > cfg["max_batch"]:
+        return CAPACITY, None, None
+    st, shared = _requests_of(shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len,
+                              shared_page_size, shared_num_pages, 0)
+    if st:
+        return st, None, None
+    st, own = _requests_of(qo_indptr, kv_indptr, kv_indices, last_page_len, page_size, num_pages, 0)
+    if st:
+        return st, None, None
+    total_qo = int(qo_indptr[-1]) if batch > 0 else 0
+    bounds = [int(x) for x in shared_qo_indptr]
+    if bounds[-1] != total_qo:
+        return INVALID_ARG, None, None
+    block_of = [-1] * num_shared
+    for q0, lq, _, lkv in own:
+        if causal and lkv < lq:
+            return INVALID_ARG, None, None
+        if lq == 0:
+            block_of.append(-1)
+            continue
+        # the block whose row range holds this request's first row
+        s = next((i for i in range(num_shared) if bounds[i] <= q0 < bounds[i + 1]), None)
+        if s is None or q0 + lq > bounds[s + 1]:
+            return INVALID_ARG, None, None
+        block_of.append(s)
+    return _plan(cfg, shared + own, num_shared, shared_page_size, block_of, total_qo, num_qo_heads,
+                 num_kv_heads, head_dim, page_size, causal)
+
+
+def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_heads, num_kv_heads, head_dim,
+          page_size, causal):
     group = num_qo_heads // num_kv_heads
-    if group > 16:
-        return UNSUPPORTED, None, None
-    if causal not in (0, 1) or cfg["num_ctas"] < 1 or cfg["split_factor"] < 1:
-        return INVALID_ARG, None, None
+    cascade = num_shared > 0
     window, sink = cfg.get("window_left", -1), cfg.get("sink_tokens", 0)
     cap = float(np.float32(cfg.get("logits_soft_cap", 0.0)))
-    if window < -1 or sink < 0 or not (cap >= 0.0) or cap == float("inf"):
-        return INVALID_ARG, None, None
     rope_max = cfg.get("rope_max_positions", 0)
     theta = float(np.float32(cfg.get("rope_theta", 10000.0)))
     rscale = float(np.float32(cfg.get("rope_scale", 1.0)))
-    if rope_max < 0 or (rope_max > 0 and not (0 < theta < float("inf") and 0 < rscale < float("inf"))):
-        return INVALID_ARG, None, None
-    if batch > cfg["max_batch"]:
-        return CAPACITY, None, None
-    if qo[0] != 0 or kvp[0] != 0:
-        return INVALID_ARG, None, None
-    for b in range(batch):
-        if qo[b + 1] < qo[b] or kvp[b + 1] < kvp[b]:
-            return INVALID_ARG, None, None
-        if kvp[b + 1] > kvp[b] and not (1 <= lpl[b] <= page_size):
-            return INVALID_ARG, None, None
-        # RoPE positions (keys 0 .. Lkv-1, queries Lkv-Lq .. Lkv-1) must lie in the table
-        n_pg = kvp[b + 1] - kvp[b]
-        lkv_b = 0 if n_pg == 0 else (n_pg - 1) * page_size + lpl[b]
-        if rope_max > 0 and (lkv_b > rope_max or qo[b + 1] - qo[b] > lkv_b):
-            return INVALID_ARG, None, None
-    if num_pages > 0:
-        idx = np.asarray(kv_indices[:kvp[batch]], dtype=np.int64)
-        if idx.size and (idx.min() < 0 or idx.max() >= num_pages):
-            return INVALID_ARG, None, None
-
+    batch = len(reqs)
     C = cfg["num_ctas"]
-    lq = [qo[b + 1] - qo[b] for b in range(batch)]
-    npg = [kvp[b + 1] - kvp[b] for b in range(batch)]
-    lkv = [0 if npg[b] == 0 else (npg[b] - 1) * page_size + lpl[b] for b in range(batch)]
-
-    granule = {TILE_DECODE: max(page_size, 64), TILE_PREFILL: max(page_size, 128)}
+    lq = [r[1] for r in reqs]
+    lkv = [r[3] for r in reqs]
+    # chunk ends fall on the pages of every cache the plan reads
+    page_gran = max(page_size, shared_page_size if cascade else page_size)
+    granule = {TILE_DECODE: max(page_gran, 64), TILE_PREFILL: max(page_gran, 128)}
 
     def ranges_of(b, T, r0, r1):
         q_first = lkv[b] - lq[b] + r0 // group
         q_last = lkv[b] - lq[b] + (r1 - 1) // group
-        hi = max(0, min(lkv[b], q_last + 1) if causal else lkv[b])
+        causal_b = causal and b >= num_shared
+        hi = max(0, min(lkv[b], q_last + 1) if causal_b else lkv[b])
         if window < 0:
             return [(0, hi)]
         lo = max(0, q_first - window) // granule[T] * granule[T]
@@ -147,56 +243,78 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
             return [(0, hi)]
         return ([(0, sink_end)] if sink_end > 0 else []) + [(lo, hi)]
 
+    def tile_of(b):
+        return TILE_DECODE if lq[b] * group <= TILE_DECODE else TILE_PREFILL
+
     # units in (b, hk, qt) order: (b, hk, qt, T, row0, row1, ranges)
     units = []
+    unit_at = {}
     total = {TILE_DECODE: 0, TILE_PREFILL: 0}
     for b in range(batch):
         R = lq[b] * group
         if R == 0:
             continue
-        T = TILE_DECODE if R <= TILE_DECODE else TILE_PREFILL
+        T = tile_of(b)
         for hk in range(num_kv_heads):
             for qt in range(_ceil_div(R, T)):
                 r0, r1 = qt * T, min(R, (qt + 1) * T)
                 rng = ranges_of(b, T, r0, r1)
+                unit_at[(b, hk, qt)] = len(units)
                 units.append((b, hk, qt, T, r0, r1, rng))
                 total[T] += sum(e - s for s, e in rng)
 
     chunk = {}
-    for T, min_chunk, gran in ((TILE_DECODE, cfg["decode_min_chunk"], max(page_size, 64)),
-                               (TILE_PREFILL, cfg["prefill_min_chunk"], max(page_size, 128))):
+    for T, min_chunk in ((TILE_DECODE, cfg["decode_min_chunk"]), (TILE_PREFILL, cfg["prefill_min_chunk"])):
         want = max(min_chunk, _ceil_div(total[T], C * cfg["split_factor"]))
-        chunk[T] = _ceil_div(want, gran) * gran
+        chunk[T] = _ceil_div(want, granule[T]) * granule[T]
     weight = {TILE_DECODE: cfg["decode_cost_weight"], TILE_PREFILL: cfg["prefill_cost_weight"]}
 
     items = []   # (sort key, fields)
     merges = []
     part_rows = 0
+    unit_parts = []  # per unit: (first partial row or -1, number of chunks)
+    prefill_caches = 0
     for (b, hk, qt, T, r0, r1, rng) in units:
-        pieces = []
-        for s_, e_ in rng:
-            for i in range(_ceil_div(e_ - s_, chunk[T])):
-                pieces.append((s_ + i * chunk[T], min(e_, s_ + (i + 1) * chunk[T])))
-        if not pieces:
-            items.append(((-ITEM_COST_TOKENS * weight[T], -T, b, hk, qt, 0), (b, hk, r0, r1, 0, 0, -1, -1)))
-            continue
-        n = len(pieces)
-        if n == 1:
-            k0, k1 = pieces[0]
-            cost = (k1 - k0 + ITEM_COST_TOKENS) * weight[T]
-            items.append(((-cost, -T, b, hk, qt, 0), (b, hk, r0, r1, k0, k1, -1, -1)))
-            continue
-        m = len(merges)
-        base = part_rows
+        if T == TILE_PREFILL:
+            prefill_caches |= 2 if b < num_shared else 1
+        pieces = [(s_ + i * chunk[T], min(e_, s_ + (i + 1) * chunk[T]))
+                  for s_, e_ in rng for i in range(_ceil_div(e_ - s_, chunk[T]))]
+        n = max(1, len(pieces))
         nrows = r1 - r0
-        merges.append((b, hk, r0, r1, n, base, 0 if T == TILE_DECODE else 1, 0))
-        part_rows += n * nrows
-        for i, (k0, k1) in enumerate(pieces):
+        base, m = -1, -1
+        if n > 1 or cascade:
+            base = part_rows
+            part_rows += n * nrows
+        if n > 1 and not cascade:
+            m = len(merges)
+            merges.append((b, hk, r0, r1, n, base, 0 if T == TILE_DECODE else 1, 0))
+        unit_parts.append((base, n))
+        for i, (k0, k1) in enumerate(pieces or [(0, 0)]):
             cost = (k1 - k0 + ITEM_COST_TOKENS) * weight[T]
-            items.append(((-cost, -T, b, hk, qt, i), (b, hk, r0, r1, k0, k1, base + i * nrows, m)))
+            part = base + i * nrows if base >= 0 else -1
+            items.append(((-cost, -T, b, hk, qt, i), (b, hk, r0, r1, k0, k1, part, m)))
+
+    # cascade merge entries, per ordinary unit: runs of at most CASCADE_ROWS
+    # rows counted from the unit's first row, cut again at the block's q-tile bounds
+    entries = []
+    for u, (b, hk, qt, T, r0, r1, _) in enumerate(units):
+        if not cascade or b < num_shared:
+            continue
+        s = block_of[b]
+        TS = tile_of(s)
+        shift = (reqs[b][0] - reqs[s][0]) * group
+        r = r0
+        while r < r1:
+            sr = r + shift
+            su = unit_at[(s, hk, sr // TS)]
+            s_r0, s_r1 = units[su][4], units[su][5]
+            r_end = min(r1, r0 + ((r - r0) // CASCADE_ROWS + 1) * CASCADE_ROWS, r + (s_r1 - sr))
+            (b0, n0), (b1, n1) = unit_parts[su], unit_parts[u]
+            entries.append((b, hk, r, r_end, n0, b0 + sr - s_r0, s_r1 - s_r0, n1, b1 + r - r0, r1 - r0, 0, 0))
+            r = r_end
 
     if len(items) > cfg["max_items"] or len(merges) > cfg["max_merge_units"] \
-            or part_rows > cfg["max_partial_rows"]:
+            or len(entries) > cfg["max_merge_units"] or part_rows > cfg["max_partial_rows"]:
         return CAPACITY, None, None
 
     items.sort(key=lambda it: it[0])
@@ -213,7 +331,8 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     off_merge = off_items + ITEM_INTS * n_items
     off_cnt = off_merge + MERGE_INTS * n_merge
     off_req = off_cnt + _align4(n_merge)
-    total_ints = off_req + REQ_INTS * batch
+    off_cascade = off_req + REQ_INTS * batch
+    total_ints = off_cascade + CASCADE_INTS * len(entries)
     if total_ints > int_workspace_ints(cfg):
         return CAPACITY, None, None
 
@@ -226,7 +345,8 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
                         off_cnt, off_req, 0, num_qo_heads, num_kv_heads, page_size, total_ints,
                         window, sink, bits(cap), rope_max,
                         bits(theta) if rope_max > 0 else 0, bits(rscale) if rope_max > 0 else 0, rope_off,
-                        sum(1 for m in merges if m[6]), part_rows, qo[batch] if batch > 0 else 0, 0, 0]
+                        sum(1 for m in merges if m[6]), part_rows, total_qo, num_shared,
+                        off_cascade if cascade else 0, len(entries), shared_page_size if cascade else 0, 0, 0]
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos
@@ -239,7 +359,9 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
     for m, fields in enumerate(merges):
         ws[off_merge + MERGE_INTS * m: off_merge + MERGE_INTS * (m + 1)] = fields
     for b in range(batch):
-        ws[off_req + REQ_INTS * b: off_req + REQ_INTS * (b + 1)] = [qo[b], lq[b], kvp[b], lkv[b]]
+        ws[off_req + REQ_INTS * b: off_req + REQ_INTS * (b + 1)] = reqs[b]
+    for e, fields in enumerate(entries):
+        ws[off_cascade + CASCADE_INTS * e: off_cascade + CASCADE_INTS * (e + 1)] = fields
 
     n_dec = sum(1 for _, f in items if lq[f[0]] * group <= 16)
     info = dict(num_ctas=C, num_items=n_items, num_merge_units=n_merge,
@@ -248,7 +370,8 @@ def make_plan(cfg: dict, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo
                 head_dim=head_dim, page_size=page_size, causal=causal, chunk_decode=chunk[16],
                 chunk_prefill=chunk[TILE_PREFILL], num_decode_items=n_dec, num_prefill_items=n_items - n_dec,
                 int_ws_bytes_used=4 * total_ints, max_partial_rows=cfg["max_partial_rows"],
-                variant=(1 if cap > 0 else 0) | (2 if window >= 0 else 0) | (4 if rope_max > 0 else 0))
+                variant=(1 if cap > 0 else 0) | (2 if window >= 0 else 0) | (4 if rope_max > 0 else 0),
+                num_shared=num_shared, num_cascade_merges=len(entries), prefill_caches=prefill_caches)
     return OK, ws, info
 
 

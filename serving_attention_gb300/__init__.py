@@ -53,14 +53,16 @@ class PlanInfo(ctypes.Structure):
                 ("num_decode_items", ctypes.c_int32), ("num_prefill_items", ctypes.c_int32),
                 ("variant", ctypes.c_int32), ("int_ws_bytes_used", ctypes.c_int64),
                 ("max_partial_rows", ctypes.c_int64), ("num_late_merge_units", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("num_shared", ctypes.c_int32), ("num_cascade_merges", ctypes.c_int32),
+                ("prefill_caches", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 EXPORTS = ["fi_default_plan_config", "fi_int_workspace_bytes", "fi_float_workspace_bytes", "fi_plan",
-           "fi_plan_host", "fi_batch_paged_attention_run", "fi_batch_paged_attention_run_static_scratch",
+           "fi_plan_host", "fi_plan_cascade", "fi_plan_cascade_host", "fi_batch_paged_attention_run",
+           "fi_batch_paged_attention_run_cascade", "fi_batch_paged_attention_run_static_scratch",
            "fi_merge_states", "fi_get_device_status", "fi_status_string", "fi_rope_init", "fi_rope_apply_k",
            "fi_selftest_bounded_wait"]
 
@@ -83,6 +85,13 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
     lib.fi_float_workspace_bytes.restype = sz
     lib.fi_plan.argtypes = [cfgp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp, infop]
     lib.fi_plan_host.argtypes = [cfgp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, sz, infop]
+    lib.fi_plan_cascade_host.argtypes = [cfgp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                         i32, i32, vp, sz, infop]
+    lib.fi_plan_cascade.argtypes = [cfgp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                    i32, vp, vp, sz, vp, infop]
+    lib.fi_batch_paged_attention_run_cascade.argtypes = [infop, vp, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp, vp,
+                                                         vp, vp, i32, vp, i32, vp, i64, i64, vp, ctypes.c_int,
+                                                         ctypes.c_float, vp, vp, vp]
     lib.fi_batch_paged_attention_run.argtypes = [infop, vp, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp, i64, i64,
                                                  vp, ctypes.c_int, ctypes.c_float, vp, vp, vp]
     lib.fi_batch_paged_attention_run_static_scratch.argtypes = [infop, vp, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp,
@@ -96,8 +105,9 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
     lib.fi_selftest_bounded_wait.restype = ctypes.c_int
     lib.fi_status_string.argtypes = [ctypes.c_int]
     lib.fi_status_string.restype = ctypes.c_char_p
-    for name in ("fi_default_plan_config", "fi_plan", "fi_plan_host", "fi_batch_paged_attention_run",
-                 "fi_merge_states", "fi_get_device_status", "fi_rope_init", "fi_rope_apply_k"):
+    for name in ("fi_default_plan_config", "fi_plan", "fi_plan_host", "fi_plan_cascade", "fi_plan_cascade_host",
+                 "fi_batch_paged_attention_run", "fi_batch_paged_attention_run_cascade", "fi_merge_states",
+                 "fi_get_device_status", "fi_rope_init", "fi_rope_apply_k"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -200,6 +210,63 @@ def plan(ws: Workspace, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_
     return info
 
 
+def _ptr_or_none(a: np.ndarray):
+    return a.ctypes.data if a.size else None
+
+
+def _cascade_args(shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len, shared_page_size,
+                  shared_num_pages, qo_indptr, kv_indptr, kv_indices, last_page_len):
+    arrs = [_i32(a) for a in (shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len,
+                              qo_indptr, kv_indptr, kv_indices, last_page_len)]
+    sqo, skvp, skvi, slpl, qo, kvp, kvi, lpl = arrs
+    head = [sqo.ctypes.data, skvp.ctypes.data, _ptr_or_none(skvi), _ptr_or_none(slpl), len(sqo) - 1,
+            shared_page_size, shared_num_pages, qo.ctypes.data, kvp.ctypes.data, _ptr_or_none(kvi),
+            _ptr_or_none(lpl), len(qo) - 1]
+    return arrs, head
+
+
+def plan_cascade_host(cfg: PlanConfig, shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len,
+                      shared_page_size: int, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads: int,
+                      num_kv_heads: int, head_dim: int, page_size: int, causal: int, num_pages: int = 0,
+                      shared_num_pages: int = 0):
+    """Host-only two-level (cascade) planning: (status, int32 workspace image or None, PlanInfo)."""
+    keep, head = _cascade_args(shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len,
+                               shared_page_size, shared_num_pages, qo_indptr, kv_indptr, kv_indices, last_page_len)
+    nbytes = int_workspace_bytes(cfg)
+    buf = np.zeros(nbytes // 4, dtype=np.int32)
+    info = PlanInfo()
+    st = load().fi_plan_cascade_host(ctypes.byref(cfg), *head, num_qo_heads, num_kv_heads, head_dim, page_size,
+                                     causal, num_pages, buf.ctypes.data, nbytes, ctypes.byref(info))
+    del keep
+    if st != 0:
+        return st, None, info
+    return st, buf[:info.int_ws_bytes_used // 4].copy(), info
+
+
+def plan_cascade(ws: Workspace, shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len,
+                 shared_page_size: int, qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads: int,
+                 num_kv_heads: int, head_dim: int, page_size: int, causal: int, num_pages: int = 0,
+                 shared_num_pages: int = 0, stream=None) -> PlanInfo:
+    """Plan a two-level (cascade) batch and enqueue the copy of the work list into ws.int_ws."""
+    keep, head = _cascade_args(shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len,
+                               shared_page_size, shared_num_pages, qo_indptr, kv_indptr, kv_indices, last_page_len)
+    i = ws._next
+    ws._next ^= 1
+    if ws._events[i] is not None:
+        ws._events[i].synchronize()  # the staging buffer's previous copy has landed
+    info = PlanInfo()
+    staging = ws._staging[i]
+    st = load().fi_plan_cascade(ctypes.byref(ws.cfg), *head, num_qo_heads, num_kv_heads, head_dim, page_size, causal,
+                                num_pages, ws.int_ws.data_ptr(), staging.data_ptr(), staging.numel(),
+                                _stream_ptr(stream), ctypes.byref(info))
+    del keep
+    _check(st, "fi_plan_cascade")
+    ev = torch.cuda.Event()
+    ev.record(stream if stream is not None else torch.cuda.current_stream())
+    ws._events[i] = ev
+    return info
+
+
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype not in _DTYPE:
         raise TypeError(f"unsupported dtype {t.dtype}")
@@ -224,6 +291,33 @@ def run(ws: Workspace, info: PlanInfo, q: torch.Tensor, k_cache: torch.Tensor, v
         lse.data_ptr() if lse is not None else None, _dtype_code(q), float(sm_scale), ws.int_ws.data_ptr(),
         ws.float_ws.data_ptr(), _stream_ptr(stream))
     _check(st, "fi_batch_paged_attention_run")
+
+
+def run_cascade(ws: Workspace, info: PlanInfo, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                kv_indices_dev: torch.Tensor, shared_k: torch.Tensor, shared_v: torch.Tensor,
+                shared_kv_indices_dev: torch.Tensor, o: torch.Tensor, lse: torch.Tensor | None, sm_scale: float,
+                stream=None):
+    """Enqueue the run of a two-level (cascade) plan: the requests' own cache
+    (k_cache, v_cache, kv_indices_dev) and the shared blocks' cache (shared_k,
+    shared_v, shared_kv_indices_dev), then the cascade merge."""
+    for t in (kv_indices_dev, shared_kv_indices_dev):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError("page tables must be contiguous int32 device tensors")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise TypeError("lse must be contiguous fp32")
+    if any(t.dtype != q.dtype for t in (k_cache, v_cache, shared_k, shared_v, o)):
+        raise TypeError("q, the caches and o must share one dtype")
+    ks = (ctypes.c_int64 * 3)(*k_cache.stride()[:3])
+    vs = (ctypes.c_int64 * 3)(*v_cache.stride()[:3])
+    sks = (ctypes.c_int64 * 3)(*shared_k.stride()[:3])
+    svs = (ctypes.c_int64 * 3)(*shared_v.stride()[:3])
+    st = load().fi_batch_paged_attention_run_cascade(
+        ctypes.byref(info), q.data_ptr(), q.stride(0), q.stride(1), q.shape[0], k_cache.data_ptr(), ks,
+        v_cache.data_ptr(), vs, k_cache.shape[0], kv_indices_dev.data_ptr(), shared_k.data_ptr(), sks,
+        shared_v.data_ptr(), svs, shared_k.shape[0], shared_kv_indices_dev.data_ptr(), shared_k.shape[1],
+        o.data_ptr(), o.stride(0), o.stride(1), lse.data_ptr() if lse is not None else None, _dtype_code(q),
+        float(sm_scale), ws.int_ws.data_ptr(), ws.float_ws.data_ptr(), _stream_ptr(stream))
+    _check(st, "fi_batch_paged_attention_run_cascade")
 
 
 STATIC_SCRATCH_PARTIAL_ROWS = 32768

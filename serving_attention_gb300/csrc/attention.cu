@@ -300,30 +300,187 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   return FI_OK;
 }
 
-extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, int64_t q_stride_tok,
-                                                  int64_t q_stride_head, int32_t q_num_tokens, const void* k_cache,
-                                                  const int64_t k_strides[3], const void* v_cache,
-                                                  const int64_t v_strides[3], int32_t num_pages,
-                                                  const int32_t* kv_indices_dev, void* o, int64_t o_stride_tok,
-                                                  int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale,
-                                                  void* int_workspace_dev, void* float_workspace_dev, void* stream) {
-  if (!info || !q || !k_cache || !v_cache || !k_strides || !v_strides || !kv_indices_dev || !o ||
-      !int_workspace_dev)
-    return FI_ERR_INVALID_ARG;
-  if (info->num_ctas < 1 || q_num_tokens < 1 || num_pages < 1 || !std::isfinite(sm_scale))
-    return FI_ERR_INVALID_ARG;
+namespace fi {
+
+// One KV cache given to a run: K and V [pages, P, Hkv, d] with their strides
+// (elements) and the device page ids of the requests that read it.
+struct CacheArgs {
+  const void* k;
+  const int64_t* k_strides;
+  const void* v;
+  const int64_t* v_strides;
+  int32_t num_pages;
+  const int32_t* kv_indices;
+  int32_t page_size;
+};
+
+fi_status check_cache(const CacheArgs& c) {
+  if (!c.k || !c.v || !c.k_strides || !c.v_strides || !c.kv_indices || c.num_pages < 1) return FI_ERR_INVALID_ARG;
+  const int P = c.page_size;
+  if (P < 1 || P > 128 || (P & (P - 1))) return FI_ERR_UNSUPPORTED;
+  if (!aligned16(c.k) || !aligned16(c.v)) return FI_ERR_ALIGNMENT;
+  for (int i = 0; i < 3; ++i)
+    if (!stride_ok(c.k_strides[i]) || !stride_ok(c.v_strides[i])) return FI_ERR_ALIGNMENT;
+  return FI_OK;
+}
+
+// The tensor maps of one cache.  Prefill-class items of a cache read it on
+// the tensor cores when every TMA box of a page is a whole number of
+// 1024-byte swizzle atoms (P >= 8) and a tile holds whole tokens (G divides
+// 128); otherwise the CUDA-core path runs them.  K and V get maps of their
+// own, each with its own strides: the copy engine does the page/slot/head
+// address arithmetic for both, so equal and unequal K/V strides (the
+// comparison of the BatchAttention PR page, "코드 분석 §2") take one path.
+fi_status build_cache(KvCache* kc, const CacheArgs& c, CUtensorMapDataType tt, int32_t num_kv_heads, int32_t G) {
+  const int P = c.page_size;
+  kc->kv_indices = c.kv_indices;
+  kc->page_size = P;
+  int lp = 0;
+  while ((1 << lp) < P) ++lp;
+  kc->log2_page = lp;
+  kc->num_pages = c.num_pages;
+  kc->tc = (P >= kMinTmaPage && kTileM % G == 0) ? 1 : 0;
+  const uint64_t kd[4] = {uint64_t(kHeadDim), uint64_t(num_kv_heads), uint64_t(P), uint64_t(c.num_pages)};
+  const int64_t ks[3] = {c.k_strides[2], c.k_strides[1], c.k_strides[0]};  // head, slot, page
+  const int64_t vs[3] = {c.v_strides[2], c.v_strides[1], c.v_strides[0]};
+  const uint32_t kbd[4] = {uint32_t(kHeadDim), 1u, uint32_t(P < kStageTokens ? P : kStageTokens), 1u};
+  if (!make_map(&kc->tm_kd, tt, c.k, 4, kd, ks, kbd, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&kc->tm_vd, tt, c.v, 4, kd, vs, kbd, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return FI_ERR_UNSUPPORTED;
+  // Page size 1 where a page's stride is a whole number R >= Hkv of head
+  // strides: each cache is a plain matrix of rows of 128 dims, row
+  // page * R + head, and the decode stages fetch four rows per TMA gather
+  // instead of one single-row box per token.
+  auto rows_per_page = [&](const int64_t* st) -> int64_t {
+    if (st[2] <= 0 || st[0] % st[2]) return 0;
+    const int64_t r = st[0] / st[2];
+    return (r >= num_kv_heads && (int64_t(c.num_pages) + 1) * r < (int64_t(1) << 31)) ? r : 0;
+  };
+  const int64_t rk = rows_per_page(c.k_strides), rv = rows_per_page(c.v_strides);
+  if (P == 1 && rk > 0 && rv > 0) {
+    const uint64_t gk[2] = {uint64_t(kHeadDim), uint64_t(c.num_pages) * uint64_t(rk)};
+    const uint64_t gv[2] = {uint64_t(kHeadDim), uint64_t(c.num_pages) * uint64_t(rv)};
+    const uint32_t gb[2] = {uint32_t(kHeadDim), 1u};
+    if (!make_map(&kc->tm_kg, tt, c.k, 2, gk, &c.k_strides[2], gb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&kc->tm_vg, tt, c.v, 2, gv, &c.v_strides[2], gb, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return FI_ERR_UNSUPPORTED;
+    kc->gather_rows = 1;
+    kc->gather_rows_k = int32_t(rk);
+    kc->gather_rows_v = int32_t(rv);
+  }
+  if (kc->tc) {
+    const uint32_t kb[4] = {64u, 1u, uint32_t(P), 1u};
+    if (!make_map(&kc->tm_k, tt, c.k, 4, kd, ks, kb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&kc->tm_v, tt, c.v, 4, kd, vs, kb, CU_TENSOR_MAP_SWIZZLE_128B))
+      return FI_ERR_UNSUPPORTED;
+  }
+  return FI_OK;
+}
+
+// Cascade merge (two-level plans), launched after the run on the same
+// stream: for every entry and packed row, the LSE-weighted merge of the
+// row's partial states -- its shared block's chunks, then its own request's
+// chunks, in that order -- written as O and LSE.  One warp per (entry, row)
+// task; an entry holds at most FI_CASCADE_ROWS rows, so the tasks are
+// (entry, 0 .. FI_CASCADE_ROWS - 1) walked with a grid stride, and the counts
+// come from the workspace header (a graph captured once replays correctly
+// for any later cascade plan).  Lane l holds dims 4l..4l+3.  Nothing is
+// written when the status word reports an error.
+template <typename T>
+__global__ void __launch_bounds__(256) cascade_merge_kernel(const int32_t* __restrict__ iws,
+                                                            const float* __restrict__ fws, int64_t partial_o_offset,
+                                                            T* o, int64_t o_stride_tok, int64_t o_stride_head,
+                                                            float* lse, int num_qo_heads, int group) {
+  const int lane = threadIdx.x & 31;
+  if (iws[FI_H_STATUS] != 0) return;
+  const int64_t tasks = int64_t(iws[FI_H_NUM_CASCADE]) * FI_CASCADE_ROWS;
+  const int32_t* ent = iws + iws[FI_H_OFF_CASCADE];
+  const int32_t* reqs = iws + iws[FI_H_OFF_REQUESTS];
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t task = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks; task += warps) {
+    const int4* e4 = reinterpret_cast<const int4*>(ent + FI_CASCADE_INTS * (task / FI_CASCADE_ROWS));
+    const int4 e0 = __ldg(e4), e1 = __ldg(e4 + 1), e2 = __ldg(e4 + 2);
+    // {b, hk, row0, row1}, {n0, base0, stride0, n1}, {base1, stride1, 0, 0}
+    const int r = int(task % FI_CASCADE_ROWS);
+    if (r >= e0.w - e0.z) continue;
+    const int n0 = e1.x, n = e1.x + e1.w;
+    // part c (c < n): partial row of the row's c-th state
+    auto part_row = [&](int c) -> int64_t {
+      return c < n0 ? int64_t(e1.y) + int64_t(c) * e1.z + r : int64_t(e2.x) + int64_t(c - n0) * e2.y + r;
+    };
+    float M = -INFINITY;
+    for (int c0 = 0; c0 < n; c0 += 32)
+      M = fmaxf(M, c0 + lane < n ? __ldcg(fws + part_row(c0 + lane)) : -INFINITY);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float Ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int c0 = 0; c0 < n; c0 += 32) {
+        const float w_mine =
+            c0 + lane < n ? ex2((__ldcg(fws + part_row(c0 + lane)) - M) * 1.4426950408889634f) : 0.f;
+        const int cn = min(32, n - c0);
+        for (int g0 = 0; g0 < cn; g0 += 8) {
+          float4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (g0 + u < cn)
+              v[u] = __ldcg(reinterpret_cast<const float4*>(fws + partial_o_offset +
+                                                            part_row(c0 + g0 + u) * kHeadDim) + lane);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float w = __shfl_sync(0xffffffffu, w_mine, (g0 + u) & 31);
+            if (g0 + u < cn) {
+              Ls += w;
+              acc.x += w * v[u].x;
+              acc.y += w * v[u].y;
+              acc.z += w * v[u].z;
+              acc.w += w * v[u].w;
+            }
+          }
+        }
+      }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    const int row = e0.z + r;
+    const int t = row / group;
+    const int head = e0.y * group + (row - t * group);
+    const int64_t tok = int64_t(reqs[FI_REQ_INTS * e0.x]) + t;
+    uint2 packed;
+    packed.x = Elem<T>::from_float2(acc.x * inv, acc.y * inv);
+    packed.y = Elem<T>::from_float2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(o + tok * o_stride_tok + int64_t(head) * o_stride_head + lane * 4) = packed;
+    if (lane == 0 && lse) lse[tok * num_qo_heads + head] = Ls > 0.f ? M + __logf(Ls) : -INFINITY;
+  }
+}
+
+template <typename T>
+cudaError_t launch_cascade_merge(const RunParams& p, int32_t blocks, cudaStream_t s) {
+  cascade_merge_kernel<T><<<unsigned(blocks), 256, 0, s>>>(p.iws, p.fws, p.partial_o_offset,
+                                                           reinterpret_cast<T*>(p.o), p.o_stride_tok,
+                                                           p.o_stride_head, p.lse, p.num_qo_heads, p.group);
+  return cudaGetLastError();
+}
+
+// The run behind both entry points: the plan's own cache, and for a cascade
+// plan the shared blocks' cache.
+fi_status run_impl(const fi_plan_info* info, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                   int32_t q_num_tokens, const CacheArgs& own, const CacheArgs* shared, void* o,
+                   int64_t o_stride_tok, int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale,
+                   void* int_workspace_dev, void* float_workspace_dev, void* stream) {
+  if (!info || !q || !o || !int_workspace_dev) return FI_ERR_INVALID_ARG;
+  if (info->num_ctas < 1 || q_num_tokens < 1 || !std::isfinite(sm_scale)) return FI_ERR_INVALID_ARG;
   if (info->num_partial_rows > 0 && !float_workspace_dev) return FI_ERR_INVALID_ARG;
+  if (info->num_shared > 0 && !shared) return FI_ERR_INVALID_ARG;  // a cascade plan needs the shared cache
   if (info->head_dim != kHeadDim) return FI_ERR_UNSUPPORTED;
   if (dtype != FI_FP16 && dtype != FI_BF16) return FI_ERR_UNSUPPORTED;
-  const int P = info->page_size;
-  if (P < 1 || P > 128 || (P & (P - 1))) return FI_ERR_UNSUPPORTED;
   if (info->num_kv_heads < 1 || info->num_qo_heads % info->num_kv_heads) return FI_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
-      !aligned16(int_workspace_dev) || (float_workspace_dev && !aligned16(float_workspace_dev)) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
+  fi_status st = check_cache(own);
+  if (st == FI_OK && shared) st = check_cache(*shared);
+  if (st != FI_OK) return st;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(int_workspace_dev) ||
+      (float_workspace_dev && !aligned16(float_workspace_dev)) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return FI_ERR_ALIGNMENT;
-  for (int i = 0; i < 3; ++i)
-    if (!stride_ok(k_strides[i]) || !stride_ok(v_strides[i])) return FI_ERR_ALIGNMENT;
   if (!stride_ok(q_stride_tok) || !stride_ok(q_stride_head) || !stride_ok(o_stride_tok) || !stride_ok(o_stride_head))
     return FI_ERR_ALIGNMENT;
 
@@ -332,15 +489,6 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   p.q = static_cast<const uint16_t*>(q);
   p.q_stride_tok = q_stride_tok;
   p.q_stride_head = q_stride_head;
-  p.k = static_cast<const uint16_t*>(k_cache);
-  p.k_stride_page = k_strides[0];
-  p.k_stride_slot = k_strides[1];
-  p.k_stride_head = k_strides[2];
-  p.v = static_cast<const uint16_t*>(v_cache);
-  p.v_stride_page = v_strides[0];
-  p.v_stride_slot = v_strides[1];
-  p.v_stride_head = v_strides[2];
-  p.kv_indices = kv_indices_dev;
   p.o = static_cast<uint16_t*>(o);
   p.o_stride_tok = o_stride_tok;
   p.o_stride_head = o_stride_head;
@@ -354,60 +502,21 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   p.num_qo_heads = info->num_qo_heads;
   p.num_kv_heads = info->num_kv_heads;
   p.group = info->num_qo_heads / info->num_kv_heads;
-  p.page_size = P;
-  int lp = 0;
-  while ((1 << lp) < P) ++lp;
-  p.log2_page = lp;
-  p.num_pages = num_pages;
-
-  // Prefill-class items go to the tensor cores when every TMA box of a page is a
-  // whole number of 1024-byte swizzle atoms (P >= 8) and a tile holds whole
-  // tokens (G divides 128); otherwise the CUDA-core path runs them.
   const int G = p.group;
-  p.tc_prefill = (P >= kMinTmaPage && kTileM % G == 0) ? 1 : 0;
-  // K and V get tensor maps of their own, each with its own strides: the
-  // copy engine does the page/slot/head address arithmetic for both, so
-  // equal and unequal K/V strides (the comparison of the BatchAttention PR
-  // page, "코드 분석 §2") take the same path.
   const CUtensorMapDataType tt = dtype == FI_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const uint64_t kd[4] = {uint64_t(kHeadDim), uint64_t(info->num_kv_heads), uint64_t(P), uint64_t(num_pages)};
-  const int64_t ks[3] = {k_strides[2], k_strides[1], k_strides[0]};  // head, slot, page
-  const int64_t vs[3] = {v_strides[2], v_strides[1], v_strides[0]};
-  const uint32_t kbd[4] = {uint32_t(kHeadDim), 1u, uint32_t(P < kStageTokens ? P : kStageTokens), 1u};
-  if (!make_map(&p.tm_kd, tt, k_cache, 4, kd, ks, kbd, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map(&p.tm_vd, tt, v_cache, 4, kd, vs, kbd, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return FI_ERR_UNSUPPORTED;
-  // Page size 1 where a page's stride is a whole number R >= Hkv of head
-  // strides: each cache is a plain matrix of rows of 128 dims, row
-  // page * R + head, and the decode stages fetch four rows per TMA gather
-  // instead of one single-row box per token.
-  auto rows_per_page = [&](const int64_t* st) -> int64_t {
-    if (st[2] <= 0 || st[0] % st[2]) return 0;
-    const int64_t r = st[0] / st[2];
-    return (r >= info->num_kv_heads && (int64_t(num_pages) + 1) * r < (int64_t(1) << 31)) ? r : 0;
-  };
-  const int64_t rk = rows_per_page(k_strides), rv = rows_per_page(v_strides);
-  if (P == 1 && rk > 0 && rv > 0) {
-    const uint64_t gk[2] = {uint64_t(kHeadDim), uint64_t(num_pages) * uint64_t(rk)};
-    const uint64_t gv[2] = {uint64_t(kHeadDim), uint64_t(num_pages) * uint64_t(rv)};
-    const uint32_t gb[2] = {uint32_t(kHeadDim), 1u};
-    if (!make_map(&p.tm_kg, tt, k_cache, 2, gk, &k_strides[2], gb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&p.tm_vg, tt, v_cache, 2, gv, &v_strides[2], gb, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return FI_ERR_UNSUPPORTED;
-    p.gather_rows = 1;
-    p.gather_rows_k = int32_t(rk);
-    p.gather_rows_v = int32_t(rv);
+  st = build_cache(&p.kv[0], own, tt, info->num_kv_heads, G);
+  if (st == FI_OK && shared) {
+    st = build_cache(&p.kv[1], *shared, tt, info->num_kv_heads, G);
+    p.has_shared = 1;
   }
-  if (p.tc_prefill) {
+  if (st != FI_OK) return st;
+  if (p.kv[0].tc || p.kv[1].tc) {
     const uint64_t qd[3] = {uint64_t(kHeadDim), uint64_t(info->num_qo_heads), uint64_t(q_num_tokens)};
     const int64_t qs[2] = {q_stride_head, q_stride_tok};
     const uint32_t qb[3] = {64u, uint32_t(G), uint32_t(kTileM / G)};
-    const uint32_t kb[4] = {64u, 1u, uint32_t(P), 1u};
     const int64_t os[2] = {o_stride_head, o_stride_tok};
     if (!make_map(&p.tm_q, tt, q, 3, qd, qs, qb, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.tm_o, tt, o, 3, qd, os, qb, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.tm_k, tt, k_cache, 4, kd, ks, kb, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&p.tm_v, tt, v_cache, 4, kd, vs, kb, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&p.tm_o, tt, o, 3, qd, os, qb, CU_TENSOR_MAP_SWIZZLE_128B))
       return FI_ERR_UNSUPPORTED;
   }
 
@@ -416,14 +525,49 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   // sliding window / sink mask, bit 2 RoPE; the plain kernel carries none.
   // The late merge follows the run when the plan in `info` has late units;
   // a graph captured from a plan without any replays no late merge, and the
-  // run then merges late units of later plans itself.
+  // run then merges late units of later plans itself.  A cascade plan's
+  // merge follows the run when `info` has cascade entries.
   p.late_merge = info->num_late_merge_units > 0 ? 1 : 0;
   cudaError_t e = dtype == FI_BF16 ? launch_variant<__nv_bfloat16>(p, info->num_ctas, info->variant, s)
                                    : launch_variant<__half>(p, info->num_ctas, info->variant, s);
   if (e == cudaSuccess && p.late_merge)
     e = dtype == FI_BF16 ? launch_late_merge<__nv_bfloat16>(p, 4 * info->num_ctas, s)
                          : launch_late_merge<__half>(p, 4 * info->num_ctas, s);
+  if (e == cudaSuccess && info->num_cascade_merges > 0)
+    e = dtype == FI_BF16 ? launch_cascade_merge<__nv_bfloat16>(p, 4 * info->num_ctas, s)
+                         : launch_cascade_merge<__half>(p, 4 * info->num_ctas, s);
   return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
+}  // namespace fi
+
+extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, int64_t q_stride_tok,
+                                                  int64_t q_stride_head, int32_t q_num_tokens, const void* k_cache,
+                                                  const int64_t k_strides[3], const void* v_cache,
+                                                  const int64_t v_strides[3], int32_t num_pages,
+                                                  const int32_t* kv_indices_dev, void* o, int64_t o_stride_tok,
+                                                  int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale,
+                                                  void* int_workspace_dev, void* float_workspace_dev, void* stream) {
+  if (!info) return FI_ERR_INVALID_ARG;
+  const CacheArgs own{k_cache, k_strides, v_cache, v_strides, num_pages, kv_indices_dev, info->page_size};
+  return run_impl(info, q, q_stride_tok, q_stride_head, q_num_tokens, own, nullptr, o, o_stride_tok, o_stride_head,
+                  lse, dtype, sm_scale, int_workspace_dev, float_workspace_dev, stream);
+}
+
+extern "C" fi_status fi_batch_paged_attention_run_cascade(
+    const fi_plan_info* info, const void* q, int64_t q_stride_tok, int64_t q_stride_head, int32_t q_num_tokens,
+    const void* k_cache, const int64_t k_strides[3], const void* v_cache, const int64_t v_strides[3],
+    int32_t num_pages, const int32_t* kv_indices_dev, const void* shared_k_cache, const int64_t shared_k_strides[3],
+    const void* shared_v_cache, const int64_t shared_v_strides[3], int32_t shared_num_pages,
+    const int32_t* shared_kv_indices_dev, int32_t shared_page_size, void* o, int64_t o_stride_tok,
+    int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale, void* int_workspace_dev,
+    void* float_workspace_dev, void* stream) {
+  if (!info) return FI_ERR_INVALID_ARG;
+  const CacheArgs own{k_cache, k_strides, v_cache, v_strides, num_pages, kv_indices_dev, info->page_size};
+  const CacheArgs shared{shared_k_cache,   shared_k_strides, shared_v_cache,  shared_v_strides,
+                         shared_num_pages, shared_kv_indices_dev, shared_page_size};
+  return run_impl(info, q, q_stride_tok, q_stride_head, q_num_tokens, own, &shared, o, o_stride_tok, o_stride_head,
+                  lse, dtype, sm_scale, int_workspace_dev, float_workspace_dev, stream);
 }
 
 extern "C" fi_status fi_rope_init(const fi_plan_config* cfg, void* int_workspace_dev, void* stream) {

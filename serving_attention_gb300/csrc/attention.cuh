@@ -50,22 +50,32 @@ static_assert(kRegsLoader * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads, 
 constexpr int kMmaWarp = 1;
 constexpr int kVWarp = 2;              // loads V tiles; warp 0 loads Q and K tiles
 
-struct RunParams {
-  CUtensorMap tm_q;  // [q tokens, Hq, d] boxes of (64 dims, G heads, 128/G tokens), 128-byte swizzle
-  CUtensorMap tm_k;  // [pages, P, Hkv, d] boxes of (64 dims, 1 head, P slots, 1 page), 128-byte swizzle
+// One KV cache as the kernel reads it: K and V [pages, P, Hkv, d], each
+// through its own tensor maps (its own strides), and the page ids of its
+// requests.
+struct KvCache {
+  CUtensorMap tm_k;   // boxes of (64 dims, 1 head, P slots, 1 page), 128-byte swizzle (tensor-core path)
   CUtensorMap tm_v;
-  CUtensorMap tm_kd;  // [pages, P, Hkv, d] boxes of (128 dims, 1 head, min(P, 128) slots, 1 page), no swizzle
+  CUtensorMap tm_kd;  // boxes of (128 dims, 1 head, min(P, 128) slots, 1 page), no swizzle (CUDA-core path)
   CUtensorMap tm_vd;
   CUtensorMap tm_kg;  // page size 1: [pages * rows_per_page, d], rows of 128 dims gathered four at a time
   CUtensorMap tm_vg;
-  CUtensorMap tm_o;   // O as [q tokens, Hq, d] with the boxes of tm_q: stores of whole 128-row output tiles
+  const int32_t* kv_indices;
+  int32_t page_size, log2_page, num_pages;
+  int32_t tc;             // prefill-class items of this cache run on the tensor cores (tm_k, tm_v built)
+  int32_t gather_rows;    // page size 1: decode stages by 4-row gathers of rows page * rows_k/v + head
+  int32_t gather_rows_k;  // page stride / head stride of K (>= Hkv)
+  int32_t gather_rows_v;  // the same for V
+};
+
+struct RunParams {
+  CUtensorMap tm_q;  // [q tokens, Hq, d] boxes of (64 dims, G heads, 128/G tokens), 128-byte swizzle
+  CUtensorMap tm_o;  // O as [q tokens, Hq, d] with the boxes of tm_q: stores of whole 128-row output tiles
+  // kv[0]: the cache of the plan's own requests; kv[1]: the shared blocks'
+  // cache of a cascade plan (requests b < num_shared of the plan read it).
+  KvCache kv[2];
   const uint16_t* q;
   int64_t q_stride_tok, q_stride_head;
-  const uint16_t* k;
-  int64_t k_stride_page, k_stride_slot, k_stride_head;
-  const uint16_t* v;
-  int64_t v_stride_page, v_stride_slot, v_stride_head;
-  const int32_t* kv_indices;
   uint16_t* o;
   int64_t o_stride_tok, o_stride_head;
   float* lse;
@@ -75,13 +85,16 @@ struct RunParams {
   int64_t max_partial_rows;  // partial-state rows the float workspace holds
   int32_t q_num_tokens;      // rows of Q and O
   float scale_log2;          // sm_scale * log2(e)
-  int32_t num_qo_heads, num_kv_heads, group, page_size, log2_page, num_pages;
-  int32_t tc_prefill;        // prefill-class items on the tensor cores (else CUDA cores)
+  int32_t num_qo_heads, num_kv_heads, group;
+  int32_t has_shared;        // kv[1] was given (a cascade run)
   int32_t late_merge;        // the late merge launch follows this run (else late units merge in the run)
-  int32_t gather_rows;       // page size 1: decode stages by 4-row gathers of rows page * rows_k/v + head
-  int32_t gather_rows_k;     // page stride / head stride of K (>= Hkv)
-  int32_t gather_rows_v;     // the same for V
 };
+
+// The cache request b reads (num_shared: the plan's shared blocks, 0 in a
+// one-level plan).
+__device__ __forceinline__ const KvCache& cache_of(const RunParams& p, int32_t b, int32_t num_shared) {
+  return p.kv[b < num_shared ? 1 : 0];
+}
 
 struct DecodeBufs {
   uint16_t k[kStages][kStageTokens][kHeadDim];

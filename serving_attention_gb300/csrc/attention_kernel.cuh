@@ -47,15 +47,13 @@ __device__ __forceinline__ int groups_in_pass(int rows) {
 // HBM; stage tokens past the chunk are masked
 // by the consumers.
 static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
-                        int32_t off_req) {
+                        int32_t off_req, int32_t num_shared) {
   const int lane = threadIdx.x & 31;
-  const int lp = p.log2_page, P = p.page_size;
-  const int boxes = P >= kStageTokens ? 1 : (kStageTokens >> lp);  // per stage and tensor
-  const int box_slots = P >= kStageTokens ? kStageTokens : P;
   constexpr uint32_t kStageBytes = 2u * kStageTokens * kHeadDim * 2u;
-  if (lane == 0) {
-    tc::prefetch_tensormap(p.gather_rows ? &p.tm_kg : &p.tm_kd);
-    tc::prefetch_tensormap(p.gather_rows ? &p.tm_vg : &p.tm_vd);
+  if (lane < 1 + (num_shared > 0)) {
+    const KvCache& kc = p.kv[lane];
+    tc::prefetch_tensormap(kc.gather_rows ? &kc.tm_kg : &kc.tm_kd);
+    tc::prefetch_tensormap(kc.gather_rows ? &kc.tm_vg : &kc.tm_vd);
   }
   uint32_t it = 0;
   int armed[kStages];
@@ -64,11 +62,15 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
   for (int32_t i = item_begin; i < item_end; ++i) {
     const Item item = load_item(p.iws, off_items, i);
     const Request rq = load_request(p.iws, off_req, item.b);
+    const KvCache& kc = cache_of(p, item.b, num_shared);
+    const int lp = kc.log2_page, P = kc.page_size;
+    const int boxes = P >= kStageTokens ? 1 : (kStageTokens >> lp);  // per stage and tensor
+    const int box_slots = P >= kStageTokens ? kStageTokens : P;
     const int nrows = item.row1 - item.row0;
     const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
     const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
     const int npages = min((rq.kv_len + P - 1) >> lp, (item.kv1 + P - 1) >> lp);  // pages the chunk touches
-    const int32_t* pages = p.kv_indices + rq.page_start;
+    const int32_t* pages = kc.kv_indices + rq.page_start;
     for (int pass = 0; pass < passes; ++pass) {
       // page ids of the next stage's boxes: lane, lane + 32, ... (box loads)
       // or 4 * lane .. 4 * lane + 3 (the four rows of a lane's gather)
@@ -77,8 +79,8 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
         const int pg0 = (item.kv0 + st * kStageTokens) >> lp;
 #pragma unroll
         for (int r = 0; r < kBoxLanes; ++r) {
-          const int bx = p.gather_rows ? kBoxLanes * lane + r : lane + 32 * r;
-          nx[r] = (bx < boxes && pg0 + bx < npages) ? __ldg(pages + pg0 + bx) : p.num_pages;
+          const int bx = kc.gather_rows ? kBoxLanes * lane + r : lane + 32 * r;
+          nx[r] = (bx < boxes && pg0 + bx < npages) ? __ldg(pages + pg0 + bx) : kc.num_pages;
         }
       };
       if (nst > 0) fetch_ids(0);
@@ -94,23 +96,23 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
         __syncwarp();
         const int j0 = item.kv0 + st * kStageTokens;
         const int slot0 = P > kStageTokens ? (j0 & (P - 1)) : 0;
-        if (p.gather_rows) {
+        if (kc.gather_rows) {
           // page size 1: lane l brings tokens 4l..4l+3 of K and of V with one
           // four-row gather each (row page * rows_per_page + hk; pages past
           // the chunk are rows past the tensor and arrive as zeros)
           static_assert(kBoxLanes == 4, "one four-row gather per lane and tensor");
-          const int rk = p.gather_rows_k, rv = p.gather_rows_v;
-          tc::tma_gather4_2d(&sm.dec.k[s][4 * lane][0], &p.tm_kg, &sm.full[s], 0, id[0] * rk + item.hk,
+          const int rk = kc.gather_rows_k, rv = kc.gather_rows_v;
+          tc::tma_gather4_2d(&sm.dec.k[s][4 * lane][0], &kc.tm_kg, &sm.full[s], 0, id[0] * rk + item.hk,
                              id[1] * rk + item.hk, id[2] * rk + item.hk, id[3] * rk + item.hk);
-          tc::tma_gather4_2d(&sm.dec.v[s][4 * lane][0], &p.tm_vg, &sm.full[s], 0, id[0] * rv + item.hk,
+          tc::tma_gather4_2d(&sm.dec.v[s][4 * lane][0], &kc.tm_vg, &sm.full[s], 0, id[0] * rv + item.hk,
                              id[1] * rv + item.hk, id[2] * rv + item.hk, id[3] * rv + item.hk);
         } else {
 #pragma unroll
           for (int r = 0; r < kBoxLanes; ++r) {
             const int bx = lane + 32 * r;
             if (bx < boxes) {
-              tc::tma_load_4d(&sm.dec.k[s][bx * box_slots][0], &p.tm_kd, &sm.full[s], 0, item.hk, slot0, id[r]);
-              tc::tma_load_4d(&sm.dec.v[s][bx * box_slots][0], &p.tm_vd, &sm.full[s], 0, item.hk, slot0, id[r]);
+              tc::tma_load_4d(&sm.dec.k[s][bx * box_slots][0], &kc.tm_kd, &sm.full[s], 0, item.hk, slot0, id[r]);
+              tc::tma_load_4d(&sm.dec.v[s][bx * box_slots][0], &kc.tm_vd, &sm.full[s], 0, item.hk, slot0, id[r]);
             }
           }
         }
@@ -359,7 +361,8 @@ __device__ void rope_decode(const RunParams& p, RunSmem& sm, int32_t item_begin,
 
 template <typename T, bool kCap, bool kMask, bool kRope>
 __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
-                        int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, const Variant var) {
+                        int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, int32_t num_shared,
+                        const Variant var) {
   const int cw = (threadIdx.x >> 5) - kFirstConsumerWarp;  // consumer warp 0..7
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
@@ -376,6 +379,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
     const int nrows = item.row1 - item.row0;
     const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
     const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
+    const bool causal_i = causal && item.b >= num_shared;  // a shared block's keys are all visible
 
     for (int pass = 0; pass < passes; ++pass) {
       const int prow0 = pass * kRowsPerPass;
@@ -405,7 +409,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
           unpack4x2<T>(u, q[r]);
 #pragma unroll
           for (int c = 0; c < 4; ++c) q[r][c] = make_float2(q[r][c].x * p.scale_log2, q[r][c].y * p.scale_log2);
-          lim = causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1;
+          lim = causal_i ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1;
           if (kMask && r == my_row) lo_mine = window_low(var, rq.kv_len - rq.qo_len + t);
         } else {
 #pragma unroll
@@ -604,19 +608,22 @@ namespace fi {
 // ---------------------------------------------------------------- kernel
 
 // A CTA's items come prefill-class (256-row tiles) first, then decode-class
-// (16-row tiles); returns the index of its first decode-class item.
-// Called by whole warps: lane l looks at item i0 + l (its request's row count
-// decides the class), so 32 items cost two dependent loads, not 64.
-__device__ __forceinline__ int32_t first_decode_item(const RunParams& p, int32_t begin, int32_t end, int32_t off_items,
-                                                     int32_t off_req) {
+// (16-row tiles); returns the index of its first item for the CUDA-core path:
+// a decode-class item, or a prefill-class item whose KV cache has no
+// tensor-core maps (pages under 8 tokens, or G not dividing 128).  The
+// tensor-core phase takes the items before it.  Called by whole warps: lane
+// l looks at item i0 + l (its request's row count decides the class), so 32
+// items cost two dependent loads, not 64.
+__device__ __forceinline__ int32_t first_cuda_core_item(const RunParams& p, int32_t begin, int32_t end,
+                                                        int32_t off_items, int32_t off_req, int32_t num_shared) {
   const int lane = threadIdx.x & 31;
   for (int32_t i0 = begin; i0 < end; i0 += 32) {
-    bool dec = true;  // past the CTA's last item counts as the boundary
+    bool cc = true;  // past the CTA's last item counts as the boundary
     if (i0 + lane < end) {
       const int32_t b = __ldg(p.iws + off_items + FI_ITEM_INTS * (i0 + lane));
-      dec = __ldg(p.iws + off_req + FI_REQ_INTS * b + 1) * p.group <= FI_TILE_DECODE;
+      cc = __ldg(p.iws + off_req + FI_REQ_INTS * b + 1) * p.group <= FI_TILE_DECODE || !cache_of(p, b, num_shared).tc;
     }
-    const unsigned m = __ballot_sync(0xffffffffu, dec);
+    const unsigned m = __ballot_sync(0xffffffffu, cc);
     if (m) return min(end, i0 + __ffs(m) - 1);
   }
   return end;
@@ -643,9 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   const int32_t h_rows = ws_header(iws, FI_H_PARTIAL_ROWS), h_qo = ws_header(iws, FI_H_TOTAL_QO);
   const int32_t h_hq = ws_header(iws, FI_H_NUM_QO_HEADS), h_hkv = ws_header(iws, FI_H_NUM_KV_HEADS);
   const int32_t h_page = ws_header(iws, FI_H_PAGE_SIZE);
+  const int32_t num_shared = ws_header(iws, FI_H_NUM_SHARED), h_spage = ws_header(iws, FI_H_SHARED_PAGE_SIZE);
   bool bad = magic != FI_PLAN_MAGIC || n_ctas != int32_t(gridDim.x) || (smem_u32(smem_raw) & 1023u) != 0 ||
              h_rows < 0 || h_rows > p.max_partial_rows || h_qo < 0 || h_qo > p.q_num_tokens ||
-             h_hq != p.num_qo_heads || h_hkv != p.num_kv_heads || h_page != p.page_size;
+             h_hq != p.num_qo_heads || h_hkv != p.num_kv_heads || h_page != p.kv[0].page_size ||
+             num_shared < 0 || (num_shared > 0 && (!p.has_shared || h_spage != p.kv[1].page_size));
   int32_t begin = 0, end = 0;
   if (!bad) {
     begin = __ldg(iws + off_cta + blockIdx.x);
@@ -669,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   var.cap_b = cap > 0.f ? 2.f / cap : 0.f;
   var.rope_table = kRope ? reinterpret_cast<const float2*>(iws + ws_header(iws, FI_H_ROPE_TABLE_OFF)) : nullptr;
   const int warp = threadIdx.x >> 5;
-  const int32_t mid = p.tc_prefill ? first_decode_item(p, begin, end, off_items, off_req) : begin;
+  const int32_t mid = first_cuda_core_item(p, begin, end, off_items, off_req, num_shared);
   const bool tc_phase = mid > begin;
 
   if (threadIdx.x == 0) {
@@ -714,14 +723,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
     if (warp < kSoftmaxWarp0) {
       tc::setmaxnreg_dec<kRegsLoader>();
       if (warp == 0) {
-        pf_produce<kRope ? kProduceQKV : kProduceQK>(p, sm, begin, mid, off_items, off_req);
+        pf_produce<kRope ? kProduceQKV : kProduceQK>(p, sm, begin, mid, off_items, off_req, num_shared);
       } else if (warp == kMmaWarp) {
         pf_mma<T, kRope>(p, sm, begin, mid, off_items);
         __syncwarp();
       } else if (kRope) {
         pf_rope<T>(p, sm, begin, mid, off_items, off_req, var);  // warps 2 and 3
       } else if (warp == kVWarp) {
-        pf_produce<kProduceV>(p, sm, begin, mid, off_items, off_req);
+        pf_produce<kProduceV>(p, sm, begin, mid, off_items, off_req, num_shared);
       }
       tc::fence_before_sync();
       named_barrier_sync_unaligned(kPhaseBarrier, kThreads);
@@ -729,7 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
       tc::setmaxnreg_inc<kRegsLaunch>();
     } else {
       tc::setmaxnreg_inc<kRegsSoftmax>();
-      pf_softmax<T, kCap, kMask>(p, sm, begin, mid, off_items, off_req, off_merge, off_cnt, causal, var);
+      pf_softmax<T, kCap, kMask>(p, sm, begin, mid, off_items, off_req, off_merge, off_cnt, causal, num_shared,
+                                 var);
       tc::setmaxnreg_dec<kRegsLaunch>();
       tc::fence_before_sync();
       named_barrier_sync_unaligned(kPhaseBarrier, kThreads);
@@ -738,9 +748,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   }
 
   if (warp == 0) {
-    produce(p, sm, mid, end, off_items, off_req);
+    produce(p, sm, mid, end, off_items, off_req, num_shared);
   } else if (warp >= kFirstConsumerWarp) {
-    consume<T, kCap, kMask, kRope>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal, var);
+    consume<T, kCap, kMask, kRope>(p, sm, mid, end, off_items, off_req, off_merge, off_cnt, causal, num_shared, var);
   } else if (kRope && warp >= 1 && warp <= 3) {
     rope_decode<T>(p, sm, mid, end, off_items, var);
   }

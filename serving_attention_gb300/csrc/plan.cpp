@@ -74,7 +74,7 @@ bool deal_before(const Chunk& x, const Chunk& y) {
 int64_t fi::plan_capacity_ints(const fi_plan_config* cfg) {
   return FI_HEADER_INTS + round4(int64_t(cfg->num_ctas) + 1) + int64_t(FI_ITEM_INTS) * cfg->max_items +
          int64_t(FI_MERGE_INTS) * cfg->max_merge_units + round4(cfg->max_merge_units) +
-         int64_t(FI_REQ_INTS) * cfg->max_batch;
+         int64_t(FI_REQ_INTS) * cfg->max_batch + int64_t(FI_CASCADE_INTS) * cfg->max_merge_units;
 }
 
 extern "C" size_t fi_int_workspace_bytes(const fi_plan_config* cfg) {
@@ -89,57 +89,85 @@ extern "C" size_t fi_float_workspace_bytes(const fi_plan_config* cfg, int32_t he
   return size_t(fi_partial_o_offset(cfg->max_partial_rows) + cfg->max_partial_rows * int64_t(head_dim)) * 4;
 }
 
-extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_indptr, const int32_t* kv_indptr,
-                                  const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch,
-                                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                                  int32_t page_size, int32_t causal, int32_t num_pages, void* workspace_host,
-                                  size_t workspace_bytes, fi_plan_info* info_out) {
-  if (!cfg || !info_out || !workspace_host || batch < 0) return FI_ERR_INVALID_ARG;
-  if (batch > 0 && (!qo_indptr || !kv_indptr || !last_page_len)) return FI_ERR_INVALID_ARG;
-  if (head_dim != 128) return FI_ERR_UNSUPPORTED;
-  if (page_size < 1 || page_size > 128 || (page_size & (page_size - 1))) return FI_ERR_UNSUPPORTED;
-  if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads) return FI_ERR_UNSUPPORTED;
-  const int32_t group = num_qo_heads / num_kv_heads;
-  if (group > 16) return FI_ERR_UNSUPPORTED;
-  if ((causal != 0 && causal != 1) || cfg->num_ctas < 1 || cfg->split_factor < 1) return FI_ERR_INVALID_ARG;
-  if (cfg->decode_min_chunk < 1 || cfg->prefill_min_chunk < 1) return FI_ERR_INVALID_ARG;
-  const int32_t window = cfg->window_left, sink = cfg->sink_tokens;
-  const float cap = cfg->logits_soft_cap;
-  if (window < -1 || sink < 0 || !(cap >= 0.f) || cap == HUGE_VALF) return FI_ERR_INVALID_ARG;
-  const int32_t rope_max = cfg->rope_max_positions;
-  if (rope_max < 0 || (rope_max > 0 && !(cfg->rope_theta > 0.f && cfg->rope_theta < HUGE_VALF &&
-                                         cfg->rope_scale > 0.f && cfg->rope_scale < HUGE_VALF)))
-    return FI_ERR_INVALID_ARG;
-  if (batch > cfg->max_batch) return FI_ERR_CAPACITY;
-  if (workspace_bytes < size_t(fi::plan_capacity_ints(cfg)) * 4) return FI_ERR_CAPACITY;
+namespace {
 
+// One request of the plan's request table: its query tokens, its pages and
+// its KV length.  A cascade plan lists its shared blocks first.
+struct Req {
+  int32_t qo_start, qo_len, page_start, kv_len;
+};
+
+// Checks one level's host arrays and appends its requests.
+fi_status read_level(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+                     const int32_t* last_page_len, int32_t batch, int32_t page_size, int32_t num_pages,
+                     int32_t rope_max, std::vector<Req>* out) {
+  if (batch > 0 && (!qo_indptr || !kv_indptr || !last_page_len)) return FI_ERR_INVALID_ARG;
   const int32_t* qo = qo_indptr;
   const int32_t* kvp = kv_indptr;
   if (batch > 0 && (qo[0] != 0 || kvp[0] != 0)) return FI_ERR_INVALID_ARG;
-  std::vector<int32_t> lq(batch), lkv(batch);
   for (int32_t b = 0; b < batch; ++b) {
     if (qo[b + 1] < qo[b] || kvp[b + 1] < kvp[b]) return FI_ERR_INVALID_ARG;
     const int32_t pages = kvp[b + 1] - kvp[b];
     if (pages > 0 && (last_page_len[b] < 1 || last_page_len[b] > page_size)) return FI_ERR_INVALID_ARG;
-    lq[b] = qo[b + 1] - qo[b];
     const int64_t len = pages == 0 ? 0 : int64_t(pages - 1) * page_size + last_page_len[b];
     if (len > INT32_MAX) return FI_ERR_UNSUPPORTED;
-    lkv[b] = int32_t(len);
+    const int32_t lq = qo[b + 1] - qo[b];
     // RoPE positions: keys 0 .. Lkv-1 and queries Lkv-Lq .. Lkv-1 inside the table
-    if (rope_max > 0 && (len > rope_max || lq[b] > len)) return FI_ERR_INVALID_ARG;
+    if (rope_max > 0 && (len > rope_max || lq > len)) return FI_ERR_INVALID_ARG;
+    out->push_back(Req{qo[b], lq, kvp[b], int32_t(len)});
   }
   if (num_pages > 0 && batch > 0) {
     if (!kv_indices && kvp[batch] > 0) return FI_ERR_INVALID_ARG;
     for (int32_t i = 0; i < kvp[batch]; ++i)
       if (kv_indices[i] < 0 || kv_indices[i] >= num_pages) return FI_ERR_INVALID_ARG;
   }
+  return FI_OK;
+}
+
+fi_status check_config(const fi_plan_config* cfg, int32_t head_dim, int32_t num_qo_heads, int32_t num_kv_heads,
+                       int32_t page_size, int32_t causal) {
+  if (head_dim != 128) return FI_ERR_UNSUPPORTED;
+  if (page_size < 1 || page_size > 128 || (page_size & (page_size - 1))) return FI_ERR_UNSUPPORTED;
+  if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads) return FI_ERR_UNSUPPORTED;
+  if (num_qo_heads / num_kv_heads > 16) return FI_ERR_UNSUPPORTED;
+  if ((causal != 0 && causal != 1) || cfg->num_ctas < 1 || cfg->split_factor < 1) return FI_ERR_INVALID_ARG;
+  if (cfg->decode_min_chunk < 1 || cfg->prefill_min_chunk < 1) return FI_ERR_INVALID_ARG;
+  const float cap = cfg->logits_soft_cap;
+  if (cfg->window_left < -1 || cfg->sink_tokens < 0 || !(cap >= 0.f) || cap == HUGE_VALF) return FI_ERR_INVALID_ARG;
+  const int32_t rope_max = cfg->rope_max_positions;
+  if (rope_max < 0 || (rope_max > 0 && !(cfg->rope_theta > 0.f && cfg->rope_theta < HUGE_VALF &&
+                                         cfg->rope_scale > 0.f && cfg->rope_scale < HUGE_VALF)))
+    return FI_ERR_INVALID_ARG;
+  return FI_OK;
+}
+
+// The plan rule over a request table.  Requests b < num_shared are the
+// shared blocks of a cascade plan: all their keys are visible, every unit of
+// the plan writes fp32 partial states, and the cascade merge entries say
+// which partial rows make up each output row.
+fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs, int32_t num_shared,
+                        int32_t shared_page_size, const std::vector<int32_t>& block_of, int32_t total_qo,
+                        int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                        int32_t causal, void* workspace_host, fi_plan_info* info_out) {
+  const int32_t batch = int32_t(reqs.size());
+  const int32_t group = num_qo_heads / num_kv_heads;
+  const bool cascade = num_shared > 0;
+  const int32_t window = cfg->window_left, sink = cfg->sink_tokens;
+  const float cap = cfg->logits_soft_cap;
+  const int32_t rope_max = cfg->rope_max_positions;
+  // Chunk boundaries fall on pages of every cache the plan reads.
+  const int32_t max_page = std::max(page_size, cascade ? shared_page_size : page_size);
 
   // Units, in (b, hk, q-tile) order, and per-class visible-KV totals.
   std::vector<Unit> units;
+  std::vector<int32_t> first_unit(batch, -1);  // index of unit (b, 0, 0)
   int64_t total_dec = 0, total_pre = 0;
   for (int32_t b = 0; b < batch; ++b) {
-    const int64_t rows = int64_t(lq[b]) * group;
+    const Req& rq = reqs[b];
+    const int64_t rows = int64_t(rq.qo_len) * group;
     if (rows == 0) continue;
+    first_unit[b] = int32_t(units.size());
+    const bool causal_b = causal && b >= num_shared;  // a shared block's keys precede all its queries
     const int32_t tile = rows <= FI_TILE_DECODE ? FI_TILE_DECODE : FI_TILE_PREFILL;
     const int32_t tiles = int32_t(ceil_div(rows, tile));
     for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
@@ -151,16 +179,16 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
         u.tile = tile;
         u.row0 = qt * tile;
         u.row1 = int32_t(std::min<int64_t>(rows, int64_t(qt + 1) * tile));
-        const int64_t q_first = int64_t(lkv[b]) - lq[b] + u.row0 / group;
-        const int64_t q_last = int64_t(lkv[b]) - lq[b] + (u.row1 - 1) / group;
-        int64_t hi = causal ? std::min<int64_t>(lkv[b], q_last + 1) : int64_t(lkv[b]);
+        const int64_t q_first = int64_t(rq.kv_len) - rq.qo_len + u.row0 / group;
+        const int64_t q_last = int64_t(rq.kv_len) - rq.qo_len + (u.row1 - 1) / group;
+        int64_t hi = causal_b ? std::min<int64_t>(rq.kv_len, q_last + 1) : int64_t(rq.kv_len);
         if (hi < 0) hi = 0;
         u.n_ranges = 1;
         u.r_begin[0] = 0;
         u.r_end[0] = hi;
         if (window >= 0) {
-          const int64_t gran = tile == FI_TILE_DECODE ? std::max(page_size, FI_GRANULE_DECODE)
-                                                      : std::max(page_size, FI_GRANULE_PREFILL);
+          const int64_t gran = tile == FI_TILE_DECODE ? std::max(max_page, FI_GRANULE_DECODE)
+                                                      : std::max(max_page, FI_GRANULE_PREFILL);
           const int64_t lo = std::max<int64_t>(0, q_first - window) / gran * gran;
           const int64_t sink_end = std::min<int64_t>(sink, hi);
           if (lo > sink_end) {
@@ -188,18 +216,24 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
     int64_t c = std::max<int64_t>(min_chunk, ceil_div(total, slots));
     return ceil_div(c, granule) * granule;
   };
-  const int64_t chunk_dec = pick_chunk(total_dec, cfg->decode_min_chunk, std::max(page_size, FI_GRANULE_DECODE));
-  const int64_t chunk_pre = pick_chunk(total_pre, cfg->prefill_min_chunk, std::max(page_size, FI_GRANULE_PREFILL));
+  const int64_t chunk_dec = pick_chunk(total_dec, cfg->decode_min_chunk, std::max(max_page, FI_GRANULE_DECODE));
+  const int64_t chunk_pre = pick_chunk(total_pre, cfg->prefill_min_chunk, std::max(max_page, FI_GRANULE_PREFILL));
 
-  // Chunks of every unit; split units become merge units in unit order.
+  // Chunks of every unit; split units become merge units in unit order.  In
+  // a cascade plan every unit writes partial states and none is merged in
+  // the run: the cascade merge combines them across the two levels.
   std::vector<Chunk> chunks;
   chunks.reserve(units.size() * 2);
   std::vector<int32_t> merge_rows;  // FI_MERGE_INTS per merge unit
+  std::vector<int64_t> unit_base(units.size(), -1), unit_n(units.size(), 0);
   int64_t partial_rows = 0;
   int32_t n_late = 0;  // merge units of prefill-class tiles, merged after the run
-  for (const Unit& u : units) {
+  int32_t prefill_caches = 0;
+  for (size_t ui = 0; ui < units.size(); ++ui) {
+    const Unit& u = units[ui];
     const int64_t chunk = u.tile == FI_TILE_DECODE ? chunk_dec : chunk_pre;
     const int64_t weight = u.tile == FI_TILE_DECODE ? cfg->decode_cost_weight : cfg->prefill_cost_weight;
+    if (u.tile == FI_TILE_PREFILL) prefill_caches |= u.b < num_shared ? 2 : 1;
     int64_t n = 0;
     for (int r = 0; r < u.n_ranges; ++r) n += ceil_div(u.r_end[r] - u.r_begin[r], chunk);
     const bool empty = n == 0;
@@ -207,15 +241,19 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
     int32_t merge_id = -1;
     int64_t base = -1;
     const int32_t nrows = u.row1 - u.row0;
-    if (n > 1) {
-      merge_id = int32_t(merge_rows.size() / FI_MERGE_INTS);
+    if (n > 1 || cascade) {
       base = partial_rows;
       partial_rows += n * nrows;
+    }
+    if (n > 1 && !cascade) {
+      merge_id = int32_t(merge_rows.size() / FI_MERGE_INTS);
       const int32_t late = u.tile == FI_TILE_DECODE ? 0 : 1;
       const int32_t m[FI_MERGE_INTS] = {u.b, u.hk, u.row0, u.row1, int32_t(n), int32_t(base), late, 0};
       merge_rows.insert(merge_rows.end(), m, m + FI_MERGE_INTS);
       n_late += late;
     }
+    unit_base[ui] = base;
+    unit_n[ui] = n;
     // chunk i of the unit: ranges in KV order, chunk numbers running across them
     int64_t i = 0;
     auto emit = [&](int64_t k0, int64_t k1) {
@@ -228,7 +266,7 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
       c.idx = int32_t(i);
       const int32_t f[FI_ITEM_INTS] = {u.b,         u.hk,       u.row0,
                                        u.row1,      int32_t(k0), int32_t(k1),
-                                       n > 1 ? int32_t(base + i * nrows) : -1, merge_id};
+                                       base >= 0 ? int32_t(base + i * nrows) : -1, merge_id};
       std::memcpy(c.fields, f, sizeof f);
       chunks.push_back(c);
       ++i;
@@ -240,9 +278,42 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
         for (int64_t k0 = u.r_begin[r]; k0 < u.r_end[r]; k0 += chunk) emit(k0, std::min(u.r_end[r], k0 + chunk));
     }
   }
+  // Cascade merge entries, in ordinary-unit order: the rows of each unit in
+  // runs of at most FI_CASCADE_ROWS from the unit's first row, also cut
+  // where they cross from one shared unit (q-tile of their block) into the
+  // next.
+  std::vector<int32_t> cascade_rows;  // FI_CASCADE_INTS per entry
+  if (cascade) {
+    for (size_t ui = 0; ui < units.size(); ++ui) {
+      const Unit& u = units[ui];
+      if (u.b < num_shared) continue;
+      const int32_t s = block_of[u.b];
+      const Req& blk = reqs[s];
+      const int64_t srows = int64_t(blk.qo_len) * group;
+      const int32_t stile = srows <= FI_TILE_DECODE ? FI_TILE_DECODE : FI_TILE_PREFILL;
+      const int32_t stiles = int32_t(ceil_div(srows, stile));
+      const int64_t shift = int64_t(reqs[u.b].qo_start - blk.qo_start) * group;  // row r -> block row r + shift
+      for (int32_t ra = u.row0; ra < u.row1;) {
+        const int64_t rs = ra + shift;
+        const int32_t qt0 = int32_t(rs / stile);
+        const size_t si = size_t(first_unit[s]) + size_t(u.hk) * stiles + qt0;
+        const Unit& su = units[si];
+        const int32_t run_end = u.row0 + ((ra - u.row0) / FI_CASCADE_ROWS + 1) * FI_CASCADE_ROWS;
+        const int32_t rb = int32_t(std::min<int64_t>(std::min(u.row1, run_end), ra + (su.row1 - rs)));
+        const int32_t e[FI_CASCADE_INTS] = {u.b, u.hk, ra, rb,
+                                            int32_t(unit_n[si]), int32_t(unit_base[si] + (rs - su.row0)),
+                                            su.row1 - su.row0, int32_t(unit_n[ui]),
+                                            int32_t(unit_base[ui] + (ra - u.row0)), u.row1 - u.row0, 0, 0};
+        cascade_rows.insert(cascade_rows.end(), e, e + FI_CASCADE_INTS);
+        ra = rb;
+      }
+    }
+  }
   const int64_t n_items = int64_t(chunks.size());
   const int64_t n_merge = int64_t(merge_rows.size() / FI_MERGE_INTS);
-  if (n_items > cfg->max_items || n_merge > cfg->max_merge_units || partial_rows > cfg->max_partial_rows)
+  const int64_t n_cascade = int64_t(cascade_rows.size() / FI_CASCADE_INTS);
+  if (n_items > cfg->max_items || n_merge > cfg->max_merge_units || n_cascade > cfg->max_merge_units ||
+      partial_rows > cfg->max_partial_rows || partial_rows > INT32_MAX)
     return FI_ERR_CAPACITY;
 
   // Longest processing time first onto the least-loaded CTA (ties: lower CTA).
@@ -266,7 +337,8 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   const int64_t off_merge = off_items + FI_ITEM_INTS * n_items;
   const int64_t off_cnt = off_merge + FI_MERGE_INTS * n_merge;
   const int64_t off_req = off_cnt + round4(n_merge);
-  const int64_t total_ints = off_req + int64_t(FI_REQ_INTS) * batch;
+  const int64_t off_cascade = off_req + int64_t(FI_REQ_INTS) * batch;
+  const int64_t total_ints = off_cascade + int64_t(FI_CASCADE_INTS) * n_cascade;
   if (total_ints > fi::plan_capacity_ints(cfg)) return FI_ERR_CAPACITY;
 
   int32_t* ws = static_cast<int32_t*>(workspace_host);
@@ -291,11 +363,12 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   if (n_merge) std::memcpy(ws + off_merge, merge_rows.data(), merge_rows.size() * 4);
   for (int32_t b = 0; b < batch; ++b) {
     int32_t* r = ws + off_req + int64_t(FI_REQ_INTS) * b;
-    r[0] = qo[b];
-    r[1] = lq[b];
-    r[2] = kvp[b];
-    r[3] = lkv[b];
+    r[0] = reqs[b].qo_start;
+    r[1] = reqs[b].qo_len;
+    r[2] = reqs[b].page_start;
+    r[3] = reqs[b].kv_len;
   }
+  if (n_cascade) std::memcpy(ws + off_cascade, cascade_rows.data(), cascade_rows.size() * 4);
   int32_t cap_bits, theta_bits = 0, scale_bits = 0;
   std::memcpy(&cap_bits, &cap, 4);
   if (rope_max > 0) {
@@ -303,13 +376,15 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
     std::memcpy(&scale_bits, &cfg->rope_scale, 4);
   }
   const int32_t rope_off = rope_max > 0 ? int32_t(fi_rope_table_offset(fi::plan_capacity_ints(cfg)) / 4) : 0;
-  const int32_t header[FI_HEADER_INTS] = {FI_PLAN_MAGIC,      int32_t(n_items),   int32_t(n_merge), C,
-                                          batch,              causal,             int32_t(off_cta), int32_t(off_items),
-                                          int32_t(off_merge), int32_t(off_cnt),   int32_t(off_req), 0,
-                                          num_qo_heads,       num_kv_heads,       page_size,        int32_t(total_ints),
-                                          window,             sink,               cap_bits,         rope_max,
-                                          theta_bits,         scale_bits,         rope_off,         n_late,
-                                          int32_t(partial_rows), batch > 0 ? qo[batch] : 0, 0, 0};
+  const int32_t header[FI_HEADER_INTS] = {
+      FI_PLAN_MAGIC,        int32_t(n_items),   int32_t(n_merge),   C,
+      batch,                causal,             int32_t(off_cta),   int32_t(off_items),
+      int32_t(off_merge),   int32_t(off_cnt),   int32_t(off_req),   0,
+      num_qo_heads,         num_kv_heads,       page_size,          int32_t(total_ints),
+      window,               sink,               cap_bits,           rope_max,
+      theta_bits,           scale_bits,         rope_off,           n_late,
+      int32_t(partial_rows), total_qo,          num_shared,         cascade ? int32_t(off_cascade) : 0,
+      int32_t(n_cascade),   cascade ? shared_page_size : 0, 0,      0};
   std::memcpy(ws, header, sizeof header);
 
   fi_plan_info info;
@@ -332,8 +407,74 @@ extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_i
   info.int_ws_bytes_used = total_ints * 4;
   info.max_partial_rows = cfg->max_partial_rows;
   info.variant = (cap > 0.f ? 1 : 0) | (window >= 0 ? 2 : 0) | (rope_max > 0 ? 4 : 0);
+  info.num_shared = num_shared;
+  info.num_cascade_merges = int32_t(n_cascade);
+  info.prefill_caches = prefill_caches;
   *info_out = info;
   return FI_OK;
+}
+
+}  // namespace
+
+extern "C" fi_status fi_plan_host(const fi_plan_config* cfg, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                  const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch,
+                                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t page_size, int32_t causal, int32_t num_pages, void* workspace_host,
+                                  size_t workspace_bytes, fi_plan_info* info_out) {
+  if (!cfg || !info_out || !workspace_host || batch < 0) return FI_ERR_INVALID_ARG;
+  fi_status st = check_config(cfg, head_dim, num_qo_heads, num_kv_heads, page_size, causal);
+  if (st != FI_OK) return st;
+  if (batch > cfg->max_batch) return FI_ERR_CAPACITY;
+  if (workspace_bytes < size_t(fi::plan_capacity_ints(cfg)) * 4) return FI_ERR_CAPACITY;
+  std::vector<Req> reqs;
+  reqs.reserve(batch);
+  st = read_level(qo_indptr, kv_indptr, kv_indices, last_page_len, batch, page_size, num_pages,
+                  cfg->rope_max_positions, &reqs);
+  if (st != FI_OK) return st;
+  return plan_requests(cfg, reqs, 0, page_size, {}, batch > 0 ? qo_indptr[batch] : 0, num_qo_heads, num_kv_heads,
+                       head_dim, page_size, causal, workspace_host, info_out);
+}
+
+extern "C" fi_status fi_plan_cascade_host(
+    const fi_plan_config* cfg, const int32_t* shared_qo_indptr, const int32_t* shared_kv_indptr,
+    const int32_t* shared_kv_indices, const int32_t* shared_last_page_len, int32_t num_shared,
+    int32_t shared_page_size, int32_t shared_num_pages, const int32_t* qo_indptr, const int32_t* kv_indptr,
+    const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t page_size, int32_t causal, int32_t num_pages,
+    void* workspace_host, size_t workspace_bytes, fi_plan_info* info_out) {
+  if (!cfg || !info_out || !workspace_host || batch < 0 || num_shared < 1) return FI_ERR_INVALID_ARG;
+  fi_status st = check_config(cfg, head_dim, num_qo_heads, num_kv_heads, page_size, causal);
+  if (st != FI_OK) return st;
+  if (shared_page_size < 1 || shared_page_size > 128 || (shared_page_size & (shared_page_size - 1)))
+    return FI_ERR_UNSUPPORTED;
+  // Positions of the two levels are not tied to one sequence here: the
+  // position-dependent variants (sliding window, sink, RoPE) are not offered.
+  if (cfg->window_left >= 0 || cfg->rope_max_positions > 0) return FI_ERR_UNSUPPORTED;
+  if (int64_t(batch) + num_shared > cfg->max_batch) return FI_ERR_CAPACITY;
+  if (workspace_bytes < size_t(fi::plan_capacity_ints(cfg)) * 4) return FI_ERR_CAPACITY;
+  std::vector<Req> reqs;
+  reqs.reserve(size_t(num_shared) + batch);
+  st = read_level(shared_qo_indptr, shared_kv_indptr, shared_kv_indices, shared_last_page_len, num_shared,
+                  shared_page_size, shared_num_pages, 0, &reqs);
+  if (st != FI_OK) return st;
+  st = read_level(qo_indptr, kv_indptr, kv_indices, last_page_len, batch, page_size, num_pages, 0, &reqs);
+  if (st != FI_OK) return st;
+  // The blocks cover the query rows exactly and no request straddles two of
+  // them; a causal request's queries are among its own keys.
+  const int32_t total_qo = batch > 0 ? qo_indptr[batch] : 0;
+  if (shared_qo_indptr[num_shared] != total_qo) return FI_ERR_INVALID_ARG;
+  std::vector<int32_t> block_of(size_t(num_shared) + batch, -1);
+  int32_t s = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const Req& rq = reqs[size_t(num_shared) + b];
+    if (causal && rq.kv_len < rq.qo_len) return FI_ERR_INVALID_ARG;
+    if (rq.qo_len == 0) continue;  // no rows, no units
+    while (s < num_shared && shared_qo_indptr[s + 1] <= rq.qo_start) ++s;
+    if (s == num_shared || rq.qo_start + rq.qo_len > shared_qo_indptr[s + 1]) return FI_ERR_INVALID_ARG;
+    block_of[size_t(num_shared) + b] = s;
+  }
+  return plan_requests(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_heads, num_kv_heads,
+                       head_dim, page_size, causal, workspace_host, info_out);
 }
 
 extern "C" fi_status fi_plan(const fi_plan_config* cfg, const int32_t* qo_indptr, const int32_t* kv_indptr,
@@ -345,6 +486,26 @@ extern "C" fi_status fi_plan(const fi_plan_config* cfg, const int32_t* qo_indptr
   fi_status st = fi_plan_host(cfg, qo_indptr, kv_indptr, kv_indices, last_page_len, batch, num_qo_heads,
                               num_kv_heads, head_dim, page_size, causal, num_pages, pinned_staging_host,
                               staging_bytes, info_out);
+  if (st != FI_OK) return st;
+  cudaError_t e = cudaMemcpyAsync(int_workspace_dev, pinned_staging_host, size_t(info_out->int_ws_bytes_used),
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
+extern "C" fi_status fi_plan_cascade(
+    const fi_plan_config* cfg, const int32_t* shared_qo_indptr, const int32_t* shared_kv_indptr,
+    const int32_t* shared_kv_indices, const int32_t* shared_last_page_len, int32_t num_shared,
+    int32_t shared_page_size, int32_t shared_num_pages, const int32_t* qo_indptr, const int32_t* kv_indptr,
+    const int32_t* kv_indices, const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t page_size, int32_t causal, int32_t num_pages,
+    void* int_workspace_dev, void* pinned_staging_host, size_t staging_bytes, void* stream,
+    fi_plan_info* info_out) {
+  if (!int_workspace_dev || !pinned_staging_host) return FI_ERR_INVALID_ARG;
+  fi_status st = fi_plan_cascade_host(cfg, shared_qo_indptr, shared_kv_indptr, shared_kv_indices,
+                                      shared_last_page_len, num_shared, shared_page_size, shared_num_pages,
+                                      qo_indptr, kv_indptr, kv_indices, last_page_len, batch, num_qo_heads,
+                                      num_kv_heads, head_dim, page_size, causal, num_pages, pinned_staging_host,
+                                      staging_bytes, info_out);
   if (st != FI_OK) return st;
   cudaError_t e = cudaMemcpyAsync(int_workspace_dev, pinned_staging_host, size_t(info_out->int_ws_bytes_used),
                                   cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));

@@ -1,10 +1,11 @@
 // plan_layout.h -- layout of the int workspace written by the planner and
 // read by the persistent kernel.  All fields are int32.
 //
-//   header[28]   FI_H_* below (the variant of the plan's config included:
+//   header[32]   FI_H_* below (the variant of the plan's config included:
 //                  window_left, sink_tokens, soft-cap as float bits, RoPE;
 //                  the partial rows and query tokens the plan uses, which the
-//                  kernel compares with the buffers it was launched with)
+//                  kernel compares with the buffers it was launched with;
+//                  the cascade fields, 0 in a one-level plan)
 //   cta_indptr   num_ctas + 1 entries: CTA c runs items [cta_indptr[c], cta_indptr[c+1])
 //   items        FI_ITEM_INTS each: {b, hk, row0, row1, kv0, kv1, part, merge}
 //                  rows are packed rows of request b (row = token * G + g),
@@ -21,6 +22,17 @@
 //                  is not followed by the late merge, as when a graph was captured
 //                  from a plan without late units, it merges them itself)
 //   requests     FI_REQ_INTS each: {qo_start, qo_len, page_start, kv_len}
+//                  (a cascade plan numbers its shared blocks first: requests
+//                  b < num_shared read the shared KV cache and see every one
+//                  of their keys; the others read the ordinary cache)
+//   cascade      FI_CASCADE_INTS each (cascade plans only):
+//                  {b, hk, row0, row1, n0, base0, stride0, n1, base1, stride1, 0, 0}:
+//                  packed rows [row0, row1) (at most FI_CASCADE_ROWS of them)
+//                  of ordinary request b; row r takes
+//                  the partial rows base0 + c * stride0 + (r - row0), c < n0
+//                  (its shared block's chunks) and base1 + c * stride1 +
+//                  (r - row0), c < n1 (its own chunks), merged in that order
+//                  by the cascade merge launched after the run
 //   ...          (the rest of the plan capacity)
 //   rope table   with RoPE: float2 (cos, sin) [rope_max_positions][64] at
 //                  fi_rope_table_offset(capacity) bytes, filled by
@@ -34,10 +46,12 @@
 #include <stdint.h>
 
 #define FI_PLAN_MAGIC 0x46495031
-#define FI_HEADER_INTS 28
+#define FI_HEADER_INTS 32
 #define FI_ITEM_INTS 8
 #define FI_MERGE_INTS 8
 #define FI_REQ_INTS 4
+#define FI_CASCADE_INTS 12
+#define FI_CASCADE_ROWS 16  // packed rows per cascade merge entry, at most
 #define FI_MERGE_LATE 6  // index of the late flag in a merge unit
 
 #define FI_TILE_DECODE 16
@@ -72,7 +86,11 @@ enum {
   FI_H_ROPE_TABLE_OFF = 22,   // ints from the workspace start to the cos/sin table
   FI_H_NUM_LATE_MERGE = 23,   // merge units flagged late
   FI_H_PARTIAL_ROWS = 24,     // fp32 partial-state rows the items write (0: no split unit)
-  FI_H_TOTAL_QO = 25          // query tokens of the batch (qo_indptr[batch]); 26, 27 stay 0
+  FI_H_TOTAL_QO = 25,         // query tokens of the batch (qo_indptr[batch])
+  FI_H_NUM_SHARED = 26,       // cascade: shared blocks (requests 0 .. num_shared - 1); 0 otherwise
+  FI_H_OFF_CASCADE = 27,      // cascade: offset of the cascade merge entries
+  FI_H_NUM_CASCADE = 28,      // cascade: merge entries
+  FI_H_SHARED_PAGE_SIZE = 29  // cascade: page size of the shared KV cache; 30, 31 stay 0
 };
 
 #define FI_ROPE_PAIRS 64  // dims i and i + 64 of head_dim 128 form a rotated pair

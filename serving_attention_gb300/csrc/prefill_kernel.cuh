@@ -63,26 +63,24 @@ enum { kProduceQK = 0, kProduceV = 1, kProduceQKV = 2 };
 
 template <int kMode>
 __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items,
-                           int32_t off_req) {
+                           int32_t off_req, int32_t num_shared) {
   constexpr bool kQK = kMode != kProduceV, kV = kMode != kProduceQK;
   const int lane = threadIdx.x & 31;
-  const int G = p.group, lp = p.log2_page, P = p.page_size;
-  const int ppt = kTileN >> lp;  // pages per KV tile
-  if (lane == 0) {
-    if (kQK) {
-      tc::prefetch_tensormap(&p.tm_q);
-      tc::prefetch_tensormap(&p.tm_k);
-    }
-    if (kV) tc::prefetch_tensormap(&p.tm_v);
+  const int G = p.group;
+  if (lane == 0 && kQK) tc::prefetch_tensormap(&p.tm_q);
+  if (lane < 1 + (num_shared > 0) && p.kv[lane].tc) {
+    if (kQK) tc::prefetch_tensormap(&p.kv[lane].tm_k);
+    if (kV) tc::prefetch_tensormap(&p.kv[lane].tm_v);
   }
   uint32_t kt = 0, pe = 0;
   int q_armed = -1, k_armed[2] = {-1, -1}, v_armed[2] = {-1, -1};  // parity of the last armed phase
   // One ring stage of K or V for the pages cur[] of the tile (one 4-D box per
   // page and 64-dim half).
   auto load_stage = [&](const CUtensorMap* map, uint64_t* full, uint16_t (*buf)[kTileN][64], int st, int hk,
-                        const int32_t (&cur)[4]) {
+                        const int32_t (&cur)[4], int P) {
     if (lane == 0) mbar_arrive_expect_tx(&full[st], kKVBytes);
     __syncwarp();
+    const int ppt = kTileN / P;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int e = lane + 32 * u;
@@ -97,8 +95,11 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
     const Request rq = load_request(p.iws, off_req, it.b);
     const int ntiles = item_kv_tiles(it);
     if (ntiles == 0) continue;
+    const KvCache& kc = cache_of(p, it.b, num_shared);
+    const int lp = kc.log2_page, P = kc.page_size;
+    const int ppt = kTileN >> lp;  // pages per KV tile
     const int npages = (rq.kv_len + P - 1) >> lp;
-    const int32_t* pages = p.kv_indices + rq.page_start;
+    const int32_t* pages = kc.kv_indices + rq.page_start;
     if (kQK) {
       const int nm = item_m_tiles(it);
       if (warp_wait(&sm.q_empty, (pe & 1) ^ 1, &sm.abort) && lane == 0) {
@@ -117,7 +118,7 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int e = lane + 32 * u, pg = pg0 + e;
-        pid[u] = (e < ppt && pg < npages) ? __ldg(pages + pg) : p.num_pages;  // out of bounds -> zeros
+        pid[u] = (e < ppt && pg < npages) ? __ldg(pages + pg) : kc.num_pages;  // out of bounds -> zeros
       }
     };
     fetch_ids(0);
@@ -129,11 +130,11 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
       for (int u = 0; u < 4; ++u) cur[u] = pid[u];
       if (j + 1 < ntiles) fetch_ids(j + 1);
       if (kQK && warp_wait(&sm.k_empty[st], ph ^ 1, &sm.abort)) {
-        load_stage(&p.tm_k, sm.k_full, sm.pf.k[st], st, it.hk, cur);
+        load_stage(&kc.tm_k, sm.k_full, sm.pf.k[st], st, it.hk, cur, P);
         k_armed[st] = ph;
       }
       if (kV && warp_wait(&sm.v_empty[st], ph ^ 1, &sm.abort)) {
-        load_stage(&p.tm_v, sm.v_full, sm.pf.v[st], st, it.hk, cur);
+        load_stage(&kc.tm_v, sm.v_full, sm.pf.v[st], st, it.hk, cur, P);
         v_armed[st] = ph;
       }
     }
@@ -333,7 +334,8 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
 
 template <typename T, bool kCap, bool kMask>
 __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items,
-                           int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, const Variant var) {
+                           int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, int32_t num_shared,
+                           const Variant var) {
   const int sw = (threadIdx.x >> 5) - kSoftmaxWarp0;  // 0..7
   const int mt = sw >> 2;                              // this warpgroup's M tile: 0 = A, 1 = B
   const int w = sw & 3;                                // == warp % 4: TMEM lanes 32w..32w+31
@@ -356,7 +358,8 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
       int lim = -1, lo = 0;  // visible KV tokens of this row: [lo, lim] and the sink (lim -1: padding row)
       if (prow < nrows) {
         const int t = (item.row0 + prow) / G;
-        lim = min(causal ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1, item.kv1 - 1);
+        const bool causal_i = causal && item.b >= num_shared;  // a shared block's keys are all visible
+        lim = min(causal_i ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1, item.kv1 - 1);
         if (kMask) lo = window_low(var, rq.kv_len - rq.qo_len + t);
       }
       // lrun: sum of the fp32 P (the exact normaliser, for LSE); lrun_r: sum

@@ -310,3 +310,21 @@ def test_select_matches_all():
     heads = np.tile([0, 7], b.total_qo)
     os_, ls = oracle.attention_select(p, rows, heads)
     assert np.array_equal(os_, o[rows, heads]) and np.array_equal(ls, lse[rows, heads])
+
+
+@pytest.mark.parametrize("seed,causal,page,spage,group", [(61, 0, 1, 16, 4), (62, 1, 4, 8, 2), (63, 1, 16, 1, 1),
+                                                         (64, 0, 2, 4, 8)])
+def test_two_level_attention_is_attention_over_the_concatenation(seed, causal, page, spage, group):
+    """The two-level (cascade) reading: each row's shared-block keys, all
+    visible, merged by LSE with its own keys under the bottom-right causal
+    mask, equals attention over block ++ own keys under the bottom-right
+    causal mask (own keys >= queries), to 1e-10."""
+    d = workloads.cascade_batch(seed, [3, 1, 2], 4, 30, 40, 2 * group, 2, page, spage, causal, kv_min=0)
+    so, sl = oracle.attention(oracle_problem(d["shared"]))
+    oo, ol = oracle.attention(oracle_problem(d["own"]))
+    fo, fl = oracle.attention(oracle_problem(d["flat"]))
+    mo, ml = oracle.merge_states(so, sl, oo, ol)
+    np.testing.assert_allclose(mo, fo, rtol=0, atol=1e-10)
+    fin = np.isfinite(fl)
+    assert np.array_equal(np.isfinite(ml), fin)
+    np.testing.assert_allclose(ml[fin], fl[fin], rtol=0, atol=1e-10)

@@ -10,7 +10,7 @@ import serving_attention_gb300 as fi
 import workloads
 from oracle import plan_ref
 
-HEADER = 24
+HEADER = 32
 
 
 def _cfg(num_ctas=148, **kw):
@@ -331,3 +331,159 @@ def test_default_capacity_holds_every_workload():
         qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
         st, ws, info = fi.plan_host(cfg, qop, kvp, np.zeros(int(kvp[-1]), np.int32), lpl, 32, 8, 128, 16, causal)
         assert st == 0, st
+
+
+# ---------------------------------------------------------------- two-level (cascade) plans
+
+
+def _cascade_both(cfg, cfgd, shared, own, hq, hkv, causal, num_pages=0, shared_num_pages=0):
+    """shared / own: (qo_indptr, kv_indptr, kv_indices, last_page_len, page_size)."""
+    sqo, skvp, skvi, slpl, sp = shared
+    qo, kvp, kvi, lpl, p = own
+    st_c, ws_c, info_c = fi.plan_cascade_host(cfg, sqo, skvp, skvi, slpl, sp, qo, kvp, kvi, lpl, hq, hkv, 128, p,
+                                              causal, num_pages, shared_num_pages)
+    st_p, ws_p, info_p = plan_ref.make_cascade_plan(cfgd, sqo, skvp, skvi, slpl, sp, shared_num_pages, qo, kvp, kvi,
+                                                    lpl, hq, hkv, 128, p, causal, num_pages)
+    assert st_c == st_p, (st_c, st_p)
+    if st_c == 0:
+        assert np.array_equal(ws_c, ws_p), np.nonzero(ws_c != ws_p)[0][:10]
+        got = info_c.as_dict()
+        for k, v in info_p.items():
+            assert got[k] == v, (k, got[k], v)
+    return st_c, ws_c, info_c
+
+
+def _random_cascade(rng):
+    nblk = int(rng.integers(1, 5))
+    sizes = rng.integers(1, 6, size=nblk)
+    B = int(sizes.sum())
+    qo = rng.choice([0, 1, 1, 2, 3, 9, 40, 70], size=B)
+    causal = int(rng.integers(0, 2))
+    kv = rng.integers(0, 2500, size=B)
+    if causal:
+        kv = np.maximum(kv, qo)
+    page, spage = int(rng.choice([1, 2, 16])), int(rng.choice([1, 8, 16, 64]))
+    skv = rng.integers(0, 9000, size=nblk)
+    skv[rng.random(nblk) < 0.2] = 0
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    first = np.concatenate([[0], np.cumsum(sizes)])
+    sqo = qop[first].astype(np.int32)
+    kvp, lpl = workloads._pages_for(kv, page)
+    skvp, slpl = workloads._pages_for(skv, spage)
+    kvi = rng.permutation(int(kvp[-1]) + 3)[:int(kvp[-1])].astype(np.int32)
+    skvi = rng.permutation(int(skvp[-1]) + 3)[:int(skvp[-1])].astype(np.int32)
+    return (sqo, skvp, skvi, slpl, spage), (qop, kvp, kvi, lpl, page), causal, kv, skv
+
+
+def _check_cascade_invariants(ws, shared, own, kv, skv, hq, hkv, causal):
+    """Every unit writes partial states and none merges in the run; every row
+    of every request is in exactly one merge entry of at most 16 rows, whose
+    two part lists are exactly the partial rows its block's chunks and its
+    own chunks wrote for that row; those chunks tile the visible keys."""
+    G = hq // hkv
+    S = len(shared[0]) - 1
+    n_items, n_merge, C = ws[1], ws[2], ws[3]
+    assert n_merge == 0 and ws[26] == S
+    off_items, off_req, off_cas, n_cas = ws[7], ws[10], ws[27], ws[28]
+    items = ws[off_items:off_items + 8 * n_items].reshape(-1, 8)
+    reqs = ws[off_req:off_req + 4 * ws[4]].reshape(-1, 4)
+    ents = ws[off_cas:off_cas + 12 * n_cas].reshape(-1, 12)
+    assert np.all(items[:, 6] >= 0) and np.all(items[:, 7] == -1)
+    parts = {}  # (b, hk, row) -> [(kv0, kv1, partial row)]
+    for b, hk, r0, r1, k0, k1, part, _ in items:
+        for r in range(r0, r1):
+            parts.setdefault((b, hk, r), []).append((k0, k1, part + r - r0))
+    qo = np.diff(own[0])
+    seen = set()
+    for b, hk, r0, r1, n0, b0, s0, n1, b1, s1, z0, z1 in ents:
+        assert 0 < r1 - r0 <= 16 and z0 == z1 == 0 and b >= S
+        blk = int(np.searchsorted(shared[0], reqs[b][0], side="right") - 1)
+        for r in range(r0, r1):
+            assert (b, hk, r) not in seen
+            seen.add((b, hk, r))
+            sr = (reqs[b][0] - reqs[blk][0]) * G + r
+            mine = sorted(parts[(b, hk, r)])
+            theirs = sorted(parts[(blk, hk, sr)])
+            assert [p for _, _, p in theirs] == [b0 + c * s0 + r - r0 for c in range(n0)]
+            assert [p for _, _, p in mine] == [b1 + c * s1 + r - r0 for c in range(n1)]
+            # the chunks tile the visible keys: all of the block's, the own causal range
+            t = r // G
+            hi = min(kv[b - S], kv[b - S] - qo[b - S] + t + 1) if causal else kv[b - S]
+            for chunks, end in ((theirs, skv[blk]), (mine, hi)):
+                ks = [(k0, k1) for k0, k1, _ in chunks if k1 > k0]
+                assert sum(k1 - k0 for k0, k1 in ks) >= end
+                covered = np.zeros(max(end, 1), bool)
+                for k0, k1 in ks:
+                    covered[k0:min(k1, end)] = True
+                assert end == 0 or covered[:end].all()
+    want = {(S + r, hk, row) for r in range(len(qo)) for hk in range(hkv) for row in range(qo[r] * G)}
+    assert seen == want
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_cascade_plan_matches_reference_random(seed):
+    rng = np.random.default_rng(700 + seed)
+    shared, own, causal, kv, skv = _random_cascade(rng)
+    hkv = int(rng.choice([1, 2, 8]))
+    group = int(rng.choice([1, 4, 8]))
+    cfg, cfgd = _cfg(num_ctas=int(rng.choice([1, 9, 152])), split_factor=int(rng.integers(1, 4)),
+                     decode_min_chunk=int(rng.choice([64, 256])), prefill_min_chunk=int(rng.choice([128, 1024])))
+    st, ws, info = _cascade_both(cfg, cfgd, shared, own, hkv * group, hkv, causal,
+                                 num_pages=int(own[1][-1]) + 3, shared_num_pages=int(shared[1][-1]) + 3)
+    assert st == 0
+    assert info.num_shared == len(shared[0]) - 1 and info.num_merge_units == 0
+    _check_cascade_invariants(ws, shared, own, kv, skv, hkv * group, hkv, causal)
+
+
+def test_cascade_plan_of_the_shared_prefix_workload():
+    """The parallel-generation case: one block holding the 8192-token dense
+    prefix (pages of 16) for 64 branches of one query each, suffixes at page 1."""
+    rng = np.random.default_rng(4000)
+    suf = rng.integers(64, 513, size=64)
+    kvp, lpl = workloads._pages_for(suf, 1)
+    qop = np.arange(65, dtype=np.int32)
+    shared = (np.array([0, 64], np.int32), np.array([0, 512], np.int32), np.arange(512, dtype=np.int32),
+              np.array([16], np.int32), 16)
+    own = (qop, kvp, rng.permutation(int(kvp[-1])).astype(np.int32), lpl, 1)
+    cfg, cfgd = _cfg(num_ctas=152)
+    st, ws, info = _cascade_both(cfg, cfgd, shared, own, 32, 8, 0)
+    assert st == 0 and info.prefill_caches == 2  # the block's 256-row units read the shared cache on tensor cores
+    _check_cascade_invariants(ws, shared, own, suf, np.array([8192]), 32, 8, 0)
+
+
+@pytest.mark.parametrize("case,status", [
+    ("straddle", 1), ("cover", 1), ("causal_short", 1), ("window", 2), ("rope", 2), ("shared_page", 2),
+    ("no_blocks", 1), ("shared_index", 1), ("capacity", 3),
+])
+def test_cascade_plan_rejects(case, status):
+    qo = np.array([0, 2, 3, 5], np.int32)
+    kvp = np.array([0, 1, 2, 3], np.int32)
+    lpl = np.array([16, 5, 16], np.int32)
+    kvi = np.array([0, 1, 2], np.int32)
+    sqo = np.array([0, 3, 5], np.int32)
+    skvp = np.array([0, 2, 3], np.int32)
+    skvi = np.array([2, 0, 1], np.int32)
+    slpl = np.array([8, 8], np.int32)
+    sp, causal, kw = 8, 1, {}
+    if case == "straddle":
+        sqo = np.array([0, 1, 5], np.int32)  # request 0's rows [0, 2) cross block boundary 1
+    elif case == "cover":
+        sqo = np.array([0, 3, 4], np.int32)  # the blocks stop before the last row
+    elif case == "causal_short":
+        lpl = np.array([1, 5, 16], np.int32)  # request 0: 2 queries, 1 own key
+    elif case == "window":
+        kw = dict(window_left=64)
+    elif case == "rope":
+        kw = dict(rope_max_positions=4096)
+    elif case == "shared_page":
+        sp = 12
+    elif case == "no_blocks":
+        sqo, skvp, skvi, slpl = np.array([0], np.int32), np.array([0], np.int32), skvi[:0], slpl[:0]
+    elif case == "shared_index":
+        skvi = np.array([2, 0, 7], np.int32)
+    elif case == "capacity":
+        kw = dict(max_merge_units=1)
+    cfg, cfgd = _cfg(**kw)
+    st, ws, _ = _cascade_both(cfg, cfgd, (sqo, skvp, skvi, slpl, sp), (qo, kvp, kvi, lpl, 16), 8, 2, causal,
+                              num_pages=3, shared_num_pages=3)
+    assert st == status and ws is None

@@ -282,6 +282,62 @@ def random_batch(seed: int, batch: int, qo_max: int, kv_max: int, num_qo_heads: 
                       pool_pages=nnz + extra_pages, rng=rng, v_pad_heads=v_pad_heads)
 
 
+def cascade_batch(seed: int, block_sizes, qo_max: int, kv_max: int, shared_max: int, num_qo_heads: int,
+                  num_kv_heads: int, page_size: int, shared_page_size: int, causal: int, dtype: str = "bf16",
+                  device="cpu", qo_min: int = 1, kv_min: int = 0, shared_min: int = 0, poison: bool = True) -> dict:
+    """A two-level batch: requests grouped into consecutive blocks of
+    block_sizes[s] requests, each block with its own shared keys (a pool of
+    pages of shared_page_size, shuffled) and each request with its own keys
+    (a pool of pages of page_size, shuffled).  Returns
+      shared -- the blocks as a batch: block s owns the query rows of its
+                requests and the block's pages;
+      own    -- the requests' own batch (its q is the queries of both levels);
+      flat   -- the same attention as one page-1 batch for the oracle: request
+                r's keys are its block's keys followed by its own (gathered).
+    With causal, every request holds at least as many own keys as queries."""
+    rng = np.random.default_rng(seed)
+    block_sizes = np.asarray(block_sizes, dtype=np.int64)
+    B = int(block_sizes.sum())
+    qo = rng.integers(qo_min, qo_max + 1, size=B)
+    kv = rng.integers(kv_min, kv_max + 1, size=B)
+    if causal:
+        kv = np.maximum(kv, qo)
+    skv = rng.integers(shared_min, shared_max + 1, size=len(block_sizes))
+    own = make_batch(f"cascade{seed}.own", dtype, qo, kv, num_qo_heads, num_kv_heads, page_size, causal, seed,
+                     device, pool_pages=int(((kv + page_size - 1) // page_size).sum()) + 2, rng=rng, poison=poison)
+    first = np.concatenate([[0], np.cumsum(block_sizes)])
+    sqo = own.qo_indptr[first].astype(np.int32)
+    shared = make_batch(f"cascade{seed}.shared", dtype, np.diff(sqo), skv, num_qo_heads, num_kv_heads,
+                        shared_page_size, 0, seed + 1, device,
+                        pool_pages=int(((skv + shared_page_size - 1) // shared_page_size).sum()) + 2, rng=rng,
+                        poison=poison)
+    shared.q = own.q
+    # flat: per request, its block's tokens then its own tokens, as pages of 1
+    def tokens(b: PagedBatch, r: int):
+        n = int(b.kv_lens()[r])
+        j = np.arange(n)
+        return b.kv_indices[b.kv_indptr[r] + j // b.page_size].astype(np.int64), j % b.page_size
+    ks, vs, lens = [], [], []
+    for s_ in range(len(block_sizes)):
+        sp, ss = tokens(shared, s_)
+        for r in range(int(first[s_]), int(first[s_ + 1])):
+            op, os_ = tokens(own, r)
+            idx = lambda a: torch.as_tensor(a, device=device, dtype=torch.long)  # noqa: E731
+            ks.append(torch.cat([shared.k[idx(sp), idx(ss)], own.k[idx(op), idx(os_)]]))
+            vs.append(torch.cat([shared.v[idx(sp), idx(ss)], own.v[idx(op), idx(os_)]]))
+            lens.append(len(sp) + len(op))
+    lens = np.asarray(lens, dtype=np.int64)
+    tot = int(lens.sum())
+    fk = torch.cat(ks).reshape(tot, 1, num_kv_heads, HEAD_DIM) if tot else own.k[:0, :1]
+    fv = torch.cat(vs).reshape(tot, 1, num_kv_heads, HEAD_DIM) if tot else own.v[:0, :1]
+    find = np.zeros(B + 1, np.int32)
+    find[1:] = np.cumsum(lens)
+    flat = PagedBatch(f"cascade{seed}.flat", dtype, own.qo_indptr, find, np.arange(tot, dtype=np.int32),
+                      np.ones(B, np.int32), num_qo_heads, num_kv_heads, 1, causal, own.sm_scale, own.q, fk, fv,
+                      fk, fv)
+    return {"shared": shared, "own": own, "flat": flat}
+
+
 def to_numpy_storage(t: torch.Tensor) -> np.ndarray:
     """uint16 bit patterns (fp16/bf16) of a tensor, on the host, strides kept."""
     if t.dtype == torch.float32:
