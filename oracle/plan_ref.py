@@ -59,7 +59,7 @@ MAGIC = 0x46495031
 TILE_DECODE, TILE_PREFILL = 16, 256
 HEADER_INTS = 32
 ROPE_PAIRS = 64
-ITEM_INTS = 8
+ITEM_INTS = 16
 MERGE_INTS = 8
 REQ_INTS = 4
 CASCADE_INTS = 12
@@ -292,7 +292,8 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
         for i, (k0, k1) in enumerate(pieces or [(0, 0)]):
             cost = (k1 - k0 + ITEM_COST_TOKENS) * weight[T]
             part = base + i * nrows if base >= 0 else -1
-            items.append(((-cost, -T, b, hk, qt, i), (b, hk, r0, r1, k0, k1, part, m)))
+            # the request's table entry rides along with the item
+            items.append(((-cost, -T, b, hk, qt, i), (b, hk, r0, r1, k0, k1, part, m, *reqs[b], 0, 0, 0, 0)))
 
     # cascade merge entries, per ordinary unit: runs of at most CASCADE_ROWS
     # rows counted from the unit's first row, cut again at the block's q-tile bounds

@@ -163,18 +163,20 @@ __device__ __forceinline__ int window_low(const Variant& v, int q_pos) {
   return v.window_left >= 0 ? q_pos - v.window_left : -1;
 }
 
-struct Item {
-  int32_t b, hk, row0, row1, kv0, kv1, part, merge;
-};
-
 struct Request {
   int32_t qo_start, qo_len, page_start, kv_len;
 };
 
+// A work item with its request's table entry (the plan writes both).
+struct Item {
+  int32_t b, hk, row0, row1, kv0, kv1, part, merge;
+  Request rq;
+};
+
 __device__ __forceinline__ Item load_item(const int32_t* iws, int32_t off_items, int32_t i) {
   const int4* p = reinterpret_cast<const int4*>(iws + off_items + FI_ITEM_INTS * i);
-  int4 a = __ldg(p), c = __ldg(p + 1);
-  return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+  const int4 a = __ldg(p), c = __ldg(p + 1), r = __ldg(p + 2);
+  return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w, Request{r.x, r.y, r.z, r.w}};
 }
 
 __device__ __forceinline__ Request load_request(const int32_t* iws, int32_t off_req, int32_t b) {

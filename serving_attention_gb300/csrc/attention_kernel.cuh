@@ -59,10 +59,27 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
   int armed[kStages];
 #pragma unroll
   for (int s = 0; s < kStages; ++s) armed[s] = -1;
-  for (int32_t i = item_begin; i < item_end; ++i) {
-    const Item item = load_item(p.iws, off_items, i);
-    const Request rq = load_request(p.iws, off_req, item.b);
-    const KvCache& kc = cache_of(p, item.b, num_shared);
+  const int G = p.group;
+  // Near the end of an item (its last stage issued, the consumers at most a
+  // ring behind), the next item's query rows and first page ids are brought
+  // into L2, so that neither the consumers' query load nor this warp's page-id
+  // load at the next item start waits on HBM.
+  auto prefetch_next = [&](const Item& nx) {
+    const int t0 = nx.row0 / G, lines = ((nx.row1 - 1) / G - t0 + 1) * G * 2;
+    for (int l = lane; l < lines; l += 32) {
+      const int tt = l / (2 * G), g = (l >> 1) % G;
+      tc::prefetch_l2(p.q + (int64_t(nx.rq.qo_start) + t0 + tt) * p.q_stride_tok +
+                      int64_t(nx.hk * G + g) * p.q_stride_head + (l & 1) * 64);
+    }
+    if (lane == 0) {
+      const KvCache& kn = cache_of(p, nx.b, num_shared);
+      tc::prefetch_l2(kn.kv_indices + nx.rq.page_start + (nx.kv0 >> kn.log2_page));
+    }
+  };
+  // One item's stages from cache kc (instantiated once per cache, so the
+  // cache's fields are kernel parameters at fixed offsets).
+  auto stream_item = [&](const KvCache& kc, const Item& item, const Item* nx) {
+    const Request& rq = item.rq;
     const int lp = kc.log2_page, P = kc.page_size;
     const int boxes = P >= kStageTokens ? 1 : (kStageTokens >> lp);  // per stage and tensor
     const int box_slots = P >= kStageTokens ? kStageTokens : P;
@@ -74,13 +91,13 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
     for (int pass = 0; pass < passes; ++pass) {
       // page ids of the next stage's boxes: lane, lane + 32, ... (box loads)
       // or 4 * lane .. 4 * lane + 3 (the four rows of a lane's gather)
-      int32_t nx[kBoxLanes];
+      int32_t nxid[kBoxLanes];
       auto fetch_ids = [&](int st) {
         const int pg0 = (item.kv0 + st * kStageTokens) >> lp;
 #pragma unroll
         for (int r = 0; r < kBoxLanes; ++r) {
           const int bx = kc.gather_rows ? kBoxLanes * lane + r : lane + 32 * r;
-          nx[r] = (bx < boxes && pg0 + bx < npages) ? __ldg(pages + pg0 + bx) : kc.num_pages;
+          nxid[r] = (bx < boxes && pg0 + bx < npages) ? __ldg(pages + pg0 + bx) : kc.num_pages;
         }
       };
       if (nst > 0) fetch_ids(0);
@@ -89,7 +106,7 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
         const uint32_t ph = (it / kStages) & 1;
         int32_t id[kBoxLanes];
 #pragma unroll
-        for (int r = 0; r < kBoxLanes; ++r) id[r] = nx[r];
+        for (int r = 0; r < kBoxLanes; ++r) id[r] = nxid[r];
         if (st + 1 < nst) fetch_ids(st + 1);
         if (!warp_wait(&sm.empty[s], ph ^ 1, &sm.abort)) continue;
         if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
@@ -117,8 +134,19 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
           }
         }
         armed[s] = ph;
+        if (nx && st + 1 == nst && pass + 1 == passes) prefetch_next(*nx);
       }
     }
+  };
+  Item next = item_begin < item_end ? load_item(p.iws, off_items, item_begin) : Item{};
+  for (int32_t i = item_begin; i < item_end; ++i) {
+    const Item item = next;
+    const bool more = i + 1 < item_end;
+    if (more) next = load_item(p.iws, off_items, i + 1);
+    if (item.b < num_shared)
+      stream_item(p.kv[1], item, more ? &next : nullptr);
+    else
+      stream_item(p.kv[0], item, more ? &next : nullptr);
   }
   // Every load this warp armed has landed before the CTA moves on.
   if (lane == 0) {
@@ -373,9 +401,11 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
   const int G = p.group;
   uint32_t it = 0;
 
+  // The next item is loaded while the current one's partial states are
+  // combined (its load is then off the path from one item to the next).
   for (int32_t i = item_begin; i < item_end; ++i) {
     const Item item = load_item(p.iws, off_items, i);
-    const Request rq = load_request(p.iws, off_req, item.b);
+    const Request& rq = item.rq;
     const int nrows = item.row1 - item.row0;
     const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
     const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
@@ -613,15 +643,16 @@ namespace fi {
 // tensor-core maps (pages under 8 tokens, or G not dividing 128).  The
 // tensor-core phase takes the items before it.  Called by whole warps: lane
 // l looks at item i0 + l (its request's row count decides the class), so 32
-// items cost two dependent loads, not 64.
+// items cost one load.
 __device__ __forceinline__ int32_t first_cuda_core_item(const RunParams& p, int32_t begin, int32_t end,
                                                         int32_t off_items, int32_t off_req, int32_t num_shared) {
   const int lane = threadIdx.x & 31;
   for (int32_t i0 = begin; i0 < end; i0 += 32) {
     bool cc = true;  // past the CTA's last item counts as the boundary
     if (i0 + lane < end) {
-      const int32_t b = __ldg(p.iws + off_items + FI_ITEM_INTS * (i0 + lane));
-      cc = __ldg(p.iws + off_req + FI_REQ_INTS * b + 1) * p.group <= FI_TILE_DECODE || !cache_of(p, b, num_shared).tc;
+      const int32_t* it = p.iws + off_items + FI_ITEM_INTS * (i0 + lane);
+      const int32_t b = __ldg(it), qo_len = __ldg(it + 9);  // the item's own copy of its request's qo_len
+      cc = qo_len * p.group <= FI_TILE_DECODE || !cache_of(p, b, num_shared).tc;
     }
     const unsigned m = __ballot_sync(0xffffffffu, cc);
     if (m) return min(end, i0 + __ffs(m) - 1);

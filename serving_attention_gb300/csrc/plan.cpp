@@ -264,9 +264,13 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
       c.hk = u.hk;
       c.qt = u.qt;
       c.idx = int32_t(i);
-      const int32_t f[FI_ITEM_INTS] = {u.b,         u.hk,       u.row0,
+      const Req& rq = reqs[u.b];
+      const int32_t f[FI_ITEM_INTS] = {u.b,         u.hk,        u.row0,
                                        u.row1,      int32_t(k0), int32_t(k1),
-                                       base >= 0 ? int32_t(base + i * nrows) : -1, merge_id};
+                                       base >= 0 ? int32_t(base + i * nrows) : -1, merge_id,
+                                       rq.qo_start, rq.qo_len,   rq.page_start,
+                                       rq.kv_len,   0,           0,
+                                       0,           0};
       std::memcpy(c.fields, f, sizeof f);
       chunks.push_back(c);
       ++i;

@@ -7,11 +7,14 @@
 //                  kernel compares with the buffers it was launched with;
 //                  the cascade fields, 0 in a one-level plan)
 //   cta_indptr   num_ctas + 1 entries: CTA c runs items [cta_indptr[c], cta_indptr[c+1])
-//   items        FI_ITEM_INTS each: {b, hk, row0, row1, kv0, kv1, part, merge}
+//   items        FI_ITEM_INTS each: {b, hk, row0, row1, kv0, kv1, part, merge,
+//                  qo_start, qo_len, page_start, kv_len, 0, 0, 0, 0}
 //                  rows are packed rows of request b (row = token * G + g),
 //                  [kv0, kv1) the KV token range of this chunk,
 //                  part = first fp32 partial-state row or -1 (unsplit),
-//                  merge = merge unit or -1
+//                  merge = merge unit or -1; then a copy of request b's
+//                  entry of the request table, so that a work item arrives
+//                  with one load instead of two dependent ones
 //   merge units  FI_MERGE_INTS each: {b, hk, row0, row1, n_chunks, part_base, late, 0};
 //                  chunk i of the unit wrote partial rows part_base + i * (row1 - row0) ...
 //                  late = 1 (units of prefill-class tiles): merged after the run by
@@ -47,7 +50,7 @@
 
 #define FI_PLAN_MAGIC 0x46495031
 #define FI_HEADER_INTS 32
-#define FI_ITEM_INTS 8
+#define FI_ITEM_INTS 16
 #define FI_MERGE_INTS 8
 #define FI_REQ_INTS 4
 #define FI_CASCADE_INTS 12

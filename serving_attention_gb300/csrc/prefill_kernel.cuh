@@ -90,12 +90,10 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
       }
     }
   };
-  for (int32_t i = b0; i < b1; ++i) {
-    const Item it = load_item(p.iws, off_items, i);
-    const Request rq = load_request(p.iws, off_req, it.b);
-    const int ntiles = item_kv_tiles(it);
-    if (ntiles == 0) continue;
-    const KvCache& kc = cache_of(p, it.b, num_shared);
+  // One item's tiles from cache kc (instantiated once per cache, so the
+  // cache's fields are kernel parameters at fixed offsets).
+  auto stream_item = [&](const KvCache& kc, const Item& it, int ntiles) {
+    const Request& rq = it.rq;
     const int lp = kc.log2_page, P = kc.page_size;
     const int ppt = kTileN >> lp;  // pages per KV tile
     const int npages = (rq.kv_len + P - 1) >> lp;
@@ -139,6 +137,15 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
       }
     }
     ++pe;
+  };
+  for (int32_t i = b0; i < b1; ++i) {
+    const Item it = load_item(p.iws, off_items, i);
+    const int ntiles = item_kv_tiles(it);
+    if (ntiles == 0) continue;
+    if (it.b < num_shared)
+      stream_item(p.kv[1], it, ntiles);
+    else
+      stream_item(p.kv[0], it, ntiles);
   }
   // Every load this warp armed has landed before the CTA moves on.
   if (lane == 0) {
@@ -202,7 +209,7 @@ __device__ void pf_rope(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1,
     const Item it = load_item(p.iws, off_items, i);
     const int ntiles = item_kv_tiles(it);
     if (ntiles == 0) continue;
-    const Request rq = load_request(p.iws, off_req, it.b);
+    const Request& rq = it.rq;
     const int nrows = it.row1 - it.row0;
     const int nm = item_m_tiles(it);
     if (!warp_wait(&sm.q_full, pe & 1, &sm.abort)) break;
@@ -350,7 +357,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
   uint32_t tiles = 0, items = 0;  // phases of s_full[mt] and o_ready[mt]
   for (int32_t i = b0; i < b1; ++i) {
     const Item item = load_item(p.iws, off_items, i);
-    const Request rq = load_request(p.iws, off_req, item.b);
+    const Request& rq = item.rq;
     const int nrows = item.row1 - item.row0;
     const int ntiles = item_kv_tiles(item);
     const int prow = mt * kTileM + r;  // packed row within the item

@@ -57,13 +57,23 @@ def test_plan_matches_reference_random(seed):
     _check_invariants(ws, qop, kv, hkv * group, hkv, causal, cfgd)
 
 
+def _items(ws, off_items, n_items):
+    """The plan's work items, [item, field]: the first 8 fields (the request's
+    copy that follows them is checked against the request table)."""
+    full = ws[off_items:off_items + plan_ref.ITEM_INTS * n_items].reshape(-1, plan_ref.ITEM_INTS)
+    off_req = ws[10]
+    req = ws[off_req:off_req + 4 * ws[4]].reshape(-1, 4)
+    assert np.array_equal(full[:, 8:12], req[full[:, 0]]) and np.all(full[:, 12:] == 0)
+    return full[:, :8]
+
+
 def _check_invariants(ws, qop, kv, hq, hkv, causal, cfgd):
     G = hq // hkv
     n_items, n_merge, C = ws[1], ws[2], ws[3]
     off_cta, off_items, off_merge, off_cnt, off_req = ws[6], ws[7], ws[8], ws[9], ws[10]
     cta = ws[off_cta:off_cta + C + 1]
     assert cta[0] == 0 and cta[-1] == n_items and np.all(np.diff(cta) >= 0)
-    items = ws[off_items:off_items + 8 * n_items].reshape(-1, 8)
+    items = _items(ws, off_items, n_items)
     assert np.all(ws[off_cnt:off_cnt + n_merge] == 0)
     req = ws[off_req:off_req + 4 * (len(qop) - 1)].reshape(-1, 4)
     assert np.array_equal(req[:, 3], kv)
@@ -126,7 +136,7 @@ def _check_variant_coverage(ws, qop, kv, hq, hkv, causal, page, window, sink):
     disjoint, start on the class granule and none is invisible to all rows."""
     G = hq // hkv
     n_items, off_items = ws[1], ws[7]
-    items = ws[off_items:off_items + 8 * n_items].reshape(-1, 8)
+    items = _items(ws, off_items, n_items)
     by_unit = {}
     for it in items:
         b, hk, r0, r1, k0, k1 = (int(x) for x in it[:6])
@@ -187,7 +197,7 @@ def test_window_skips_chunks():
         cfg, _ = _cfg(num_ctas=152, **kw)
         st, ws, _ = fi.plan_host(cfg, qop, kvp, kvi, lpl, 32, 8, 128, 16, 0)
         assert st == 0
-        items = ws[ws[7]:ws[7] + 8 * ws[1]].reshape(-1, 8)
+        items = _items(ws, ws[7], ws[1])
         return int((items[:, 5] - items[:, 4]).sum())
 
     full = planned_kv()
@@ -385,7 +395,7 @@ def _check_cascade_invariants(ws, shared, own, kv, skv, hq, hkv, causal):
     n_items, n_merge, C = ws[1], ws[2], ws[3]
     assert n_merge == 0 and ws[26] == S
     off_items, off_req, off_cas, n_cas = ws[7], ws[10], ws[27], ws[28]
-    items = ws[off_items:off_items + 8 * n_items].reshape(-1, 8)
+    items = _items(ws, off_items, n_items)
     reqs = ws[off_req:off_req + 4 * ws[4]].reshape(-1, 4)
     ents = ws[off_cas:off_cas + 12 * n_cas].reshape(-1, 12)
     assert np.all(items[:, 6] >= 0) and np.all(items[:, 7] == -1)
