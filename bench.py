@@ -857,6 +857,8 @@ PROFILE_CASES = {
     "ragged_prefill": lambda dev: __import__("workloads").ragged_prefill(device=dev),
     "ragged_prefill_4": lambda dev: __import__("workloads").ragged_prefill(device=dev, batch=4),
     "continuous_batch": lambda dev: __import__("workloads").continuous_batch(device=dev),
+    # the mix with 30 of its 120 decode requests: the same kernel on about a GB (counter captures)
+    "continuous_batch_small": lambda dev: __import__("workloads").continuous_batch(device=dev, n_decode=30),
     "mla_decode": lambda dev: __import__("workloads").mla_decode(device=dev),
     "mla_decode_16": lambda dev: __import__("workloads").mla_decode(device=dev, batch=16),
     "shared_prefix": None,  # the cascade step: one persistent launch + the cascade merge
