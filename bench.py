@@ -665,10 +665,17 @@ def bench_variants(dev, flush, reps=5):
 
 
 def bench_rope(dev, flush, reps=5):
-    """RoPE on unrotated cached keys: fused into the attention loaders, against
-    the unfused form -- every key rotated into a copy by a separate pass
-    (fi_rope_apply_k: read K, write K), then the plain kernel -- and against
-    the plain kernel alone (no rotation at all)."""
+    """RoPE on unrotated queries and cached keys: fused into the attention
+    loaders, against the unfused form -- the queries and every cached key
+    rotated into copies by separate passes (fi_rope_apply_q, fi_rope_apply_k:
+    read, rotate, write), then the plain kernel on the copies -- and against
+    the plain kernel alone (no rotation at all).  The library's RoPE path for
+    a batch is `rope_ms`: the fused run, except that with query and key
+    buffers the queries and keys of prefill-class requests (keys read by
+    every 256-row item of their request) are rotated once by a pass before
+    the kernel (fi_batch_paged_attention_run_rope_prerotated,
+    `prerotated_ms`); decode-class requests stay fully fused.
+    fusion_speedup = unfused / rope_ms."""
     import torch
 
     import serving_attention_gb300 as fi
@@ -682,7 +689,9 @@ def bench_rope(dev, flush, reps=5):
         o = torch.empty_like(b.q)
         lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=dev)
         k_rot = torch.empty_like(b.k)
-        max_kv = int(b.kv_lens().max())
+        q_rot = torch.empty_like(b.q)
+        k_rot16 = torch.empty(b.k.shape, dtype=torch.float16, device=dev)
+        q_rot16 = torch.empty(b.q.shape, dtype=torch.float16, device=dev)
         cfg_p = fi.default_plan_config(dev.index)
         cfg_r = fi.default_plan_config(dev.index, rope_max_positions=max_pos, rope_theta=theta)
         ws_p, ws_r = fi.Workspace(cfg_p, device=dev), fi.Workspace(cfg_r, device=dev)
@@ -694,20 +703,29 @@ def bench_rope(dev, flush, reps=5):
             fi.run(ws_r, info_r, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
 
         def unfused():
-            fi.rope_apply_k(ws_r, info_r, b.k, k_rot, kvi, max_kv)
-            fi.run(ws_p, info_p, b.q, k_rot, b.v, kvi, o, lse, b.sm_scale)
+            fi.rope_apply_q(ws_r, info_r, b.q, q_rot)
+            fi.rope_apply_k(ws_r, info_r, b.k, k_rot, kvi)
+            fi.run(ws_p, info_p, q_rot, k_rot, b.v, kvi, o, lse, b.sm_scale)
 
         def plain():
             fi.run(ws_p, info_p, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
 
-        t = {k: _graph_ms(f, flush, reps) for k, f in (("fused", fused), ("unfused", unfused), ("plain", plain))}
+        def prerotated():
+            fi.run_rope_prerotated(ws_r, info_r, b.q, b.k, b.v, kvi, q_rot16, k_rot16, o, lse, b.sm_scale)
+
+        t = {k: _graph_ms(f, flush, reps) for k, f in (("fused", fused), ("unfused", unfused), ("plain", plain),
+                                                         ("prerotated", prerotated))}
         assert fi.device_status(ws_r) == 0 and fi.device_status(ws_p) == 0
-        res[name] = {"fused_ms": t["fused"], "unfused_ms": t["unfused"], "plain_ms": t["plain"],
-                     "fusion_speedup": t["unfused"] / t["fused"], "fused_cost_vs_plain": t["fused"] / t["plain"]}
-        del b, o, lse, kvi, k_rot, ws_p, ws_r
+        rope_ms = t["prerotated"] if info_r.num_prefill_items > 0 else t["fused"]
+        res[name] = {"fused_ms": t["fused"], "prerotated_ms": t["prerotated"], "rope_ms": rope_ms,
+                     "unfused_ms": t["unfused"], "plain_ms": t["plain"], "fusion_speedup": t["unfused"] / rope_ms,
+                     "fully_fused_speedup": t["unfused"] / t["fused"], "fused_cost_vs_plain": t["fused"] / t["plain"]}
+        del b, o, lse, kvi, k_rot, q_rot, k_rot16, q_rot16, ws_p, ws_r
         torch.cuda.empty_cache()
-    res["workload"] = ("cached keys unrotated; llama8b_decode with theta 5e5, ragged_prefill with theta 1e4; "
-                       "unfused = fi_rope_apply_k over every cached key, then the plain kernel")
+    res["workload"] = ("queries and cached keys unrotated; llama8b_decode with theta 5e5, ragged_prefill with theta "
+                       "1e4; unfused = fi_rope_apply_q and fi_rope_apply_k (every query and cached key), then the "
+                       "plain kernel; rope_ms = the library's path: prerotated when the plan has prefill-class units, "
+                       "else fully fused")
     return res
 
 

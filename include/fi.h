@@ -90,7 +90,11 @@ typedef struct {
      *     FI_ERR_INVALID_ARG), and the int workspace then also holds a
      *     cos/sin table for these positions, filled by fi_rope_init;
      *   rope_theta > 0 (10000 for Llama 2, 500000 for Llama 3);
-     *   rope_scale > 0 divides the positions (1 = no scaling). */
+     *   rope_scale > 0 divides the positions (1 = no scaling).
+     * Rotated keys (and the tensor-core path's rotated queries) are fp16
+     * whatever the cache type; a rotated value past the fp16 range (|x| >
+     * 65504, reachable from bf16 inputs) records FI_ERR_DEVICE_CHECK in the
+     * status word, and the outputs of that run are undefined. */
     int32_t rope_max_positions;
     float rope_theta;
     float rope_scale;
@@ -142,19 +146,33 @@ fi_status fi_rope_init(const fi_plan_config* cfg, void* int_workspace_dev, void*
 
 /*
  * fi_rope_apply_k -- the unfused form: rotate, outside attention, every key
- * of the plan's requests (key j at position j, the same rotation the fused
- * kernel applies) from k_in into k_out, both [num_pages, page_size,
+ * of the plan's requests (key j at position j, the rotation the fused
+ * kernel applies; paper summary, "주요 성능 테스트 결과 / 2. 커널 수준 성능",
+ * compares the two forms) from k_in into k_out, both [num_pages, page_size,
  * num_kv_heads, 128] with their own strides (elements, multiples of 16
  * bytes) and the plan's page ids; k_out may be k_in.  Output in the cache's
  * own type.  Uses the plan in int_workspace_dev (request table and RoPE
- * table: the plan must have been made with RoPE, else FI_ERR_INVALID_ARG);
- * max_kv_len bounds the requests' KV lengths (keys past it are not rotated).
- * Asynchronous on `stream`.
+ * table): FI_ERR_INVALID_ARG for a plan made without RoPE or a cascade plan.
+ * One kernel, flat over the plan's key slots, its counts read from the
+ * workspace (a captured graph serves later plans).  An fp16 cache whose
+ * rotated value leaves the fp16 range records FI_ERR_DEVICE_CHECK in the
+ * status word.  Asynchronous on `stream`.
  */
-fi_status fi_rope_apply_k(const fi_plan_info* info, const void* int_workspace_dev, int32_t max_kv_len,
-                          const void* k_in, const int64_t k_in_strides[3], void* k_out,
-                          const int64_t k_out_strides[3], const int32_t* kv_indices_dev, fi_dtype dtype,
-                          void* stream);
+fi_status fi_rope_apply_k(const fi_plan_info* info, void* int_workspace_dev, const void* k_in,
+                          const int64_t k_in_strides[3], void* k_out, const int64_t k_out_strides[3],
+                          const int32_t* kv_indices_dev, fi_dtype dtype, void* stream);
+
+/*
+ * fi_rope_apply_q -- the unfused form for queries: rotate every query row of
+ * the plan's requests (token t of a request at position kv_len - qo_len + t)
+ * from q_in [tokens, num_qo_heads, 128] (strides q_in_stride_tok,
+ * q_in_stride_head, 1) into q_out (its own strides; q_out may be q_in), in
+ * the input's own type.  Arguments, checks, status and stream behaviour as
+ * fi_rope_apply_k.
+ */
+fi_status fi_rope_apply_q(const fi_plan_info* info, void* int_workspace_dev, const void* q_in,
+                          int64_t q_in_stride_tok, int64_t q_in_stride_head, void* q_out, int64_t q_out_stride_tok,
+                          int64_t q_out_stride_head, fi_dtype dtype, void* stream);
 
 /*
  * fi_plan -- build the load-balanced split-KV work list on the host and copy
@@ -304,6 +322,48 @@ fi_status fi_batch_paged_attention_run(const fi_plan_info* info, const void* q, 
                                        const int32_t* kv_indices_dev, void* o, int64_t o_stride_tok,
                                        int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale,
                                        void* int_workspace_dev, void* float_workspace_dev, void* stream);
+
+/*
+ * fi_batch_paged_attention_run_rope_prerotated -- fi_batch_paged_attention_run
+ * for a plan made with RoPE (fi_plan_config.rope_max_positions > 0), with the
+ * queries and keys of prefill-class requests (more than 16 packed query rows)
+ * rotated once before the kernel instead of inside it (paper summary, "주요
+ * 성능 테스트 결과 / 2. 커널 수준 성능": RoPE fused with attention).
+ * Decode-class requests read each key once, and the kernel keeps rotating
+ * their queries and keys as it loads them.  A prefill-class request's keys
+ * are read by every 256-row work item of the request (tens of times for a
+ * long causal prefill), and the tensor-core phase has only two warps free to
+ * rotate them, so they are rotated by one pass over the request's keys into
+ * k_rot -- its queries into q_rot -- and the tensor cores read both from
+ * there.  The arguments are those of fi_batch_paged_attention_run plus two
+ * caller-owned device buffers in **fp16** (rotated values are fp16 whatever
+ * the cache type, as on the fused path: q and k meet only each other in
+ * S = q.k):
+ *   q_rot [q_num_tokens, num_qo_heads, 128], strides (q_rot_stride_tok,
+ *         q_rot_stride_head, 1), rows of prefill-class requests written;
+ *   k_rot [num_pages, page_size, num_kv_heads, 128], strides k_rot_strides,
+ *         written at the pages of prefill-class requests (same page ids as
+ *         the cache); the rest of both buffers is left alone.
+ * Strides are elements, multiples of 16 bytes.  FI_ERR_INVALID_ARG for a plan
+ * without RoPE or a cascade plan.  With pages under 8 tokens (no tensor-core
+ * path), or when `info` has no prefill-class item, the call is the fully
+ * fused run and the buffers are not touched.  Otherwise two kernels on
+ * `stream`: the rotation pass (its counts read from the workspace, so a
+ * captured graph serves later plans), then the run -- on the kernel without
+ * RoPE when `info` has no decode-class item.  That kernel refuses a
+ * workspace re-planned since with decode-class items (FI_ERR_DEVICE_CHECK,
+ * nothing written): capture such graphs from a plan with decode-class items.
+ * A rotated value past the fp16 range (|x| > 65504, reachable from bf16
+ * inputs) records FI_ERR_DEVICE_CHECK; the outputs of that run are then
+ * undefined.  The fully fused run reports the same.  Asynchronous.
+ */
+fi_status fi_batch_paged_attention_run_rope_prerotated(
+    const fi_plan_info* info, const void* q, int64_t q_stride_tok, int64_t q_stride_head, int32_t q_num_tokens,
+    const void* k_cache, const int64_t k_strides[3], const void* v_cache, const int64_t v_strides[3],
+    int32_t num_pages, const int32_t* kv_indices_dev, void* q_rot, int64_t q_rot_stride_tok,
+    int64_t q_rot_stride_head, void* k_rot, const int64_t k_rot_strides[3], void* o, int64_t o_stride_tok,
+    int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale, void* int_workspace_dev,
+    void* float_workspace_dev, void* stream);
 
 /*
  * fi_batch_paged_attention_run_cascade -- the run of a plan made by

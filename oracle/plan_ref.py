@@ -44,7 +44,7 @@ Rule:
  6. Output: header (with the variant: window, sink, soft-cap bits, and for
     RoPE its position capacity, theta and scale bits and the table offset;
     then the count of late units, the partial rows used, the batch's query
-    tokens and two zero fields), per-CTA
+    tokens, the cascade fields, the count of 16-row items and a zero field), per-CTA
     CSR offsets, items in CTA order (within a CTA the 256-row items first,
     then the 16-row items, each in the order dealt), merge units, zeroed merge
     counters, request table.
@@ -342,12 +342,13 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
         return int(np.array([x], dtype=np.float32).view(np.int32)[0])
 
     rope_off = (int_workspace_ints(cfg) * 4 + 255) // 256 * 256 // 4 if rope_max > 0 else 0
+    n_dec = sum(1 for _, f in items if lq[f[0]] * group <= 16)
     ws[:HEADER_INTS] = [MAGIC, n_items, n_merge, C, batch, causal, off_cta, off_items, off_merge,
                         off_cnt, off_req, 0, num_qo_heads, num_kv_heads, page_size, total_ints,
                         window, sink, bits(cap), rope_max,
                         bits(theta) if rope_max > 0 else 0, bits(rscale) if rope_max > 0 else 0, rope_off,
                         sum(1 for m in merges if m[6]), part_rows, total_qo, num_shared,
-                        off_cascade if cascade else 0, len(entries), shared_page_size if cascade else 0, 0, 0]
+                        off_cascade if cascade else 0, len(entries), shared_page_size if cascade else 0, n_dec, 0]
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos
@@ -364,7 +365,6 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
     for e, fields in enumerate(entries):
         ws[off_cascade + CASCADE_INTS * e: off_cascade + CASCADE_INTS * (e + 1)] = fields
 
-    n_dec = sum(1 for _, f in items if lq[f[0]] * group <= 16)
     info = dict(num_ctas=C, num_items=n_items, num_merge_units=n_merge,
                 num_late_merge_units=sum(1 for m in merges if m[6]), batch=batch,
                 num_partial_rows=part_rows, num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads,

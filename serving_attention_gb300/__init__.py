@@ -62,9 +62,10 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ["fi_default_plan_config", "fi_int_workspace_bytes", "fi_float_workspace_bytes", "fi_plan",
            "fi_plan_host", "fi_plan_cascade", "fi_plan_cascade_host", "fi_batch_paged_attention_run",
-           "fi_batch_paged_attention_run_cascade", "fi_batch_paged_attention_run_static_scratch",
+           "fi_batch_paged_attention_run_cascade", "fi_batch_paged_attention_run_rope_prerotated",
+           "fi_batch_paged_attention_run_static_scratch",
            "fi_merge_states", "fi_get_device_status", "fi_status_string", "fi_rope_init", "fi_rope_apply_k",
-           "fi_selftest_bounded_wait"]
+           "fi_rope_apply_q", "fi_selftest_bounded_wait"]
 
 _lib = None
 
@@ -89,6 +90,9 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
                                          i32, i32, vp, sz, infop]
     lib.fi_plan_cascade.argtypes = [cfgp, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                     i32, vp, vp, sz, vp, infop]
+    lib.fi_batch_paged_attention_run_rope_prerotated.argtypes = [infop, vp, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp,
+                                                                 i64, i64, vp, vp, vp, i64, i64, vp, ctypes.c_int,
+                                                                 ctypes.c_float, vp, vp, vp]
     lib.fi_batch_paged_attention_run_cascade.argtypes = [infop, vp, i64, i64, i32, vp, vp, vp, vp, i32, vp, vp, vp,
                                                          vp, vp, i32, vp, i32, vp, i64, i64, vp, ctypes.c_int,
                                                          ctypes.c_float, vp, vp, vp]
@@ -100,14 +104,16 @@ def load(build_if_stale: bool = True) -> ctypes.CDLL:
     lib.fi_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int, vp]
     lib.fi_get_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.fi_rope_init.argtypes = [cfgp, vp, vp]
-    lib.fi_rope_apply_k.argtypes = [infop, vp, i32, vp, vp, vp, vp, vp, ctypes.c_int, vp]
+    lib.fi_rope_apply_k.argtypes = [infop, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp]
+    lib.fi_rope_apply_q.argtypes = [infop, vp, vp, i64, i64, vp, i64, i64, ctypes.c_int, vp]
     lib.fi_selftest_bounded_wait.argtypes = [vp, vp]
     lib.fi_selftest_bounded_wait.restype = ctypes.c_int
     lib.fi_status_string.argtypes = [ctypes.c_int]
     lib.fi_status_string.restype = ctypes.c_char_p
     for name in ("fi_default_plan_config", "fi_plan", "fi_plan_host", "fi_plan_cascade", "fi_plan_cascade_host",
-                 "fi_batch_paged_attention_run", "fi_batch_paged_attention_run_cascade", "fi_merge_states",
-                 "fi_get_device_status", "fi_rope_init", "fi_rope_apply_k"):
+                 "fi_batch_paged_attention_run", "fi_batch_paged_attention_run_cascade",
+                 "fi_batch_paged_attention_run_rope_prerotated", "fi_merge_states",
+                 "fi_get_device_status", "fi_rope_init", "fi_rope_apply_k", "fi_rope_apply_q"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -293,6 +299,32 @@ def run(ws: Workspace, info: PlanInfo, q: torch.Tensor, k_cache: torch.Tensor, v
     _check(st, "fi_batch_paged_attention_run")
 
 
+def run_rope_prerotated(ws: Workspace, info: PlanInfo, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        kv_indices_dev: torch.Tensor, q_rot: torch.Tensor, k_rot: torch.Tensor, o: torch.Tensor,
+                        lse: torch.Tensor | None, sm_scale: float, stream=None):
+    """run() of a RoPE plan with the queries and keys of prefill-class
+    requests rotated once into q_rot and k_rot (fp16, the shapes of q and the
+    cache) before the kernel."""
+    if kv_indices_dev.dtype != torch.int32 or not kv_indices_dev.is_contiguous():
+        raise TypeError("kv_indices must be a contiguous int32 device tensor")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise TypeError("lse must be contiguous fp32")
+    if q.dtype != k_cache.dtype or q.dtype != v_cache.dtype or q.dtype != o.dtype:
+        raise TypeError("q, k, v and o share one dtype")
+    if k_rot.dtype != torch.float16 or q_rot.dtype != torch.float16:
+        raise TypeError("q_rot and k_rot are fp16")
+    ks = (ctypes.c_int64 * 3)(*k_cache.stride()[:3])
+    vs = (ctypes.c_int64 * 3)(*v_cache.stride()[:3])
+    rs = (ctypes.c_int64 * 3)(*k_rot.stride()[:3])
+    st = load().fi_batch_paged_attention_run_rope_prerotated(
+        ctypes.byref(info), q.data_ptr(), q.stride(0), q.stride(1), q.shape[0], k_cache.data_ptr(), ks,
+        v_cache.data_ptr(), vs, k_cache.shape[0], kv_indices_dev.data_ptr(), q_rot.data_ptr(), q_rot.stride(0),
+        q_rot.stride(1), k_rot.data_ptr(), rs, o.data_ptr(),
+        o.stride(0), o.stride(1), lse.data_ptr() if lse is not None else None, _dtype_code(q), float(sm_scale),
+        ws.int_ws.data_ptr(), ws.float_ws.data_ptr(), _stream_ptr(stream))
+    _check(st, "fi_batch_paged_attention_run_rope_prerotated")
+
+
 def run_cascade(ws: Workspace, info: PlanInfo, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                 kv_indices_dev: torch.Tensor, shared_k: torch.Tensor, shared_v: torch.Tensor,
                 shared_kv_indices_dev: torch.Tensor, o: torch.Tensor, lse: torch.Tensor | None, sm_scale: float,
@@ -356,14 +388,22 @@ def merge_states(v_a, s_a, v_b, s_b, v_out, s_out, stream=None):
     _check(st, "fi_merge_states")
 
 
-def rope_apply_k(ws: Workspace, info: PlanInfo, k_in, k_out, kv_indices, max_kv_len: int, stream=None):
+def rope_apply_k(ws: Workspace, info: PlanInfo, k_in, k_out, kv_indices, stream=None):
     """Unfused RoPE: rotate the keys of the plan's requests from k_in into k_out
     ([pages, page_size, Hkv, 128], same dtype; k_out may be k_in)."""
     ks_in = (ctypes.c_int64 * 3)(*k_in.stride()[:3])
     ks_out = (ctypes.c_int64 * 3)(*k_out.stride()[:3])
-    _check(load().fi_rope_apply_k(ctypes.byref(info), ws.int_ws.data_ptr(), int(max_kv_len), k_in.data_ptr(), ks_in,
-                                  k_out.data_ptr(), ks_out, kv_indices.data_ptr(), _dtype_code(k_in),
-                                  _stream_ptr(stream)), "fi_rope_apply_k")
+    _check(load().fi_rope_apply_k(ctypes.byref(info), ws.int_ws.data_ptr(), k_in.data_ptr(), ks_in, k_out.data_ptr(),
+                                  ks_out, kv_indices.data_ptr(), _dtype_code(k_in), _stream_ptr(stream)),
+           "fi_rope_apply_k")
+
+
+def rope_apply_q(ws: Workspace, info: PlanInfo, q_in, q_out, stream=None):
+    """Unfused RoPE: rotate the query rows of the plan's requests from q_in
+    into q_out ([tokens, Hq, 128], same dtype; q_out may be q_in)."""
+    _check(load().fi_rope_apply_q(ctypes.byref(info), ws.int_ws.data_ptr(), q_in.data_ptr(), q_in.stride(0),
+                                  q_in.stride(1), q_out.data_ptr(), q_out.stride(0), q_out.stride(1),
+                                  _dtype_code(q_in), _stream_ptr(stream)), "fi_rope_apply_q")
 
 
 def selftest_bounded_wait(ws, stream=None):

@@ -178,37 +178,272 @@ __global__ void rope_table_kernel(float2* table, int64_t entries, double theta, 
   table[idx] = make_float2(float(cs), float(sn));
 }
 
-// Standalone RoPE of the keys of a plan's requests (key j at position j),
-// from k_in to k_out (same page ids; they may be the same cache).  One block
-// per request and 64-key chunk; a task is one key, one KV head and one
-// 8-dim chunk of each half.
-template <typename T>
-__global__ void __launch_bounds__(256) rope_apply_k_kernel(const int32_t* __restrict__ iws, const uint16_t* k_in,
-                                                           int64_t ki0, int64_t ki1, int64_t ki2, uint16_t* k_out,
-                                                           int64_t ko0, int64_t ko1, int64_t ko2,
-                                                           const int32_t* __restrict__ kv_indices, int log2_page,
-                                                           int num_kv_heads) {
-  const int b = blockIdx.y;
-  if (b >= __ldg(iws + FI_H_BATCH)) return;
-  const Request rq = load_request(iws, __ldg(iws + FI_H_OFF_REQUESTS), b);
-  const int j0 = blockIdx.x * 64;
-  if (j0 >= rq.kv_len) return;
+// Rotation passes outside attention -- the standalone forms and the pass of
+// the pre-rotated run -- flat over the requests they rotate, so that one
+// long request is spread over the whole grid.  Each CTA first lists those
+// requests (for the pre-rotated run only prefill-class ones) with prefix sums
+// of their pages and query tokens in shared memory; past kRopeListCap
+// requests it walks the whole request table instead, skipping row by row.
+// Unit u < nk covers 32 consecutive key slots of the listed requests' pages,
+// unit u >= nk 32 of their query tokens; key j of a request sits at position
+// j, its query token t at kv_len - qo_len + t.  Warp 0 finds the rows of a
+// CTA's next unit (a binary search over the prefix sums per row) while the
+// block rotates the current one.  A task is one row (slot or token, and a
+// head) and one 8-dim chunk of each half; a thread issues the loads of four
+// tasks before it rotates any.  The counts come from the plan in the
+// workspace, so a graph captured once serves later plans.  fp16 output past
+// the fp16 range (|x| > 65504, which a bf16 input can reach) records
+// kStatusRange.
+struct RopePass {
+  int32_t* iws;
+  const uint16_t* k_in;
+  int64_t ki[3];
+  uint16_t* k_out;
+  int64_t ko[3];
+  const int32_t* kv_indices;
+  const uint16_t* q_in;
+  int64_t qi_tok, qi_head;
+  uint16_t* q_out;
+  int64_t qo_tok, qo_head;
+  int log2_page, num_kv_heads, num_qo_heads, group;
+  int keys, queries;  // what the pass rotates
+  int prefill_only;   // leave decode-class requests (at most 16 packed rows) alone
+};
+
+constexpr int kRopeUnitRows = 32, kRopeLoadsAhead = 4, kRopeThreads = 256, kRopeListCap = 1024;
+
+template <typename T, typename TOut>
+__global__ void __launch_bounds__(kRopeThreads, 3) rope_pass_kernel(const __grid_constant__ RopePass a) {
+  __shared__ int32_t s_req[kRopeListCap];                      // listed request
+  __shared__ int32_t s_pages[kRopeListCap + 1], s_toks[kRopeListCap + 1];  // prefix sums over the list
+  __shared__ int32_t s_warp[kRopeThreads / 32], s_n;
+  // per unit row, double-buffered: element offsets of the row (head 0), -1
+  // when it is not rotated, and its position
+  __shared__ int64_t s_in[2][kRopeUnitRows], s_out[2][kRopeUnitRows];
+  __shared__ int32_t s_pos[2][kRopeUnitRows];
+  const int32_t* iws = a.iws;
+  const int batch = __ldg(iws + FI_H_BATCH);
+  if (batch <= 0) return;
+  const int32_t off_req = __ldg(iws + FI_H_OFF_REQUESTS);
   const float2* table = reinterpret_cast<const float2*>(iws + __ldg(iws + FI_H_ROPE_TABLE_OFF));
-  const int P = 1 << log2_page;
-  const int tasks = 64 * num_kv_heads * 8;
-  for (int task = threadIdx.x; task < tasks; task += blockDim.x) {
-    const int key = task / (num_kv_heads * 8), rem = task - key * (num_kv_heads * 8);
-    const int h = rem >> 3, c = rem & 7;
-    const int j = j0 + key;
-    if (j >= rq.kv_len) continue;
-    const int64_t page = __ldg(kv_indices + rq.page_start + (j >> log2_page));
-    const int slot = j & (P - 1);
-    const int64_t ib = page * ki0 + slot * ki1 + h * ki2 + 8 * c, ob = page * ko0 + slot * ko1 + h * ko2 + 8 * c;
-    uint4 lo = *reinterpret_cast<const uint4*>(k_in + ib), hi = *reinterpret_cast<const uint4*>(k_in + ib + 64);
-    rope_pairs8<T, T>(lo, hi, table + int64_t(j) * FI_ROPE_PAIRS + 8 * c);
-    *reinterpret_cast<uint4*>(k_out + ob) = lo;
-    *reinterpret_cast<uint4*>(k_out + ob + 64) = hi;
+  const int P = 1 << a.log2_page;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto wanted = [&](const Request& rq) { return !(a.prefill_only && rq.qo_len * a.group <= FI_TILE_DECODE); };
+
+  // The list: requests in table order, block-wide compaction 256 at a time.
+  if (tid == 0) s_n = 0;
+  __syncthreads();
+  bool listed = true;
+  for (int b0 = 0; b0 < batch && listed; b0 += kRopeThreads) {
+    const int b = b0 + tid;
+    bool take = false;
+    if (b < batch) take = wanted(load_request(iws, off_req, b));
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (lane == 0) s_warp[warp] = __popc(m);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kRopeThreads / 32; ++w) {
+      before += w < warp ? s_warp[w] : 0;
+      total += s_warp[w];
+    }
+    const int n0 = s_n;
+    if (n0 + total > kRopeListCap) {
+      listed = false;  // every thread sees the same counts
+    } else if (take) {
+      s_req[n0 + before + __popc(m & ((1u << lane) - 1u))] = b;
+    }
+    __syncthreads();
+    if (tid == 0 && listed) s_n = n0 + total;
+    __syncthreads();
   }
+  const int n = listed ? s_n : batch;
+  if (listed) {
+    // prefix sums of pages and tokens: thread t sums entries [4t, 4t + 4)
+    // of each group of 1024, then a scan of the 256 partial sums
+    int carry_p = 0, carry_t = 0;
+    if (tid == 0) s_pages[0] = s_toks[0] = 0;
+    for (int e0 = 0; e0 < n; e0 += 4 * kRopeThreads) {
+      int vp[4], vt[4], sp = 0, st = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = e0 + 4 * tid + k;
+        vp[k] = vt[k] = 0;
+        if (e < n) {
+          const Request rq = load_request(iws, off_req, s_req[e]);
+          vp[k] = a.keys ? (rq.kv_len + P - 1) >> a.log2_page : 0;
+          vt[k] = a.queries ? rq.qo_len : 0;
+        }
+        sp += vp[k];
+        st += vt[k];
+      }
+      int ip = sp, it = st;  // inclusive warp scan
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int up = __shfl_up_sync(0xffffffffu, ip, d), ut = __shfl_up_sync(0xffffffffu, it, d);
+        if (lane >= d) {
+          ip += up;
+          it += ut;
+        }
+      }
+      __syncthreads();
+      if (lane == 31) {
+        s_warp[warp] = ip;
+        s_in[0][warp] = it;  // borrowed as scratch before the units start
+      }
+      __syncthreads();
+      int wp = 0, wt = 0, tp = 0, tt = 0;
+      for (int w = 0; w < kRopeThreads / 32; ++w) {
+        wp += w < warp ? s_warp[w] : 0;
+        wt += w < warp ? int(s_in[0][w]) : 0;
+        tp += s_warp[w];
+        tt += int(s_in[0][w]);
+      }
+      int rp = carry_p + wp + ip - sp, rt = carry_t + wt + it - st;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = e0 + 4 * tid + k;
+        rp += vp[k];
+        rt += vt[k];
+        if (e < n) {
+          s_pages[e + 1] = rp;
+          s_toks[e + 1] = rt;
+        }
+      }
+      carry_p += tp;
+      carry_t += tt;
+    }
+    __syncthreads();
+  }
+  // Entry e of the list (or request e of the table): its request, and the
+  // first page and token of its share of the flat unit space.
+  auto req_of = [&](int e) { return listed ? s_req[e] : e; };
+  auto first_page = [&](int e) {
+    if (listed) return s_pages[e];
+    if (e == batch) {
+      const Request l = load_request(iws, off_req, batch - 1);
+      return l.page_start + ((l.kv_len + P - 1) >> a.log2_page);
+    }
+    return __ldg(iws + off_req + FI_REQ_INTS * e + 2);
+  };
+  auto first_token = [&](int e) {
+    if (listed) return s_toks[e];
+    if (e == batch) {
+      const Request l = load_request(iws, off_req, batch - 1);
+      return l.qo_start + l.qo_len;
+    }
+    return __ldg(iws + off_req + FI_REQ_INTS * e);
+  };
+  const int64_t slots = a.keys ? int64_t(first_page(n)) << a.log2_page : 0;
+  const int64_t total_qo = a.queries ? first_token(n) : 0;
+  const int64_t nk = (slots + kRopeUnitRows - 1) / kRopeUnitRows;
+  const int64_t nu = nk + (total_qo + kRopeUnitRows - 1) / kRopeUnitRows;
+  // rows of unit u into buffer `buf` (lane = row of the unit; warp 0 only)
+  auto find_rows = [&](int64_t u, int buf) {
+    const bool key_unit = u < nk;
+    const int64_t x = (key_unit ? u : u - nk) * kRopeUnitRows + lane;
+    int64_t bi = -1, bo = -1;
+    int pos = 0;
+    if (x < (key_unit ? slots : total_qo)) {
+      const int64_t g = key_unit ? (x >> a.log2_page) : x;  // flat page, or flat query token
+      int lo = 0, hi = n - 1;  // the last entry whose first page (token) is at or before g
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((key_unit ? first_page(mid) : first_token(mid)) <= g)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      const Request rq = load_request(iws, off_req, req_of(lo));
+      if (listed || wanted(rq)) {
+        if (key_unit) {
+          const int slot = int(x & (P - 1));
+          const int64_t pg = g - first_page(lo);  // page of the request
+          const int64_t j = (pg << a.log2_page) + slot;
+          if (j < rq.kv_len) {
+            const int64_t page = __ldg(a.kv_indices + rq.page_start + pg);
+            bi = page * a.ki[0] + slot * a.ki[1];
+            bo = page * a.ko[0] + slot * a.ko[1];
+            pos = int(j);
+          }
+        } else {
+          const int64_t t = g - first_token(lo);  // token of the request
+          bi = (rq.qo_start + t) * a.qi_tok;
+          bo = (rq.qo_start + t) * a.qo_tok;
+          pos = rq.kv_len - rq.qo_len + int(t);
+        }
+      }
+    }
+    s_in[buf][lane] = bi;
+    s_out[buf][lane] = bo;
+    s_pos[buf][lane] = pos;
+  };
+  __half2 amax = __float2half2_rn(0.f);
+  int buf = 0;
+  if (warp == 0 && blockIdx.x < nu) find_rows(blockIdx.x, 0);
+  __syncthreads();
+  for (int64_t u = blockIdx.x; u < nu; u += gridDim.x, buf ^= 1) {
+    // the next unit's rows go to the other buffer, read after the barrier below
+    if (warp == 0 && u + gridDim.x < nu) find_rows(u + gridDim.x, buf ^ 1);
+    const bool key_unit = u < nk;
+    const int H = key_unit ? a.num_kv_heads : a.num_qo_heads;
+    const uint16_t* src = key_unit ? a.k_in : a.q_in;
+    uint16_t* dst = key_unit ? a.k_out : a.q_out;
+    const int64_t hs_in = key_unit ? a.ki[2] : a.qi_head, hs_out = key_unit ? a.ko[2] : a.qo_head;
+    const int tasks = kRopeUnitRows * H * 8;
+    for (int t0 = tid; t0 < tasks; t0 += kRopeLoadsAhead * kRopeThreads) {
+      uint4 lo[kRopeLoadsAhead], hi[kRopeLoadsAhead];
+      int64_t ob[kRopeLoadsAhead];
+      const float2* cs[kRopeLoadsAhead];
+#pragma unroll
+      for (int k = 0; k < kRopeLoadsAhead; ++k) {
+        const int t = t0 + k * kRopeThreads;
+        ob[k] = -1;
+        if (t < tasks) {
+          const int r = t / (H * 8), rem = t - r * (H * 8);
+          const int h = rem >> 3, c = rem & 7;
+          const int64_t ib = s_in[buf][r];
+          if (ib >= 0) {
+            const int64_t i = ib + h * hs_in + 8 * c;
+            lo[k] = *reinterpret_cast<const uint4*>(src + i);
+            hi[k] = *reinterpret_cast<const uint4*>(src + i + 64);
+            ob[k] = s_out[buf][r] + h * hs_out + 8 * c;
+            cs[k] = table + int64_t(s_pos[buf][r]) * FI_ROPE_PAIRS + 8 * c;
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kRopeLoadsAhead; ++k) {
+        if (ob[k] < 0) continue;
+        rope_pairs8<T, TOut>(lo[k], hi[k], cs[k]);
+        if (std::is_same<TOut, __half>::value) {
+          absmax_f16x8(amax, lo[k]);
+          absmax_f16x8(amax, hi[k]);
+        }
+        *reinterpret_cast<uint4*>(dst + ob[k]) = lo[k];
+        *reinterpret_cast<uint4*>(dst + ob[k] + 64) = hi[k];
+      }
+    }
+    __syncthreads();  // this unit's rows are read; the next unit's are written
+  }
+  if (std::is_same<TOut, __half>::value && f16x2_has_inf(amax)) atomicOr(a.iws + FI_H_STATUS, kStatusRange);
+}
+
+inline int log2_of(int page_size) {
+  int lp = 0;
+  while ((1 << lp) < page_size) ++lp;
+  return lp;
+}
+
+// Three CTAs per planned CTA of the run (the kernel's residency bound).
+inline cudaError_t launch_rope_pass(const RopePass& rp, fi_dtype dtype, bool to_f16, int num_ctas, cudaStream_t s) {
+  const unsigned grid = unsigned(3 * (num_ctas > 0 ? num_ctas : 1));
+  if (dtype == FI_BF16 && to_f16)
+    rope_pass_kernel<__nv_bfloat16, __half><<<grid, kRopeThreads, 0, s>>>(rp);
+  else if (dtype == FI_BF16)
+    rope_pass_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, kRopeThreads, 0, s>>>(rp);
+  else
+    rope_pass_kernel<__half, __half><<<grid, kRopeThreads, 0, s>>>(rp);
+  return cudaGetLastError();
 }
 
 template <typename T>
@@ -467,7 +702,9 @@ cudaError_t launch_cascade_merge(const RunParams& p, int32_t blocks, cudaStream_
 fi_status run_impl(const fi_plan_info* info, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
                    int32_t q_num_tokens, const CacheArgs& own, const CacheArgs* shared, void* o,
                    int64_t o_stride_tok, int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale,
-                   void* int_workspace_dev, void* float_workspace_dev, void* stream) {
+                   void* int_workspace_dev, void* float_workspace_dev, void* stream, void* k_rot = nullptr,
+                   const int64_t* k_rot_strides = nullptr, void* q_rot = nullptr, int64_t q_rot_stride_tok = 0,
+                   int64_t q_rot_stride_head = 0) {
   if (!info || !q || !o || !int_workspace_dev) return FI_ERR_INVALID_ARG;
   if (info->num_ctas < 1 || q_num_tokens < 1 || !std::isfinite(sm_scale)) return FI_ERR_INVALID_ARG;
   if (info->num_partial_rows > 0 && !float_workspace_dev) return FI_ERR_INVALID_ARG;
@@ -510,12 +747,38 @@ fi_status run_impl(const fi_plan_info* info, const void* q, int64_t q_stride_tok
     p.has_shared = 1;
   }
   if (st != FI_OK) return st;
+  if (k_rot) {
+    // RoPE with the queries and keys of prefill-class requests pre-rotated
+    // into q_rot and k_rot (fp16): the tensor-core path reads them there; V,
+    // and the CUDA-core path's queries and keys (rotated inside the kernel),
+    // stay where they are.  A plan without prefill-class items (or pages
+    // with no tensor-core path) makes this the fully fused run: no pass, and
+    // a graph captured from it stays correct for any later plan (its
+    // tensor-core items then rotate inside the kernel).
+    if (!(info->variant & 4) || !k_rot_strides || !q_rot) return FI_ERR_INVALID_ARG;
+    if (!aligned16(k_rot) || !aligned16(q_rot) || !stride_ok(q_rot_stride_tok) || !stride_ok(q_rot_stride_head))
+      return FI_ERR_ALIGNMENT;
+    for (int i = 0; i < 3; ++i)
+      if (!stride_ok(k_rot_strides[i])) return FI_ERR_ALIGNMENT;
+    if (p.kv[0].tc && info->num_prefill_items > 0) {
+      const int P = own.page_size;
+      const uint64_t kd[4] = {uint64_t(kHeadDim), uint64_t(info->num_kv_heads), uint64_t(P), uint64_t(own.num_pages)};
+      const int64_t ks[3] = {k_rot_strides[2], k_rot_strides[1], k_rot_strides[0]};
+      const uint32_t kb[4] = {64u, 1u, uint32_t(P), 1u};
+      if (!make_map(&p.kv[0].tm_k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_rot, 4, kd, ks, kb, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FI_ERR_UNSUPPORTED;
+      p.qk_prerotated = 1;
+    }
+  }
   if (p.kv[0].tc || p.kv[1].tc) {
     const uint64_t qd[3] = {uint64_t(kHeadDim), uint64_t(info->num_qo_heads), uint64_t(q_num_tokens)};
     const int64_t qs[2] = {q_stride_head, q_stride_tok};
     const uint32_t qb[3] = {64u, uint32_t(G), uint32_t(kTileM / G)};
     const int64_t os[2] = {o_stride_head, o_stride_tok};
-    if (!make_map(&p.tm_q, tt, q, 3, qd, qs, qb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    const int64_t qrs[2] = {q_rot_stride_head, q_rot_stride_tok};
+    const bool qr = p.qk_prerotated != 0;
+    if (!make_map(&p.tm_q, qr ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : tt, qr ? q_rot : q, 3, qd, qr ? qrs : qs, qb,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&p.tm_o, tt, o, 3, qd, os, qb, CU_TENSOR_MAP_SWIZZLE_128B))
       return FI_ERR_UNSUPPORTED;
   }
@@ -528,8 +791,23 @@ fi_status run_impl(const fi_plan_info* info, const void* q, int64_t q_stride_tok
   // run then merges late units of later plans itself.  A cascade plan's
   // merge follows the run when `info` has cascade entries.
   p.late_merge = info->num_late_merge_units > 0 ? 1 : 0;
-  cudaError_t e = dtype == FI_BF16 ? launch_variant<__nv_bfloat16>(p, info->num_ctas, info->variant, s)
-                                   : launch_variant<__half>(p, info->num_ctas, info->variant, s);
+  cudaError_t e = cudaSuccess;
+  int variant = info->variant;
+  if (p.qk_prerotated) {
+    RopePass rp{p.iws, static_cast<const uint16_t*>(own.k), {own.k_strides[0], own.k_strides[1], own.k_strides[2]},
+                static_cast<uint16_t*>(k_rot), {k_rot_strides[0], k_rot_strides[1], k_rot_strides[2]},
+                own.kv_indices, static_cast<const uint16_t*>(q), q_stride_tok, q_stride_head,
+                static_cast<uint16_t*>(q_rot), q_rot_stride_tok, q_rot_stride_head, log2_of(own.page_size),
+                info->num_kv_heads, info->num_qo_heads, G, 1, 1, 1};
+    e = launch_rope_pass(rp, dtype, true, info->num_ctas, s);
+    // With every item on the tensor-core path nothing is left to rotate in
+    // the kernel: the instantiation without RoPE runs (it refuses a plan
+    // with CUDA-core items, which a later re-plan could bring).
+    if (info->num_decode_items == 0) variant &= ~4;
+  }
+  if (e == cudaSuccess)
+    e = dtype == FI_BF16 ? launch_variant<__nv_bfloat16>(p, info->num_ctas, variant, s)
+                         : launch_variant<__half>(p, info->num_ctas, variant, s);
   if (e == cudaSuccess && p.late_merge)
     e = dtype == FI_BF16 ? launch_late_merge<__nv_bfloat16>(p, 4 * info->num_ctas, s)
                          : launch_late_merge<__half>(p, 4 * info->num_ctas, s);
@@ -552,6 +830,20 @@ extern "C" fi_status fi_batch_paged_attention_run(const fi_plan_info* info, cons
   const CacheArgs own{k_cache, k_strides, v_cache, v_strides, num_pages, kv_indices_dev, info->page_size};
   return run_impl(info, q, q_stride_tok, q_stride_head, q_num_tokens, own, nullptr, o, o_stride_tok, o_stride_head,
                   lse, dtype, sm_scale, int_workspace_dev, float_workspace_dev, stream);
+}
+
+extern "C" fi_status fi_batch_paged_attention_run_rope_prerotated(
+    const fi_plan_info* info, const void* q, int64_t q_stride_tok, int64_t q_stride_head, int32_t q_num_tokens,
+    const void* k_cache, const int64_t k_strides[3], const void* v_cache, const int64_t v_strides[3],
+    int32_t num_pages, const int32_t* kv_indices_dev, void* q_rot, int64_t q_rot_stride_tok,
+    int64_t q_rot_stride_head, void* k_rot, const int64_t k_rot_strides[3], void* o, int64_t o_stride_tok,
+    int64_t o_stride_head, float* lse, fi_dtype dtype, float sm_scale, void* int_workspace_dev,
+    void* float_workspace_dev, void* stream) {
+  if (!info || !k_rot || !q_rot) return FI_ERR_INVALID_ARG;
+  const CacheArgs own{k_cache, k_strides, v_cache, v_strides, num_pages, kv_indices_dev, info->page_size};
+  return run_impl(info, q, q_stride_tok, q_stride_head, q_num_tokens, own, nullptr, o, o_stride_tok, o_stride_head,
+                  lse, dtype, sm_scale, int_workspace_dev, float_workspace_dev, stream, k_rot, k_rot_strides, q_rot,
+                  q_rot_stride_tok, q_rot_stride_head);
 }
 
 extern "C" fi_status fi_batch_paged_attention_run_cascade(
@@ -584,36 +876,48 @@ extern "C" fi_status fi_rope_init(const fi_plan_config* cfg, void* int_workspace
   return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 
-extern "C" fi_status fi_rope_apply_k(const fi_plan_info* info, const void* int_workspace_dev, int32_t max_kv_len,
-                                     const void* k_in, const int64_t k_in_strides[3], void* k_out,
-                                     const int64_t k_out_strides[3], const int32_t* kv_indices_dev, fi_dtype dtype,
-                                     void* stream) {
-  if (!info || !int_workspace_dev || !k_in || !k_out || !k_in_strides || !k_out_strides || !kv_indices_dev ||
-      max_kv_len < 0)
+extern "C" fi_status fi_rope_apply_k(const fi_plan_info* info, void* int_workspace_dev, const void* k_in,
+                                     const int64_t k_in_strides[3], void* k_out, const int64_t k_out_strides[3],
+                                     const int32_t* kv_indices_dev, fi_dtype dtype, void* stream) {
+  if (!info || !int_workspace_dev || !k_in || !k_out || !k_in_strides || !k_out_strides || !kv_indices_dev)
     return FI_ERR_INVALID_ARG;
-  if (!(info->variant & 4)) return FI_ERR_INVALID_ARG;  // the plan carries no RoPE table
+  if (!(info->variant & 4) || info->num_shared > 0) return FI_ERR_INVALID_ARG;  // no RoPE table, or two caches
   if (info->head_dim != kHeadDim) return FI_ERR_UNSUPPORTED;
   if (dtype != FI_FP16 && dtype != FI_BF16) return FI_ERR_UNSUPPORTED;
-  if (!aligned16(k_in) || !aligned16(k_out)) return FI_ERR_ALIGNMENT;
+  if (!aligned16(k_in) || !aligned16(k_out) || !aligned16(int_workspace_dev)) return FI_ERR_ALIGNMENT;
   for (int i = 0; i < 3; ++i)
     if (!stride_ok(k_in_strides[i]) || !stride_ok(k_out_strides[i])) return FI_ERR_ALIGNMENT;
-  if (info->batch == 0 || max_kv_len == 0) return FI_OK;
-  int lp = 0;
-  while ((1 << lp) < info->page_size) ++lp;
-  const dim3 grid(unsigned((max_kv_len + 63) / 64), unsigned(info->batch));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int32_t* iws = static_cast<const int32_t*>(int_workspace_dev);
-  const uint16_t* ki = static_cast<const uint16_t*>(k_in);
-  uint16_t* ko = static_cast<uint16_t*>(k_out);
-  if (dtype == FI_BF16)
-    rope_apply_k_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(iws, ki, k_in_strides[0], k_in_strides[1], k_in_strides[2],
-                                                            ko, k_out_strides[0], k_out_strides[1], k_out_strides[2],
-                                                            kv_indices_dev, lp, info->num_kv_heads);
-  else
-    rope_apply_k_kernel<__half><<<grid, 256, 0, s>>>(iws, ki, k_in_strides[0], k_in_strides[1], k_in_strides[2], ko,
-                                                     k_out_strides[0], k_out_strides[1], k_out_strides[2],
-                                                     kv_indices_dev, lp, info->num_kv_heads);
-  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+  if (info->batch == 0) return FI_OK;
+  const RopePass rp{static_cast<int32_t*>(int_workspace_dev), static_cast<const uint16_t*>(k_in),
+                    {k_in_strides[0], k_in_strides[1], k_in_strides[2]}, static_cast<uint16_t*>(k_out),
+                    {k_out_strides[0], k_out_strides[1], k_out_strides[2]}, kv_indices_dev, nullptr, 0, 0, nullptr,
+                    0, 0, log2_of(info->page_size), info->num_kv_heads, info->num_qo_heads,
+                    info->num_qo_heads / info->num_kv_heads, 1, 0, 0};
+  return launch_rope_pass(rp, dtype, false, info->num_ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FI_OK
+             : FI_ERR_CUDA;
+}
+
+extern "C" fi_status fi_rope_apply_q(const fi_plan_info* info, void* int_workspace_dev, const void* q_in,
+                                     int64_t q_in_stride_tok, int64_t q_in_stride_head, void* q_out,
+                                     int64_t q_out_stride_tok, int64_t q_out_stride_head, fi_dtype dtype,
+                                     void* stream) {
+  if (!info || !int_workspace_dev || !q_in || !q_out) return FI_ERR_INVALID_ARG;
+  if (!(info->variant & 4) || info->num_shared > 0) return FI_ERR_INVALID_ARG;
+  if (info->head_dim != kHeadDim) return FI_ERR_UNSUPPORTED;
+  if (dtype != FI_FP16 && dtype != FI_BF16) return FI_ERR_UNSUPPORTED;
+  if (!aligned16(q_in) || !aligned16(q_out) || !aligned16(int_workspace_dev)) return FI_ERR_ALIGNMENT;
+  if (!stride_ok(q_in_stride_tok) || !stride_ok(q_in_stride_head) || !stride_ok(q_out_stride_tok) ||
+      !stride_ok(q_out_stride_head))
+    return FI_ERR_ALIGNMENT;
+  if (info->batch == 0) return FI_OK;
+  const RopePass rp{static_cast<int32_t*>(int_workspace_dev), nullptr, {0, 0, 0}, nullptr, {0, 0, 0}, nullptr,
+                    static_cast<const uint16_t*>(q_in), q_in_stride_tok, q_in_stride_head,
+                    static_cast<uint16_t*>(q_out), q_out_stride_tok, q_out_stride_head, log2_of(info->page_size),
+                    info->num_kv_heads, info->num_qo_heads, info->num_qo_heads / info->num_kv_heads, 0, 1, 0};
+  return launch_rope_pass(rp, dtype, false, info->num_ctas, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FI_OK
+             : FI_ERR_CUDA;
 }
 
 extern "C" fi_status fi_merge_states(const void* v_a, const float* s_a, const void* v_b, const float* s_b,
@@ -682,7 +986,9 @@ extern "C" fi_status fi_get_device_status(const void* int_workspace_dev, void* s
                       cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return FI_ERR_CUDA;
-  *status_out = (word & kStatusTimeout) ? FI_ERR_TIMEOUT : (word & kStatusBadPlan) ? FI_ERR_DEVICE_CHECK : FI_OK;
+  *status_out = (word & kStatusTimeout)                   ? FI_ERR_TIMEOUT
+                : (word & (kStatusBadPlan | kStatusRange)) ? FI_ERR_DEVICE_CHECK
+                                                           : FI_OK;
   return FI_OK;
 }
 

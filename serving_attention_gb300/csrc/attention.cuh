@@ -87,6 +87,8 @@ struct RunParams {
   float scale_log2;          // sm_scale * log2(e)
   int32_t num_qo_heads, num_kv_heads, group;
   int32_t has_shared;        // kv[1] was given (a cascade run)
+  int32_t qk_prerotated;     // RoPE: tm_q and kv[0].tm_k read queries and keys of prefill-class requests
+                             // already rotated (fp16) by a pass before the run
   int32_t late_merge;        // the late merge launch follows this run (else late units merge in the run)
 };
 

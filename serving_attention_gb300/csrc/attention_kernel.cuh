@@ -277,9 +277,10 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 // rounded once to fp16 whatever the input type: fp16 keeps 11 significant
 // bits where bf16 keeps 8, and the rotated q and k meet only each other
 // (S = q.k), so the score does not carry a bf16 rounding of the rotation.
-// Rotated values must stay inside the fp16 range (|x| < 65504).  (TOut
-// other than fp16: the standalone rotation utility, which writes the cache's
-// own type.)
+// Rotated values must stay inside the fp16 range (|x| <= 65504): every role
+// and pass that rotates into fp16 keeps a running maximum (absmax_f16x8)
+// and records kStatusRange when it reaches inf.  (TOut other than fp16: the
+// standalone rotation utilities, which write the input's own type.)
 template <typename T, typename TOut = __half>
 __device__ __forceinline__ void rope_rotate8(uint4& lo, uint4& hi, const float2 (&cs)[8]) {
   float a[8], b[8];
@@ -293,6 +294,23 @@ __device__ __forceinline__ void rope_rotate8(uint4& lo, uint4& hi, const float2 
   }
   lo = pack8<TOut>(ra);
   hi = pack8<TOut>(rb);
+}
+
+// Range guard of the fp16 rotation: m = max(m, |x|) over the eight fp16
+// values of u (packed max; an input NaN is passed over, an overflow to inf
+// is kept), and whether a running maximum has reached inf.
+__device__ __forceinline__ void absmax_f16x8(__half2& m, const uint4& u) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __half2 h;
+    memcpy(&h, &w[k], 4);
+    m = __hmax2(m, __habs2(h));
+  }
+}
+
+__device__ __forceinline__ bool f16x2_has_inf(__half2 m) {
+  return __hisinf(__low2half(m)) != 0 || __hisinf(__high2half(m)) != 0;
 }
 
 // (cos, sin) of 8 consecutive frequencies of one position: 64 bytes of the table.
@@ -340,6 +358,7 @@ __device__ void rope_decode(const RunParams& p, RunSmem& sm, int32_t item_begin,
   const int c = rt & 7, g = rt >> 3;
   float2 step[8];
   rope_load8(step, var.rope_table + kGroups * FI_ROPE_PAIRS + 8 * c);
+  __half2 amax = __float2half2_rn(0.f);
   uint32_t it = 0;
   for (int32_t i = item_begin; i < item_end; ++i) {
     const Item item = load_item(p.iws, off_items, i);
@@ -369,6 +388,12 @@ __device__ void rope_decode(const RunParams& p, RunSmem& sm, int32_t item_begin,
           uint4 lo = *plo, hi = *phi, lo2 = *plo2, hi2 = *phi2;
           rope_rotate8<T>(lo, hi, cs);
           if (second) rope_rotate8<T>(lo2, hi2, cs2);
+          absmax_f16x8(amax, lo);
+          absmax_f16x8(amax, hi);
+          if (second) {
+            absmax_f16x8(amax, lo2);
+            absmax_f16x8(amax, hi2);
+          }
           *plo = lo;
           *phi = hi;
           if (second) {
@@ -385,6 +410,7 @@ __device__ void rope_decode(const RunParams& p, RunSmem& sm, int32_t item_begin,
       }
     }
   }
+  if (f16x2_has_inf(amax)) atomicOr(p.iws + FI_H_STATUS, kStatusRange);
 }
 
 template <typename T, bool kCap, bool kMask, bool kRope>
@@ -682,10 +708,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   const int32_t h_hq = ws_header(iws, FI_H_NUM_QO_HEADS), h_hkv = ws_header(iws, FI_H_NUM_KV_HEADS);
   const int32_t h_page = ws_header(iws, FI_H_PAGE_SIZE);
   const int32_t num_shared = ws_header(iws, FI_H_NUM_SHARED), h_spage = ws_header(iws, FI_H_SHARED_PAGE_SIZE);
+  // Pre-rotated operands without the RoPE instantiation: every item must be
+  // a tensor-core item (the CUDA-core path would read unrotated keys).
+  const int32_t h_dec = ws_header(iws, FI_H_NUM_DECODE_ITEMS);
   bool bad = magic != FI_PLAN_MAGIC || n_ctas != int32_t(gridDim.x) || (smem_u32(smem_raw) & 1023u) != 0 ||
              h_rows < 0 || h_rows > p.max_partial_rows || h_qo < 0 || h_qo > p.q_num_tokens ||
              h_hq != p.num_qo_heads || h_hkv != p.num_kv_heads || h_page != p.kv[0].page_size ||
-             num_shared < 0 || (num_shared > 0 && (!p.has_shared || h_spage != p.kv[1].page_size));
+             num_shared < 0 || (num_shared > 0 && (!p.has_shared || h_spage != p.kv[1].page_size)) ||
+             (!kRope && p.qk_prerotated && h_dec != 0);
   int32_t begin = 0, end = 0;
   if (!bad) {
     begin = __ldg(iws + off_cta + blockIdx.x);
@@ -753,12 +783,20 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
     // the loader warpgroup takes its share back after it.
     if (warp < kSoftmaxWarp0) {
       tc::setmaxnreg_dec<kRegsLoader>();
+      // With RoPE, warps 2 and 3 rotate Q and K tiles in shared memory and
+      // warp 0 loads all three operands -- unless a pass before the run has
+      // rotated them (then the plain roles, fp16 Q and K; a plan with no
+      // CUDA-core item then runs on the instantiation without RoPE)
+      const bool rot_roles = kRope && !p.qk_prerotated;
       if (warp == 0) {
-        pf_produce<kRope ? kProduceQKV : kProduceQK>(p, sm, begin, mid, off_items, off_req, num_shared);
+        if (rot_roles)
+          pf_produce<kProduceQKV>(p, sm, begin, mid, off_items, off_req, num_shared);
+        else
+          pf_produce<kProduceQK>(p, sm, begin, mid, off_items, off_req, num_shared);
       } else if (warp == kMmaWarp) {
         pf_mma<T, kRope>(p, sm, begin, mid, off_items);
         __syncwarp();
-      } else if (kRope) {
+      } else if (rot_roles) {
         pf_rope<T>(p, sm, begin, mid, off_items, off_req, var);  // warps 2 and 3
       } else if (warp == kVWarp) {
         pf_produce<kProduceV>(p, sm, begin, mid, off_items, off_req, num_shared);

@@ -31,8 +31,6 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <functional>
-#include <queue>
 #include <utility>
 #include <vector>
 
@@ -58,9 +56,15 @@ struct Chunk {
   int32_t fields[FI_ITEM_INTS];
 };
 
+// The deal's sort key of a chunk (the chunk itself stays where it is).
+struct DealKey {
+  int64_t cost;
+  int32_t tile, b, hk, qt, idx, pos;
+};
+
 // Order of the longest-processing-time deal: cost descending, then the
 // prefill class first, then (b, hk, q-tile, chunk) ascending.  Keys are unique.
-bool deal_before(const Chunk& x, const Chunk& y) {
+bool deal_before(const DealKey& x, const DealKey& y) {
   if (x.cost != y.cost) return x.cost > y.cost;
   if (x.tile != y.tile) return x.tile > y.tile;
   if (x.b != y.b) return x.b < y.b;
@@ -68,6 +72,31 @@ bool deal_before(const Chunk& x, const Chunk& y) {
   if (x.qt != y.qt) return x.qt < y.qt;
   return x.idx < y.idx;
 }
+
+// Min-heap of (load, CTA), ties to the lower CTA: the least-loaded CTA is at
+// the top, and giving it an item is one sift-down from the top.
+struct CtaHeap {
+  std::vector<std::pair<int64_t, int32_t>> h;
+  explicit CtaHeap(int32_t n) : h(size_t(n)) {
+    for (int32_t c = 0; c < n; ++c) h[size_t(c)] = {0, c};  // already a heap: equal loads, rising CTAs
+  }
+  int32_t top() const { return h[0].second; }
+  void add_to_top(int64_t cost) {
+    auto x = h[0];
+    x.first += cost;
+    const size_t n = h.size();
+    size_t i = 0;
+    while (true) {
+      size_t c = 2 * i + 1;
+      if (c >= n) break;
+      if (c + 1 < n && h[c + 1] < h[c]) ++c;
+      if (!(h[c] < x)) break;
+      h[i] = h[c];
+      i = c;
+    }
+    h[i] = x;
+  }
+};
 
 }  // namespace
 
@@ -118,8 +147,13 @@ fi_status read_level(const int32_t* qo_indptr, const int32_t* kv_indptr, const i
   }
   if (num_pages > 0 && batch > 0) {
     if (!kv_indices && kvp[batch] > 0) return FI_ERR_INVALID_ARG;
-    for (int32_t i = 0; i < kvp[batch]; ++i)
-      if (kv_indices[i] < 0 || kv_indices[i] >= num_pages) return FI_ERR_INVALID_ARG;
+    // one pass without early exit (it vectorises): every id in [0, num_pages),
+    // negative ids read as unsigned values past num_pages
+    uint32_t bad = 0;
+    const uint32_t* ids = reinterpret_cast<const uint32_t*>(kv_indices);
+    const uint32_t np = uint32_t(num_pages);
+    for (int32_t i = 0; i < kvp[batch]; ++i) bad |= uint32_t(ids[i] >= np);
+    if (bad) return FI_ERR_INVALID_ARG;
   }
   return FI_OK;
 }
@@ -160,6 +194,7 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
 
   // Units, in (b, hk, q-tile) order, and per-class visible-KV totals.
   std::vector<Unit> units;
+  units.reserve(size_t(batch) * num_kv_heads);
   std::vector<int32_t> first_unit(batch, -1);  // index of unit (b, 0, 0)
   int64_t total_dec = 0, total_pre = 0;
   for (int32_t b = 0; b < batch; ++b) {
@@ -321,19 +356,21 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
     return FI_ERR_CAPACITY;
 
   // Longest processing time first onto the least-loaded CTA (ties: lower CTA).
-  std::sort(chunks.begin(), chunks.end(), deal_before);
-  const int32_t C = cfg->num_ctas;
-  using Load = std::pair<int64_t, int32_t>;
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
-  for (int32_t c = 0; c < C; ++c) least.push(Load(0, c));
-  std::vector<int32_t> owner(chunks.size());
-  std::vector<int32_t> per_cta(C, 0);
+  std::vector<DealKey> order(chunks.size());
   for (size_t i = 0; i < chunks.size(); ++i) {
-    Load l = least.top();
-    least.pop();
-    owner[i] = l.second;
-    per_cta[l.second] += 1;
-    least.push(Load(l.first + chunks[i].cost, l.second));
+    const Chunk& c = chunks[i];
+    order[i] = DealKey{c.cost, c.tile, c.b, c.hk, c.qt, c.idx, int32_t(i)};
+  }
+  std::sort(order.begin(), order.end(), deal_before);
+  const int32_t C = cfg->num_ctas;
+  CtaHeap least(C);
+  std::vector<int32_t> owner(chunks.size());  // by position in `order`
+  std::vector<int32_t> per_cta(C, 0);
+  for (size_t i = 0; i < order.size(); ++i) {
+    const int32_t c = least.top();
+    owner[i] = c;
+    per_cta[c] += 1;
+    least.add_to_top(order[i].cost);
   }
 
   const int64_t off_cta = FI_HEADER_INTS;
@@ -357,10 +394,11 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
   int64_t n_decode = 0;
   for (int pass = 0; pass < 2; ++pass) {
     const int32_t tile = pass == 0 ? FI_TILE_PREFILL : FI_TILE_DECODE;
-    for (size_t i = 0; i < chunks.size(); ++i) {
-      if (chunks[i].tile != tile) continue;
+    for (size_t i = 0; i < order.size(); ++i) {
+      if (order[i].tile != tile) continue;
       const int32_t slot = fill[owner[i]]++;
-      std::memcpy(ws + off_items + int64_t(FI_ITEM_INTS) * slot, chunks[i].fields, sizeof chunks[i].fields);
+      const Chunk& c = chunks[size_t(order[i].pos)];
+      std::memcpy(ws + off_items + int64_t(FI_ITEM_INTS) * slot, c.fields, sizeof c.fields);
       if (tile == FI_TILE_DECODE) ++n_decode;
     }
   }
@@ -388,7 +426,7 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
       window,               sink,               cap_bits,           rope_max,
       theta_bits,           scale_bits,         rope_off,           n_late,
       int32_t(partial_rows), total_qo,          num_shared,         cascade ? int32_t(off_cascade) : 0,
-      int32_t(n_cascade),   cascade ? shared_page_size : 0, 0,      0};
+      int32_t(n_cascade),   cascade ? shared_page_size : 0, int32_t(n_decode), 0};
   std::memcpy(ws, header, sizeof header);
 
   fi_plan_info info;

@@ -158,9 +158,12 @@ __device__ void pf_produce(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
   __syncwarp();
 }
 
+// Out of line: inlined into the kernel body, this role's code slowed the
+// other tensor-core roles of the RoPE instantiation by about 9% even in
+// runs where it does not execute (operands rotated by a pass).
 template <typename T>
-__device__ void pf_rope(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items, int32_t off_req,
-                        const Variant& var) {
+__device__ __noinline__ void pf_rope(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items,
+                                     int32_t off_req, const Variant var) {
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   // Warps 2 and 3 (the loads all go through warp 0 with RoPE).  Lane = (8-
@@ -170,12 +173,15 @@ __device__ void pf_rope(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1,
   const int c = lane & 7, g = (lane >> 3) + 4 * ((threadIdx.x >> 5) - kVWarp);
   float2 step[8];
   rope_load8(step, var.rope_table + kStride * FI_ROPE_PAIRS + 8 * c);
+  __half2 amax = __float2half2_rn(0.f);
   auto rotate_row = [&](uint16_t* lo_half, uint16_t* hi_half, int row, const float2 (&cs)[8]) {
     const int pc = c ^ (row & 7);  // swizzled position of 16-byte chunk c
     uint4* plo = reinterpret_cast<uint4*>(lo_half + row * 64 + pc * 8);
     uint4* phi = reinterpret_cast<uint4*>(hi_half + row * 64 + pc * 8);
     uint4 lo = *plo, hi = *phi;
     rope_rotate8<T>(lo, hi, cs);
+    absmax_f16x8(amax, lo);
+    absmax_f16x8(amax, hi);
     *plo = lo;
     *phi = hi;
   };
@@ -230,13 +236,15 @@ __device__ void pf_rope(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1,
       if (lane == 0) mbar_arrive(&sm.k_rot[st]);
     }
   }
+  if (f16x2_has_inf(amax)) atomicOr(p.iws + FI_H_STATUS, kStatusRange);
 }
 
 template <typename T, bool kRope>
 __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, int32_t off_items) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-  // rotated Q and K (RoPE) are fp16 whatever the input type; P and V keep it
-  constexpr uint32_t idesc_qk = tc::idesc_f16(kBf16 && !kRope, false, kTileM, kTileN);
+  // rotated Q and K (RoPE, in the kernel or by a pass before it) are fp16
+  // whatever the input type; P and V keep it
+  const uint32_t idesc_qk = tc::idesc_f16(kBf16 && !kRope && !p.qk_prerotated, false, kTileM, kTileN);
   constexpr uint32_t idesc_pv = tc::idesc_f16(kBf16, true, kTileM, kHeadDim);
   const int lane = threadIdx.x & 31;
   const uint32_t tmem = sm.tmem_base;
@@ -280,8 +288,10 @@ __device__ void pf_mma(const RunParams& p, RunSmem& sm, int32_t b0, int32_t b1, 
     if (ntiles == 0) continue;
     const int nm = item_m_tiles(it);
     // with RoPE the operands are read once the rotation warp has released them
-    uint64_t* const q_bar = kRope ? &sm.q_rot : &sm.q_full;
-    uint64_t* const k_bars = kRope ? sm.k_rot : sm.k_full;
+    // (operands rotated by a pass before the run arrive ready: the plain waits)
+    const bool rot_roles = kRope && !p.qk_prerotated;
+    uint64_t* const q_bar = rot_roles ? &sm.q_rot : &sm.q_full;
+    uint64_t* const k_bars = rot_roles ? sm.k_rot : sm.k_full;
     bool ok = warp_wait_all(2, q_bar, pe & 1, &k_bars[kt & 1], (kt >> 1) & 1, nullptr, 0, nullptr, 0, &sm.abort);
     if (!ok) break;
     tc::fence_after_sync();

@@ -7,8 +7,9 @@
 
 namespace fi {
 
-// Device status bits, OR-ed into the int workspace's status word.
-enum : int32_t { kStatusTimeout = 1, kStatusBadPlan = 2 };
+// Device status bits, OR-ed into the int workspace's status word
+// (kStatusRange: a value rotated into fp16 left the fp16 range).
+enum : int32_t { kStatusTimeout = 1, kStatusBadPlan = 2, kStatusRange = 4 };
 
 // A bounded wait gives up after this many SM clocks (about half a second at
 // 2 GHz) and reports kStatusTimeout instead of hanging the GPU.

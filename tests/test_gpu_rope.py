@@ -104,7 +104,7 @@ def test_unfused_rotation_utility():
     ws = fi.Workspace(cfg, device=DEV)
     info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 0, b.num_pages)
     k_rot = torch.zeros_like(b.k)
-    fi.rope_apply_k(ws, info, b.k, k_rot, torch.as_tensor(b.kv_indices, device=DEV), int(b.kv_lens().max()))
+    fi.rope_apply_k(ws, info, b.k, k_rot, torch.as_tensor(b.kv_indices, device=DEV))
     torch.cuda.synchronize()
     k64, r64 = b.k.double().cpu().numpy(), k_rot.double().cpu().numpy()
     freq = 10000.0 ** (-2.0 * np.arange(64) / 128)
@@ -119,3 +119,188 @@ def test_unfused_rotation_utility():
             want = np.concatenate([x0 * c - x1 * sn, x1 * c + x0 * sn], axis=-1)
             assert np.all(np.abs(r64[pg, sl] - want) <= 2.0 ** -8 * np.abs(want) + 1e-30), (r, j)
     assert np.all(r64[~used] == 0)
+
+
+def _rotated64(x64, pos, theta=10000.0):
+    """fp64 RoPE of rows x64[..., 128] at positions pos (broadcast over the leading axes)."""
+    ang = np.asarray(pos, np.float64)[..., None] * theta ** (-2.0 * np.arange(64) / 128)
+    c, sn = np.cos(ang), np.sin(ang)
+    while c.ndim < x64.ndim:
+        c, sn = c[..., None, :], sn[..., None, :]
+    x0, x1 = x64[..., :64], x64[..., 64:]
+    return np.concatenate([x0 * c - x1 * sn, x1 * c + x0 * sn], axis=-1)
+
+
+def test_unfused_query_rotation_utility():
+    """fi_rope_apply_q rotates every query row (token t of a request at
+    kv_len - qo_len + t), each element within one bf16 rounding of the fp64
+    rotation; in place it gives the same bits as into a copy."""
+    b = workloads.random_batch(452, batch=5, qo_max=40, kv_max=900, num_qo_heads=8, num_kv_heads=2, page_size=16,
+                               causal=1, device=DEV, kv_min=40)
+    ws = fi.Workspace(_cfg(2048), device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    q_rot = torch.zeros_like(b.q)
+    fi.rope_apply_q(ws, info, b.q, q_rot)
+    q_in_place = b.q.clone()
+    fi.rope_apply_q(ws, info, q_in_place, q_in_place)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0
+    assert torch.equal(q_rot, q_in_place)
+    q64, r64 = b.q.double().cpu().numpy(), q_rot.double().cpu().numpy()
+    kv = b.kv_lens()
+    for r in range(b.batch):
+        q0, q1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
+        pos = int(kv[r]) - (q1 - q0) + np.arange(q1 - q0)
+        want = _rotated64(q64[q0:q1], pos)
+        assert np.all(np.abs(r64[q0:q1] - want) <= 2.0 ** -8 * np.abs(want) + 1e-5), r
+
+
+def test_rotation_utilities_past_the_list_capacity():
+    """More requests than a rotation CTA lists in shared memory (1024): the
+    passes walk the whole request table instead, with the same results --
+    every key and query row against the fp64 rotation."""
+    b = workloads.random_batch(453, batch=1100, qo_max=2, kv_max=40, num_qo_heads=8, num_kv_heads=2, page_size=16,
+                               causal=1, device=DEV, kv_min=2)
+    ws = fi.Workspace(_cfg(2048), device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    k_rot, q_rot = torch.zeros_like(b.k), torch.zeros_like(b.q)
+    fi.rope_apply_k(ws, info, b.k, k_rot, kvi)
+    fi.rope_apply_q(ws, info, b.q, q_rot)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0
+    k64, kr = b.k.double().cpu().numpy(), k_rot.double().cpu().numpy()
+    q64, qr = b.q.double().cpu().numpy(), q_rot.double().cpu().numpy()
+    kv = b.kv_lens()
+    pg, sl, pos, tok, qpos = [], [], [], [], []
+    for r in range(b.batch):
+        pages = b.kv_indices[b.kv_indptr[r]:b.kv_indptr[r + 1]]
+        j = np.arange(int(kv[r]))
+        pg.append(pages[j // 16]); sl.append(j % 16); pos.append(j)
+        q0, q1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
+        tok.append(np.arange(q0, q1)); qpos.append(int(kv[r]) - (q1 - q0) + np.arange(q1 - q0))
+    pg, sl, pos = np.concatenate(pg), np.concatenate(sl), np.concatenate(pos)
+    tok, qpos = np.concatenate(tok), np.concatenate(qpos)
+    want_k, want_q = _rotated64(k64[pg, sl], pos), _rotated64(q64[tok], qpos)
+    assert np.all(np.abs(kr[pg, sl] - want_k) <= 2.0 ** -8 * np.abs(want_k) + 1e-5)
+    assert np.all(np.abs(qr[tok] - want_q) <= 2.0 ** -8 * np.abs(want_q) + 1e-5)
+
+
+def _prerotated_pass_check(b, q_rot, k_rot):
+    """The pass wrote the fp16 rotation (one fp16 rounding of the fp64 value;
+    1e-5 absolute covers the fp32 arithmetic where the two products cancel)
+    of exactly the prefill-class requests' query
+    rows and keys, and left every other element of both buffers alone."""
+    q64, k64 = b.q.double().cpu().numpy(), b.k.double().cpu().numpy()
+    qr, kr = q_rot.double().cpu().numpy(), k_rot.double().cpu().numpy()
+    kv, G = b.kv_lens(), b.num_qo_heads // b.num_kv_heads
+    q_seen = np.zeros(qr.shape[0], bool)
+    k_seen = np.zeros(kr.shape[:2], bool)
+    for r in range(b.batch):
+        q0, q1 = int(b.qo_indptr[r]), int(b.qo_indptr[r + 1])
+        if (q1 - q0) * G <= 16:
+            continue
+        pos = int(kv[r]) - (q1 - q0) + np.arange(q1 - q0)
+        want = _rotated64(q64[q0:q1], pos)
+        assert np.all(np.abs(qr[q0:q1] - want) <= 2.0 ** -10 * np.abs(want) + 1e-5), r
+        q_seen[q0:q1] = True
+        pages = b.kv_indices[b.kv_indptr[r]:b.kv_indptr[r + 1]]
+        for j in range(int(kv[r])):
+            pg, sl = int(pages[j // b.page_size]), j % b.page_size
+            want = _rotated64(k64[pg, sl], j)
+            assert np.all(np.abs(kr[pg, sl] - want) <= 2.0 ** -10 * np.abs(want) + 1e-5), (r, j)
+            k_seen[pg, sl] = True
+    assert np.isnan(qr[~q_seen]).all() and np.isnan(kr[~k_seen]).all()
+
+
+@pytest.mark.parametrize("qo,kv,causal,dtype", [
+    ([100], [900], 1, "bf16"),           # 400 rows: two items sharing the pre-rotated keys
+    ([64, 33, 1, 1], [1000, 40, 700, 300], 1, "bf16"),  # prefill-class and decode-class requests in one batch
+    ([40], [300], 0, "fp16"),
+])
+def test_rope_prerotated_keys(qo, kv, causal, dtype):
+    """Queries and keys of prefill-class requests rotated once into fp16
+    copies before the kernel (the tensor cores read them there), decode-class
+    requests rotated inside the kernel: against the oracle, and close to the fully
+    fused run (the two walk the cos/sin table differently, so the fp16 keys
+    may differ in their last bit)."""
+    b = workloads.make_batch("tcp", dtype, qo, kv, 8, 2, 16, causal, 600 + kv[0], DEV,
+                             pool_pages=sum((k + 15) // 16 for k in kv) + 2)
+    cfg = _cfg(4096)
+    ws = fi.Workspace(cfg, device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, causal, b.num_pages)
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    k_rot = torch.full(b.k.shape, float("nan"), dtype=torch.float16, device=DEV)
+    q_rot = torch.full(b.q.shape, float("nan"), dtype=torch.float16, device=DEV)
+    o = torch.full_like(b.q, float("nan"))
+    lse = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    fi.run_rope_prerotated(ws, info, b.q, b.k, b.v, kvi, q_rot, k_rot, o, lse, b.sm_scale)
+    o_f = torch.full_like(b.q, float("nan"))
+    l_f = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    fi.run(ws, info, b.q, b.k, b.v, kvi, o_f, l_f, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0 and info.num_prefill_items > 0
+    o_ref, l_ref = oracle.attention(oracle_problem(b, rope=1))
+    n = b.total_qo
+    err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
+    assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
+    assert float((o[:n].float() - o_f[:n].float()).abs().max()) <= O_TOL
+    assert float((lse[:n] - l_f[:n]).abs().max()) <= LSE_TOL
+    _prerotated_pass_check(b, q_rot, k_rot)
+
+
+def test_rope_prerotated_refuses_a_replanned_workspace_with_cuda_core_items():
+    """A plan whose items all run on the tensor cores sends the pre-rotated
+    run to the kernel without RoPE; if the workspace has since been re-planned
+    with decode-class items (which only the RoPE kernel rotates), the kernel
+    records FI_ERR_DEVICE_CHECK and writes nothing."""
+    qo, kv = [64, 1], [1000, 300]
+    b = workloads.make_batch("tcx", "bf16", qo, kv, 8, 2, 16, 1, 611, DEV, pool_pages=sum((k + 15) // 16 for k in kv) + 2)
+    ws = fi.Workspace(_cfg(4096), device=DEV)
+    qo_a, kv_a = np.array([0, 64], np.int32), np.array([0, 63], np.int32)  # request 0 alone: 256 rows
+    info_a = fi.plan(ws, qo_a, kv_a, b.kv_indices[:63], np.array([1000 - 62 * 16], np.int32), 8, 2, 128, 16, 1,
+                     b.num_pages)
+    assert info_a.num_decode_items == 0
+    info_b = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    assert info_b.num_decode_items > 0
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    k_rot = torch.zeros(b.k.shape, dtype=torch.float16, device=DEV)
+    q_rot = torch.zeros(b.q.shape, dtype=torch.float16, device=DEV)
+    o = torch.full_like(b.q, float("nan"))
+    lse = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    fi.run_rope_prerotated(ws, info_a, b.q, b.k, b.v, kvi, q_rot, k_rot, o, lse, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 6  # FI_ERR_DEVICE_CHECK
+    assert torch.isnan(o).all() and torch.isnan(lse).all()
+
+
+@pytest.mark.parametrize("path", ["fused", "prerotated"])
+def test_rope_fp16_range_guard(path):
+    """A bf16 key whose rotation leaves the fp16 range (bf16 holds 1.5e5,
+    fp16 tops out at 65504) is reported as FI_ERR_DEVICE_CHECK by the role or
+    pass that rotated it; the same batch in range reports nothing."""
+    qo, kv = [64], [500]
+    b = workloads.make_batch("tcg", "bf16", qo, kv, 8, 2, 16, 1, 612, DEV, pool_pages=(500 + 15) // 16 + 2)
+    ws = fi.Workspace(_cfg(4096), device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    k_rot = torch.zeros(b.k.shape, dtype=torch.float16, device=DEV)
+    q_rot = torch.zeros(b.q.shape, dtype=torch.float16, device=DEV)
+    o = torch.empty_like(b.q)
+    lse = torch.empty(b.q.shape[:2], dtype=torch.float32, device=DEV)
+
+    def go():
+        if path == "fused":
+            fi.run(ws, info, b.q, b.k, b.v, kvi, o, lse, b.sm_scale)
+        else:
+            fi.run_rope_prerotated(ws, info, b.q, b.k, b.v, kvi, q_rot, k_rot, o, lse, b.sm_scale)
+        torch.cuda.synchronize()
+        return fi.device_status(ws)
+
+    assert go() == 0
+    page = int(b.kv_indices[3])
+    b.k[page, 5, 1, 7] = 1.5e5  # key 53 of the request, KV head 1, dim 7
+    assert go() == 6
+    fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    b.k[page, 5, 1, 7] = 1.0
+    assert go() == 0  # a new plan clears the status word
