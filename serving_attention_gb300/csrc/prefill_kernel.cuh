@@ -394,11 +394,16 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         tc::tmem_ld_wait();
         const int kbase = item.kv0 + j * kTileN;
         if (kCap) {  // capped log2-domain logits; the mask below then works on them
+          const float kb = c * var.cap_b;
 #pragma unroll
           for (int h = 0; h < 4; ++h)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              sv[h][e] = __float_as_uint(soft_cap_log2(__uint_as_float(sv[h][e]) * c, var.cap_a, var.cap_b));
+            for (int e = 0; e < 32; e += 2) {
+              const float2 v =
+                  soft_cap_log2_x2(make_float2(__uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1])), kb, var.cap_a);
+              sv[h][e] = __float_as_uint(v.x);
+              sv[h][e + 1] = __float_as_uint(v.y);
+            }
         }
         if (kbase + kTileN - 1 > lim || (kMask && kbase < lo)) {  // causal diagonal, chunk end, padding row, window
 #pragma unroll

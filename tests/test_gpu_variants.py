@@ -98,3 +98,21 @@ def test_windowed_ragged_prefill_sampled():
     err_o, err_l = compare(o[torch.as_tensor(rr), torch.as_tensor(hh)], lse[torch.as_tensor(rr), torch.as_tensor(hh)],
                            o_ref, l_ref)
     assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
+
+
+def test_soft_cap_extreme_logits():
+    """Soft-cap on logits far past the cap (keys scaled by 1e4, |y| well above
+    the exponential's range of 126) and exactly zero: the capped logits sit
+    at +-cap, and O and LSE still meet the bar against the oracle."""
+    b = workloads.make_batch("capx", "bf16", [64, 3], [300, 40], 8, 2, 16, 1, 733, DEV,
+                             pool_pages=(300 + 15) // 16 + (40 + 15) // 16 + 2)
+    b.k.mul_(1.0e4)
+    b.k[:, 3].zero_()  # slot 3 of every page: logit exactly 0
+    cfg = fi.default_plan_config(0, logits_soft_cap=30.0)
+    o, lse, info, ws = gpu_run(b, cfg=cfg)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0 and info.num_prefill_items > 0
+    o_ref, l_ref = oracle.attention(oracle_problem(b, -1, 0, 30.0))
+    n = b.total_qo
+    err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
+    assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
