@@ -58,7 +58,7 @@ def _kernel_hash() -> str:
     files build other kernels and are left out)."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "serving_attention_gb300", "csrc", "*"))):
-        if os.path.basename(f).startswith("mla"):
+        if os.path.basename(f).startswith("mla") or not os.path.isfile(f):
             continue
         with open(f, "rb") as fh:
             h.update(fh.read())
@@ -872,6 +872,7 @@ def _shared_prefix_runs(dev):
 PROFILE_CASES = {
     "llama8b_decode": lambda dev: __import__("workloads").llama8b_decode(device=dev),
     "llama8b_decode_16": lambda dev: __import__("workloads").llama8b_decode(device=dev, batch=16),
+    "tiny_decode": lambda dev: __import__("workloads").tiny_decode(device=dev),
     "ragged_prefill": lambda dev: __import__("workloads").ragged_prefill(device=dev),
     "ragged_prefill_4": lambda dev: __import__("workloads").ragged_prefill(device=dev, batch=4),
     "continuous_batch": lambda dev: __import__("workloads").continuous_batch(device=dev),
