@@ -417,7 +417,7 @@ fi_status fi_batch_paged_attention_run_cascade(
  * array never written past its end).
  *
  * The first call on a device looks up the array's device address on that
- * device (the current one); make that first call before any stream capture.
+ * device (the current one).
  * All calls share the one array and it keeps the last call's contents;
  * nothing in it has to start at zero (every partial row is written before it
  * is read; the merge counters live in the int workspace).  Calls whose
