@@ -104,3 +104,46 @@ def test_mla_run_rejects_bad_arguments_before_cuda():
     bad[0] = ctypes.byref(info_split)
     bad[20] = None
     assert lib.fi_mla_decode_run(*bad) == 1                     # split chunks need the float workspace
+
+
+def test_rope_utilities_reject_bad_arguments_before_cuda():
+    """The rotation passes refuse, before any CUDA call: a plan without RoPE,
+    a cascade plan (two caches), misaligned buffers and unsupported types."""
+    lib = fi.load()
+    rope = fi.PlanInfo(num_ctas=1, batch=1, head_dim=128, page_size=16, num_qo_heads=8, num_kv_heads=2, variant=4)
+    plain = fi.PlanInfo(num_ctas=1, batch=1, head_dim=128, page_size=16, num_qo_heads=8, num_kv_heads=2, variant=0)
+    cascade = fi.PlanInfo(num_ctas=1, batch=2, head_dim=128, page_size=16, num_qo_heads=8, num_kv_heads=2,
+                          variant=4, num_shared=1)
+    ks = (ctypes.c_int64 * 3)(4096, 256, 128)
+    # fake pointers: every case returns before touching memory
+    assert lib.fi_rope_apply_k(ctypes.byref(plain), 16, 32, ks, 48, ks, 64, fi.BF16, None) == 1
+    assert lib.fi_rope_apply_k(ctypes.byref(cascade), 16, 32, ks, 48, ks, 64, fi.BF16, None) == 1
+    assert lib.fi_rope_apply_k(ctypes.byref(rope), 16, 34, ks, 48, ks, 64, fi.BF16, None) == 4
+    assert lib.fi_rope_apply_k(ctypes.byref(rope), 16, 32, ks, 48, ks, 64, fi.FP32, None) == 2
+    assert lib.fi_rope_apply_q(ctypes.byref(plain), 16, 32, 1024, 128, 48, 1024, 128, fi.BF16, None) == 1
+    assert lib.fi_rope_apply_q(ctypes.byref(cascade), 16, 32, 1024, 128, 48, 1024, 128, fi.BF16, None) == 1
+    assert lib.fi_rope_apply_q(ctypes.byref(rope), 16, 32, 1020, 128, 48, 1024, 128, fi.BF16, None) == 4
+    assert lib.fi_rope_apply_q(ctypes.byref(rope), None, 32, 1024, 128, 48, 1024, 128, fi.BF16, None) == 1
+
+
+def test_prerotated_run_rejects_bad_arguments_before_cuda():
+    """The pre-rotated run needs a RoPE plan and both rotation buffers, and
+    refuses a cascade plan (it reads one cache)."""
+    lib = fi.load()
+    ks = (ctypes.c_int64 * 3)(4096, 256, 128)
+
+    def call(info, q_rot=208, k_rot=224):
+        return lib.fi_batch_paged_attention_run_rope_prerotated(
+            ctypes.byref(info), 16, 1024, 128, 4, 32, ks, 64, ks, 10, 48, q_rot, 1024, 128, k_rot, ks, 80, 1024, 128,
+            None, fi.BF16, 0.1, 96, 112, None)
+
+    rope = fi.PlanInfo(num_ctas=1, batch=1, head_dim=128, page_size=16, num_qo_heads=8, num_kv_heads=2, variant=4)
+    plain = fi.PlanInfo(num_ctas=1, batch=1, head_dim=128, page_size=16, num_qo_heads=8, num_kv_heads=2, variant=0)
+    cascade = fi.PlanInfo(num_ctas=1, batch=2, head_dim=128, page_size=16, num_qo_heads=8, num_kv_heads=2,
+                          variant=4, num_shared=1)
+    assert call(rope, q_rot=None) == 1
+    assert call(rope, k_rot=None) == 1
+    assert call(cascade) == 1
+    # (a plan without RoPE and misaligned rotation buffers are refused after
+    # the tensor maps are built, which needs the CUDA driver: GPU tests)
+    del plain
