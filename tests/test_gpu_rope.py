@@ -304,3 +304,28 @@ def test_rope_fp16_range_guard(path):
     fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
     b.k[page, 5, 1, 7] = 1.0
     assert go() == 0  # a new plan clears the status word
+
+
+def test_prerotated_run_refusals():
+    """A plan made without RoPE, or rotation buffers off the 16-byte grid, are
+    refused on the host before anything is enqueued (outputs untouched)."""
+    b = workloads.make_batch("tcr2", "bf16", [40], [300], 8, 2, 16, 1, 613, DEV, pool_pages=(300 + 15) // 16 + 2)
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    o = torch.full_like(b.q, float("nan"))
+    lse = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    k_rot = torch.zeros(b.k.shape, dtype=torch.float16, device=DEV)
+    q_rot = torch.zeros(b.q.shape, dtype=torch.float16, device=DEV)
+    ws_p = fi.Workspace(fi.default_plan_config(0), device=DEV)
+    info_p = fi.plan(ws_p, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    with pytest.raises(fi.FIError) as e:
+        fi.run_rope_prerotated(ws_p, info_p, b.q, b.k, b.v, kvi, q_rot, k_rot, o, lse, b.sm_scale)
+    assert e.value.status == 1
+    ws_r = fi.Workspace(_cfg(4096), device=DEV)
+    info_r = fi.plan(ws_r, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    flat = torch.zeros(k_rot.numel() + 8, dtype=torch.float16, device=DEV)
+    k_off = flat[1:1 + k_rot.numel()].view(k_rot.shape)  # 2 bytes off the 16-byte grid
+    with pytest.raises(fi.FIError) as e:
+        fi.run_rope_prerotated(ws_r, info_r, b.q, b.k, b.v, kvi, q_rot, k_off, o, lse, b.sm_scale)
+    assert e.value.status == 4
+    torch.cuda.synchronize()
+    assert torch.isnan(o).all()
