@@ -429,9 +429,10 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
 
   // Items in the order dealt; each pass of an item loads its query rows,
   // streams the item's KV stages and combines the half-warps' states.
-  // (Loading the next item's descriptor a whole item ahead, or splitting the
-  // combine's loop over the idle lanes, measured slower on the decode
-  // workloads: the added live registers cost more than the latency saved.)
+  // (Loading the next item's descriptor a whole item ahead, its query rows
+  // before this item's combine, or splitting the combine's loop over the
+  // idle lanes, measured slower on some of the workloads: the added live
+  // registers spill, which costs more than the latency saved.)
   for (int32_t i = item_begin; i < item_end; ++i) {
     const Item item = load_item(p.iws, off_items, i);
     const Request& rq = item.rq;
@@ -455,6 +456,18 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
       // for the packed fp32 FMA (dims 2i, 2i+1 of this lane's 8).
       float2 q[kRowsPerGroup][4];
       int lim_mine = -1, lo_mine = 0;  // this lane's row: visible keys [lo, lim] (and the sink)
+      // The group's row loads go out together, before any of them is used
+      // (inside the per-row branch below they were issued one after another).
+      uint4 qraw[kRowsPerGroup];
+#pragma unroll
+      for (int r = 0; r < kRowsPerGroup; ++r) {
+        const int prow = prow0 + g * kRowsPerGroup + r;
+        const int row = item.row0 + (prow < nrows ? prow : 0);
+        const int t = row / G;
+        const int head = item.hk * G + (row - t * G);
+        qraw[r] = __ldg(reinterpret_cast<const uint4*>(p.q + int64_t(rq.qo_start + t) * p.q_stride_tok +
+                                                       int64_t(head) * p.q_stride_head + L * 8));
+      }
 #pragma unroll
       for (int r = 0; r < kRowsPerGroup; ++r) {
         const int prow = prow0 + g * kRowsPerGroup + r;
@@ -462,10 +475,7 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
         if (prow < nrows) {
           const int row = item.row0 + prow;
           const int t = row / G;
-          const int head = item.hk * G + (row - t * G);
-          const uint4 u = __ldg(reinterpret_cast<const uint4*>(
-              p.q + int64_t(rq.qo_start + t) * p.q_stride_tok + int64_t(head) * p.q_stride_head + L * 8));
-          unpack4x2<T>(u, q[r]);
+          unpack4x2<T>(qraw[r], q[r]);
 #pragma unroll
           for (int c = 0; c < 4; ++c) q[r][c] = make_float2(q[r][c].x * p.scale_log2, q[r][c].y * p.scale_log2);
           lim = causal_i ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1;
