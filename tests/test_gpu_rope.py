@@ -329,3 +329,39 @@ def test_prerotated_run_refusals():
     assert e.value.status == 4
     torch.cuda.synchronize()
     assert torch.isnan(o).all()
+
+
+@pytest.mark.parametrize("page,qo,kv", [
+    (8, [64, 0, 40], [300, 100, 200]),        # a request with no query rows (nothing to rotate for it)
+    (64, [33, 5, 100], [1000, 700, 100]),     # pages of 64: a 32-row pass unit spans half a page
+    (32, [20, 1, 48], [20, 600, 48]),         # qo_len == kv_len: positions start at 0
+])
+def test_rope_prerotated_page_sizes(page, qo, kv):
+    """The pre-rotation pass at other page sizes and with empty or exactly
+    causal requests: against the oracle, and its buffers hold exactly the
+    fp16 rotation of the prefill-class rows and keys.  Outputs here reach
+    |o| > 2, where half an ulp of the stored bf16 value (2^-7 = 0.0078) is
+    nearly the whole flat bar by itself and the fp16 rounding of the rotated
+    q and k adds about 5e-4: above |o| = 2 the bar adds the storage rounding
+    (2^-8 |o_ref|), as the peaked-softmax parity test does above 4; below 2
+    it is the flat 8e-3.  (The fully fused run gives the same bits.)"""
+    b = workloads.make_batch("tcq", "bf16", qo, kv, 8, 2, page, 1, 620 + page, DEV,
+                             pool_pages=sum((k + page - 1) // page for k in kv) + 2)
+    ws = fi.Workspace(_cfg(4096), device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, page, 1, b.num_pages)
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    k_rot = torch.full(b.k.shape, float("nan"), dtype=torch.float16, device=DEV)
+    q_rot = torch.full(b.q.shape, float("nan"), dtype=torch.float16, device=DEV)
+    o = torch.full_like(b.q, float("nan"))
+    lse = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    fi.run_rope_prerotated(ws, info, b.q, b.k, b.v, kvi, q_rot, k_rot, o, lse, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0 and info.num_prefill_items > 0
+    o_ref, l_ref = oracle.attention(oracle_problem(b, rope=1))
+    n = b.total_qo
+    err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
+    assert err_l <= LSE_TOL, err_l
+    err = np.abs(o[:n].float().cpu().numpy() - o_ref)
+    bar = np.where(np.abs(o_ref) < 2.0, O_TOL, O_TOL + 2.0 ** -8 * np.abs(o_ref))
+    assert (err <= bar).all(), float((err - bar).max())
+    _prerotated_pass_check(b, q_rot, k_rot)
