@@ -365,3 +365,28 @@ def test_rope_prerotated_page_sizes(page, qo, kv):
     bar = np.where(np.abs(o_ref) < 2.0, O_TOL, O_TOL + 2.0 ** -8 * np.abs(o_ref))
     assert (err <= bar).all(), float((err - bar).max())
     _prerotated_pass_check(b, q_rot, k_rot)
+
+
+@pytest.mark.parametrize("qo,kv", [([64, 40], [900, 300]), ([64, 1, 40], [900, 500, 300])])
+def test_rope_prerotated_with_window_sink_cap(qo, kv):
+    """The pre-rotated run on a plan with RoPE, a sliding window, sinks and a
+    soft-cap: all tensor-core items (the kernel without RoPE, cap and mask
+    kept) and with a decode-class request (the full RoPE kernel)."""
+    b = workloads.make_batch("tcw", "bf16", qo, kv, 8, 2, 16, 1, 640 + len(qo), DEV,
+                             pool_pages=sum((k + 15) // 16 for k in kv) + 2)
+    cfg = _cfg(4096, window_left=200, sink_tokens=4, logits_soft_cap=30.0)
+    ws = fi.Workspace(cfg, device=DEV)
+    info = fi.plan(ws, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 128, 16, 1, b.num_pages)
+    assert info.variant == 7
+    kvi = torch.as_tensor(b.kv_indices, device=DEV)
+    k_rot = torch.zeros(b.k.shape, dtype=torch.float16, device=DEV)
+    q_rot = torch.zeros(b.q.shape, dtype=torch.float16, device=DEV)
+    o = torch.full_like(b.q, float("nan"))
+    lse = torch.full(b.q.shape[:2], float("nan"), dtype=torch.float32, device=DEV)
+    fi.run_rope_prerotated(ws, info, b.q, b.k, b.v, kvi, q_rot, k_rot, o, lse, b.sm_scale)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0
+    o_ref, l_ref = oracle.attention(oracle_problem(b, 200, 4, 30.0, rope=1))
+    n = b.total_qo
+    err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
+    assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
