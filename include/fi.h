@@ -193,6 +193,12 @@ fi_status fi_rope_apply_q(const fi_plan_info* info, void* int_workspace_dev, con
  * Supported: head_dim == 128; page_size a power of two in [1, 128];
  * num_qo_heads % num_kv_heads == 0 with group size <= 16.
  *
+ * Work units are (request, KV head, tile of packed query rows), split into
+ * KV chunks.  With page_size 1, no RoPE and a group size G in {4, 8, 16}
+ * whose 32 / G divides num_kv_heads, a one-token request's units take 32 / G
+ * KV heads at once (32 packed rows): such a unit pays the per-item cost once
+ * for all its heads and each token of its KV arrives in one copy.
+ *
  * pinned_staging_host: caller-owned pinned host buffer of at least
  * fi_int_workspace_bytes(cfg) bytes; the plan is written there and copied
  * from there asynchronously, so it must not be reused until the copy on

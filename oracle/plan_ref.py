@@ -25,9 +25,16 @@ Rule:
     class granule (below); if lo <= min(S, hi) one range [0, hi), else the
     sink range [0, min(S, hi)) (when not empty) followed by [lo, hi).
     kv_eff = the summed length of the ranges.
- 3. Per class, total = sum of kv_eff; chunk = max(min_chunk,
+    Multi-head units: when Lq = 1, the request reads the plan's own cache,
+    the page size is 1, there is no RoPE, G is a multiple of 4 with G <= 16
+    and H = 32 / G divides Hkv, the decode-class units are (b, hk) for hk a
+    multiple of H, each taking KV heads hk .. hk + H - 1 at once: 32 rows,
+    row = h * G + g for head hk + h, all of query token 0.
+ 3. Per class, total = sum of kv_eff (times H for a multi-head unit); chunk = max(min_chunk,
     ceil(total / (num_ctas * split_factor))) rounded up to a multiple of the
     class granule max(page_size, 64) (decode) or max(page_size, 128) (prefill).
+    A multi-head unit's chunk is max(granule, floor(chunk / H / granule) *
+    granule) keys (the K/V bytes of a one-head chunk).
  4. A unit with kv_eff = 0 gives one empty item.  Otherwise each range
     [s, e) splits into ceil((e - s) / chunk) items [s + i*chunk,
     min(e, s + (i+1)*chunk)), ranges in order, chunk numbers running across
@@ -37,7 +44,8 @@ Rule:
     the flag 1 in its seventh field ("late": merged after the run by a
     launch of its own), a 16-row unit 0 (merged inside the run); a header
     field counts the late units.
- 5. cost = (kv length of the item + 256) * class weight, the 256 standing for
+ 5. cost = (kv length of the item * H + 256) * class weight (H = 1 for a
+    one-head unit), the 256 standing for
     the fixed per-item latency of the kernel.  Items are sorted by
     (-cost, -T, b, hk, qt, chunk) and each goes to the CTA with the smallest
     load, ties to the smaller CTA index (longest processing time first).
@@ -45,7 +53,8 @@ Rule:
     RoPE its position capacity, theta and scale bits and the table offset;
     then the count of late units, the partial rows used, the batch's query
     tokens, the cascade fields, the count of 16-row items and a zero field), per-CTA
-    CSR offsets, items in CTA order (within a CTA the 256-row items first,
+    CSR offsets, items in CTA order (an item: its 8 fields, its request's
+    table entry, H for a multi-head unit or 0, three zeros; within a CTA the 256-row items first,
     then the 16-row items, each in the order dealt), merge units, zeroed merge
     counters, request table.
 """
@@ -65,6 +74,7 @@ REQ_INTS = 4
 CASCADE_INTS = 12
 CASCADE_ROWS = 16
 ITEM_COST_TOKENS = 256
+MH_ROWS = 32  # packed query rows of a multi-head decode unit (its KV heads x G)
 
 # fi_status values
 OK, INVALID_ARG, UNSUPPORTED, CAPACITY = 0, 1, 2, 3
@@ -230,9 +240,10 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
     page_gran = max(page_size, shared_page_size if cascade else page_size)
     granule = {TILE_DECODE: max(page_gran, 64), TILE_PREFILL: max(page_gran, 128)}
 
-    def ranges_of(b, T, r0, r1):
-        q_first = lkv[b] - lq[b] + r0 // group
-        q_last = lkv[b] - lq[b] + (r1 - 1) // group
+    def ranges_of(b, T, r0, r1, heads=1):
+        # query tokens of the first and last rows (a multi-head unit: token 0)
+        q_first = lkv[b] - lq[b] + (0 if heads > 1 else r0 // group)
+        q_last = lkv[b] - lq[b] + (0 if heads > 1 else (r1 - 1) // group)
         causal_b = causal and b >= num_shared
         hi = max(0, min(lkv[b], q_last + 1) if causal_b else lkv[b])
         if window < 0:
@@ -246,7 +257,13 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
     def tile_of(b):
         return TILE_DECODE if lq[b] * group <= TILE_DECODE else TILE_PREFILL
 
-    # units in (b, hk, qt) order: (b, hk, qt, T, row0, row1, ranges)
+    # units in (b, hk, qt) order: (b, hk, qt, T, row0, row1, ranges, heads).  A
+    # one-token request of the plan's own page-1 cache takes MH_ROWS / G KV
+    # heads at once (rows = head offset * G + g) when G is a multiple of 4 and
+    # those heads tile [0, Hkv): a short request then pays the per-item cost
+    # once per unit instead of once per head.
+    mh = MH_ROWS // group if (group % 4 == 0 and group <= MH_ROWS // 2
+                              and num_kv_heads % (MH_ROWS // group) == 0) else 1
     units = []
     unit_at = {}
     total = {TILE_DECODE: 0, TILE_PREFILL: 0}
@@ -255,30 +272,36 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
         if R == 0:
             continue
         T = tile_of(b)
-        for hk in range(num_kv_heads):
+        cache_page = shared_page_size if b < num_shared else page_size
+        heads = mh if (T == TILE_DECODE and lq[b] == 1 and cache_page == 1 and rope_max == 0
+                       and b >= num_shared) else 1
+        for hk in range(0, num_kv_heads, heads):
             for qt in range(_ceil_div(R, T)):
-                r0, r1 = qt * T, min(R, (qt + 1) * T)
-                rng = ranges_of(b, T, r0, r1)
+                r0, r1 = (0, R * heads) if heads > 1 else (qt * T, min(R, (qt + 1) * T))
+                rng = ranges_of(b, T, r0, r1, heads)
                 unit_at[(b, hk, qt)] = len(units)
-                units.append((b, hk, qt, T, r0, r1, rng))
-                total[T] += sum(e - s for s, e in rng)
+                units.append((b, hk, qt, T, r0, r1, rng, heads))
+                total[T] += sum(e - s for s, e in rng) * heads
 
     chunk = {}
     for T, min_chunk in ((TILE_DECODE, cfg["decode_min_chunk"]), (TILE_PREFILL, cfg["prefill_min_chunk"])):
         want = max(min_chunk, _ceil_div(total[T], C * cfg["split_factor"]))
         chunk[T] = _ceil_div(want, granule[T]) * granule[T]
     weight = {TILE_DECODE: cfg["decode_cost_weight"], TILE_PREFILL: cfg["prefill_cost_weight"]}
+    # a multi-head unit's chunk holds the K/V bytes of a one-head chunk
+    chunk_mh = max(granule[TILE_DECODE], chunk[TILE_DECODE] // mh // granule[TILE_DECODE] * granule[TILE_DECODE])
 
     items = []   # (sort key, fields)
     merges = []
     part_rows = 0
     unit_parts = []  # per unit: (first partial row or -1, number of chunks)
     prefill_caches = 0
-    for (b, hk, qt, T, r0, r1, rng) in units:
+    for (b, hk, qt, T, r0, r1, rng, heads) in units:
         if T == TILE_PREFILL:
             prefill_caches |= 2 if b < num_shared else 1
-        pieces = [(s_ + i * chunk[T], min(e_, s_ + (i + 1) * chunk[T]))
-                  for s_, e_ in rng for i in range(_ceil_div(e_ - s_, chunk[T]))]
+        ck = chunk_mh if heads > 1 else chunk[T]
+        pieces = [(s_ + i * ck, min(e_, s_ + (i + 1) * ck))
+                  for s_, e_ in rng for i in range(_ceil_div(e_ - s_, ck))]
         n = max(1, len(pieces))
         nrows = r1 - r0
         base, m = -1, -1
@@ -290,29 +313,37 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
             merges.append((b, hk, r0, r1, n, base, 0 if T == TILE_DECODE else 1, 0))
         unit_parts.append((base, n))
         for i, (k0, k1) in enumerate(pieces or [(0, 0)]):
-            cost = (k1 - k0 + ITEM_COST_TOKENS) * weight[T]
+            cost = ((k1 - k0) * heads + ITEM_COST_TOKENS) * weight[T]
             part = base + i * nrows if base >= 0 else -1
             # the request's table entry rides along with the item
-            items.append(((-cost, -T, b, hk, qt, i), (b, hk, r0, r1, k0, k1, part, m, *reqs[b], 0, 0, 0, 0)))
+            items.append(((-cost, -T, b, hk, qt, i),
+                          (b, hk, r0, r1, k0, k1, part, m, *reqs[b], heads if heads > 1 else 0, 0, 0, 0)))
 
     # cascade merge entries, per ordinary unit: runs of at most CASCADE_ROWS
     # rows counted from the unit's first row, cut again at the block's q-tile bounds
     entries = []
-    for u, (b, hk, qt, T, r0, r1, _) in enumerate(units):
+    for u, (b, hk_u, qt, T, r0_u, r1_u, _, heads) in enumerate(units):
         if not cascade or b < num_shared:
             continue
         s = block_of[b]
         TS = tile_of(s)
         shift = (reqs[b][0] - reqs[s][0]) * group
-        r = r0
-        while r < r1:
-            sr = r + shift
-            su = unit_at[(s, hk, sr // TS)]
-            s_r0, s_r1 = units[su][4], units[su][5]
-            r_end = min(r1, r0 + ((r - r0) // CASCADE_ROWS + 1) * CASCADE_ROWS, r + (s_r1 - sr))
-            (b0, n0), (b1, n1) = unit_parts[su], unit_parts[u]
-            entries.append((b, hk, r, r_end, n0, b0 + sr - s_r0, s_r1 - s_r0, n1, b1 + r - r0, r1 - r0, 0, 0))
-            r = r_end
+        # a multi-head unit: entries per KV head, rows numbered as for one
+        # head, head h's partial rows at offset h * G of the unit's
+        for h in range(heads):
+            hk = hk_u + h
+            r0, r1 = (0, group) if heads > 1 else (r0_u, r1_u)
+            b1, n1 = unit_parts[u]
+            own0 = b1 + (h * group if heads > 1 else 0)
+            r = r0
+            while r < r1:
+                sr = r + shift
+                su = unit_at[(s, hk, sr // TS)]
+                s_r0, s_r1 = units[su][4], units[su][5]
+                r_end = min(r1, r0 + ((r - r0) // CASCADE_ROWS + 1) * CASCADE_ROWS, r + (s_r1 - sr))
+                b0, n0 = unit_parts[su]
+                entries.append((b, hk, r, r_end, n0, b0 + sr - s_r0, s_r1 - s_r0, n1, own0 + r - r0, r1_u - r0_u, 0, 0))
+                r = r_end
 
     if len(items) > cfg["max_items"] or len(merges) > cfg["max_merge_units"] \
             or len(entries) > cfg["max_merge_units"] or part_rows > cfg["max_partial_rows"]:

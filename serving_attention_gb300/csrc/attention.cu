@@ -603,6 +603,16 @@ fi_status build_cache(KvCache* kc, const CacheArgs& c, CUtensorMapDataType tt, i
     kc->gather_rows_k = int32_t(rk);
     kc->gather_rows_v = int32_t(rv);
   }
+  // Page size 1 with multi-head decode units (GQA groups a multiple of 4):
+  // one box per token holds that token's rows of the unit's H KV heads.
+  const int32_t mh = fi_mh_heads(G, num_kv_heads);
+  if (P == 1 && mh > 1) {
+    const uint32_t hb[4] = {uint32_t(kHeadDim), uint32_t(mh), 1u, 1u};
+    if (!make_map(&kc->tm_kh, tt, c.k, 4, kd, ks, hb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&kc->tm_vh, tt, c.v, 4, kd, vs, hb, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return FI_ERR_UNSUPPORTED;
+    kc->mh_heads = mh;
+  }
   if (kc->tc) {
     const uint32_t kb[4] = {64u, 1u, uint32_t(P), 1u};
     if (!make_map(&kc->tm_k, tt, c.k, 4, kd, ks, kb, CU_TENSOR_MAP_SWIZZLE_128B) ||

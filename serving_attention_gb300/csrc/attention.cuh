@@ -12,7 +12,8 @@ namespace fi {
 constexpr int kHeadDim = 128;
 
 // CUDA-core path (16-row decode tiles; prefill-class items too when pages are < 8 tokens)
-constexpr int kStageTokens = 128;      // KV tokens per pipeline stage
+constexpr int kLog2StageTokens = 7;
+constexpr int kStageTokens = 1 << kLog2StageTokens;  // KV rows per pipeline stage (tokens of one head)
 constexpr int kStages = 3;             // depth of the K/V ring
 constexpr int kBoxLanes = kStageTokens / 32;  // page boxes a producer lane issues per stage at page size 1
 constexpr int kConsumerWarps = 8;
@@ -60,12 +61,15 @@ struct KvCache {
   CUtensorMap tm_vd;
   CUtensorMap tm_kg;  // page size 1: [pages * rows_per_page, d], rows of 128 dims gathered four at a time
   CUtensorMap tm_vg;
+  CUtensorMap tm_kh;  // page size 1, multi-head units: boxes of (128 dims, mh_heads heads, 1 slot, 1 page)
+  CUtensorMap tm_vh;
   const int32_t* kv_indices;
   int32_t page_size, log2_page, num_pages;
   int32_t tc;             // prefill-class items of this cache run on the tensor cores (tm_k, tm_v built)
   int32_t gather_rows;    // page size 1: decode stages by 4-row gathers of rows page * rows_k/v + head
   int32_t gather_rows_k;  // page stride / head stride of K (>= Hkv)
   int32_t gather_rows_v;  // the same for V
+  int32_t mh_heads;       // KV heads of a multi-head unit's box (tm_kh, tm_vh built), else 0
 };
 
 struct RunParams {
@@ -188,16 +192,25 @@ struct Request {
 };
 
 // A work item with its request's table entry (the plan writes both).
+// heads: the KV heads hk .. hk + heads - 1 the item takes (1, or H of a
+// multi-head unit, whose packed row r is head hk + r / G, query token 0).
 struct Item {
   int32_t b, hk, row0, row1, kv0, kv1, part, merge;
   Request rq;
+  int32_t heads;
 };
 
 __device__ __forceinline__ Item load_item(const int32_t* iws, int32_t off_items, int32_t i) {
   const int4* p = reinterpret_cast<const int4*>(iws + off_items + FI_ITEM_INTS * i);
   const int4 a = __ldg(p), c = __ldg(p + 1), r = __ldg(p + 2);
-  return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w, Request{r.x, r.y, r.z, r.w}};
+  const int32_t h = __ldg(reinterpret_cast<const int32_t*>(p + 3));
+  return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w, Request{r.x, r.y, r.z, r.w}, h > 1 ? h : 1};
 }
+
+// Query token of packed row r of an item: r / G, and 0 in a multi-head item
+// (one query token; its row r < heads * G is query head hk * G + r).  The
+// query head is hk * G + r - t * G.
+__device__ __forceinline__ int row_token(const Item& it, int r, int G) { return r / (it.heads * G); }
 
 __device__ __forceinline__ Request load_request(const int32_t* iws, int32_t off_req, int32_t b) {
   int4 a = __ldg(reinterpret_cast<const int4*>(iws + off_req + FI_REQ_INTS * b));

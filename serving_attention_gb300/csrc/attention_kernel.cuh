@@ -7,7 +7,9 @@
 //  * warp 0 streams the chunk's K and V, 128 tokens per stage, into a 3-deep
 //    shared-memory ring: one TMA box per page and tensor, completion counted
 //    in bytes on the stage's mbarrier (see produce()).  Each K/V row of one
-//    head is 256 contiguous bytes.
+//    head is 256 contiguous bytes.  A multi-head item (one query token, pages
+//    of one token) takes H KV heads at once: a stage then holds 128 / H
+//    tokens, each token's H rows brought by one box.
 //  * warps 4..11 hold the G query heads that share KV head hk (GQA packing,
 //    wiki page "Decode 어텐션") in registers, 4 packed rows per half-warp,
 //    and score every KV token read from shared memory once for all of them.
@@ -15,6 +17,9 @@
 //    products are reduced with a 5-shuffle butterfly that leaves each lane
 //    the full score of one row.  Softmax is online with a lazily moved
 //    running max (log2 domain).
+//  * a multi-head item's 32 packed rows are the G query heads of each of its
+//    H KV heads; each row group of 4 lies in one KV head and scores that
+//    head's rows of the stage.
 //  * the half-warps' states are merged in shared memory; an unsplit item
 //    writes O (storage type) and LSE (natural log), a split item writes its
 //    fp32 partial state, and the CTA that finishes the last chunk of a split
@@ -40,7 +45,9 @@ __device__ __forceinline__ int groups_in_pass(int rows) {
 
 // K and V of one stage: 128 tokens of one KV head.  One unswizzled 4-D TMA box
 // (128 dims, 1 head, min(P, 128) slots, 1 page) per page and tensor, issued by
-// lane (box % 32); the page ids of the next stage are loaded one stage ahead
+// lane (box % 32); a multi-head item's stage is 128 / H tokens of H heads,
+// one box (128 dims, H heads, 1 slot, 1 page) per token and tensor, rows
+// token-major.  The page ids of the next stage are loaded one stage ahead
 // into the issuing lanes' registers (the wiki page's page-index prefetch,
 // "1) 블록-스파스 KV 포맷").  Pages past the chunk (which need not fill its last
 // stage) are addressed out of bounds and arrive as zeros without a read of
@@ -54,6 +61,9 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
     const KvCache& kc = p.kv[lane];
     tc::prefetch_tensormap(kc.gather_rows ? &kc.tm_kg : &kc.tm_kd);
     tc::prefetch_tensormap(kc.gather_rows ? &kc.tm_vg : &kc.tm_vd);
+  } else if (lane == 2 && p.kv[0].mh_heads) {
+    tc::prefetch_tensormap(&p.kv[0].tm_kh);
+    tc::prefetch_tensormap(&p.kv[0].tm_vh);
   }
   uint32_t it = 0;
   int armed[kStages];
@@ -65,11 +75,12 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
   // into L2, so that neither the consumers' query load nor this warp's page-id
   // load at the next item start waits on HBM.
   auto prefetch_next = [&](const Item& nx) {
-    const int t0 = nx.row0 / G, lines = ((nx.row1 - 1) / G - t0 + 1) * G * 2;
+    const int lines = (nx.row1 - nx.row0) * 2;  // two 128-byte lines per packed row
     for (int l = lane; l < lines; l += 32) {
-      const int tt = l / (2 * G), g = (l >> 1) % G;
-      tc::prefetch_l2(p.q + (int64_t(nx.rq.qo_start) + t0 + tt) * p.q_stride_tok +
-                      int64_t(nx.hk * G + g) * p.q_stride_head + (l & 1) * 64);
+      const int row = nx.row0 + (l >> 1);
+      const int t = row_token(nx, row, G);
+      tc::prefetch_l2(p.q + (int64_t(nx.rq.qo_start) + t) * p.q_stride_tok +
+                      int64_t(nx.hk * G + row - t * G) * p.q_stride_head + (l & 1) * 64);
     }
     if (lane == 0) {
       const KvCache& kn = cache_of(p, nx.b, num_shared);
@@ -81,11 +92,14 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
   auto stream_item = [&](const KvCache& kc, const Item& item, const Item* nx) {
     const Request& rq = item.rq;
     const int lp = kc.log2_page, P = kc.page_size;
-    const int boxes = P >= kStageTokens ? 1 : (kStageTokens >> lp);  // per stage and tensor
+    const int H = item.heads;             // a multi-head item (page size 1): H KV heads per token
+    const int stok = kStageTokens / H;    // tokens per stage
+    const bool gather = kc.gather_rows && H == 1;
+    const int boxes = H > 1 ? stok : P >= kStageTokens ? 1 : (kStageTokens >> lp);  // per stage and tensor
     const int box_slots = P >= kStageTokens ? kStageTokens : P;
     const int nrows = item.row1 - item.row0;
     const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
-    const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
+    const int nst = (item.kv1 - item.kv0 + stok - 1) / stok;
     const int npages = min((rq.kv_len + P - 1) >> lp, (item.kv1 + P - 1) >> lp);  // pages the chunk touches
     const int32_t* pages = kc.kv_indices + rq.page_start;
     for (int pass = 0; pass < passes; ++pass) {
@@ -93,10 +107,10 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
       // or 4 * lane .. 4 * lane + 3 (the four rows of a lane's gather)
       int32_t nxid[kBoxLanes];
       auto fetch_ids = [&](int st) {
-        const int pg0 = (item.kv0 + st * kStageTokens) >> lp;
+        const int pg0 = (item.kv0 + st * stok) >> lp;
 #pragma unroll
         for (int r = 0; r < kBoxLanes; ++r) {
-          const int bx = kc.gather_rows ? kBoxLanes * lane + r : lane + 32 * r;
+          const int bx = gather ? kBoxLanes * lane + r : lane + 32 * r;
           nxid[r] = (bx < boxes && pg0 + bx < npages) ? __ldg(pages + pg0 + bx) : kc.num_pages;
         }
       };
@@ -111,9 +125,21 @@ static __device__ void produce(const RunParams& p, RunSmem& sm, int32_t item_beg
         if (!warp_wait(&sm.empty[s], ph ^ 1, &sm.abort)) continue;
         if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
         __syncwarp();
-        const int j0 = item.kv0 + st * kStageTokens;
+        const int j0 = item.kv0 + st * stok;
         const int slot0 = P > kStageTokens ? (j0 & (P - 1)) : 0;
-        if (kc.gather_rows) {
+        if (H > 1) {
+          // multi-head item: one box per token and tensor with the token's
+          // rows of KV heads hk .. hk + H - 1 (H * 256 contiguous bytes of
+          // the stage, token-major: stage row = token * H + head offset)
+#pragma unroll
+          for (int r = 0; r < kBoxLanes; ++r) {
+            const int bx = lane + 32 * r;
+            if (bx < boxes) {
+              tc::tma_load_4d(&sm.dec.k[s][bx * H][0], &kc.tm_kh, &sm.full[s], 0, item.hk, 0, id[r]);
+              tc::tma_load_4d(&sm.dec.v[s][bx * H][0], &kc.tm_vh, &sm.full[s], 0, item.hk, 0, id[r]);
+            }
+          }
+        } else if (gather) {
           // page size 1: lane l brings tokens 4l..4l+3 of K and of V with one
           // four-row gather each (row page * rows_per_page + hk; pages past
           // the chunk are rows past the tensor and arrive as zeros)
@@ -210,7 +236,7 @@ __device__ void merge_split_unit(const RunParams& p, const Item& item, const Req
       }
       const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
       const int row = item.row0 + pr;
-      const int t = row / G;
+      const int t = row_token(item, row, G);
       const int head = item.hk * G + (row - t * G);
       const int64_t tok = rq.qo_start + t;
       uint2 packed;
@@ -413,10 +439,13 @@ __device__ void rope_decode(const RunParams& p, RunSmem& sm, int32_t item_begin,
   if (f16x2_has_inf(amax)) atomicOr(p.iws + FI_H_STATUS, kStatusRange);
 }
 
+// One pass of up to kRowsPerPass packed rows of an item: load the rows'
+// queries, stream the item's KV stages through the ring (advancing the ring
+// counter it, returned), combine the half-warps' states and write O and LSE
+// or the partial state.
 template <typename T, bool kCap, bool kMask, bool kRope>
-__device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
-                        int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, int32_t num_shared,
-                        const Variant var) {
+__device__ __forceinline__ uint32_t consume_pass(const RunParams& p, RunSmem& sm, const Item& item, int pass,
+                                                 uint32_t it, int causal, int32_t num_shared, const Variant& var) {
   const int cw = (threadIdx.x >> 5) - kFirstConsumerWarp;  // consumer warp 0..7
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4;
@@ -425,6 +454,258 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
   const int my_row = L >> 2;  // row of the group whose full score this lane holds
   const int ct = cw * 32 + lane;  // consumer thread 0..255
   const int G = p.group;
+  const Request& rq = item.rq;
+  const int nrows = item.row1 - item.row0;
+  // a multi-head item: H KV heads, rows all of query token 0; its stages
+  // hold kStageTokens / H tokens of H rows each
+  const int H = item.heads;
+  const int nst = ((item.kv1 - item.kv0) * H + kStageTokens - 1) >> kLog2StageTokens;
+  const bool causal_i = causal && item.b >= num_shared;  // a shared block's keys are all visible
+
+  const int prow0 = pass * kRowsPerPass;
+  const int prows = min(kRowsPerPass, nrows - prow0);
+  const int ng = groups_in_pass(prows);
+  const int wpg = kConsumerWarps / ng;
+  const int g = cw % ng;
+  const int slice = cw / ng;
+  const int nhw = 2 * wpg;             // half-warps sharing this row group
+  const int hw = slice * 2 + half;     // index among them
+  // Stage rows this half-warp scores: rb, rb + rs, ...  A multi-head
+  // stage is token-major (row = token * H + head offset) and the group's
+  // 4 rows share one head (G is a multiple of 4 there), hsel
+  // (g * 4 / G with H = 32 / G, and 0 for a one-head item: g < 8)
+  const int hsel = (g * H) >> 3;
+  const int rb = hw * H + hsel, rs = nhw * H;
+
+  // Query rows of this group, pre-scaled by scale*log2(e), as dim pairs
+  // for the packed fp32 FMA (dims 2i, 2i+1 of this lane's 8).
+  float2 q[kRowsPerGroup][4];
+  int lim_mine = -1, lo_mine = 0;  // this lane's row: visible keys [lo, lim] (and the sink)
+  // The group's row loads go out together, before any of them is used
+  // (inside the per-row branch below they were issued one after another).
+  uint4 qraw[kRowsPerGroup];
+#pragma unroll
+  for (int r = 0; r < kRowsPerGroup; ++r) {
+    const int prow = prow0 + g * kRowsPerGroup + r;
+    const int row = item.row0 + (prow < nrows ? prow : 0);
+    const int t = row_token(item, row, G);
+    const int head = item.hk * G + (row - t * G);
+    qraw[r] = __ldg(reinterpret_cast<const uint4*>(p.q + int64_t(rq.qo_start + t) * p.q_stride_tok +
+                                                   int64_t(head) * p.q_stride_head + L * 8));
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerGroup; ++r) {
+    const int prow = prow0 + g * kRowsPerGroup + r;
+    int lim = -1;
+    if (prow < nrows) {
+      const int row = item.row0 + prow;
+      const int t = row_token(item, row, G);
+      unpack4x2<T>(qraw[r], q[r]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) q[r][c] = make_float2(q[r][c].x * p.scale_log2, q[r][c].y * p.scale_log2);
+      lim = causal_i ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1;
+      if (kMask && r == my_row) lo_mine = window_low(var, rq.kv_len - rq.qo_len + t);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) q[r][c] = make_float2(0.f, 0.f);
+    }
+    if (r == my_row) lim_mine = lim;
+  }
+  if (kRope) {
+    // Rotate the query rows: this lane holds dims 8L..8L+7, the lane L^8
+    // of the same half-warp the other member of each pair.
+    const int f0 = (L & 7) * 8;
+    const float sgn = L < 8 ? -1.f : 1.f;
+#pragma unroll
+    for (int r = 0; r < kRowsPerGroup; ++r) {
+      float2 pq[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        pq[c] = make_float2(__shfl_xor_sync(0xffffffffu, q[r][c].x, 8), __shfl_xor_sync(0xffffffffu, q[r][c].y, 8));
+      const int prow = prow0 + g * kRowsPerGroup + r;
+      if (prow < nrows) {
+        const int t = row_token(item, item.row0 + prow, G);
+        const float4* cs = reinterpret_cast<const float4*>(
+            var.rope_table + int64_t(rq.kv_len - rq.qo_len + t) * FI_ROPE_PAIRS + f0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 w = __ldg(cs + c);  // (cos, sin) of dims 2c and 2c+1 of the lane
+          q[r][c] = make_float2(fmaf(q[r][c].x, w.x, sgn * pq[c].x * w.y), fmaf(q[r][c].y, w.z, sgn * pq[c].y * w.w));
+        }
+      }
+    }
+  }
+  // Visibility in stage rows: row tok * H + hsel of the stage at key j0
+  // holds key j0 + tok.  It is visible to this lane's row iff row <= vhi;
+  // with a window iff (unsigned)(row - vlo) < vis_cnt (one range
+  // compare) or row < vsink.  Every bound is clipped to the row's last
+  // visible key in the chunk, so neither a stage running past the chunk
+  // nor a sink longer than the chunk or than the row's causal range
+  // brings in a key the row does not see; all three move down by
+  // kStageTokens rows per stage.
+  const int hi_mine = min(lim_mine, item.kv1 - 1);
+  const int lo_c = max(lo_mine, item.kv0) - item.kv0;  // keys before the chunk are not in any stage
+  int vhi = max(hi_mine - item.kv0, -1) * H + hsel;
+  int vlo = lo_c * H + hsel;
+  int vsink = max(min(var.sink, hi_mine + 1) - item.kv0, 0) * H + hsel;
+  const unsigned vis_cnt = kMask ? unsigned(max(0, hi_mine + 1 - item.kv0 - lo_c) * H) : 0u;
+
+  float2 o[kRowsPerGroup][4];
+#pragma unroll
+  for (int r = 0; r < kRowsPerGroup; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[r][c] = make_float2(0.f, 0.f);
+  float m = -INFINITY, l = 0.f;
+
+  const int nblk = kStageTokens / (rs * kTokBlock);
+  for (int st = 0; st < nst; ++st, ++it) {
+    const int s = it % kStages;
+    const uint32_t ph = (it / kStages) & 1;
+    // warp-uniform result: the body below shuffles across the warp
+    if (warp_wait(kRope ? &sm.rot[s] : &sm.full[s], ph, &sm.abort)) {
+      for (int blk = 0; blk < nblk; ++blk) {
+        float sc[kTokBlock];
+#pragma unroll
+        for (int u = 0; u < kTokBlock; ++u) {
+          const int tok = rb + (blk * kTokBlock + u) * rs;  // stage row
+          const uint4 kv = *reinterpret_cast<const uint4*>(&sm.dec.k[s][tok][L * 8]);
+          float2 f[4];
+          unpack4x2<std::conditional_t<kRope, __half, T>>(kv, f);  // rotated keys are fp16
+          float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            a0 = fma2(q[0][c], f[c], a0);
+            a1 = fma2(q[1][c], f[c], a1);
+            a2 = fma2(q[2][c], f[c], a2);
+            a3 = fma2(q[3][c], f[c], a3);
+          }
+          float sfull = reduce_rows4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y, L);
+          if (kCap) sfull = soft_cap_log2(sfull, var.cap_a, var.cap_b);
+          const bool seen = kMask ? (unsigned(tok - vlo) < vis_cnt || tok < vsink) : tok <= vhi;
+          sc[u] = seen ? sfull : -INFINITY;
+        }
+        float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        float m_new = m;
+        if (mx > m + kLazyRescale) m_new = mx;  // also taken on the first visible key (m = -inf)
+        const float alpha = (m_new == m) ? 1.f : ex2(m - m_new);
+        float ps[kTokBlock];
+        float psum = 0.f;
+#pragma unroll
+        for (int u = 0; u < kTokBlock; ++u) {
+          ps[u] = (m_new == -INFINITY) ? 0.f : ex2(sc[u] - m_new);
+          psum += ps[u];
+        }
+        l = l * alpha + psum;
+        m = m_new;
+        float* x = reinterpret_cast<float*>(sm.dec.xch[hwid]);
+        if ((L & 3) == 0) {
+#pragma unroll
+          for (int u = 0; u < kTokBlock; ++u) x[u * 4 + my_row] = ps[u];
+          x[kTokBlock * 4 + my_row] = alpha;
+        }
+        __syncwarp();
+        const float4 al = sm.dec.xch[hwid][kTokBlock];
+        if (__any_sync(0xffffffffu, al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            o[0][c] = make_float2(o[0][c].x * al.x, o[0][c].y * al.x);
+            o[1][c] = make_float2(o[1][c].x * al.y, o[1][c].y * al.y);
+            o[2][c] = make_float2(o[2][c].x * al.z, o[2][c].y * al.z);
+            o[3][c] = make_float2(o[3][c].x * al.w, o[3][c].y * al.w);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kTokBlock; ++u) {
+          const int tok = rb + (blk * kTokBlock + u) * rs;
+          const float4 pu = sm.dec.xch[hwid][u];
+          const uint4 vv = *reinterpret_cast<const uint4*>(&sm.dec.v[s][tok][L * 8]);
+          float2 f[4];
+          unpack4x2<T>(vv, f);
+          const float2 p0 = make_float2(pu.x, pu.x), p1 = make_float2(pu.y, pu.y);
+          const float2 p2 = make_float2(pu.z, pu.z), p3 = make_float2(pu.w, pu.w);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            o[0][c] = fma2(p0, f[c], o[0][c]);
+            o[1][c] = fma2(p1, f[c], o[1][c]);
+            o[2][c] = fma2(p2, f[c], o[2][c]);
+            o[3][c] = fma2(p3, f[c], o[3][c]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+    vhi -= kStageTokens;
+    vlo -= kStageTokens;
+    vsink -= kStageTokens;
+  }
+
+  // This half-warp's state -> shared memory, then merge per row.
+#pragma unroll
+  for (int r = 0; r < kRowsPerGroup; ++r) {
+    float4* dst = reinterpret_cast<float4*>(&sm.dec.comb_o[hwid][r][L * 8]);
+    dst[0] = make_float4(o[r][0].x, o[r][0].y, o[r][1].x, o[r][1].y);
+    dst[1] = make_float4(o[r][2].x, o[r][2].y, o[r][3].x, o[r][3].y);
+  }
+  if ((L & 3) == 0) {
+    sm.dec.comb_m[hwid][my_row] = m;
+    sm.dec.comb_l[hwid][my_row] = l;
+  }
+  named_barrier_sync(1, 32 * kConsumerWarps);
+  if (!sm.abort) {
+    for (int task = ct; task < prows * 32; task += 32 * kConsumerWarps) {
+      const int pr = task >> 5, ch = task & 31;
+      const int gg = pr / kRowsPerGroup, r = pr % kRowsPerGroup;
+      float M = -INFINITY;
+      for (int sl = 0; sl < wpg; ++sl)
+        for (int h2 = 0; h2 < 2; ++h2) M = fmaxf(M, sm.dec.comb_m[(gg + sl * ng) * 2 + h2][r]);
+      float Ls = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (M != -INFINITY) {
+        for (int sl = 0; sl < wpg; ++sl)
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int id = (gg + sl * ng) * 2 + h2;
+            const float w = ex2(sm.dec.comb_m[id][r] - M);
+            Ls += w * sm.dec.comb_l[id][r];
+            const float4 v = *reinterpret_cast<const float4*>(&sm.dec.comb_o[id][r][ch * 4]);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+          }
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+      const float lse_v = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+      const int prow = prow0 + pr;
+      if (item.part < 0) {
+        const int row = item.row0 + prow;
+        const int t = row_token(item, row, G);
+        const int head = item.hk * G + (row - t * G);
+        const int64_t tok = rq.qo_start + t;
+        uint2 packed;
+        packed.x = Elem<T>::from_float2(acc.x, acc.y);
+        packed.y = Elem<T>::from_float2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + ch * 4) =
+            packed;
+        if (ch == 0 && p.lse) p.lse[tok * p.num_qo_heads + head] = lse_v;
+      } else {
+        const int64_t prw = int64_t(item.part) + prow;
+        *reinterpret_cast<float4*>(p.fws + p.partial_o_offset + prw * kHeadDim + ch * 4) = acc;
+        if (ch == 0) p.fws[prw] = lse_v;
+      }
+    }
+  }
+  named_barrier_sync(1, 32 * kConsumerWarps);
+  return it;
+}
+
+template <typename T, bool kCap, bool kMask, bool kRope>
+__device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int32_t item_end, int32_t off_items,
+                        int32_t off_req, int32_t off_merge, int32_t off_cnt, int causal, int32_t num_shared,
+                        const Variant var) {
+  const int ct = threadIdx.x - 32 * kFirstConsumerWarp;  // consumer thread 0..255
   uint32_t it = 0;
 
   // Items in the order dealt; each pass of an item loads its query rows,
@@ -435,236 +716,12 @@ __device__ void consume(const RunParams& p, RunSmem& sm, int32_t item_begin, int
   // registers spill, which costs more than the latency saved.)
   for (int32_t i = item_begin; i < item_end; ++i) {
     const Item item = load_item(p.iws, off_items, i);
-    const Request& rq = item.rq;
-    const int nrows = item.row1 - item.row0;
-    const int passes = (nrows + kRowsPerPass - 1) / kRowsPerPass;
-    const int nst = (item.kv1 - item.kv0 + kStageTokens - 1) / kStageTokens;
-    const bool causal_i = causal && item.b >= num_shared;  // a shared block's keys are all visible
-
-    for (int pass = 0; pass < passes; ++pass) {
-      const int prow0 = pass * kRowsPerPass;
-      const int prows = min(kRowsPerPass, nrows - prow0);
-      const int ng = groups_in_pass(prows);
-      const int wpg = kConsumerWarps / ng;
-      const int g = cw % ng;
-      const int slice = cw / ng;
-      const int nhw = 2 * wpg;             // half-warps sharing this row group
-      const int hw = slice * 2 + half;     // index among them
-      const int blocks = kStageTokens / (nhw * kTokBlock);
-
-      // Query rows of this group, pre-scaled by scale*log2(e), as dim pairs
-      // for the packed fp32 FMA (dims 2i, 2i+1 of this lane's 8).
-      float2 q[kRowsPerGroup][4];
-      int lim_mine = -1, lo_mine = 0;  // this lane's row: visible keys [lo, lim] (and the sink)
-      // The group's row loads go out together, before any of them is used
-      // (inside the per-row branch below they were issued one after another).
-      uint4 qraw[kRowsPerGroup];
-#pragma unroll
-      for (int r = 0; r < kRowsPerGroup; ++r) {
-        const int prow = prow0 + g * kRowsPerGroup + r;
-        const int row = item.row0 + (prow < nrows ? prow : 0);
-        const int t = row / G;
-        const int head = item.hk * G + (row - t * G);
-        qraw[r] = __ldg(reinterpret_cast<const uint4*>(p.q + int64_t(rq.qo_start + t) * p.q_stride_tok +
-                                                       int64_t(head) * p.q_stride_head + L * 8));
-      }
-#pragma unroll
-      for (int r = 0; r < kRowsPerGroup; ++r) {
-        const int prow = prow0 + g * kRowsPerGroup + r;
-        int lim = -1;
-        if (prow < nrows) {
-          const int row = item.row0 + prow;
-          const int t = row / G;
-          unpack4x2<T>(qraw[r], q[r]);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) q[r][c] = make_float2(q[r][c].x * p.scale_log2, q[r][c].y * p.scale_log2);
-          lim = causal_i ? rq.kv_len - rq.qo_len + t : rq.kv_len - 1;
-          if (kMask && r == my_row) lo_mine = window_low(var, rq.kv_len - rq.qo_len + t);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) q[r][c] = make_float2(0.f, 0.f);
-        }
-        if (r == my_row) lim_mine = lim;
-      }
-      if (kRope) {
-        // Rotate the query rows: this lane holds dims 8L..8L+7, the lane L^8
-        // of the same half-warp the other member of each pair.
-        const int f0 = (L & 7) * 8;
-        const float sgn = L < 8 ? -1.f : 1.f;
-#pragma unroll
-        for (int r = 0; r < kRowsPerGroup; ++r) {
-          float2 pq[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            pq[c] = make_float2(__shfl_xor_sync(0xffffffffu, q[r][c].x, 8), __shfl_xor_sync(0xffffffffu, q[r][c].y, 8));
-          const int prow = prow0 + g * kRowsPerGroup + r;
-          if (prow < nrows) {
-            const int t = (item.row0 + prow) / G;
-            const float4* cs = reinterpret_cast<const float4*>(
-                var.rope_table + int64_t(rq.kv_len - rq.qo_len + t) * FI_ROPE_PAIRS + f0);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const float4 w = __ldg(cs + c);  // (cos, sin) of dims 2c and 2c+1 of the lane
-              q[r][c] = make_float2(fmaf(q[r][c].x, w.x, sgn * pq[c].x * w.y), fmaf(q[r][c].y, w.z, sgn * pq[c].y * w.w));
-            }
-          }
-        }
-      }
-      // With a window, key j of the chunk is visible to this lane's row iff
-      // (unsigned)(j - lo_mine) < vis_cnt or j < sink (one range compare).
-      const unsigned vis_cnt = kMask ? unsigned(max(0, min(lim_mine, item.kv1 - 1) + 1 - lo_mine)) : 0u;
-
-      float2 o[kRowsPerGroup][4];
-#pragma unroll
-      for (int r = 0; r < kRowsPerGroup; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) o[r][c] = make_float2(0.f, 0.f);
-      float m = -INFINITY, l = 0.f;
-
-      for (int st = 0; st < nst; ++st, ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        // warp-uniform result: the body below shuffles across the warp
-        if (warp_wait(kRope ? &sm.rot[s] : &sm.full[s], ph, &sm.abort)) {
-          const int j0 = item.kv0 + st * kStageTokens;
-          for (int blk = 0; blk < blocks; ++blk) {
-            float sc[kTokBlock];
-#pragma unroll
-            for (int u = 0; u < kTokBlock; ++u) {
-              const int tok = hw + (blk * kTokBlock + u) * nhw;
-              const uint4 kv = *reinterpret_cast<const uint4*>(&sm.dec.k[s][tok][L * 8]);
-              float2 f[4];
-              unpack4x2<std::conditional_t<kRope, __half, T>>(kv, f);  // rotated keys are fp16
-              float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                a0 = fma2(q[0][c], f[c], a0);
-                a1 = fma2(q[1][c], f[c], a1);
-                a2 = fma2(q[2][c], f[c], a2);
-                a3 = fma2(q[3][c], f[c], a3);
-              }
-              float sfull = reduce_rows4(a0.x + a0.y, a1.x + a1.y, a2.x + a2.y, a3.x + a3.y, L);
-              if (kCap) sfull = soft_cap_log2(sfull, var.cap_a, var.cap_b);
-              const int j = j0 + tok;
-              const bool seen = kMask ? (unsigned(j - lo_mine) < vis_cnt || j < var.sink)
-                                      : (j < item.kv1 && j <= lim_mine);
-              sc[u] = seen ? sfull : -INFINITY;
-            }
-            float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-            float m_new = m;
-            if (mx > m + kLazyRescale) m_new = mx;  // also taken on the first visible key (m = -inf)
-            const float alpha = (m_new == m) ? 1.f : ex2(m - m_new);
-            float ps[kTokBlock];
-            float psum = 0.f;
-#pragma unroll
-            for (int u = 0; u < kTokBlock; ++u) {
-              ps[u] = (m_new == -INFINITY) ? 0.f : ex2(sc[u] - m_new);
-              psum += ps[u];
-            }
-            l = l * alpha + psum;
-            m = m_new;
-            float* x = reinterpret_cast<float*>(sm.dec.xch[hwid]);
-            if ((L & 3) == 0) {
-#pragma unroll
-              for (int u = 0; u < kTokBlock; ++u) x[u * 4 + my_row] = ps[u];
-              x[kTokBlock * 4 + my_row] = alpha;
-            }
-            __syncwarp();
-            const float4 al = sm.dec.xch[hwid][kTokBlock];
-            if (__any_sync(0xffffffffu, al.x != 1.f || al.y != 1.f || al.z != 1.f || al.w != 1.f)) {
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                o[0][c] = make_float2(o[0][c].x * al.x, o[0][c].y * al.x);
-                o[1][c] = make_float2(o[1][c].x * al.y, o[1][c].y * al.y);
-                o[2][c] = make_float2(o[2][c].x * al.z, o[2][c].y * al.z);
-                o[3][c] = make_float2(o[3][c].x * al.w, o[3][c].y * al.w);
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < kTokBlock; ++u) {
-              const int tok = hw + (blk * kTokBlock + u) * nhw;
-              const float4 pu = sm.dec.xch[hwid][u];
-              const uint4 vv = *reinterpret_cast<const uint4*>(&sm.dec.v[s][tok][L * 8]);
-              float2 f[4];
-              unpack4x2<T>(vv, f);
-              const float2 p0 = make_float2(pu.x, pu.x), p1 = make_float2(pu.y, pu.y);
-              const float2 p2 = make_float2(pu.z, pu.z), p3 = make_float2(pu.w, pu.w);
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                o[0][c] = fma2(p0, f[c], o[0][c]);
-                o[1][c] = fma2(p1, f[c], o[1][c]);
-                o[2][c] = fma2(p2, f[c], o[2][c]);
-                o[3][c] = fma2(p3, f[c], o[3][c]);
-              }
-            }
-            __syncwarp();
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
-      }
-
-      // This half-warp's state -> shared memory, then merge per row.
-#pragma unroll
-      for (int r = 0; r < kRowsPerGroup; ++r) {
-        float4* dst = reinterpret_cast<float4*>(&sm.dec.comb_o[hwid][r][L * 8]);
-        dst[0] = make_float4(o[r][0].x, o[r][0].y, o[r][1].x, o[r][1].y);
-        dst[1] = make_float4(o[r][2].x, o[r][2].y, o[r][3].x, o[r][3].y);
-      }
-      if ((L & 3) == 0) {
-        sm.dec.comb_m[hwid][my_row] = m;
-        sm.dec.comb_l[hwid][my_row] = l;
-      }
-      named_barrier_sync(1, 32 * kConsumerWarps);
-      if (!sm.abort) {
-        for (int task = ct; task < prows * 32; task += 32 * kConsumerWarps) {
-          const int pr = task >> 5, ch = task & 31;
-          const int gg = pr / kRowsPerGroup, r = pr % kRowsPerGroup;
-          float M = -INFINITY;
-          for (int sl = 0; sl < wpg; ++sl)
-            for (int h2 = 0; h2 < 2; ++h2) M = fmaxf(M, sm.dec.comb_m[(gg + sl * ng) * 2 + h2][r]);
-          float Ls = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (M != -INFINITY) {
-            for (int sl = 0; sl < wpg; ++sl)
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int id = (gg + sl * ng) * 2 + h2;
-                const float w = ex2(sm.dec.comb_m[id][r] - M);
-                Ls += w * sm.dec.comb_l[id][r];
-                const float4 v = *reinterpret_cast<const float4*>(&sm.dec.comb_o[id][r][ch * 4]);
-                acc.x += w * v.x;
-                acc.y += w * v.y;
-                acc.z += w * v.z;
-                acc.w += w * v.w;
-              }
-          }
-          const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-          acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-          const float lse_v = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
-          const int prow = prow0 + pr;
-          if (item.part < 0) {
-            const int row = item.row0 + prow;
-            const int t = row / G;
-            const int head = item.hk * G + (row - t * G);
-            const int64_t tok = rq.qo_start + t;
-            uint2 packed;
-            packed.x = Elem<T>::from_float2(acc.x, acc.y);
-            packed.y = Elem<T>::from_float2(acc.z, acc.w);
-            *reinterpret_cast<uint2*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + ch * 4) =
-                packed;
-            if (ch == 0 && p.lse) p.lse[tok * p.num_qo_heads + head] = lse_v;
-          } else {
-            const int64_t prw = int64_t(item.part) + prow;
-            *reinterpret_cast<float4*>(p.fws + p.partial_o_offset + prw * kHeadDim + ch * 4) = acc;
-            if (ch == 0) p.fws[prw] = lse_v;
-          }
-        }
-      }
-      named_barrier_sync(1, 32 * kConsumerWarps);
-    }
-
+    const int passes = (item.row1 - item.row0 + kRowsPerPass - 1) / kRowsPerPass;
+    for (int pass = 0; pass < passes; ++pass)
+      it = consume_pass<T, kCap, kMask, kRope>(p, sm, item, pass, it, causal, num_shared, var);
     if (item.merge >= 0)
-      merge_split_unit<T>(p, item, rq, off_merge, off_cnt, ct, 32 * kConsumerWarps, 1, &sm.merge_last, sm.abort);
+      merge_split_unit<T>(p, item, item.rq, off_merge, off_cnt, ct, 32 * kConsumerWarps, 1, &sm.merge_last,
+                          sm.abort);
   }
 }
 
@@ -721,14 +778,17 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   const int32_t h_hq = ws_header(iws, FI_H_NUM_QO_HEADS), h_hkv = ws_header(iws, FI_H_NUM_KV_HEADS);
   const int32_t h_page = ws_header(iws, FI_H_PAGE_SIZE);
   const int32_t num_shared = ws_header(iws, FI_H_NUM_SHARED), h_spage = ws_header(iws, FI_H_SHARED_PAGE_SIZE);
-  // Pre-rotated operands without the RoPE instantiation: every item must be
-  // a tensor-core item (the CUDA-core path would read unrotated keys).
+  // A RoPE plan runs on the RoPE instantiation, or -- its operands rotated by
+  // a pass before the run -- on the plain one when every item is a
+  // tensor-core item (the CUDA-core path would read unrotated keys); a plan
+  // without RoPE runs on the plain instantiation only.
   const int32_t h_dec = ws_header(iws, FI_H_NUM_DECODE_ITEMS);
+  const bool h_rope = ws_header(iws, FI_H_ROPE_MAX_POS) > 0;
   bool bad = magic != FI_PLAN_MAGIC || n_ctas != int32_t(gridDim.x) || (smem_u32(smem_raw) & 1023u) != 0 ||
              h_rows < 0 || h_rows > p.max_partial_rows || h_qo < 0 || h_qo > p.q_num_tokens ||
              h_hq != p.num_qo_heads || h_hkv != p.num_kv_heads || h_page != p.kv[0].page_size ||
              num_shared < 0 || (num_shared > 0 && (!p.has_shared || h_spage != p.kv[1].page_size)) ||
-             (!kRope && p.qk_prerotated && h_dec != 0);
+             (kRope ? !h_rope : h_rope && !(p.qk_prerotated && h_dec == 0));
   int32_t begin = 0, end = 0;
   if (!bad) {
     begin = __ldg(iws + off_cta + blockIdx.x);

@@ -45,6 +45,7 @@ inline int64_t round4(int64_t n) { return (n + 3) & ~int64_t(3); }
 
 struct Unit {
   int32_t b, hk, qt, tile, row0, row1;
+  int32_t heads;                 // KV heads hk .. hk + heads - 1 (more than one: a multi-head decode unit)
   int64_t r_begin[2], r_end[2];  // visible KV ranges, in KV order
   int32_t n_ranges;
   int64_t kv_eff;                // summed length of the ranges
@@ -205,17 +206,29 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
     const bool causal_b = causal && b >= num_shared;  // a shared block's keys precede all its queries
     const int32_t tile = rows <= FI_TILE_DECODE ? FI_TILE_DECODE : FI_TILE_PREFILL;
     const int32_t tiles = int32_t(ceil_div(rows, tile));
-    for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
+    // One query token of the plan's own page-1 cache: fi_mh_heads() KV heads
+    // per unit (FI_MH_ROWS packed rows), so that short requests pay the
+    // per-item cost once per unit, not once per head, and every TMA box brings
+    // one token of all the unit's heads.
+    const int32_t cache_page = b < num_shared ? shared_page_size : page_size;
+    const int32_t heads = (tile == FI_TILE_DECODE && rq.qo_len == 1 && cache_page == 1 && rope_max == 0 &&
+                           b >= num_shared)
+                              ? fi_mh_heads(group, num_kv_heads)
+                              : 1;
+    for (int32_t hk = 0; hk < num_kv_heads; hk += heads) {
       for (int32_t qt = 0; qt < tiles; ++qt) {
         Unit u;
         u.b = b;
         u.hk = hk;
         u.qt = qt;
         u.tile = tile;
+        u.heads = heads;
         u.row0 = qt * tile;
-        u.row1 = int32_t(std::min<int64_t>(rows, int64_t(qt + 1) * tile));
-        const int64_t q_first = int64_t(rq.kv_len) - rq.qo_len + u.row0 / group;
-        const int64_t q_last = int64_t(rq.kv_len) - rq.qo_len + (u.row1 - 1) / group;
+        u.row1 = heads > 1 ? int32_t(rows * heads) : int32_t(std::min<int64_t>(rows, int64_t(qt + 1) * tile));
+        // query tokens of the unit's first and last rows (a multi-head unit: token 0)
+        const int64_t t_first = heads > 1 ? 0 : u.row0 / group, t_last = heads > 1 ? 0 : (u.row1 - 1) / group;
+        const int64_t q_first = int64_t(rq.kv_len) - rq.qo_len + t_first;
+        const int64_t q_last = int64_t(rq.kv_len) - rq.qo_len + t_last;
         int64_t hi = causal_b ? std::min<int64_t>(rq.kv_len, q_last + 1) : int64_t(rq.kv_len);
         if (hi < 0) hi = 0;
         u.n_ranges = 1;
@@ -240,7 +253,7 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
         }
         u.kv_eff = 0;
         for (int r = 0; r < u.n_ranges; ++r) u.kv_eff += u.r_end[r] - u.r_begin[r];
-        (tile == FI_TILE_DECODE ? total_dec : total_pre) += u.kv_eff;
+        (tile == FI_TILE_DECODE ? total_dec : total_pre) += u.kv_eff * heads;
         units.push_back(u);
       }
     }
@@ -251,8 +264,12 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
     int64_t c = std::max<int64_t>(min_chunk, ceil_div(total, slots));
     return ceil_div(c, granule) * granule;
   };
-  const int64_t chunk_dec = pick_chunk(total_dec, cfg->decode_min_chunk, std::max(max_page, FI_GRANULE_DECODE));
+  const int64_t gran_dec = std::max(max_page, FI_GRANULE_DECODE);
+  const int64_t chunk_dec = pick_chunk(total_dec, cfg->decode_min_chunk, gran_dec);
   const int64_t chunk_pre = pick_chunk(total_pre, cfg->prefill_min_chunk, std::max(max_page, FI_GRANULE_PREFILL));
+  // a multi-head unit's chunk: the K/V bytes of a one-head chunk
+  const int32_t mh = fi_mh_heads(group, num_kv_heads);
+  const int64_t chunk_mh = std::max(gran_dec, chunk_dec / mh / gran_dec * gran_dec);
 
   // Chunks of every unit; split units become merge units in unit order.  In
   // a cascade plan every unit writes partial states and none is merged in
@@ -266,7 +283,7 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
   int32_t prefill_caches = 0;
   for (size_t ui = 0; ui < units.size(); ++ui) {
     const Unit& u = units[ui];
-    const int64_t chunk = u.tile == FI_TILE_DECODE ? chunk_dec : chunk_pre;
+    const int64_t chunk = u.tile == FI_TILE_DECODE ? (u.heads > 1 ? chunk_mh : chunk_dec) : chunk_pre;
     const int64_t weight = u.tile == FI_TILE_DECODE ? cfg->decode_cost_weight : cfg->prefill_cost_weight;
     if (u.tile == FI_TILE_PREFILL) prefill_caches |= u.b < num_shared ? 2 : 1;
     int64_t n = 0;
@@ -293,7 +310,7 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
     int64_t i = 0;
     auto emit = [&](int64_t k0, int64_t k1) {
       Chunk c;
-      c.cost = (k1 - k0 + FI_ITEM_COST_TOKENS) * weight;
+      c.cost = ((k1 - k0) * u.heads + FI_ITEM_COST_TOKENS) * weight;
       c.tile = u.tile;
       c.b = u.b;
       c.hk = u.hk;
@@ -304,7 +321,7 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
                                        u.row1,      int32_t(k0), int32_t(k1),
                                        base >= 0 ? int32_t(base + i * nrows) : -1, merge_id,
                                        rq.qo_start, rq.qo_len,   rq.page_start,
-                                       rq.kv_len,   0,           0,
+                                       rq.kv_len,   u.heads > 1 ? u.heads : 0, 0,
                                        0,           0};
       std::memcpy(c.fields, f, sizeof f);
       chunks.push_back(c);
@@ -332,19 +349,26 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
       const int32_t stile = srows <= FI_TILE_DECODE ? FI_TILE_DECODE : FI_TILE_PREFILL;
       const int32_t stiles = int32_t(ceil_div(srows, stile));
       const int64_t shift = int64_t(reqs[u.b].qo_start - blk.qo_start) * group;  // row r -> block row r + shift
-      for (int32_t ra = u.row0; ra < u.row1;) {
-        const int64_t rs = ra + shift;
-        const int32_t qt0 = int32_t(rs / stile);
-        const size_t si = size_t(first_unit[s]) + size_t(u.hk) * stiles + qt0;
-        const Unit& su = units[si];
-        const int32_t run_end = u.row0 + ((ra - u.row0) / FI_CASCADE_ROWS + 1) * FI_CASCADE_ROWS;
-        const int32_t rb = int32_t(std::min<int64_t>(std::min(u.row1, run_end), ra + (su.row1 - rs)));
-        const int32_t e[FI_CASCADE_INTS] = {u.b, u.hk, ra, rb,
-                                            int32_t(unit_n[si]), int32_t(unit_base[si] + (rs - su.row0)),
-                                            su.row1 - su.row0, int32_t(unit_n[ui]),
-                                            int32_t(unit_base[ui] + (ra - u.row0)), u.row1 - u.row0, 0, 0};
-        cascade_rows.insert(cascade_rows.end(), e, e + FI_CASCADE_INTS);
-        ra = rb;
+      // A multi-head unit's entries are per KV head, in one-head row numbering;
+      // head h's rows sit at offset h * G of the unit's partial rows.
+      for (int32_t h = 0; h < u.heads; ++h) {
+        const int32_t hk = u.hk + h;
+        const int32_t row0 = u.heads > 1 ? 0 : u.row0, row1 = u.heads > 1 ? group : u.row1;
+        const int64_t own0 = unit_base[ui] + (u.heads > 1 ? int64_t(h) * group : 0);  // partial row of row0
+        for (int32_t ra = row0; ra < row1;) {
+          const int64_t rs = ra + shift;
+          const int32_t qt0 = int32_t(rs / stile);
+          const size_t si = size_t(first_unit[s]) + size_t(hk) * stiles + qt0;
+          const Unit& su = units[si];
+          const int32_t run_end = row0 + ((ra - row0) / FI_CASCADE_ROWS + 1) * FI_CASCADE_ROWS;
+          const int32_t rb = int32_t(std::min<int64_t>(std::min(row1, run_end), ra + (su.row1 - rs)));
+          const int32_t e[FI_CASCADE_INTS] = {u.b, hk, ra, rb,
+                                              int32_t(unit_n[si]), int32_t(unit_base[si] + (rs - su.row0)),
+                                              su.row1 - su.row0, int32_t(unit_n[ui]),
+                                              int32_t(own0 + (ra - row0)), u.row1 - u.row0, 0, 0};
+          cascade_rows.insert(cascade_rows.end(), e, e + FI_CASCADE_INTS);
+          ra = rb;
+        }
       }
     }
   }

@@ -8,8 +8,13 @@
 //                  the cascade fields, 0 in a one-level plan)
 //   cta_indptr   num_ctas + 1 entries: CTA c runs items [cta_indptr[c], cta_indptr[c+1])
 //   items        FI_ITEM_INTS each: {b, hk, row0, row1, kv0, kv1, part, merge,
-//                  qo_start, qo_len, page_start, kv_len, 0, 0, 0, 0}
+//                  qo_start, qo_len, page_start, kv_len, heads, 0, 0, 0}
 //                  rows are packed rows of request b (row = token * G + g),
+//                  heads = 0 for one KV head hk; heads = FI_MH_ROWS / G for
+//                  a multi-head decode unit, which takes KV heads
+//                  hk .. hk + heads - 1 of a one-token request of the plan's
+//                  own page-1 cache at once (row = head offset * G + g; see
+//                  fi_mh_heads),
 //                  [kv0, kv1) the KV token range of this chunk,
 //                  part = first fp32 partial-state row or -1 (unsplit),
 //                  merge = merge unit or -1; then a copy of request b's
@@ -62,6 +67,8 @@
 #define FI_GRANULE_DECODE 64
 #define FI_GRANULE_PREFILL 128
 #define FI_ITEM_COST_TOKENS 256  // fixed cost of a work item in the deal, in KV tokens of its class
+#define FI_MH_ROWS 32            // packed query rows of a multi-head decode unit (heads * G)
+#define FI_ITEM_HEADS 12         // item field: KV heads of a multi-head unit, else 0
 
 enum {
   FI_H_MAGIC = 0,
@@ -110,3 +117,13 @@ static inline int64_t fi_rope_table_rows(int32_t rope_max_positions) {
 static inline int64_t fi_rope_table_offset(int64_t plan_ints) { return (plan_ints * 4 + 255) / 256 * 256; }
 
 static inline int64_t fi_partial_o_offset(int64_t max_partial_rows) { return (max_partial_rows + 63) / 64 * 64; }
+
+// KV heads of a multi-head decode unit for GQA group G and Hkv KV heads, or 1
+// when such units cannot be formed: the unit's FI_MH_ROWS packed rows are
+// eight groups of four rows, each group inside one KV head (G a multiple of
+// 4), and the heads tile [0, Hkv).
+static inline int32_t fi_mh_heads(int32_t group, int32_t num_kv_heads) {
+  if (group < 4 || group > FI_MH_ROWS / 2 || group % 4) return 1;
+  const int32_t h = FI_MH_ROWS / group;
+  return num_kv_heads % h == 0 ? h : 1;
+}

@@ -58,13 +58,31 @@ def test_plan_matches_reference_random(seed):
 
 
 def _items(ws, off_items, n_items):
-    """The plan's work items, [item, field]: the first 8 fields (the request's
-    copy that follows them is checked against the request table)."""
+    """The plan's work items, [item, field]: the first 8 fields, and per item
+    its KV-head count (1, or H of a multi-head unit); the request's copy that
+    follows the 8 fields is checked against the request table."""
     full = ws[off_items:off_items + plan_ref.ITEM_INTS * n_items].reshape(-1, plan_ref.ITEM_INTS)
     off_req = ws[10]
     req = ws[off_req:off_req + 4 * ws[4]].reshape(-1, 4)
-    assert np.array_equal(full[:, 8:12], req[full[:, 0]]) and np.all(full[:, 12:] == 0)
-    return full[:, :8]
+    assert np.array_equal(full[:, 8:12], req[full[:, 0]]) and np.all(full[:, 13:] == 0)
+    assert np.all(np.isin(full[:, 12], (0, 2, 4, 8)))
+    return full[:, :8], np.maximum(full[:, 12], 1)
+
+
+def _per_head(items, heads, G):
+    """Items with every multi-head item split into one item per KV head, in
+    one-head numbering: head hk + h holds rows 0..G of the unit's rows
+    h*G .. h*G + G - 1, so its partial rows start at part + h*G."""
+    out = []
+    for it, H in zip(items, heads):
+        b, hk, r0, r1, k0, k1, part, merge = (int(x) for x in it)
+        if H == 1:
+            out.append((b, hk, r0, r1, k0, k1, part, merge))
+            continue
+        assert (r0, r1) == (0, H * G) and H * G == plan_ref.MH_ROWS and hk % H == 0
+        for h in range(H):
+            out.append((b, hk + h, 0, G, k0, k1, part + h * G if part >= 0 else -1, merge))
+    return np.array(out, dtype=np.int64).reshape(-1, 8)
 
 
 def _check_invariants(ws, qop, kv, hq, hkv, causal, cfgd):
@@ -73,52 +91,60 @@ def _check_invariants(ws, qop, kv, hq, hkv, causal, cfgd):
     off_cta, off_items, off_merge, off_cnt, off_req = ws[6], ws[7], ws[8], ws[9], ws[10]
     cta = ws[off_cta:off_cta + C + 1]
     assert cta[0] == 0 and cta[-1] == n_items and np.all(np.diff(cta) >= 0)
-    items = _items(ws, off_items, n_items)
+    items, heads = _items(ws, off_items, n_items)
     assert np.all(ws[off_cnt:off_cnt + n_merge] == 0)
     req = ws[off_req:off_req + 4 * (len(qop) - 1)].reshape(-1, 4)
     assert np.array_equal(req[:, 3], kv)
+    # multi-head items: one query token of a decode-class request
+    for it in items[heads > 1]:
+        assert qop[it[0] + 1] - qop[it[0]] == 1
     # coverage: per (b, hk) the row ranges tile [0, R); per unit the chunks tile [0, kv_eff)
     by_unit = {}
-    for it in items:
+    for it, H in zip(items, heads):
         b, hk, r0, r1, k0, k1, part, merge = (int(x) for x in it)
-        by_unit.setdefault((b, hk, r0, r1), []).append((k0, k1, part, merge))
+        by_unit.setdefault((b, hk, r0, r1, int(H)), []).append((k0, k1, part, merge))
+    rows_of = {}  # (b, hk) -> [(r0, r1) in one-head numbering]
+    for (b, hk, r0, r1, H) in by_unit:
+        for h in range(H):
+            rows_of.setdefault((b, hk + h), []).append((r0, r1) if H == 1 else (0, G))
     for b in range(len(qop) - 1):
         R = int(qop[b + 1] - qop[b]) * G
         for hk in range(hkv):
-            units = sorted((r0, r1) for (bb, h, r0, r1) in by_unit if bb == b and h == hk)
+            units = sorted(rows_of.get((b, hk), []))
             if R == 0:
                 assert not units
                 continue
             assert units[0][0] == 0 and units[-1][1] == R
             assert all(units[i][1] == units[i + 1][0] for i in range(len(units) - 1))
-            for (r0, r1) in units:
-                chunks = sorted(by_unit[(b, hk, r0, r1)])
-                lq, lkv = int(qop[b + 1] - qop[b]), int(kv[b])
-                t_last = (r1 - 1) // G
-                need = min(lkv, max(0, lkv - lq + t_last + 1)) if causal else lkv
-                assert chunks[0][0] == 0 and chunks[-1][1] == need
-                assert all(chunks[i][1] == chunks[i + 1][0] for i in range(len(chunks) - 1))
-                if need > 0:
-                    assert all(k1 > k0 for (k0, k1, _, _) in chunks), "empty chunk in a non-empty unit"
-                else:
-                    assert len(chunks) == 1
-                if len(chunks) > 1:
-                    m = chunks[0][3]
-                    assert m >= 0 and all(c[3] == m for c in chunks)
-                    mu = ws[off_merge + 8 * m: off_merge + 8 * m + 8]
-                    assert tuple(mu[:4]) == (b, hk, r0, r1) and mu[4] == len(chunks)
-                    # merged after the run exactly when the unit is of the prefill class
-                    assert mu[6] == (1 if lq * G > 16 else 0) and mu[7] == 0
-                    parts = [c[2] for c in chunks]
-                    assert parts == [mu[5] + i * (r1 - r0) for i in range(len(chunks))]
-                else:
-                    assert chunks[0][2] == -1 and chunks[0][3] == -1
+    for (b, hk, r0, r1, H), chunks in by_unit.items():
+        chunks = sorted(chunks)
+        lq, lkv = int(qop[b + 1] - qop[b]), int(kv[b])
+        t_last = 0 if H > 1 else (r1 - 1) // G
+        need = min(lkv, max(0, lkv - lq + t_last + 1)) if causal else lkv
+        assert chunks[0][0] == 0 and chunks[-1][1] == need
+        assert all(chunks[i][1] == chunks[i + 1][0] for i in range(len(chunks) - 1))
+        if need > 0:
+            assert all(k1 > k0 for (k0, k1, _, _) in chunks), "empty chunk in a non-empty unit"
+        else:
+            assert len(chunks) == 1
+        if len(chunks) > 1:
+            m = chunks[0][3]
+            assert m >= 0 and all(c[3] == m for c in chunks)
+            mu = ws[off_merge + 8 * m: off_merge + 8 * m + 8]
+            assert tuple(mu[:4]) == (b, hk, r0, r1) and mu[4] == len(chunks)
+            # merged after the run exactly when the unit is of the prefill class
+            assert mu[6] == (1 if lq * G > 16 else 0) and mu[7] == 0
+            parts = [c[2] for c in chunks]
+            assert parts == [mu[5] + i * (r1 - r0) for i in range(len(chunks))]
+        else:
+            assert chunks[0][2] == -1 and chunks[0][3] == -1
     # LPT bound: max CTA load <= mean load + largest item
     w = {16: cfgd["decode_cost_weight"], plan_ref.TILE_PREFILL: cfgd["prefill_cost_weight"]}
     cost = []
-    for it in items:
+    for it, H in zip(items, heads):
         R = int(qop[it[0] + 1] - qop[it[0]]) * G
-        cost.append((int(it[5]) - int(it[4]) + plan_ref.ITEM_COST_TOKENS) * w[16 if R <= 16 else plan_ref.TILE_PREFILL])
+        cost.append(((int(it[5]) - int(it[4])) * int(H) + plan_ref.ITEM_COST_TOKENS)
+                    * w[16 if R <= 16 else plan_ref.TILE_PREFILL])
     cost = np.array(cost, dtype=np.int64)
     loads = np.array([cost[cta[c]:cta[c + 1]].sum() for c in range(C)])
     if cost.size:
@@ -136,7 +162,7 @@ def _check_variant_coverage(ws, qop, kv, hq, hkv, causal, page, window, sink):
     disjoint, start on the class granule and none is invisible to all rows."""
     G = hq // hkv
     n_items, off_items = ws[1], ws[7]
-    items = _items(ws, off_items, n_items)
+    items = _per_head(*_items(ws, off_items, n_items), G)
     by_unit = {}
     for it in items:
         b, hk, r0, r1, k0, k1 = (int(x) for x in it[:6])
@@ -197,8 +223,8 @@ def test_window_skips_chunks():
         cfg, _ = _cfg(num_ctas=152, **kw)
         st, ws, _ = fi.plan_host(cfg, qop, kvp, kvi, lpl, 32, 8, 128, 16, 0)
         assert st == 0
-        items = _items(ws, ws[7], ws[1])
-        return int((items[:, 5] - items[:, 4]).sum())
+        items, heads = _items(ws, ws[7], ws[1])
+        return int(((items[:, 5] - items[:, 4]) * heads).sum())
 
     full = planned_kv()
     windowed = planned_kv(window_left=4096, sink_tokens=4)
@@ -395,7 +421,7 @@ def _check_cascade_invariants(ws, shared, own, kv, skv, hq, hkv, causal):
     n_items, n_merge, C = ws[1], ws[2], ws[3]
     assert n_merge == 0 and ws[26] == S
     off_items, off_req, off_cas, n_cas = ws[7], ws[10], ws[27], ws[28]
-    items = _items(ws, off_items, n_items)
+    items = _per_head(*_items(ws, off_items, n_items), G)
     reqs = ws[off_req:off_req + 4 * ws[4]].reshape(-1, 4)
     ents = ws[off_cas:off_cas + 12 * n_cas].reshape(-1, 12)
     assert np.all(items[:, 6] >= 0) and np.all(items[:, 7] == -1)
@@ -459,6 +485,35 @@ def test_cascade_plan_of_the_shared_prefix_workload():
     st, ws, info = _cascade_both(cfg, cfgd, shared, own, 32, 8, 0)
     assert st == 0 and info.prefill_caches == 2  # the block's 256-row units read the shared cache on tensor cores
     _check_cascade_invariants(ws, shared, own, suf, np.array([8192]), 32, 8, 0)
+    # every suffix unit takes all 8 KV heads of its branch (32 rows: G = 4)
+    items, heads = _items(ws, ws[7], ws[1])
+    own_items = items[:, 0] >= 1
+    assert np.all(heads[own_items] == 8) and np.all(heads[~own_items] == 1)
+    assert np.all(items[own_items, 1] == 0) and np.all(items[own_items, 3] == 32)
+
+
+@pytest.mark.parametrize("group,hkv,heads", [(4, 8, 8), (8, 4, 4), (16, 2, 2), (4, 4, 1), (2, 8, 1), (8, 2, 1)])
+def test_multi_head_units_of_a_page_1_decode(group, hkv, heads):
+    """One-token requests on pages of 1 form units of 32 / G KV heads when G
+    is a multiple of 4 and those heads tile Hkv; a longer request, another
+    page size or a RoPE plan keeps one head per unit."""
+    rng = np.random.default_rng(4100 + group)
+    kv = rng.integers(1, 2000, size=12)
+    qo = np.ones(12, np.int64)
+    qo[3] = 3  # a three-token request keeps one head per unit
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    for page, rope in ((1, 0), (2, 0), (1, 4096)):
+        kvp, lpl = workloads._pages_for(kv, page)
+        nnz = int(kvp[-1])
+        kvi = rng.permutation(nnz).astype(np.int32)
+        cfg, cfgd = _cfg(num_ctas=152, rope_max_positions=rope)
+        st, ws, _ = _plan_both(cfg, cfgd, qop, kvp, kvi, lpl, hkv * group, hkv, page, 1, nnz)
+        assert st == 0
+        _check_invariants(ws, qop, kv, hkv * group, hkv, 1, cfgd)
+        items, h = _items(ws, ws[7], ws[1])
+        want = heads if (page == 1 and rope == 0) else 1
+        assert np.all(h[items[:, 0] == 3] == 1)
+        assert np.all(h[items[:, 0] != 3] == want)
 
 
 @pytest.mark.parametrize("case,status", [
