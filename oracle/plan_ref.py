@@ -52,7 +52,8 @@ Rule:
  6. Output: header (with the variant: window, sink, soft-cap bits, and for
     RoPE its position capacity, theta and scale bits and the table offset;
     then the count of late units, the partial rows used, the batch's query
-    tokens, the cascade fields, the count of 16-row items and a zero field), per-CTA
+    tokens, the cascade fields, the count of 16-row items and the most rows of
+    a cascade merge entry (0 without cascade)), per-CTA
     CSR offsets, items in CTA order (an item: its 8 fields, its request's
     table entry, H for a multi-head unit or 0, three zeros; within a CTA the 256-row items first,
     then the 16-row items, each in the order dealt), merge units, zeroed merge
@@ -379,7 +380,8 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
                         window, sink, bits(cap), rope_max,
                         bits(theta) if rope_max > 0 else 0, bits(rscale) if rope_max > 0 else 0, rope_off,
                         sum(1 for m in merges if m[6]), part_rows, total_qo, num_shared,
-                        off_cascade if cascade else 0, len(entries), shared_page_size if cascade else 0, n_dec, 0]
+                        off_cascade if cascade else 0, len(entries), shared_page_size if cascade else 0, n_dec,
+                        max((e[3] - e[2] for e in entries), default=0)]
     pos = 0
     for c in range(C):
         ws[off_cta + c] = pos

@@ -79,6 +79,30 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
   if (part == 0) so[st] = lse;
 }
 
+// Programmatic dependent launch: a merge that follows the run is enqueued
+// with programmatic stream serialization, and the run lets its dependents be
+// scheduled from its start, so the merge's blocks take SMs as the run's CTAs
+// leave instead of after the whole grid has finished and a new launch has
+// gone through; each waits here until the run grid has completed and its
+// memory is visible (launched without the attribute, the wait returns at
+// once).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_behind_run(void (*kernel)(KArgs...), int32_t blocks, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, KArgs(args)...);
+}
+
 // Late merge of split units (those the plan marks late: prefill-class
 // tiles), launched after the run on the same stream.  Tasks are (merge unit,
 // packed row) pairs, unit-major, walked by every warp of a fixed grid with a
@@ -95,6 +119,7 @@ __global__ void __launch_bounds__(256) late_merge_kernel(const int32_t* __restri
                                                          T* o, int64_t o_stride_tok, int64_t o_stride_head,
                                                          float* lse, int num_qo_heads, int group) {
   const int lane = threadIdx.x & 31;
+  grid_dependency_wait();  // launched early behind the run: its partial rows are written from here on
   if (iws[FI_H_STATUS] != 0 || iws[FI_H_NUM_LATE_MERGE] == 0) return;
   const int64_t tasks = int64_t(iws[FI_H_NUM_MERGE]) * FI_TILE_PREFILL;
   const int32_t* merge = iws + iws[FI_H_OFF_MERGE];
@@ -159,10 +184,9 @@ __global__ void __launch_bounds__(256) late_merge_kernel(const int32_t* __restri
 
 template <typename T>
 cudaError_t launch_late_merge(const RunParams& p, int32_t blocks, cudaStream_t s) {
-  late_merge_kernel<T><<<unsigned(blocks), 256, 0, s>>>(p.iws, p.fws, p.partial_o_offset, reinterpret_cast<T*>(p.o),
-                                                        p.o_stride_tok, p.o_stride_head, p.lse, p.num_qo_heads,
-                                                        p.group);
-  return cudaGetLastError();
+  return launch_behind_run(late_merge_kernel<T>, blocks, s, static_cast<const int32_t*>(p.iws),
+                           static_cast<const float*>(p.fws), p.partial_o_offset, reinterpret_cast<T*>(p.o),
+                           p.o_stride_tok, p.o_stride_head, p.lse, int(p.num_qo_heads), int(p.group));
 }
 
 // RoPE table: (cos, sin) of (pos / scale) * theta^(-2i/128) for pos <
@@ -631,30 +655,58 @@ fi_status build_cache(KvCache* kc, const CacheArgs& c, CUtensorMapDataType tt, i
 // come from the workspace header (a graph captured once replays correctly
 // for any later cascade plan).  Lane l holds dims 4l..4l+3.  Nothing is
 // written when the status word reports an error.
+constexpr int kMergeGroup = 16;  // partial states whose O slices a merge lane loads at once
+
 template <typename T>
 __global__ void __launch_bounds__(256) cascade_merge_kernel(const int32_t* __restrict__ iws,
                                                             const float* __restrict__ fws, int64_t partial_o_offset,
                                                             T* o, int64_t o_stride_tok, int64_t o_stride_head,
                                                             float* lse, int num_qo_heads, int group) {
   const int lane = threadIdx.x & 31;
-  if (iws[FI_H_STATUS] != 0) return;
-  const int64_t tasks = int64_t(iws[FI_H_NUM_CASCADE]) * FI_CASCADE_ROWS;
+  // (entry, row) tasks, the plan's largest entry giving the row count of all.
+  // The plan (copied in before the run) is read before the dependency wait,
+  // the task's entry included; the status word and the partial rows, which
+  // the run writes, after it.
+  const int rows_max = iws[FI_H_CASCADE_ROWS_MAX];
+  const int64_t tasks = int64_t(iws[FI_H_NUM_CASCADE]) * rows_max;
   const int32_t* ent = iws + iws[FI_H_OFF_CASCADE];
   const int32_t* reqs = iws + iws[FI_H_OFF_REQUESTS];
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t task = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks; task += warps) {
-    const int4* e4 = reinterpret_cast<const int4*>(ent + FI_CASCADE_INTS * (task / FI_CASCADE_ROWS));
-    const int4 e0 = __ldg(e4), e1 = __ldg(e4 + 1), e2 = __ldg(e4 + 2);
-    // {b, hk, row0, row1}, {n0, base0, stride0, n1}, {base1, stride1, 0, 0}
-    const int r = int(task % FI_CASCADE_ROWS);
+  int64_t task = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int4 e0, e1, e2;  // {b, hk, row0, row1}, {n0, base0, stride0, n1}, {base1, stride1, 0, 0}
+  int64_t qo_start = 0;
+  auto load_entry = [&] {
+    const int4* e4 = reinterpret_cast<const int4*>(ent + FI_CASCADE_INTS * (task / rows_max));
+    e0 = __ldg(e4);
+    e1 = __ldg(e4 + 1);
+    e2 = __ldg(e4 + 2);
+    qo_start = __ldg(reqs + FI_REQ_INTS * e0.x);
+  };
+  if (task < tasks) load_entry();
+  grid_dependency_wait();  // launched early behind the run: its partial rows are written from here on
+  if (iws[FI_H_STATUS] != 0) return;
+  for (bool first = true; task < tasks; task += warps, first = false) {
+    if (!first) load_entry();
+    const int r = int(task % rows_max);
     if (r >= e0.w - e0.z) continue;
     const int n0 = e1.x, n = e1.x + e1.w;
     // part c (c < n): partial row of the row's c-th state
     auto part_row = [&](int c) -> int64_t {
       return c < n0 ? int64_t(e1.y) + int64_t(c) * e1.z + r : int64_t(e2.x) + int64_t(c - n0) * e2.y + r;
     };
-    float M = -INFINITY;
-    for (int c0 = 0; c0 < n; c0 += 32)
+    auto o_of = [&](int c) {
+      return __ldcg(reinterpret_cast<const float4*>(fws + partial_o_offset + part_row(c) * kHeadDim) + lane);
+    };
+    // This lane's LSE (state `lane`) and the first kMergeGroup states' O
+    // slices depend only on the entry: they go out together, so a row of at
+    // most kMergeGroup states costs two dependent rounds (entry, states).
+    const float lse_lane = lane < n ? __ldcg(fws + part_row(lane)) : -INFINITY;
+    float4 v[kMergeGroup];
+#pragma unroll
+    for (int u = 0; u < kMergeGroup; ++u)
+      if (u < n) v[u] = o_of(u);
+    float M = lse_lane;
+    for (int c0 = 32; c0 < n; c0 += 32)
       M = fmaxf(M, c0 + lane < n ? __ldcg(fws + part_row(c0 + lane)) : -INFINITY);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -662,18 +714,17 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(const int32_t* __res
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
       for (int c0 = 0; c0 < n; c0 += 32) {
-        const float w_mine =
-            c0 + lane < n ? ex2((__ldcg(fws + part_row(c0 + lane)) - M) * 1.4426950408889634f) : 0.f;
+        const float lse_c = c0 == 0 ? lse_lane : c0 + lane < n ? __ldcg(fws + part_row(c0 + lane)) : -INFINITY;
+        const float w_mine = c0 + lane < n ? ex2((lse_c - M) * 1.4426950408889634f) : 0.f;
         const int cn = min(32, n - c0);
-        for (int g0 = 0; g0 < cn; g0 += 8) {
-          float4 v[8];
+        for (int g0 = 0; g0 < cn; g0 += kMergeGroup) {
+          if (c0 + g0 > 0) {  // later groups: their O slices now
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (g0 + u < cn)
-              v[u] = __ldcg(reinterpret_cast<const float4*>(fws + partial_o_offset +
-                                                            part_row(c0 + g0 + u) * kHeadDim) + lane);
+            for (int u = 0; u < kMergeGroup; ++u)
+              if (g0 + u < cn) v[u] = o_of(c0 + g0 + u);
+          }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+          for (int u = 0; u < kMergeGroup; ++u) {
             const float w = __shfl_sync(0xffffffffu, w_mine, (g0 + u) & 31);
             if (g0 + u < cn) {
               Ls += w;
@@ -690,7 +741,7 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(const int32_t* __res
     const int row = e0.z + r;
     const int t = row / group;
     const int head = e0.y * group + (row - t * group);
-    const int64_t tok = int64_t(reqs[FI_REQ_INTS * e0.x]) + t;
+    const int64_t tok = qo_start + t;
     uint2 packed;
     packed.x = Elem<T>::from_float2(acc.x * inv, acc.y * inv);
     packed.y = Elem<T>::from_float2(acc.z * inv, acc.w * inv);
@@ -701,10 +752,9 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(const int32_t* __res
 
 template <typename T>
 cudaError_t launch_cascade_merge(const RunParams& p, int32_t blocks, cudaStream_t s) {
-  cascade_merge_kernel<T><<<unsigned(blocks), 256, 0, s>>>(p.iws, p.fws, p.partial_o_offset,
-                                                           reinterpret_cast<T*>(p.o), p.o_stride_tok,
-                                                           p.o_stride_head, p.lse, p.num_qo_heads, p.group);
-  return cudaGetLastError();
+  return launch_behind_run(cascade_merge_kernel<T>, blocks, s, static_cast<const int32_t*>(p.iws),
+                           static_cast<const float*>(p.fws), p.partial_o_offset, reinterpret_cast<T*>(p.o),
+                           p.o_stride_tok, p.o_stride_head, p.lse, int(p.num_qo_heads), int(p.group));
 }
 
 // The run behind both entry points: the plan's own cache, and for a cascade

@@ -375,6 +375,10 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
   const int64_t n_items = int64_t(chunks.size());
   const int64_t n_merge = int64_t(merge_rows.size() / FI_MERGE_INTS);
   const int64_t n_cascade = int64_t(cascade_rows.size() / FI_CASCADE_INTS);
+  int32_t cascade_rows_max = 0;  // the merge launch gives each entry this many row tasks
+  for (int64_t e = 0; e < n_cascade; ++e)
+    cascade_rows_max = std::max(cascade_rows_max, cascade_rows[size_t(e) * FI_CASCADE_INTS + 3] -
+                                                      cascade_rows[size_t(e) * FI_CASCADE_INTS + 2]);
   if (n_items > cfg->max_items || n_merge > cfg->max_merge_units || n_cascade > cfg->max_merge_units ||
       partial_rows > cfg->max_partial_rows || partial_rows > INT32_MAX)
     return FI_ERR_CAPACITY;
@@ -450,7 +454,7 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
       window,               sink,               cap_bits,           rope_max,
       theta_bits,           scale_bits,         rope_off,           n_late,
       int32_t(partial_rows), total_qo,          num_shared,         cascade ? int32_t(off_cascade) : 0,
-      int32_t(n_cascade),   cascade ? shared_page_size : 0, int32_t(n_decode), 0};
+      int32_t(n_cascade),   cascade ? shared_page_size : 0, int32_t(n_decode), cascade_rows_max};
   std::memcpy(ws, header, sizeof header);
 
   fi_plan_info info;

@@ -101,7 +101,8 @@ enum {
   FI_H_OFF_CASCADE = 27,      // cascade: offset of the cascade merge entries
   FI_H_NUM_CASCADE = 28,      // cascade: merge entries
   FI_H_SHARED_PAGE_SIZE = 29, // cascade: page size of the shared KV cache
-  FI_H_NUM_DECODE_ITEMS = 30  // items of 16-row tiles (the CUDA-core path); 31 stays 0
+  FI_H_NUM_DECODE_ITEMS = 30, // items of 16-row tiles (the CUDA-core path)
+  FI_H_CASCADE_ROWS_MAX = 31  // cascade: the most packed rows of one merge entry; 0 otherwise
 };
 
 #define FI_ROPE_PAIRS 64  // dims i and i + 64 of head_dim 128 form a rotated pair

@@ -165,3 +165,27 @@ def test_one_level_run_refuses_a_cascade_plan():
         fi.run(ws, info, own.q, own.k, own.v, torch.as_tensor(own.kv_indices, device=DEV), torch.empty_like(own.q),
                None, own.sm_scale)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("seed,kv_max,shared_min,shared_max", [
+    (341, 3, 6000, 9000),   # long blocks on the tensor cores, one to three own keys per branch
+    (342, 900, 0, 40),      # short blocks, long own keys
+])
+def test_cascade_long_blocks_or_long_suffixes(seed, kv_max, shared_min, shared_max):
+    """Blocks of 20 to 28 packed rows (tensor-core units) with one-token
+    branches at page 1 (multi-head units), either side the longer one; the
+    merge launch behind the run waits for it, and two runs give the same
+    bits."""
+    d = workloads.cascade_batch(seed, [6, 7, 5], 1, kv_max, shared_max, 32, 8, 1, 16, 0, device=DEV,
+                                shared_min=shared_min)
+    o, lse, info, ws = cascade_run(d)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0 and info.num_cascade_merges > 0
+    assert info.prefill_caches & 2  # the blocks' units run on the tensor cores
+    o_ref, l_ref = oracle.attention(oracle_problem(d["flat"]))
+    n = d["own"].total_qo
+    err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
+    assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
+    o2, lse2, _, _ = cascade_run(d, ws=ws, o=torch.full_like(o, float("nan")), lse=torch.full_like(lse, float("nan")))
+    torch.cuda.synchronize()
+    assert torch.equal(o2[:n], o[:n]) and torch.equal(lse2[:n], lse[:n])

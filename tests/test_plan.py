@@ -424,6 +424,7 @@ def _check_cascade_invariants(ws, shared, own, kv, skv, hq, hkv, causal):
     items = _per_head(*_items(ws, off_items, n_items), G)
     reqs = ws[off_req:off_req + 4 * ws[4]].reshape(-1, 4)
     ents = ws[off_cas:off_cas + 12 * n_cas].reshape(-1, 12)
+    assert ws[31] == (ents[:, 3] - ents[:, 2]).max()  # the merge launch's row tasks per entry
     assert np.all(items[:, 6] >= 0) and np.all(items[:, 7] == -1)
     parts = {}  # (b, hk, row) -> [(kv0, kv1, partial row)]
     for b, hk, r0, r1, k0, k1, part, _ in items:
