@@ -23,7 +23,7 @@ constexpr int kRowsPerGroup = 4;       // query rows a half-warp carries in regi
 constexpr int kGroupsPerPass = 8;
 constexpr int kRowsPerPass = kRowsPerGroup * kGroupsPerPass;
 constexpr int kHalfWarps = 2 * kConsumerWarps;
-constexpr int kTokBlock = 4;           // tokens a half-warp scores before one softmax update
+constexpr int kTokBlock = 8;           // tokens a half-warp scores before one softmax update
 constexpr float kLazyRescale = 8.0f;   // log2 units: keep a stale max until it is 2^8 off
 
 // Tensor-core path (prefill-class items of up to two 128-row M tiles):
@@ -105,10 +105,12 @@ __device__ __forceinline__ const KvCache& cache_of(const RunParams& p, int32_t b
 struct DecodeBufs {
   uint16_t k[kStages][kStageTokens][kHeadDim];
   uint16_t v[kStages][kStageTokens][kHeadDim];
-  float comb_o[kHalfWarps][kRowsPerGroup][kHeadDim];
+  union {  // xch while the stages stream, comb_o in the combine after them
+    float comb_o[kHalfWarps][kRowsPerGroup][kHeadDim];
+    float4 xch[kHalfWarps][kTokBlock + 1];  // per half-warp: p of each token (4 rows), then alpha
+  };
   float comb_m[kHalfWarps][kRowsPerGroup];
   float comb_l[kHalfWarps][kRowsPerGroup];
-  float4 xch[kHalfWarps][kTokBlock + 1];  // per half-warp: p of each token (4 rows), then alpha
 };
 
 // Every [128][64] block is one 16 KB operand half: 128 rows of 64 elements

@@ -584,7 +584,14 @@ __device__ __forceinline__ uint32_t consume_pass(const RunParams& p, RunSmem& sm
           const bool seen = kMask ? (unsigned(tok - vlo) < vis_cnt || tok < vsink) : tok <= vhi;
           sc[u] = seen ? sfull : -INFINITY;
         }
-        float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        float mt[kTokBlock];  // pairwise (tree) maximum of the block's logits
+#pragma unroll
+        for (int u = 0; u < kTokBlock; ++u) mt[u] = sc[u];
+#pragma unroll
+        for (int w = kTokBlock / 2; w > 0; w >>= 1)
+#pragma unroll
+          for (int u = 0; u < w; ++u) mt[u] = fmaxf(mt[u], mt[u + w]);
+        const float mx = mt[0];
         float m_new = m;
         if (mx > m + kLazyRescale) m_new = mx;  // also taken on the first visible key (m = -inf)
         const float alpha = (m_new == m) ? 1.f : ex2(m - m_new);
@@ -641,7 +648,9 @@ __device__ __forceinline__ uint32_t consume_pass(const RunParams& p, RunSmem& sm
     vsink -= kStageTokens;
   }
 
-  // This half-warp's state -> shared memory, then merge per row.
+  // This half-warp's state -> shared memory, then merge per row (comb_o
+  // shares its bytes with the exchange buffers of the stage loop).
+  named_barrier_sync(1, 32 * kConsumerWarps);
 #pragma unroll
   for (int r = 0; r < kRowsPerGroup; ++r) {
     float4* dst = reinterpret_cast<float4*>(&sm.dec.comb_o[hwid][r][L * 8]);
