@@ -57,8 +57,8 @@ typedef struct {
     int64_t max_partial_rows;    /* rows of fp32 partial state (head_dim floats + 1 LSE each) */
     int32_t decode_min_chunk;    /* smallest KV chunk of a 16-row tile, tokens (default 256) */
     int32_t prefill_min_chunk;   /* smallest KV chunk of a 256-row tile, tokens (default 1024) */
-    int32_t decode_cost_weight;  /* cost of one KV token in a 16-row tile (default 4) */
-    int32_t prefill_cost_weight; /* cost of one KV token in a 256-row tile (default 6) */
+    int32_t decode_cost_weight;  /* cost of one KV token in a 16-row tile (default 8) */
+    int32_t prefill_cost_weight; /* cost of one KV token in a 256-row tile (default 9) */
     int32_t split_factor;        /* target chunks per CTA per tile class (default 1) */
     /* Mask and logit variant, constant for a model (FlashInfer 0.6 wiki page,
      * "Blackwell (SM100/SM103) 전용 경로 / CuTe-DSL GQA Decode 커널": sliding

@@ -144,8 +144,8 @@ def default_plan_config(device: int = 0, **overrides) -> PlanConfig:
 def make_plan_config(num_ctas: int, **overrides) -> PlanConfig:
     """A config without asking the device (host-side planning and tests)."""
     cfg = PlanConfig(num_ctas=num_ctas, max_batch=8192, max_items=1 << 17, max_merge_units=1 << 15,
-                     max_partial_rows=1 << 19, decode_min_chunk=256, prefill_min_chunk=1024, decode_cost_weight=4,
-                     prefill_cost_weight=6, split_factor=1, window_left=-1, sink_tokens=0, logits_soft_cap=0.0,
+                     max_partial_rows=1 << 19, decode_min_chunk=256, prefill_min_chunk=1024, decode_cost_weight=8,
+                     prefill_cost_weight=9, split_factor=1, window_left=-1, sink_tokens=0, logits_soft_cap=0.0,
                      rope_max_positions=0, rope_theta=10000.0, rope_scale=1.0)
     for k, v in overrides.items():
         setattr(cfg, k, v)

@@ -547,8 +547,8 @@ extern "C" fi_status fi_default_plan_config(int device, fi_plan_config* out) {
   out->max_partial_rows = int64_t(1) << 19;
   out->decode_min_chunk = 256;
   out->prefill_min_chunk = 1024;
-  out->decode_cost_weight = 4;
-  out->prefill_cost_weight = 6;
+  out->decode_cost_weight = 8;
+  out->prefill_cost_weight = 9;
   out->split_factor = 1;
   out->window_left = -1;
   out->sink_tokens = 0;
