@@ -648,6 +648,59 @@ __device__ __forceinline__ uint32_t consume_pass(const RunParams& p, RunSmem& sm
     vsink -= kStageTokens;
   }
 
+  // Eight row groups (a pass of more than 16 rows): each warp holds one
+  // group, its two half-warps the same 4 rows over different tokens.  Their
+  // states merge by shuffles, half-warp 0's first, and half-warp h writes
+  // rows 2h and 2h + 1; no shared memory and no barrier.
+  if (ng == kGroupsPerPass) {
+    float w0[kRowsPerGroup], w1[kRowsPerGroup], Mr[kRowsPerGroup], Lr[kRowsPerGroup];
+#pragma unroll
+    for (int r = 0; r < kRowsPerGroup; ++r) {
+      const float m0 = __shfl_sync(0xffffffffu, m, r * 4), m1 = __shfl_sync(0xffffffffu, m, 16 + r * 4);
+      const float l0 = __shfl_sync(0xffffffffu, l, r * 4), l1 = __shfl_sync(0xffffffffu, l, 16 + r * 4);
+      Mr[r] = fmaxf(m0, m1);
+      w0[r] = m0 == -INFINITY ? 0.f : ex2(m0 - Mr[r]);
+      w1[r] = m1 == -INFINITY ? 0.f : ex2(m1 - Mr[r]);
+      Lr[r] = w0[r] * l0 + w1[r] * l1;
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerGroup; ++r) {
+      const float inv = Lr[r] > 0.f ? 1.f / Lr[r] : 0.f;
+      float v[8];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float2 x = o[r][c];
+        const float2 y = make_float2(__shfl_xor_sync(0xffffffffu, x.x, 16), __shfl_xor_sync(0xffffffffu, x.y, 16));
+        const float2 a = half ? y : x, b = half ? x : y;  // half-warp 0's state first in both halves
+        v[2 * c] = (a.x * w0[r] + b.x * w1[r]) * inv;
+        v[2 * c + 1] = (a.y * w0[r] + b.y * w1[r]) * inv;
+      }
+      const int prow = prow0 + g * kRowsPerGroup + r;
+      if ((r >> 1) != half || prow >= nrows) continue;
+      const float lse_v = Lr[r] > 0.f ? (Mr[r] + __log2f(Lr[r])) * 0.69314718055994531f : -INFINITY;
+      if (item.part < 0) {
+        const int row = item.row0 + prow;
+        const int t = row_token(item, row, G);
+        const int head = item.hk * G + (row - t * G);
+        const int64_t tok = rq.qo_start + t;
+        uint4 packed;
+        packed.x = Elem<T>::from_float2(v[0], v[1]);
+        packed.y = Elem<T>::from_float2(v[2], v[3]);
+        packed.z = Elem<T>::from_float2(v[4], v[5]);
+        packed.w = Elem<T>::from_float2(v[6], v[7]);
+        *reinterpret_cast<uint4*>(p.o + tok * p.o_stride_tok + int64_t(head) * p.o_stride_head + L * 8) = packed;
+        if (L == 0 && p.lse) p.lse[tok * p.num_qo_heads + head] = lse_v;
+      } else {
+        const int64_t prw = int64_t(item.part) + prow;
+        float4* dst = reinterpret_cast<float4*>(p.fws + p.partial_o_offset + prw * kHeadDim + L * 8);
+        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+        if (L == 0) p.fws[prw] = lse_v;
+      }
+    }
+    return it;
+  }
+
   // This half-warp's state -> shared memory, then merge per row (comb_o
   // shares its bytes with the exchange buffers of the stage loop).
   named_barrier_sync(1, 32 * kConsumerWarps);
