@@ -79,30 +79,6 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const T* __restrict__
   if (part == 0) so[st] = lse;
 }
 
-// Programmatic dependent launch: a merge that follows the run is enqueued
-// with programmatic stream serialization, and the run lets its dependents be
-// scheduled from its start, so the merge's blocks take SMs as the run's CTAs
-// leave instead of after the whole grid has finished and a new launch has
-// gone through; each waits here until the run grid has completed and its
-// memory is visible (launched without the attribute, the wait returns at
-// once).
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch_behind_run(void (*kernel)(KArgs...), int32_t blocks, cudaStream_t s, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(blocks));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, KArgs(args)...);
-}
-
 // Late merge of split units (those the plan marks late: prefill-class
 // tiles), launched after the run on the same stream.  Tasks are (merge unit,
 // packed row) pairs, unit-major, walked by every warp of a fixed grid with a
@@ -184,7 +160,7 @@ __global__ void __launch_bounds__(256) late_merge_kernel(const int32_t* __restri
 
 template <typename T>
 cudaError_t launch_late_merge(const RunParams& p, int32_t blocks, cudaStream_t s) {
-  return launch_behind_run(late_merge_kernel<T>, blocks, s, static_cast<const int32_t*>(p.iws),
+  return launch_behind_run(late_merge_kernel<T>, blocks, 256, s, static_cast<const int32_t*>(p.iws),
                            static_cast<const float*>(p.fws), p.partial_o_offset, reinterpret_cast<T*>(p.o),
                            p.o_stride_tok, p.o_stride_head, p.lse, int(p.num_qo_heads), int(p.group));
 }
@@ -752,7 +728,7 @@ __global__ void __launch_bounds__(256) cascade_merge_kernel(const int32_t* __res
 
 template <typename T>
 cudaError_t launch_cascade_merge(const RunParams& p, int32_t blocks, cudaStream_t s) {
-  return launch_behind_run(cascade_merge_kernel<T>, blocks, s, static_cast<const int32_t*>(p.iws),
+  return launch_behind_run(cascade_merge_kernel<T>, blocks, 256, s, static_cast<const int32_t*>(p.iws),
                            static_cast<const float*>(p.fws), p.partial_o_offset, reinterpret_cast<T*>(p.o),
                            p.o_stride_tok, p.o_stride_head, p.lse, int(p.num_qo_heads), int(p.group));
 }

@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_attention_kernel(const __gr
   RunSmem& sm = *reinterpret_cast<RunSmem*>(smem_raw);
   // A merge launched behind this run may be scheduled from now on: its blocks
   // take SMs as this grid's CTAs leave and wait for the grid to complete.
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
+  if (threadIdx.x == 0) let_dependents_start();
   const int32_t* iws = p.iws;
   const int32_t magic = ws_header(iws, FI_H_MAGIC);
   const int32_t n_items = ws_header(iws, FI_H_NUM_ITEMS);

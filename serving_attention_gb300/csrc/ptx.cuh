@@ -1,6 +1,7 @@
 // ptx.cuh -- thin inline-PTX wrappers (mbarrier, cp.async, named barriers,
 // bounded waits) shared by the kernels of this library.  sm_103a only.
 #pragma once
+#include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -226,5 +227,32 @@ struct Elem<__half> {
     return *reinterpret_cast<uint32_t*>(&h);
   }
 };
+
+// Programmatic dependent launch: a merge that follows a kernel is enqueued
+// with programmatic stream serialization, and that kernel lets its
+// dependents be scheduled from its start (`let_dependents_start`), so the
+// merge's blocks take SMs as the kernel's CTAs leave instead of after the
+// whole grid has finished and a new launch has gone through; each waits in
+// `grid_dependency_wait` until the preceding grid has completed and its
+// memory is visible (launched without the attribute, the wait returns at
+// once).
+__device__ __forceinline__ void let_dependents_start() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_behind_run(void (*kernel)(KArgs...), int32_t blocks, int threads, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(unsigned(threads));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, KArgs(args)...);
+}
+
 
 }  // namespace fi
