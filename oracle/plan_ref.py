@@ -31,10 +31,13 @@ Rule:
     multiple of H, each taking KV heads hk .. hk + H - 1 at once: 32 rows,
     row = h * G + g for head hk + h, all of query token 0.
  3. Per class, total = sum of kv_eff (times H for a multi-head unit); chunk = max(min_chunk,
-    ceil(total / (num_ctas * split_factor))) rounded up to a multiple of the
+    ceil(total / (ctas * split_factor))) rounded up to a multiple of the
     class granule max(page_size, 64) (decode) or max(page_size, 128) (prefill).
-    A multi-head unit's chunk is max(granule, floor(chunk / H / granule) *
-    granule) keys (the K/V bytes of a one-head chunk).
+    ctas = num_ctas, except for the decode class when the prefill-class
+    items (n_pre of them: per 256-row unit, its ranges' chunk counts, at
+    least 1) are at least one and at most num_ctas / 2: then num_ctas - n_pre.
+    A multi-head unit's chunk is max(granule, ceil(ceil(chunk / H) / granule)
+    * granule) keys (the K/V bytes of a one-head chunk).
  4. A unit with kv_eff = 0 gives one empty item.  Otherwise each range
     [s, e) splits into ceil((e - s) / chunk) items [s + i*chunk,
     min(e, s + (i+1)*chunk)), ranges in order, chunk numbers running across
@@ -284,13 +287,19 @@ def _plan(cfg, reqs, num_shared, shared_page_size, block_of, total_qo, num_qo_he
                 units.append((b, hk, qt, T, r0, r1, rng, heads))
                 total[T] += sum(e - s for s, e in rng) * heads
 
-    chunk = {}
-    for T, min_chunk in ((TILE_DECODE, cfg["decode_min_chunk"]), (TILE_PREFILL, cfg["prefill_min_chunk"])):
-        want = max(min_chunk, _ceil_div(total[T], C * cfg["split_factor"]))
-        chunk[T] = _ceil_div(want, granule[T]) * granule[T]
+    def pick(T, min_chunk, ctas):
+        want = max(min_chunk, _ceil_div(total[T], ctas * cfg["split_factor"]))
+        return _ceil_div(want, granule[T]) * granule[T]
+
+    chunk = {TILE_PREFILL: pick(TILE_PREFILL, cfg["prefill_min_chunk"], C)}
+    # prefill-class items; the decode class counts the CTAs they leave free when they take at most half
+    n_pre = sum(max(1, sum(_ceil_div(e - s, chunk[TILE_PREFILL]) for s, e in u[6]))
+                for u in units if u[3] == TILE_PREFILL)
+    chunk[TILE_DECODE] = pick(TILE_DECODE, cfg["decode_min_chunk"], C - n_pre if 0 < 2 * n_pre <= C else C)
     weight = {TILE_DECODE: cfg["decode_cost_weight"], TILE_PREFILL: cfg["prefill_cost_weight"]}
-    # a multi-head unit's chunk holds the K/V bytes of a one-head chunk
-    chunk_mh = max(granule[TILE_DECODE], chunk[TILE_DECODE] // mh // granule[TILE_DECODE] * granule[TILE_DECODE])
+    # a multi-head unit's chunk holds the K/V bytes of a one-head chunk, rounded up to the granule
+    g = granule[TILE_DECODE]
+    chunk_mh = max(g, _ceil_div(_ceil_div(chunk[TILE_DECODE], mh), g) * g)
 
     items = []   # (sort key, fields)
     merges = []

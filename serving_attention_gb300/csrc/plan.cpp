@@ -19,8 +19,10 @@
 //    class granule, and the sink range [0, min(S, hi)) comes first unless
 //    the two touch (then one range [0, hi));
 //  * per tile class, a KV chunk length = max(min_chunk, total / (CTAs * split))
-//    rounded up to the class granule; units longer than a chunk are split
-//    into chunks whose fp32 partial states are merged by the kernel;
+//    rounded up to the class granule, where the decode class counts only the
+//    CTAs left free by the prefill-class items when those take at most half
+//    of them; units longer than a chunk are split into chunks whose fp32
+//    partial states are merged by the kernel;
 //  * chunks are dealt out longest-first to the least-loaded CTA (LPT); an
 //    item's cost is its KV length plus a fixed FI_ITEM_COST_TOKENS (the
 //    per-item latency of the kernel), times the class weight, so that many
@@ -259,17 +261,28 @@ fi_status plan_requests(const fi_plan_config* cfg, const std::vector<Req>& reqs,
     }
   }
 
-  const int64_t slots = int64_t(cfg->num_ctas) * cfg->split_factor;
-  auto pick_chunk = [&](int64_t total, int64_t min_chunk, int64_t granule) {
+  auto pick_chunk = [&](int64_t total, int64_t min_chunk, int64_t granule, int64_t slots) {
     int64_t c = std::max<int64_t>(min_chunk, ceil_div(total, slots));
     return ceil_div(c, granule) * granule;
   };
   const int64_t gran_dec = std::max(max_page, FI_GRANULE_DECODE);
-  const int64_t chunk_dec = pick_chunk(total_dec, cfg->decode_min_chunk, gran_dec);
-  const int64_t chunk_pre = pick_chunk(total_pre, cfg->prefill_min_chunk, std::max(max_page, FI_GRANULE_PREFILL));
-  // a multi-head unit's chunk: the K/V bytes of a one-head chunk
+  const int64_t chunk_pre = pick_chunk(total_pre, cfg->prefill_min_chunk, std::max(max_page, FI_GRANULE_PREFILL),
+                                       int64_t(cfg->num_ctas) * cfg->split_factor);
+  // Prefill-class items are long; when they take at most half the CTAs, the
+  // decode work is spread over the CTAs they leave free (finer decode chunks
+  // would only add per-item costs beside them).
+  int64_t n_pre = 0;
+  for (const Unit& u : units) {
+    if (u.tile != FI_TILE_PREFILL) continue;
+    int64_t n = 0;
+    for (int r = 0; r < u.n_ranges; ++r) n += ceil_div(u.r_end[r] - u.r_begin[r], chunk_pre);
+    n_pre += std::max<int64_t>(n, 1);
+  }
+  const int64_t dec_ctas = (n_pre > 0 && 2 * n_pre <= cfg->num_ctas) ? cfg->num_ctas - n_pre : cfg->num_ctas;
+  const int64_t chunk_dec = pick_chunk(total_dec, cfg->decode_min_chunk, gran_dec, dec_ctas * cfg->split_factor);
+  // a multi-head unit's chunk: the K/V bytes of a one-head chunk, rounded up
   const int32_t mh = fi_mh_heads(group, num_kv_heads);
-  const int64_t chunk_mh = std::max(gran_dec, chunk_dec / mh / gran_dec * gran_dec);
+  const int64_t chunk_mh = std::max(gran_dec, ceil_div(ceil_div(chunk_dec, mh), gran_dec) * gran_dec);
 
   // Chunks of every unit; split units become merge units in unit order.  In
   // a cascade plan every unit writes partial states and none is merged in

@@ -553,3 +553,37 @@ def test_cascade_plan_rejects(case, status):
     st, ws, _ = _cascade_both(cfg, cfgd, (sqo, skvp, skvi, slpl, sp), (qo, kvp, kvi, lpl, 16), 8, 2, causal,
                               num_pages=3, shared_num_pages=3)
     assert st == status and ws is None
+
+
+@pytest.mark.parametrize("num_ctas,page", [(152, 16), (60, 16), (152, 1)])
+def test_decode_chunk_counts_the_ctas_prefill_items_leave(num_ctas, page):
+    """Decode chunks are sized over the CTAs the prefill-class items leave
+    free when those take at most half the CTAs (48 of 152 here; 48 of 60 is
+    more than half, so all 60 count), and a multi-head unit's chunk is the
+    one-head chunk over its heads, rounded up to the granule."""
+    rng = np.random.default_rng(4300 + num_ctas + page)
+    hkv, group = 8, 4
+    kv = np.concatenate([[3000, 3000], rng.integers(100, 5000, size=40)])
+    qo = np.concatenate([[64, 64], np.ones(40, np.int64)])  # two 256-row requests, 40 one-token ones
+    qop = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    kvp, lpl = workloads._pages_for(kv, page)
+    nnz = int(kvp[-1])
+    kvi = rng.permutation(nnz).astype(np.int32)
+    cfg, cfgd = _cfg(num_ctas=num_ctas)
+    st, ws, info = _plan_both(cfg, cfgd, qop, kvp, kvi, lpl, hkv * group, hkv, page, 0, nnz)
+    assert st == 0
+    _check_invariants(ws, qop, kv, hkv * group, hkv, 0, cfgd)
+    assert info.chunk_prefill == 1024
+    n_pre = 2 * hkv * 3  # per KV head, 3000 keys in chunks of 1024
+    free = num_ctas - n_pre if 2 * n_pre <= num_ctas else num_ctas
+    total_dec = int(kv[2:].sum()) * hkv
+    gran = max(page, 64)
+    want = -(-max(256, -(-total_dec // free)) // gran) * gran
+    assert info.chunk_decode == want
+    items, heads = _items(ws, ws[7], ws[1])
+    dec = items[items[:, 0] >= 2]
+    lens = dec[:, 5] - dec[:, 4]
+    if page == 1:  # 8 heads per unit: chunks of ceil(want / 8) rounded up to 64 keys
+        assert np.all(heads[items[:, 0] >= 2] == 8)
+        want = -(-(-(-want // 8)) // 64) * 64
+    assert lens.max() == min(want, kv[2:].max())
