@@ -363,7 +363,7 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
   const uint32_t s_cols = tl + mt * kTileN, o_cols = tl + kTmemO + mt * kHeadDim;
   const int G = p.group;
   const float c = p.scale_log2;
-  const float cs = kCap ? 1.f : c;  // scale still to apply to the (capped) logits
+  const float cs = kCap ? var.cap_a : c;  // log2-domain factor of the (tanh of the) logits
   uint32_t tiles = 0, items = 0;  // phases of s_full[mt] and o_ready[mt]
   for (int32_t i = b0; i < b1; ++i) {
     const Item item = load_item(p.iws, off_items, i);
@@ -393,16 +393,16 @@ __device__ void pf_softmax(const RunParams& p, RunSmem& sm, int32_t b0, int32_t 
         for (int h = 0; h < 4; ++h) tc::tmem_ld32(s_cols + 32 * h, sv[h]);
         tc::tmem_ld_wait();
         const int kbase = item.kv0 + j * kTileN;
-        if (kCap) {  // capped log2-domain logits; the mask below then works on them
-          const float kb = c * var.cap_b;
+        if (kCap) {  // tanh(scale * s / cap), which cs = cap * log2(e) turns into the capped log2-domain logit
+          const float kb = c * var.cap_b * 0.34657359f;  // scale * log2(e) * (2 / cap) * ln(2) / 2 = scale / cap
+          const float2 kb2 = make_float2(kb, kb), zero = make_float2(0.f, 0.f);
 #pragma unroll
           for (int h = 0; h < 4; ++h)
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              const float2 v =
-                  soft_cap_log2_x2(make_float2(__uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1])), kb, var.cap_a);
-              sv[h][e] = __float_as_uint(v.x);
-              sv[h][e + 1] = __float_as_uint(v.y);
+              const float2 y = fma2(make_float2(__uint_as_float(sv[h][e]), __uint_as_float(sv[h][e + 1])), kb2, zero);
+              sv[h][e] = __float_as_uint(tanh_approx(y.x));
+              sv[h][e + 1] = __float_as_uint(tanh_approx(y.y));
             }
         }
         if (kbase + kTileN - 1 > lim || (kMask && kbase < lo)) {  // causal diagonal, chunk end, padding row, window

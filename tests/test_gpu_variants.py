@@ -116,3 +116,25 @@ def test_soft_cap_extreme_logits():
     n = b.total_qo
     err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
     assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
+
+
+@pytest.mark.parametrize("dtype,cap,qscale", [("fp16", 30.0, 20.0), ("fp16", 50.0, 40.0), ("bf16", 5.0, 4.0),
+                                              ("bf16", 2.0, 1.5)])
+def test_soft_cap_logits_near_the_cap(dtype, cap, qscale):
+    """Logits of the order of the cap itself (queries scaled so that s / cap
+    spreads over about +-1), where the capped logit bends most and a relative
+    error in tanh weighs most: tensor-core tiles against the oracle.  Caps of
+    30 and 50 run in fp16: logits that large make rows so peaked that in bf16
+    the 16-bit rounding of P and of the stored O alone reaches the flat bar
+    (8.2e-3 measured at cap 30), as with the peaked-softmax cases."""
+    b = workloads.make_batch("capn", dtype, [64, 40], [700, 300], 8, 2, 16, 1, 761 + int(cap), DEV,
+                             pool_pages=(700 + 15) // 16 + (300 + 15) // 16 + 2)
+    b.q.mul_(qscale)
+    cfg = fi.default_plan_config(0, logits_soft_cap=cap)
+    o, lse, info, ws = gpu_run(b, cfg=cfg)
+    torch.cuda.synchronize()
+    assert fi.device_status(ws) == 0 and info.num_prefill_items > 0
+    o_ref, l_ref = oracle.attention(oracle_problem(b, -1, 0, cap))
+    n = b.total_qo
+    err_o, err_l = compare(o[:n], lse[:n], o_ref, l_ref)
+    assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
