@@ -410,6 +410,10 @@ __device__ void softmax_role(const Params& p, Smem& sm, uint32_t rank, int32_t b
     // (rows past the heads are zeros).
     ok = warp_wait(&sm.q_empty, (nu & 1) ^ 1, &sm.abort);
     if (!ok) break;
+    // q_empty completes through the MMA warp's tcgen05.commit; the fence
+    // orders this warp's tensor-memory stores below after that wait, so no
+    // store can overtake an S MMA of the previous chunk still reading Q.
+    tc::fence_after_sync();
     {
       const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + int64_t(u.b) * p.qn_stride_tok +
                                                         int64_t(row_ok ? r : 0) * p.qn_stride_head) +

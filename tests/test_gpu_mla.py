@@ -83,6 +83,22 @@ def test_mla_random_batches(seed):
     _compare(*_run(b, mla.default_config(0, min_chunk=256))[:2], *_oracle(b))
 
 
+
+@pytest.mark.parametrize("seed", [821, 822, 823])
+def test_mla_query_rewrites_at_chunk_boundaries(seed):
+    """Chunks of 64 tokens: every CTA pair runs many chunks in a row, and at
+    each chunk boundary the softmax warps rewrite the query rows in tensor
+    memory once the previous chunk's last S MMA has read them.  Two runs on
+    NaN-poisoned outputs give the same bits, every element is written, and
+    both match the oracle."""
+    b = workloads.random_mla_batch(seed, batch=40, kv_max=2500, num_heads=128, page_size=64, device=DEV)
+    cfg = mla.default_config(0, min_chunk=64)
+    o1, l1, info, ws = _run(b, cfg)
+    assert info.num_parts > 0
+    o2, l2, _, _ = _run(b, cfg, ws)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    _compare(o1, l1, *_oracle(b))
+
 def test_mla_full_size_sampled():
     """The 64-request length-mix workload; the oracle on six requests,
     the longest and the shortest among them."""
